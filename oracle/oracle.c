@@ -1,0 +1,242 @@
+/*
+ * oracle.c -- plain CPU reference of the DAC-style vocoder decoder.
+ *
+ * TEST INFRASTRUCTURE ONLY (see oracle.h): used by the tests, the smoke check
+ * and the CPU baseline of the benchmark; never by the product path.
+ *
+ * Double precision throughout.  Each layer is its textbook definition written
+ * as direct loops.  The only liberty taken is the position of the independent
+ * output-time loop: it is innermost so that the compiler can vectorise it,
+ * which leaves the order in which each output element sums its terms exactly
+ * the order of the definition (input channel, then tap).
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+int oracle_param_count(const oracle_arch *a) {
+  return 2 + a->n_stages * (3 + 6 * a->n_dilations) + 3;
+}
+
+long oracle_hop(const oracle_arch *a) {
+  long h = 1;
+  for (int i = 0; i < a->n_stages; ++i) h *= a->strides[i];
+  return h;
+}
+
+/* minimaxmusic.cpp Architecture, "Models": w = g * v / ||v||, axis 0. */
+int oracle_fold_weight_norm(const float *g, const float *v, int dim0, long rest, double *w) {
+  for (int i = 0; i < dim0; ++i) {
+    const float *row = v + (long)i * rest;
+    double ss = 0.0;
+    for (long j = 0; j < rest; ++j) ss += (double)row[j] * (double)row[j];
+    double norm = sqrt(ss);
+    if (!(norm > 0.0)) return -1;
+    double scale = (double)g[i] / norm;
+    for (long j = 0; j < rest; ++j) w[(long)i * rest + j] = scale * (double)row[j];
+  }
+  return 0;
+}
+
+/* minimaxmusic.cpp Architecture, "Flow VAE": y = x + sin^2(a x) / (a + 1e-9). */
+void oracle_snake_row(const double *x, long n, double alpha, int identity, double *y) {
+  if (identity) {
+    if (y != x) memmove(y, x, (size_t)n * sizeof(double));
+    return;
+  }
+  double inv_b = 1.0 / (alpha + 1e-9);
+  for (long i = 0; i < n; ++i) {
+    double s = sin(alpha * x[i]);
+    y[i] = x[i] + s * s * inv_b;
+  }
+}
+
+int oracle_conv1d(const double *x, int Cin, int T, const double *w, const double *b, int Cout,
+                  int K, int dil, int pad_left, int pad_right, double *y) {
+  long T_out = (long)T + pad_left + pad_right - (long)dil * (K - 1);
+  if (T_out < 0 || Cin <= 0 || Cout <= 0 || K <= 0 || dil <= 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int co = 0; co < Cout; ++co) {
+    double *yr = y + (long)co * T_out;
+    double bias = b ? b[co] : 0.0;
+    for (long t = 0; t < T_out; ++t) yr[t] = bias;
+    for (int ci = 0; ci < Cin; ++ci) {
+      const double *xr = x + (long)ci * T;
+      for (int k = 0; k < K; ++k) {
+        double wv = w[((long)co * Cin + ci) * K + k];
+        long shift = (long)k * dil - pad_left; /* input index = t + shift */
+        long t_lo = shift < 0 ? -shift : 0;
+        long t_hi = T - shift; /* exclusive: t + shift < T */
+        if (t_hi > T_out) t_hi = T_out;
+        for (long t = t_lo; t < t_hi; ++t) yr[t] += wv * xr[t + shift];
+      }
+    }
+  }
+  return 0;
+}
+
+/* qwentts.cpp Architecture, "Custom GGML ops": col2im_1d scatter-add of the
+ * [K*OC, T_in] column matrix into [T_out, OC] at position t*s + k - p. */
+int oracle_conv_transpose1d(const double *x, int Cin, int T, const double *w, const double *b,
+                            int Cout, int K, int stride, int pad_left, int T_out, double *y) {
+  if (T_out < 0 || Cin <= 0 || Cout <= 0 || K <= 0 || stride <= 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int co = 0; co < Cout; ++co) {
+    double *yr = y + (long)co * T_out;
+    for (long j = 0; j < T_out; ++j) yr[j] = 0.0;
+    for (int ci = 0; ci < Cin; ++ci) {
+      const double *xr = x + (long)ci * T;
+      const double *wr = w + ((long)ci * Cout + co) * K;
+      for (long t = 0; t < T; ++t) {
+        for (int k = 0; k < K; ++k) {
+          long j = t * stride + k - pad_left;
+          if (j >= 0 && j < T_out) yr[j] += wr[k] * xr[t];
+        }
+      }
+    }
+    if (b)
+      for (long j = 0; j < T_out; ++j) yr[j] += b[co];
+  }
+  return 0;
+}
+
+/* Snake applied per channel row of a [C][L] activation, alpha[c] per channel. */
+static void snake_rows(const double *x, int C, long L, const double *alpha, int identity,
+                       double *y) {
+#pragma omp parallel for schedule(static)
+  for (int c = 0; c < C; ++c) oracle_snake_row(x + (long)c * L, L, alpha[c], identity, y + (long)c * L);
+}
+
+static void conv_pads(int padding, int K, int dil, int *pl, int *pr) {
+  int span = dil * (K - 1);
+  if (padding == ORACLE_PAD_CAUSAL) {
+    *pl = span;
+    *pr = 0;
+  } else {
+    *pl = span / 2;
+    *pr = span - span / 2;
+  }
+}
+
+/* minimaxmusic.cpp Architecture, "Flow VAE":
+ *   conv_in k7 -> for each block: snake -> conv_t (stride s, k = 2s, pad s/2)
+ *   -> 3 x res_unit (skip -> snake1 -> conv1 k7 dil d -> snake2 -> conv2 k1 -> + skip)
+ *   -> snake_out -> conv_out k7 (with bias) -> tanh.
+ * Causal variant (qwentts.cpp Architecture, "Audio tokenizer decoder" and
+ * "Streaming decode"): every stride-1 conv pads (k-1)*d on the left only and the
+ * transposed conv keeps the first T*s samples of its col2im output. */
+int oracle_decode(const oracle_arch *a, const double *const *params, const float *latent, int B,
+                  int T, double *audio, double *pre_tanh) {
+  if (!a || !params || !latent || !audio || B <= 0 || T <= 0) return -1;
+  const int ident = (a->flags & ORACLE_FLAG_SNAKE_IDENTITY) != 0;
+  const long hop = oracle_hop(a);
+  const long L_out = (long)T * hop;
+
+  /* largest activation (channels x length) over the stack */
+  long max_elems = (long)a->latent_channels * T;
+  {
+    long L = T;
+    long e = (long)a->channels0 * L;
+    if (e > max_elems) max_elems = e;
+    for (int i = 0; i < a->n_stages; ++i) {
+      L *= a->strides[i];
+      e = (long)a->widths[i] * L;
+      if (e > max_elems) max_elems = e;
+    }
+  }
+  double *x = (double *)malloc((size_t)max_elems * sizeof(double));
+  double *s = (double *)malloc((size_t)max_elems * sizeof(double));
+  double *h = (double *)malloc((size_t)max_elems * sizeof(double));
+  if (!x || !s || !h) {
+    free(x), free(s), free(h);
+    return -2;
+  }
+
+  for (int bi = 0; bi < B; ++bi) {
+    int p = 0;
+    /* latent item, widened to double */
+    const float *lat = latent + (long)bi * a->latent_channels * T;
+    for (long i = 0; i < (long)a->latent_channels * T; ++i) s[i] = (double)lat[i];
+
+    /* conv_in: no Snake in front of it */
+    int pl, pr;
+    conv_pads(a->padding, a->in_kernel, 1, &pl, &pr);
+    oracle_conv1d(s, a->latent_channels, T, params[p], params[p + 1], a->channels0, a->in_kernel, 1,
+                  pl, pr, x);
+    p += 2;
+
+    int C = a->channels0;
+    long L = T;
+    for (int st = 0; st < a->n_stages; ++st) {
+      const int stride = a->strides[st];
+      const int Cout = a->widths[st];
+      /* snake -> transposed conv, k = 2s */
+      snake_rows(x, C, L, params[p], ident, s);
+      const int Kt = 2 * stride;
+      const int pad_t = (a->padding == ORACLE_PAD_CAUSAL) ? 0 : stride / 2;
+      oracle_conv_transpose1d(s, C, (int)L, params[p + 1], params[p + 2], Cout, Kt, stride, pad_t,
+                              (int)(L * stride), x);
+      p += 3;
+      C = Cout;
+      L *= stride;
+      /* residual units */
+      for (int r = 0; r < a->n_dilations; ++r) {
+        const int d = a->dilations[r];
+        snake_rows(x, C, L, params[p], ident, s);
+        conv_pads(a->padding, a->res_kernel, d, &pl, &pr);
+        oracle_conv1d(s, C, (int)L, params[p + 1], params[p + 2], C, a->res_kernel, d, pl, pr, h);
+        snake_rows(h, C, L, params[p + 3], ident, s);
+        oracle_conv1d(s, C, (int)L, params[p + 4], params[p + 5], C, 1, 1, 0, 0, h);
+        for (long i = 0; i < (long)C * L; ++i) x[i] += h[i];
+        p += 6;
+      }
+    }
+    /* snake_out -> conv_out (with bias) -> tanh */
+    snake_rows(x, C, L, params[p], ident, s);
+    conv_pads(a->padding, a->out_kernel, 1, &pl, &pr);
+    double *y = audio + (long)bi * L_out;
+    oracle_conv1d(s, C, (int)L, params[p + 1], params[p + 2], 1, a->out_kernel, 1, pl, pr, y);
+    if (pre_tanh) memcpy(pre_tanh + (long)bi * L_out, y, (size_t)L_out * sizeof(double));
+    if (!(a->flags & ORACLE_FLAG_NO_TANH))
+      for (long i = 0; i < L_out; ++i) y[i] = tanh(y[i]);
+  }
+  free(x), free(s), free(h);
+  return 0;
+}
+
+/* minimaxmusic.cpp Architecture, "Decode and stitch": the first window keeps
+ * its left edge, later windows crop crop_left latents on the left, all but the
+ * last crop crop_right on the right; segments are concatenated and clamped. */
+long oracle_stitched_length(int n_win, int win_frames, int crop_left, int crop_right, int hop) {
+  if (n_win <= 0 || win_frames <= 0 || hop <= 0 || crop_left < 0 || crop_right < 0) return -1;
+  long frames = 0;
+  for (int w = 0; w < n_win; ++w) {
+    int lo = (w == 0) ? 0 : crop_left;
+    int hi = (w == n_win - 1) ? win_frames : win_frames - crop_right;
+    if (hi < lo) return -1;
+    frames += hi - lo;
+  }
+  return frames * hop;
+}
+
+int oracle_stitch(const double *decoded, int n_win, int n_sides, int win_frames, int crop_left,
+                  int crop_right, int hop, double *out) {
+  long len = oracle_stitched_length(n_win, win_frames, crop_left, crop_right, hop);
+  if (len < 0 || n_sides <= 0) return -1;
+  const long win_len = (long)win_frames * hop;
+  for (int side = 0; side < n_sides; ++side) {
+    long pos = 0;
+    for (int w = 0; w < n_win; ++w) {
+      int lo = (w == 0) ? 0 : crop_left;
+      int hi = (w == n_win - 1) ? win_frames : win_frames - crop_right;
+      const double *src = decoded + ((long)w * n_sides + side) * win_len;
+      for (long j = (long)lo * hop; j < (long)hi * hop; ++j) {
+        double v = src[j];
+        out[(long)side * len + pos++] = v < -1.0 ? -1.0 : (v > 1.0 ? 1.0 : v);
+      }
+    }
+  }
+  return 0;
+}

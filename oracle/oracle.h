@@ -1,0 +1,118 @@
+/*
+ * oracle.h -- plain CPU reference of the DAC-style vocoder decoder.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This library exists so that the tests, the smoke
+ * check and the CPU baseline of the benchmark can compare the GPU path against
+ * an obviously correct implementation.  Nothing on the product path may link,
+ * load or call it, and it shares no code with the CUDA library.
+ *
+ * Every function works in double precision (fp32 inputs are widened once) and
+ * follows the plain definition of the operation, with direct loops and no
+ * blocking, fusion or algebraic rewriting:
+ *
+ *   Snake           minimaxmusic.cpp Architecture, section "Flow VAE":
+ *                   y = x + sin^2(a*x) / (a + 1e-9), with a used as stored
+ *                   (MiniMax-Music-3 -> CMF README, "What the conversion had to
+ *                   get right": Snake reads alpha verbatim).
+ *   weight norm     minimaxmusic.cpp Architecture, sections "Models" and "Flow
+ *                   VAE": w = g * v / ||v|| along axis 0 of the stored tensor.
+ *   conv1d          cross-correlation with zero padding and dilation, the
+ *                   textbook definition of a 1-D convolution layer.
+ *   convtranspose1d scatter-add of every input column into the output at
+ *                   t*s + k - p, i.e. the col2im_1d op of qwentts.cpp
+ *                   Architecture, section "Custom GGML ops", with
+ *                   T_out = (T_in - 1)*s + K - 2p.
+ *   decoder         minimaxmusic.cpp Architecture, section "Flow VAE" (layer
+ *                   list), qwentts.cpp Architecture, section "Audio tokenizer
+ *                   decoder" (causal speech variant).
+ *   stitch          minimaxmusic.cpp Architecture, section "Decode and stitch".
+ *
+ * Parity pins: every function here is checked by tests that do not reuse its
+ * code (closed forms, dense-matrix brute force, adjoint identities, library
+ * routines on small cases, linearity, impulse responses, shift equivariance,
+ * locality, causality).  No function is "parity unpinned".
+ */
+#ifndef VOCODER_ORACLE_H
+#define VOCODER_ORACLE_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* padding modes of the whole stack */
+#define ORACLE_PAD_SYMMETRIC 0 /* music decoder: k-tap convs pad d(k-1)/2 per side, ConvT crops s/2 */
+#define ORACLE_PAD_CAUSAL 1    /* speech codec: convs pad d(k-1) on the left, ConvT keeps the first T*s */
+
+/* test switches (used by the linearity and impulse-response pins) */
+#define ORACLE_FLAG_SNAKE_IDENTITY 1 /* replace every Snake by the identity */
+#define ORACLE_FLAG_NO_TANH 2        /* leave out the final tanh           */
+
+typedef struct {
+  int latent_channels; /* C_lat                                   */
+  int channels0;       /* C_0, output channels of conv_in         */
+  int in_kernel;       /* conv_in taps (7)                         */
+  int n_stages;        /* upsampling stages                        */
+  const int *strides;  /* [n_stages]                               */
+  const int *widths;   /* [n_stages], output channels of stage i   */
+  int n_dilations;     /* residual units per stage (3)             */
+  const int *dilations;/* [n_dilations] (1, 3, 9)                  */
+  int res_kernel;      /* dilated conv taps in a residual unit (7) */
+  int out_kernel;      /* conv_out taps (7)                        */
+  int padding;         /* ORACLE_PAD_*                             */
+  int flags;           /* ORACLE_FLAG_*                            */
+} oracle_arch;
+
+/* number of parameter tensors of the stack, in the canonical order:
+ *   conv_in.w [C0][Cl][Kin], conv_in.b [C0],
+ *   for each stage i (Cin -> Cout = widths[i], stride s):
+ *     snake.alpha [Cin], convT.w [Cin][Cout][2s], convT.b [Cout],
+ *     for each dilation d: snake1.alpha [Cout], conv1.w [Cout][Cout][Kres],
+ *       conv1.b [Cout], snake2.alpha [Cout], conv2.w [Cout][Cout][1], conv2.b [Cout]
+ *   snake_out.alpha [C_last], conv_out.w [1][C_last][Kout], conv_out.b [1]      */
+int oracle_param_count(const oracle_arch *a);
+
+/* w[i, :] = g[i] * v[i, :] / ||v[i, :]||, the norm taken over everything but
+ * axis 0 of the stored tensor (Conv1d [Cout][Cin][K]: per output channel;
+ * ConvTranspose1d [Cin][Cout][K]: per input channel).  Returns -1 when a row of
+ * v has zero norm, else 0. */
+int oracle_fold_weight_norm(const float *g, const float *v, int dim0, long rest, double *w);
+
+/* y[i] = x[i] + sin^2(alpha*x[i]) / (alpha + 1e-9) for one channel row of n values.
+ * identity != 0 gives y = x. */
+void oracle_snake_row(const double *x, long n, double alpha, int identity, double *y);
+
+/* y[co][t] = b[co] + sum_ci sum_k w[co][ci][k] * x[ci][t + k*dil - pad_left],
+ * x taken as zero outside [0, T).  Output length T + pad_left + pad_right - dil*(K-1).
+ * b may be NULL (zero bias). */
+int oracle_conv1d(const double *x, int Cin, int T, const double *w, const double *b, int Cout,
+                  int K, int dil, int pad_left, int pad_right, double *y);
+
+/* y[co][t*s + k - pad_left] += w[ci][co][k] * x[ci][t] for every t, k, ci with the
+ * target index in [0, T_out); then y[co][j] += b[co].  b may be NULL. */
+int oracle_conv_transpose1d(const double *x, int Cin, int T, const double *w, const double *b,
+                            int Cout, int K, int stride, int pad_left, int T_out, double *y);
+
+/* total upsampling factor (product of strides) */
+long oracle_hop(const oracle_arch *a);
+
+/* Full decode.  params: oracle_param_count(a) pointers to double arrays in the
+ * canonical order (weights already folded; a NULL bias means zero).
+ * latent [B][Cl][T] fp32 -> audio [B][T*hop] double.  When pre_tanh is not NULL
+ * it receives the conv_out result before tanh ([B][T*hop]).  0 on success. */
+int oracle_decode(const oracle_arch *a, const double *const *params, const float *latent, int B,
+                  int T, double *audio, double *pre_tanh);
+
+/* Overlap-crop stitch (minimaxmusic.cpp Architecture, "Decode and stitch"):
+ * decoded [n_win*n_sides][win_frames*hop] with item index 2w+side ordering
+ * generalised to w*n_sides + side.  Window 0 keeps its left edge, later windows
+ * drop crop_left frames on the left, all but the last drop crop_right frames on
+ * the right; the kept pieces are concatenated per side and clamped to [-1, 1].
+ * out [n_sides][oracle_stitched_length(...)]. */
+long oracle_stitched_length(int n_win, int win_frames, int crop_left, int crop_right, int hop);
+int oracle_stitch(const double *decoded, int n_win, int n_sides, int win_frames, int crop_left,
+                  int crop_right, int hop, double *out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,205 @@
+"""ctypes wrapper around the CPU oracle (oracle.c).
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, by the smoke check and by the
+benchmark's CPU-baseline / reference leg.  The product path never imports it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+FLAG_SNAKE_IDENTITY = 1
+FLAG_NO_TANH = 2
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (plain C99 + OpenMP, IEEE arithmetic)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= max(os.path.getmtime(_SRC),
+                                              os.path.getmtime(os.path.join(_HERE, "oracle.h")))):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O3", "-std=c99", "-fopenmp", "-fPIC", "-shared", "-Wall", "-o", tmp, _SRC,
+           "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            D = ctypes.POINTER(ctypes.c_double)
+            F = ctypes.POINTER(ctypes.c_float)
+            lib.oracle_fold_weight_norm.argtypes = [F, F, ctypes.c_int, ctypes.c_long, D]
+            lib.oracle_fold_weight_norm.restype = ctypes.c_int
+            lib.oracle_snake_row.argtypes = [D, ctypes.c_long, ctypes.c_double, ctypes.c_int, D]
+            lib.oracle_snake_row.restype = None
+            lib.oracle_conv1d.argtypes = [D, ctypes.c_int, ctypes.c_int, D, D, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, D]
+            lib.oracle_conv1d.restype = ctypes.c_int
+            lib.oracle_conv_transpose1d.argtypes = [D, ctypes.c_int, ctypes.c_int, D, D,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_int, D]
+            lib.oracle_conv_transpose1d.restype = ctypes.c_int
+            lib.oracle_decode.argtypes = [ctypes.c_void_p, ctypes.POINTER(D), F, ctypes.c_int,
+                                          ctypes.c_int, D, D]
+            lib.oracle_decode.restype = ctypes.c_int
+            lib.oracle_stitched_length.argtypes = [ctypes.c_int] * 5
+            lib.oracle_stitched_length.restype = ctypes.c_long
+            lib.oracle_stitch.argtypes = [D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, D]
+            lib.oracle_stitch.restype = ctypes.c_int
+            lib.oracle_param_count.argtypes = [ctypes.c_void_p]
+            lib.oracle_param_count.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _d(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+class _ArchC(ctypes.Structure):
+    _fields_ = [("latent_channels", ctypes.c_int), ("channels0", ctypes.c_int),
+                ("in_kernel", ctypes.c_int), ("n_stages", ctypes.c_int),
+                ("strides", ctypes.POINTER(ctypes.c_int)), ("widths", ctypes.POINTER(ctypes.c_int)),
+                ("n_dilations", ctypes.c_int), ("dilations", ctypes.POINTER(ctypes.c_int)),
+                ("res_kernel", ctypes.c_int), ("out_kernel", ctypes.c_int),
+                ("padding", ctypes.c_int), ("flags", ctypes.c_int)]
+
+
+def fold_weight_norm(g: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """w = g * v / ||v|| along axis 0 (double result)."""
+    lib = _load()
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    w = np.empty(v.shape, dtype=np.float64)
+    rest = int(np.prod(v.shape[1:])) if v.ndim > 1 else 1
+    rc = lib.oracle_fold_weight_norm(_f(g), _f(v), int(v.shape[0]), rest, _d(w))
+    if rc != 0:
+        raise ValueError("weight norm: a row of v has zero norm")
+    return w
+
+
+def snake(x: np.ndarray, alpha: np.ndarray, identity: bool = False) -> np.ndarray:
+    """Per-channel Snake of a [C, L] array."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    C, L = x.shape
+    for c in range(C):
+        lib.oracle_snake_row(_d(x[c]), L, float(alpha[c]), int(identity), _d(y[c]))
+    return y
+
+
+def conv1d(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray], dil: int, pad_left: int,
+           pad_right: int) -> np.ndarray:
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    Cin, T = x.shape
+    Cout, Cin2, K = w.shape
+    assert Cin2 == Cin
+    T_out = T + pad_left + pad_right - dil * (K - 1)
+    y = np.empty((Cout, T_out), dtype=np.float64)
+    bb = None if b is None else np.ascontiguousarray(b, dtype=np.float64)
+    rc = lib.oracle_conv1d(_d(x), Cin, T, _d(w), None if bb is None else _d(bb), Cout, K, dil,
+                           pad_left, pad_right, _d(y))
+    assert rc == 0
+    return y
+
+
+def conv_transpose1d(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray], stride: int,
+                     pad_left: int, T_out: int) -> np.ndarray:
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    Cin, T = x.shape
+    Cin2, Cout, K = w.shape
+    assert Cin2 == Cin
+    y = np.empty((Cout, T_out), dtype=np.float64)
+    bb = None if b is None else np.ascontiguousarray(b, dtype=np.float64)
+    rc = lib.oracle_conv_transpose1d(_d(x), Cin, T, _d(w), None if bb is None else _d(bb), Cout, K,
+                                     stride, pad_left, T_out, _d(y))
+    assert rc == 0
+    return y
+
+
+def fold_params(params: Sequence) -> list:
+    """Raw canonical parameters (RawConv / alpha arrays) -> list of double arrays
+    (folded weight, bias, alpha, ...) in the canonical order."""
+    out = []
+    for p in params:
+        if hasattr(p, "g"):
+            out.append(fold_weight_norm(p.g, p.v))
+            out.append(None if p.b is None else np.ascontiguousarray(p.b, dtype=np.float64))
+        else:
+            out.append(np.ascontiguousarray(p, dtype=np.float64))
+    return out
+
+
+def decode(arch, params: Sequence, latent: np.ndarray, flags: int = 0, folded: Optional[list] = None,
+           return_pre_tanh: bool = False):
+    """Full decode of latent [B, C_lat, T] -> audio [B, T*hop] (double)."""
+    lib = _load()
+    if folded is None:
+        folded = fold_params(params)
+    latent = np.ascontiguousarray(latent, dtype=np.float32)
+    B, Cl, T = latent.shape
+    assert Cl == arch.latent_channels
+    strides = (ctypes.c_int * len(arch.strides))(*arch.strides)
+    widths = (ctypes.c_int * len(arch.widths))(*arch.widths)
+    dils = (ctypes.c_int * len(arch.dilations))(*arch.dilations)
+    a = _ArchC(arch.latent_channels, arch.channels0, arch.in_kernel, len(arch.strides), strides,
+               widths, len(arch.dilations), dils, arch.res_kernel, arch.out_kernel, arch.padding,
+               flags)
+    n = lib.oracle_param_count(ctypes.byref(a))
+    assert n == len(folded), (n, len(folded))
+    ptrs = (ctypes.POINTER(ctypes.c_double) * n)()
+    for i, t in enumerate(folded):
+        ptrs[i] = ctypes.cast(None, ctypes.POINTER(ctypes.c_double)) if t is None else _d(t)
+    hop = int(np.prod(arch.strides))
+    audio = np.empty((B, T * hop), dtype=np.float64)
+    pre = np.empty((B, T * hop), dtype=np.float64) if return_pre_tanh else None
+    rc = lib.oracle_decode(ctypes.byref(a), ptrs, _f(latent), B, T, _d(audio),
+                           None if pre is None else _d(pre))
+    if rc != 0:
+        raise RuntimeError(f"oracle_decode failed ({rc})")
+    return (audio, pre) if return_pre_tanh else audio
+
+
+def stitched_length(n_win, win_frames, crop_left, crop_right, hop) -> int:
+    return int(_load().oracle_stitched_length(n_win, win_frames, crop_left, crop_right, hop))
+
+
+def stitch(decoded: np.ndarray, n_win: int, n_sides: int, win_frames: int, crop_left: int,
+           crop_right: int, hop: int) -> np.ndarray:
+    lib = _load()
+    decoded = np.ascontiguousarray(decoded, dtype=np.float64)
+    n = stitched_length(n_win, win_frames, crop_left, crop_right, hop)
+    if n < 0:
+        raise ValueError("bad stitch geometry")
+    out = np.empty((n_sides, n), dtype=np.float64)
+    rc = lib.oracle_stitch(_d(decoded), n_win, n_sides, win_frames, crop_left, crop_right, hop,
+                           _d(out))
+    assert rc == 0
+    return out

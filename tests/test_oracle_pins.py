@@ -1,0 +1,432 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: a closed form,
+a library routine (numpy / torch CPU in fp64) on small cases, an adjoint
+identity, a dense brute force, linearity, an impulse response built with
+np.convolve, shift equivariance, locality from the layer list, causality, or a
+value the pages print.  A plausible slip in the oracle (a dropped term, a wrong
+sign, index, padding or operand order) fails at least one of them."""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from dac_vocoder_decode_gb300 import workloads as W
+from oracle import oracle as O
+from tests.util import frame_margins, latent_span
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+SMALL_MUSIC = W.Arch(latent_channels=4, channels0=8, strides=(8, 8, 4, 2), widths=(8, 4, 4, 4))
+SMALL_SPEECH = W.Arch(latent_channels=4, channels0=8, strides=(8, 5, 4, 4, 3),
+                      widths=(8, 4, 4, 4, 4), padding=W.PAD_CAUSAL)
+
+
+# --------------------------------------------------------------------------- Snake
+@pytest.mark.parametrize("alpha", [0.5, 1.0, 2.0, 1.37])
+def test_snake_closed_form_points(alpha):
+    """x = 0 -> 0; x = k*pi/alpha -> x (sin^2 vanishes); x = pi/(2 alpha) -> x + 1/(alpha + 1e-9)."""
+    x = np.array([[0.0, math.pi / alpha, -3 * math.pi / alpha, 7 * math.pi / alpha,
+                   math.pi / (2 * alpha), -math.pi / (2 * alpha)]])
+    y = O.snake(x, np.array([alpha]))[0]
+    inv_b = 1.0 / (alpha + 1e-9)
+    assert y[0] == 0.0
+    np.testing.assert_allclose(y[1:4], x[0, 1:4], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(y[4], x[0, 4] + inv_b, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(y[5], x[0, 5] + inv_b, rtol=0, atol=1e-13)
+
+
+def test_snake_reads_alpha_verbatim():
+    """MiniMax-Music-3 -> CMF README ("What the conversion had to get right"):
+    alpha is used as stored, not exponentiated.  With alpha = 2 the peak of
+    sin^2 sits at pi/4 and adds 1/2; an exp(alpha) reading would not."""
+    y = O.snake(np.array([[math.pi / 4]]), np.array([2.0]))[0, 0]
+    assert abs(y - (math.pi / 4 + 0.5)) < 1e-9
+    a = math.exp(2.0)
+    y_exp = math.pi / 4 + math.sin(a * math.pi / 4) ** 2 / a
+    assert abs(y - y_exp) > 0.1
+
+
+def test_snake_period_and_identity():
+    """sin^2 has period pi/alpha, so Snake(x + pi/alpha) = Snake(x) + pi/alpha."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 50)) * 4
+    alpha = np.array([0.6, 1.1, 1.45])
+    y = O.snake(x, alpha)
+    y2 = O.snake(x + (math.pi / alpha)[:, None], alpha)
+    np.testing.assert_allclose(y2 - y, np.broadcast_to((math.pi / alpha)[:, None], y.shape),
+                               atol=1e-12)
+    assert np.all(y - x >= 0)  # the added term is a square over a positive alpha
+    np.testing.assert_array_equal(O.snake(x, alpha, identity=True), x)
+
+
+# --------------------------------------------------------------------------- weight norm
+def test_fold_row_norm_is_abs_g():
+    rng = np.random.default_rng(1)
+    v = rng.standard_normal((6, 5, 7)).astype(np.float32)
+    g = rng.standard_normal(6).astype(np.float32)
+    w = O.fold_weight_norm(g, v)
+    norms = np.sqrt((w.reshape(6, -1) ** 2).sum(1))
+    np.testing.assert_allclose(norms, np.abs(g.astype(np.float64)), rtol=1e-14)
+    # direction of each row is that of v (times the sign of g)
+    vd = v.reshape(6, -1).astype(np.float64)
+    cos = (w.reshape(6, -1) * vd).sum(1) / (norms * np.sqrt((vd ** 2).sum(1)))
+    np.testing.assert_allclose(cos, np.sign(g), atol=1e-13)
+
+
+def test_fold_scale_invariant_and_axis0():
+    """w does not change under v -> c v (c > 0); the norm runs over axis 0 of the
+    stored tensor, so for a ConvTranspose1d [Cin, Cout, K] it is per input channel."""
+    rng = np.random.default_rng(2)
+    v = rng.standard_normal((4, 3, 6)).astype(np.float32)  # ConvT layout [Cin, Cout, K]
+    g = np.array([0.5, 1.0, 2.0, 3.0], dtype=np.float32)
+    w1 = O.fold_weight_norm(g, v)
+    w2 = O.fold_weight_norm(g, (v * np.float32(4.0)))
+    np.testing.assert_allclose(w1, w2, rtol=1e-6)
+    per_cin = np.sqrt((w1 ** 2).sum(axis=(1, 2)))
+    np.testing.assert_allclose(per_cin, g, rtol=1e-14)
+    # cross-check with torch's weight-norm parametrisation (dim 0), fp64
+    wt = torch._weight_norm(torch.from_numpy(v.astype(np.float64)),
+                            torch.from_numpy(g.astype(np.float64)).view(4, 1, 1), 0)
+    np.testing.assert_allclose(w1, wt.numpy(), rtol=1e-13, atol=1e-15)
+
+
+def test_fold_zero_row_rejected():
+    v = np.zeros((2, 3), dtype=np.float32)
+    v[0] = 1
+    with pytest.raises(ValueError):
+        O.fold_weight_norm(np.ones(2, np.float32), v)
+
+
+# --------------------------------------------------------------------------- conv1d
+@pytest.mark.parametrize("K,d,pl,pr", [(7, 1, 3, 3), (7, 3, 9, 9), (7, 9, 27, 27), (1, 1, 0, 0),
+                                       (7, 9, 54, 0), (3, 2, 0, 0)])
+def test_conv1d_matches_library_and_correlate(K, d, pl, pr):
+    rng = np.random.default_rng(K * 100 + d)
+    Cin, Cout, T = 3, 4, 70
+    x = rng.standard_normal((Cin, T))
+    w = rng.standard_normal((Cout, Cin, K))
+    b = rng.standard_normal(Cout)
+    y = O.conv1d(x, w, b, d, pl, pr)
+    # torch (fp64, CPU) with explicit zero padding
+    xt = torch.nn.functional.pad(torch.from_numpy(x)[None], (pl, pr))
+    yt = torch.nn.functional.conv1d(xt, torch.from_numpy(w), torch.from_numpy(b), dilation=d)[0]
+    np.testing.assert_allclose(y, yt.numpy(), rtol=0, atol=1e-12)
+    # numpy: correlate each channel pair with the dilated kernel
+    xp = np.pad(x, ((0, 0), (pl, pr)))
+    ref = np.zeros_like(y) + b[:, None]
+    for co in range(Cout):
+        for ci in range(Cin):
+            kd = np.zeros(d * (K - 1) + 1)
+            kd[::d] = w[co, ci]
+            ref[co] += np.correlate(xp[ci], kd, mode="valid")
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-12)
+
+
+def test_conv1d_impulse_picks_kernel_taps():
+    """A unit impulse at position t0 returns the kernel taps reversed in time:
+    y[co][t0 + pl - k d] = w[co][0][k]."""
+    K, d, pl = 7, 3, 9
+    x = np.zeros((1, 80))
+    x[0, 40] = 1.0
+    w = np.arange(1, 8, dtype=np.float64).reshape(1, 1, 7)
+    y = O.conv1d(x, w, None, d, pl, pl)[0]
+    for k in range(K):
+        assert y[40 + pl - k * d] == w[0, 0, k]
+    assert np.count_nonzero(y) == K
+
+
+# --------------------------------------------------------------------------- transposed conv
+@pytest.mark.parametrize("s,causal", [(2, False), (4, False), (8, False), (5, True), (3, True),
+                                      (8, True)])
+def test_conv_transpose_scatter_matches_library_and_zero_stuffing(s, causal):
+    rng = np.random.default_rng(s * 10 + causal)
+    Cin, Cout, T = 3, 2, 23
+    K = 2 * s
+    p = 0 if causal else s // 2
+    x = rng.standard_normal((Cin, T))
+    w = rng.standard_normal((Cin, Cout, K))
+    b = rng.standard_normal(Cout)
+    T_out = T * s
+    y = O.conv_transpose1d(x, w, b, s, p, T_out)
+    # (a) torch fp64: full transposed conv, then crop p on the left and keep T*s
+    full = torch.nn.functional.conv_transpose1d(torch.from_numpy(x)[None], torch.from_numpy(w),
+                                                torch.from_numpy(b), stride=s)[0].numpy()
+    assert full.shape[1] == (T - 1) * s + K
+    np.testing.assert_allclose(y, full[:, p:p + T_out], rtol=0, atol=1e-12)
+    # (b) textbook identity: zero-stuff x by s, convolve with the kernel, crop
+    ref = np.zeros((Cout, T_out)) + b[:, None]
+    for co in range(Cout):
+        for ci in range(Cin):
+            up = np.zeros(T * s)
+            up[::s] = x[ci]
+            c = np.convolve(up, w[ci, co])  # c[j] = sum_k w[k] up[j-k]
+            ref[co] += c[p:p + T_out]
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("s", [2, 4, 8])
+def test_conv_transpose_is_adjoint_of_strided_conv(s):
+    """<ConvT_w(x), y> = <x, Conv_w,stride s(y)> with the same weights and no bias;
+    the strided conv is built here by dense brute force from its definition."""
+    rng = np.random.default_rng(77 + s)
+    Cin, Cout, T = 3, 2, 11
+    K, p = 2 * s, s // 2
+    x = rng.standard_normal((Cin, T))
+    w = rng.standard_normal((Cin, Cout, K))
+    yv = rng.standard_normal((Cout, T * s))
+    lhs = np.sum(O.conv_transpose1d(x, w, None, s, p, T * s) * yv)
+    z = np.zeros((Cin, T))  # z[ci][t] = sum_co sum_k w[ci][co][k] y[co][t s + k - p]
+    for ci in range(Cin):
+        for t in range(T):
+            for co in range(Cout):
+                for k in range(K):
+                    j = t * s + k - p
+                    if 0 <= j < T * s:
+                        z[ci, t] += w[ci, co, k] * yv[co, j]
+    rhs = np.sum(x * z)
+    assert abs(lhs - rhs) < 1e-10 * max(1.0, abs(lhs))
+
+
+def test_col2im_length_formula():
+    """qwentts.cpp Architecture, "Custom GGML ops": T_out = (T_in - 1) s + K - 2p;
+    with K = 2s and p = s/2 that is T_in * s."""
+    for s in (2, 4, 8):
+        for T in (1, 5, 689):
+            assert (T - 1) * s + 2 * s - 2 * (s // 2) == T * s
+
+
+# --------------------------------------------------------------------------- decoder
+def _small_workload(arch, B=2, T=40, seed=11, recipe="calibrated"):
+    return W.make_custom(arch, B, T, seed, recipe)
+
+
+def test_pages_lengths_golden():
+    """The pages' own numbers: 12 latent frames -> 6144 samples per side at hop 512
+    (MiniMax-Music-3 -> CMF README, "What is verified, and how"); the speech codec
+    turns each 12.5 Hz frame into 1920 samples at 24 kHz (qwentts.cpp Architecture,
+    "Audio tokenizer decoder")."""
+    with open(os.path.join(GOLDEN, "pages_values.json")) as f:
+        g = json.load(f)
+    wl = _small_workload(SMALL_MUSIC, B=2, T=g["music_frames"], seed=3)
+    y = O.decode(wl.arch, wl.params, wl.latent)
+    assert y.shape == (2, g["music_samples_per_side"])
+    assert wl.arch.hop == g["music_hop"] == W.MUSIC.hop
+    assert W.SPEECH.hop == g["speech_hop"]
+    assert np.all(np.abs(y) <= 1.0)
+    assert np.std(y) > 1e-3  # above silence
+    assert np.max(np.abs(y[0] - y[1])) > 0  # left differs from right
+
+
+def test_tiny_workload_length():
+    wl = W.make_workload("tiny")
+    y = O.decode(wl.arch, wl.params, wl.latent)
+    assert y.shape == (1, 16384)
+    assert np.all(np.isfinite(y)) and np.all(np.abs(y) <= 1)
+
+
+def test_decoder_linearity_without_nonlinearities():
+    """Snake -> identity, tanh removed, biases 0: D(a x + b y) = a D(x) + b D(y)."""
+    wl = _small_workload(SMALL_MUSIC, B=1, T=24, seed=5)
+    params = [W.RawConv(p.g, p.v, None) if isinstance(p, W.RawConv) else p for p in wl.params]
+    fl = O.FLAG_SNAKE_IDENTITY | O.FLAG_NO_TANH
+    rng = np.random.default_rng(9)
+    # multiples of 1/64: a x + b y below is then exact in fp32 (no input rounding)
+    x = (np.round(rng.standard_normal(wl.latent.shape) * 64) / 64).astype(np.float32)
+    y = (np.round(rng.standard_normal(wl.latent.shape) * 64) / 64).astype(np.float32)
+    a, b = 0.75, -1.25
+    comb = (np.float64(a) * x + np.float64(b) * y)
+    assert np.all(comb.astype(np.float32) == comb)
+    folded = O.fold_params(params)
+    dx = O.decode(wl.arch, params, x, fl, folded)
+    dy = O.decode(wl.arch, params, y, fl, folded)
+    dc = O.decode(wl.arch, params, comb.astype(np.float32), fl, folded)
+    np.testing.assert_allclose(dc, a * dx + b * dy, rtol=0, atol=1e-11 * np.max(np.abs(dc)))
+
+
+def _impulse_response_closed_form(arch, folded, T, t0):
+    """The decoder with every width 1, Snake = identity, no tanh and no bias is a
+    multirate LTI chain.  Build its response to a unit impulse at frame t0 with
+    np.convolve: a k-tap conv with left pad pl is y[t] = sum_k w[k] x[t + k d - pl];
+    a transposed conv is (zero-stuffed x) convolved with w, cropped by p; a
+    residual unit is x + w2 * conv1(x)."""
+    def corr(x, w, d, pl):
+        K = len(w)
+        kd = np.zeros(d * (K - 1) + 1)
+        kd[::d] = w
+        # y[t] = sum_m kd[m] x[t + m - pl]  ->  full convolution with the reversed kernel
+        full = np.convolve(x, kd[::-1])  # full[n] = sum_m kd[m] x[n - (len-1) + m]
+        off = len(kd) - 1 - pl
+        out = np.zeros(len(x))
+        for t in range(len(x)):
+            n = t + off
+            if 0 <= n < len(full):
+                out[t] = full[n]
+        return out
+
+    causal = arch.padding == W.PAD_CAUSAL
+    def pad_l(K, d):
+        return d * (K - 1) if causal else d * (K - 1) // 2
+
+    x = np.zeros(T)
+    x[t0] = 1.0
+    it = iter(folded)
+    w_in = next(it); next(it)
+    x = corr(x, w_in[0, 0], 1, pad_l(arch.in_kernel, 1))
+    for s in arch.strides:
+        next(it)  # alpha
+        wt = next(it); next(it)
+        up = np.zeros(len(x) * s)
+        up[::s] = x
+        c = np.convolve(up, wt[0, 0])
+        p = 0 if causal else s // 2
+        x = c[p:p + len(up)]
+        for d in arch.dilations:
+            next(it); w1 = next(it); next(it); next(it); w2 = next(it); next(it)
+            x = x + w2[0, 0, 0] * corr(x, w1[0, 0], d, pad_l(arch.res_kernel, d))
+    next(it)
+    w_out = next(it)
+    return corr(x, w_out[0, 0], 1, pad_l(arch.out_kernel, 1))
+
+
+@pytest.mark.parametrize("arch", [
+    W.Arch(latent_channels=1, channels0=1, strides=(8, 8, 4, 2), widths=(1, 1, 1, 1)),
+    W.Arch(latent_channels=1, channels0=1, strides=(8, 5, 4, 4, 3), widths=(1, 1, 1, 1, 1),
+           padding=W.PAD_CAUSAL)], ids=["music", "speech_causal"])
+def test_impulse_response_width_one(arch):
+    wl = _small_workload(arch, B=1, T=30, seed=21)
+    params = [W.RawConv(p.g, p.v, None) if isinstance(p, W.RawConv) else p for p in wl.params]
+    folded = O.fold_params(params)
+    lat = np.zeros((1, 1, 30), dtype=np.float32)
+    lat[0, 0, 13] = 1.0
+    y = O.decode(arch, params, lat, O.FLAG_SNAKE_IDENTITY | O.FLAG_NO_TANH, folded)[0]
+    ref = _impulse_response_closed_form(arch, folded, 30, 13)
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-12 * max(1.0, np.max(np.abs(ref))))
+    assert np.max(np.abs(ref)) > 0
+
+
+def test_shift_equivariance():
+    """Shifting the latent by one frame shifts the audio by hop samples, away from
+    the ends (holds for the full nonlinear decoder)."""
+    arch = SMALL_MUSIC
+    wl = _small_workload(arch, B=1, T=48, seed=31)
+    folded = O.fold_params(wl.params)
+    lat = wl.latent
+    lat2 = np.concatenate([np.zeros_like(lat[:, :, :1]), lat[:, :, :-1]], axis=2)
+    y = O.decode(arch, wl.params, lat, 0, folded)[0]
+    y2 = O.decode(arch, wl.params, lat2, 0, folded)[0]
+    left, right = frame_margins(arch)
+    hop = arch.hop
+    lo, hi = (left + 2) * hop, (48 - right - 2) * hop
+    np.testing.assert_allclose(y2[lo + hop:hi + hop], y[lo:hi], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("arch", [SMALL_MUSIC, SMALL_SPEECH], ids=["music", "speech_causal"])
+def test_locality_from_layer_list(arch):
+    """Changing latent frame t0 changes exactly the samples whose receptive field
+    (derived from taps, dilations, strides and paddings) contains t0; every other
+    sample is bit-identical."""
+    T, t0 = 60, 30
+    wl = _small_workload(arch, B=1, T=T, seed=41)
+    folded = O.fold_params(wl.params)
+    y = O.decode(arch, wl.params, wl.latent, 0, folded)[0]
+    lat2 = wl.latent.copy()
+    lat2[0, :, t0] += 1.0
+    y2 = O.decode(arch, wl.params, lat2, 0, folded)[0]
+    changed = y != y2
+    hop = arch.hop
+    may = np.zeros(T * hop, dtype=bool)
+    for j in range(T * hop):
+        lo, hi = latent_span(arch, j)
+        may[j] = lo <= t0 <= hi
+    assert not np.any(changed & ~may)
+    assert np.any(changed)
+    if arch.padding == W.PAD_CAUSAL:
+        assert not np.any(changed[:t0 * hop])  # causality: nothing before the frame moves
+        assert changed[t0 * hop:(t0 + 1) * hop].any()
+
+
+def test_receptive_field_bound():
+    """The music decoder's receptive field is under 13 latent frames per side, so
+    crops of 86 / 258 frames leave every kept sample seam-exact."""
+    left, right = frame_margins(W.MUSIC)
+    assert left <= 13 and right <= 13
+    assert W.STITCH_CROP_LEFT > left and W.STITCH_CROP_RIGHT > right
+
+
+def test_batch_items_independent_and_stereo_fold():
+    """The decode of a batch equals the decodes of its items; a 128-channel latent
+    is two 64-channel tracks (channels 0..63 = left) decoded independently, and
+    the two sides differ (MiniMax-Music-3 -> CMF README, "What the conversion had
+    to get right"; minimaxmusic.cpp Architecture, "Flow VAE")."""
+    arch = SMALL_MUSIC
+    wl = _small_workload(arch, B=1, T=20, seed=51)
+    folded = O.fold_params(wl.params)
+    rng = np.random.default_rng(3)
+    stereo = rng.standard_normal((1, 2 * arch.latent_channels, 20)).astype(np.float32)
+    folded_lat = stereo.reshape(2, arch.latent_channels, 20)  # [b,2C,t] -> [2b,C,t]
+    yb = O.decode(arch, wl.params, folded_lat, 0, folded)
+    yl = O.decode(arch, wl.params, stereo[:, :arch.latent_channels], 0, folded)
+    yr = O.decode(arch, wl.params, stereo[:, arch.latent_channels:], 0, folded)
+    np.testing.assert_array_equal(yb[0], yl[0])
+    np.testing.assert_array_equal(yb[1], yr[0])
+    assert np.max(np.abs(yb[0] - yb[1])) > 1e-3
+
+
+def test_calibrated_tiny_is_nonlinear_and_unsaturated():
+    """The calibrated synthetic weights give a pre-tanh signal with RMS in
+    [0.05, 1], so the tests exercise the nonlinear regime without saturating."""
+    wl = W.make_workload("tiny_cal")
+    y, pre = O.decode(wl.arch, wl.params, wl.latent, return_pre_tanh=True)
+    rms = float(np.sqrt(np.mean(pre ** 2)))
+    assert 0.05 <= rms <= 1.0, rms
+    yl = O.decode(wl.arch, wl.params, wl.latent, O.FLAG_SNAKE_IDENTITY)
+    assert np.max(np.abs(yl - y)) > 1e-2  # Snake matters
+
+
+# --------------------------------------------------------------------------- stitch
+def test_stitch_length_and_clamp():
+    assert O.stitched_length(8, 689, 86, 258, 512) == 3104 * 512 == 1589248
+    assert O.stitched_length(1, 689, 86, 258, 512) == 689 * 512
+    dec = np.full((2, 5 * 4), 2.0)
+    dec[1] = -3.0
+    out = O.stitch(dec, 1, 2, 5, 1, 1, 4)
+    np.testing.assert_array_equal(out, np.stack([np.ones(20), -np.ones(20)]))
+
+
+def test_stitch_piece_positions():
+    """Window w contributes frames [w == 0 ? 0 : cl, w == last ? W : W - cr)."""
+    n_win, n_sides, Wf, cl, cr, hop = 3, 2, 10, 2, 3, 4
+    dec = np.zeros((n_win * n_sides, Wf * hop))
+    for w in range(n_win):
+        for side in range(n_sides):
+            dec[w * n_sides + side] = (w * 10 + side + np.arange(Wf * hop) / 1000.0) / 100.0
+    out = O.stitch(dec, n_win, n_sides, Wf, cl, cr, hop)
+    assert out.shape == (2, (7 + 5 + 8) * hop)
+    np.testing.assert_array_equal(out[1, :7 * hop], dec[1, :7 * hop])
+    np.testing.assert_array_equal(out[0, 7 * hop:12 * hop], dec[2, cl * hop:(Wf - cr) * hop])
+    np.testing.assert_array_equal(out[1, 12 * hop:], dec[5, cl * hop:])
+
+
+@pytest.mark.slow
+def test_windowed_stitch_equals_single_pass():
+    """Windows cut at hop 345 from one continuous latent, decoded and stitched
+    with crops 86 / 258, equal a single pass over the whole latent: every kept
+    sample lies more than the receptive field away from its window's edges."""
+    arch = W.Arch(latent_channels=4, channels0=4, strides=(8, 8, 4, 2), widths=(4, 2, 2, 2))
+    wl = _small_workload(arch, B=1, T=8, seed=61)
+    folded = O.fold_params(wl.params)
+    rng = np.random.default_rng(62)
+    total = W.STITCH_HOP_FRAMES * (W.STITCH_WINDOWS - 1) + W.STITCH_WIN_FRAMES
+    cont = rng.standard_normal((2, 4, total)).astype(np.float32)
+    wins = np.stack([cont[side, :, w * 345:w * 345 + 689] for w in range(8) for side in range(2)])
+    dec = O.decode(arch, wl.params, wins, 0, folded)
+    st = O.stitch(dec, 8, 2, 689, 86, 258, arch.hop)
+    full = O.decode(arch, wl.params, cont, 0, folded)
+    assert st.shape == full.shape == (2, 1589248)
+    np.testing.assert_allclose(st, full, rtol=0, atol=1e-13)
