@@ -1,0 +1,345 @@
+"""ctypes binding of libvocoder.so (include/vocoder.h), with the same entry-point names.
+
+Argument marshalling only: every step of the decode runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  If the compiled library
+is missing this module raises instead of falling back to anything else; build
+it with ``python -m dac_vocoder_decode_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+from . import build as _build
+
+VOC_ABI_VERSION = 1
+VOC_OK = 0
+VOC_INVALID_ARG = -1
+VOC_UNSUPPORTED = -2
+VOC_CUDA_ERROR = -3
+VOC_OOM = -4
+VOC_WORKSPACE_TOO_SMALL = -5
+VOC_NONFINITE = -6
+VOC_CANCELLED = -7
+VOC_DEVICE_TIMEOUT = -8
+VOC_PAD_SYMMETRIC = 0
+VOC_PAD_CAUSAL = 1
+VOC_PREC_BF16X3 = 0
+VOC_FLAG_CHECK_FINITE = 1
+VOC_FLAG_SYNC = 2
+VOC_FLAG_PROFILE = 4
+
+STATUS_NAMES = {0: "VOC_OK", -1: "VOC_INVALID_ARG", -2: "VOC_UNSUPPORTED", -3: "VOC_CUDA_ERROR",
+                -4: "VOC_OOM", -5: "VOC_WORKSPACE_TOO_SMALL", -6: "VOC_NONFINITE",
+                -7: "VOC_CANCELLED", -8: "VOC_DEVICE_TIMEOUT"}
+
+EXPORTED = [
+    "vocoder_abi_version", "vocoder_param_count", "vocoder_param_shape",
+    "vocoder_fold_weight_norm", "vocoder_create", "vocoder_hop", "vocoder_workspace_bytes",
+    "vocoder_workspace_bytes_host", "vocoder_decode", "vocoder_decode_host",
+    "vocoder_stitched_length", "vocoder_stitch", "vocoder_op_conv1d",
+    "vocoder_op_conv_transpose1d", "vocoder_launches_per_decode", "vocoder_profile_count",
+    "vocoder_profile_entry", "vocoder_last_error", "vocoder_destroy",
+]
+
+
+class VocoderError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class VocDesc(ctypes.Structure):
+    _fields_ = [("abi_version", ctypes.c_int), ("latent_channels", ctypes.c_int),
+                ("in_kernel", ctypes.c_int), ("channels0", ctypes.c_int),
+                ("n_stages", ctypes.c_int), ("strides", ctypes.POINTER(ctypes.c_int)),
+                ("widths", ctypes.POINTER(ctypes.c_int)), ("n_dilations", ctypes.c_int),
+                ("dilations", ctypes.POINTER(ctypes.c_int)), ("res_kernel", ctypes.c_int),
+                ("out_kernel", ctypes.c_int), ("out_channels", ctypes.c_int),
+                ("padding", ctypes.c_int), ("precision", ctypes.c_int)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Load libvocoder.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "`python -m dac_vocoder_decode_gb300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    F = ctypes.POINTER(ctypes.c_float)
+    lib.vocoder_abi_version.restype = I
+    lib.vocoder_abi_version.argtypes = []
+    lib.vocoder_param_count.restype = I
+    lib.vocoder_param_count.argtypes = [ctypes.POINTER(VocDesc)]
+    lib.vocoder_param_shape.restype = I
+    lib.vocoder_param_shape.argtypes = [ctypes.POINTER(VocDesc), I, ctypes.POINTER(I),
+                                        ctypes.POINTER(I)]
+    lib.vocoder_fold_weight_norm.restype = I
+    lib.vocoder_fold_weight_norm.argtypes = [F, F, I, ctypes.c_longlong, F]
+    lib.vocoder_create.restype = I
+    lib.vocoder_create.argtypes = [ctypes.POINTER(VocDesc), ctypes.POINTER(F), I,
+                                   ctypes.POINTER(P)]
+    lib.vocoder_hop.restype = ctypes.c_longlong
+    lib.vocoder_hop.argtypes = [P]
+    lib.vocoder_workspace_bytes.restype = ctypes.c_size_t
+    lib.vocoder_workspace_bytes.argtypes = [P, I, I]
+    lib.vocoder_workspace_bytes_host.restype = ctypes.c_size_t
+    lib.vocoder_workspace_bytes_host.argtypes = [P, I, I]
+    lib.vocoder_decode.restype = I
+    lib.vocoder_decode.argtypes = [P, P, I, I, P, P, ctypes.c_size_t, P, ctypes.c_uint]
+    lib.vocoder_decode_host.restype = I
+    lib.vocoder_decode_host.argtypes = [P, P, I, I, P, P, ctypes.c_size_t, P, ctypes.c_uint]
+    lib.vocoder_stitched_length.restype = ctypes.c_longlong
+    lib.vocoder_stitched_length.argtypes = [I, I, I, I, I]
+    lib.vocoder_stitch.restype = I
+    lib.vocoder_stitch.argtypes = [P, I, I, I, I, I, I, P, P]
+    lib.vocoder_op_conv1d.restype = I
+    lib.vocoder_op_conv1d.argtypes = [P, I, I, I, F, F, I, I, I, I, F, P, P]
+    lib.vocoder_op_conv_transpose1d.restype = I
+    lib.vocoder_op_conv_transpose1d.argtypes = [P, I, I, I, F, F, I, I, I, F, P, P]
+    lib.vocoder_launches_per_decode.restype = I
+    lib.vocoder_launches_per_decode.argtypes = [P, I, I]
+    lib.vocoder_profile_count.restype = I
+    lib.vocoder_profile_count.argtypes = [P]
+    lib.vocoder_profile_entry.restype = I
+    lib.vocoder_profile_entry.argtypes = [P, I, ctypes.POINTER(ctypes.c_char_p),
+                                          ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(ctypes.c_double)]
+    lib.vocoder_last_error.restype = ctypes.c_char_p
+    lib.vocoder_last_error.argtypes = [P]
+    lib.vocoder_destroy.restype = None
+    lib.vocoder_destroy.argtypes = [P]
+    _lib = lib
+    return lib
+
+
+def _check(status: int, handle=None):
+    if status != VOC_OK:
+        msg = load_library().vocoder_last_error(handle)
+        raise VocoderError(status, msg.decode() if msg else "")
+
+
+def _fptr(a: Optional[np.ndarray]):
+    if a is None:
+        return ctypes.cast(None, ctypes.POINTER(ctypes.c_float))
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    if hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    return ctypes.c_void_p(int(stream))
+
+
+def make_desc(arch) -> VocDesc:
+    """voc_desc for an Arch (layer shapes from workloads.Arch or any object with the same fields)."""
+    strides = (ctypes.c_int * len(arch.strides))(*arch.strides)
+    widths = (ctypes.c_int * len(arch.widths))(*arch.widths)
+    dils = (ctypes.c_int * len(arch.dilations))(*arch.dilations)
+    d = VocDesc(VOC_ABI_VERSION, arch.latent_channels, arch.in_kernel, arch.channels0,
+                len(arch.strides), strides, widths, len(arch.dilations), dils, arch.res_kernel,
+                arch.out_kernel, 1, arch.padding, VOC_PREC_BF16X3)
+    d._keep = (strides, widths, dils)
+    return d
+
+
+# ------------------------------------------------------------------ entry points
+def vocoder_abi_version() -> int:
+    return load_library().vocoder_abi_version()
+
+
+def vocoder_param_count(arch) -> int:
+    return load_library().vocoder_param_count(ctypes.byref(make_desc(arch)))
+
+
+def vocoder_param_shape(arch, index: int):
+    dims = (ctypes.c_int * 3)()
+    nd = ctypes.c_int()
+    _check(load_library().vocoder_param_shape(ctypes.byref(make_desc(arch)), index, dims,
+                                               ctypes.byref(nd)))
+    return tuple(dims[i] for i in range(nd.value))
+
+
+def vocoder_fold_weight_norm(g: np.ndarray, v: np.ndarray) -> np.ndarray:
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    w = np.empty_like(v)
+    rest = int(np.prod(v.shape[1:])) if v.ndim > 1 else 1
+    _check(load_library().vocoder_fold_weight_norm(_fptr(g), _fptr(v), int(v.shape[0]), rest,
+                                                    _fptr(w)))
+    return w
+
+
+def vocoder_create(arch, params: Sequence[Optional[np.ndarray]]) -> ctypes.c_void_p:
+    """params: folded fp32 arrays in the canonical order (None for a zero bias)."""
+    lib = load_library()
+    keep = [None if p is None else np.ascontiguousarray(p, dtype=np.float32) for p in params]
+    arr = (ctypes.POINTER(ctypes.c_float) * len(keep))(*[_fptr(p) for p in keep])
+    h = ctypes.c_void_p()
+    _check(lib.vocoder_create(ctypes.byref(make_desc(arch)), arr, len(keep), ctypes.byref(h)))
+    return h
+
+
+def vocoder_destroy(h) -> None:
+    load_library().vocoder_destroy(h)
+
+
+def vocoder_hop(h) -> int:
+    return int(load_library().vocoder_hop(h))
+
+
+def vocoder_workspace_bytes(h, B: int, T: int) -> int:
+    return int(load_library().vocoder_workspace_bytes(h, B, T))
+
+
+def vocoder_workspace_bytes_host(h, B: int, T: int) -> int:
+    return int(load_library().vocoder_workspace_bytes_host(h, B, T))
+
+
+def vocoder_launches_per_decode(h, B: int, T: int) -> int:
+    return int(load_library().vocoder_launches_per_decode(h, B, T))
+
+
+def vocoder_decode(h, latent, audio, ws, stream=None, flags: int = 0) -> None:
+    """latent [B,C,T] fp32 CUDA tensor -> audio [B,1,T*hop] fp32 CUDA tensor; ws uint8 CUDA tensor."""
+    B, _, T = latent.shape
+    _check(load_library().vocoder_decode(h, ctypes.c_void_p(latent.data_ptr()), B, T,
+                                          ctypes.c_void_p(audio.data_ptr()),
+                                          ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                          _stream_ptr(stream), flags), h)
+
+
+def vocoder_decode_host(h, latent_host, audio_host, ws, stream=None, flags: int = 0) -> None:
+    """Host (ideally pinned) CPU tensors in and out; copies happen inside the library."""
+    B, _, T = latent_host.shape
+    _check(load_library().vocoder_decode_host(h, ctypes.c_void_p(latent_host.data_ptr()), B, T,
+                                               ctypes.c_void_p(audio_host.data_ptr()),
+                                               ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                               _stream_ptr(stream), flags), h)
+
+
+def vocoder_stitched_length(n_win, win_frames, crop_left, crop_right, hop) -> int:
+    return int(load_library().vocoder_stitched_length(n_win, win_frames, crop_left, crop_right,
+                                                      hop))
+
+
+def vocoder_stitch(decoded, n_win, n_sides, win_frames, crop_left, crop_right, hop, out,
+                   stream=None) -> None:
+    _check(load_library().vocoder_stitch(ctypes.c_void_p(decoded.data_ptr()), n_win, n_sides,
+                                          win_frames, crop_left, crop_right, hop,
+                                          ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)))
+
+
+def vocoder_op_conv1d(x, w: np.ndarray, b: Optional[np.ndarray], dil: int, padding: int,
+                      alpha: Optional[np.ndarray], y, stream=None) -> None:
+    B, Cin, T = x.shape
+    Cout, _, K = w.shape
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    b = None if b is None else np.ascontiguousarray(b, dtype=np.float32)
+    alpha = None if alpha is None else np.ascontiguousarray(alpha, dtype=np.float32)
+    _check(load_library().vocoder_op_conv1d(ctypes.c_void_p(x.data_ptr()), B, Cin, T, _fptr(w),
+                                             _fptr(b), Cout, K, dil, padding, _fptr(alpha),
+                                             ctypes.c_void_p(y.data_ptr()), _stream_ptr(stream)))
+
+
+def vocoder_op_conv_transpose1d(x, w: np.ndarray, b: Optional[np.ndarray], stride: int,
+                                padding: int, alpha: Optional[np.ndarray], y,
+                                stream=None) -> None:
+    B, Cin, T = x.shape
+    _, Cout, K = w.shape
+    assert K == 2 * stride
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    b = None if b is None else np.ascontiguousarray(b, dtype=np.float32)
+    alpha = None if alpha is None else np.ascontiguousarray(alpha, dtype=np.float32)
+    _check(load_library().vocoder_op_conv_transpose1d(
+        ctypes.c_void_p(x.data_ptr()), B, Cin, T, _fptr(w), _fptr(b), Cout, stride, padding,
+        _fptr(alpha), ctypes.c_void_p(y.data_ptr()), _stream_ptr(stream)))
+
+
+def vocoder_profile(h) -> List[dict]:
+    """Per-kernel records of the last decode run with VOC_FLAG_PROFILE."""
+    lib = load_library()
+    out = []
+    for i in range(lib.vocoder_profile_count(h)):
+        name = ctypes.c_char_p()
+        ms, fl, by = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+        _check(lib.vocoder_profile_entry(h, i, ctypes.byref(name), ctypes.byref(ms),
+                                          ctypes.byref(fl), ctypes.byref(by)), h)
+        out.append(dict(name=name.value.decode(), ms=ms.value, flops=fl.value, bytes=by.value))
+    return out
+
+
+def vocoder_last_error(h=None) -> str:
+    m = load_library().vocoder_last_error(h)
+    return m.decode() if m else ""
+
+
+# ------------------------------------------------------------------ convenience
+def fold_params(params) -> list:
+    """Raw canonical parameters (weight-norm g/v pairs and alphas) -> folded fp32
+    arrays through the library's host fold (vocoder_fold_weight_norm)."""
+    out = []
+    for p in params:
+        if hasattr(p, "g"):
+            out.append(vocoder_fold_weight_norm(p.g, p.v))
+            out.append(None if p.b is None else np.ascontiguousarray(p.b, dtype=np.float32))
+        else:
+            out.append(np.ascontiguousarray(p, dtype=np.float32))
+    return out
+
+
+class Vocoder:
+    """A decoder on the current CUDA device (owns its library context)."""
+
+    def __init__(self, arch, folded_params):
+        self.arch = arch
+        self.handle = vocoder_create(arch, folded_params)
+        self.hop = vocoder_hop(self.handle)
+
+    def close(self):
+        if self.handle:
+            vocoder_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace_bytes(self, B: int, T: int) -> int:
+        return vocoder_workspace_bytes(self.handle, B, T)
+
+    def alloc_workspace(self, B: int, T: int, host_io: bool = False):
+        import torch
+        n = (vocoder_workspace_bytes_host if host_io else vocoder_workspace_bytes)(self.handle, B, T)
+        return torch.empty(n, dtype=torch.uint8, device="cuda")
+
+    def decode(self, latent, ws=None, audio=None, stream=None, flags: int = 0):
+        import torch
+        B, _, T = latent.shape
+        if ws is None:
+            ws = self.alloc_workspace(B, T)
+        if audio is None:
+            audio = torch.empty((B, 1, T * self.hop), dtype=torch.float32, device=latent.device)
+        vocoder_decode(self.handle, latent, audio, ws, stream, flags)
+        return audio

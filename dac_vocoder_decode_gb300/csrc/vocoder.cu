@@ -1,0 +1,987 @@
+// vocoder.cu -- C ABI of the GB300 vocoder decoder (declared in include/vocoder.h):
+// validation, weight folding and packing, workspace planning, TMA descriptors and
+// the launch sequence of one decode.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "vocoder.h"
+#include "conv_gemm.cuh"
+#include "stream_kernels.cuh"
+
+#define VOC_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using voc::ConvGemmArgs;
+
+constexpr int kSmemMax = 227 * 1024;         // opt-in shared memory per block
+constexpr long long kWaitBudget = 4000000000LL;  // cycles (~2 s) before a wait gives up
+constexpr int kHeadTile = 128;
+
+thread_local std::string g_err;  // last error without a context
+
+int rup(int x, int m) { return (x + m - 1) / m * m; }
+size_t rupz(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+uint16_t f2bf(float f) {  // round to nearest even (finite inputs)
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+float bf2f(uint16_t h) {
+  uint32_t u = static_cast<uint32_t>(h) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+enum Buf { BUF_H0 = 0, BUF_H1 = 1, BUF_HB = 2, BUF_FY = 3, BUF_COUNT = 4 };
+
+struct Layer {
+  std::string name;
+  bool convT = false;
+  int Cin = 0, Cout = 0, Cp_in = 0, Cp_out = 0, K = 0, dil = 1, stride = 1;
+  int level = 0;            // input rate: L_in = T * prod(strides[0..level-1])
+  ConvGemmArgs g{};         // geometry; sizes and pointers filled per launch
+  size_t smem = 0;
+  uint8_t *w_dev = nullptr;
+  float *bias_dev = nullptr, *alpha_dev = nullptr, *invb_dev = nullptr;
+  int in_buf = -1, f32_buf = -1, hl_buf = -1, skip_buf = -1;
+  int epi_flags = 0;
+};
+
+struct OutHead {
+  int C = 0, Cp = 0, K = 0, pad_left = 0, level = 0;
+  float *w_dev = nullptr, *b_dev = nullptr;
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool set_kernel_attrs(std::string &why) {
+  static cudaError_t st = cudaErrorUnknown;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    st = cudaFuncSetAttribute(voc::conv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemMax);
+    if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(voc::out_head_kernel<kHeadTile>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  });
+  if (st != cudaSuccess) why = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(st);
+  return st == cudaSuccess;
+}
+
+}  // namespace
+
+struct vocoder {
+  voc_desc desc{};
+  std::vector<int> strides, widths, dils;
+  int device = 0, num_sms = 0;
+  int Cp_lat = 0;
+  long long hop = 1;
+  std::vector<Layer> layers;
+  OutHead head;
+  std::vector<void *> allocs;
+  std::string err;
+  int *err_dev = nullptr;   // device error word of the kernels (bounded waits)
+  int *flag_dev = nullptr;  // finite-check flag
+  long long wait_budget = kWaitBudget;
+  // TMA descriptors for the last (workspace, B, T)
+  void *map_ws = nullptr;
+  int map_B = -1, map_T = -1;
+  std::vector<CUtensorMap> maps;
+  // profiling of the last decode with VOC_FLAG_PROFILE
+  std::vector<cudaEvent_t> events;
+  std::vector<std::string> prof_names;
+  std::vector<double> prof_flops, prof_bytes;
+  std::vector<float> prof_ms;
+  int prof_n = 0;
+  bool prof_ready = false;
+};
+
+namespace {
+
+voc_status fail(vocoder *ctx, voc_status st, const std::string &msg) {
+  if (ctx)
+    ctx->err = msg;
+  else
+    g_err = msg;
+  return st;
+}
+
+voc_status cuda_fail(vocoder *ctx, cudaError_t e, const char *what) {
+  return fail(ctx, e == cudaErrorMemoryAllocation ? VOC_OOM : VOC_CUDA_ERROR,
+              std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------------ planning
+// Plan the GEMM geometry of one conv (convT = false) or transposed conv layer.
+bool plan_gemm(Layer &L, int padding, std::string &why) {
+  ConvGemmArgs &g = L.g;
+  L.Cp_in = rup(L.Cin, 16);
+  L.Cp_out = rup(L.Cout, 16);
+  g.Cp_in = L.Cp_in;
+  g.Cp_out = L.Cp_out;
+  g.KB = (L.Cp_in % 32 == 0) ? 32 : 16;
+  g.nkb = L.Cp_in / g.KB;
+  int group, off_min, off_max;
+  if (L.convT) {
+    const int s = L.stride;
+    g.taps = 2;
+    g.N_total = s * L.Cp_out;
+    g.s_rows = s;
+    if (padding == VOC_PAD_SYMMETRIC) {
+      // phases r < s/2 read rows t and t-1 (q = 0), phases r >= s/2 rows t+1 and t (q = 1)
+      group = (s / 2) * L.Cp_out;
+      off_min = -1, off_max = 1;
+      g.shift0_q0 = 1, g.shift0_q1 = 2;
+    } else {
+      group = g.N_total;  // causal: every phase reads rows t and t-1
+      off_min = -1, off_max = 0;
+      g.shift0_q0 = 1, g.shift0_q1 = 1;
+    }
+    g.tap_step = -1;
+  } else {
+    const int span = L.dil * (L.K - 1);
+    const int pad_left = (padding == VOC_PAD_CAUSAL) ? span : span / 2;
+    g.taps = L.K;
+    g.N_total = L.Cp_out;
+    g.s_rows = 1;
+    group = g.N_total;
+    off_min = -pad_left, off_max = span - pad_left;
+    g.shift0_q0 = g.shift0_q1 = 0;
+    g.tap_step = L.dil;
+  }
+  g.N_tile = 0;
+  for (int t = 256; t >= 16; t -= 16)
+    if (group % t == 0) {
+      g.N_tile = t;
+      break;
+    }
+  if (!g.N_tile) {
+    why = "no column tile divides " + std::to_string(group);
+    return false;
+  }
+  g.n_tiles = g.N_total / g.N_tile;
+  g.q_split_tile = (L.convT && padding == VOC_PAD_SYMMETRIC) ? group / g.N_tile : g.n_tiles;
+  g.off_min = off_min;
+  g.rows = rup(voc::kTileM + off_max - off_min, 8);
+  if (g.rows > 256) {
+    why = "tap span too wide for one staged tile (" + std::to_string(off_max - off_min) + ")";
+    return false;
+  }
+  const int chunkA = g.rows * 16;
+  g.a_bytes = rup(2 * (g.KB / 8) * chunkA, 1024);
+  g.b_bytes = 4 * g.KB * g.N_tile;
+  g.na = 2;
+  const int avail = kSmemMax - 1024 - 256 - g.na * g.a_bytes;
+  g.nb = std::min(8, avail / g.b_bytes);
+  if (g.nb < 2) {
+    why = "shared memory plan does not fit";
+    return false;
+  }
+  int ac = 32;
+  while (ac < g.N_tile) ac *= 2;
+  g.acc_cols = ac;
+  L.smem = 1024 + (size_t)g.na * g.a_bytes + (size_t)g.nb * g.b_bytes + 256;
+  return true;
+}
+
+// Value of the GEMM weight for column n, input channel ci, tap `tap`.
+float weight_value(const Layer &L, int padding, const float *w, int n, int ci, int tap) {
+  if (ci >= L.Cin) return 0.f;
+  if (!L.convT) {
+    if (n >= L.Cout) return 0.f;
+    return w[((size_t)n * L.Cin + ci) * L.K + tap];
+  }
+  const int s = L.stride;
+  const int r = n / L.Cp_out, co = n % L.Cp_out;
+  if (co >= L.Cout) return 0.f;
+  const int p = (padding == VOC_PAD_CAUSAL) ? 0 : s / 2;
+  const int k = (r + p) % s + tap * s;  // tap 0: k0 at row t+q, tap 1: k0+s at row t+q-1
+  return w[((size_t)ci * L.Cout + co) * (2 * s) + k];
+}
+
+std::vector<uint16_t> pack_weights(const Layer &L, int padding, const float *w) {
+  const ConvGemmArgs &g = L.g;
+  const size_t tile = (size_t)2 * g.KB * g.N_tile;
+  std::vector<uint16_t> out((size_t)g.n_tiles * g.taps * g.nkb * tile);
+  for (int nt = 0; nt < g.n_tiles; ++nt)
+    for (int tap = 0; tap < g.taps; ++tap)
+      for (int kb = 0; kb < g.nkb; ++kb) {
+        uint16_t *base = out.data() + (((size_t)nt * g.taps + tap) * g.nkb + kb) * tile;
+        for (int c = 0; c < g.KB / 8; ++c)
+          for (int n = 0; n < g.N_tile; ++n)
+            for (int e = 0; e < 8; ++e) {
+              const float v = weight_value(L, padding, w, nt * g.N_tile + n, kb * g.KB + c * 8 + e, tap);
+              const uint16_t hi = f2bf(v);
+              const uint16_t lo = f2bf(v - bf2f(hi));
+              const size_t idx = ((size_t)c * g.N_tile + n) * 8 + e;
+              base[idx] = hi;
+              base[(size_t)g.KB * g.N_tile + idx] = lo;
+            }
+      }
+  return out;
+}
+
+template <class T>
+voc_status upload(vocoder *ctx, std::vector<void *> &allocs, const std::vector<T> &host, T **dev) {
+  cudaError_t e = cudaMalloc(reinterpret_cast<void **>(dev), host.size() * sizeof(T));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMalloc");
+  allocs.push_back(*dev);
+  e = cudaMemcpy(*dev, host.data(), host.size() * sizeof(T), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemcpy");
+  return VOC_OK;
+}
+
+// Per-column epilogue vectors of a layer: bias, and the Snake of the layer that
+// consumes this output (alpha == nullptr: none).
+voc_status upload_columns(vocoder *ctx, std::vector<void *> &allocs, Layer &L, const float *bias,
+                          const float *alpha) {
+  const int N = L.g.N_total;
+  std::vector<float> b(N, 0.f), a(N, 1.f), ib(N, 0.f);
+  for (int n = 0; n < N; ++n) {
+    const int co = n % L.Cp_out;
+    if (co < L.Cout) {
+      if (bias) b[n] = bias[co];
+      if (alpha) {
+        a[n] = alpha[co];
+        ib[n] = static_cast<float>(1.0 / (static_cast<double>(alpha[co]) + 1e-9));
+      }
+    }
+  }
+  voc_status st = upload(ctx, allocs, b, &L.bias_dev);
+  if (st != VOC_OK) return st;
+  if (alpha) {
+    st = upload(ctx, allocs, a, &L.alpha_dev);
+    if (st != VOC_OK) return st;
+    st = upload(ctx, allocs, ib, &L.invb_dev);
+    if (st != VOC_OK) return st;
+  }
+  return VOC_OK;
+}
+
+voc_status upload_layer(vocoder *ctx, std::vector<void *> &allocs, Layer &L, int padding,
+                        const float *w, const float *bias, const float *alpha) {
+  std::vector<uint16_t> packed = pack_weights(L, padding, w);
+  uint16_t *wd = nullptr;
+  voc_status st = upload(ctx, allocs, packed, &wd);
+  if (st != VOC_OK) return st;
+  L.w_dev = reinterpret_cast<uint8_t *>(wd);
+  return upload_columns(ctx, allocs, L, bias, alpha);
+}
+
+bool check_desc(const voc_desc *d, std::string &why) {
+  if (!d) return why = "desc is NULL", false;
+  if (d->abi_version != VOC_ABI_VERSION)
+    return why = "abi_version " + std::to_string(d->abi_version) + " != " +
+                 std::to_string(VOC_ABI_VERSION),
+           false;
+  if (d->latent_channels < 1 || d->latent_channels > 8192) return why = "latent_channels", false;
+  if (d->channels0 < 1 || d->channels0 > 8192) return why = "channels0", false;
+  for (int k : {d->in_kernel, d->res_kernel, d->out_kernel})
+    if (k < 1 || k > 15 || k % 2 == 0) return why = "kernel sizes must be odd in [1, 15]", false;
+  if (d->n_stages < 1 || d->n_stages > 8) return why = "n_stages", false;
+  if (!d->strides || !d->widths) return why = "strides / widths NULL", false;
+  if (d->n_dilations < 1 || d->n_dilations > 4 || !d->dilations) return why = "dilations", false;
+  if (d->out_channels != 1) return why = "out_channels must be 1", false;
+  if (d->padding != VOC_PAD_SYMMETRIC && d->padding != VOC_PAD_CAUSAL) return why = "padding", false;
+  if (d->precision != VOC_PREC_BF16X3) return why = "precision", false;
+  for (int i = 0; i < d->n_stages; ++i) {
+    if (d->strides[i] < 1 || d->strides[i] > 16) return why = "stride out of [1, 16]", false;
+    if (d->padding == VOC_PAD_SYMMETRIC && d->strides[i] % 2)
+      return why = "odd stride needs VOC_PAD_CAUSAL (symmetric crop s/2)", false;
+    if (d->widths[i] < 1 || d->widths[i] > 8192) return why = "width out of range", false;
+  }
+  for (int j = 0; j < d->n_dilations; ++j)
+    if (d->dilations[j] < 1 || d->dilations[j] * (d->res_kernel - 1) > 120)
+      return why = "dilation * (res_kernel - 1) must be in [1, 120]", false;
+  if (d->in_kernel - 1 > 120 || d->out_kernel - 1 > 120) return why = "kernel too wide", false;
+  return true;
+}
+
+int param_count(const voc_desc *d) { return 2 + d->n_stages * (3 + 6 * d->n_dilations) + 3; }
+
+// kind of every canonical parameter: 'w' weight, 'b' bias, 'a' Snake alpha
+std::string param_kinds(const voc_desc *d) {
+  std::string k = "wb";
+  for (int i = 0; i < d->n_stages; ++i) {
+    k += "awb";
+    for (int j = 0; j < d->n_dilations; ++j) k += "awbawb";
+  }
+  return k + "awb";
+}
+
+// level lengths L_lv = T * prod(strides[0..lv-1])
+long long level_len(const vocoder *ctx, int lv, int T) {
+  long long L = T;
+  for (int i = 0; i < lv; ++i) L *= ctx->strides[i];
+  return L;
+}
+
+size_t buf_bytes(const vocoder *ctx, int B, int T) {
+  size_t m = (size_t)B * T * std::max(ctx->Cp_lat, rup(ctx->desc.channels0, 16));
+  for (int i = 0; i < ctx->desc.n_stages; ++i)
+    m = std::max(m, (size_t)B * (size_t)level_len(ctx, i + 1, T) * (size_t)rup(ctx->widths[i], 16));
+  return rupz(m * 4, 256);
+}
+
+voc_status encode_map(vocoder *ctx, CUtensorMap *map, const void *base, int Cp, long long L, int B,
+                      int rows) {
+  auto enc = encode_fn();
+  if (!enc) return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled entry point unavailable");
+  const cuuint64_t dims[3] = {(cuuint64_t)(2 * Cp), (cuuint64_t)L, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)(4 * Cp), (cuuint64_t)(4 * Cp) * (cuuint64_t)L};
+  const cuuint32_t box[3] = {8u, (cuuint32_t)rows, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+  return VOC_OK;
+}
+
+void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *const *bufs,
+                      ConvGemmArgs &a) {
+  a = L.g;
+  const long long L_in = level_len(ctx, L.level, T);
+  a.B = B;
+  a.L_in = static_cast<int>(L_in);
+  a.m_tiles = static_cast<int>((L_in + voc::kTileM - 1) / voc::kTileM);
+  a.wB = L.w_dev;
+  a.bias = L.bias_dev;
+  a.alpha = L.alpha_dev;
+  a.invb = L.invb_dev;
+  a.skip = L.skip_buf >= 0 ? static_cast<const float *>(bufs[L.skip_buf]) : nullptr;
+  a.out_f32 = L.f32_buf >= 0 ? static_cast<float *>(bufs[L.f32_buf]) : nullptr;
+  a.out_hl = L.hl_buf >= 0 ? static_cast<__nv_bfloat16 *>(bufs[L.hl_buf]) : nullptr;
+  a.flags = L.epi_flags;
+  a.timeout = ctx->wait_budget;
+  a.err = ctx->err_dev;
+}
+
+void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops, double &bytes) {
+  const double L_in = (double)level_len(ctx, L.level, T);
+  const double L_out = L_in * (L.convT ? L.stride : 1);
+  flops = L.convT ? 4.0 * L.Cin * L.Cout * B * L_out : 2.0 * L.Cin * L.Cout * L.K * B * L_in;
+  const ConvGemmArgs &g = L.g;
+  double by = 4.0 * B * L_in * L.Cp_in + (double)g.n_tiles * g.taps * g.nkb * g.b_bytes;
+  const double out_elems = (double)B * L_out * L.Cp_out;
+  if (L.skip_buf >= 0) by += 4.0 * out_elems;
+  if (L.f32_buf >= 0) by += 4.0 * out_elems;
+  if (L.hl_buf >= 0) by += 4.0 * out_elems;
+  bytes = by;
+}
+
+voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map, const ConvGemmArgs &a,
+                       cudaStream_t stream) {
+  const long long tiles = (long long)a.B * a.m_tiles * a.n_tiles;
+  const int grid = static_cast<int>(std::min<long long>(tiles, ctx->num_sms));
+  voc::conv_gemm_kernel<<<grid, voc::kGemmThreads, L.smem, stream>>>(map, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, ("launch " + L.name).c_str());
+  return VOC_OK;
+}
+
+voc_status launch_out_head(vocoder *ctx, const OutHead &h, const float *y, int B, long long L,
+                           float *audio, cudaStream_t stream) {
+  const size_t smem = ((size_t)(kHeadTile + h.K - 1) * (h.Cp + 4) + (size_t)h.Cp * h.K) * 4;
+  dim3 grid(static_cast<unsigned>((L + kHeadTile - 1) / kHeadTile), static_cast<unsigned>(B));
+  voc::out_head_kernel<kHeadTile><<<grid, kHeadTile, smem, stream>>>(
+      y, static_cast<int>(L), h.Cp, h.K, h.pad_left, h.w_dev, h.b_dev, audio);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "launch out_head");
+  return VOC_OK;
+}
+
+voc_status launch_prep(vocoder *ctx, const float *x, int B, int C, int T, int Cp, const float *alpha,
+                       const float *invb, __nv_bfloat16 *hl, cudaStream_t stream) {
+  dim3 grid((T + 31) / 32, (Cp + 31) / 32, B);
+  voc::prep_hl_kernel<<<grid, dim3(32, 8), 0, stream>>>(x, C, T, Cp, alpha, invb, hl);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "launch prep");
+  return VOC_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+VOC_API int vocoder_abi_version(void) { return VOC_ABI_VERSION; }
+
+VOC_API int vocoder_param_count(const voc_desc *desc) {
+  std::string why;
+  if (!check_desc(desc, why)) return -1;
+  return param_count(desc);
+}
+
+VOC_API voc_status vocoder_param_shape(const voc_desc *d, int index, int dims[3], int *ndim) {
+  std::string why;
+  if (!check_desc(d, why)) return fail(nullptr, VOC_INVALID_ARG, why);
+  if (!dims || !ndim) return fail(nullptr, VOC_INVALID_ARG, "dims / ndim NULL");
+  const int n = param_count(d);
+  if (index < 0 || index >= n) return fail(nullptr, VOC_INVALID_ARG, "index out of range");
+  auto set = [&](int nd, int a, int b = 0, int c = 0) {
+    *ndim = nd;
+    dims[0] = a, dims[1] = b, dims[2] = c;
+    return VOC_OK;
+  };
+  if (index == 0) return set(3, d->channels0, d->latent_channels, d->in_kernel);
+  if (index == 1) return set(1, d->channels0);
+  int i = index - 2;
+  int C = d->channels0;
+  const int per_stage = 3 + 6 * d->n_dilations;
+  for (int s = 0; s < d->n_stages; ++s) {
+    const int Co = d->widths[s];
+    if (i < per_stage) {
+      if (i == 0) return set(1, C);
+      if (i == 1) return set(3, C, Co, 2 * d->strides[s]);
+      if (i == 2) return set(1, Co);
+      const int j = (i - 3) % 6;
+      if (j == 1) return set(3, Co, Co, d->res_kernel);
+      if (j == 4) return set(3, Co, Co, 1);
+      return set(1, Co);
+    }
+    i -= per_stage;
+    C = Co;
+  }
+  if (i == 0) return set(1, C);
+  if (i == 1) return set(3, 1, C, d->out_kernel);
+  return set(1, 1);
+}
+
+VOC_API voc_status vocoder_fold_weight_norm(const float *g, const float *v, int dim0,
+                                            long long rest, float *w) {
+  if (!g || !v || !w || dim0 <= 0 || rest <= 0)
+    return fail(nullptr, VOC_INVALID_ARG, "fold: NULL pointer or non-positive size");
+  for (int i = 0; i < dim0; ++i) {
+    const float *row = v + (size_t)i * rest;
+    double ss = 0.0;
+    for (long long j = 0; j < rest; ++j) ss += (double)row[j] * (double)row[j];
+    const double nrm = std::sqrt(ss);
+    if (!(nrm > 0.0) || !std::isfinite(nrm))
+      return fail(nullptr, VOC_INVALID_ARG, "fold: row " + std::to_string(i) + " has zero or non-finite norm");
+    const double sc = (double)g[i] / nrm;
+    for (long long j = 0; j < rest; ++j) {
+      const float x = static_cast<float>(sc * (double)row[j]);
+      if (!std::isfinite(x)) return fail(nullptr, VOC_INVALID_ARG, "fold: non-finite result");
+      w[(size_t)i * rest + j] = x;
+    }
+  }
+  return VOC_OK;
+}
+
+VOC_API void vocoder_destroy(vocoder *ctx) {
+  if (!ctx) return;
+  for (void *p : ctx->allocs) cudaFree(p);
+  for (cudaEvent_t e : ctx->events) cudaEventDestroy(e);
+  delete ctx;
+}
+
+VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *params, int n_params,
+                                  vocoder **out) {
+  if (!out) return fail(nullptr, VOC_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  std::string why;
+  if (!check_desc(desc, why)) return fail(nullptr, VOC_INVALID_ARG, "desc: " + why);
+  if (!params) return fail(nullptr, VOC_INVALID_ARG, "params is NULL");
+  if (n_params != param_count(desc))
+    return fail(nullptr, VOC_INVALID_ARG, "n_params " + std::to_string(n_params) + " != " +
+                                              std::to_string(param_count(desc)));
+  // every entry but the biases is required; all values must be finite; alpha > 0
+  const std::string kinds = param_kinds(desc);
+  for (int i = 0; i < n_params; ++i) {
+    if (!params[i]) {
+      if (kinds[i] == 'b') continue;
+      return fail(nullptr, VOC_INVALID_ARG, "params[" + std::to_string(i) + "] is NULL");
+    }
+    int dims[3], nd;
+    vocoder_param_shape(desc, i, dims, &nd);
+    size_t n = 1;
+    for (int k = 0; k < nd; ++k) n *= dims[k];
+    for (size_t k = 0; k < n; ++k) {
+      const float x = params[i][k];
+      if (!std::isfinite(x))
+        return fail(nullptr, VOC_INVALID_ARG, "params[" + std::to_string(i) + "] not finite");
+      if (kinds[i] == 'a' && !(x > 0.f))
+        return fail(nullptr, VOC_INVALID_ARG, "Snake alpha must be positive");
+    }
+  }
+  if (!set_kernel_attrs(why)) return fail(nullptr, VOC_CUDA_ERROR, why);
+
+  vocoder *ctx = new vocoder();
+  ctx->desc = *desc;
+  ctx->strides.assign(desc->strides, desc->strides + desc->n_stages);
+  ctx->widths.assign(desc->widths, desc->widths + desc->n_stages);
+  ctx->dils.assign(desc->dilations, desc->dilations + desc->n_dilations);
+  ctx->desc.strides = ctx->strides.data();
+  ctx->desc.widths = ctx->widths.data();
+  ctx->desc.dilations = ctx->dils.data();
+  for (int s : ctx->strides) ctx->hop *= s;
+  ctx->Cp_lat = rup(desc->latent_channels, 16);
+  auto bail = [&](voc_status st) {
+    g_err = ctx->err;
+    vocoder_destroy(ctx);
+    return st;
+  };
+  cudaError_t e = cudaGetDevice(&ctx->device);
+  if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaGetDevice"));
+  e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
+  if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaDeviceGetAttribute"));
+  int cc_major = 0, cc_minor = 0;
+  cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, ctx->device);
+  cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
+  if (cc_major != 10 || cc_minor != 3)
+    return bail(fail(ctx, VOC_UNSUPPORTED, "this build targets sm_103 (GB300) only"));
+  e = cudaMalloc(&ctx->err_dev, 2 * sizeof(int));
+  if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaMalloc"));
+  ctx->allocs.push_back(ctx->err_dev);
+  ctx->flag_dev = ctx->err_dev + 1;
+  cudaMemset(ctx->err_dev, 0, 2 * sizeof(int));
+
+  const int pad = desc->padding;
+  const int nd = desc->n_dilations;
+  int p = 0;
+  voc_status st;
+  // conv_in (no Snake in front); its epilogue applies the Snake of stage 0's ConvT
+  {
+    Layer L;
+    L.name = "conv_in";
+    L.Cin = desc->latent_channels, L.Cout = desc->channels0, L.K = desc->in_kernel, L.dil = 1;
+    L.level = 0;
+    if (!plan_gemm(L, pad, why)) return bail(fail(ctx, VOC_UNSUPPORTED, "conv_in: " + why));
+    L.in_buf = BUF_H0, L.hl_buf = BUF_H1;
+    st = upload_layer(ctx, ctx->allocs, L, pad, params[0], params[1], params[2]);
+    if (st != VOC_OK) return bail(st);
+    ctx->layers.push_back(L);
+    p = 2;
+  }
+  int C = desc->channels0;
+  for (int i = 0; i < desc->n_stages; ++i) {
+    const int A = (i % 2 == 0) ? BUF_H0 : BUF_H1;  // Snake1 inputs of this stage
+    const int X = (i % 2 == 0) ? BUF_H1 : BUF_H0;  // Snake'd input of this stage's ConvT
+    const int Co = ctx->widths[i];
+    {
+      Layer L;
+      L.name = "convT" + std::to_string(i);
+      L.convT = true;
+      L.Cin = C, L.Cout = Co, L.stride = ctx->strides[i], L.K = 2 * L.stride;
+      L.level = i;
+      if (!plan_gemm(L, pad, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L.name + ": " + why));
+      L.in_buf = X, L.f32_buf = BUF_FY, L.hl_buf = A;
+      st = upload_layer(ctx, ctx->allocs, L, pad, params[p + 1], params[p + 2], params[p + 3]);
+      if (st != VOC_OK) return bail(st);
+      ctx->layers.push_back(L);
+      p += 3;
+    }
+    C = Co;
+    for (int j = 0; j < nd; ++j) {
+      const float *w1 = params[p + 1], *b1 = params[p + 2], *a2 = params[p + 3];
+      const float *w2 = params[p + 4], *b2 = params[p + 5];
+      p += 6;
+      Layer L1;
+      L1.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".conv1";
+      L1.Cin = C, L1.Cout = C, L1.K = desc->res_kernel, L1.dil = ctx->dils[j];
+      L1.level = i + 1;
+      if (!plan_gemm(L1, pad, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L1.name + ": " + why));
+      L1.in_buf = A, L1.hl_buf = BUF_HB;
+      st = upload_layer(ctx, ctx->allocs, L1, pad, w1, b1, a2);
+      if (st != VOC_OK) return bail(st);
+      ctx->layers.push_back(L1);
+
+      Layer L2;
+      L2.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".conv2";
+      L2.Cin = C, L2.Cout = C, L2.K = 1, L2.dil = 1;
+      L2.level = i + 1;
+      if (!plan_gemm(L2, pad, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L2.name + ": " + why));
+      L2.in_buf = BUF_HB, L2.skip_buf = BUF_FY;
+      const float *next_alpha = params[p];  // next snake1 / next stage's snake / snake_out
+      if (j < nd - 1) {
+        L2.f32_buf = BUF_FY, L2.hl_buf = A;
+      } else if (i < desc->n_stages - 1) {
+        L2.hl_buf = A;  // becomes the next stage's ConvT input
+      } else {
+        L2.f32_buf = BUF_FY, L2.epi_flags = voc::EPI_F32_SNAKE;  // Snake_out(y) for the head
+      }
+      st = upload_layer(ctx, ctx->allocs, L2, pad, w2, b2, next_alpha);
+      if (st != VOC_OK) return bail(st);
+      ctx->layers.push_back(L2);
+    }
+  }
+  // out head: Snake already applied by the last conv2 epilogue
+  {
+    OutHead &h = ctx->head;
+    h.C = C, h.Cp = rup(C, 16), h.K = desc->out_kernel;
+    h.pad_left = (pad == VOC_PAD_CAUSAL) ? h.K - 1 : (h.K - 1) / 2;
+    h.level = desc->n_stages;
+    const float *w = params[p + 1], *b = params[p + 2];
+    std::vector<float> wp((size_t)h.Cp * h.K, 0.f), bp(1, b ? b[0] : 0.f);
+    for (int c = 0; c < C; ++c)
+      for (int k = 0; k < h.K; ++k) wp[(size_t)c * h.K + k] = w[(size_t)c * h.K + k];
+    st = upload(ctx, ctx->allocs, wp, &h.w_dev);
+    if (st != VOC_OK) return bail(st);
+    st = upload(ctx, ctx->allocs, bp, &h.b_dev);
+    if (st != VOC_OK) return bail(st);
+  }
+  *out = ctx;
+  return VOC_OK;
+}
+
+VOC_API long long vocoder_hop(const vocoder *ctx) { return ctx ? ctx->hop : -1; }
+
+VOC_API size_t vocoder_workspace_bytes(const vocoder *ctx, int B, int T) {
+  if (!ctx || B < 1 || T < 1) return 0;
+  if ((long long)T * ctx->hop > 0x7FFFFFFFLL) return 0;
+  return BUF_COUNT * buf_bytes(ctx, B, T);
+}
+
+VOC_API size_t vocoder_workspace_bytes_host(const vocoder *ctx, int B, int T) {
+  const size_t w = vocoder_workspace_bytes(ctx, B, T);
+  if (!w) return 0;
+  return w + rupz((size_t)B * ctx->desc.latent_channels * T * 4, 256) +
+         rupz((size_t)B * T * ctx->hop * 4, 256);
+}
+
+VOC_API int vocoder_launches_per_decode(const vocoder *ctx, int B, int T) {
+  if (!ctx || B < 1 || T < 1) return -1;
+  return 2 + static_cast<int>(ctx->layers.size());
+}
+
+namespace {
+voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *audio, void *ws,
+                       size_t ws_bytes, cudaStream_t stream, unsigned flags) {
+  const size_t need = vocoder_workspace_bytes(ctx, B, T);
+  if (!need) return fail(ctx, VOC_INVALID_ARG, "invalid B / T");
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(ctx, VOC_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < need)
+    return fail(ctx, VOC_WORKSPACE_TOO_SMALL,
+                "workspace " + std::to_string(ws_bytes) + " < " + std::to_string(need));
+  if (reinterpret_cast<uintptr_t>(latent) & 15)
+    return fail(ctx, VOC_INVALID_ARG, "latent not 16-byte aligned");
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != ctx->device) return fail(ctx, VOC_INVALID_ARG, "current device differs from the context's");
+
+  const size_t bb = buf_bytes(ctx, B, T);
+  void *bufs[BUF_COUNT];
+  for (int i = 0; i < BUF_COUNT; ++i) bufs[i] = static_cast<uint8_t *>(ws) + i * bb;
+
+  // TMA descriptors depend on the workspace address and the sizes only
+  if (ctx->map_ws != ws || ctx->map_B != B || ctx->map_T != T) {
+    ctx->maps.resize(ctx->layers.size());
+    for (size_t i = 0; i < ctx->layers.size(); ++i) {
+      const Layer &L = ctx->layers[i];
+      voc_status st = encode_map(ctx, &ctx->maps[i], bufs[L.in_buf], L.Cp_in,
+                                 level_len(ctx, L.level, T), B, L.g.rows);
+      if (st != VOC_OK) {
+        ctx->map_ws = nullptr;
+        return st;
+      }
+    }
+    ctx->map_ws = ws, ctx->map_B = B, ctx->map_T = T;
+  }
+
+  const bool prof = (flags & VOC_FLAG_PROFILE) != 0;
+  const int n_launch = vocoder_launches_per_decode(ctx, B, T);
+  if (prof) {
+    while ((int)ctx->events.size() < 2 * n_launch) {
+      cudaEvent_t ev;
+      cudaError_t e = cudaEventCreate(&ev);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaEventCreate");
+      ctx->events.push_back(ev);
+    }
+    ctx->prof_names.assign(n_launch, "");
+    ctx->prof_flops.assign(n_launch, 0.0);
+    ctx->prof_bytes.assign(n_launch, 0.0);
+    ctx->prof_ms.assign(n_launch, -1.f);
+    ctx->prof_n = n_launch;
+    ctx->prof_ready = false;
+  }
+  int li = 0;
+  auto rec = [&](int which) {
+    if (prof) cudaEventRecord(ctx->events[2 * li + which], stream);
+  };
+
+  voc_status st;
+  rec(0);
+  st = launch_prep(ctx, latent, B, ctx->desc.latent_channels, T, ctx->Cp_lat, nullptr, nullptr,
+                   static_cast<__nv_bfloat16 *>(bufs[BUF_H0]), stream);
+  if (st != VOC_OK) return st;
+  rec(1);
+  if (prof) {
+    ctx->prof_names[li] = "prep_latent";
+    ctx->prof_bytes[li] = (double)B * T * (4.0 * ctx->desc.latent_channels + 4.0 * ctx->Cp_lat);
+  }
+  ++li;
+  for (size_t i = 0; i < ctx->layers.size(); ++i, ++li) {
+    const Layer &L = ctx->layers[i];
+    ConvGemmArgs a;
+    gemm_launch_args(ctx, L, B, T, bufs, a);
+    rec(0);
+    st = launch_gemm(ctx, L, ctx->maps[i], a, stream);
+    if (st != VOC_OK) return st;
+    rec(1);
+    if (prof) {
+      ctx->prof_names[li] = L.name;
+      layer_cost(ctx, L, B, T, ctx->prof_flops[li], ctx->prof_bytes[li]);
+    }
+  }
+  const long long Lf = level_len(ctx, ctx->desc.n_stages, T);
+  rec(0);
+  st = launch_out_head(ctx, ctx->head, static_cast<const float *>(bufs[BUF_FY]), B, Lf, audio,
+                       stream);
+  if (st != VOC_OK) return st;
+  rec(1);
+  if (prof) {
+    ctx->prof_names[li] = "out_head";
+    ctx->prof_flops[li] = 2.0 * ctx->head.C * ctx->head.K * B * (double)Lf;
+    ctx->prof_bytes[li] = (double)B * Lf * (4.0 * ctx->head.Cp + 4.0);
+    ctx->prof_ready = true;
+  }
+  ++li;
+
+  if (flags & VOC_FLAG_CHECK_FINITE) {
+    cudaMemsetAsync(ctx->flag_dev, 0, sizeof(int), stream);
+    const long long n = (long long)B * Lf;
+    const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 4L * ctx->num_sms));
+    voc::finite_check_kernel<<<blocks, 256, 0, stream>>>(audio, n, ctx->flag_dev);
+    int flag = 0;
+    cudaError_t e = cudaMemcpyAsync(&flag, ctx->flag_dev, sizeof(int), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "finite check");
+    if (flag) return fail(ctx, VOC_NONFINITE, "decoded audio contains NaN or Inf");
+  }
+  if (flags & (VOC_FLAG_SYNC | VOC_FLAG_CHECK_FINITE)) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+    int word = 0;
+    e = cudaMemcpy(&word, ctx->err_dev, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "read device error word");
+    if (word) {
+      cudaMemset(ctx->err_dev, 0, sizeof(int));
+      return fail(ctx, VOC_DEVICE_TIMEOUT,
+                  "a kernel gave up a bounded wait (code " + std::to_string(word) + ")");
+    }
+  }
+  return VOC_OK;
+}
+}  // namespace
+
+VOC_API voc_status vocoder_decode(vocoder *ctx, const float *latent_dev, int B, int T,
+                                  float *audio_dev, void *ws_dev, size_t ws_bytes,
+                                  voc_stream_t stream, unsigned flags) {
+  if (!ctx) return fail(nullptr, VOC_INVALID_ARG, "ctx is NULL");
+  if (!latent_dev || !audio_dev) return fail(ctx, VOC_INVALID_ARG, "latent / audio NULL");
+  if (B < 1 || T < 1) return fail(ctx, VOC_INVALID_ARG, "B and T must be positive");
+  return decode_impl(ctx, latent_dev, B, T, audio_dev, ws_dev, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream), flags);
+}
+
+VOC_API voc_status vocoder_decode_host(vocoder *ctx, const float *latent_host, int B, int T,
+                                       float *audio_host, void *ws_dev, size_t ws_bytes,
+                                       voc_stream_t stream, unsigned flags) {
+  if (!ctx) return fail(nullptr, VOC_INVALID_ARG, "ctx is NULL");
+  if (!latent_host || !audio_host) return fail(ctx, VOC_INVALID_ARG, "latent / audio NULL");
+  if (B < 1 || T < 1) return fail(ctx, VOC_INVALID_ARG, "B and T must be positive");
+  const size_t need = vocoder_workspace_bytes_host(ctx, B, T);
+  if (!need) return fail(ctx, VOC_INVALID_ARG, "invalid B / T");
+  if (!ws_dev || (reinterpret_cast<uintptr_t>(ws_dev) & 255))
+    return fail(ctx, VOC_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < need)
+    return fail(ctx, VOC_WORKSPACE_TOO_SMALL,
+                "workspace " + std::to_string(ws_bytes) + " < " + std::to_string(need));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t wdec = vocoder_workspace_bytes(ctx, B, T);
+  const size_t lat_bytes = (size_t)B * ctx->desc.latent_channels * T * 4;
+  const size_t aud_bytes = (size_t)B * T * ctx->hop * 4;
+  uint8_t *base = static_cast<uint8_t *>(ws_dev);
+  float *lat_d = reinterpret_cast<float *>(base + wdec);
+  float *aud_d = reinterpret_cast<float *>(base + wdec + rupz(lat_bytes, 256));
+  cudaError_t e = cudaMemcpyAsync(lat_d, latent_host, lat_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "copy latent in");
+  voc_status st = decode_impl(ctx, lat_d, B, T, aud_d, ws_dev, wdec, s, flags);
+  if (st != VOC_OK) return st;
+  e = cudaMemcpyAsync(audio_host, aud_d, aud_bytes, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "copy audio out");
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+  return VOC_OK;
+}
+
+VOC_API long long vocoder_stitched_length(int n_win, int win_frames, int crop_left, int crop_right,
+                                          int hop) {
+  if (n_win < 1 || win_frames < 1 || crop_left < 0 || crop_right < 0 || hop < 1) return -1;
+  long long frames = 0;
+  for (int w = 0; w < n_win; ++w) {
+    const int lo = (w == 0) ? 0 : crop_left;
+    const int hi = (w == n_win - 1) ? win_frames : win_frames - crop_right;
+    if (hi < lo) return -1;
+    frames += hi - lo;
+  }
+  return frames * hop;
+}
+
+VOC_API voc_status vocoder_stitch(const float *decoded_dev, int n_win, int n_sides, int win_frames,
+                                  int crop_left, int crop_right, int hop, float *out_dev,
+                                  voc_stream_t stream) {
+  if (!decoded_dev || !out_dev) return fail(nullptr, VOC_INVALID_ARG, "stitch: NULL buffer");
+  if (n_sides < 1 || n_sides > 65535) return fail(nullptr, VOC_INVALID_ARG, "stitch: n_sides");
+  const long long len = vocoder_stitched_length(n_win, win_frames, crop_left, crop_right, hop);
+  if (len < 0) return fail(nullptr, VOC_INVALID_ARG, "stitch: invalid window geometry");
+  if (len == 0) return VOC_OK;
+  dim3 grid(static_cast<unsigned>((len + 255) / 256), static_cast<unsigned>(n_sides));
+  voc::stitch_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      decoded_dev, n_win, n_sides, win_frames, crop_left, crop_right, hop, len, out_dev);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "launch stitch");
+  return VOC_OK;
+}
+
+namespace {
+// Shared body of the single-layer operations.
+voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, const float *w_host,
+                    const float *b_host, const float *alpha_host, float *y_dev, cudaStream_t stream) {
+  std::string why;
+  if (!set_kernel_attrs(why)) return fail(nullptr, VOC_CUDA_ERROR, why);
+  if (!plan_gemm(L, padding, why)) return fail(nullptr, VOC_UNSUPPORTED, why);
+  int dev = 0, sms = 0, major = 0, minor = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return fail(nullptr, VOC_UNSUPPORTED, "this build targets sm_103 only");
+  vocoder tmp;  // carries the allocations, the error word and the launch settings
+  tmp.num_sms = sms;
+  tmp.device = dev;
+  tmp.strides = {L.convT ? L.stride : 1};
+  auto done = [&](voc_status st) {
+    if (st != VOC_OK) g_err = tmp.err;
+    for (void *p : tmp.allocs) cudaFree(p);
+    return st;
+  };
+  voc_status st = upload_layer(&tmp, tmp.allocs, L, padding, w_host, b_host, nullptr);
+  if (st != VOC_OK) return done(st);
+  cudaError_t e = cudaMalloc(&tmp.err_dev, sizeof(int));
+  if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
+  tmp.allocs.push_back(tmp.err_dev);
+  cudaMemsetAsync(tmp.err_dev, 0, sizeof(int), stream);
+  float *alpha_d = nullptr, *invb_d = nullptr;
+  if (alpha_host) {
+    std::vector<float> a(alpha_host, alpha_host + L.Cin), ib(L.Cin);
+    for (int c = 0; c < L.Cin; ++c) ib[c] = static_cast<float>(1.0 / ((double)a[c] + 1e-9));
+    if ((st = upload(&tmp, tmp.allocs, a, &alpha_d)) != VOC_OK) return done(st);
+    if ((st = upload(&tmp, tmp.allocs, ib, &invb_d)) != VOC_OK) return done(st);
+  }
+  const int s = L.convT ? L.stride : 1;
+  void *hl = nullptr, *rows = nullptr;
+  e = cudaMalloc(&hl, (size_t)B * T * L.Cp_in * 4);
+  if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
+  tmp.allocs.push_back(hl);
+  e = cudaMalloc(&rows, (size_t)B * T * s * L.Cp_out * 4);
+  if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
+  tmp.allocs.push_back(rows);
+  if ((st = launch_prep(&tmp, x_dev, B, L.Cin, T, L.Cp_in, alpha_d, invb_d,
+                        static_cast<__nv_bfloat16 *>(hl), stream)) != VOC_OK)
+    return done(st);
+  CUtensorMap map;
+  if ((st = encode_map(&tmp, &map, hl, L.Cp_in, T, B, L.g.rows)) != VOC_OK) return done(st);
+  void *bufs[BUF_COUNT] = {hl, nullptr, nullptr, rows};
+  L.level = 0;
+  L.in_buf = 0, L.f32_buf = BUF_FY;
+  ConvGemmArgs a;
+  gemm_launch_args(&tmp, L, B, T, bufs, a);
+  if ((st = launch_gemm(&tmp, L, map, a, stream)) != VOC_OK) return done(st);
+  dim3 grid((T * s + 31) / 32, (L.Cout + 31) / 32, B);
+  voc::rows_to_cf_kernel<<<grid, dim3(32, 8), 0, stream>>>(static_cast<const float *>(rows), T * s,
+                                                           L.Cp_out, L.Cout, y_dev);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "launch rows_to_cf"));
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaStreamSynchronize"));
+  int word = 0;
+  cudaMemcpy(&word, tmp.err_dev, sizeof(int), cudaMemcpyDeviceToHost);
+  if (word) return done(fail(&tmp, VOC_DEVICE_TIMEOUT, "a kernel gave up a bounded wait"));
+  return done(VOC_OK);
+}
+}  // namespace
+
+VOC_API voc_status vocoder_op_conv1d(const float *x_dev, int B, int Cin, int T, const float *w_host,
+                                     const float *b_host, int Cout, int K, int dil, int padding,
+                                     const float *alpha_host, float *y_dev, voc_stream_t stream) {
+  if (!x_dev || !w_host || !y_dev) return fail(nullptr, VOC_INVALID_ARG, "NULL pointer");
+  if (B < 1 || Cin < 1 || T < 1 || Cout < 1 || K < 1 || K > 15 || K % 2 == 0 || dil < 1 ||
+      dil * (K - 1) > 120 || (padding != VOC_PAD_SYMMETRIC && padding != VOC_PAD_CAUSAL))
+    return fail(nullptr, VOC_INVALID_ARG, "invalid conv1d shape");
+  Layer L;
+  L.name = "op_conv1d";
+  L.Cin = Cin, L.Cout = Cout, L.K = K, L.dil = dil;
+  return op_layer(L, padding, x_dev, B, T, w_host, b_host, alpha_host, y_dev,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+VOC_API voc_status vocoder_op_conv_transpose1d(const float *x_dev, int B, int Cin, int T,
+                                               const float *w_host, const float *b_host, int Cout,
+                                               int stride, int padding, const float *alpha_host,
+                                               float *y_dev, voc_stream_t stream) {
+  if (!x_dev || !w_host || !y_dev) return fail(nullptr, VOC_INVALID_ARG, "NULL pointer");
+  if (B < 1 || Cin < 1 || T < 1 || Cout < 1 || stride < 1 || stride > 16 ||
+      (padding != VOC_PAD_SYMMETRIC && padding != VOC_PAD_CAUSAL) ||
+      (padding == VOC_PAD_SYMMETRIC && stride % 2))
+    return fail(nullptr, VOC_INVALID_ARG, "invalid conv_transpose1d shape");
+  Layer L;
+  L.name = "op_convT";
+  L.convT = true;
+  L.Cin = Cin, L.Cout = Cout, L.stride = stride, L.K = 2 * stride;
+  return op_layer(L, padding, x_dev, B, T, w_host, b_host, alpha_host, y_dev,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+VOC_API int vocoder_profile_count(const vocoder *ctx) {
+  return (ctx && ctx->prof_ready) ? ctx->prof_n : 0;
+}
+
+VOC_API voc_status vocoder_profile_entry(vocoder *ctx, int index, const char **name, double *ms,
+                                         double *flops, double *bytes) {
+  if (!ctx) return fail(nullptr, VOC_INVALID_ARG, "ctx is NULL");
+  if (!ctx->prof_ready || index < 0 || index >= ctx->prof_n)
+    return fail(ctx, VOC_INVALID_ARG, "no profile entry " + std::to_string(index));
+  if (ctx->prof_ms[index] < 0.f) {
+    cudaError_t e = cudaEventSynchronize(ctx->events[2 * index + 1]);
+    if (e == cudaSuccess)
+      e = cudaEventElapsedTime(&ctx->prof_ms[index], ctx->events[2 * index], ctx->events[2 * index + 1]);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "profile event");
+  }
+  if (name) *name = ctx->prof_names[index].c_str();
+  if (ms) *ms = ctx->prof_ms[index];
+  if (flops) *flops = ctx->prof_flops[index];
+  if (bytes) *bytes = ctx->prof_bytes[index];
+  return VOC_OK;
+}
+
+VOC_API const char *vocoder_last_error(const vocoder *ctx) {
+  return ctx ? ctx->err.c_str() : g_err.c_str();
+}

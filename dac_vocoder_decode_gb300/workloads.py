@@ -17,7 +17,8 @@ is synthetic):
     bias ~ N(0, 0.02), with gain 1 for conv_in, sqrt(s/2) for the transposed
     conv of stride s (variance preserving: its norm runs over C_out * 2s taps
     and each output sample sees 2 taps of 2*C_out inputs), 0.5 for the two
-    convolutions of a residual unit and 0.5 for conv_out.
+    convolutions of a residual unit and 0.3 for conv_out (set once so that
+    the pre-tanh RMS of every calibrated workload lies in [0.05, 1]).
 * seeds: 1000 * workload index + {0: latent, 1: weights, 2: alpha}, numpy PCG64.
 """
 from __future__ import annotations
@@ -178,6 +179,8 @@ def gen_params(arch: Arch, recipe: str, seed_w: int, seed_a: int) -> list:
         elif ".convT." in name:
             stride = shape[2] // 2
             gain = math.sqrt(stride / 2.0)
+        elif name.startswith("conv_out"):
+            gain = 0.3
         else:
             gain = 0.5
         v, g = conv(shape, gain)

@@ -1,0 +1,208 @@
+/*
+ * vocoder.h -- C ABI of the GB300 DAC-style vocoder decoder.
+ *
+ * The decoder turns a latent sequence into a waveform (minimaxmusic.cpp
+ * Architecture, section "Flow VAE"):
+ *
+ *   conv_in k7 (C_lat -> C0)
+ *   for every upsampling stage (stride s, C_in -> C_out):
+ *       Snake -> ConvTranspose1d (k = 2s, pad s/2) -> 3 residual units,
+ *       residual unit (dilation d in 1, 3, 9):
+ *           y = x + conv2_k1( Snake2( conv1_k7_dil_d( Snake1(x) ) ) )
+ *   Snake -> conv_out k7 (C_last -> 1, with bias) -> tanh
+ *
+ * with Snake(x) = x + sin^2(a x) / (a + 1e-9), the per-channel a used as stored
+ * (MiniMax-Music-3 -> CMF README, "What the conversion had to get right").
+ * The speech-codec variant (qwentts.cpp Architecture, "Audio tokenizer
+ * decoder") runs the same stack causally: k-tap convs pad (k-1)d on the left
+ * only and each transposed conv keeps the first T*s samples of its col2im output.
+ *
+ * Conventions (pattern of qwentts.cpp Architecture, "Public API" / "ABI
+ * guarantee"): plain C99, an opaque handle, negative status codes, a last-error
+ * string, an ABI version checked at create time, and every argument validated
+ * before any device work.  Only vocoder_* symbols are exported.
+ *
+ * Devices, streams, ownership:
+ *   - A context lives on the CUDA device that is current when vocoder_create is
+ *     called; all later calls on it must run with that device current.
+ *   - The library owns its device copy of the weights (create .. destroy).
+ *   - The caller owns every latent / audio / workspace buffer.  "_dev" pointers
+ *     are device memory of the context's device, "_host" pointers host memory.
+ *   - Work is enqueued on the caller's stream (a cudaStream_t passed as
+ *     voc_stream_t; NULL is the legacy default stream) and is asynchronous
+ *     unless a flag below asks for a synchronisation.
+ *   - A context is not thread-safe: use it from one thread and one stream at a
+ *     time.
+ * Precision: fp32 storage and accumulation; every convolution runs on the
+ * tensor cores as three bf16 products of a hi/lo split of both operands
+ * (hi*hi + hi*lo + lo*hi), which carries about 16 significant bits per operand.
+ */
+#ifndef GB300_VOCODER_H
+#define GB300_VOCODER_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VOC_ABI_VERSION 1
+
+typedef struct vocoder vocoder_t;             /* opaque context */
+typedef struct CUstream_st *voc_stream_t;     /* a cudaStream_t */
+
+typedef enum {
+  VOC_OK = 0,
+  VOC_INVALID_ARG = -1,         /* a pointer, size or description is invalid       */
+  VOC_UNSUPPORTED = -2,         /* valid in principle, not supported by this build  */
+  VOC_CUDA_ERROR = -3,          /* a CUDA runtime call or a kernel launch failed    */
+  VOC_OOM = -4,                 /* device or host allocation failed                 */
+  VOC_WORKSPACE_TOO_SMALL = -5, /* ws_bytes below vocoder_workspace_bytes()         */
+  VOC_NONFINITE = -6,           /* VOC_FLAG_CHECK_FINITE found a NaN / Inf          */
+  VOC_CANCELLED = -7,           /* reserved for cancellable entry points            */
+  VOC_DEVICE_TIMEOUT = -8       /* a kernel gave up a bounded wait (see VOC_FLAG_SYNC) */
+} voc_status;
+
+enum { VOC_PAD_SYMMETRIC = 0, VOC_PAD_CAUSAL = 1 };
+enum { VOC_PREC_BF16X3 = 0 };
+
+/* flags of vocoder_decode / vocoder_decode_host */
+enum {
+  VOC_FLAG_CHECK_FINITE = 1, /* scan the audio for NaN / Inf; implies a stream sync   */
+  VOC_FLAG_SYNC = 2,         /* synchronise the stream and report device timeouts     */
+  VOC_FLAG_PROFILE = 4       /* record a CUDA event around every kernel of the decode */
+};
+
+/* Architecture of the decoder.  All arrays are borrowed for the duration of
+ * vocoder_create only. */
+typedef struct {
+  int abi_version;      /* VOC_ABI_VERSION                                  */
+  int latent_channels;  /* C_lat (64 music, 1024 speech)                    */
+  int in_kernel;        /* conv_in taps (odd, 1..15; 7)                     */
+  int channels0;        /* C0, conv_in output channels                       */
+  int n_stages;         /* upsampling stages (1..8)                          */
+  const int *strides;   /* [n_stages] (even unless VOC_PAD_CAUSAL)           */
+  const int *widths;    /* [n_stages] output channels of each stage          */
+  int n_dilations;      /* residual units per stage (1..4; 3)                */
+  const int *dilations; /* [n_dilations] (1, 3, 9)                           */
+  int res_kernel;       /* dilated conv taps (odd; 7)                        */
+  int out_kernel;       /* conv_out taps (odd; 7)                            */
+  int out_channels;     /* 1                                                 */
+  int padding;          /* VOC_PAD_SYMMETRIC | VOC_PAD_CAUSAL                */
+  int precision;        /* VOC_PREC_BF16X3                                   */
+} voc_desc;
+
+/* ABI version of the library (VOC_ABI_VERSION of the build). */
+int vocoder_abi_version(void);
+
+/* Number of parameter tensors of the architecture, or -1 for an invalid desc.
+ * Canonical order and PyTorch layouts (weights already folded):
+ *   conv_in.w [C0][C_lat][in_kernel], conv_in.b [C0],
+ *   per stage i (C_in -> C_out = widths[i], stride s):
+ *     snake.alpha [C_in], convT.w [C_in][C_out][2s], convT.b [C_out],
+ *     per dilation: snake1.alpha [C_out], conv1.w [C_out][C_out][res_kernel],
+ *                   conv1.b [C_out], snake2.alpha [C_out], conv2.w [C_out][C_out][1],
+ *                   conv2.b [C_out],
+ *   snake_out.alpha [C_last], conv_out.w [1][C_last][out_kernel], conv_out.b [1]. */
+int vocoder_param_count(const voc_desc *desc);
+
+/* Shape of parameter `index`: writes up to 3 dims and their count. */
+voc_status vocoder_param_shape(const voc_desc *desc, int index, int dims[3], int *ndim);
+
+/* Weight-norm fold (minimaxmusic.cpp Architecture, "Models" / "Flow VAE"):
+ *   w[i, :] = g[i] * v[i, :] / ||v[i, :]||  for i < dim0, rows of `rest` values,
+ * the norm running over every axis but axis 0 of the stored tensor (Conv1d
+ * [Cout][Cin][K]: rest = Cin*K; ConvTranspose1d [Cin][Cout][K]: rest = Cout*K).
+ * Host memory; accumulates in double; w may not alias v.  VOC_INVALID_ARG for a
+ * NULL pointer, non-positive sizes, a zero-norm row or a non-finite result. */
+voc_status vocoder_fold_weight_norm(const float *g, const float *v, int dim0, long long rest,
+                                    float *w);
+
+/* Create a decoder on the current device.  params: vocoder_param_count(desc)
+ * host pointers in the canonical order; a NULL bias means zero, every other
+ * entry is required.  The weights are re-laid out per tap, split into bf16 hi/lo
+ * and copied to the device; the host arrays are not retained.  On failure *out
+ * is NULL and vocoder_last_error(NULL) describes the problem. */
+voc_status vocoder_create(const voc_desc *desc, const float *const *params, int n_params,
+                          vocoder_t **out);
+
+/* Upsampling factor (product of the strides), or -1 for NULL. */
+long long vocoder_hop(const vocoder_t *ctx);
+
+/* Device workspace that vocoder_decode needs for B items of T latent frames
+ * (0 for invalid sizes).  vocoder_workspace_bytes_host adds room for the
+ * host-buffer entry point's staging copies. */
+size_t vocoder_workspace_bytes(const vocoder_t *ctx, int B, int T);
+size_t vocoder_workspace_bytes_host(const vocoder_t *ctx, int B, int T);
+
+/* Decode B mono items (a stereo track is folded by the caller into 2 items,
+ * channels 0..C_lat-1 left):
+ *   latent_dev [B][C_lat][T] fp32, time contiguous  ->  audio_dev [B][1][T*hop] fp32.
+ * ws_dev: device workspace of at least vocoder_workspace_bytes(ctx, B, T) bytes,
+ * 256-byte aligned, not used by anything else until the decode has finished on
+ * `stream`.  latent_dev must be 16-byte aligned.  Asynchronous on `stream`
+ * unless flags contain VOC_FLAG_SYNC or VOC_FLAG_CHECK_FINITE. */
+voc_status vocoder_decode(vocoder_t *ctx, const float *latent_dev, int B, int T, float *audio_dev,
+                          void *ws_dev, size_t ws_bytes, voc_stream_t stream, unsigned flags);
+
+/* Same decode from and to HOST buffers: copies the latent in, decodes, copies
+ * the audio out and synchronises `stream` before returning.  ws_bytes >=
+ * vocoder_workspace_bytes_host(ctx, B, T).  Page-locked host buffers give
+ * asynchronous copies; pageable ones work but are slower. */
+voc_status vocoder_decode_host(vocoder_t *ctx, const float *latent_host, int B, int T,
+                               float *audio_host, void *ws_dev, size_t ws_bytes,
+                               voc_stream_t stream, unsigned flags);
+
+/* Overlap-crop stitch (minimaxmusic.cpp Architecture, "Decode and stitch"):
+ *   decoded_dev [n_win*n_sides][win_frames*hop], item index w*n_sides + side;
+ * window 0 keeps its left edge, later windows drop crop_left frames on the
+ * left, all but the last drop crop_right frames on the right; the kept pieces
+ * are concatenated per side and clamped to [-1, 1] into
+ *   out_dev [n_sides][vocoder_stitched_length(...)].
+ * Asynchronous on `stream`.  Buffers must be 16-byte aligned. */
+long long vocoder_stitched_length(int n_win, int win_frames, int crop_left, int crop_right,
+                                  int hop);
+voc_status vocoder_stitch(const float *decoded_dev, int n_win, int n_sides, int win_frames,
+                          int crop_left, int crop_right, int hop, float *out_dev,
+                          voc_stream_t stream);
+
+/* Single-layer operations on the same kernels as vocoder_decode, for per-layer
+ * checks.  Channels-first fp32 device tensors; they allocate and free their own
+ * temporaries and synchronise `stream` before returning.
+ *   vocoder_op_conv1d:   y[b][co][t] = bias[co] + sum_ci sum_k
+ *                          w[co][ci][k] * S(x)[b][ci][t + k*dil - pad_left]
+ *     (y [B][Cout][T]; pad_left = dil*(K-1)/2 symmetric or dil*(K-1) causal)
+ *   vocoder_op_conv_transpose1d: y[b][co][t*s + k - p] += w[ci][co][k] * S(x)[b][ci][t]
+ *     plus bias (y [B][Cout][T*s], K = 2s; p = s/2 symmetric, 0 causal)
+ * where S is Snake with per-channel alpha_host [Cin], or the identity when
+ * alpha_host is NULL.  Weights are host fp32 in PyTorch layouts; b_host may be NULL. */
+voc_status vocoder_op_conv1d(const float *x_dev, int B, int Cin, int T, const float *w_host,
+                             const float *b_host, int Cout, int K, int dil, int padding,
+                             const float *alpha_host, float *y_dev, voc_stream_t stream);
+voc_status vocoder_op_conv_transpose1d(const float *x_dev, int B, int Cin, int T,
+                                       const float *w_host, const float *b_host, int Cout,
+                                       int stride, int padding, const float *alpha_host,
+                                       float *y_dev, voc_stream_t stream);
+
+/* Kernel launches that one vocoder_decode(ctx, ., B, T, ...) enqueues. */
+int vocoder_launches_per_decode(const vocoder_t *ctx, int B, int T);
+
+/* Per-kernel record of the last decode that ran with VOC_FLAG_PROFILE (valid
+ * after the stream has been synchronised): name, device time (ms), algorithmic
+ * FLOPs (2 per multiply-add, transposed conv counted without zero-stuffing) and
+ * algorithmic bytes (each input read once, each output written once). */
+int vocoder_profile_count(const vocoder_t *ctx);
+voc_status vocoder_profile_entry(vocoder_t *ctx, int index, const char **name, double *ms,
+                                 double *flops, double *bytes);
+
+/* Message of the last failed call on ctx (ctx == NULL: of the last failure on
+ * this thread without a context).  Valid until the next call on ctx. */
+const char *vocoder_last_error(const vocoder_t *ctx);
+
+/* Free the context and its device weights (NULL is ignored). */
+void vocoder_destroy(vocoder_t *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

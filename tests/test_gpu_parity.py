@@ -1,0 +1,249 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the CPU oracle.
+
+Per-layer checks run each tensor-core layer kind (k7 dilated conv, k1 conv,
+conv_in, polyphase transposed conv, symmetric and causal) on shapes that span
+several 128-row tiles, a ragged tail and several column tiles.  End-to-end
+checks decode every workload: the small ones in full, the full-size ones
+element by element on sampled windows that the oracle computes exactly from
+latent slices covering the receptive field.
+
+Tolerances: decoded audio (in [-1, 1]) must satisfy max |gpu - oracle| <= 2e-3
+and SNR >= 60 dB.  Single layers are held to a bound derived from the bf16x3
+arithmetic: each product carries a relative error of about 2^-16 (the dropped
+lo*lo term and the two splits), so |err| <= 2^-14 * sum |w x| leaves a 4x margin
+over the fp32-accumulated worst case of these sizes."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU-only machines, never run there
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from dac_vocoder_decode_gb300 import binding as V  # noqa: E402
+from dac_vocoder_decode_gb300 import workloads as W  # noqa: E402
+from oracle import oracle as O  # noqa: E402
+from tests import gpu_common as G  # noqa: E402
+from tests.util import snr_db  # noqa: E402
+
+LAYER_REL = 2.0 ** -14
+
+
+# ----------------------------------------------------------------------------- single layers
+CONV_CASES = [
+    # B, Cin, Cout, T, K, dil, padding
+    (2, 96, 96, 300, 7, 1, W.PAD_SYMMETRIC),
+    (1, 96, 96, 257, 7, 3, W.PAD_SYMMETRIC),
+    (2, 192, 192, 200, 7, 9, W.PAD_SYMMETRIC),
+    (1, 384, 384, 130, 7, 9, W.PAD_CAUSAL),
+    (2, 768, 768, 129, 1, 1, W.PAD_SYMMETRIC),
+    (1, 64, 1536, 150, 7, 1, W.PAD_SYMMETRIC),   # conv_in shape
+    (1, 1024, 256, 70, 7, 1, W.PAD_CAUSAL),      # speech conv_in (cut to 256 outputs)
+    (1, 4, 4, 140, 7, 3, W.PAD_SYMMETRIC),       # padded channels (tiny decoder)
+    (1, 48, 48, 400, 7, 9, W.PAD_CAUSAL),
+    (3, 16, 40, 33, 7, 1, W.PAD_SYMMETRIC),      # ragged T shorter than one tile
+]
+
+
+@pytest.mark.parametrize("case", CONV_CASES, ids=[str(c) for c in CONV_CASES])
+@pytest.mark.parametrize("with_snake", [True, False])
+def test_op_conv1d(case, with_snake):
+    B, Cin, Cout, T, K, dil, padding = case
+    rng = np.random.default_rng(hash(case) % 2**32)
+    x = rng.standard_normal((B, Cin, T)).astype(np.float32)
+    w = (rng.standard_normal((Cout, Cin, K)) / np.sqrt(Cin * K)).astype(np.float32)
+    b = (rng.standard_normal(Cout) * 0.1).astype(np.float32)
+    alpha = rng.uniform(0.5, 1.5, Cin).astype(np.float32) if with_snake else None
+    y = torch.empty((B, Cout, T), dtype=torch.float32, device="cuda")
+    V.vocoder_op_conv1d(torch.from_numpy(x).cuda(), w, b, dil, padding, alpha, y)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    span = dil * (K - 1)
+    pl = span if padding == W.PAD_CAUSAL else span // 2
+    wd = w.astype(np.float64)
+    for bi in range(B):
+        xs = O.snake(x[bi], alpha) if with_snake else x[bi].astype(np.float64)
+        ref = O.conv1d(xs, wd, b, dil, pl, span - pl)
+        mag = O.conv1d(np.abs(xs), np.abs(wd), None, dil, pl, span - pl)
+        err = np.abs(got[bi] - ref)
+        assert np.all(err <= LAYER_REL * mag + 1e-6), (bi, float(err.max()), float(mag.max()))
+
+
+CONVT_CASES = [
+    # B, Cin, Cout, T, stride, padding
+    (2, 192, 96, 300, 2, W.PAD_SYMMETRIC),
+    (1, 384, 192, 140, 4, W.PAD_SYMMETRIC),
+    (2, 768, 384, 129, 8, W.PAD_SYMMETRIC),
+    (1, 1536, 768, 40, 8, W.PAD_SYMMETRIC),
+    (1, 96, 48, 200, 3, W.PAD_CAUSAL),
+    (2, 768, 384, 65, 5, W.PAD_CAUSAL),
+    (1, 192, 96, 131, 4, W.PAD_CAUSAL),
+    (1, 8, 4, 50, 2, W.PAD_SYMMETRIC),           # padded channels
+]
+
+
+@pytest.mark.parametrize("case", CONVT_CASES, ids=[str(c) for c in CONVT_CASES])
+def test_op_conv_transpose1d(case):
+    B, Cin, Cout, T, s, padding = case
+    rng = np.random.default_rng(hash(case) % 2**32)
+    x = rng.standard_normal((B, Cin, T)).astype(np.float32)
+    w = (rng.standard_normal((Cin, Cout, 2 * s)) / np.sqrt(Cin)).astype(np.float32)
+    b = (rng.standard_normal(Cout) * 0.1).astype(np.float32)
+    alpha = rng.uniform(0.5, 1.5, Cin).astype(np.float32)
+    y = torch.empty((B, Cout, T * s), dtype=torch.float32, device="cuda")
+    V.vocoder_op_conv_transpose1d(torch.from_numpy(x).cuda(), w, b, s, padding, alpha, y)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    p = 0 if padding == W.PAD_CAUSAL else s // 2
+    wd = w.astype(np.float64)
+    for bi in range(B):
+        xs = O.snake(x[bi], alpha)
+        ref = O.conv_transpose1d(xs, wd, b, s, p, T * s)
+        mag = O.conv_transpose1d(np.abs(xs), np.abs(wd), None, s, p, T * s)
+        err = np.abs(got[bi] - ref)
+        assert np.all(err <= LAYER_REL * mag + 1e-6), (bi, float(err.max()), float(mag.max()))
+
+
+# ----------------------------------------------------------------------------- full decodes
+@pytest.mark.parametrize("name", ["tiny", "tiny_cal"])
+def test_decode_tiny_full(name):
+    wl = G.workload(name)
+    voc = G.gpu_decoder(wl)
+    got = G.gpu_decode(voc, wl.latent)
+    ref = O.decode(wl.arch, None, wl.latent, 0, G.oracle_folded(name))
+    G.compare_audio(ref, got, name)
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 31, 129])
+def test_decode_edge_lengths(T):
+    """Single frame, lengths inside one tile, one past a tile (in latent frames;
+    every stage multiplies the rows, so the later layers see ragged tails too)."""
+    wl = G.workload("tiny_cal")
+    lat = np.random.default_rng(T).standard_normal((2, 16, T)).astype(np.float32)
+    voc = G.gpu_decoder(wl)
+    got = G.gpu_decode(voc, lat)
+    ref = O.decode(wl.arch, None, lat, 0, G.oracle_folded("tiny_cal"))
+    assert got.shape == (2, T * 512)
+    G.compare_audio(ref, got, f"T={T}")
+
+
+def test_batch_equals_items():
+    """Items of a batch decode independently: identical to one-item decodes, bit for bit."""
+    wl = G.workload("tiny_cal")
+    lat = np.random.default_rng(4).standard_normal((3, 16, 40)).astype(np.float32)
+    voc = G.gpu_decoder(wl)
+    yb = G.gpu_decode(voc, lat)
+    for i in range(3):
+        yi = G.gpu_decode(voc, lat[i:i + 1])
+        np.testing.assert_array_equal(yb[i], yi[0])
+
+
+def _sampled_full_size(name, n_items=None, width=8, n=3):
+    wl = G.workload(name)
+    folded = G.oracle_folded(name)
+    voc = G.gpu_decoder(wl)
+    got = G.gpu_decode(voc, wl.latent)
+    hop = wl.arch.hop
+    assert got.shape == (wl.B, wl.T * hop)
+    assert np.all(np.abs(got) <= 1.0)
+    items = range(wl.B) if n_items is None else range(min(n_items, wl.B))
+    worst_err, worst_snr = 0.0, np.inf
+    for item in items:
+        for (a, b) in G.sampled_windows(wl.arch, wl.T, n=n, width=width):
+            ref = G.oracle_window(wl, folded, item, a, b)
+            err, snr = G.compare_audio(ref, got[item, a * hop:b * hop], f"{name}[{item}][{a}:{b}]")
+            worst_err, worst_snr = max(worst_err, err), min(worst_snr, snr)
+    return got, worst_err, worst_snr
+
+
+def test_decode_music_window_sampled():
+    _sampled_full_size("music_window")
+
+
+def test_decode_speech_sampled():
+    _sampled_full_size("speech", n_items=3)
+
+
+@pytest.mark.slow
+def test_decode_music_long_sampled():
+    _sampled_full_size("music_long", n=4)
+
+
+def test_music_batch8_stitch():
+    """Windowed workload: GPU decode of the 16 window items, GPU stitch, checked
+    (a) bit-exactly against the oracle's stitch of the same decoded windows and
+    (b) against the oracle's single pass over the continuous latent at sampled
+    positions (the windows' crops exceed the receptive field)."""
+    wl = G.workload("music_batch8")
+    st = wl.stitch
+    voc = G.gpu_decoder(wl)
+    lat = torch.from_numpy(wl.latent).cuda()
+    audio = voc.decode(lat, flags=V.VOC_FLAG_SYNC)
+    n = V.vocoder_stitched_length(st["n_win"], st["win_frames"], st["crop_left"],
+                                  st["crop_right"], st["hop"])
+    assert n == 1589248
+    out = torch.empty((st["n_sides"], n), dtype=torch.float32, device="cuda")
+    V.vocoder_stitch(audio, st["n_win"], st["n_sides"], st["win_frames"], st["crop_left"],
+                     st["crop_right"], st["hop"], out)
+    torch.cuda.synchronize()
+    dec = audio[:, 0].cpu().numpy().astype(np.float64)
+    ref_st = O.stitch(dec, st["n_win"], st["n_sides"], st["win_frames"], st["crop_left"],
+                      st["crop_right"], st["hop"])
+    np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64), ref_st)
+    # against a single pass of the continuous latent
+    cont = W.Workload(name="cont", arch=wl.arch, latent=wl.continuous_latent, params=wl.params)
+    folded = G.oracle_folded("music_batch8")
+    got = out.cpu().numpy().astype(np.float64)
+    hop = wl.arch.hop
+    total = wl.continuous_latent.shape[2]
+    for side in range(2):
+        for (a, b) in [(0, 6), (428, 434), (773, 779), (1500, 1506), (total - 6, total)]:
+            ref = G.oracle_window(cont, folded, side, a, b)
+            G.compare_audio(ref, got[side, a * hop:b * hop], f"stitch side {side} [{a}:{b}]")
+
+
+# ----------------------------------------------------------------------------- API paths
+def test_decode_host_matches_device():
+    wl = G.workload("tiny_cal")
+    voc = G.gpu_decoder(wl)
+    lat = torch.from_numpy(wl.latent).pin_memory()
+    out = torch.empty((wl.B, 1, wl.T * 512), dtype=torch.float32).pin_memory()
+    ws = voc.alloc_workspace(wl.B, wl.T, host_io=True)
+    V.vocoder_decode_host(voc.handle, lat, out, ws)
+    dev = G.gpu_decode(voc, wl.latent)
+    np.testing.assert_array_equal(out[:, 0].numpy().astype(np.float64), dev)
+
+
+def test_workspace_too_small_and_nonfinite():
+    wl = G.workload("tiny_cal")
+    voc = G.gpu_decoder(wl)
+    lat = torch.from_numpy(wl.latent).cuda()
+    audio = torch.empty((1, 1, wl.T * 512), device="cuda")
+    need = voc.workspace_bytes(1, wl.T)
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(V.VocoderError) as e:
+        V.vocoder_decode(voc.handle, lat, audio, small)
+    assert e.value.status == V.VOC_WORKSPACE_TOO_SMALL
+    bad = lat.clone()
+    bad[0, 3, 5] = float("nan")
+    ws = voc.alloc_workspace(1, wl.T)
+    with pytest.raises(V.VocoderError) as e:
+        V.vocoder_decode(voc.handle, bad, audio, ws, flags=V.VOC_FLAG_CHECK_FINITE)
+    assert e.value.status == V.VOC_NONFINITE
+    # the context stays usable after the error
+    V.vocoder_decode(voc.handle, lat, audio, ws, flags=V.VOC_FLAG_CHECK_FINITE | V.VOC_FLAG_SYNC)
+
+
+def test_profile_records_every_launch():
+    wl = G.workload("tiny_cal")
+    voc = G.gpu_decoder(wl)
+    lat = torch.from_numpy(wl.latent).cuda()
+    voc.decode(lat, flags=V.VOC_FLAG_PROFILE | V.VOC_FLAG_SYNC)
+    prof = V.vocoder_profile(voc.handle)
+    assert len(prof) == V.vocoder_launches_per_decode(voc.handle, 1, wl.T)
+    assert all(p["ms"] >= 0 for p in prof)
+    assert sum(p["flops"] for p in prof) > 0
