@@ -40,6 +40,7 @@ EXPORTED = [
     "vocoder_abi_version", "vocoder_param_count", "vocoder_param_shape",
     "vocoder_fold_weight_norm", "vocoder_create", "vocoder_hop", "vocoder_workspace_bytes",
     "vocoder_workspace_bytes_host", "vocoder_decode", "vocoder_decode_host",
+    "vocoder_decode_static",
     "vocoder_stitched_length", "vocoder_stitch", "vocoder_op_conv1d",
     "vocoder_op_conv_transpose1d", "vocoder_launches_per_decode", "vocoder_profile_count",
     "vocoder_profile_entry", "vocoder_last_error", "vocoder_destroy",
@@ -104,6 +105,8 @@ def load_library():
     lib.vocoder_decode.argtypes = [P, P, I, I, P, P, ctypes.c_size_t, P, ctypes.c_uint]
     lib.vocoder_decode_host.restype = I
     lib.vocoder_decode_host.argtypes = [P, P, I, I, P, P, ctypes.c_size_t, P, ctypes.c_uint]
+    lib.vocoder_decode_static.restype = I
+    lib.vocoder_decode_static.argtypes = [P, P, I, I, P, P, ctypes.c_uint]
     lib.vocoder_stitched_length.restype = ctypes.c_longlong
     lib.vocoder_stitched_length.argtypes = [I, I, I, I, I]
     lib.vocoder_stitch.restype = I
@@ -235,6 +238,19 @@ def vocoder_decode_host(h, latent_host, audio_host, ws, stream=None, flags: int 
                                                ctypes.c_void_p(audio_host.data_ptr()),
                                                ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                                                _stream_ptr(stream), flags), h)
+
+
+VOC_STATIC_WORKSPACE_BYTES = 64 << 20
+
+
+def vocoder_decode_static(h, latent, audio, stream=None, flags: int = 0) -> None:
+    """Decode with the library's built-in workspace array: no device allocation
+    happens in this call (for callers that may not allocate while they run, such
+    as real-time audio threads).  Calls that overlap on the GPU race on the array."""
+    B, _, T = latent.shape
+    _check(load_library().vocoder_decode_static(h, ctypes.c_void_p(latent.data_ptr()), B, T,
+                                                 ctypes.c_void_p(audio.data_ptr()),
+                                                 _stream_ptr(stream), flags), h)
 
 
 def vocoder_stitched_length(n_win, win_frames, crop_left, crop_right, hop) -> int:

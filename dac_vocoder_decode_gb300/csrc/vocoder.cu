@@ -832,6 +832,49 @@ VOC_API voc_status vocoder_decode_host(vocoder *ctx, const float *latent_host, i
   return VOC_OK;
 }
 
+// ------------------------------------------------------------------ no-allocation decode
+// The workspace of vocoder_decode_static: one array per device, in the library's module.
+static __device__ __align__(256) uint8_t g_static_ws[VOC_STATIC_WORKSPACE_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_ws_addr[kMaxDevices] = {};  // device address of g_static_ws, per device
+}  // namespace
+
+VOC_API voc_status vocoder_decode_static(vocoder *ctx, const float *latent_dev, int B, int T,
+                                         float *audio_dev, voc_stream_t stream, unsigned flags) {
+  if (!ctx) return fail(nullptr, VOC_INVALID_ARG, "ctx is NULL");
+  if (!latent_dev || !audio_dev) return fail(ctx, VOC_INVALID_ARG, "latent / audio NULL");
+  if (B < 1 || T < 1) return fail(ctx, VOC_INVALID_ARG, "B and T must be positive");
+  if (flags & VOC_FLAG_PROFILE)
+    return fail(ctx, VOC_INVALID_ARG, "VOC_FLAG_PROFILE is not available without allocation");
+  const size_t need = vocoder_workspace_bytes(ctx, B, T);
+  if (!need) return fail(ctx, VOC_INVALID_ARG, "invalid B / T");
+  if (need > VOC_STATIC_WORKSPACE_BYTES)
+    return fail(ctx, VOC_WORKSPACE_TOO_SMALL,
+                "B=" + std::to_string(B) + ", T=" + std::to_string(T) + " needs " +
+                    std::to_string(need) + " bytes of workspace; the built-in array holds " +
+                    std::to_string(VOC_STATIC_WORKSPACE_BYTES) + " (use vocoder_decode)");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ctx, VOC_UNSUPPORTED, "device index too large");
+  void *ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ws_addr[dev]) {
+      void *p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_static_ws);  // host code may not use &g_static_ws itself
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetSymbolAddress");
+      g_static_ws_addr[dev] = p;
+    }
+    ws = g_static_ws_addr[dev];
+  }
+  return decode_impl(ctx, latent_dev, B, T, audio_dev, ws, VOC_STATIC_WORKSPACE_BYTES,
+                     reinterpret_cast<cudaStream_t>(stream), flags);
+}
+
 VOC_API long long vocoder_stitched_length(int n_win, int win_frames, int crop_left, int crop_right,
                                           int hop) {
   if (n_win < 1 || win_frames < 1 || crop_left < 0 || crop_right < 0 || hop < 1) return -1;

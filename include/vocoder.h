@@ -153,6 +153,34 @@ voc_status vocoder_decode_host(vocoder_t *ctx, const float *latent_host, int B, 
                                float *audio_host, void *ws_dev, size_t ws_bytes,
                                voc_stream_t stream, unsigned flags);
 
+/* Decode without allocating any device memory.  No counterpart on the source
+ * pages: this entry point exists for callers that must not call cudaMalloc
+ * while they run -- a real-time audio thread, where cudaMalloc can synchronise
+ * the device and stall long enough to drop an audio buffer, or a host
+ * application whose own allocator has already reserved the device memory and
+ * forbids allocations behind its back.  The context must still be created
+ * beforehand (vocoder_create allocates the weights once, at set-up time).
+ *
+ * Same inputs, outputs and results as vocoder_decode, but the workspace is a
+ * file-scope device array of VOC_STATIC_WORKSPACE_BYTES inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *   - Sizes whose vocoder_workspace_bytes(ctx, B, T) exceeds
+ *     VOC_STATIC_WORKSPACE_BYTES are rejected with VOC_WORKSPACE_TOO_SMALL.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array, which keeps the contents of the last
+ *     call.  The decode writes each workspace byte before reading it, so
+ *     nothing needs clearing, but calls that overlap on the GPU (other
+ *     streams, other threads, other contexts) race on the array and corrupt
+ *     each other's audio: serialise them.
+ *   - VOC_FLAG_PROFILE is rejected (VOC_INVALID_ARG); the other flags behave
+ *     as in vocoder_decode.
+ * The function itself calls no cudaMalloc, cudaFree or allocating routine. */
+#define VOC_STATIC_WORKSPACE_BYTES (64ull << 20)
+voc_status vocoder_decode_static(vocoder_t *ctx, const float *latent_dev, int B, int T,
+                                 float *audio_dev, voc_stream_t stream, unsigned flags);
+
 /* Overlap-crop stitch (minimaxmusic.cpp Architecture, "Decode and stitch"):
  *   decoded_dev [n_win*n_sides][win_frames*hop], item index w*n_sides + side;
  * window 0 keeps its left edge, later windows drop crop_left frames on the

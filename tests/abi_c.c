@@ -61,6 +61,8 @@ int main(void) {
                        (voc_stream_t)0, 0) == VOC_INVALID_ARG);
   CHECK(vocoder_decode_host((vocoder_t *)0, (const float *)0, 1, 1, (float *)0, (void *)0, 0,
                             (voc_stream_t)0, 0) == VOC_INVALID_ARG);
+  CHECK(vocoder_decode_static((vocoder_t *)0, (const float *)0, 1, 1, (float *)0, (voc_stream_t)0,
+                              0) == VOC_INVALID_ARG);
   CHECK(vocoder_stitched_length(8, 689, 86, 258, 512) == 1589248LL);
   CHECK(vocoder_stitched_length(0, 689, 86, 258, 512) == -1);
   CHECK(vocoder_stitch((const float *)0, 8, 2, 689, 86, 258, 512, (float *)0, (voc_stream_t)0) ==
