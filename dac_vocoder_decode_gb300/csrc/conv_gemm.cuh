@@ -23,20 +23,30 @@
 // 16-byte shift of the descriptor start address and all taps reuse one staged
 // halo tile (128 + span rows) loaded by TMA with zero fill outside [0, L).
 //
-// Roles: warp 0 lane 0 issues TMA / bulk copies, warp 1 lane 0 issues MMAs,
-// warps 2..5 run the epilogue (TMEM -> registers -> bias, residual, Snake of
-// the next layer, hi/lo split -> global).  The grid is persistent; two TMEM
+// Roles: warp 0 lane 0 issues the A (TMA) and weight (bulk) copies, warp 1 lane 0
+// issues MMAs, warps 2..9 run the epilogue (TMEM -> registers -> bias, residual,
+// Snake of the next layer, hi/lo split -> global), warp 10 lane 0 prefetches the
+// residual input of the epilogue by TMA.  The grid is persistent; 2 to 4 TMEM
 // accumulators let the epilogue of one tile overlap the mainloop of the next.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
+#include "snake.cuh"
 
 namespace voc {
 
 constexpr int kTileM = 128;
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;                            // two per TMEM lane quadrant
+constexpr int kSkipWarp = 2 + kEpiWarps;                // residual prefetch warp
+constexpr int kGemmThreads = 32 * (kSkipWarp + 1);      // 352
+constexpr int kMaxAcc = 4;
+
+// bytes of per-warp epilogue staging (an fp32 tile and a hi/lo tile of 32 rows x cw columns)
+__host__ __device__ constexpr int epi_stage_bytes(int cw) { return kEpiWarps * 2 * 32 * cw * 4; }
+// bytes of one residual slot (128 rows x cw fp32 columns)
+__host__ __device__ constexpr int skip_slot_bytes(int cw) { return kTileM * cw * 4; }
 
 enum : int {
   EPI_F32_SNAKE = 1,  // the fp32 output receives Snake(v) instead of v
@@ -47,6 +57,7 @@ enum : int {
   ERR_TIMEOUT_PRODUCER = 1,
   ERR_TIMEOUT_MMA = 2,
   ERR_TIMEOUT_EPILOGUE = 4,
+  ERR_TIMEOUT_SKIP = 8,
 };
 
 struct ConvGemmArgs {
@@ -56,14 +67,14 @@ struct ConvGemmArgs {
   int shift0_q0, shift0_q1, tap_step;  // row shift of tap 0 (per ConvT phase group), per-tap step
   int q_split_tile;        // n-tiles >= this belong to phase group q = 1
   int N_tile, n_tiles, N_total, m_tiles;
-  int na, nb;              // A / B ring slots
+  int na, nb, ns;          // A / B / residual ring slots
   int a_bytes, b_bytes;    // slot strides in bytes (b_bytes = one packed weight tile)
-  int acc_cols;            // TMEM columns per accumulator (power of two >= 32)
+  int acc_cols, n_acc;     // TMEM columns per accumulator (power of two >= 32), accumulators
   const uint8_t *wB;       // packed weight tiles [n_tile][tap][kb][hi|lo][chunk][n][8]
   const float *bias;       // [N_total] per-column bias
   const float *alpha;      // [N_total] Snake alpha of the next layer, or null
   const float *invb;       // [N_total] 1/(alpha + 1e-9)
-  const float *skip;       // fp32 residual [B][L_in][N_total] or null
+  const float *skip;       // fp32 residual [B][L_in][N_total] or null (read through tmapS)
   float *out_f32;          // fp32 output [B][L_in][N_total] or null
   __nv_bfloat16 *out_hl;   // hi/lo output rows [B][L_in*s_rows][2*Cp_out] or null
   int Cp_out, s_rows;
@@ -72,100 +83,172 @@ struct ConvGemmArgs {
   int *err;                // device error word
 };
 
-__device__ __forceinline__ void store_hl16(__nv_bfloat16 *dst, int Cp, const float (&s)[16]) {
-  uint32_t hi[8], lo[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    __nv_bfloat16 h0 = __float2bfloat16_rn(s[2 * i]);
-    __nv_bfloat16 h1 = __float2bfloat16_rn(s[2 * i + 1]);
-    __nv_bfloat16 l0 = __float2bfloat16_rn(s[2 * i] - __bfloat162float(h0));
-    __nv_bfloat16 l1 = __float2bfloat16_rn(s[2 * i + 1] - __bfloat162float(h1));
-    hi[i] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
-            (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
-    lo[i] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
-            (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
-  }
-  uint4 *dh = reinterpret_cast<uint4 *>(dst);
-  uint4 *dl = reinterpret_cast<uint4 *>(dst + Cp);
-  dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-  dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-  dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-  dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+__device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
-__device__ __forceinline__ void load16(const float *src, float (&v)[16]) {
+template <int N>
+__device__ __forceinline__ void ldg_vec(const float *src, float (&v)[N]) {
   const float4 *s4 = reinterpret_cast<const float4 *>(src);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float4 a = __ldg(s4 + j);
+  for (int j = 0; j < N / 4; ++j) {
+    const float4 a = __ldg(s4 + j);
     v[4 * j] = a.x, v[4 * j + 1] = a.y, v[4 * j + 2] = a.z, v[4 * j + 3] = a.w;
   }
 }
 
-__device__ __forceinline__ void store16(float *dst, const float (&v)[16]) {
-  float4 *d4 = reinterpret_cast<float4 *>(dst);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-}
+// Shared tiles of rows of CW fp32 (CW*4 bytes) whose 16-byte chunks are XOR-
+// swizzled by the row index: the layout the TMA writes with 128-byte (CW = 32)
+// or 64-byte (CW = 16) swizzling from a 1024-byte aligned base.  Row-wise and
+// column-wise 16-byte accesses by a warp are then free of bank conflicts.
+template <int CW>
+struct Stage {
+  static constexpr int NCH = CW / 4;        // 16-byte chunks per row
+  static constexpr int RB = CW * 4;         // bytes per row
+  static constexpr int RPI = 32 / NCH;      // rows per warp-wide 16-byte access
+  __device__ static __forceinline__ uint32_t at(uint32_t base, int r, int c) {
+    const int sw = (NCH == 8) ? (r & 7) : ((r >> 1) & 3);
+    return base + static_cast<uint32_t>(r * RB + ((c ^ sw) << 4));
+  }
+};
 
-// Epilogue of 16 consecutive columns n0..n0+15 of D row `drow` (= b*L_in + t).
-__device__ __forceinline__ void epilogue16(const ConvGemmArgs &p, size_t drow, int n0,
-                                           float (&v)[16]) {
-  float tmp[16];
-  load16(p.bias + n0, tmp);
+// Epilogue of one warp for 32 rows (its TMEM lane quadrant) x CW columns.
+// Global stores go through the warp's staging tiles: the thread of row r writes
+// its row, then every lane moves 16-byte pieces so that one warp-wide store covers
+// whole row segments (CW = 32: 4 rows x 128 B).  The residual input arrives in a
+// shared slot filled by the prefetch warp (slot row r = tile row r).
+template <int CW>
+__device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t stf, uint32_t sth,
+                                               uint32_t sslot, uint32_t sfull, uint32_t sempty,
+                                               uint32_t sparity, const volatile int *abort_flag,
+                                               int lane, int quad, int b, int t0w, int n0,
+                                               uint32_t taddr) {
+  using S = Stage<CW>;
+  float v[CW];
+  tmem_ld(taddr, v);
+  {
+    float bb[CW];
+    ldg_vec(p.bias + n0, bb);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] += tmp[i];
+    for (int i = 0; i < CW; ++i) v[i] += bb[i];
+  }
+  const size_t row0 = (size_t)b * p.L_in;  // D row of t = 0 in this item
   if (p.skip) {
-    load16(p.skip + drow * p.N_total + n0, tmp);  // read before the (possibly in-place) store
+    if (!mbar_wait(sfull, sparity, p.timeout, abort_flag)) return false;
+    const int r = quad * 32 + lane;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] += tmp[i];
+    for (int c = 0; c < S::NCH; ++c) {
+      const uint4 x = lds128(S::at(sslot, r, c));
+      v[4 * c] += __uint_as_float(x.x), v[4 * c + 1] += __uint_as_float(x.y);
+      v[4 * c + 2] += __uint_as_float(x.z), v[4 * c + 3] += __uint_as_float(x.w);
+    }
+    mbar_arrive(sempty);
   }
+  float sn[CW];
   if (p.alpha) {
-    float a[16], ib[16], s[16];
-    load16(p.alpha + n0, a);
-    load16(p.invb + n0, ib);
+    float a[CW], ib[CW];
+    ldg_vec(p.alpha + n0, a);
+    ldg_vec(p.invb + n0, ib);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float sn = sinf(a[i] * v[i]);
-      s[i] = fmaf(ib[i] * sn, sn, v[i]);  // Snake: v + sin^2(a v) / (a + 1e-9)
-    }
-    if (p.out_f32) store16(p.out_f32 + drow * p.N_total + n0, (p.flags & EPI_F32_SNAKE) ? s : v);
-    if (p.out_hl) {
-      const int r = n0 / p.Cp_out;
-      const int co = n0 - r * p.Cp_out;
-      store_hl16(p.out_hl + (drow * p.s_rows + r) * (size_t)(2 * p.Cp_out) + co, p.Cp_out, s);
-    }
+    for (int i = 0; i < CW; ++i) sn[i] = snake(v[i], a[i], ib[i]);
   } else {
-    if (p.out_f32) store16(p.out_f32 + drow * p.N_total + n0, v);
-    if (p.out_hl) {
-      const int r = n0 / p.Cp_out;
-      const int co = n0 - r * p.Cp_out;
-      store_hl16(p.out_hl + (drow * p.s_rows + r) * (size_t)(2 * p.Cp_out) + co, p.Cp_out, v);
+#pragma unroll
+    for (int i = 0; i < CW; ++i) sn[i] = v[i];
+  }
+  if (p.out_f32) {
+    const bool snake_out = (p.flags & EPI_F32_SNAKE) != 0;
+#pragma unroll
+    for (int c = 0; c < S::NCH; ++c) {
+      const float *src = snake_out ? sn : v;
+      sts128(S::at(stf, lane, c),
+             make_uint4(__float_as_uint(src[4 * c]), __float_as_uint(src[4 * c + 1]),
+                        __float_as_uint(src[4 * c + 2]), __float_as_uint(src[4 * c + 3])));
     }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < S::NCH; ++i) {
+      const int r = i * S::RPI + lane / S::NCH, c = lane % S::NCH;
+      const int t = t0w + r;
+      const uint4 x = lds128(S::at(stf, r, c));
+      if (t < p.L_in)
+        *reinterpret_cast<uint4 *>(p.out_f32 + (row0 + t) * p.N_total + n0 + 4 * c) = x;
+    }
+    __syncwarp();
+  }
+  if (p.out_hl) {
+    uint32_t hw[CW / 2], lw[CW / 2];
+#pragma unroll
+    for (int i = 0; i < CW / 2; ++i) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(sn[2 * i]);
+      const __nv_bfloat16 h1 = __float2bfloat16_rn(sn[2 * i + 1]);
+      const __nv_bfloat16 l0 = __float2bfloat16_rn(sn[2 * i] - __bfloat162float(h0));
+      const __nv_bfloat16 l1 = __float2bfloat16_rn(sn[2 * i + 1] - __bfloat162float(h1));
+      hw[i] = pack_bf16x2(h0, h1);
+      lw[i] = pack_bf16x2(l0, l1);
+    }
+#pragma unroll
+    for (int c = 0; c < S::NCH / 2; ++c) {
+      sts128(S::at(sth, lane, c), make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]));
+      sts128(S::at(sth, lane, S::NCH / 2 + c),
+             make_uint4(lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]));
+    }
+    __syncwarp();
+    const int ph = n0 / p.Cp_out;  // ConvT phase of these columns (0 for a conv)
+    const int co0 = n0 - ph * p.Cp_out;
+#pragma unroll
+    for (int i = 0; i < S::NCH; ++i) {
+      const int r = i * S::RPI + lane / S::NCH, c = lane % S::NCH;
+      const int t = t0w + r;
+      const uint4 x = lds128(S::at(sth, r, c));
+      if (t < p.L_in) {
+        const size_t orow = (row0 + t) * p.s_rows + ph;
+        const int col = (c < S::NCH / 2) ? co0 + 8 * c : p.Cp_out + co0 + 8 * (c - S::NCH / 2);
+        *reinterpret_cast<uint4 *>(p.out_hl + orow * (size_t)(2 * p.Cp_out) + col) = x;
+      }
+    }
+    __syncwarp();
+  }
+  return true;
+}
+
+// Wait (bounded) until every fill issued into a ring of `slots` barriers has
+// landed: the last fill of slot s (its cnt-th) completes the phase of parity (cnt-1)&1.
+__device__ __forceinline__ void drain_ring(uint64_t *full, int slots, int issued, long long budget) {
+  const volatile int never = 0;
+  for (int s = 0; s < slots && s < issued; ++s) {
+    const int cnt = (issued - s + slots - 1) / slots;
+    mbar_wait(smem_u32(full + s), static_cast<uint32_t>(cnt - 1) & 1u, budget, &never);
   }
 }
 
+template <int CW>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    conv_gemm_kernel(const __grid_constant__ CUtensorMap tmapA, const ConvGemmArgs p) {
+    conv_gemm_kernel(const __grid_constant__ CUtensorMap tmapA,
+                     const __grid_constant__ CUtensorMap tmapS, const ConvGemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *smA = smem;
   uint8_t *smB = smA + (size_t)p.na * p.a_bytes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smB + (size_t)p.nb * p.b_bytes);
+  uint8_t *smE = smB + (size_t)p.nb * p.b_bytes;   // epilogue staging
+  uint8_t *smS = smE + epi_stage_bytes(CW);         // residual slots
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smS + (size_t)p.ns * skip_slot_bytes(CW));
   uint64_t *fullA = bars;
   uint64_t *emptyA = fullA + p.na;
   uint64_t *fullB = emptyA + p.na;
   uint64_t *emptyB = fullB + p.nb;
   uint64_t *accFull = emptyB + p.nb;
-  uint64_t *accEmpty = accFull + 2;
-  uint64_t *drain = accEmpty + 2;
+  uint64_t *accEmpty = accFull + kMaxAcc;
+  uint64_t *skipFull = accEmpty + kMaxAcc;
+  uint64_t *skipEmpty = skipFull + p.ns;
+  uint64_t *drain = skipEmpty + p.ns;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t tmem_cols = 2u * p.acc_cols;
+  const uint32_t tmem_cols = static_cast<uint32_t>(p.n_acc * p.acc_cols);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.na; ++i) {
@@ -176,9 +259,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(fullB + i), 1);
       mbar_init(smem_u32(emptyB + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(smem_u32(accFull + i), 1);
-      mbar_init(smem_u32(accEmpty + i), 4 * 32);
+      mbar_init(smem_u32(accEmpty + i), kEpiWarps * 32);
+    }
+    for (int i = 0; i < p.ns; ++i) {
+      mbar_init(smem_u32(skipFull + i), 1);
+      mbar_init(smem_u32(skipEmpty + i), 4 * 32);  // the four quadrant warps of one half
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -198,10 +285,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int kchunks = p.KB / 8;
   const uint32_t chunkA = static_cast<uint32_t>(p.rows) * 16u;
   const uint32_t chunkB = static_cast<uint32_t>(p.N_tile) * 16u;
+  const int n_chunks = p.N_tile / CW;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------------------ producer
+      // ------------------------------------------------------------ A / weight producer
       prefetch_tmap(&tmapA);
       const uint32_t a_tx = 2u * kchunks * chunkA;
       int ia = 0, ib = 0;
@@ -247,17 +335,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) {
         atomicOr(p.err, ERR_TIMEOUT_PRODUCER);
         *abort_flag = 1;
-        // let every copy already issued land before the CTA can exit: the last
-        // fill of slot s (its cnt-th) completes the phase of parity (cnt-1)&1
-        const volatile int never = 0;
-        for (int s = 0; s < p.na && s < ia; ++s) {
-          const int cnt = (ia - s + p.na - 1) / p.na;
-          mbar_wait(smem_u32(fullA + s), static_cast<uint32_t>(cnt - 1) & 1u, p.timeout, &never);
-        }
-        for (int s = 0; s < p.nb && s < ib; ++s) {
-          const int cnt = (ib - s + p.nb - 1) / p.nb;
-          mbar_wait(smem_u32(fullB + s), static_cast<uint32_t>(cnt - 1) & 1u, p.timeout, &never);
-        }
+        drain_ring(fullA, p.na, ia, p.timeout);  // copies in flight land before the CTA exits
+        drain_ring(fullB, p.nb, ib, p.timeout);
       }
     }
   } else if (warp == 1) {
@@ -269,8 +348,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
         const int nt = tile % p.n_tiles;
         const int shift0 = (nt >= p.q_split_tile) ? p.shift0_q1 : p.shift0_q0;
-        const int acc = it & 1;
-        const uint32_t phacc = static_cast<uint32_t>(it >> 1) & 1u;
+        const int acc = it % p.n_acc;
+        const uint32_t phacc = static_cast<uint32_t>(it / p.n_acc) & 1u;
         if (!mbar_wait(smem_u32(accEmpty + acc), phacc ^ 1u, p.timeout, abort_flag)) {
           ok = false;
           break;
@@ -325,36 +404,79 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_wait(smem_u32(drain), 0u, p.timeout, &never);
       }
     }
+  } else if (warp == kSkipWarp) {
+    if (lane == 0 && p.skip) {
+      // ------------------------------------------------------------ residual prefetch
+      prefetch_tmap(&tmapS);
+      const uint32_t bytes = static_cast<uint32_t>(skip_slot_bytes(CW));
+      int ks = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        const int nt = tile % p.n_tiles;
+        const int rest = tile / p.n_tiles;
+        const int mt = rest % p.m_tiles;
+        const int b = rest / p.m_tiles;
+        for (int c = 0; c < n_chunks; ++c, ++ks) {
+          const int slot = ks % p.ns;
+          const uint32_t ph = static_cast<uint32_t>(ks / p.ns) & 1u;
+          if (!mbar_wait(smem_u32(skipEmpty + slot), ph ^ 1u, p.timeout, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fs = smem_u32(skipFull + slot);
+          mbar_arrive_expect_tx(fs, bytes);
+          tma_load_3d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, nt * p.N_tile + c * CW,
+                      mt * kTileM, b);
+        }
+      }
+      if (!ok) {
+        atomicOr(p.err, ERR_TIMEOUT_SKIP);
+        *abort_flag = 1;
+        drain_ring(skipFull, p.ns, ks, p.timeout);
+      }
+    }
   } else {
     // -------------------------------------------------------------- epilogue
+    const int e = warp - 2;     // epilogue warp 0..7
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
-    const int row = quad * 32 + lane;
+    const int half = e / 4;     // the two warps of a quadrant take alternate column chunks
+    const uint32_t stf = smem_u32(smE) + static_cast<uint32_t>(e * 2 * 32 * CW * 4);
+    const uint32_t sth = stf + 32 * CW * 4;
+    const uint32_t sbase = smem_u32(smS);
+    const int ns = p.ns > 0 ? p.ns : 1;
     int it = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
       const int nt = tile % p.n_tiles;
       const int rest = tile / p.n_tiles;
       const int mt = rest % p.m_tiles;
       const int b = rest / p.m_tiles;
-      const int acc = it & 1;
-      const uint32_t phacc = static_cast<uint32_t>(it >> 1) & 1u;
+      const int acc = it % p.n_acc;
+      const uint32_t phacc = static_cast<uint32_t>(it / p.n_acc) & 1u;
       if (!mbar_wait(smem_u32(accFull + acc), phacc, p.timeout, abort_flag)) {
-        atomicOr(p.err, ERR_TIMEOUT_EPILOGUE);
-        *abort_flag = 1;
+        ok = false;
         break;
       }
       tc_fence_after();
-      const int t = mt * kTileM + row;
-      const bool valid = t < p.L_in;
-      const size_t drow = (size_t)b * p.L_in + t;
+      const int t0w = mt * kTileM + quad * 32;
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * p.acc_cols) +
                              (static_cast<uint32_t>(quad * 32) << 16);
-      for (int c = 0; c < p.N_tile / 16; ++c) {
-        float v[16];
-        tmem_ld16(tbase + c * 16, v);
-        if (valid) epilogue16(p, drow, nt * p.N_tile + c * 16, v);
+      for (int c = half; c < n_chunks && ok; c += 2) {
+        const int kc = it * n_chunks + c;  // residual chunk counter (fill order of the slots)
+        const int slot = kc % ns;
+        ok = epilogue_chunk<CW>(
+            p, stf, sth, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
+            smem_u32(skipFull + slot), smem_u32(skipEmpty + slot),
+            static_cast<uint32_t>(kc / ns) & 1u, abort_flag, lane, quad, b, t0w,
+            nt * p.N_tile + c * CW, tbase + c * CW);
       }
+      if (!ok) break;
       tc_fence_before();
       mbar_arrive(smem_u32(accEmpty + acc));
+    }
+    if (!ok) {
+      atomicOr(p.err, ERR_TIMEOUT_EPILOGUE);
+      *abort_flag = 1;
     }
   }
 

@@ -1,0 +1,37 @@
+// snake.cuh -- Snake activation, y = x + sin^2(a x) / (a + 1e-9), with the
+// per-channel a used as stored (minimaxmusic.cpp Architecture, "Flow VAE";
+// MiniMax-Music-3 -> CMF README, "What the conversion had to get right").
+// inv_b = 1/(a + 1e-9) is formed on the host.
+#pragma once
+
+namespace voc {
+
+// sin^2 has period pi, so with x = k*pi + r and |r| <= pi/2, sin^2(x) = sin^2(r).
+// k*pi is removed with a two-constant (Cody & Waite) reduction: kPiHi = 201/64
+// carries the leading 8 bits of pi, so k*kPiHi is exact for |k| < 2^16, and kPiLo
+// holds pi - 201/64.  The hardware approximation __sinf is then evaluated on
+// [-pi/2, pi/2] (within [-pi, pi], where its absolute error is about 2^-21).
+// Arguments beyond 8192 in magnitude go to sinf.
+constexpr float kInvPi = 0.318309886183790671538f;
+constexpr float kPiHi = 3.140625f;
+constexpr float kPiLo = 9.67653589793238462643e-4f;
+
+__device__ __noinline__ float sin2_wide(float x) {
+  const float s = sinf(x);
+  return s * s;
+}
+
+__device__ __forceinline__ float sin2(float x) {
+  if (fabsf(x) > 8192.f) return sin2_wide(x);
+  const float k = rintf(x * kInvPi);
+  float r = fmaf(-k, kPiHi, x);
+  r = fmaf(-k, kPiLo, r);
+  const float s = __sinf(r);
+  return s * s;
+}
+
+__device__ __forceinline__ float snake(float v, float a, float inv_b) {
+  return fmaf(inv_b, sin2(a * v), v);
+}
+
+}  // namespace voc

@@ -9,13 +9,9 @@
 
 #include <cstdint>
 
-namespace voc {
+#include "snake.cuh"
 
-// Snake of one value: v + sin^2(a v) * inv_b  (minimaxmusic.cpp Architecture, "Flow VAE")
-__device__ __forceinline__ float snake1(float v, float a, float inv_b) {
-  const float sn = sinf(a * v);
-  return fmaf(inv_b * sn, sn, v);
-}
+namespace voc {
 
 // x [B][C][T] fp32 -> hl [B][T][2*Cp] bf16 (per row: Cp hi values, then Cp lo values);
 // channels C..Cp-1 are written as zeros.  alpha == nullptr: no Snake.
@@ -32,7 +28,7 @@ __global__ void prep_hl_kernel(const float *__restrict__ x, int C, int T, int Cp
     float v = 0.f;
     if (c < C && t < T) {
       v = x[((size_t)b * C + c) * T + t];
-      if (alpha) v = snake1(v, alpha[c], invb[c]);
+      if (alpha) v = snake(v, alpha[c], invb[c]);
     }
     tile[i][threadIdx.x] = v;
   }

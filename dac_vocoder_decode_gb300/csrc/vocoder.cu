@@ -59,6 +59,7 @@ struct Layer {
   float *bias_dev = nullptr, *alpha_dev = nullptr, *invb_dev = nullptr;
   int in_buf = -1, f32_buf = -1, hl_buf = -1, skip_buf = -1;
   int epi_flags = 0;
+  int cw = 32;              // epilogue column chunk (32, or 16 when 32 does not divide the tile)
 };
 
 struct OutHead {
@@ -84,8 +85,11 @@ bool set_kernel_attrs(std::string &why) {
   static cudaError_t st = cudaErrorUnknown;
   static std::once_flag once;
   std::call_once(once, [] {
-    st = cudaFuncSetAttribute(voc::conv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemMax);
+    st = cudaFuncSetAttribute(voc::conv_gemm_kernel<32>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::out_head_kernel<kHeadTile>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
@@ -112,7 +116,7 @@ struct vocoder {
   // TMA descriptors for the last (workspace, B, T)
   void *map_ws = nullptr;
   int map_B = -1, map_T = -1;
-  std::vector<CUtensorMap> maps;
+  std::vector<CUtensorMap> maps, skip_maps;
   // profiling of the last decode with VOC_FLAG_PROFILE
   std::vector<cudaEvent_t> events;
   std::vector<std::string> prof_names;
@@ -139,7 +143,7 @@ voc_status cuda_fail(vocoder *ctx, cudaError_t e, const char *what) {
 
 // ------------------------------------------------------------------ planning
 // Plan the GEMM geometry of one conv (convT = false) or transposed conv layer.
-bool plan_gemm(Layer &L, int padding, std::string &why) {
+bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   ConvGemmArgs &g = L.g;
   L.Cp_in = rup(L.Cin, 16);
   L.Cp_out = rup(L.Cout, 16);
@@ -193,11 +197,21 @@ bool plan_gemm(Layer &L, int padding, std::string &why) {
     why = "tap span too wide for one staged tile (" + std::to_string(off_max - off_min) + ")";
     return false;
   }
+  L.cw = (g.N_tile % 32 == 0 && L.Cp_out % 32 == 0) ? 32 : 16;
+  const int epi = voc::epi_stage_bytes(L.cw);
   const int chunkA = g.rows * 16;
   g.a_bytes = rup(2 * (g.KB / 8) * chunkA, 1024);
   g.b_bytes = 4 * g.KB * g.N_tile;
   g.na = 2;
-  const int avail = kSmemMax - 1024 - 256 - g.na * g.a_bytes;
+  // residual slots (layers with a skip input): as many as leave >= 3 weight stages, 2..4
+  g.ns = 0;
+  int avail = kSmemMax - 1024 - 256 - g.na * g.a_bytes - epi;
+  if (has_skip) {
+    const int sb = voc::skip_slot_bytes(L.cw);
+    g.ns = 4;
+    while (g.ns > 2 && (avail - g.ns * sb) / g.b_bytes < 3) --g.ns;
+    avail -= g.ns * sb;
+  }
   g.nb = std::min(8, avail / g.b_bytes);
   if (g.nb < 2) {
     why = "shared memory plan does not fit";
@@ -206,7 +220,9 @@ bool plan_gemm(Layer &L, int padding, std::string &why) {
   int ac = 32;
   while (ac < g.N_tile) ac *= 2;
   g.acc_cols = ac;
-  L.smem = 1024 + (size_t)g.na * g.a_bytes + (size_t)g.nb * g.b_bytes + 256;
+  g.n_acc = std::min(voc::kMaxAcc, 512 / ac);
+  L.smem = 1024 + (size_t)g.na * g.a_bytes + (size_t)g.nb * g.b_bytes + epi +
+           (size_t)g.ns * voc::skip_slot_bytes(L.cw) + 256;
   return true;
 }
 
@@ -365,6 +381,25 @@ voc_status encode_map(vocoder *ctx, CUtensorMap *map, const void *base, int Cp, 
   return VOC_OK;
 }
 
+// Residual (skip) input of an epilogue: fp32 rows [B][L][N_total], read in boxes of
+// 128 rows x cw columns with the swizzle the epilogue's shared reads expect.
+voc_status encode_skip_map(vocoder *ctx, CUtensorMap *map, const void *base, int N_total,
+                           long long L, int B, int cw) {
+  auto enc = encode_fn();
+  if (!enc) return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled entry point unavailable");
+  const cuuint64_t dims[3] = {(cuuint64_t)N_total, (cuuint64_t)L, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)(4 * N_total), (cuuint64_t)(4 * N_total) * (cuuint64_t)L};
+  const cuuint32_t box[3] = {(cuuint32_t)cw, (cuuint32_t)voc::kTileM, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   cw == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled (residual) failed (" + std::to_string((int)r) + ")");
+  return VOC_OK;
+}
+
 void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *const *bufs,
                       ConvGemmArgs &a) {
   a = L.g;
@@ -397,11 +432,14 @@ void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops,
   bytes = by;
 }
 
-voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map, const ConvGemmArgs &a,
-                       cudaStream_t stream) {
+voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
+                       const CUtensorMap &smap, const ConvGemmArgs &a, cudaStream_t stream) {
   const long long tiles = (long long)a.B * a.m_tiles * a.n_tiles;
   const int grid = static_cast<int>(std::min<long long>(tiles, ctx->num_sms));
-  voc::conv_gemm_kernel<<<grid, voc::kGemmThreads, L.smem, stream>>>(map, a);
+  if (L.cw == 32)
+    voc::conv_gemm_kernel<32><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
+  else
+    voc::conv_gemm_kernel<16><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, ("launch " + L.name).c_str());
   return VOC_OK;
@@ -572,7 +610,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     L.name = "conv_in";
     L.Cin = desc->latent_channels, L.Cout = desc->channels0, L.K = desc->in_kernel, L.dil = 1;
     L.level = 0;
-    if (!plan_gemm(L, pad, why)) return bail(fail(ctx, VOC_UNSUPPORTED, "conv_in: " + why));
+    if (!plan_gemm(L, pad, false, why)) return bail(fail(ctx, VOC_UNSUPPORTED, "conv_in: " + why));
     L.in_buf = BUF_H0, L.hl_buf = BUF_H1;
     st = upload_layer(ctx, ctx->allocs, L, pad, params[0], params[1], params[2]);
     if (st != VOC_OK) return bail(st);
@@ -590,7 +628,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       L.convT = true;
       L.Cin = C, L.Cout = Co, L.stride = ctx->strides[i], L.K = 2 * L.stride;
       L.level = i;
-      if (!plan_gemm(L, pad, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L.name + ": " + why));
+      if (!plan_gemm(L, pad, false, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L.name + ": " + why));
       L.in_buf = X, L.f32_buf = BUF_FY, L.hl_buf = A;
       st = upload_layer(ctx, ctx->allocs, L, pad, params[p + 1], params[p + 2], params[p + 3]);
       if (st != VOC_OK) return bail(st);
@@ -606,7 +644,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       L1.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".conv1";
       L1.Cin = C, L1.Cout = C, L1.K = desc->res_kernel, L1.dil = ctx->dils[j];
       L1.level = i + 1;
-      if (!plan_gemm(L1, pad, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L1.name + ": " + why));
+      if (!plan_gemm(L1, pad, false, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L1.name + ": " + why));
       L1.in_buf = A, L1.hl_buf = BUF_HB;
       st = upload_layer(ctx, ctx->allocs, L1, pad, w1, b1, a2);
       if (st != VOC_OK) return bail(st);
@@ -616,7 +654,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       L2.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".conv2";
       L2.Cin = C, L2.Cout = C, L2.K = 1, L2.dil = 1;
       L2.level = i + 1;
-      if (!plan_gemm(L2, pad, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L2.name + ": " + why));
+      if (!plan_gemm(L2, pad, true, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L2.name + ": " + why));
       L2.in_buf = BUF_HB, L2.skip_buf = BUF_FY;
       const float *next_alpha = params[p];  // next snake1 / next stage's snake / snake_out
       if (j < nd - 1) {
@@ -693,10 +731,14 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
   // TMA descriptors depend on the workspace address and the sizes only
   if (ctx->map_ws != ws || ctx->map_B != B || ctx->map_T != T) {
     ctx->maps.resize(ctx->layers.size());
+    ctx->skip_maps.assign(ctx->layers.size(), CUtensorMap{});
     for (size_t i = 0; i < ctx->layers.size(); ++i) {
       const Layer &L = ctx->layers[i];
       voc_status st = encode_map(ctx, &ctx->maps[i], bufs[L.in_buf], L.Cp_in,
                                  level_len(ctx, L.level, T), B, L.g.rows);
+      if (st == VOC_OK && L.skip_buf >= 0)
+        st = encode_skip_map(ctx, &ctx->skip_maps[i], bufs[L.skip_buf], L.g.N_total,
+                             level_len(ctx, L.level, T), B, L.cw);
       if (st != VOC_OK) {
         ctx->map_ws = nullptr;
         return st;
@@ -742,7 +784,7 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
     ConvGemmArgs a;
     gemm_launch_args(ctx, L, B, T, bufs, a);
     rec(0);
-    st = launch_gemm(ctx, L, ctx->maps[i], a, stream);
+    st = launch_gemm(ctx, L, ctx->maps[i], ctx->skip_maps[i], a, stream);
     if (st != VOC_OK) return st;
     rec(1);
     if (prof) {
@@ -910,7 +952,7 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
                     const float *b_host, const float *alpha_host, float *y_dev, cudaStream_t stream) {
   std::string why;
   if (!set_kernel_attrs(why)) return fail(nullptr, VOC_CUDA_ERROR, why);
-  if (!plan_gemm(L, padding, why)) return fail(nullptr, VOC_UNSUPPORTED, why);
+  if (!plan_gemm(L, padding, false, why)) return fail(nullptr, VOC_UNSUPPORTED, why);
   int dev = 0, sms = 0, major = 0, minor = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -957,7 +999,8 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
   L.in_buf = 0, L.f32_buf = BUF_FY;
   ConvGemmArgs a;
   gemm_launch_args(&tmp, L, B, T, bufs, a);
-  if ((st = launch_gemm(&tmp, L, map, a, stream)) != VOC_OK) return done(st);
+  const CUtensorMap no_skip{};
+  if ((st = launch_gemm(&tmp, L, map, no_skip, a, stream)) != VOC_OK) return done(st);
   dim3 grid((T * s + 31) / 32, (L.Cout + 31) / 32, B);
   voc::rows_to_cf_kernel<<<grid, dim3(32, 8), 0, stream>>>(static_cast<const float *>(rows), T * s,
                                                            L.Cp_out, L.Cout, y_dev);

@@ -73,6 +73,29 @@ def test_op_conv1d(case, with_snake):
         assert np.all(err <= LAYER_REL * mag + 1e-6), (bi, float(err.max()), float(mag.max()))
 
 
+def test_snake_accuracy_wide_range():
+    """The GPU Snake (sin^2 reduced by multiples of pi, then __sinf; sinf beyond
+    |a x| > 8192) through a 1x1 identity conv, so y = Snake(x) carried as a bf16
+    hi/lo pair.  Bound: 2^-16 |y| for the hi/lo split plus 4e-6 absolute for the
+    reduction (k * ulp(pi_lo) <= 2^-22) and __sinf (about 2^-21 on [-pi, pi])."""
+    rng = np.random.default_rng(7)
+    C, T = 32, 3000
+    parts = [rng.uniform(-4, 4, (C, 1000)), rng.uniform(-300, 300, (C, 1000)),
+             rng.uniform(-2e4, 2e4, (C, 1000))]
+    x = np.concatenate(parts, axis=1).astype(np.float32)[None]
+    x[0, :, :8] = 0.0
+    alpha = rng.uniform(0.5, 1.5, C).astype(np.float32)
+    w = np.eye(C, dtype=np.float32)[:, :, None]
+    y = torch.empty((1, C, T), dtype=torch.float32, device="cuda")
+    V.vocoder_op_conv1d(torch.from_numpy(x).cuda(), w, None, 1, W.PAD_SYMMETRIC, alpha, y)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy()[0].astype(np.float64)
+    ref = O.snake(x[0], alpha)
+    err = np.abs(got - ref)
+    assert np.all(err <= 2.0 ** -16 * np.abs(ref) + 4e-6), float(np.max(err - 2.0 ** -16 * np.abs(ref)))
+    assert np.all(got[:, :8] == 0.0)
+
+
 CONVT_CASES = [
     # B, Cin, Cout, T, stride, padding
     (2, 192, 96, 300, 2, W.PAD_SYMMETRIC),
