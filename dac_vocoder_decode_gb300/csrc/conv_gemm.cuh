@@ -2,32 +2,37 @@
 // layer of the decoder: conv_in (k7), the polyphase ConvTranspose1d, the k7
 // dilated conv1 and the k1 conv2 of each residual unit.
 //
-// GEMM view (channels-last activations, time on M, output columns on N):
+// GEMM view (time on M, output columns on N):
 //   D[t][n] = sum_tap sum_ci A[t + off(tap, n)][ci] * Wt[tap][n][ci]
 // * regular conv: off(tap) = tap*dil - pad_left, n = output channel;
 // * ConvTranspose1d of stride s, K = 2s, left crop p (polyphase form): the
 //   output sample t*s + r of channel co is column n = r*C_out + co and
 //     out[t*s + r][co] = sum_ci W[ci][co][k0] x[t+q][ci] + W[ci][co][k0+s] x[t+q-1][ci]
 //   with q = floor((r+p)/s), k0 = (r+p) mod s, i.e. two taps at row offsets q and
-//   q-1.  Row t of D is then exactly the contiguous channels-last output rows
-//   t*s .. t*s+s-1, so the overlap-add of col2im happens inside the MMA and no
+//   q-1.  The overlap-add of col2im happens inside the MMA accumulation and no
 //   column matrix is ever written.
 //
-// Operands: every activation that enters an MMA is stored as a bf16 pair
-// (hi, lo) with hi = bf16(x), lo = bf16(x - hi); weights are pre-split the same
-// way on the host.  Each K step issues three MMAs, hi*hi + hi*lo + lo*hi, into
-// one fp32 TMEM accumulator.
+// Activation layout in global memory ("chunk-major"): a bf16 hi/lo tensor of C
+// channels and length L is [B][2C/8][L][8] -- 8-channel chunks of the hi parts,
+// then of the lo parts, each chunk a contiguous run of L 16-byte rows; an fp32
+// tensor is [B][C/4][L][4].  hi = bf16(x), lo = bf16(x - hi).
 //
-// Shared-memory layout (no swizzle, K-major): an A stage holds, for each 8-channel
-// chunk, `rows` consecutive time rows of 16 bytes, so the row offset of a tap is a
-// 16-byte shift of the descriptor start address and all taps reuse one staged
-// halo tile (128 + span rows) loaded by TMA with zero fill outside [0, L).
+// Operands: each K step issues three MMAs, hi*hi + hi*lo + lo*hi, into one fp32
+// TMEM accumulator; weights are pre-split into hi/lo on the host.
+//
+// Shared-memory layout of an A stage (no swizzle, K-major canonical layout): for
+// each 8-channel chunk, `rows` consecutive time rows of 16 bytes -- exactly the
+// chunk-major global layout, so one TMA box per k-block fetches contiguous runs.
+// The row offset of a tap is a 16-byte shift of the descriptor start address, so
+// all taps reuse one staged halo tile (128 + span rows, zero fill outside [0, L)).
 //
 // Roles: warp 0 lane 0 issues the A (TMA) and weight (bulk) copies, warp 1 lane 0
 // issues MMAs, warps 2..9 run the epilogue (TMEM -> registers -> bias, residual,
-// Snake of the next layer, hi/lo split -> global), warp 10 lane 0 prefetches the
-// residual input of the epilogue by TMA.  The grid is persistent; 2 to 4 TMEM
-// accumulators let the epilogue of one tile overlap the mainloop of the next.
+// Snake of the next layer, hi/lo split -> global; with the chunk-major layout the
+// 32 lanes of a warp store 32 consecutive rows of one chunk: 512 contiguous
+// bytes), warp 10 lane 0 prefetches the residual input of the epilogue by TMA.
+// The grid is persistent; 2 to 4 TMEM accumulators let the epilogue of one tile
+// overlap the mainloop of the next.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -43,9 +48,7 @@ constexpr int kSkipWarp = 2 + kEpiWarps;                // residual prefetch war
 constexpr int kGemmThreads = 32 * (kSkipWarp + 1);      // 352
 constexpr int kMaxAcc = 4;
 
-// bytes of per-warp epilogue staging (an fp32 tile and a hi/lo tile of 32 rows x cw columns)
-__host__ __device__ constexpr int epi_stage_bytes(int cw) { return kEpiWarps * 2 * 32 * cw * 4; }
-// bytes of one residual slot (128 rows x cw fp32 columns)
+// bytes of one residual slot (128 rows x cw fp32 columns, as cw/4 chunks of 128 x 16 B)
 __host__ __device__ constexpr int skip_slot_bytes(int cw) { return kTileM * cw * 4; }
 
 enum : int {
@@ -74,14 +77,40 @@ struct ConvGemmArgs {
   const float *bias;       // [N_total] per-column bias
   const float *alpha;      // [N_total] Snake alpha of the next layer, or null
   const float *invb;       // [N_total] 1/(alpha + 1e-9)
-  const float *skip;       // fp32 residual [B][L_in][N_total] or null (read through tmapS)
-  float *out_f32;          // fp32 output [B][L_in][N_total] or null
-  __nv_bfloat16 *out_hl;   // hi/lo output rows [B][L_in*s_rows][2*Cp_out] or null
-  int Cp_out, s_rows;
+  const float *skip;       // fp32 residual (chunk-major, Cp_out channels) or null: read via TMA
+  float *out_f32;          // fp32 output, chunk-major [B][Cp_out/4][L_in*s_rows][4], or null
+  __nv_bfloat16 *out_hl;   // hi/lo output, chunk-major [B][2*Cp_out/8][L_in*s_rows][8], or null
+  int Cp_out, s_rows;      // output channels (padded), output rows per D row
   int flags;
   long long timeout;       // cycles a wait may take before the kernel gives up
   int *err;                // device error word
+  // extents used by the self-checking build (VOC_CHECKS)
+  long long f32_elems, hl_elems, w_bytes;
+  int smem_bytes, L_a, chunks_a, chunks_s;
+  int *dbg;                // [4]: first failed check code and three values
 };
+
+#ifdef VOC_CHECKS
+// Record the first failed check (code, three values), raise the abort flag; the caller skips
+// the access.
+__device__ __forceinline__ void check_fail(const ConvGemmArgs &p, volatile int *abort_flag,
+                                           int code, long long a, long long b, long long c) {
+  if (atomicCAS(p.dbg, 0, code) == 0) {
+    p.dbg[1] = static_cast<int>(a);
+    p.dbg[2] = static_cast<int>(b);
+    p.dbg[3] = static_cast<int>(c);
+  }
+  atomicOr(p.err, 0x100);
+  *abort_flag = 1;
+}
+#define VOC_CHECK(cond, code, a, b, c)                                   \
+  if (!(cond)) {                                                         \
+    check_fail(p, abort_flag, code, (long long)(a), (long long)(b), (long long)(c)); \
+    return false;                                                        \
+  }
+#else
+#define VOC_CHECK(cond, code, a, b, c)
+#endif
 
 __device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
@@ -98,33 +127,16 @@ __device__ __forceinline__ void ldg_vec(const float *src, float (&v)[N]) {
   }
 }
 
-// Shared tiles of rows of CW fp32 (CW*4 bytes) whose 16-byte chunks are XOR-
-// swizzled by the row index: the layout the TMA writes with 128-byte (CW = 32)
-// or 64-byte (CW = 16) swizzling from a 1024-byte aligned base.  Row-wise and
-// column-wise 16-byte accesses by a warp are then free of bank conflicts.
+// Epilogue of one warp for 32 rows (its TMEM lane quadrant) x CW columns
+// n0..n0+CW-1, which lie in one ConvT phase because CW divides C_out.
 template <int CW>
-struct Stage {
-  static constexpr int NCH = CW / 4;        // 16-byte chunks per row
-  static constexpr int RB = CW * 4;         // bytes per row
-  static constexpr int RPI = 32 / NCH;      // rows per warp-wide 16-byte access
-  __device__ static __forceinline__ uint32_t at(uint32_t base, int r, int c) {
-    const int sw = (NCH == 8) ? (r & 7) : ((r >> 1) & 3);
-    return base + static_cast<uint32_t>(r * RB + ((c ^ sw) << 4));
-  }
-};
-
-// Epilogue of one warp for 32 rows (its TMEM lane quadrant) x CW columns.
-// Global stores go through the warp's staging tiles: the thread of row r writes
-// its row, then every lane moves 16-byte pieces so that one warp-wide store covers
-// whole row segments (CW = 32: 4 rows x 128 B).  The residual input arrives in a
-// shared slot filled by the prefetch warp (slot row r = tile row r).
-template <int CW>
-__device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t stf, uint32_t sth,
-                                               uint32_t sslot, uint32_t sfull, uint32_t sempty,
-                                               uint32_t sparity, const volatile int *abort_flag,
-                                               int lane, int quad, int b, int t0w, int n0,
-                                               uint32_t taddr) {
-  using S = Stage<CW>;
+__device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t sslot,
+                                               uint32_t sfull, uint32_t sempty, uint32_t sparity,
+                                               volatile int *abort_flag, int row_in_tile,
+                                               int b, int t, int n0, uint32_t taddr,
+                                               uint32_t smem_lo, uint32_t smem_hi) {
+  VOC_CHECK((taddr & 0xFFFFu) + CW <= (uint32_t)(p.n_acc * p.acc_cols), 11, taddr & 0xFFFF, CW, 0);
+  VOC_CHECK(n0 + CW <= p.N_total, 12, n0, p.N_total, 0);
   float v[CW];
   tmem_ld(taddr, v);
   {
@@ -133,15 +145,14 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
 #pragma unroll
     for (int i = 0; i < CW; ++i) v[i] += bb[i];
   }
-  const size_t row0 = (size_t)b * p.L_in;  // D row of t = 0 in this item
   if (p.skip) {
+    VOC_CHECK(sslot >= smem_lo && sslot + skip_slot_bytes(CW) <= smem_hi, 13, sslot, smem_lo, smem_hi);
     if (!mbar_wait(sfull, sparity, p.timeout, abort_flag)) return false;
-    const int r = quad * 32 + lane;
 #pragma unroll
-    for (int c = 0; c < S::NCH; ++c) {
-      const uint4 x = lds128(S::at(sslot, r, c));
-      v[4 * c] += __uint_as_float(x.x), v[4 * c + 1] += __uint_as_float(x.y);
-      v[4 * c + 2] += __uint_as_float(x.z), v[4 * c + 3] += __uint_as_float(x.w);
+    for (int j = 0; j < CW / 4; ++j) {
+      const uint4 x = lds128(sslot + static_cast<uint32_t>((j * kTileM + row_in_tile) * 16));
+      v[4 * j] += __uint_as_float(x.x), v[4 * j + 1] += __uint_as_float(x.y);
+      v[4 * j + 2] += __uint_as_float(x.z), v[4 * j + 3] += __uint_as_float(x.w);
     }
     mbar_arrive(sempty);
   }
@@ -156,25 +167,20 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
 #pragma unroll
     for (int i = 0; i < CW; ++i) sn[i] = v[i];
   }
+  if (t >= p.L_in) return true;
+  const int ph = n0 / p.Cp_out;  // ConvT phase of these columns (0 for a conv)
+  const int co0 = n0 - ph * p.Cp_out;
+  const size_t L_out = (size_t)p.L_in * p.s_rows;
+  const size_t row = (size_t)t * p.s_rows + ph;
   if (p.out_f32) {
-    const bool snake_out = (p.flags & EPI_F32_SNAKE) != 0;
+    const float *src = (p.flags & EPI_F32_SNAKE) ? sn : v;
+    VOC_CHECK((((long long)b * (p.Cp_out / 4) + co0 / 4 + CW / 4 - 1) * (long long)L_out + row) * 4 + 4 <= p.f32_elems,
+              14, b, co0, row);
+    float *base = p.out_f32 + ((size_t)b * (p.Cp_out / 4) + co0 / 4) * L_out * 4 + row * 4;
 #pragma unroll
-    for (int c = 0; c < S::NCH; ++c) {
-      const float *src = snake_out ? sn : v;
-      sts128(S::at(stf, lane, c),
-             make_uint4(__float_as_uint(src[4 * c]), __float_as_uint(src[4 * c + 1]),
-                        __float_as_uint(src[4 * c + 2]), __float_as_uint(src[4 * c + 3])));
-    }
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < S::NCH; ++i) {
-      const int r = i * S::RPI + lane / S::NCH, c = lane % S::NCH;
-      const int t = t0w + r;
-      const uint4 x = lds128(S::at(stf, r, c));
-      if (t < p.L_in)
-        *reinterpret_cast<uint4 *>(p.out_f32 + (row0 + t) * p.N_total + n0 + 4 * c) = x;
-    }
-    __syncwarp();
+    for (int j = 0; j < CW / 4; ++j)
+      *reinterpret_cast<float4 *>(base + (size_t)j * L_out * 4) =
+          make_float4(src[4 * j], src[4 * j + 1], src[4 * j + 2], src[4 * j + 3]);
   }
   if (p.out_hl) {
     uint32_t hw[CW / 2], lw[CW / 2];
@@ -187,27 +193,18 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
       hw[i] = pack_bf16x2(h0, h1);
       lw[i] = pack_bf16x2(l0, l1);
     }
+    const size_t item = (size_t)b * (2 * p.Cp_out / 8);
+    VOC_CHECK((((long long)item + p.Cp_out / 8 + co0 / 8 + CW / 8 - 1) * (long long)L_out + row) * 8 + 8 <= p.hl_elems,
+              15, b, co0, row);
+    __nv_bfloat16 *hbase = p.out_hl + (item + co0 / 8) * L_out * 8 + row * 8;
+    __nv_bfloat16 *lbase = p.out_hl + (item + p.Cp_out / 8 + co0 / 8) * L_out * 8 + row * 8;
 #pragma unroll
-    for (int c = 0; c < S::NCH / 2; ++c) {
-      sts128(S::at(sth, lane, c), make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]));
-      sts128(S::at(sth, lane, S::NCH / 2 + c),
-             make_uint4(lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]));
+    for (int j = 0; j < CW / 8; ++j) {
+      *reinterpret_cast<uint4 *>(hbase + (size_t)j * L_out * 8) =
+          make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
+      *reinterpret_cast<uint4 *>(lbase + (size_t)j * L_out * 8) =
+          make_uint4(lw[4 * j], lw[4 * j + 1], lw[4 * j + 2], lw[4 * j + 3]);
     }
-    __syncwarp();
-    const int ph = n0 / p.Cp_out;  // ConvT phase of these columns (0 for a conv)
-    const int co0 = n0 - ph * p.Cp_out;
-#pragma unroll
-    for (int i = 0; i < S::NCH; ++i) {
-      const int r = i * S::RPI + lane / S::NCH, c = lane % S::NCH;
-      const int t = t0w + r;
-      const uint4 x = lds128(S::at(sth, r, c));
-      if (t < p.L_in) {
-        const size_t orow = (row0 + t) * p.s_rows + ph;
-        const int col = (c < S::NCH / 2) ? co0 + 8 * c : p.Cp_out + co0 + 8 * (c - S::NCH / 2);
-        *reinterpret_cast<uint4 *>(p.out_hl + orow * (size_t)(2 * p.Cp_out) + col) = x;
-      }
-    }
-    __syncwarp();
   }
   return true;
 }
@@ -231,8 +228,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *smA = smem;
   uint8_t *smB = smA + (size_t)p.na * p.a_bytes;
-  uint8_t *smE = smB + (size_t)p.nb * p.b_bytes;   // epilogue staging
-  uint8_t *smS = smE + epi_stage_bytes(CW);         // residual slots
+  uint8_t *smS = smB + (size_t)p.nb * p.b_bytes;   // residual slots
   uint64_t *bars = reinterpret_cast<uint64_t *>(smS + (size_t)p.ns * skip_slot_bytes(CW));
   uint64_t *fullA = bars;
   uint64_t *emptyA = fullA + p.na;
@@ -249,6 +245,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t tmem_cols = static_cast<uint32_t>(p.n_acc * p.acc_cols);
+#ifdef VOC_CHECKS
+  // the barrier block must end inside the dynamic allocation
+  if (reinterpret_cast<const volatile uint8_t *>(abort_flag + 1) > smem_raw + p.smem_bytes) {
+    if (threadIdx.x == 0 && atomicCAS(p.dbg, 0, 1) == 0) {
+      p.dbg[1] = static_cast<int>(reinterpret_cast<const volatile uint8_t *>(abort_flag + 1) - smem_raw);
+      p.dbg[2] = p.smem_bytes;
+    }
+    return;
+  }
+#endif
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.na; ++i) {
@@ -292,6 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // ------------------------------------------------------------ A / weight producer
       prefetch_tmap(&tmapA);
       const uint32_t a_tx = 2u * kchunks * chunkA;
+      const int lo_chunk0 = p.Cp_in / 8;
       int ia = 0, ib = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
@@ -308,13 +315,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           const uint32_t fa = smem_u32(fullA + sa);
-          mbar_arrive_expect_tx(fa, a_tx);
           const uint32_t dstA = smem_u32(smA + (size_t)sa * p.a_bytes);
-          for (int c = 0; c < kchunks; ++c) {
-            const int x = kb * p.KB + c * 8;
-            tma_load_3d(dstA + c * chunkA, &tmapA, fa, x, y0, b);
-            tma_load_3d(dstA + (kchunks + c) * chunkA, &tmapA, fa, p.Cp_in + x, y0, b);
+#ifdef VOC_CHECKS
+          if (!(dstA + a_tx <= smem_u32(smB) && lo_chunk0 + (kb + 1) * kchunks <= p.chunks_a &&
+                2 * kchunks * chunkA <= (uint32_t)p.a_bytes)) {
+            check_fail(p, abort_flag, 21, dstA, kb, p.chunks_a);
+            ok = false;
+            break;
           }
+#endif
+          mbar_arrive_expect_tx(fa, a_tx);
+          tma_load_4d(dstA, &tmapA, fa, 0, y0, kb * kchunks, b);                 // hi chunks
+          tma_load_4d(dstA + kchunks * chunkA, &tmapA, fa, 0, y0, lo_chunk0 + kb * kchunks, b);
           ++ia;
           for (int tap = 0; tap < p.taps; ++tap) {
             const int sb = ib % p.nb;
@@ -324,8 +336,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               break;
             }
             const uint32_t fb = smem_u32(fullB + sb);
-            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(p.b_bytes));
             const size_t widx = ((size_t)nt * p.taps + tap) * p.nkb + kb;
+#ifdef VOC_CHECKS
+            if (!((long long)(widx + 1) * p.b_bytes <= p.w_bytes &&
+                  smem_u32(smB + (size_t)(sb + 1) * p.b_bytes) <= smem_u32(smS))) {
+              check_fail(p, abort_flag, 22, widx, sb, p.w_bytes);
+              ok = false;
+              break;
+            }
+#endif
+            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(p.b_bytes));
             bulk_load(smem_u32(smB + (size_t)sb * p.b_bytes), p.wB + widx * p.b_bytes,
                       static_cast<uint32_t>(p.b_bytes), fb);
             ++ib;
@@ -343,6 +363,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       const uint32_t idesc = idesc_bf16_f32(kTileM, p.N_tile);
+      // descriptor increments: +1 in the start-address field is +16 bytes
+      const uint64_t dA_lo = (uint64_t)((kchunks * chunkA) >> 4);
+      const uint64_t dA_k = (uint64_t)((2 * chunkA) >> 4);
+      const uint64_t dB_lo = (uint64_t)((kchunks * chunkB) >> 4);
+      const uint64_t dB_k = (uint64_t)((2 * chunkB) >> 4);
       int ia = 0, ib = 0, it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
@@ -373,13 +398,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t bBase = smem_u32(smB + (size_t)sb * p.b_bytes);
-            const uint32_t aTap = aBase + static_cast<uint32_t>(shift0 + tap * p.tap_step) * 16u;
+#ifdef VOC_CHECKS
+            {
+              const int sh = shift0 + tap * p.tap_step;
+              if (!(sh >= 0 && sh + kTileM <= p.rows)) {
+                check_fail(p, abort_flag, 31, sh, tap, p.rows);
+                ok = false;
+                break;
+              }
+            }
+#endif
+            const uint64_t a0 = smem_desc(
+                aBase + static_cast<uint32_t>(shift0 + tap * p.tap_step) * 16u, chunkA, 128);
+            const uint64_t b0 = smem_desc(smem_u32(smB + (size_t)sb * p.b_bytes), chunkB, 128);
             for (int ks = 0; ks < kchunks / 2; ++ks) {
-              const uint64_t a_hi = smem_desc(aTap + (2 * ks) * chunkA, chunkA, 128);
-              const uint64_t a_lo = smem_desc(aTap + (kchunks + 2 * ks) * chunkA, chunkA, 128);
-              const uint64_t b_hi = smem_desc(bBase + (2 * ks) * chunkB, chunkB, 128);
-              const uint64_t b_lo = smem_desc(bBase + (kchunks + 2 * ks) * chunkB, chunkB, 128);
+              const uint64_t a_hi = a0 + ks * dA_k, a_lo = a_hi + dA_lo;
+              const uint64_t b_hi = b0 + ks * dB_k, b_lo = b_hi + dB_lo;
               const uint32_t accum = (kb | tap | ks) ? 1u : 0u;
               mma_bf16(d_tmem, a_hi, b_hi, idesc, accum);
               mma_bf16(d_tmem, a_hi, b_lo, idesc, 1u);
@@ -408,31 +442,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0 && p.skip) {
       // ------------------------------------------------------------ residual prefetch
       prefetch_tmap(&tmapS);
+      // Chunk c of a tile is consumed by the epilogue half c & 1; each half has its own
+      // ring of ns/2 slots filled in that half's consumption order, so a slot is only ever
+      // waited on by one sequence of consumers, at most one fill ahead.
       const uint32_t bytes = static_cast<uint32_t>(skip_slot_bytes(CW));
-      int ks = 0;
+      const int nsh = p.ns / 2;
+      int cnt[2] = {0, 0};
       bool ok = true;
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
         const int nt = tile % p.n_tiles;
         const int rest = tile / p.n_tiles;
         const int mt = rest % p.m_tiles;
         const int b = rest / p.m_tiles;
-        for (int c = 0; c < n_chunks; ++c, ++ks) {
-          const int slot = ks % p.ns;
-          const uint32_t ph = static_cast<uint32_t>(ks / p.ns) & 1u;
+        for (int c = 0; c < n_chunks; ++c) {
+          const int h = c & 1;
+          const int k = cnt[h]++;
+          const int slot = h * nsh + k % nsh;
+          const uint32_t ph = static_cast<uint32_t>(k / nsh) & 1u;
           if (!mbar_wait(smem_u32(skipEmpty + slot), ph ^ 1u, p.timeout, abort_flag)) {
             ok = false;
             break;
           }
           const uint32_t fs = smem_u32(skipFull + slot);
+#ifdef VOC_CHECKS
+          if (!(smem_u32(smS + (size_t)(slot + 1) * bytes) <= smem_u32(bars) &&
+                (nt * p.N_tile + c * CW) / 4 + CW / 4 <= p.chunks_s)) {
+            check_fail(p, abort_flag, 41, slot, nt * p.N_tile + c * CW, p.chunks_s);
+            ok = false;
+            break;
+          }
+#endif
           mbar_arrive_expect_tx(fs, bytes);
-          tma_load_3d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, nt * p.N_tile + c * CW,
-                      mt * kTileM, b);
+          tma_load_4d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, 0, mt * kTileM,
+                      (nt * p.N_tile + c * CW) / 4, b);
         }
       }
       if (!ok) {
         atomicOr(p.err, ERR_TIMEOUT_SKIP);
         *abort_flag = 1;
-        drain_ring(skipFull, p.ns, ks, p.timeout);
+        drain_ring(skipFull, nsh, cnt[0], p.timeout);
+        drain_ring(skipFull + nsh, nsh, cnt[1], p.timeout);
       }
     }
   } else {
@@ -440,10 +489,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int e = warp - 2;     // epilogue warp 0..7
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int half = e / 4;     // the two warps of a quadrant take alternate column chunks
-    const uint32_t stf = smem_u32(smE) + static_cast<uint32_t>(e * 2 * 32 * CW * 4);
-    const uint32_t sth = stf + 32 * CW * 4;
+    const int row_in_tile = quad * 32 + lane;
     const uint32_t sbase = smem_u32(smS);
-    const int ns = p.ns > 0 ? p.ns : 1;
+    const int nsh = p.ns > 0 ? p.ns / 2 : 1;  // residual slots of this half's ring
+    int kh = 0;                              // residual chunks this half has consumed
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
@@ -458,17 +507,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      const int t0w = mt * kTileM + quad * 32;
+      const int t = mt * kTileM + row_in_tile;
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * p.acc_cols) +
                              (static_cast<uint32_t>(quad * 32) << 16);
-      for (int c = half; c < n_chunks && ok; c += 2) {
-        const int kc = it * n_chunks + c;  // residual chunk counter (fill order of the slots)
-        const int slot = kc % ns;
-        ok = epilogue_chunk<CW>(
-            p, stf, sth, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
-            smem_u32(skipFull + slot), smem_u32(skipEmpty + slot),
-            static_cast<uint32_t>(kc / ns) & 1u, abort_flag, lane, quad, b, t0w,
-            nt * p.N_tile + c * CW, tbase + c * CW);
+      for (int c = half; c < n_chunks && ok; c += 2, ++kh) {
+        const int slot = half * nsh + kh % nsh;
+        ok = epilogue_chunk<CW>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
+                                smem_u32(skipFull + slot), smem_u32(skipEmpty + slot),
+                                static_cast<uint32_t>(kh / nsh) & 1u, abort_flag, row_in_tile, b,
+                                t, nt * p.N_tile + c * CW, tbase + c * CW, sbase,
+                                smem_u32(bars));
       }
       if (!ok) break;
       tc_fence_before();

@@ -64,6 +64,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
       "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// 4-D tiled tensor load into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint32_t bar, int x,
+                                            int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
 // Plain bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar) {

@@ -1,9 +1,9 @@
 // stream_kernels.cuh -- the bandwidth-bound kernels around the tensor-core convs:
-//   prep_hl_kernel      channels-first fp32 -> channels-last bf16 hi/lo rows (+ optional Snake)
-//   out_head_kernel     Snake'd fp32 rows -> k-tap conv to one channel (+bias) -> tanh
+//   prep_hl_kernel      channels-first fp32 -> chunk-major bf16 hi/lo (+ optional Snake)
+//   out_head_kernel     Snake'd chunk-major fp32 -> k-tap conv to one channel (+bias) -> tanh
 //   stitch_kernel       overlap-crop stitch + clamp of windowed decodes
 //   finite_check_kernel flags a NaN / Inf in a buffer
-//   rows_to_cf_kernel   channels-last fp32 rows -> channels-first fp32 (single-layer ops)
+//   rows_to_cf_kernel   chunk-major fp32 -> channels-first fp32 (single-layer ops)
 #pragma once
 #include <cuda_bf16.h>
 
@@ -13,43 +13,49 @@
 
 namespace voc {
 
-// x [B][C][T] fp32 -> hl [B][T][2*Cp] bf16 (per row: Cp hi values, then Cp lo values);
-// channels C..Cp-1 are written as zeros.  alpha == nullptr: no Snake.
-// Block (32, 8), grid (ceil(T/32), ceil(Cp/32), B).
+// x [B][C][T] fp32 -> hl chunk-major [B][2*Cp/8][T][8] bf16: 8-channel chunks of the
+// hi parts, then of the lo parts (hi = bf16(v), lo = bf16(v - hi)); channels C..Cp-1
+// are zeros.  alpha == nullptr: no Snake.  One thread per (b, chunk, t):
+// block 256, grid (ceil(T/256), Cp/8, B).
 __global__ void prep_hl_kernel(const float *__restrict__ x, int C, int T, int Cp,
                                const float *__restrict__ alpha, const float *__restrict__ invb,
                                __nv_bfloat16 *__restrict__ hl) {
-  __shared__ float tile[32][33];
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int c8 = blockIdx.y;
   const int b = blockIdx.z;
-  const int t0 = blockIdx.x * 32;
-  const int c0 = blockIdx.y * 32;
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int c = c0 + i, t = t0 + threadIdx.x;
-    float v = 0.f;
-    if (c < C && t < T) {
-      v = x[((size_t)b * C + c) * T + t];
-      if (alpha) v = snake(v, alpha[c], invb[c]);
+  if (t >= T) return;
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    float v[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int c = c8 * 8 + e + u;
+      v[u] = 0.f;
+      if (c < C) {
+        v[u] = x[((size_t)b * C + c) * T + t];
+        if (alpha) v[u] = snake(v[u], alpha[c], invb[c]);
+      }
     }
-    tile[i][threadIdx.x] = v;
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(v[0]), h1 = __float2bfloat16_rn(v[1]);
+    const __nv_bfloat16 l0 = __float2bfloat16_rn(v[0] - __bfloat162float(h0));
+    const __nv_bfloat16 l1 = __float2bfloat16_rn(v[1] - __bfloat162float(h1));
+    hw[e / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+    lw[e / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
+                (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
   }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int t = t0 + i, c = c0 + threadIdx.x;
-    if (t < T && c < Cp) {
-      const float v = tile[threadIdx.x][i];
-      const __nv_bfloat16 h = __float2bfloat16_rn(v);
-      const __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
-      __nv_bfloat16 *row = hl + ((size_t)b * T + t) * (size_t)(2 * Cp);
-      row[c] = h;
-      row[Cp + c] = l;
-    }
-  }
+  const size_t item = (size_t)b * (2 * Cp / 8);
+  *reinterpret_cast<uint4 *>(hl + ((item + c8) * T + t) * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4 *>(hl + ((item + Cp / 8 + c8) * T + t) * 8) =
+      make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
-// audio[b][t] = tanh(bias + sum_k sum_c w[c][k] * y[b][t + k - pad_left][c]), y zero outside
-// [0, L).  y rows are Cp floats (already Snake'd), w [Cp][K] (zero past the real channels).
-// One thread per output sample, TILE samples per block, rows staged in shared memory with a
-// padded stride (Cp + 4 floats) so that float4 reads of consecutive rows hit distinct banks.
+// audio[b][t] = tanh(bias + sum_k sum_c w[c][k] * y[b][c][t + k - pad_left]), y zero outside
+// [0, L).  y is fp32 chunk-major [B][Cp/4][L][4] (already Snake'd), w [Cp][K] (zero past the
+// real channels).  One thread per output sample, TILE samples per block; the block stages
+// its rows chunk by chunk in shared memory ([Cp/4][TILE+K-1][4]), so the global reads are
+// contiguous runs and a warp's shared reads hit consecutive 16-byte words.
 template <int TILE>
 __global__ void __launch_bounds__(TILE) out_head_kernel(const float *__restrict__ y, int L, int Cp,
                                                         int K, int pad_left,
@@ -57,35 +63,30 @@ __global__ void __launch_bounds__(TILE) out_head_kernel(const float *__restrict_
                                                         const float *__restrict__ bias,
                                                         float *__restrict__ audio) {
   extern __shared__ float4 sm4[];
-  float *sm = reinterpret_cast<float *>(sm4);
   const int b = blockIdx.y;
   const int t0 = blockIdx.x * TILE;
   const int rows = TILE + K - 1;
-  const int ld = Cp + 4;
-  float *xs = sm;
-  float *ws = sm + (size_t)rows * ld;
+  const int nch = Cp / 4;
+  float4 *xs = sm4;                                            // [nch][rows]
+  float *ws = reinterpret_cast<float *>(sm4 + (size_t)nch * rows);  // [Cp][K]
   for (int i = threadIdx.x; i < Cp * K; i += TILE) ws[i] = w[i];
-  const int nvec = Cp / 4;
-  for (int i = threadIdx.x; i < rows * nvec; i += TILE) {
-    const int r = i / nvec, c4 = i - r * nvec;
+  const float4 *yb = reinterpret_cast<const float4 *>(y) + (size_t)b * nch * L;
+  for (int i = threadIdx.x; i < nch * rows; i += TILE) {
+    const int j = i / rows, r = i - j * rows;
     const int t = t0 - pad_left + r;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t >= 0 && t < L)
-      v = __ldg(reinterpret_cast<const float4 *>(y + ((size_t)b * L + t) * Cp) + c4);
-    *reinterpret_cast<float4 *>(xs + (size_t)r * ld + 4 * c4) = v;
+    xs[i] = (t >= 0 && t < L) ? __ldg(yb + (size_t)j * L + t) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
   const int t = t0 + threadIdx.x;
   if (t >= L) return;
   float acc = 0.f;
   for (int k = 0; k < K; ++k) {
-    const float *xr = xs + (size_t)(threadIdx.x + k) * ld;
-    for (int c4 = 0; c4 < nvec; ++c4) {
-      const float4 xv = *reinterpret_cast<const float4 *>(xr + 4 * c4);
-      acc = fmaf(ws[(4 * c4 + 0) * K + k], xv.x, acc);
-      acc = fmaf(ws[(4 * c4 + 1) * K + k], xv.y, acc);
-      acc = fmaf(ws[(4 * c4 + 2) * K + k], xv.z, acc);
-      acc = fmaf(ws[(4 * c4 + 3) * K + k], xv.w, acc);
+    for (int j = 0; j < nch; ++j) {
+      const float4 xv = xs[(size_t)j * rows + threadIdx.x + k];
+      acc = fmaf(ws[(4 * j + 0) * K + k], xv.x, acc);
+      acc = fmaf(ws[(4 * j + 1) * K + k], xv.y, acc);
+      acc = fmaf(ws[(4 * j + 2) * K + k], xv.z, acc);
+      acc = fmaf(ws[(4 * j + 3) * K + k], xv.w, acc);
     }
   }
   audio[(size_t)b * L + t] = tanhf(bias[0] + acc);
@@ -122,22 +123,20 @@ __global__ void finite_check_kernel(const float *__restrict__ x, long long n, in
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
 }
 
-// rows [B][L][ld] fp32 (first C columns used) -> cf [B][C][L].  Block (32, 8),
-// grid (ceil(L/32), ceil(C/32), B).
-__global__ void rows_to_cf_kernel(const float *__restrict__ rows, int L, int ld, int C,
+// fp32 chunk-major [B][Cp/4][L][4] -> channels-first [B][C][L] (first C channels).
+// One thread per (b, 4-channel chunk, t): block 256, grid (ceil(L/256), Cp/4, B).
+__global__ void rows_to_cf_kernel(const float *__restrict__ src, int L, int Cp, int C,
                                   float *__restrict__ cf) {
-  __shared__ float tile[32][33];
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int j = blockIdx.y;
   const int b = blockIdx.z;
-  const int t0 = blockIdx.x * 32;
-  const int c0 = blockIdx.y * 32;
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int t = t0 + i, c = c0 + threadIdx.x;
-    tile[i][threadIdx.x] = (t < L && c < C) ? rows[((size_t)b * L + t) * ld + c] : 0.f;
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int c = c0 + i, t = t0 + threadIdx.x;
-    if (c < C && t < L) cf[((size_t)b * C + c) * L + t] = tile[threadIdx.x][i];
+  if (t >= L) return;
+  const float4 v = reinterpret_cast<const float4 *>(src)[((size_t)b * (Cp / 4) + j) * L + t];
+  const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = 4 * j + u;
+    if (c < C) cf[((size_t)b * C + c) * L + t] = e[u];
   }
 }
 

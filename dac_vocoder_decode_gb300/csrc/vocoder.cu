@@ -27,6 +27,8 @@ using voc::ConvGemmArgs;
 constexpr int kSmemMax = 227 * 1024;         // opt-in shared memory per block
 constexpr long long kWaitBudget = 4000000000LL;  // cycles (~2 s) before a wait gives up
 constexpr int kHeadTile = 128;
+// mbarriers (2 per A, weight and residual slot, 2 per accumulator, 1 drain), TMEM slot, flag
+constexpr int kBarrierBytes = 512;
 
 thread_local std::string g_err;  // last error without a context
 
@@ -149,8 +151,6 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   L.Cp_out = rup(L.Cout, 16);
   g.Cp_in = L.Cp_in;
   g.Cp_out = L.Cp_out;
-  g.KB = (L.Cp_in % 32 == 0) ? 32 : 16;
-  g.nkb = L.Cp_in / g.KB;
   int group, off_min, off_max;
   if (L.convT) {
     const int s = L.stride;
@@ -198,18 +198,24 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     return false;
   }
   L.cw = (g.N_tile % 32 == 0 && L.Cp_out % 32 == 0) ? 32 : 16;
-  const int epi = voc::epi_stage_bytes(L.cw);
+  // channels per k-block: the largest multiple of 16 dividing Cp_in that keeps a weight
+  // stage within 36 KB and an A stage within 72 KB (fewer, longer pipeline stages)
+  g.KB = 16;
+  for (int kb = 16; kb <= L.Cp_in; kb += 16)
+    if (L.Cp_in % kb == 0 && 4 * kb * g.N_tile <= 36 * 1024 && 4 * kb * g.rows <= 72 * 1024)
+      g.KB = kb;
+  g.nkb = L.Cp_in / g.KB;
   const int chunkA = g.rows * 16;
   g.a_bytes = rup(2 * (g.KB / 8) * chunkA, 1024);
   g.b_bytes = 4 * g.KB * g.N_tile;
   g.na = 2;
   // residual slots (layers with a skip input): as many as leave >= 3 weight stages, 2..4
   g.ns = 0;
-  int avail = kSmemMax - 1024 - 256 - g.na * g.a_bytes - epi;
-  if (has_skip) {
+  int avail = kSmemMax - 1024 - kBarrierBytes - g.na * g.a_bytes;
+  if (has_skip) {  // two rings (one per epilogue half) of 1 or 2 slots each
     const int sb = voc::skip_slot_bytes(L.cw);
     g.ns = 4;
-    while (g.ns > 2 && (avail - g.ns * sb) / g.b_bytes < 3) --g.ns;
+    if ((avail - g.ns * sb) / g.b_bytes < 3) g.ns = 2;
     avail -= g.ns * sb;
   }
   g.nb = std::min(8, avail / g.b_bytes);
@@ -221,8 +227,8 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   while (ac < g.N_tile) ac *= 2;
   g.acc_cols = ac;
   g.n_acc = std::min(voc::kMaxAcc, 512 / ac);
-  L.smem = 1024 + (size_t)g.na * g.a_bytes + (size_t)g.nb * g.b_bytes + epi +
-           (size_t)g.ns * voc::skip_slot_bytes(L.cw) + 256;
+  L.smem = 1024 + (size_t)g.na * g.a_bytes + (size_t)g.nb * g.b_bytes +
+           (size_t)g.ns * voc::skip_slot_bytes(L.cw) + kBarrierBytes;
   return true;
 }
 
@@ -365,43 +371,44 @@ size_t buf_bytes(const vocoder *ctx, int B, int T) {
   return rupz(m * 4, 256);
 }
 
+// A operand: bf16 hi/lo chunk-major [B][2*Cp/8][L][8], read in boxes of 8 channels x
+// `rows` time rows x `kchunks` chunks (zero fill outside [0, L)).
 voc_status encode_map(vocoder *ctx, CUtensorMap *map, const void *base, int Cp, long long L, int B,
-                      int rows) {
+                      int rows, int kchunks) {
   auto enc = encode_fn();
   if (!enc) return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled entry point unavailable");
-  const cuuint64_t dims[3] = {(cuuint64_t)(2 * Cp), (cuuint64_t)L, (cuuint64_t)B};
-  const cuuint64_t strides[2] = {(cuuint64_t)(4 * Cp), (cuuint64_t)(4 * Cp) * (cuuint64_t)L};
-  const cuuint32_t box[3] = {8u, (cuuint32_t)rows, 1u};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+  const cuuint64_t dims[4] = {8u, (cuuint64_t)L, (cuuint64_t)(2 * Cp / 8), (cuuint64_t)B};
+  const cuuint64_t strides[3] = {16u, 16u * (cuuint64_t)L, 16u * (cuuint64_t)L * (2 * Cp / 8)};
+  const cuuint32_t box[4] = {8u, (cuuint32_t)rows, (cuuint32_t)kchunks, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
   return VOC_OK;
 }
 
-// Residual (skip) input of an epilogue: fp32 rows [B][L][N_total], read in boxes of
-// 128 rows x cw columns with the swizzle the epilogue's shared reads expect.
-voc_status encode_skip_map(vocoder *ctx, CUtensorMap *map, const void *base, int N_total,
-                           long long L, int B, int cw) {
+// Residual (skip) input of an epilogue: fp32 chunk-major [B][Cp/4][L][4], read in boxes of
+// 4 channels x 128 rows x cw/4 chunks.
+voc_status encode_skip_map(vocoder *ctx, CUtensorMap *map, const void *base, int Cp, long long L,
+                           int B, int cw) {
   auto enc = encode_fn();
   if (!enc) return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled entry point unavailable");
-  const cuuint64_t dims[3] = {(cuuint64_t)N_total, (cuuint64_t)L, (cuuint64_t)B};
-  const cuuint64_t strides[2] = {(cuuint64_t)(4 * N_total), (cuuint64_t)(4 * N_total) * (cuuint64_t)L};
-  const cuuint32_t box[3] = {(cuuint32_t)cw, (cuuint32_t)voc::kTileM, 1u};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   cw == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const cuuint64_t dims[4] = {4u, (cuuint64_t)L, (cuuint64_t)(Cp / 4), (cuuint64_t)B};
+  const cuuint64_t strides[3] = {16u, 16u * (cuuint64_t)L, 16u * (cuuint64_t)L * (Cp / 4)};
+  const cuuint32_t box[4] = {4u, (cuuint32_t)voc::kTileM, (cuuint32_t)(cw / 4), 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled (residual) failed (" + std::to_string((int)r) + ")");
   return VOC_OK;
 }
 
 void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *const *bufs,
-                      ConvGemmArgs &a) {
+                      size_t bbytes, ConvGemmArgs &a) {
   a = L.g;
   const long long L_in = level_len(ctx, L.level, T);
   a.B = B;
@@ -417,7 +424,32 @@ void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *co
   a.flags = L.epi_flags;
   a.timeout = ctx->wait_budget;
   a.err = ctx->err_dev;
+  a.f32_elems = L.f32_buf >= 0 ? (long long)(bbytes / 4) : 0;
+  a.hl_elems = L.hl_buf >= 0 ? (long long)(bbytes / 2) : 0;
+  a.w_bytes = (long long)L.g.n_tiles * L.g.taps * L.g.nkb * L.g.b_bytes;
+  a.smem_bytes = static_cast<int>(L.smem);
+  a.L_a = static_cast<int>(L_in);
+  a.chunks_a = 2 * L.Cp_in / 8;
+  a.chunks_s = L.Cp_out / 4;
+  a.dbg = ctx->err_dev + 4;
 }
+
+#ifdef VOC_CHECKS
+// Self-checking build: wait for every launch and report the first failed check.
+voc_status check_launch(vocoder *ctx, const std::string &name, cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, ("after " + name).c_str());
+  int w[8] = {0};
+  cudaMemcpy(w, ctx->err_dev, sizeof(w), cudaMemcpyDeviceToHost);
+  if (w[0] || w[4]) {
+    char buf[256];
+    snprintf(buf, sizeof buf, "%s: error word %d, check %d (%d, %d, %d)", name.c_str(), w[0], w[4],
+             w[5], w[6], w[7]);
+    return fail(ctx, VOC_DEVICE_TIMEOUT, buf);
+  }
+  return VOC_OK;
+}
+#endif
 
 void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops, double &bytes) {
   const double L_in = (double)level_len(ctx, L.level, T);
@@ -447,7 +479,7 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
 
 voc_status launch_out_head(vocoder *ctx, const OutHead &h, const float *y, int B, long long L,
                            float *audio, cudaStream_t stream) {
-  const size_t smem = ((size_t)(kHeadTile + h.K - 1) * (h.Cp + 4) + (size_t)h.Cp * h.K) * 4;
+  const size_t smem = ((size_t)(kHeadTile + h.K - 1) * h.Cp + (size_t)h.Cp * h.K) * 4;
   dim3 grid(static_cast<unsigned>((L + kHeadTile - 1) / kHeadTile), static_cast<unsigned>(B));
   voc::out_head_kernel<kHeadTile><<<grid, kHeadTile, smem, stream>>>(
       y, static_cast<int>(L), h.Cp, h.K, h.pad_left, h.w_dev, h.b_dev, audio);
@@ -458,8 +490,8 @@ voc_status launch_out_head(vocoder *ctx, const OutHead &h, const float *y, int B
 
 voc_status launch_prep(vocoder *ctx, const float *x, int B, int C, int T, int Cp, const float *alpha,
                        const float *invb, __nv_bfloat16 *hl, cudaStream_t stream) {
-  dim3 grid((T + 31) / 32, (Cp + 31) / 32, B);
-  voc::prep_hl_kernel<<<grid, dim3(32, 8), 0, stream>>>(x, C, T, Cp, alpha, invb, hl);
+  dim3 grid((T + 255) / 256, Cp / 8, B);
+  voc::prep_hl_kernel<<<grid, 256, 0, stream>>>(x, C, T, Cp, alpha, invb, hl);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch prep");
   return VOC_OK;
@@ -594,11 +626,11 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
   cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
   if (cc_major != 10 || cc_minor != 3)
     return bail(fail(ctx, VOC_UNSUPPORTED, "this build targets sm_103 (GB300) only"));
-  e = cudaMalloc(&ctx->err_dev, 2 * sizeof(int));
+  e = cudaMalloc(&ctx->err_dev, 8 * sizeof(int));  // [0] error word, [1] finite flag, [4..7] checks
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaMalloc"));
   ctx->allocs.push_back(ctx->err_dev);
   ctx->flag_dev = ctx->err_dev + 1;
-  cudaMemset(ctx->err_dev, 0, 2 * sizeof(int));
+  cudaMemset(ctx->err_dev, 0, 8 * sizeof(int));
 
   const int pad = desc->padding;
   const int nd = desc->n_dilations;
@@ -735,9 +767,9 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
     for (size_t i = 0; i < ctx->layers.size(); ++i) {
       const Layer &L = ctx->layers[i];
       voc_status st = encode_map(ctx, &ctx->maps[i], bufs[L.in_buf], L.Cp_in,
-                                 level_len(ctx, L.level, T), B, L.g.rows);
+                                 level_len(ctx, L.level, T), B, L.g.rows, L.g.KB / 8);
       if (st == VOC_OK && L.skip_buf >= 0)
-        st = encode_skip_map(ctx, &ctx->skip_maps[i], bufs[L.skip_buf], L.g.N_total,
+        st = encode_skip_map(ctx, &ctx->skip_maps[i], bufs[L.skip_buf], L.Cp_out,
                              level_len(ctx, L.level, T), B, L.cw);
       if (st != VOC_OK) {
         ctx->map_ws = nullptr;
@@ -773,6 +805,9 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
   st = launch_prep(ctx, latent, B, ctx->desc.latent_channels, T, ctx->Cp_lat, nullptr, nullptr,
                    static_cast<__nv_bfloat16 *>(bufs[BUF_H0]), stream);
   if (st != VOC_OK) return st;
+#ifdef VOC_CHECKS
+  if ((st = check_launch(ctx, "prep_latent", stream)) != VOC_OK) return st;
+#endif
   rec(1);
   if (prof) {
     ctx->prof_names[li] = "prep_latent";
@@ -782,10 +817,13 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
   for (size_t i = 0; i < ctx->layers.size(); ++i, ++li) {
     const Layer &L = ctx->layers[i];
     ConvGemmArgs a;
-    gemm_launch_args(ctx, L, B, T, bufs, a);
+    gemm_launch_args(ctx, L, B, T, bufs, bb, a);
     rec(0);
     st = launch_gemm(ctx, L, ctx->maps[i], ctx->skip_maps[i], a, stream);
     if (st != VOC_OK) return st;
+#ifdef VOC_CHECKS
+    if ((st = check_launch(ctx, L.name, stream)) != VOC_OK) return st;
+#endif
     rec(1);
     if (prof) {
       ctx->prof_names[li] = L.name;
@@ -797,6 +835,9 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
   st = launch_out_head(ctx, ctx->head, static_cast<const float *>(bufs[BUF_FY]), B, Lf, audio,
                        stream);
   if (st != VOC_OK) return st;
+#ifdef VOC_CHECKS
+  if ((st = check_launch(ctx, "out_head", stream)) != VOC_OK) return st;
+#endif
   rec(1);
   if (prof) {
     ctx->prof_names[li] = "out_head";
@@ -970,10 +1011,7 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
   };
   voc_status st = upload_layer(&tmp, tmp.allocs, L, padding, w_host, b_host, nullptr);
   if (st != VOC_OK) return done(st);
-  cudaError_t e = cudaMalloc(&tmp.err_dev, sizeof(int));
-  if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
-  tmp.allocs.push_back(tmp.err_dev);
-  cudaMemsetAsync(tmp.err_dev, 0, sizeof(int), stream);
+  cudaError_t e;
   float *alpha_d = nullptr, *invb_d = nullptr;
   if (alpha_host) {
     std::vector<float> a(alpha_host, alpha_host + L.Cin), ib(L.Cin);
@@ -993,17 +1031,21 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
                         static_cast<__nv_bfloat16 *>(hl), stream)) != VOC_OK)
     return done(st);
   CUtensorMap map;
-  if ((st = encode_map(&tmp, &map, hl, L.Cp_in, T, B, L.g.rows)) != VOC_OK) return done(st);
+  if ((st = encode_map(&tmp, &map, hl, L.Cp_in, T, B, L.g.rows, L.g.KB / 8)) != VOC_OK) return done(st);
   void *bufs[BUF_COUNT] = {hl, nullptr, nullptr, rows};
   L.level = 0;
   L.in_buf = 0, L.f32_buf = BUF_FY;
   ConvGemmArgs a;
-  gemm_launch_args(&tmp, L, B, T, bufs, a);
+  e = cudaMalloc(&tmp.err_dev, 8 * sizeof(int));
+  if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
+  tmp.allocs.push_back(tmp.err_dev);
+  cudaMemsetAsync(tmp.err_dev, 0, 8 * sizeof(int), stream);
+  gemm_launch_args(&tmp, L, B, T, bufs, (size_t)B * T * s * L.Cp_out * 4, a);
   const CUtensorMap no_skip{};
   if ((st = launch_gemm(&tmp, L, map, no_skip, a, stream)) != VOC_OK) return done(st);
-  dim3 grid((T * s + 31) / 32, (L.Cout + 31) / 32, B);
-  voc::rows_to_cf_kernel<<<grid, dim3(32, 8), 0, stream>>>(static_cast<const float *>(rows), T * s,
-                                                           L.Cp_out, L.Cout, y_dev);
+  dim3 grid((T * s + 255) / 256, L.Cp_out / 4, B);
+  voc::rows_to_cf_kernel<<<grid, 256, 0, stream>>>(static_cast<const float *>(rows), T * s,
+                                                   L.Cp_out, L.Cout, y_dev);
   e = cudaGetLastError();
   if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "launch rows_to_cf"));
   e = cudaStreamSynchronize(stream);
