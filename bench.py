@@ -40,6 +40,40 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_FLUSH_BYTES = 256 << 20
 
 
+def source_hash() -> str:
+    """Hash of the CUDA sources and the C header: identifies the kernels a profile was taken on."""
+    import glob
+    import hashlib
+    h = hashlib.sha1()
+    files = sorted(glob.glob(os.path.join(ROOT, "dac_vocoder_decode_gb300", "csrc", "*.cu*")) +
+                   glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, layer: str):
+    """DRAM bytes (read + write) of one launch of `layer`, from the ncu summary committed
+    under profiles/, or None when there is none or it was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        text = f.read()
+    if f"source hash: {source_hash()}" not in text:
+        return None
+    for ln in text.splitlines():
+        cells = [c.strip() for c in ln.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == layer:
+            try:
+                return int(cells[3])
+            except ValueError:
+                return None
+    return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -120,6 +154,19 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(value: float, device="cpu") -> float:
+    """Largest value over all ranks of the default process group (the step time that
+    the slowest replica needed); the value itself when there is no group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 # ----------------------------------------------------------------------------- CPU legs
@@ -233,11 +280,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     clk = clocks.stop()
     ms = statistics.mean(step_ms)
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dev)
     total_samples = B * T * hop * world
     value = total_samples / (ms_max / 1e3)
 
@@ -252,11 +295,7 @@ def run_ours(args, rank, world, local_rank):
         t0 = time.perf_counter()
         V.vocoder_decode_host(voc.handle, lat_h, aud_h, ws_h, stream)
         e2e_s.append(time.perf_counter() - t0)
-    e2e_t = statistics.mean(e2e_s)
-    if world > 1:
-        t = torch.tensor([e2e_t], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_t = float(t.item())
+    e2e_t = max_over_ranks(statistics.mean(e2e_s), dev)
 
     # per-kernel roofline: bf16x3 issues three bf16 MMAs per useful multiply-add
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -275,16 +314,17 @@ def run_ours(args, rank, world, local_rank):
                            gbs=round(gbs, 1), ai=round(ai, 1), bound=bound, frac=round(frac, 3)))
     dom = max(stages, key=lambda s: s["ms"])
     dom_rec = next(per_kernel[i] for i in per_kernel if per_kernel[i]["name"] == dom["name"])
+    traffic = measured_traffic(args.workload, dom["name"])
     if dom["bound"] == "tensor":
         roof = {"bound": "tensor", "kernel": dom["name"], "achieved": dom["tflops"],
                 "peak": round(tc_peak, 1), "unit": "TFLOP/s", "frac": dom["frac"],
-                "traffic": None,
+                "traffic": traffic,
                 "per_launch": {"flops": dom_rec["flops"], "bytes": dom_rec["bytes"],
                                "avg_ms": dom["ms"]},
                 "peak_note": f"bf16 dense {peaks_kind} burst / 3 (three bf16 MMAs per useful MAC)"}
     else:
         roof = {"bound": "hbm", "kernel": dom["name"], "achieved": dom["gbs"], "peak": hbm,
-                "unit": "GB/s", "frac": dom["frac"], "traffic": None,
+                "unit": "GB/s", "frac": dom["frac"], "traffic": traffic,
                 "per_launch": {"flops": dom_rec["flops"], "bytes": dom_rec["bytes"],
                                "avg_ms": dom["ms"]},
                 "peak_note": f"HBM copy bandwidth ({peaks_kind})"}
@@ -321,9 +361,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="music_window", choices=sorted(W.WORKLOADS))
-    ap.add_argument("--cpu-frames", type=int, default=160,
-                    help="latent frames of one item the CPU baseline decodes")
-    ap.add_argument("--ref-frames", type=int, default=24,
+    ap.add_argument("--cpu-frames", type=int, default=689,
+                    help="latent frames of one item the CPU baseline decodes (about 10 s on 16 cores)")
+    ap.add_argument("--ref-frames", type=int, default=48,
                     help="latent frames of one item per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
