@@ -15,7 +15,7 @@ import numpy as np
 
 from . import build as _build
 
-VOC_ABI_VERSION = 1
+VOC_ABI_VERSION = 2
 VOC_OK = 0
 VOC_INVALID_ARG = -1
 VOC_UNSUPPORTED = -2
@@ -42,7 +42,8 @@ EXPORTED = [
     "vocoder_workspace_bytes_host", "vocoder_decode", "vocoder_decode_host",
     "vocoder_decode_static",
     "vocoder_stitched_length", "vocoder_stitch", "vocoder_op_conv1d",
-    "vocoder_op_conv_transpose1d", "vocoder_launches_per_decode", "vocoder_profile_count",
+    "vocoder_op_conv_transpose1d", "vocoder_op_residual_unit", "vocoder_launches_per_decode",
+    "vocoder_profile_count",
     "vocoder_profile_entry", "vocoder_last_error", "vocoder_destroy",
 ]
 
@@ -60,7 +61,8 @@ class VocDesc(ctypes.Structure):
                 ("widths", ctypes.POINTER(ctypes.c_int)), ("n_dilations", ctypes.c_int),
                 ("dilations", ctypes.POINTER(ctypes.c_int)), ("res_kernel", ctypes.c_int),
                 ("out_kernel", ctypes.c_int), ("out_channels", ctypes.c_int),
-                ("padding", ctypes.c_int), ("precision", ctypes.c_int)]
+                ("padding", ctypes.c_int), ("precision", ctypes.c_int),
+                ("fuse_max_channels", ctypes.c_int)]
 
 
 _lib = None
@@ -115,6 +117,8 @@ def load_library():
     lib.vocoder_op_conv1d.argtypes = [P, I, I, I, F, F, I, I, I, I, F, P, P]
     lib.vocoder_op_conv_transpose1d.restype = I
     lib.vocoder_op_conv_transpose1d.argtypes = [P, I, I, I, F, F, I, I, I, F, P, P]
+    lib.vocoder_op_residual_unit.restype = I
+    lib.vocoder_op_residual_unit.argtypes = [P, I, I, I, F, F, F, I, I, F, F, F, I, P, P]
     lib.vocoder_launches_per_decode.restype = I
     lib.vocoder_launches_per_decode.argtypes = [P, I, I]
     lib.vocoder_profile_count.restype = I
@@ -153,14 +157,14 @@ def _stream_ptr(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(int(stream))
 
 
-def make_desc(arch) -> VocDesc:
+def make_desc(arch, fuse_max_channels: int = 0) -> VocDesc:
     """voc_desc for an Arch (layer shapes from workloads.Arch or any object with the same fields)."""
     strides = (ctypes.c_int * len(arch.strides))(*arch.strides)
     widths = (ctypes.c_int * len(arch.widths))(*arch.widths)
     dils = (ctypes.c_int * len(arch.dilations))(*arch.dilations)
     d = VocDesc(VOC_ABI_VERSION, arch.latent_channels, arch.in_kernel, arch.channels0,
                 len(arch.strides), strides, widths, len(arch.dilations), dils, arch.res_kernel,
-                arch.out_kernel, 1, arch.padding, VOC_PREC_BF16X3)
+                arch.out_kernel, 1, arch.padding, VOC_PREC_BF16X3, fuse_max_channels)
     d._keep = (strides, widths, dils)
     return d
 
@@ -192,13 +196,15 @@ def vocoder_fold_weight_norm(g: np.ndarray, v: np.ndarray) -> np.ndarray:
     return w
 
 
-def vocoder_create(arch, params: Sequence[Optional[np.ndarray]]) -> ctypes.c_void_p:
+def vocoder_create(arch, params: Sequence[Optional[np.ndarray]],
+                   fuse_max_channels: int = 0) -> ctypes.c_void_p:
     """params: folded fp32 arrays in the canonical order (None for a zero bias)."""
     lib = load_library()
     keep = [None if p is None else np.ascontiguousarray(p, dtype=np.float32) for p in params]
     arr = (ctypes.POINTER(ctypes.c_float) * len(keep))(*[_fptr(p) for p in keep])
     h = ctypes.c_void_p()
-    _check(lib.vocoder_create(ctypes.byref(make_desc(arch)), arr, len(keep), ctypes.byref(h)))
+    _check(lib.vocoder_create(ctypes.byref(make_desc(arch, fuse_max_channels)), arr, len(keep),
+                              ctypes.byref(h)))
     return h
 
 
@@ -291,6 +297,20 @@ def vocoder_op_conv_transpose1d(x, w: np.ndarray, b: Optional[np.ndarray], strid
         _fptr(alpha), ctypes.c_void_p(y.data_ptr()), _stream_ptr(stream)))
 
 
+def vocoder_op_residual_unit(x, alpha1: np.ndarray, w1: np.ndarray, b1: Optional[np.ndarray],
+                             dil: int, alpha2: np.ndarray, w2: np.ndarray,
+                             b2: Optional[np.ndarray], padding: int, y, stream=None) -> None:
+    """y = x + conv2(Snake2(conv1(Snake1(x)) + b1)) + b2 on the decoder's kernels."""
+    B, C, T = x.shape
+    K = w1.shape[2]
+    arrs = [np.ascontiguousarray(a, dtype=np.float32) if a is not None else None
+            for a in (alpha1, w1, b1, alpha2, w2, b2)]
+    _check(load_library().vocoder_op_residual_unit(
+        ctypes.c_void_p(x.data_ptr()), B, C, T, _fptr(arrs[0]), _fptr(arrs[1]), _fptr(arrs[2]),
+        K, dil, _fptr(arrs[3]), _fptr(arrs[4]), _fptr(arrs[5]), padding,
+        ctypes.c_void_p(y.data_ptr()), _stream_ptr(stream)))
+
+
 def vocoder_profile(h) -> List[dict]:
     """Per-kernel records of the last decode run with VOC_FLAG_PROFILE."""
     lib = load_library()
@@ -326,9 +346,9 @@ def fold_params(params) -> list:
 class Vocoder:
     """A decoder on the current CUDA device (owns its library context)."""
 
-    def __init__(self, arch, folded_params):
+    def __init__(self, arch, folded_params, fuse_max_channels: int = 0):
         self.arch = arch
-        self.handle = vocoder_create(arch, folded_params)
+        self.handle = vocoder_create(arch, folded_params, fuse_max_channels)
         self.hop = vocoder_hop(self.handle)
 
     def close(self):

@@ -140,4 +140,22 @@ __global__ void rows_to_cf_kernel(const float *__restrict__ src, int L, int Cp, 
   }
 }
 
+// channels-first fp32 [B][C][L] -> chunk-major fp32 [B][Cp/4][L][4] (zeros past C).
+// One thread per (b, 4-channel chunk, t): block 256, grid (ceil(L/256), Cp/4, B).
+__global__ void cf_to_rows_kernel(const float *__restrict__ cf, int L, int Cp, int C,
+                                  float *__restrict__ dst) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int j = blockIdx.y;
+  const int b = blockIdx.z;
+  if (t >= L) return;
+  float e[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = 4 * j + u;
+    e[u] = (c < C) ? cf[((size_t)b * C + c) * L + t] : 0.f;
+  }
+  reinterpret_cast<float4 *>(dst)[((size_t)b * (Cp / 4) + j) * L + t] =
+      make_float4(e[0], e[1], e[2], e[3]);
+}
+
 }  // namespace voc

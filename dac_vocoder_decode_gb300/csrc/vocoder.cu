@@ -16,6 +16,7 @@
 
 #include "vocoder.h"
 #include "conv_gemm.cuh"
+#include "ru_gemm.cuh"
 #include "stream_kernels.cuh"
 
 #define VOC_API extern "C" __attribute__((visibility("default")))
@@ -62,6 +63,9 @@ struct Layer {
   int in_buf = -1, f32_buf = -1, hl_buf = -1, skip_buf = -1;
   int epi_flags = 0;
   int cw = 32;              // epilogue column chunk (32, or 16 when 32 does not divide the tile)
+  // fused residual unit (conv1 k-tap + conv2 1x1 in one kernel)
+  bool ru = false;
+  voc::RuExtra rx{};
 };
 
 struct OutHead {
@@ -93,6 +97,12 @@ bool set_kernel_attrs(std::string &why) {
       st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(voc::ru_gemm_kernel<32>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(voc::ru_gemm_kernel<16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::out_head_kernel<kHeadTile>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
   });
@@ -115,6 +125,7 @@ struct vocoder {
   int *err_dev = nullptr;   // device error word of the kernels (bounded waits)
   int *flag_dev = nullptr;  // finite-check flag
   long long wait_budget = kWaitBudget;
+  int fuse_max_c = 0;       // residual units of up to this many (padded) channels run fused
   // TMA descriptors for the last (workspace, B, T)
   void *map_ws = nullptr;
   int map_B = -1, map_T = -1;
@@ -232,6 +243,67 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   return true;
 }
 
+// Plan a fused residual unit (L.K taps at dilation L.dil, then 1x1, C -> C): the conv1
+// geometry of plan_gemm, one column tile (N = Cp <= kRuMaxC), the conv1 result kept in a
+// shared H tile of 128 rows x Cp hi/lo pairs, and a k-block common to both convolutions.
+constexpr int kRuMaxC = 192;
+constexpr int kFuseDefault = 64;  // fused units win when their k-blocks need not shrink
+bool plan_ru(Layer &L, int padding, std::string &why) {
+  ConvGemmArgs &g = L.g;
+  L.Cp_in = L.Cp_out = rup(L.Cout, 16);
+  if (L.Cp_out > kRuMaxC) {
+    why = "too many channels for the fused residual unit";
+    return false;
+  }
+  g.Cp_in = g.Cp_out = L.Cp_out;
+  const int span = L.dil * (L.K - 1);
+  const int pad_left = (padding == VOC_PAD_CAUSAL) ? span : span / 2;
+  g.taps = L.K;
+  g.N_total = g.N_tile = L.Cp_out;
+  g.n_tiles = 1;
+  g.q_split_tile = 1;
+  g.s_rows = 1;
+  g.off_min = -pad_left;
+  g.shift0_q0 = g.shift0_q1 = 0;
+  g.tap_step = L.dil;
+  g.rows = rup(voc::kTileM + span, 8);
+  if (g.rows > 256) {
+    why = "tap span too wide for one staged tile";
+    return false;
+  }
+  L.cw = (g.N_tile % 32 == 0) ? 32 : 16;
+  L.rx.h_bytes = 4 * voc::kTileM * L.Cp_out;
+  const int chunkA = g.rows * 16;
+  const int sb = voc::skip_slot_bytes(L.cw);
+  g.na = 2;
+  g.KB = 0;
+  for (int kb = 16; kb <= L.Cp_in; kb += 16) {  // largest k-block that leaves >= 2 weight stages
+    if (L.Cp_in % kb || 4 * kb * g.N_tile > 36 * 1024 || 4 * kb * g.rows > 72 * 1024) continue;
+    const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
+    const int b_bytes = 4 * kb * g.N_tile;
+    int avail = kSmemMax - 1024 - kBarrierBytes - g.na * a_bytes - L.rx.h_bytes;
+    const int ns = ((avail - 4 * sb) / b_bytes >= 3) ? 4 : 2;
+    avail -= ns * sb;
+    const int nb = std::min(8, avail / b_bytes);
+    if (nb < 2) continue;
+    g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = b_bytes, g.nb = nb, g.ns = ns;
+  }
+  if (!g.KB) {
+    why = "shared memory plan of the fused residual unit does not fit";
+    return false;
+  }
+  g.nkb = L.Cp_in / g.KB;
+  int ac = 32;
+  while (ac < g.N_tile) ac *= 2;
+  g.acc_cols = ac;
+  L.rx.n_buf = (4 * ac <= 512) ? 2 : 1;
+  g.n_acc = 2 * L.rx.n_buf;  // accumulators in TMEM (conv1 and conv2 of each buffer)
+  L.smem = 1024 + (size_t)g.na * g.a_bytes + (size_t)g.nb * g.b_bytes + L.rx.h_bytes +
+           (size_t)g.ns * sb + kBarrierBytes;
+  L.ru = true;
+  return true;
+}
+
 // Value of the GEMM weight for column n, input channel ci, tap `tap`.
 float weight_value(const Layer &L, int padding, const float *w, int n, int ci, int tap) {
   if (ci >= L.Cin) return 0.f;
@@ -314,6 +386,26 @@ voc_status upload_layer(vocoder *ctx, std::vector<void *> &allocs, Layer &L, int
   if (st != VOC_OK) return st;
   L.w_dev = reinterpret_cast<uint8_t *>(wd);
   return upload_columns(ctx, allocs, L, bias, alpha);
+}
+
+// Weights of a fused residual unit: conv1 (L.K taps) and conv2 (1x1) packed with the same
+// k-block and column tile; epilogue 1 columns from (b1, alpha2), epilogue 2 from (b2, next).
+voc_status upload_ru(vocoder *ctx, std::vector<void *> &allocs, Layer &L, int padding,
+                     const float *w1, const float *b1, const float *a2, const float *w2,
+                     const float *b2, const float *next_alpha) {
+  voc_status st = upload_layer(ctx, allocs, L, padding, w1, b2, next_alpha);
+  if (st != VOC_OK) return st;
+  Layer L2 = L;
+  L2.K = 1;
+  L2.g.taps = 1;
+  std::vector<uint16_t> packed = pack_weights(L2, padding, w2);
+  uint16_t *wd = nullptr;
+  if ((st = upload(ctx, allocs, packed, &wd)) != VOC_OK) return st;
+  L.rx.wB2 = reinterpret_cast<const uint8_t *>(wd);
+  Layer Lh = L;
+  if ((st = upload_columns(ctx, allocs, Lh, b1, a2)) != VOC_OK) return st;
+  L.rx.bias_h = Lh.bias_dev, L.rx.alpha_h = Lh.alpha_dev, L.rx.invb_h = Lh.invb_dev;
+  return VOC_OK;
 }
 
 bool check_desc(const voc_desc *d, std::string &why) {
@@ -455,8 +547,9 @@ void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops,
   const double L_in = (double)level_len(ctx, L.level, T);
   const double L_out = L_in * (L.convT ? L.stride : 1);
   flops = L.convT ? 4.0 * L.Cin * L.Cout * B * L_out : 2.0 * L.Cin * L.Cout * L.K * B * L_in;
+  if (L.ru) flops = 2.0 * L.Cin * L.Cout * (L.K + 1) * B * L_in;
   const ConvGemmArgs &g = L.g;
-  double by = 4.0 * B * L_in * L.Cp_in + (double)g.n_tiles * g.taps * g.nkb * g.b_bytes;
+  double by = 4.0 * B * L_in * L.Cp_in + (double)g.n_tiles * (g.taps + (L.ru ? 1 : 0)) * g.nkb * g.b_bytes;
   const double out_elems = (double)B * L_out * L.Cp_out;
   if (L.skip_buf >= 0) by += 4.0 * out_elems;
   if (L.f32_buf >= 0) by += 4.0 * out_elems;
@@ -468,10 +561,16 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
                        const CUtensorMap &smap, const ConvGemmArgs &a, cudaStream_t stream) {
   const long long tiles = (long long)a.B * a.m_tiles * a.n_tiles;
   const int grid = static_cast<int>(std::min<long long>(tiles, ctx->num_sms));
-  if (L.cw == 32)
+  if (L.ru) {
+    if (L.cw == 32)
+      voc::ru_gemm_kernel<32><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a, L.rx);
+    else
+      voc::ru_gemm_kernel<16><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a, L.rx);
+  } else if (L.cw == 32) {
     voc::conv_gemm_kernel<32><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
-  else
+  } else {
     voc::conv_gemm_kernel<16><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, ("launch " + L.name).c_str());
   return VOC_OK;
@@ -612,6 +711,8 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
   ctx->desc.dilations = ctx->dils.data();
   for (int s : ctx->strides) ctx->hop *= s;
   ctx->Cp_lat = rup(desc->latent_channels, 16);
+  ctx->fuse_max_c = desc->fuse_max_channels == 0 ? kFuseDefault
+                    : (desc->fuse_max_channels < 0 ? 0 : desc->fuse_max_channels);
   auto bail = [&](voc_status st) {
     g_err = ctx->err;
     vocoder_destroy(ctx);
@@ -649,11 +750,20 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     ctx->layers.push_back(L);
     p = 2;
   }
+  // Three equal hi/lo buffers (H0, H1, HB) and the fp32 residual stream FY.  A layer that
+  // reads a hi/lo buffer with a halo never writes that buffer in the same launch (other
+  // tiles still read its halo rows); the fp32 stream is read row for row, so the residual
+  // layers update it in place.
+  auto other = [](int a, int b) {
+    for (int c : {(int)BUF_H0, (int)BUF_H1, (int)BUF_HB})
+      if (c != a && c != b) return c;
+    return -1;
+  };
+  int x_buf = BUF_H1;  // Snake'd input of the next ConvT (written by conv_in)
   int C = desc->channels0;
   for (int i = 0; i < desc->n_stages; ++i) {
-    const int A = (i % 2 == 0) ? BUF_H0 : BUF_H1;  // Snake1 inputs of this stage
-    const int X = (i % 2 == 0) ? BUF_H1 : BUF_H0;  // Snake'd input of this stage's ConvT
     const int Co = ctx->widths[i];
+    int cur = other(x_buf, BUF_HB);  // Snake1 input of the stage's first residual unit
     {
       Layer L;
       L.name = "convT" + std::to_string(i);
@@ -661,7 +771,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       L.Cin = C, L.Cout = Co, L.stride = ctx->strides[i], L.K = 2 * L.stride;
       L.level = i;
       if (!plan_gemm(L, pad, false, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L.name + ": " + why));
-      L.in_buf = X, L.f32_buf = BUF_FY, L.hl_buf = A;
+      L.in_buf = x_buf, L.f32_buf = BUF_FY, L.hl_buf = cur;
       st = upload_layer(ctx, ctx->allocs, L, pad, params[p + 1], params[p + 2], params[p + 3]);
       if (st != VOC_OK) return bail(st);
       ctx->layers.push_back(L);
@@ -672,34 +782,57 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       const float *w1 = params[p + 1], *b1 = params[p + 2], *a2 = params[p + 3];
       const float *w2 = params[p + 4], *b2 = params[p + 5];
       p += 6;
+      const float *next_alpha = params[p];  // next snake1 / next stage's snake / snake_out
+      const bool last_stage = (i == desc->n_stages - 1);
+      Layer R;  // the whole unit in one kernel when it fits and is enabled
+      R.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".ru";
+      R.Cin = C, R.Cout = C, R.K = desc->res_kernel, R.dil = ctx->dils[j];
+      R.level = i + 1;
+      if (rup(C, 16) <= ctx->fuse_max_c && plan_ru(R, pad, why)) {
+        const int out = other(cur, -1);  // never the buffer this unit reads
+        R.in_buf = cur, R.skip_buf = BUF_FY;
+        if (j < nd - 1) {
+          R.f32_buf = BUF_FY, R.hl_buf = out;
+        } else if (!last_stage) {
+          R.hl_buf = out;  // the next stage's ConvT input
+        } else {
+          R.f32_buf = BUF_FY, R.epi_flags = voc::EPI_F32_SNAKE;  // Snake_out(y) for the head
+        }
+        st = upload_ru(ctx, ctx->allocs, R, pad, w1, b1, a2, w2, b2, next_alpha);
+        if (st != VOC_OK) return bail(st);
+        ctx->layers.push_back(R);
+        if (R.hl_buf >= 0) cur = out;
+        continue;
+      }
+      const int tmp = other(cur, x_buf == cur ? -1 : x_buf);  // conv1 output, read by conv2
       Layer L1;
       L1.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".conv1";
       L1.Cin = C, L1.Cout = C, L1.K = desc->res_kernel, L1.dil = ctx->dils[j];
       L1.level = i + 1;
       if (!plan_gemm(L1, pad, false, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L1.name + ": " + why));
-      L1.in_buf = A, L1.hl_buf = BUF_HB;
+      L1.in_buf = cur, L1.hl_buf = tmp;
       st = upload_layer(ctx, ctx->allocs, L1, pad, w1, b1, a2);
       if (st != VOC_OK) return bail(st);
       ctx->layers.push_back(L1);
 
-      Layer L2;
+      Layer L2;  // 1x1: reads `tmp` row for row, so it may write `cur`
       L2.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".conv2";
       L2.Cin = C, L2.Cout = C, L2.K = 1, L2.dil = 1;
       L2.level = i + 1;
       if (!plan_gemm(L2, pad, true, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L2.name + ": " + why));
-      L2.in_buf = BUF_HB, L2.skip_buf = BUF_FY;
-      const float *next_alpha = params[p];  // next snake1 / next stage's snake / snake_out
+      L2.in_buf = tmp, L2.skip_buf = BUF_FY;
       if (j < nd - 1) {
-        L2.f32_buf = BUF_FY, L2.hl_buf = A;
-      } else if (i < desc->n_stages - 1) {
-        L2.hl_buf = A;  // becomes the next stage's ConvT input
+        L2.f32_buf = BUF_FY, L2.hl_buf = cur;
+      } else if (!last_stage) {
+        L2.hl_buf = cur;
       } else {
-        L2.f32_buf = BUF_FY, L2.epi_flags = voc::EPI_F32_SNAKE;  // Snake_out(y) for the head
+        L2.f32_buf = BUF_FY, L2.epi_flags = voc::EPI_F32_SNAKE;
       }
       st = upload_layer(ctx, ctx->allocs, L2, pad, w2, b2, next_alpha);
       if (st != VOC_OK) return bail(st);
       ctx->layers.push_back(L2);
     }
+    x_buf = cur;
   }
   // out head: Snake already applied by the last conv2 epilogue
   {
@@ -1086,6 +1219,108 @@ VOC_API voc_status vocoder_op_conv_transpose1d(const float *x_dev, int B, int Ci
   L.Cin = Cin, L.Cout = Cout, L.stride = stride, L.K = 2 * stride;
   return op_layer(L, padding, x_dev, B, T, w_host, b_host, alpha_host, y_dev,
                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+VOC_API voc_status vocoder_op_residual_unit(const float *x_dev, int B, int C, int T,
+                                            const float *alpha1_host, const float *w1_host,
+                                            const float *b1_host, int K, int dil,
+                                            const float *alpha2_host, const float *w2_host,
+                                            const float *b2_host, int padding, float *y_dev,
+                                            voc_stream_t stream_) {
+  if (!x_dev || !y_dev || !w1_host || !w2_host || !alpha1_host || !alpha2_host)
+    return fail(nullptr, VOC_INVALID_ARG, "NULL pointer");
+  if (B < 1 || C < 1 || T < 1 || K < 1 || K > 15 || K % 2 == 0 || dil < 1 ||
+      dil * (K - 1) > 120 || (padding != VOC_PAD_SYMMETRIC && padding != VOC_PAD_CAUSAL))
+    return fail(nullptr, VOC_INVALID_ARG, "invalid residual unit shape");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  std::string why;
+  if (!set_kernel_attrs(why)) return fail(nullptr, VOC_CUDA_ERROR, why);
+  int dev = 0, sms = 0, major = 0, minor = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return fail(nullptr, VOC_UNSUPPORTED, "this build targets sm_103 only");
+  vocoder tmp;
+  tmp.num_sms = sms;
+  tmp.device = dev;
+  tmp.strides = {1};
+  auto done = [&](voc_status st) {
+    if (st != VOC_OK) g_err = tmp.err;
+    for (void *q : tmp.allocs) cudaFree(q);
+    return st;
+  };
+  const int Cp = rup(C, 16);
+  const size_t bb = (size_t)B * T * Cp * 4;
+  void *bufs[BUF_COUNT] = {nullptr, nullptr, nullptr, nullptr};
+  for (int i : {(int)BUF_H0, (int)BUF_HB, (int)BUF_FY}) {
+    cudaError_t e = cudaMalloc(&bufs[i], bb);
+    if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
+    tmp.allocs.push_back(bufs[i]);
+  }
+  cudaError_t e = cudaMalloc(&tmp.err_dev, 8 * sizeof(int));
+  if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
+  tmp.allocs.push_back(tmp.err_dev);
+  cudaMemsetAsync(tmp.err_dev, 0, 8 * sizeof(int), stream);
+  voc_status st;
+  float *alpha_d = nullptr, *invb_d = nullptr;
+  {
+    std::vector<float> a(alpha1_host, alpha1_host + C), ib(C);
+    for (int c = 0; c < C; ++c) ib[c] = static_cast<float>(1.0 / ((double)a[c] + 1e-9));
+    if ((st = upload(&tmp, tmp.allocs, a, &alpha_d)) != VOC_OK) return done(st);
+    if ((st = upload(&tmp, tmp.allocs, ib, &invb_d)) != VOC_OK) return done(st);
+  }
+  // A = Snake1(x) as hi/lo; the residual stream x as fp32 chunk-major (updated in place)
+  if ((st = launch_prep(&tmp, x_dev, B, C, T, Cp, alpha_d, invb_d,
+                        static_cast<__nv_bfloat16 *>(bufs[BUF_H0]), stream)) != VOC_OK)
+    return done(st);
+  voc::cf_to_rows_kernel<<<dim3((T + 255) / 256, Cp / 4, B), 256, 0, stream>>>(
+      x_dev, T, Cp, C, static_cast<float *>(bufs[BUF_FY]));
+  std::vector<Layer> layers;
+  Layer R;
+  R.name = "op_ru";
+  R.Cin = C, R.Cout = C, R.K = K, R.dil = dil;
+  if (plan_ru(R, padding, why)) {
+    R.in_buf = BUF_H0, R.skip_buf = BUF_FY, R.f32_buf = BUF_FY;
+    if ((st = upload_ru(&tmp, tmp.allocs, R, padding, w1_host, b1_host, alpha2_host, w2_host,
+                        b2_host, nullptr)) != VOC_OK)
+      return done(st);
+    layers.push_back(R);
+  } else {
+    Layer L1, L2;
+    L1.name = "op_conv1", L2.name = "op_conv2";
+    L1.Cin = L1.Cout = L2.Cin = L2.Cout = C;
+    L1.K = K, L1.dil = dil, L2.K = 1, L2.dil = 1;
+    if (!plan_gemm(L1, padding, false, why) || !plan_gemm(L2, padding, true, why))
+      return done(fail(&tmp, VOC_UNSUPPORTED, why));
+    L1.in_buf = BUF_H0, L1.hl_buf = BUF_HB;
+    L2.in_buf = BUF_HB, L2.skip_buf = BUF_FY, L2.f32_buf = BUF_FY;
+    if ((st = upload_layer(&tmp, tmp.allocs, L1, padding, w1_host, b1_host, alpha2_host)) != VOC_OK ||
+        (st = upload_layer(&tmp, tmp.allocs, L2, padding, w2_host, b2_host, nullptr)) != VOC_OK)
+      return done(st);
+    layers.push_back(L1);
+    layers.push_back(L2);
+  }
+  for (const Layer &L : layers) {
+    CUtensorMap map, smap{};
+    if ((st = encode_map(&tmp, &map, bufs[L.in_buf], L.Cp_in, T, B, L.g.rows, L.g.KB / 8)) != VOC_OK)
+      return done(st);
+    if (L.skip_buf >= 0 &&
+        (st = encode_skip_map(&tmp, &smap, bufs[L.skip_buf], L.Cp_out, T, B, L.cw)) != VOC_OK)
+      return done(st);
+    ConvGemmArgs a;
+    gemm_launch_args(&tmp, L, B, T, bufs, bb, a);
+    if ((st = launch_gemm(&tmp, L, map, smap, a, stream)) != VOC_OK) return done(st);
+  }
+  voc::rows_to_cf_kernel<<<dim3((T + 255) / 256, Cp / 4, B), 256, 0, stream>>>(
+      static_cast<const float *>(bufs[BUF_FY]), T, Cp, C, y_dev);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "residual unit"));
+  int word = 0;
+  cudaMemcpy(&word, tmp.err_dev, sizeof(int), cudaMemcpyDeviceToHost);
+  if (word) return done(fail(&tmp, VOC_DEVICE_TIMEOUT, "a kernel gave up a bounded wait"));
+  return done(VOC_OK);
 }
 
 VOC_API int vocoder_profile_count(const vocoder *ctx) {

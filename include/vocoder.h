@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define VOC_ABI_VERSION 1
+#define VOC_ABI_VERSION 2
 
 typedef struct vocoder vocoder_t;             /* opaque context */
 typedef struct CUstream_st *voc_stream_t;     /* a cudaStream_t */
@@ -90,6 +90,10 @@ typedef struct {
   int out_channels;     /* 1                                                 */
   int padding;          /* VOC_PAD_SYMMETRIC | VOC_PAD_CAUSAL                */
   int precision;        /* VOC_PREC_BF16X3                                   */
+  int fuse_max_channels;/* residual units of up to this many channels run as one
+                           kernel (conv1 result kept on chip); 0 = library default,
+                           -1 = never.  A performance choice only: results agree
+                           within the decode tolerance either way.              */
 } voc_desc;
 
 /* ABI version of the library (VOC_ABI_VERSION of the build). */
@@ -211,6 +215,21 @@ voc_status vocoder_op_conv_transpose1d(const float *x_dev, int B, int Cin, int T
                                        const float *w_host, const float *b_host, int Cout,
                                        int stride, int padding, const float *alpha_host,
                                        float *y_dev, voc_stream_t stream);
+
+/* One residual unit (minimaxmusic.cpp Architecture, "Flow VAE": skip -> snake1 -> conv1
+ * k-tap dilated -> snake2 -> conv2 1x1 -> + skip) on the decoder's own kernels:
+ *   y = x + conv2( S2( conv1( S1(x) ) + b1 ) ) + b2
+ * x_dev, y_dev [B][C][T] fp32 channels-first (may not alias); w1_host [C][C][K],
+ * w2_host [C][C][1], alpha1/alpha2 [C] (required), b1/b2 [C] or NULL; padding as for
+ * vocoder_op_conv1d.  Up to 192 channels the unit runs as one fused kernel (the conv1
+ * result stays in shared memory), above as two.  Allocates its temporaries and
+ * synchronises `stream` before returning. */
+voc_status vocoder_op_residual_unit(const float *x_dev, int B, int C, int T,
+                                    const float *alpha1_host, const float *w1_host,
+                                    const float *b1_host, int K, int dil,
+                                    const float *alpha2_host, const float *w2_host,
+                                    const float *b2_host, int padding, float *y_dev,
+                                    voc_stream_t stream);
 
 /* Kernel launches that one vocoder_decode(ctx, ., B, T, ...) enqueues. */
 int vocoder_launches_per_decode(const vocoder_t *ctx, int B, int T);

@@ -73,6 +73,10 @@ int main(void) {
   CHECK(vocoder_op_conv_transpose1d((const float *)0, 1, 1, 1, (const float *)0, (const float *)0,
                                     1, 2, VOC_PAD_SYMMETRIC, (const float *)0, (float *)0,
                                     (voc_stream_t)0) == VOC_INVALID_ARG);
+  CHECK(vocoder_op_residual_unit((const float *)0, 1, 1, 1, (const float *)0, (const float *)0,
+                                 (const float *)0, 7, 1, (const float *)0, (const float *)0,
+                                 (const float *)0, VOC_PAD_SYMMETRIC, (float *)0,
+                                 (voc_stream_t)0) == VOC_INVALID_ARG);
   CHECK(vocoder_launches_per_decode((const vocoder_t *)0, 1, 1) == -1);
   CHECK(vocoder_profile_count((const vocoder_t *)0) == 0);
   CHECK(vocoder_profile_entry((vocoder_t *)0, 0, (const char **)0, (double *)0, (double *)0,

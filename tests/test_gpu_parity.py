@@ -131,6 +131,54 @@ def test_op_conv_transpose1d(case):
         assert np.all(err <= LAYER_REL * mag + 1e-6), (bi, float(err.max()), float(mag.max()))
 
 
+RU_CASES = [
+    # B, C, T, dil, padding   (C <= 192: fused kernel; above: conv1 + conv2 kernels)
+    (2, 96, 300, 9, W.PAD_SYMMETRIC),
+    (1, 96, 257, 1, W.PAD_CAUSAL),
+    (2, 192, 200, 3, W.PAD_SYMMETRIC),
+    (1, 48, 400, 9, W.PAD_CAUSAL),
+    (3, 16, 70, 3, W.PAD_SYMMETRIC),
+    (1, 4, 129, 9, W.PAD_SYMMETRIC),
+    (1, 32, 1000, 1, W.PAD_SYMMETRIC),
+    (2, 384, 130, 9, W.PAD_SYMMETRIC),
+    (1, 768, 140, 3, W.PAD_CAUSAL),
+]
+
+
+@pytest.mark.parametrize("case", RU_CASES, ids=[str(c) for c in RU_CASES])
+def test_op_residual_unit(case):
+    """y = x + conv2(Snake2(conv1(Snake1(x)) + b1)) + b2.  Bound: the conv2 error
+    2^-14 sum|w2 s2| plus the conv1 error carried through Snake2 (slope <= 2) and
+    conv2, plus the hi/lo split of Snake2's output."""
+    B, C, T, d, padding = case
+    rng = np.random.default_rng(hash(case) % 2**32)
+    x = rng.standard_normal((B, C, T)).astype(np.float32)
+    w1 = (rng.standard_normal((C, C, 7)) * 0.5 / np.sqrt(7 * C)).astype(np.float32)
+    w2 = (rng.standard_normal((C, C, 1)) * 0.5 / np.sqrt(C)).astype(np.float32)
+    b1 = (rng.standard_normal(C) * 0.02).astype(np.float32)
+    b2 = (rng.standard_normal(C) * 0.02).astype(np.float32)
+    a1 = rng.uniform(0.5, 1.5, C).astype(np.float32)
+    a2 = rng.uniform(0.5, 1.5, C).astype(np.float32)
+    y = torch.empty((B, C, T), dtype=torch.float32, device="cuda")
+    V.vocoder_op_residual_unit(torch.from_numpy(x).cuda(), a1, w1, b1, d, a2, w2, b2, padding, y)
+    torch.cuda.synchronize()
+    got = y.cpu().numpy().astype(np.float64)
+    span = 6 * d
+    pl = span if padding == W.PAD_CAUSAL else span // 2
+    w1d, w2d = w1.astype(np.float64), w2.astype(np.float64)
+    for bi in range(B):
+        s1 = O.snake(x[bi], a1)
+        h = O.conv1d(s1, w1d, b1, d, pl, span - pl)
+        s2 = O.snake(h, a2)
+        ref = x[bi].astype(np.float64) + O.conv1d(s2, w2d, b2, 1, 0, 0)
+        m1 = O.conv1d(np.abs(s1), np.abs(w1d), None, d, pl, span - pl)
+        m2 = O.conv1d(np.abs(s2), np.abs(w2d), None, 1, 0, 0)
+        carried = O.conv1d(2 * LAYER_REL * m1 + 2.0 ** -16 * np.abs(s2), np.abs(w2d), None, 1, 0, 0)
+        bound = LAYER_REL * m2 + carried + 2e-6
+        err = np.abs(got[bi] - ref)
+        assert np.all(err <= bound), (bi, float(np.max(err - bound)))
+
+
 # ----------------------------------------------------------------------------- full decodes
 @pytest.mark.parametrize("name", ["tiny", "tiny_cal"])
 def test_decode_tiny_full(name):
@@ -163,6 +211,23 @@ def test_batch_equals_items():
     for i in range(3):
         yi = G.gpu_decode(voc, lat[i:i + 1])
         np.testing.assert_array_equal(yb[i], yi[0])
+
+
+MID_MUSIC = W.Arch(latent_channels=64, channels0=384, strides=(8, 8, 4, 2), widths=(192, 96, 96, 48))
+MID_SPEECH = W.Arch(latent_channels=64, channels0=256, strides=(8, 5, 4, 4, 3),
+                    widths=(192, 96, 48, 48, 32), padding=W.PAD_CAUSAL)
+
+
+@pytest.mark.parametrize("arch", [MID_MUSIC, MID_SPEECH], ids=["music", "speech_causal"])
+@pytest.mark.parametrize("fuse", [-1, 192], ids=["unfused", "fused"])
+def test_decode_fusion_variants(arch, fuse):
+    """Residual units as one fused kernel or as conv1 + conv2 kernels, over many tiles per
+    CTA (several waves), checked sample by sample against the oracle."""
+    wl = W.make_custom(arch, B=2, T=60, seed=71)
+    voc = V.Vocoder(arch, V.fold_params(wl.params), fuse_max_channels=fuse)
+    got = G.gpu_decode(voc, wl.latent)
+    ref = O.decode(arch, wl.params, wl.latent)
+    G.compare_audio(ref, got, f"fuse={fuse}")
 
 
 def _sampled_full_size(name, n_items=None, width=8, n=3):
