@@ -15,7 +15,7 @@ import numpy as np
 
 from . import build as _build
 
-VOC_ABI_VERSION = 2
+VOC_ABI_VERSION = 3
 VOC_OK = 0
 VOC_INVALID_ARG = -1
 VOC_UNSUPPORTED = -2
@@ -62,7 +62,7 @@ class VocDesc(ctypes.Structure):
                 ("dilations", ctypes.POINTER(ctypes.c_int)), ("res_kernel", ctypes.c_int),
                 ("out_kernel", ctypes.c_int), ("out_channels", ctypes.c_int),
                 ("padding", ctypes.c_int), ("precision", ctypes.c_int),
-                ("fuse_max_channels", ctypes.c_int)]
+                ("fuse_max_channels", ctypes.c_int), ("cta_pair", ctypes.c_int)]
 
 
 _lib = None
@@ -157,14 +157,14 @@ def _stream_ptr(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(int(stream))
 
 
-def make_desc(arch, fuse_max_channels: int = 0) -> VocDesc:
+def make_desc(arch, fuse_max_channels: int = 0, cta_pair: int = 0) -> VocDesc:
     """voc_desc for an Arch (layer shapes from workloads.Arch or any object with the same fields)."""
     strides = (ctypes.c_int * len(arch.strides))(*arch.strides)
     widths = (ctypes.c_int * len(arch.widths))(*arch.widths)
     dils = (ctypes.c_int * len(arch.dilations))(*arch.dilations)
     d = VocDesc(VOC_ABI_VERSION, arch.latent_channels, arch.in_kernel, arch.channels0,
                 len(arch.strides), strides, widths, len(arch.dilations), dils, arch.res_kernel,
-                arch.out_kernel, 1, arch.padding, VOC_PREC_BF16X3, fuse_max_channels)
+                arch.out_kernel, 1, arch.padding, VOC_PREC_BF16X3, fuse_max_channels, cta_pair)
     d._keep = (strides, widths, dils)
     return d
 
@@ -197,13 +197,14 @@ def vocoder_fold_weight_norm(g: np.ndarray, v: np.ndarray) -> np.ndarray:
 
 
 def vocoder_create(arch, params: Sequence[Optional[np.ndarray]],
-                   fuse_max_channels: int = 0) -> ctypes.c_void_p:
+                   fuse_max_channels: int = 0, cta_pair: int = 0) -> ctypes.c_void_p:
     """params: folded fp32 arrays in the canonical order (None for a zero bias)."""
     lib = load_library()
     keep = [None if p is None else np.ascontiguousarray(p, dtype=np.float32) for p in params]
     arr = (ctypes.POINTER(ctypes.c_float) * len(keep))(*[_fptr(p) for p in keep])
     h = ctypes.c_void_p()
-    _check(lib.vocoder_create(ctypes.byref(make_desc(arch, fuse_max_channels)), arr, len(keep),
+    _check(lib.vocoder_create(ctypes.byref(make_desc(arch, fuse_max_channels, cta_pair)), arr,
+                              len(keep),
                               ctypes.byref(h)))
     return h
 
@@ -346,9 +347,9 @@ def fold_params(params) -> list:
 class Vocoder:
     """A decoder on the current CUDA device (owns its library context)."""
 
-    def __init__(self, arch, folded_params, fuse_max_channels: int = 0):
+    def __init__(self, arch, folded_params, fuse_max_channels: int = 0, cta_pair: int = 0):
         self.arch = arch
-        self.handle = vocoder_create(arch, folded_params, fuse_max_channels)
+        self.handle = vocoder_create(arch, folded_params, fuse_max_channels, cta_pair)
         self.hop = vocoder_hop(self.handle)
 
     def close(self):

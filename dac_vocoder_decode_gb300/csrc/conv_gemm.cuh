@@ -26,11 +26,13 @@
 // The row offset of a tap is a 16-byte shift of the descriptor start address, so
 // all taps reuse one staged halo tile (128 + span rows, zero fill outside [0, L)).
 //
-// Roles: warp 0 lane 0 issues the A (TMA) and weight (bulk) copies, warp 1 lane 0
-// issues MMAs, warps 2..9 run the epilogue (TMEM -> registers -> bias, residual,
-// Snake of the next layer, hi/lo split -> global; with the chunk-major layout the
-// 32 lanes of a warp store 32 consecutive rows of one chunk: 512 contiguous
-// bytes), warp 10 lane 0 prefetches the residual input of the epilogue by TMA.
+// Roles: warp 0 lane 0 issues the A copies (one 5-D TMA box per k-block: the hi and
+// lo planes of its channel chunks), warp 1 lane 0 issues MMAs, warps 2..9 run the
+// epilogue (TMEM -> registers -> bias, residual, Snake of the next layer, hi/lo split
+// -> global; with the chunk-major layout the 32 lanes of a warp store 32 consecutive
+// rows of one chunk: 512 contiguous bytes), warps 10 and 11 prefetch the residual
+// input of the two epilogue halves by TMA, warp 12 issues the weight copies.  The MMA
+// warp runs its loop convergently and issues through an elected lane.
 // The grid is persistent; 2 to 4 TMEM accumulators let the epilogue of one tile
 // overlap the mainloop of the next.
 #pragma once
@@ -44,8 +46,11 @@ namespace voc {
 
 constexpr int kTileM = 128;
 constexpr int kEpiWarps = 8;                            // two per TMEM lane quadrant
-constexpr int kSkipWarp = 2 + kEpiWarps;                // residual prefetch warp
-constexpr int kGemmThreads = 32 * (kSkipWarp + 1);      // 352
+constexpr int kSkipWarp = 2 + kEpiWarps;                // residual prefetch (10, 11: one per half)
+constexpr int kBWarp = kSkipWarp + 2;                   // weight copies (12)
+constexpr int kBWarps = 1;
+constexpr int kGemmThreads = 32 * (kBWarp + kBWarps);   // 448
+constexpr int kRuThreads = 32 * (kSkipWarp + 1);        // 352: fused residual-unit kernel
 constexpr int kMaxAcc = 4;
 
 // bytes of one residual slot (128 rows x cw fp32 columns, as cw/4 chunks of 128 x 16 B)
@@ -219,7 +224,26 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, int slots, int issued
   }
 }
 
-template <int CW>
+// PAIR = false: one CTA per 128-row tile.  PAIR = true: the grid is made of 2-CTA clusters
+// and each cluster computes a 256-row tile with the CTA-pair MMA (cta_group::2): each CTA
+// stages its own 128-row A halo tile and half of every weight tile (columns
+// [rank*N/2, (rank+1)*N/2), packed as separate column tiles), so the weights streamed
+// through L2 and shared memory per output row are halved and the tensor core reads half of
+// B from each SM.  The even CTA issues the MMAs; the odd CTA's MMA thread relays the
+// completion of its own copies to the even CTA's `pair` barriers; the MMA commits
+// multicast to both CTAs' barriers; the odd CTA's epilogue warps release an accumulator by
+// arriving on the even CTA's barrier.
+// drain_ring for a ring whose slots lie `stride` barriers apart.
+__device__ __forceinline__ void drain_ring_strided(uint64_t *full, int slots, int stride,
+                                                   int issued, long long budget) {
+  const volatile int never = 0;
+  for (int s = 0; s < slots && s < issued; ++s) {
+    const int cnt = (issued - s + slots - 1) / slots;
+    mbar_wait(smem_u32(full + s * stride), static_cast<uint32_t>(cnt - 1) & 1u, budget, &never);
+  }
+}
+
+template <int CW, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap tmapA,
                      const __grid_constant__ CUtensorMap tmapS, const ConvGemmArgs p) {
@@ -238,13 +262,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t *accEmpty = accFull + kMaxAcc;
   uint64_t *skipFull = accEmpty + kMaxAcc;
   uint64_t *skipEmpty = skipFull + p.ns;
-  uint64_t *drain = skipEmpty + p.ns;
+  uint64_t *pairA = skipEmpty + p.ns;  // even CTA: the odd CTA's A stage has landed
+  uint64_t *pairB = pairA + p.na;      // even CTA: the odd CTA's weight stage has landed
+  uint64_t *drain = pairB + p.nb;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t tmem_cols = static_cast<uint32_t>(p.n_acc * p.acc_cols);
+  constexpr int kM = PAIR ? 2 * kTileM : kTileM;  // rows of one tile job
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int job0 = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int job_step = PAIR ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+  const int row0 = static_cast<int>(rank) * kTileM;  // this CTA's rows within a tile job
 #ifdef VOC_CHECKS
   // the barrier block must end inside the dynamic allocation
   if (reinterpret_cast<const volatile uint8_t *>(abort_flag + 1) > smem_raw + p.smem_bytes) {
@@ -252,22 +283,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       p.dbg[1] = static_cast<int>(reinterpret_cast<const volatile uint8_t *>(abort_flag + 1) - smem_raw);
       p.dbg[2] = p.smem_bytes;
     }
-    return;
+    return;  // uniform over the grid: every CTA computes the same layout
   }
 #endif
+  // set this CTA's and (pair) the other CTA's abort flag
+  auto raise_abort = [&]() {
+    *abort_flag = 1;
+    if (PAIR) st_cluster_u32(mapa_shared(smem_u32(const_cast<int *>(abort_flag)), rank ^ 1u), 1u);
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.na; ++i) {
       mbar_init(smem_u32(fullA + i), 1);
       mbar_init(smem_u32(emptyA + i), 1);
+      mbar_init(smem_u32(pairA + i), 1);
     }
     for (int i = 0; i < p.nb; ++i) {
       mbar_init(smem_u32(fullB + i), 1);
       mbar_init(smem_u32(emptyB + i), 1);
+      mbar_init(smem_u32(pairB + i), 1);
     }
     for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(smem_u32(accFull + i), 1);
-      mbar_init(smem_u32(accEmpty + i), kEpiWarps * 32);
+      mbar_init(smem_u32(accEmpty + i), (PAIR ? 2 : 1) * kEpiWarps);  // one arrival per warp
     }
     for (int i = 0; i < p.ns; ++i) {
       mbar_init(smem_u32(skipFull + i), 1);
@@ -279,35 +317,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_proxy_async_smem();
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), tmem_cols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), tmem_cols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), tmem_cols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();  // the other CTA's barriers are initialised before any remote arrival
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
 
-  const int total_tiles = p.B * p.m_tiles * p.n_tiles;
+  const int total_jobs = p.B * p.m_tiles * p.n_tiles;
   const int kchunks = p.KB / 8;
   const uint32_t chunkA = static_cast<uint32_t>(p.rows) * 16u;
-  const uint32_t chunkB = static_cast<uint32_t>(p.N_tile) * 16u;
+  const int n_half = PAIR ? p.N_tile / 2 : p.N_tile;  // weight rows staged by this CTA
+  const uint32_t chunkB = static_cast<uint32_t>(n_half) * 16u;
   const int n_chunks = p.N_tile / CW;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------------------ A / weight producer
+      // ------------------------------------------------------------ A producer
       prefetch_tmap(&tmapA);
       const uint32_t a_tx = 2u * kchunks * chunkA;
-      const int lo_chunk0 = p.Cp_in / 8;
-      int ia = 0, ib = 0;
+      int ia = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-        const int nt = tile % p.n_tiles;
-        const int rest = tile / p.n_tiles;
+      for (int job = job0; job < total_jobs && ok; job += job_step) {
+        const int rest = job / p.n_tiles;
         const int mt = rest % p.m_tiles;
         const int b = rest / p.m_tiles;
-        const int y0 = mt * kTileM + p.off_min;
-        for (int kb = 0; kb < p.nkb && ok; ++kb) {
+        const int y0 = mt * kM + row0 + p.off_min;
+        for (int kb = 0; kb < p.nkb; ++kb) {
           const int sa = ia % p.na;
           const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;
           if (!mbar_wait(smem_u32(emptyA + sa), pha ^ 1u, p.timeout, abort_flag)) {
@@ -317,52 +362,76 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t fa = smem_u32(fullA + sa);
           const uint32_t dstA = smem_u32(smA + (size_t)sa * p.a_bytes);
 #ifdef VOC_CHECKS
-          if (!(dstA + a_tx <= smem_u32(smB) && lo_chunk0 + (kb + 1) * kchunks <= p.chunks_a &&
-                2 * kchunks * chunkA <= (uint32_t)p.a_bytes)) {
+          if (!(dstA + a_tx <= smem_u32(smB) && (kb + 1) * kchunks <= p.chunks_a / 2 &&
+                a_tx <= (uint32_t)p.a_bytes)) {
             check_fail(p, abort_flag, 21, dstA, kb, p.chunks_a);
             ok = false;
             break;
           }
 #endif
           mbar_arrive_expect_tx(fa, a_tx);
-          tma_load_4d(dstA, &tmapA, fa, 0, y0, kb * kchunks, b);                 // hi chunks
-          tma_load_4d(dstA + kchunks * chunkA, &tmapA, fa, 0, y0, lo_chunk0 + kb * kchunks, b);
+          tma_load_5d(dstA, &tmapA, fa, 0, y0, kb * kchunks, 0, b);  // hi and lo chunks
+          ++ia;
+        }
+      }
+      if (!ok) {
+        atomicOr(p.err, ERR_TIMEOUT_PRODUCER);
+        raise_abort();
+        drain_ring(fullA, p.na, ia, p.timeout);  // copies in flight land before the CTA exits
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && PAIR && rank != 0) {
+      // ------------------------------------------------------------ odd CTA: relay
+      // Tell the even CTA that each of this CTA's stages has landed, in the order the
+      // MMA thread consumes them.  A slot is refilled only after the MMAs that read it
+      // completed, which needs this relay's arrival first, so no phase is ever skipped.
+      const uint32_t remA = mapa_shared(smem_u32(pairA), 0u);
+      const uint32_t remB = mapa_shared(smem_u32(pairB), 0u);
+      int ia = 0, ib = 0;
+      bool ok = true;
+      for (int job = job0; job < total_jobs && ok; job += job_step) {
+        for (int kb = 0; kb < p.nkb && ok; ++kb) {
+          const int sa = ia % p.na;
+          if (!mbar_wait(smem_u32(fullA + sa), static_cast<uint32_t>(ia / p.na) & 1u, p.timeout,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(remA + static_cast<uint32_t>(sa * 8));
           ++ia;
           for (int tap = 0; tap < p.taps; ++tap) {
             const int sb = ib % p.nb;
-            const uint32_t phb = static_cast<uint32_t>(ib / p.nb) & 1u;
-            if (!mbar_wait(smem_u32(emptyB + sb), phb ^ 1u, p.timeout, abort_flag)) {
+            if (!mbar_wait(smem_u32(fullB + sb), static_cast<uint32_t>(ib / p.nb) & 1u,
+                           p.timeout, abort_flag)) {
               ok = false;
               break;
             }
-            const uint32_t fb = smem_u32(fullB + sb);
-            const size_t widx = ((size_t)nt * p.taps + tap) * p.nkb + kb;
-#ifdef VOC_CHECKS
-            if (!((long long)(widx + 1) * p.b_bytes <= p.w_bytes &&
-                  smem_u32(smB + (size_t)(sb + 1) * p.b_bytes) <= smem_u32(smS))) {
-              check_fail(p, abort_flag, 22, widx, sb, p.w_bytes);
-              ok = false;
-              break;
-            }
-#endif
-            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(p.b_bytes));
-            bulk_load(smem_u32(smB + (size_t)sb * p.b_bytes), p.wB + widx * p.b_bytes,
-                      static_cast<uint32_t>(p.b_bytes), fb);
+            mbar_arrive_cluster(remB + static_cast<uint32_t>(sb * 8));
             ++ib;
           }
         }
       }
       if (!ok) {
-        atomicOr(p.err, ERR_TIMEOUT_PRODUCER);
-        *abort_flag = 1;
-        drain_ring(fullA, p.na, ia, p.timeout);  // copies in flight land before the CTA exits
-        drain_ring(fullB, p.nb, ib, p.timeout);
+        atomicOr(p.err, ERR_TIMEOUT_MMA);
+        raise_abort();
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_bf16_f32(kTileM, p.N_tile);
+    } else if (!PAIR || rank == 0) {
+      // ------------------------------------------------------------ MMA issuer (whole warp)
+      // Every lane runs the loop; waits are made warp-uniform; one elected lane issues
+      // each MMA and commit (the same lane every time: the warp is converged).
+      auto wait_all = [&](uint32_t bar, uint32_t parity, bool cluster) {
+        const bool got = cluster ? mbar_wait_cluster(bar, parity, p.timeout, abort_flag)
+                                 : mbar_wait(bar, parity, p.timeout, abort_flag);
+        return __all_sync(0xffffffffu, got);
+      };
+      auto commit = [&](uint64_t *bar) {
+        if (PAIR)
+          mma_commit_pair_warp(smem_u32(bar), 3);
+        else
+          mma_commit_warp(smem_u32(bar));
+      };
+      const uint32_t idesc = idesc_bf16_f32(kM, p.N_tile);
       // descriptor increments: +1 in the start-address field is +16 bytes
       const uint64_t dA_lo = (uint64_t)((kchunks * chunkA) >> 4);
       const uint64_t dA_k = (uint64_t)((2 * chunkA) >> 4);
@@ -370,12 +439,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint64_t dB_k = (uint64_t)((2 * chunkB) >> 4);
       int ia = 0, ib = 0, it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
-        const int nt = tile % p.n_tiles;
+      for (int job = job0; job < total_jobs && ok; job += job_step, ++it) {
+        const int nt = job % p.n_tiles;
         const int shift0 = (nt >= p.q_split_tile) ? p.shift0_q1 : p.shift0_q0;
         const int acc = it % p.n_acc;
         const uint32_t phacc = static_cast<uint32_t>(it / p.n_acc) & 1u;
-        if (!mbar_wait(smem_u32(accEmpty + acc), phacc ^ 1u, p.timeout, abort_flag)) {
+        if (!wait_all(smem_u32(accEmpty + acc), phacc ^ 1u, PAIR)) {
           ok = false;
           break;
         }
@@ -384,7 +453,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int kb = 0; kb < p.nkb && ok; ++kb) {
           const int sa = ia % p.na;
           const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;
-          if (!mbar_wait(smem_u32(fullA + sa), pha, p.timeout, abort_flag)) {
+          if (!wait_all(smem_u32(fullA + sa), pha, false) ||
+              (PAIR && !wait_all(smem_u32(pairA + sa), pha, true))) {
             ok = false;
             break;
           }
@@ -393,7 +463,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int tap = 0; tap < p.taps; ++tap) {
             const int sb = ib % p.nb;
             const uint32_t phb = static_cast<uint32_t>(ib / p.nb) & 1u;
-            if (!mbar_wait(smem_u32(fullB + sb), phb, p.timeout, abort_flag)) {
+            if (!wait_all(smem_u32(fullB + sb), phb, false) ||
+                (PAIR && !wait_all(smem_u32(pairB + sb), phb, true))) {
               ok = false;
               break;
             }
@@ -401,8 +472,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #ifdef VOC_CHECKS
             {
               const int sh = shift0 + tap * p.tap_step;
-              if (!(sh >= 0 && sh + kTileM <= p.rows)) {
-                check_fail(p, abort_flag, 31, sh, tap, p.rows);
+              if (!__all_sync(0xffffffffu, sh >= 0 && sh + kTileM <= p.rows)) {
+                if (lane == 0) check_fail(p, abort_flag, 31, sh, tap, p.rows);
                 ok = false;
                 break;
               }
@@ -415,48 +486,103 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const uint64_t a_hi = a0 + ks * dA_k, a_lo = a_hi + dA_lo;
               const uint64_t b_hi = b0 + ks * dB_k, b_lo = b_hi + dB_lo;
               const uint32_t accum = (kb | tap | ks) ? 1u : 0u;
-              mma_bf16(d_tmem, a_hi, b_hi, idesc, accum);
-              mma_bf16(d_tmem, a_hi, b_lo, idesc, 1u);
-              mma_bf16(d_tmem, a_lo, b_hi, idesc, 1u);
+              if (PAIR) {
+                mma_bf16_pair_warp(d_tmem, a_hi, b_hi, idesc, accum);
+                mma_bf16_pair_warp(d_tmem, a_hi, b_lo, idesc, 1u);
+                mma_bf16_pair_warp(d_tmem, a_lo, b_hi, idesc, 1u);
+              } else {
+                mma_bf16_warp(d_tmem, a_hi, b_hi, idesc, accum);
+                mma_bf16_warp(d_tmem, a_hi, b_lo, idesc, 1u);
+                mma_bf16_warp(d_tmem, a_lo, b_hi, idesc, 1u);
+              }
             }
-            mma_commit(smem_u32(emptyB + sb));
+            commit(emptyB + sb);
             ++ib;
           }
           if (!ok) break;
-          mma_commit(smem_u32(emptyA + sa));
+          commit(emptyA + sa);
           ++ia;
         }
         if (!ok) break;
-        mma_commit(smem_u32(accFull + acc));
+        commit(accFull + acc);
       }
       if (!ok) {
-        atomicOr(p.err, ERR_TIMEOUT_MMA);
-        *abort_flag = 1;
+        if (lane == 0) {
+          atomicOr(p.err, ERR_TIMEOUT_MMA);
+          raise_abort();
+        }
         // wait until every MMA issued so far has finished reading shared memory
-        mma_commit(smem_u32(drain));
+        if (PAIR)
+          mma_commit_pair_warp(smem_u32(drain), 1);
+        else
+          mma_commit_warp(smem_u32(drain));
         const volatile int never = 0;
         mbar_wait(smem_u32(drain), 0u, p.timeout, &never);
       }
     }
-  } else if (warp == kSkipWarp) {
+  } else if (warp >= kBWarp) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ weight producer
+      // Stage ib goes to slot ib % nb (with several producer warps, nb is a multiple of
+      // their count and warp kBWarp + j fills the slots congruent to j).
+      const int j = warp - kBWarp;
+      int ib = 0, mine = 0;
+      bool ok = true;
+      for (int job = job0; job < total_jobs && ok; job += job_step) {
+        const int nt = job % p.n_tiles;
+        const int wt = PAIR ? 2 * nt + static_cast<int>(rank) : nt;  // packed weight tile
+        for (int kb = 0; kb < p.nkb && ok; ++kb) {
+          for (int tap = 0; tap < p.taps; ++tap, ++ib) {
+            if (ib % kBWarps != j) continue;
+            const int sb = ib % p.nb;
+            const uint32_t phb = static_cast<uint32_t>(ib / p.nb) & 1u;
+            if (!mbar_wait(smem_u32(emptyB + sb), phb ^ 1u, p.timeout, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(fullB + sb);
+            const size_t widx = ((size_t)wt * p.taps + tap) * p.nkb + kb;
+#ifdef VOC_CHECKS
+            if (!((long long)(widx + 1) * p.b_bytes <= p.w_bytes && (p.nb % kBWarps) == 0 &&
+                  smem_u32(smB + (size_t)(sb + 1) * p.b_bytes) <= smem_u32(smS))) {
+              check_fail(p, abort_flag, 22, widx, sb, p.w_bytes);
+              ok = false;
+              break;
+            }
+#endif
+            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(p.b_bytes));
+            bulk_load(smem_u32(smB + (size_t)sb * p.b_bytes), p.wB + widx * p.b_bytes,
+                      static_cast<uint32_t>(p.b_bytes), fb);
+            ++mine;
+          }
+        }
+      }
+      if (!ok) {
+        atomicOr(p.err, ERR_TIMEOUT_PRODUCER);
+        raise_abort();
+        // this warp's slots j, j + kBWarps, ... form a ring of nb / kBWarps slots
+        drain_ring_strided(fullB + j, p.nb / kBWarps, kBWarps, mine, p.timeout);
+      }
+    }
+  } else if (warp == kSkipWarp || warp == kSkipWarp + 1) {
     if (lane == 0 && p.skip) {
       // ------------------------------------------------------------ residual prefetch
       prefetch_tmap(&tmapS);
       // Chunk c of a tile is consumed by the epilogue half c & 1; each half has its own
-      // ring of ns/2 slots filled in that half's consumption order, so a slot is only ever
-      // waited on by one sequence of consumers, at most one fill ahead.
+      // ring of ns/2 slots, filled by its own warp in that half's consumption order, so a
+      // slot is only ever waited on by one sequence of consumers, at most one fill ahead.
       const uint32_t bytes = static_cast<uint32_t>(skip_slot_bytes(CW));
       const int nsh = p.ns / 2;
-      int cnt[2] = {0, 0};
+      const int h = warp - kSkipWarp;
+      int cnt = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-        const int nt = tile % p.n_tiles;
-        const int rest = tile / p.n_tiles;
+      for (int job = job0; job < total_jobs && ok; job += job_step) {
+        const int nt = job % p.n_tiles;
+        const int rest = job / p.n_tiles;
         const int mt = rest % p.m_tiles;
         const int b = rest / p.m_tiles;
-        for (int c = 0; c < n_chunks; ++c) {
-          const int h = c & 1;
-          const int k = cnt[h]++;
+        for (int c = h; c < n_chunks; c += 2) {
+          const int k = cnt++;
           const int slot = h * nsh + k % nsh;
           const uint32_t ph = static_cast<uint32_t>(k / nsh) & 1u;
           if (!mbar_wait(smem_u32(skipEmpty + slot), ph ^ 1u, p.timeout, abort_flag)) {
@@ -473,15 +599,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
 #endif
           mbar_arrive_expect_tx(fs, bytes);
-          tma_load_4d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, 0, mt * kTileM,
+          tma_load_4d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, 0, mt * kM + row0,
                       (nt * p.N_tile + c * CW) / 4, b);
         }
       }
       if (!ok) {
         atomicOr(p.err, ERR_TIMEOUT_SKIP);
-        *abort_flag = 1;
-        drain_ring(skipFull, nsh, cnt[0], p.timeout);
-        drain_ring(skipFull + nsh, nsh, cnt[1], p.timeout);
+        raise_abort();
+        drain_ring(skipFull + h * nsh, nsh, cnt, p.timeout);
       }
     }
   } else {
@@ -492,22 +617,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row_in_tile = quad * 32 + lane;
     const uint32_t sbase = smem_u32(smS);
     const int nsh = p.ns > 0 ? p.ns / 2 : 1;  // residual slots of this half's ring
+    // where this warp reports a free accumulator: this CTA's barrier, or the even CTA's
+    const uint32_t acc_empty0 = PAIR ? mapa_shared(smem_u32(accEmpty), 0u) : smem_u32(accEmpty);
     int kh = 0;                              // residual chunks this half has consumed
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
-      const int nt = tile % p.n_tiles;
-      const int rest = tile / p.n_tiles;
+    for (int job = job0; job < total_jobs && ok; job += job_step, ++it) {
+      const int nt = job % p.n_tiles;
+      const int rest = job / p.n_tiles;
       const int mt = rest % p.m_tiles;
       const int b = rest / p.m_tiles;
       const int acc = it % p.n_acc;
       const uint32_t phacc = static_cast<uint32_t>(it / p.n_acc) & 1u;
-      if (!mbar_wait(smem_u32(accFull + acc), phacc, p.timeout, abort_flag)) {
+      // decisions stay warp-uniform: tcgen05.ld is a warp-collective instruction
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(accFull + acc), phacc, p.timeout, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int t = mt * kTileM + row_in_tile;
+      const int t = mt * kM + row0 + row_in_tile;
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * p.acc_cols) +
                              (static_cast<uint32_t>(quad * 32) << 16);
       for (int c = half; c < n_chunks && ok; c += 2, ++kh) {
@@ -517,24 +645,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                 static_cast<uint32_t>(kh / nsh) & 1u, abort_flag, row_in_tile, b,
                                 t, nt * p.N_tile + c * CW, tbase + c * CW, sbase,
                                 smem_u32(bars));
+        ok = __all_sync(0xffffffffu, ok);
       }
-      if (!ok) break;
+      // every lane's TMEM reads of this accumulator are complete before lane 0 frees it
       tc_fence_before();
-      mbar_arrive(smem_u32(accEmpty + acc));
+      __syncwarp();
+      if (!ok) break;
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(acc * 8));
+        else
+          mbar_arrive(smem_u32(accEmpty + acc));
+      }
     }
     if (!ok) {
       atomicOr(p.err, ERR_TIMEOUT_EPILOGUE);
-      *abort_flag = 1;
+      raise_abort();
     }
   }
 
   __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();  // neither CTA leaves while the other may still reach its shared memory
+  else
+    __syncthreads();
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, tmem_cols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, tmem_cols);
+    else
+      tmem_dealloc(tmem_base, tmem_cols);
   }
 }
 

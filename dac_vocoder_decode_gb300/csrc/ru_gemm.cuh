@@ -62,7 +62,7 @@ __device__ __forceinline__ void ru_epilogue1(const ConvGemmArgs &p, const RuExtr
 }
 
 template <int CW>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kRuThreads, 1)
     ru_gemm_kernel(const __grid_constant__ CUtensorMap tmapA,
                    const __grid_constant__ CUtensorMap tmapS, const ConvGemmArgs p,
                    const RuExtra x) {
@@ -142,7 +142,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // ------------------------------------------------------------ A / weight producer
       prefetch_tmap(&tmapA);
       const uint32_t a_tx = 2u * kchunks * chunkA;
-      const int lo_chunk0 = p.Cp_in / 8;
       int ia = 0, ib = 0;
       bool ok = true;
       auto load_b = [&](const uint8_t *src) -> bool {
@@ -169,8 +168,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t fa = smem_u32(fullA + sa);
           const uint32_t dstA = smem_u32(smA + (size_t)sa * p.a_bytes);
           mbar_arrive_expect_tx(fa, a_tx);
-          tma_load_4d(dstA, &tmapA, fa, 0, y0, kb * kchunks, b);
-          tma_load_4d(dstA + kchunks * chunkA, &tmapA, fa, 0, y0, lo_chunk0 + kb * kchunks, b);
+          tma_load_5d(dstA, &tmapA, fa, 0, y0, kb * kchunks, 0, b);  // hi and lo chunks
           ++ia;
           for (int tap = 0; tap < p.taps && ok; ++tap)
             ok = load_b(p.wB + ((size_t)tap * p.nkb + kb) * p.b_bytes);
@@ -185,8 +183,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
+    {
+      // ------------------------------------------------------------ MMA issuer (whole warp)
+      // warp-uniform waits, one elected lane issues each MMA and commit
+      auto wait_all = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.timeout, abort_flag));
+      };
       const uint32_t idesc = idesc_bf16_f32(kTileM, p.N_tile);
       const uint64_t dA_lo = (uint64_t)((kchunks * chunkA) >> 4);
       const uint64_t dA_k = (uint64_t)((2 * chunkA) >> 4);
@@ -200,13 +202,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       auto wait_b = [&](uint64_t &b0) -> bool {
         const int sb = ib % p.nb;
         const uint32_t phb = static_cast<uint32_t>(ib / p.nb) & 1u;
-        if (!mbar_wait(smem_u32(fullB + sb), phb, p.timeout, abort_flag)) return false;
+        if (!wait_all(smem_u32(fullB + sb), phb)) return false;
         tc_fence_after();
         b0 = smem_desc(smem_u32(smB + (size_t)sb * p.b_bytes), chunkB, 128);
         return true;
       };
       auto release_b = [&]() {
-        mma_commit(smem_u32(emptyB + ib % p.nb));
+        mma_commit_warp(smem_u32(emptyB + ib % p.nb));
         ++ib;
       };
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d1 = tmem_base + static_cast<uint32_t>(2 * j * p.acc_cols);
         const uint32_t d2 = d1 + static_cast<uint32_t>(p.acc_cols);
         // conv1 (k taps, dilated) -> accumulator 1
-        if (!mbar_wait(smem_u32(acc1Empty + j), ph ^ 1u, p.timeout, abort_flag)) {
+        if (!wait_all(smem_u32(acc1Empty + j), ph ^ 1u)) {
           ok = false;
           break;
         }
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int kb = 0; kb < p.nkb && ok; ++kb) {
           const int sa = ia % p.na;
           const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;
-          if (!mbar_wait(smem_u32(fullA + sa), pha, p.timeout, abort_flag)) {
+          if (!wait_all(smem_u32(fullA + sa), pha)) {
             ok = false;
             break;
           }
@@ -241,21 +243,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const uint64_t a_hi = a0 + ks * dA_k, a_lo = a_hi + dA_lo;
               const uint64_t b_hi = b0 + ks * dB_k, b_lo = b_hi + dB_lo;
               const uint32_t accum = (kb | tap | ks) ? 1u : 0u;
-              mma_bf16(d1, a_hi, b_hi, idesc, accum);
-              mma_bf16(d1, a_hi, b_lo, idesc, 1u);
-              mma_bf16(d1, a_lo, b_hi, idesc, 1u);
+              mma_bf16_warp(d1, a_hi, b_hi, idesc, accum);
+              mma_bf16_warp(d1, a_hi, b_lo, idesc, 1u);
+              mma_bf16_warp(d1, a_lo, b_hi, idesc, 1u);
             }
             release_b();
           }
           if (!ok) break;
-          mma_commit(smem_u32(emptyA + sa));
+          mma_commit_warp(smem_u32(emptyA + sa));
           ++ia;
         }
         if (!ok) break;
-        mma_commit(smem_u32(acc1Full + j));
+        mma_commit_warp(smem_u32(acc1Full + j));
         // conv2 (1x1) on H -> accumulator 2, once the epilogue has written H
-        if (!mbar_wait(smem_u32(hFull), static_cast<uint32_t>(it) & 1u, p.timeout, abort_flag) ||
-            !mbar_wait(smem_u32(acc2Empty + j), ph ^ 1u, p.timeout, abort_flag)) {
+        if (!wait_all(smem_u32(hFull), static_cast<uint32_t>(it) & 1u) ||
+            !wait_all(smem_u32(acc2Empty + j), ph ^ 1u)) {
           ok = false;
           break;
         }
@@ -271,20 +273,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t a_hi = a0 + ks * dH_k, a_lo = a_hi + dH_lo;
             const uint64_t b_hi = b0 + ks * dB_k, b_lo = b_hi + dB_lo;
             const uint32_t accum = (kb | ks) ? 1u : 0u;
-            mma_bf16(d2, a_hi, b_hi, idesc, accum);
-            mma_bf16(d2, a_hi, b_lo, idesc, 1u);
-            mma_bf16(d2, a_lo, b_hi, idesc, 1u);
+            mma_bf16_warp(d2, a_hi, b_hi, idesc, accum);
+            mma_bf16_warp(d2, a_hi, b_lo, idesc, 1u);
+            mma_bf16_warp(d2, a_lo, b_hi, idesc, 1u);
           }
           release_b();
         }
         if (!ok) break;
-        mma_commit(smem_u32(acc2Full + j));
-        mma_commit(smem_u32(hEmpty));  // H may be rewritten once these MMAs have read it
+        mma_commit_warp(smem_u32(acc2Full + j));
+        mma_commit_warp(smem_u32(hEmpty));  // H may be rewritten once these MMAs have read it
       }
       if (!ok) {
-        atomicOr(p.err, ERR_TIMEOUT_MMA);
-        *abort_flag = 1;
-        mma_commit(smem_u32(drain));
+        if (lane == 0) {
+          atomicOr(p.err, ERR_TIMEOUT_MMA);
+          *abort_flag = 1;
+        }
+        mma_commit_warp(smem_u32(drain));
         const volatile int never = 0;
         mbar_wait(smem_u32(drain), 0u, p.timeout, &never);
       }

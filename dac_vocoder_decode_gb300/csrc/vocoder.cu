@@ -30,6 +30,7 @@ constexpr long long kWaitBudget = 4000000000LL;  // cycles (~2 s) before a wait 
 constexpr int kHeadTile = 128;
 // mbarriers (2 per A, weight and residual slot, 2 per accumulator, 1 drain), TMEM slot, flag
 constexpr int kBarrierBytes = 512;
+constexpr int kBStageMax = 36 * 1024;  // bytes of one weight stage (per CTA)
 
 thread_local std::string g_err;  // last error without a context
 
@@ -63,6 +64,8 @@ struct Layer {
   int in_buf = -1, f32_buf = -1, hl_buf = -1, skip_buf = -1;
   int epi_flags = 0;
   int cw = 32;              // epilogue column chunk (32, or 16 when 32 does not divide the tile)
+  bool pair = false;        // CTA-pair kernel: 256-row tiles, half of each weight tile per CTA
+  int max_clusters = 0;     // pair: co-resident 2-CTA clusters of this launch shape
   // fused residual unit (conv1 k-tap + conv2 1x1 in one kernel)
   bool ru = false;
   voc::RuExtra rx{};
@@ -91,10 +94,16 @@ bool set_kernel_attrs(std::string &why) {
   static cudaError_t st = cudaErrorUnknown;
   static std::once_flag once;
   std::call_once(once, [] {
-    st = cudaFuncSetAttribute(voc::conv_gemm_kernel<32>,
+    st = cudaFuncSetAttribute(voc::conv_gemm_kernel<32, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
-      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16>,
+      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<32, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::ru_gemm_kernel<32>,
@@ -126,6 +135,7 @@ struct vocoder {
   int *flag_dev = nullptr;  // finite-check flag
   long long wait_budget = kWaitBudget;
   int fuse_max_c = 0;       // residual units of up to this many (padded) channels run fused
+  bool use_pair = true;     // conv layers on CTA pairs
   // TMA descriptors for the last (workspace, B, T)
   void *map_ws = nullptr;
   int map_B = -1, map_T = -1;
@@ -209,37 +219,77 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     return false;
   }
   L.cw = (g.N_tile % 32 == 0 && L.Cp_out % 32 == 0) ? 32 : 16;
-  // channels per k-block: the largest multiple of 16 dividing Cp_in that keeps a weight
-  // stage within 36 KB and an A stage within 72 KB (fewer, longer pipeline stages)
-  g.KB = 16;
-  for (int kb = 16; kb <= L.Cp_in; kb += 16)
-    if (L.Cp_in % kb == 0 && 4 * kb * g.N_tile <= 36 * 1024 && 4 * kb * g.rows <= 72 * 1024)
-      g.KB = kb;
-  g.nkb = L.Cp_in / g.KB;
+  // weight columns staged per CTA: the whole tile, or (CTA pair) one half of it
+  const int n_stage = L.pair ? g.N_tile / 2 : g.N_tile;
+  // Channels per k-block: the largest multiple of 16 dividing Cp_in whose weight stage
+  // stays within kBStageMax and A stage within 72 KB and that still leaves two weight
+  // slots.  Each stage costs a copy request and a barrier round trip whatever its size,
+  // so fewer, larger stages run faster.
   const int chunkA = g.rows * 16;
-  g.a_bytes = rup(2 * (g.KB / 8) * chunkA, 1024);
-  g.b_bytes = 4 * g.KB * g.N_tile;
-  g.na = 2;
-  // residual slots (layers with a skip input): as many as leave >= 3 weight stages, 2..4
-  g.ns = 0;
-  int avail = kSmemMax - 1024 - kBarrierBytes - g.na * g.a_bytes;
-  if (has_skip) {  // two rings (one per epilogue half) of 1 or 2 slots each
-    const int sb = voc::skip_slot_bytes(L.cw);
-    g.ns = 4;
-    if ((avail - g.ns * sb) / g.b_bytes < 3) g.ns = 2;
-    avail -= g.ns * sb;
+  const int sb = has_skip ? voc::skip_slot_bytes(L.cw) : 0;
+  g.KB = 0;
+  for (int kb = L.Cp_in - L.Cp_in % 16; kb >= 16 && !g.KB; kb -= 16) {
+    if (L.Cp_in % kb || 4 * kb * n_stage > kBStageMax || 4 * kb * g.rows > 72 * 1024) continue;
+    const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
+    const int b_bytes = 4 * kb * n_stage;
+    int avail = kSmemMax - 1024 - kBarrierBytes - 2 * a_bytes;
+    int ns = 0;
+    if (has_skip) {  // two rings (one per epilogue half) of 1 or 2 slots each
+      ns = ((avail - 4 * sb) / b_bytes >= 3) ? 4 : 2;
+      avail -= ns * sb;
+    }
+    int nb = std::min(8, avail / b_bytes);
+    nb -= nb % voc::kBWarps;  // each weight-producer warp owns every kBWarps-th slot
+    if (nb < 2) continue;
+    g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = b_bytes, g.nb = nb, g.ns = ns, g.na = 2;
   }
-  g.nb = std::min(8, avail / g.b_bytes);
-  if (g.nb < 2) {
+  if (!g.KB) {
     why = "shared memory plan does not fit";
     return false;
   }
+  g.nkb = L.Cp_in / g.KB;
   int ac = 32;
   while (ac < g.N_tile) ac *= 2;
   g.acc_cols = ac;
   g.n_acc = std::min(voc::kMaxAcc, 512 / ac);
   L.smem = 1024 + (size_t)g.na * g.a_bytes + (size_t)g.nb * g.b_bytes +
            (size_t)g.ns * voc::skip_slot_bytes(L.cw) + kBarrierBytes;
+  return true;
+}
+
+// Resident 2-CTA clusters of a pair layer's launch shape (0: none fit, or the query failed).
+int pair_clusters(const Layer &L) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2, attr[0].val.clusterDim.y = 1, attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(voc::kGemmThreads);
+  cfg.dynamicSmemBytes = L.smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const cudaError_t e =
+      (L.cw == 32) ? cudaOccupancyMaxActiveClusters(&n, voc::conv_gemm_kernel<32, true>, &cfg)
+                   : cudaOccupancyMaxActiveClusters(&n, voc::conv_gemm_kernel<16, true>, &cfg);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// plan_gemm, on CTA pairs when `pair` is set and a pair launch of the layer fits the device
+bool plan_layer(bool pair, Layer &L, int padding, bool has_skip, std::string &why) {
+  L.pair = pair;
+  if (!plan_gemm(L, padding, has_skip, why)) return false;
+  if (L.pair) {
+    L.max_clusters = pair_clusters(L);
+    if (L.max_clusters < 1) {
+      L.pair = false;
+      return plan_gemm(L, padding, has_skip, why);
+    }
+  }
   return true;
 }
 
@@ -319,23 +369,27 @@ float weight_value(const Layer &L, int padding, const float *w, int n, int ci, i
   return w[((size_t)ci * L.Cout + co) * (2 * s) + k];
 }
 
+// Weight tiles as the kernel stages them: [tile][tap][kb][hi|lo][chunk][n][8] with tiles of
+// `pw` columns (N_tile, or N_tile / 2 for the CTA pair: CTA r of a pair stages tile 2 nt + r).
 std::vector<uint16_t> pack_weights(const Layer &L, int padding, const float *w) {
   const ConvGemmArgs &g = L.g;
-  const size_t tile = (size_t)2 * g.KB * g.N_tile;
-  std::vector<uint16_t> out((size_t)g.n_tiles * g.taps * g.nkb * tile);
-  for (int nt = 0; nt < g.n_tiles; ++nt)
+  const int pw = L.pair ? g.N_tile / 2 : g.N_tile;
+  const int n_pt = g.N_total / pw;
+  const size_t tile = (size_t)2 * g.KB * pw;
+  std::vector<uint16_t> out((size_t)n_pt * g.taps * g.nkb * tile);
+  for (int nt = 0; nt < n_pt; ++nt)
     for (int tap = 0; tap < g.taps; ++tap)
       for (int kb = 0; kb < g.nkb; ++kb) {
         uint16_t *base = out.data() + (((size_t)nt * g.taps + tap) * g.nkb + kb) * tile;
         for (int c = 0; c < g.KB / 8; ++c)
-          for (int n = 0; n < g.N_tile; ++n)
+          for (int n = 0; n < pw; ++n)
             for (int e = 0; e < 8; ++e) {
-              const float v = weight_value(L, padding, w, nt * g.N_tile + n, kb * g.KB + c * 8 + e, tap);
+              const float v = weight_value(L, padding, w, nt * pw + n, kb * g.KB + c * 8 + e, tap);
               const uint16_t hi = f2bf(v);
               const uint16_t lo = f2bf(v - bf2f(hi));
-              const size_t idx = ((size_t)c * g.N_tile + n) * 8 + e;
+              const size_t idx = ((size_t)c * pw + n) * 8 + e;
               base[idx] = hi;
-              base[(size_t)g.KB * g.N_tile + idx] = lo;
+              base[(size_t)g.KB * pw + idx] = lo;
             }
       }
   return out;
@@ -424,6 +478,7 @@ bool check_desc(const voc_desc *d, std::string &why) {
   if (d->out_channels != 1) return why = "out_channels must be 1", false;
   if (d->padding != VOC_PAD_SYMMETRIC && d->padding != VOC_PAD_CAUSAL) return why = "padding", false;
   if (d->precision != VOC_PREC_BF16X3) return why = "precision", false;
+  if (d->cta_pair < -1 || d->cta_pair > 1) return why = "cta_pair must be -1, 0 or 1", false;
   for (int i = 0; i < d->n_stages; ++i) {
     if (d->strides[i] < 1 || d->strides[i] > 16) return why = "stride out of [1, 16]", false;
     if (d->padding == VOC_PAD_SYMMETRIC && d->strides[i] % 2)
@@ -469,11 +524,13 @@ voc_status encode_map(vocoder *ctx, CUtensorMap *map, const void *base, int Cp, 
                       int rows, int kchunks) {
   auto enc = encode_fn();
   if (!enc) return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled entry point unavailable");
-  const cuuint64_t dims[4] = {8u, (cuuint64_t)L, (cuuint64_t)(2 * Cp / 8), (cuuint64_t)B};
-  const cuuint64_t strides[3] = {16u, 16u * (cuuint64_t)L, 16u * (cuuint64_t)L * (2 * Cp / 8)};
-  const cuuint32_t box[4] = {8u, (cuuint32_t)rows, (cuuint32_t)kchunks, 1u};
-  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+  // [B][hi|lo][Cp/8][L][8]: one box covers `kchunks` chunks of both planes
+  const cuuint64_t dims[5] = {8u, (cuuint64_t)L, (cuuint64_t)(Cp / 8), 2u, (cuuint64_t)B};
+  const cuuint64_t strides[4] = {16u, 16u * (cuuint64_t)L, 16u * (cuuint64_t)L * (Cp / 8),
+                                 16u * (cuuint64_t)L * (2 * Cp / 8)};
+  const cuuint32_t box[5] = {8u, (cuuint32_t)rows, (cuuint32_t)kchunks, 2u, 1u};
+  const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -505,7 +562,8 @@ void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *co
   const long long L_in = level_len(ctx, L.level, T);
   a.B = B;
   a.L_in = static_cast<int>(L_in);
-  a.m_tiles = static_cast<int>((L_in + voc::kTileM - 1) / voc::kTileM);
+  const int kM = L.pair ? 2 * voc::kTileM : voc::kTileM;  // rows of one tile job
+  a.m_tiles = static_cast<int>((L_in + kM - 1) / kM);
   a.wB = L.w_dev;
   a.bias = L.bias_dev;
   a.alpha = L.alpha_dev;
@@ -518,7 +576,7 @@ void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *co
   a.err = ctx->err_dev;
   a.f32_elems = L.f32_buf >= 0 ? (long long)(bbytes / 4) : 0;
   a.hl_elems = L.hl_buf >= 0 ? (long long)(bbytes / 2) : 0;
-  a.w_bytes = (long long)L.g.n_tiles * L.g.taps * L.g.nkb * L.g.b_bytes;
+  a.w_bytes = (long long)L.g.n_tiles * (L.pair ? 2 : 1) * L.g.taps * L.g.nkb * L.g.b_bytes;
   a.smem_bytes = static_cast<int>(L.smem);
   a.L_a = static_cast<int>(L_in);
   a.chunks_a = 2 * L.Cp_in / 8;
@@ -549,7 +607,8 @@ void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops,
   flops = L.convT ? 4.0 * L.Cin * L.Cout * B * L_out : 2.0 * L.Cin * L.Cout * L.K * B * L_in;
   if (L.ru) flops = 2.0 * L.Cin * L.Cout * (L.K + 1) * B * L_in;
   const ConvGemmArgs &g = L.g;
-  double by = 4.0 * B * L_in * L.Cp_in + (double)g.n_tiles * (g.taps + (L.ru ? 1 : 0)) * g.nkb * g.b_bytes;
+  double by = 4.0 * B * L_in * L.Cp_in +
+              (double)g.n_tiles * (L.pair ? 2 : 1) * (g.taps + (L.ru ? 1 : 0)) * g.nkb * g.b_bytes;
   const double out_elems = (double)B * L_out * L.Cp_out;
   if (L.skip_buf >= 0) by += 4.0 * out_elems;
   if (L.f32_buf >= 0) by += 4.0 * out_elems;
@@ -560,16 +619,33 @@ void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops,
 voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
                        const CUtensorMap &smap, const ConvGemmArgs &a, cudaStream_t stream) {
   const long long tiles = (long long)a.B * a.m_tiles * a.n_tiles;
+  if (L.pair) {  // persistent grid of 2-CTA clusters, at most as many as can be resident
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2, attr[0].val.clusterDim.y = 1, attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min<long long>(tiles, L.max_clusters)));
+    cfg.blockDim = dim3(voc::kGemmThreads);
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = (L.cw == 32)
+                        ? cudaLaunchKernelEx(&cfg, voc::conv_gemm_kernel<32, true>, map, smap, a)
+                        : cudaLaunchKernelEx(&cfg, voc::conv_gemm_kernel<16, true>, map, smap, a);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, ("launch " + L.name).c_str());
+    return VOC_OK;
+  }
   const int grid = static_cast<int>(std::min<long long>(tiles, ctx->num_sms));
   if (L.ru) {
     if (L.cw == 32)
-      voc::ru_gemm_kernel<32><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a, L.rx);
+      voc::ru_gemm_kernel<32><<<grid, voc::kRuThreads, L.smem, stream>>>(map, smap, a, L.rx);
     else
-      voc::ru_gemm_kernel<16><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a, L.rx);
+      voc::ru_gemm_kernel<16><<<grid, voc::kRuThreads, L.smem, stream>>>(map, smap, a, L.rx);
   } else if (L.cw == 32) {
-    voc::conv_gemm_kernel<32><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
+    voc::conv_gemm_kernel<32, false><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
   } else {
-    voc::conv_gemm_kernel<16><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
+    voc::conv_gemm_kernel<16, false><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, ("launch " + L.name).c_str());
@@ -713,6 +789,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
   ctx->Cp_lat = rup(desc->latent_channels, 16);
   ctx->fuse_max_c = desc->fuse_max_channels == 0 ? kFuseDefault
                     : (desc->fuse_max_channels < 0 ? 0 : desc->fuse_max_channels);
+  ctx->use_pair = desc->cta_pair > 0;
   auto bail = [&](voc_status st) {
     g_err = ctx->err;
     vocoder_destroy(ctx);
@@ -743,7 +820,8 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     L.name = "conv_in";
     L.Cin = desc->latent_channels, L.Cout = desc->channels0, L.K = desc->in_kernel, L.dil = 1;
     L.level = 0;
-    if (!plan_gemm(L, pad, false, why)) return bail(fail(ctx, VOC_UNSUPPORTED, "conv_in: " + why));
+    if (!plan_layer(ctx->use_pair, L, pad, false, why))
+      return bail(fail(ctx, VOC_UNSUPPORTED, "conv_in: " + why));
     L.in_buf = BUF_H0, L.hl_buf = BUF_H1;
     st = upload_layer(ctx, ctx->allocs, L, pad, params[0], params[1], params[2]);
     if (st != VOC_OK) return bail(st);
@@ -770,7 +848,8 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       L.convT = true;
       L.Cin = C, L.Cout = Co, L.stride = ctx->strides[i], L.K = 2 * L.stride;
       L.level = i;
-      if (!plan_gemm(L, pad, false, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L.name + ": " + why));
+      if (!plan_layer(ctx->use_pair, L, pad, false, why))
+        return bail(fail(ctx, VOC_UNSUPPORTED, L.name + ": " + why));
       L.in_buf = x_buf, L.f32_buf = BUF_FY, L.hl_buf = cur;
       st = upload_layer(ctx, ctx->allocs, L, pad, params[p + 1], params[p + 2], params[p + 3]);
       if (st != VOC_OK) return bail(st);
@@ -809,7 +888,8 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       L1.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".conv1";
       L1.Cin = C, L1.Cout = C, L1.K = desc->res_kernel, L1.dil = ctx->dils[j];
       L1.level = i + 1;
-      if (!plan_gemm(L1, pad, false, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L1.name + ": " + why));
+      if (!plan_layer(ctx->use_pair, L1, pad, false, why))
+        return bail(fail(ctx, VOC_UNSUPPORTED, L1.name + ": " + why));
       L1.in_buf = cur, L1.hl_buf = tmp;
       st = upload_layer(ctx, ctx->allocs, L1, pad, w1, b1, a2);
       if (st != VOC_OK) return bail(st);
@@ -819,7 +899,8 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       L2.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".conv2";
       L2.Cin = C, L2.Cout = C, L2.K = 1, L2.dil = 1;
       L2.level = i + 1;
-      if (!plan_gemm(L2, pad, true, why)) return bail(fail(ctx, VOC_UNSUPPORTED, L2.name + ": " + why));
+      if (!plan_layer(ctx->use_pair, L2, pad, true, why))
+        return bail(fail(ctx, VOC_UNSUPPORTED, L2.name + ": " + why));
       L2.in_buf = tmp, L2.skip_buf = BUF_FY;
       if (j < nd - 1) {
         L2.f32_buf = BUF_FY, L2.hl_buf = cur;
@@ -1126,7 +1207,7 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
                     const float *b_host, const float *alpha_host, float *y_dev, cudaStream_t stream) {
   std::string why;
   if (!set_kernel_attrs(why)) return fail(nullptr, VOC_CUDA_ERROR, why);
-  if (!plan_gemm(L, padding, false, why)) return fail(nullptr, VOC_UNSUPPORTED, why);
+  if (!plan_layer(false, L, padding, false, why)) return fail(nullptr, VOC_UNSUPPORTED, why);
   int dev = 0, sms = 0, major = 0, minor = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1291,7 +1372,7 @@ VOC_API voc_status vocoder_op_residual_unit(const float *x_dev, int B, int C, in
     L1.name = "op_conv1", L2.name = "op_conv2";
     L1.Cin = L1.Cout = L2.Cin = L2.Cout = C;
     L1.K = K, L1.dil = dil, L2.K = 1, L2.dil = 1;
-    if (!plan_gemm(L1, padding, false, why) || !plan_gemm(L2, padding, true, why))
+    if (!plan_layer(false, L1, padding, false, why) || !plan_layer(false, L2, padding, true, why))
       return done(fail(&tmp, VOC_UNSUPPORTED, why));
     L1.in_buf = BUF_H0, L1.hl_buf = BUF_HB;
     L2.in_buf = BUF_HB, L2.skip_buf = BUF_FY, L2.f32_buf = BUF_FY;

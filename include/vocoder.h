@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define VOC_ABI_VERSION 2
+#define VOC_ABI_VERSION 3
 
 typedef struct vocoder vocoder_t;             /* opaque context */
 typedef struct CUstream_st *voc_stream_t;     /* a cudaStream_t */
@@ -94,6 +94,10 @@ typedef struct {
                            kernel (conv1 result kept on chip); 0 = library default,
                            -1 = never.  A performance choice only: results agree
                            within the decode tolerance either way.              */
+  int cta_pair;         /* conv layers run on CTA pairs (2-CTA clusters sharing one
+                           256-row MMA, each SM staging half of the weights):
+                           0 = library default (off), 1 = on, -1 = off.  A
+                           performance choice only, like fuse_max_channels.     */
 } voc_desc;
 
 /* ABI version of the library (VOC_ABI_VERSION of the build). */

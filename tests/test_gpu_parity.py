@@ -230,10 +230,24 @@ def test_decode_fusion_variants(arch, fuse):
     G.compare_audio(ref, got, f"fuse={fuse}")
 
 
-def _sampled_full_size(name, n_items=None, width=8, n=3):
+@pytest.mark.parametrize("arch", [MID_MUSIC, MID_SPEECH], ids=["music", "speech_causal"])
+def test_decode_cta_pair(arch):
+    """Every tensor-core layer on 2-CTA clusters (one 256-row MMA per pair, each CTA staging
+    half of the weights) over several waves, checked sample by sample against the oracle,
+    and against the single-CTA decode of the same input."""
+    wl = W.make_custom(arch, B=2, T=60, seed=72)
+    pair = V.Vocoder(arch, V.fold_params(wl.params), cta_pair=1)
+    single = V.Vocoder(arch, V.fold_params(wl.params), cta_pair=-1)
+    got = G.gpu_decode(pair, wl.latent)
+    ref = O.decode(arch, wl.params, wl.latent)
+    G.compare_audio(ref, got, "cta_pair=1")
+    G.compare_audio(G.gpu_decode(single, wl.latent), got, "pair vs single")
+
+
+def _sampled_full_size(name, n_items=None, width=8, n=3, cta_pair=0):
     wl = G.workload(name)
     folded = G.oracle_folded(name)
-    voc = G.gpu_decoder(wl)
+    voc = V.Vocoder(wl.arch, V.fold_params(wl.params), cta_pair=cta_pair)
     got = G.gpu_decode(voc, wl.latent)
     hop = wl.arch.hop
     assert got.shape == (wl.B, wl.T * hop)
@@ -250,6 +264,10 @@ def _sampled_full_size(name, n_items=None, width=8, n=3):
 
 def test_decode_music_window_sampled():
     _sampled_full_size("music_window")
+
+
+def test_decode_music_window_sampled_cta_pair():
+    _sampled_full_size("music_window", cta_pair=1)
 
 
 def test_decode_speech_sampled():
