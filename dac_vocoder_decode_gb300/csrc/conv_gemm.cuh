@@ -87,6 +87,8 @@ struct ConvGemmArgs {
   __nv_bfloat16 *out_hl;   // hi/lo output, chunk-major [B][2*Cp_out/8][L_in*s_rows][8], or null
   int Cp_out, s_rows;      // output channels (padded), output rows per D row
   int flags;
+  int b_resident;          // 1: the nb = taps * nkb weight slots hold this CTA's whole column
+                           // tile, loaded once (every CTA keeps one column tile)
   long long timeout;       // cycles a wait may take before the kernel gives up
   int *err;                // device error word
   // extents used by the self-checking build (VOC_CHECKS)
@@ -391,6 +393,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int ia = 0, ib = 0;
       bool ok = true;
       for (int job = job0; job < total_jobs && ok; job += job_step) {
+        const bool relay_b = !p.b_resident || job == job0;  // resident slots land once
         for (int kb = 0; kb < p.nkb && ok; ++kb) {
           const int sa = ia % p.na;
           if (!mbar_wait(smem_u32(fullA + sa), static_cast<uint32_t>(ia / p.na) & 1u, p.timeout,
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           mbar_arrive_cluster(remA + static_cast<uint32_t>(sa * 8));
           ++ia;
-          for (int tap = 0; tap < p.taps; ++tap) {
+          for (int tap = 0; tap < p.taps && relay_b; ++tap) {
             const int sb = ib % p.nb;
             if (!mbar_wait(smem_u32(fullB + sb), static_cast<uint32_t>(ib / p.nb) & 1u,
                            p.timeout, abort_flag)) {
@@ -432,39 +435,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mma_commit_warp(smem_u32(bar));
       };
       const uint32_t idesc = idesc_bf16_f32(kM, p.N_tile);
-      // descriptor increments: +1 in the start-address field is +16 bytes
-      const uint64_t dA_lo = (uint64_t)((kchunks * chunkA) >> 4);
-      const uint64_t dA_k = (uint64_t)((2 * chunkA) >> 4);
-      const uint64_t dB_lo = (uint64_t)((kchunks * chunkB) >> 4);
-      const uint64_t dB_k = (uint64_t)((2 * chunkB) >> 4);
-      int ia = 0, ib = 0, it = 0;
+      // Descriptor low words step by 16-byte units: +1 is +16 bytes of start address.  The
+      // ring positions (slot, phase) advance incrementally: this loop is issue-bound, so it
+      // avoids divisions by run-time ring sizes.
+      const uint32_t dA_lo = (kchunks * chunkA) >> 4;
+      const uint32_t dA_k = (2 * chunkA) >> 4;
+      const uint32_t dB_lo = (kchunks * chunkB) >> 4;
+      const uint32_t dB_k = (2 * chunkB) >> 4;
+      const uint32_t desc_hi = static_cast<uint32_t>(smem_desc(0u, 0u, 128) >> 32);
+      const uint32_t a_desc0 = static_cast<uint32_t>(smem_desc(smem_u32(smA), chunkA, 128));
+      const uint32_t b_desc0 = static_cast<uint32_t>(smem_desc(smem_u32(smB), chunkB, 128));
+      const uint32_t a_slot_step = static_cast<uint32_t>(p.a_bytes) >> 4;
+      const uint32_t b_slot_step = static_cast<uint32_t>(p.b_bytes) >> 4;
+      const int nks = kchunks / 2;
+      int sa = 0, sb = 0, acc = 0;
+      uint32_t pha = 0, phb = 0, phacc = 0;
       bool ok = true;
-      for (int job = job0; job < total_jobs && ok; job += job_step, ++it) {
+      for (int job = job0; job < total_jobs && ok; job += job_step) {
         const int nt = job % p.n_tiles;
         const int shift0 = (nt >= p.q_split_tile) ? p.shift0_q1 : p.shift0_q0;
-        const int acc = it % p.n_acc;
-        const uint32_t phacc = static_cast<uint32_t>(it / p.n_acc) & 1u;
         if (!wait_all(smem_u32(accEmpty + acc), phacc ^ 1u, PAIR)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.acc_cols);
+        uint32_t accum = 0u;  // the first MMA of a job overwrites the accumulator
         for (int kb = 0; kb < p.nkb && ok; ++kb) {
-          const int sa = ia % p.na;
-          const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;
           if (!wait_all(smem_u32(fullA + sa), pha, false) ||
               (PAIR && !wait_all(smem_u32(pairA + sa), pha, true))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t aBase = smem_u32(smA + (size_t)sa * p.a_bytes);
-          for (int tap = 0; tap < p.taps; ++tap) {
-            const int sb = ib % p.nb;
-            const uint32_t phb = static_cast<uint32_t>(ib / p.nb) & 1u;
-            if (!wait_all(smem_u32(fullB + sb), phb, false) ||
-                (PAIR && !wait_all(smem_u32(pairB + sb), phb, true))) {
+          uint32_t a0 = a_desc0 + sa * a_slot_step + static_cast<uint32_t>(shift0);
+          for (int tap = 0; tap < p.taps; ++tap, a0 += static_cast<uint32_t>(p.tap_step)) {
+            // a resident slot completes its first phase only
+            const uint32_t wph = p.b_resident ? 0u : phb;
+            if (!wait_all(smem_u32(fullB + sb), wph, false) ||
+                (PAIR && !wait_all(smem_u32(pairB + sb), wph, true))) {
               ok = false;
               break;
             }
@@ -479,32 +488,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               }
             }
 #endif
-            const uint64_t a0 = smem_desc(
-                aBase + static_cast<uint32_t>(shift0 + tap * p.tap_step) * 16u, chunkA, 128);
-            const uint64_t b0 = smem_desc(smem_u32(smB + (size_t)sb * p.b_bytes), chunkB, 128);
-            for (int ks = 0; ks < kchunks / 2; ++ks) {
-              const uint64_t a_hi = a0 + ks * dA_k, a_lo = a_hi + dA_lo;
-              const uint64_t b_hi = b0 + ks * dB_k, b_lo = b_hi + dB_lo;
-              const uint32_t accum = (kb | tap | ks) ? 1u : 0u;
-              if (PAIR) {
-                mma_bf16_pair_warp(d_tmem, a_hi, b_hi, idesc, accum);
-                mma_bf16_pair_warp(d_tmem, a_hi, b_lo, idesc, 1u);
-                mma_bf16_pair_warp(d_tmem, a_lo, b_hi, idesc, 1u);
-              } else {
-                mma_bf16_warp(d_tmem, a_hi, b_hi, idesc, accum);
-                mma_bf16_warp(d_tmem, a_hi, b_lo, idesc, 1u);
-                mma_bf16_warp(d_tmem, a_lo, b_hi, idesc, 1u);
-              }
+            uint32_t a_hi = a0, b_hi = b_desc0 + sb * b_slot_step;
+            for (int ks = 0; ks < nks; ++ks, a_hi += dA_k, b_hi += dB_k) {
+              mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi, desc_hi, idesc, accum);
+              mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi + dB_lo, desc_hi, idesc, 1u);
+              mma_bf16_warp_lo<PAIR>(d_tmem, a_hi + dA_lo, b_hi, desc_hi, idesc, 1u);
+              accum = 1u;
             }
-            commit(emptyB + sb);
-            ++ib;
+            if (!p.b_resident) commit(emptyB + sb);
+            if (++sb == p.nb) sb = 0, phb ^= 1u;
           }
           if (!ok) break;
           commit(emptyA + sa);
-          ++ia;
+          if (++sa == p.na) sa = 0, pha ^= 1u;
         }
         if (!ok) break;
         commit(accFull + acc);
+        if (++acc == p.n_acc) acc = 0, phacc ^= 1u;
       }
       if (!ok) {
         if (lane == 0) {
@@ -528,7 +528,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int j = warp - kBWarp;
       int ib = 0, mine = 0;
       bool ok = true;
-      for (int job = job0; job < total_jobs && ok; job += job_step) {
+      // resident weights: one pass over the stages of the first job fills every slot
+      const int job_end = p.b_resident ? min(total_jobs, job0 + 1) : total_jobs;
+      for (int job = job0; job < job_end && ok; job += job_step) {
         const int nt = job % p.n_tiles;
         const int wt = PAIR ? 2 * nt + static_cast<int>(rank) : nt;  // packed weight tile
         for (int kb = 0; kb < p.nkb && ok; ++kb) {
@@ -619,16 +621,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int nsh = p.ns > 0 ? p.ns / 2 : 1;  // residual slots of this half's ring
     // where this warp reports a free accumulator: this CTA's barrier, or the even CTA's
     const uint32_t acc_empty0 = PAIR ? mapa_shared(smem_u32(accEmpty), 0u) : smem_u32(accEmpty);
-    int kh = 0;                              // residual chunks this half has consumed
-    int it = 0;
+    int kslot = 0;                           // this half's residual ring position
+    uint32_t kph = 0;
+    int acc = 0;                             // accumulator ring position
+    uint32_t phacc = 0;
     bool ok = true;
-    for (int job = job0; job < total_jobs && ok; job += job_step, ++it) {
+    for (int job = job0; job < total_jobs && ok; job += job_step) {
       const int nt = job % p.n_tiles;
       const int rest = job / p.n_tiles;
       const int mt = rest % p.m_tiles;
       const int b = rest / p.m_tiles;
-      const int acc = it % p.n_acc;
-      const uint32_t phacc = static_cast<uint32_t>(it / p.n_acc) & 1u;
       // decisions stay warp-uniform: tcgen05.ld is a warp-collective instruction
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(accFull + acc), phacc, p.timeout, abort_flag))) {
         ok = false;
@@ -638,14 +640,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int t = mt * kM + row0 + row_in_tile;
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * p.acc_cols) +
                              (static_cast<uint32_t>(quad * 32) << 16);
-      for (int c = half; c < n_chunks && ok; c += 2, ++kh) {
-        const int slot = half * nsh + kh % nsh;
+      for (int c = half; c < n_chunks && ok; c += 2) {
+        const int slot = half * nsh + kslot;
         ok = epilogue_chunk<CW>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
-                                smem_u32(skipFull + slot), smem_u32(skipEmpty + slot),
-                                static_cast<uint32_t>(kh / nsh) & 1u, abort_flag, row_in_tile, b,
-                                t, nt * p.N_tile + c * CW, tbase + c * CW, sbase,
-                                smem_u32(bars));
+                                smem_u32(skipFull + slot), smem_u32(skipEmpty + slot), kph,
+                                abort_flag, row_in_tile, b, t, nt * p.N_tile + c * CW,
+                                tbase + c * CW, sbase, smem_u32(bars));
         ok = __all_sync(0xffffffffu, ok);
+        if (++kslot == nsh) kslot = 0, kph ^= 1u;
       }
       // every lane's TMEM reads of this accumulator are complete before lane 0 frees it
       tc_fence_before();
@@ -657,6 +659,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else
           mbar_arrive(smem_u32(accEmpty + acc));
       }
+      if (++acc == p.n_acc) acc = 0, phacc ^= 1u;
     }
     if (!ok) {
       atomicOr(p.err, ERR_TIMEOUT_EPILOGUE);

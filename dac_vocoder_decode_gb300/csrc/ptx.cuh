@@ -270,6 +270,36 @@ __device__ __forceinline__ void mma_bf16_pair_warp(uint32_t d_tmem, uint64_t ade
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// As mma_bf16_warp / mma_bf16_pair_warp with the two shared-memory descriptors given as
+// their low words and one common high word (stride field and version bit, equal for A
+// and B).  The start-address field (bits 0..13) of a shared-memory descriptor never
+// carries into the leading-byte-offset field for offsets inside the 227 KB window, so
+// the low words can be stepped with 32-bit adds.
+template <bool PAIR>
+__device__ __forceinline__ void mma_bf16_warp_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                                 uint32_t desc_hi, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  if (PAIR)
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %3};\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %3};\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -290,7 +320,10 @@ __device__ __forceinline__ void mma_commit_pair_warp(uint32_t bar, uint16_t cta_
 
 // 32 lanes x 16 consecutive 32-bit columns; thread i of the warp gets lane
 // (warp quadrant base + i).  Load and wait in one asm block so that no use of
-// the registers can be scheduled before the data has arrived.
+// the registers can be scheduled before the data has arrived.  No memory clobber:
+// the load touches no memory the compiler tracks, and the compiler may then issue
+// independent global or shared loads ahead of it; as a volatile asm it keeps its
+// place among the barrier and fence instructions.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
@@ -300,8 +333,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
+      : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -319,8 +351,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
+      : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }

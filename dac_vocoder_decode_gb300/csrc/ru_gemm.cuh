@@ -197,23 +197,22 @@ __global__ void __launch_bounds__(kRuThreads, 1)
       const uint64_t dH_lo = (uint64_t)(((p.Cp_out / 8) * chunkH) >> 4);
       const uint64_t dH_k = (uint64_t)((2 * chunkH) >> 4);
       const uint64_t h0 = smem_desc(smem_u32(smH), chunkH, 128);
-      int ia = 0, ib = 0, it = 0;
+      // ring positions advance incrementally (no divisions in the issue loop)
+      int sa = 0, sb = 0, j = 0;
+      uint32_t pha = 0, phb = 0, ph = 0;
+      int it = 0;
       bool ok = true;
       auto wait_b = [&](uint64_t &b0) -> bool {
-        const int sb = ib % p.nb;
-        const uint32_t phb = static_cast<uint32_t>(ib / p.nb) & 1u;
         if (!wait_all(smem_u32(fullB + sb), phb)) return false;
         tc_fence_after();
         b0 = smem_desc(smem_u32(smB + (size_t)sb * p.b_bytes), chunkB, 128);
         return true;
       };
       auto release_b = [&]() {
-        mma_commit_warp(smem_u32(emptyB + ib % p.nb));
-        ++ib;
+        mma_commit_warp(smem_u32(emptyB + sb));
+        if (++sb == p.nb) sb = 0, phb ^= 1u;
       };
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
-        const int j = it % x.n_buf;
-        const uint32_t ph = static_cast<uint32_t>(it / x.n_buf) & 1u;
         const uint32_t d1 = tmem_base + static_cast<uint32_t>(2 * j * p.acc_cols);
         const uint32_t d2 = d1 + static_cast<uint32_t>(p.acc_cols);
         // conv1 (k taps, dilated) -> accumulator 1
@@ -223,8 +222,6 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         }
         tc_fence_after();
         for (int kb = 0; kb < p.nkb && ok; ++kb) {
-          const int sa = ia % p.na;
-          const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;
           if (!wait_all(smem_u32(fullA + sa), pha)) {
             ok = false;
             break;
@@ -251,7 +248,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
           }
           if (!ok) break;
           mma_commit_warp(smem_u32(emptyA + sa));
-          ++ia;
+          if (++sa == p.na) sa = 0, pha ^= 1u;
         }
         if (!ok) break;
         mma_commit_warp(smem_u32(acc1Full + j));
@@ -282,6 +279,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         if (!ok) break;
         mma_commit_warp(smem_u32(acc2Full + j));
         mma_commit_warp(smem_u32(hEmpty));  // H may be rewritten once these MMAs have read it
+        if (++j == x.n_buf) j = 0, ph ^= 1u;
       }
       if (!ok) {
         if (lane == 0) {

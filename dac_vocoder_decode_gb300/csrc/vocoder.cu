@@ -28,8 +28,12 @@ using voc::ConvGemmArgs;
 constexpr int kSmemMax = 227 * 1024;         // opt-in shared memory per block
 constexpr long long kWaitBudget = 4000000000LL;  // cycles (~2 s) before a wait gives up
 constexpr int kHeadTile = 128;
-// mbarriers (2 per A, weight and residual slot, 2 per accumulator, 1 drain), TMEM slot, flag
-constexpr int kBarrierBytes = 512;
+// mbarriers (3 per A and weight slot, 2 per residual slot and accumulator, 1 drain), TMEM
+// slot, flag
+constexpr int kBarrierBytes = 1024;
+constexpr int kMaxResidentStages = 32;  // weight slots of a resident plan
+constexpr int kMaxResidentTiles = 8;    // column tiles of a resident plan (one per CTA)
+constexpr int kMinAInFlight = 48 * 1024;  // A ring bytes a resident plan must keep
 constexpr int kBStageMax = 36 * 1024;  // bytes of one weight stage (per CTA)
 
 thread_local std::string g_err;  // last error without a context
@@ -228,6 +232,25 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   const int chunkA = g.rows * 16;
   const int sb = has_skip ? voc::skip_slot_bytes(L.cw) : 0;
   g.KB = 0;
+  g.b_resident = 0;
+  // Resident weights: when the whole column tile of a CTA (taps x Cp_in x n_stage hi/lo
+  // pairs) fits beside the A ring and the residual slots, it is loaded once and kept; the
+  // k-block is then the largest that leaves three A stages (else two) and at least
+  // kMinAInFlight bytes of A in flight (the 1x1 convs wait on their A loads otherwise).
+  const int w_tile = 4 * L.Cp_in * n_stage * g.taps;
+  for (int min_na = 3; min_na >= 2 && !g.KB && g.n_tiles <= kMaxResidentTiles; --min_na)
+    for (int kb = L.Cp_in - L.Cp_in % 16; kb >= 16 && !g.KB; kb -= 16) {
+      if (L.Cp_in % kb || 4 * kb * g.rows > 72 * 1024) continue;
+      if (g.taps * (L.Cp_in / kb) > kMaxResidentStages) continue;
+      const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
+      const int ns = has_skip ? 4 : 0;
+      const int avail = kSmemMax - 1024 - kBarrierBytes - w_tile - ns * sb;
+      const int na = std::min(4, avail / a_bytes);
+      if (na < min_na || na * a_bytes < kMinAInFlight) continue;
+      g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = 4 * kb * n_stage, g.na = na, g.ns = ns;
+      g.nb = g.taps * (L.Cp_in / kb);
+      g.b_resident = 1;
+    }
   for (int kb = L.Cp_in - L.Cp_in % 16; kb >= 16 && !g.KB; kb -= 16) {
     if (L.Cp_in % kb || 4 * kb * n_stage > kBStageMax || 4 * kb * g.rows > 72 * 1024) continue;
     const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
@@ -285,7 +308,8 @@ bool plan_layer(bool pair, Layer &L, int padding, bool has_skip, std::string &wh
   if (!plan_gemm(L, padding, has_skip, why)) return false;
   if (L.pair) {
     L.max_clusters = pair_clusters(L);
-    if (L.max_clusters < 1) {
+    // a resident plan needs at least one cluster per column tile
+    if (L.max_clusters < std::max(1, L.g.b_resident ? L.g.n_tiles : 1)) {
       L.pair = false;
       return plan_gemm(L, padding, has_skip, why);
     }
@@ -619,12 +643,18 @@ void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops,
 voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
                        const CUtensorMap &smap, const ConvGemmArgs &a, cudaStream_t stream) {
   const long long tiles = (long long)a.B * a.m_tiles * a.n_tiles;
+  // Persistent grid: one CTA (or cluster) per unit, at most one per job.  With resident
+  // weights every CTA must keep one column tile, so its job stride is a multiple of n_tiles.
+  auto persistent = [&](long long units) {
+    if (tiles <= units) return tiles;
+    return a.b_resident ? units - units % a.n_tiles : units;
+  };
   if (L.pair) {  // persistent grid of 2-CTA clusters, at most as many as can be resident
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2, attr[0].val.clusterDim.y = 1, attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * static_cast<unsigned>(std::min<long long>(tiles, L.max_clusters)));
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(persistent(L.max_clusters)));
     cfg.blockDim = dim3(voc::kGemmThreads);
     cfg.dynamicSmemBytes = L.smem;
     cfg.stream = stream;
@@ -636,7 +666,8 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
     if (e != cudaSuccess) return cuda_fail(ctx, e, ("launch " + L.name).c_str());
     return VOC_OK;
   }
-  const int grid = static_cast<int>(std::min<long long>(tiles, ctx->num_sms));
+  const int grid = static_cast<int>(L.ru ? std::min<long long>(tiles, ctx->num_sms)
+                                         : persistent(ctx->num_sms));
   if (L.ru) {
     if (L.cw == 32)
       voc::ru_gemm_kernel<32><<<grid, voc::kRuThreads, L.smem, stream>>>(map, smap, a, L.rx);
