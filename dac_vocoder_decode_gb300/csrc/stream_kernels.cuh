@@ -1,6 +1,7 @@
 // stream_kernels.cuh -- the bandwidth-bound kernels around the tensor-core convs:
 //   prep_hl_kernel      channels-first fp32 -> chunk-major bf16 hi/lo (+ optional Snake)
 //   out_head_kernel     Snake'd chunk-major fp32 -> k-tap conv to one channel (+bias) -> tanh
+//   out_head_reg_kernel the same for 7 taps, register-blocked (the decoder's head)
 //   stitch_kernel       overlap-crop stitch + clamp of windowed decodes
 //   finite_check_kernel flags a NaN / Inf in a buffer
 //   rows_to_cf_kernel   chunk-major fp32 -> channels-first fp32 (single-layer ops)
@@ -90,6 +91,62 @@ __global__ void __launch_bounds__(TILE) out_head_kernel(const float *__restrict_
     }
   }
   audio[(size_t)b * L + t] = tanhf(bias[0] + acc);
+}
+
+// Same operation for a fixed tap count K, register-blocked: each thread computes TPT
+// consecutive samples and keeps, per 4-channel chunk, the TPT + K - 1 input rows it needs in
+// registers (neighbouring threads share rows through L1), two chunks at a time so that the
+// loads of both are in flight together.  Weights are re-laid as w4[k][Cp/4] float4 (channel
+// quadruples) and read by all lanes at once.  No shared memory and no block barrier.
+// Requires Cp a multiple of 8.
+template <int K, int TPT>
+__global__ void __launch_bounds__(256) out_head_reg_kernel(const float *__restrict__ y, int L,
+                                                            int Cp, int pad_left,
+                                                            const float4 *__restrict__ w4,
+                                                            const float *__restrict__ bias,
+                                                            float *__restrict__ audio) {
+  constexpr int R = TPT + K - 1;  // input rows per chunk
+  const int b = blockIdx.y;
+  const long long t0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * TPT;
+  if (t0 >= L) return;
+  const int nch = Cp / 4;
+  const float4 *yb = reinterpret_cast<const float4 *>(y) + (size_t)b * nch * L;
+  float acc[TPT];
+#pragma unroll
+  for (int i = 0; i < TPT; ++i) acc[i] = 0.f;
+  const long long r0 = t0 - pad_left;
+  const bool interior = r0 >= 0 && r0 + R <= L;
+  for (int j0 = 0; j0 < nch; j0 += 2) {
+    float4 xs[2][R];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float4 *row = yb + (size_t)(j0 + u) * L;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const long long t = r0 + r;
+        xs[u][r] = (interior || (t >= 0 && t < L)) ? __ldg(row + t)
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const float4 wk = __ldg(w4 + (size_t)k * nch + j0 + u);
+#pragma unroll
+        for (int i = 0; i < TPT; ++i) {
+          const float4 xv = xs[u][i + k];
+          acc[i] = fmaf(wk.x, xv.x, acc[i]);
+          acc[i] = fmaf(wk.y, xv.y, acc[i]);
+          acc[i] = fmaf(wk.z, xv.z, acc[i]);
+          acc[i] = fmaf(wk.w, xv.w, acc[i]);
+        }
+      }
+  }
+  const float bb = bias[0];
+#pragma unroll
+  for (int i = 0; i < TPT; ++i)
+    if (t0 + i < L) audio[(size_t)b * L + t0 + i] = tanhf(bb + acc[i]);
 }
 
 // Overlap-crop stitch (minimaxmusic.cpp Architecture, "Decode and stitch"):

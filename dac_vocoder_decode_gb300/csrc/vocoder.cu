@@ -78,7 +78,9 @@ struct Layer {
 struct OutHead {
   int C = 0, Cp = 0, K = 0, pad_left = 0, level = 0;
   float *w_dev = nullptr, *b_dev = nullptr;
+  float *w4_dev = nullptr;  // [K][Cp/4] channel quadruples for the register-blocked kernel
 };
+constexpr int kHeadTpt = 2;  // samples per thread of the register-blocked head
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -685,6 +687,16 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
 
 voc_status launch_out_head(vocoder *ctx, const OutHead &h, const float *y, int B, long long L,
                            float *audio, cudaStream_t stream) {
+  if (h.K == 7 && h.w4_dev) {
+    const long long threads = (L + kHeadTpt - 1) / kHeadTpt;
+    dim3 grid(static_cast<unsigned>((threads + 255) / 256), static_cast<unsigned>(B));
+    voc::out_head_reg_kernel<7, kHeadTpt><<<grid, 256, 0, stream>>>(
+        y, static_cast<int>(L), h.Cp, h.pad_left, reinterpret_cast<const float4 *>(h.w4_dev),
+        h.b_dev, audio);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "launch out_head");
+    return VOC_OK;
+  }
   const size_t smem = ((size_t)(kHeadTile + h.K - 1) * h.Cp + (size_t)h.Cp * h.K) * 4;
   dim3 grid(static_cast<unsigned>((L + kHeadTile - 1) / kHeadTile), static_cast<unsigned>(B));
   voc::out_head_kernel<kHeadTile><<<grid, kHeadTile, smem, stream>>>(
@@ -957,6 +969,11 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     for (int c = 0; c < C; ++c)
       for (int k = 0; k < h.K; ++k) wp[(size_t)c * h.K + k] = w[(size_t)c * h.K + k];
     st = upload(ctx, ctx->allocs, wp, &h.w_dev);
+    if (st != VOC_OK) return bail(st);
+    std::vector<float> w4((size_t)h.K * h.Cp, 0.f);  // [k][c/4][c%4]
+    for (int c = 0; c < C; ++c)
+      for (int k = 0; k < h.K; ++k) w4[((size_t)k * (h.Cp / 4) + c / 4) * 4 + c % 4] = w[(size_t)c * h.K + k];
+    st = upload(ctx, ctx->allocs, w4, &h.w4_dev);
     if (st != VOC_OK) return bail(st);
     st = upload(ctx, ctx->allocs, bp, &h.b_dev);
     if (st != VOC_OK) return bail(st);

@@ -230,6 +230,20 @@ def test_decode_fusion_variants(arch, fuse):
     G.compare_audio(ref, got, f"fuse={fuse}")
 
 
+ODD_HEAD = W.Arch(latent_channels=16, channels0=64, strides=(4, 2), widths=(32, 16),
+                  in_kernel=5, res_kernel=5, out_kernel=9)
+
+
+def test_decode_other_kernel_sizes():
+    """conv_in, residual and output kernels of 5, 5 and 9 taps (the 7-tap output head has its
+    own register-blocked kernel; other tap counts take the general one)."""
+    wl = W.make_custom(ODD_HEAD, B=2, T=50, seed=73)
+    voc = V.Vocoder(ODD_HEAD, V.fold_params(wl.params))
+    got = G.gpu_decode(voc, wl.latent)
+    ref = O.decode(ODD_HEAD, wl.params, wl.latent)
+    G.compare_audio(ref, got, "kernel sizes 5/5/9")
+
+
 @pytest.mark.parametrize("arch", [MID_MUSIC, MID_SPEECH], ids=["music", "speech_causal"])
 def test_decode_cta_pair(arch):
     """Every tensor-core layer on 2-CTA clusters (one 256-row MMA per pair, each CTA staging
