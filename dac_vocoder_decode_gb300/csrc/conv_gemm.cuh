@@ -165,11 +165,18 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
   }
   float sn[CW];
   if (p.alpha) {
-    float a[CW], ib[CW];
-    ldg_vec(p.alpha + n0, a);
-    ldg_vec(p.invb + n0, ib);
+    // 16 columns at a time keeps the register footprint of the branch-free Snake down
 #pragma unroll
-    for (int i = 0; i < CW; ++i) sn[i] = snake(v[i], a[i], ib[i]);
+    for (int h = 0; h < CW; h += 16) {
+      float a[16], ib[16], vv[16], out[16];
+      ldg_vec(p.alpha + n0 + h, a);
+      ldg_vec(p.invb + n0 + h, ib);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) vv[i] = v[h + i];
+      snake_n<16>(vv, a, ib, out);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sn[h + i] = out[i];
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < CW; ++i) sn[i] = v[i];

@@ -39,11 +39,14 @@ __device__ __forceinline__ void ru_epilogue1(const ConvGemmArgs &p, const RuExtr
   ldg_vec(x.bias_h + n0, bb);
   ldg_vec(x.alpha_h + n0, a);
   ldg_vec(x.invb_h + n0, ib);
+#pragma unroll
+  for (int i = 0; i < CW; ++i) v[i] += bb[i];
+  float sn[CW];
+  snake_n<CW>(v, a, ib, sn);
   uint32_t hw[CW / 2], lw[CW / 2];
 #pragma unroll
   for (int i = 0; i < CW / 2; ++i) {
-    const float s0 = snake(v[2 * i] + bb[2 * i], a[2 * i], ib[2 * i]);
-    const float s1 = snake(v[2 * i + 1] + bb[2 * i + 1], a[2 * i + 1], ib[2 * i + 1]);
+    const float s0 = sn[2 * i], s1 = sn[2 * i + 1];
     const __nv_bfloat16 h0 = __float2bfloat16_rn(s0), h1 = __float2bfloat16_rn(s1);
     const __nv_bfloat16 l0 = __float2bfloat16_rn(s0 - __bfloat162float(h0));
     const __nv_bfloat16 l1 = __float2bfloat16_rn(s1 - __bfloat162float(h1));

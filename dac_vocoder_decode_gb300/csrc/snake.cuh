@@ -21,8 +21,8 @@ __device__ __noinline__ float sin2_wide(float x) {
   return s * s;
 }
 
-__device__ __forceinline__ float sin2(float x) {
-  if (fabsf(x) > 8192.f) return sin2_wide(x);
+// Reduction and __sinf for |x| <= 8192 (no branch).
+__device__ __forceinline__ float sin2_fast(float x) {
   const float k = rintf(x * kInvPi);
   float r = fmaf(-k, kPiHi, x);
   r = fmaf(-k, kPiLo, r);
@@ -30,8 +30,35 @@ __device__ __forceinline__ float sin2(float x) {
   return s * s;
 }
 
+__device__ __forceinline__ float sin2(float x) {
+  if (fabsf(x) > 8192.f) return sin2_wide(x);
+  return sin2_fast(x);
+}
+
 __device__ __forceinline__ float snake(float v, float a, float inv_b) {
   return fmaf(inv_b, sin2(a * v), v);
+}
+
+// Snake of N values.  The common path has no branch per value, so the compiler can
+// interleave the N independent computations; the values with |a v| > 8192 (if any) are
+// redone with sinf afterwards, under one branch per call.
+template <int N>
+__device__ __forceinline__ void snake_n(const float (&v)[N], const float (&a)[N],
+                                        const float (&inv_b)[N], float (&out)[N]) {
+  bool wide = false;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float ax = a[i] * v[i];
+    wide |= fabsf(ax) > 8192.f;
+    out[i] = fmaf(inv_b[i], sin2_fast(ax), v[i]);
+  }
+  if (wide) {  // unrolled too: a run-time index would put the arrays in local memory
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const float ax = a[i] * v[i];
+      if (fabsf(ax) > 8192.f) out[i] = fmaf(inv_b[i], sin2_wide(ax), v[i]);
+    }
+  }
 }
 
 }  // namespace voc

@@ -224,7 +224,9 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     why = "tap span too wide for one staged tile (" + std::to_string(off_max - off_min) + ")";
     return false;
   }
-  L.cw = (g.N_tile % 32 == 0 && L.Cp_out % 32 == 0) ? 32 : 16;
+  // epilogue column chunk: 32 when it divides the tile into an even number of chunks (the two
+  // epilogue halves take alternate chunks), else 16
+  L.cw = (g.N_tile % 64 == 0 && L.Cp_out % 32 == 0) ? 32 : 16;
   // weight columns staged per CTA: the whole tile, or (CTA pair) one half of it
   const int n_stage = L.pair ? g.N_tile / 2 : g.N_tile;
   // Channels per k-block: the largest multiple of 16 dividing Cp_in whose weight stage
@@ -247,17 +249,23 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
       const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
       const int ns = has_skip ? 4 : 0;
       const int avail = kSmemMax - 1024 - kBarrierBytes - w_tile - ns * sb;
-      const int na = std::min(4, avail / a_bytes);
+      // a 1x1 conv consumes each A stage almost at once: its A ring hides the HBM latency
+      const int na = std::min(g.taps == 1 ? 8 : 4, avail / a_bytes);
       if (na < min_na || na * a_bytes < kMinAInFlight) continue;
       g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = 4 * kb * n_stage, g.na = na, g.ns = ns;
       g.nb = g.taps * (L.Cp_in / kb);
       g.b_resident = 1;
     }
+  // streaming weights: a 1x1 conv gets up to four A stages (its A comes from HBM and is
+  // consumed at once; its weight stages come from L2), a k-tap conv two
+  const int na_want = g.taps == 1 ? 4 : 2;
   for (int kb = L.Cp_in - L.Cp_in % 16; kb >= 16 && !g.KB; kb -= 16) {
     if (L.Cp_in % kb || 4 * kb * n_stage > kBStageMax || 4 * kb * g.rows > 72 * 1024) continue;
     const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
     const int b_bytes = 4 * kb * n_stage;
-    int avail = kSmemMax - 1024 - kBarrierBytes - 2 * a_bytes;
+    int na = na_want;
+    while (na > 2 && kSmemMax - 1024 - kBarrierBytes - na * a_bytes < 3 * b_bytes) --na;
+    int avail = kSmemMax - 1024 - kBarrierBytes - na * a_bytes;
     int ns = 0;
     if (has_skip) {  // two rings (one per epilogue half) of 1 or 2 slots each
       ns = ((avail - 4 * sb) / b_bytes >= 3) ? 4 : 2;
@@ -266,7 +274,7 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     int nb = std::min(8, avail / b_bytes);
     nb -= nb % voc::kBWarps;  // each weight-producer warp owns every kBWarps-th slot
     if (nb < 2) continue;
-    g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = b_bytes, g.nb = nb, g.ns = ns, g.na = 2;
+    g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = b_bytes, g.nb = nb, g.ns = ns, g.na = na;
   }
   if (!g.KB) {
     why = "shared memory plan does not fit";
@@ -347,7 +355,7 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
     why = "tap span too wide for one staged tile";
     return false;
   }
-  L.cw = (g.N_tile % 32 == 0) ? 32 : 16;
+  L.cw = (g.N_tile % 64 == 0) ? 32 : 16;  // an even number of chunks, as in plan_gemm
   L.rx.h_bytes = 4 * voc::kTileM * L.Cp_out;
   const int chunkA = g.rows * 16;
   const int sb = voc::skip_slot_bytes(L.cw);
