@@ -27,12 +27,13 @@
 // all taps reuse one staged halo tile (128 + span rows, zero fill outside [0, L)).
 //
 // Roles: warp 0 lane 0 issues the A copies (one 5-D TMA box per k-block: the hi and
-// lo planes of its channel chunks), warp 1 lane 0 issues MMAs, warps 2..9 run the
-// epilogue (TMEM -> registers -> bias, residual, Snake of the next layer, hi/lo split
-// -> global; with the chunk-major layout the 32 lanes of a warp store 32 consecutive
-// rows of one chunk: 512 contiguous bytes), warps 10 and 11 prefetch the residual
-// input of the two epilogue halves by TMA, warp 12 issues the weight copies.  The MMA
-// warp runs its loop convergently and issues through an elected lane.
+// lo planes of its channel chunks), warp 1 runs the MMA loop (convergently; an elected
+// lane issues), warps 2..13 run the epilogue in three groups of four warps, one warp per
+// TMEM lane quadrant, group g taking column chunks g, g+3, ... (TMEM -> registers ->
+// bias, residual, Snake of the next layer, hi/lo split -> global; with the chunk-major
+// layout the 32 lanes of a warp store 32 consecutive rows of one chunk: 512 contiguous
+// bytes), warps 14..16 prefetch the residual input of the three groups by TMA, warp 17
+// issues the weight copies.
 // The grid is persistent; 2 to 4 TMEM accumulators let the epilogue of one tile
 // overlap the mainloop of the next.
 #pragma once
@@ -45,12 +46,17 @@
 namespace voc {
 
 constexpr int kTileM = 128;
-constexpr int kEpiWarps = 8;                            // two per TMEM lane quadrant
-constexpr int kSkipWarp = 2 + kEpiWarps;                // residual prefetch (10, 11: one per half)
-constexpr int kBWarp = kSkipWarp + 2;                   // weight copies (12)
+constexpr int kEpiGroups = 3;                           // epilogue groups of 4 warps (one per
+                                                        // TMEM lane quadrant)
+constexpr int kEpiWarps = 4 * kEpiGroups;               // warps 2..13
+constexpr int kSkipWarp = 2 + kEpiWarps;                // residual prefetch, one warp per group
+constexpr int kBWarp = kSkipWarp + kEpiGroups;          // weight copies
 constexpr int kBWarps = 1;
-constexpr int kGemmThreads = 32 * (kBWarp + kBWarps);   // 448
-constexpr int kRuThreads = 32 * (kSkipWarp + 1);        // 352: fused residual-unit kernel
+constexpr int kGemmThreads = 32 * (kBWarp + kBWarps);   // 576
+// the fused residual-unit kernel: 8 epilogue warps (two per quadrant), one residual warp
+constexpr int kRuEpiWarps = 8;
+constexpr int kRuSkipWarp = 2 + kRuEpiWarps;
+constexpr int kRuThreads = 32 * (kRuSkipWarp + 1);      // 352
 constexpr int kMaxAcc = 4;
 
 // bytes of one residual slot (128 rows x cw fp32 columns, as cw/4 chunks of 128 x 16 B)
@@ -318,7 +324,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int i = 0; i < p.ns; ++i) {
       mbar_init(smem_u32(skipFull + i), 1);
-      mbar_init(smem_u32(skipEmpty + i), 4 * 32);  // the four quadrant warps of one half
+      mbar_init(smem_u32(skipEmpty + i), 4 * 32);  // the four quadrant warps of one group
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -573,15 +579,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         drain_ring_strided(fullB + j, p.nb / kBWarps, kBWarps, mine, p.timeout);
       }
     }
-  } else if (warp == kSkipWarp || warp == kSkipWarp + 1) {
+  } else if (warp >= kSkipWarp && warp < kBWarp) {
     if (lane == 0 && p.skip) {
       // ------------------------------------------------------------ residual prefetch
       prefetch_tmap(&tmapS);
-      // Chunk c of a tile is consumed by the epilogue half c & 1; each half has its own
-      // ring of ns/2 slots, filled by its own warp in that half's consumption order, so a
-      // slot is only ever waited on by one sequence of consumers, at most one fill ahead.
+      // Chunk c of a tile is consumed by epilogue group c % kEpiGroups; each group has its
+      // own ring of ns / kEpiGroups slots, filled by its own warp in that group's
+      // consumption order, so a slot is only ever waited on by one sequence of consumers,
+      // at most one fill ahead.
       const uint32_t bytes = static_cast<uint32_t>(skip_slot_bytes(CW));
-      const int nsh = p.ns / 2;
+      const int nsh = p.ns / kEpiGroups;
       const int h = warp - kSkipWarp;
       int cnt = 0;
       bool ok = true;
@@ -590,7 +597,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int rest = job / p.n_tiles;
         const int mt = rest % p.m_tiles;
         const int b = rest / p.m_tiles;
-        for (int c = h; c < n_chunks; c += 2) {
+        for (int c = h; c < n_chunks; c += kEpiGroups) {
           const int k = cnt++;
           const int slot = h * nsh + k % nsh;
           const uint32_t ph = static_cast<uint32_t>(k / nsh) & 1u;
@@ -620,15 +627,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int e = warp - 2;     // epilogue warp 0..7
+    const int e = warp - 2;     // epilogue warp 0..kEpiWarps-1
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
-    const int half = e / 4;     // the two warps of a quadrant take alternate column chunks
+    const int half = e / 4;     // this warp's group: column chunks half, half + kEpiGroups, ...
     const int row_in_tile = quad * 32 + lane;
     const uint32_t sbase = smem_u32(smS);
-    const int nsh = p.ns > 0 ? p.ns / 2 : 1;  // residual slots of this half's ring
+    const int nsh = p.ns > 0 ? p.ns / kEpiGroups : 1;  // residual slots of this group's ring
     // where this warp reports a free accumulator: this CTA's barrier, or the even CTA's
     const uint32_t acc_empty0 = PAIR ? mapa_shared(smem_u32(accEmpty), 0u) : smem_u32(accEmpty);
-    int kslot = 0;                           // this half's residual ring position
+    int kslot = 0;                           // this group's residual ring position
     uint32_t kph = 0;
     int acc = 0;                             // accumulator ring position
     uint32_t phacc = 0;
@@ -647,7 +654,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int t = mt * kM + row0 + row_in_tile;
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * p.acc_cols) +
                              (static_cast<uint32_t>(quad * 32) << 16);
-      for (int c = half; c < n_chunks && ok; c += 2) {
+      for (int c = half; c < n_chunks && ok; c += kEpiGroups) {
         const int slot = half * nsh + kslot;
         ok = epilogue_chunk<CW>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
                                 smem_u32(skipFull + slot), smem_u32(skipEmpty + slot), kph,

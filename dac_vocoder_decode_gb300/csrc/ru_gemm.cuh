@@ -108,11 +108,11 @@ __global__ void __launch_bounds__(kRuThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(acc1Full + i), 1);
-      mbar_init(smem_u32(acc1Empty + i), kEpiWarps * 32);
+      mbar_init(smem_u32(acc1Empty + i), kRuEpiWarps * 32);
       mbar_init(smem_u32(acc2Full + i), 1);
-      mbar_init(smem_u32(acc2Empty + i), kEpiWarps * 32);
+      mbar_init(smem_u32(acc2Empty + i), kRuEpiWarps * 32);
     }
-    mbar_init(smem_u32(hFull), kEpiWarps * 32);
+    mbar_init(smem_u32(hFull), kRuEpiWarps * 32);
     mbar_init(smem_u32(hEmpty), 1);
     for (int i = 0; i < p.ns; ++i) {
       mbar_init(smem_u32(skipFull + i), 1);
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         mbar_wait(smem_u32(drain), 0u, p.timeout, &never);
       }
     }
-  } else if (warp == kSkipWarp) {
+  } else if (warp == kRuSkipWarp) {
     if (lane == 0 && p.skip) {
       // ------------------------------------------------------------ residual prefetch
       prefetch_tmap(&tmapS);

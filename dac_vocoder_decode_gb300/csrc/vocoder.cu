@@ -30,7 +30,7 @@ constexpr long long kWaitBudget = 4000000000LL;  // cycles (~2 s) before a wait 
 constexpr int kHeadTile = 128;
 // mbarriers (3 per A and weight slot, 2 per residual slot and accumulator, 1 drain), TMEM
 // slot, flag
-constexpr int kBarrierBytes = 1024;
+constexpr int kBarrierBytes = 1536;
 constexpr int kMaxResidentStages = 32;  // weight slots of a resident plan
 constexpr int kMaxResidentTiles = 8;    // column tiles of a resident plan (one per CTA)
 constexpr int kMinAInFlight = 48 * 1024;  // A ring bytes a resident plan must keep
@@ -224,9 +224,9 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     why = "tap span too wide for one staged tile (" + std::to_string(off_max - off_min) + ")";
     return false;
   }
-  // epilogue column chunk: 32 when it divides the tile into an even number of chunks (the two
-  // epilogue halves take alternate chunks), else 16
-  L.cw = (g.N_tile % 64 == 0 && L.Cp_out % 32 == 0) ? 32 : 16;
+  // epilogue column chunk: 16 columns (three groups of epilogue warps take every third
+  // chunk; 16-column chunks keep the register footprint within the 576-thread block)
+  L.cw = 16;
   // weight columns staged per CTA: the whole tile, or (CTA pair) one half of it
   const int n_stage = L.pair ? g.N_tile / 2 : g.N_tile;
   // Channels per k-block: the largest multiple of 16 dividing Cp_in whose weight stage
@@ -247,7 +247,7 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
       if (L.Cp_in % kb || 4 * kb * g.rows > 72 * 1024) continue;
       if (g.taps * (L.Cp_in / kb) > kMaxResidentStages) continue;
       const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
-      const int ns = has_skip ? 4 : 0;
+      const int ns = has_skip ? 2 * voc::kEpiGroups : 0;
       const int avail = kSmemMax - 1024 - kBarrierBytes - w_tile - ns * sb;
       // a 1x1 conv consumes each A stage almost at once: its A ring hides the HBM latency
       const int na = std::min(g.taps == 1 ? 8 : 4, avail / a_bytes);
@@ -267,8 +267,9 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     while (na > 2 && kSmemMax - 1024 - kBarrierBytes - na * a_bytes < 3 * b_bytes) --na;
     int avail = kSmemMax - 1024 - kBarrierBytes - na * a_bytes;
     int ns = 0;
-    if (has_skip) {  // two rings (one per epilogue half) of 1 or 2 slots each
-      ns = ((avail - 4 * sb) / b_bytes >= 3) ? 4 : 2;
+    if (has_skip) {  // one ring per epilogue group, of 2 slots (1 when space is short)
+      ns = ((avail - 2 * voc::kEpiGroups * sb) / b_bytes >= 3) ? 2 * voc::kEpiGroups
+                                                                : voc::kEpiGroups;
       avail -= ns * sb;
     }
     int nb = std::min(8, avail / b_bytes);
@@ -278,6 +279,12 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   }
   if (!g.KB) {
     why = "shared memory plan does not fit";
+    return false;
+  }
+  // mbarriers: full/empty/pair per A and weight slot, full/empty per residual slot and
+  // accumulator, one drain; then the TMEM address slot and the abort flag
+  if ((3 * g.na + 3 * g.nb + 2 * g.ns + 2 * voc::kMaxAcc + 1) * 8 + 8 > kBarrierBytes) {
+    why = "too many pipeline slots for the barrier block";
     return false;
   }
   g.nkb = L.Cp_in / g.KB;
