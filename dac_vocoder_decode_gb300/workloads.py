@@ -46,6 +46,9 @@ class Arch:
     res_kernel: int = 7
     out_kernel: int = 7
     padding: int = PAD_SYMMETRIC
+    # 0, or P: a 1x1 projection C_lat -> P (bias, no weight norm) before conv_in (the
+    # published music model's dec_in_proj 64 -> 1024; conv_in then maps P -> channels0)
+    in_proj_channels: int = 0
 
     @property
     def hop(self) -> int:
@@ -62,7 +65,12 @@ class Arch:
         conv weights [C_out, C_in, K]; transposed-conv weights [C_in, C_out, K];
         biases [C_out]; Snake alphas [C]."""
         out: List[Tuple[str, Tuple[int, ...]]] = []
-        out.append(("conv_in.w", (self.channels0, self.latent_channels, self.in_kernel)))
+        c_in = self.latent_channels
+        if self.in_proj_channels:
+            out.append(("in_proj.w", (self.in_proj_channels, self.latent_channels, 1)))
+            out.append(("in_proj.b", (self.in_proj_channels,)))
+            c_in = self.in_proj_channels
+        out.append(("conv_in.w", (self.channels0, c_in, self.in_kernel)))
         out.append(("conv_in.b", (self.channels0,)))
         for i, ((cin, cout), s) in enumerate(zip(self.stage_channels(), self.strides)):
             out.append((f"block{i}.snake.alpha", (cin,)))
@@ -88,6 +96,14 @@ class RawConv:
 
     g: np.ndarray  # [v.shape[0]]
     v: np.ndarray  # PyTorch layout
+    b: Optional[np.ndarray]
+
+
+@dataclasses.dataclass
+class PlainConv:
+    """A convolution stored without weight norm (the input projection)."""
+
+    w: np.ndarray  # PyTorch layout
     b: Optional[np.ndarray]
 
 
@@ -118,6 +134,8 @@ MUSIC = Arch(latent_channels=64, channels0=1536, strides=(8, 8, 4, 2), widths=(7
 SPEECH = Arch(latent_channels=1024, channels0=1536, strides=(8, 5, 4, 4, 3),
               widths=(768, 384, 192, 96, 48), padding=PAD_CAUSAL)
 TINY = Arch(latent_channels=16, channels0=64, strides=(8, 8, 4, 2), widths=(32, 16, 8, 4))
+# the published music model's front end: dec_in_proj 64 -> 1024, conv_in 1024 -> 1536
+MUSIC_FULL = dataclasses.replace(MUSIC, in_proj_channels=1024)
 
 # name -> (index used for seeds, arch, latent shape, weight recipe, description)
 WORKLOADS = {
@@ -174,6 +192,13 @@ def gen_params(arch: Arch, recipe: str, seed_w: int, seed_a: int) -> list:
             i += 1
             continue
         assert name.endswith(".w")
+        if name.startswith("in_proj"):
+            # no weight norm: w ~ N(0, 1/C_lat) (calibrated, variance preserving) or N(0, .02)
+            std = 0.02 if recipe == "literal" else 1.0 / math.sqrt(shape[1])
+            w = (rw.standard_normal(shape, dtype=np.float32) * np.float32(std))
+            out.append(PlainConv(w=w, b=bias(shapes[i + 1][1][0])))
+            i += 2
+            continue
         if name.startswith("conv_in"):
             gain = 1.0
         elif ".convT." in name:

@@ -17,7 +17,7 @@
 #include <string.h>
 
 int oracle_param_count(const oracle_arch *a) {
-  return 2 + a->n_stages * (3 + 6 * a->n_dilations) + 3;
+  return (a->in_proj_channels > 0 ? 2 : 0) + 2 + a->n_stages * (3 + 6 * a->n_dilations) + 3;
 }
 
 long oracle_hop(const oracle_arch *a) {
@@ -136,6 +136,7 @@ int oracle_decode(const oracle_arch *a, const double *const *params, const float
 
   /* largest activation (channels x length) over the stack */
   long max_elems = (long)a->latent_channels * T;
+  if ((long)a->in_proj_channels * T > max_elems) max_elems = (long)a->in_proj_channels * T;
   {
     long L = T;
     long e = (long)a->channels0 * L;
@@ -160,11 +161,19 @@ int oracle_decode(const oracle_arch *a, const double *const *params, const float
     const float *lat = latent + (long)bi * a->latent_channels * T;
     for (long i = 0; i < (long)a->latent_channels * T; ++i) s[i] = (double)lat[i];
 
-    /* conv_in: no Snake in front of it */
+    /* optional 1x1 input projection (minimaxmusic.cpp Architecture, "Flow VAE": dec_in_proj,
+       not weight normalised), then conv_in; no Snake in front of either */
+    int c_in = a->latent_channels;
+    if (a->in_proj_channels > 0) {
+      oracle_conv1d(s, a->latent_channels, T, params[p], params[p + 1], a->in_proj_channels, 1, 1,
+                    0, 0, h);
+      memcpy(s, h, (size_t)a->in_proj_channels * T * sizeof(double));
+      c_in = a->in_proj_channels;
+      p += 2;
+    }
     int pl, pr;
     conv_pads(a->padding, a->in_kernel, 1, &pl, &pr);
-    oracle_conv1d(s, a->latent_channels, T, params[p], params[p + 1], a->channels0, a->in_kernel, 1,
-                  pl, pr, x);
+    oracle_conv1d(s, c_in, T, params[p], params[p + 1], a->channels0, a->in_kernel, 1, pl, pr, x);
     p += 2;
 
     int C = a->channels0;

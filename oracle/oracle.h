@@ -60,10 +60,14 @@ typedef struct {
   int out_kernel;      /* conv_out taps (7)                        */
   int padding;         /* ORACLE_PAD_*                             */
   int flags;           /* ORACLE_FLAG_*                            */
+  int in_proj_channels;/* 0, or P: a 1x1 projection C_lat -> P (with bias, no weight norm)
+                          before conv_in, which then maps P -> C_0 (the published music
+                          model's dec_in_proj 64 -> 1024)                              */
 } oracle_arch;
 
 /* number of parameter tensors of the stack, in the canonical order:
- *   conv_in.w [C0][Cl][Kin], conv_in.b [C0],
+ *   [in_proj.w [P][Cl][1], in_proj.b [P]]   (only when in_proj_channels = P > 0)
+ *   conv_in.w [C0][Cl or P][Kin], conv_in.b [C0],
  *   for each stage i (Cin -> Cout = widths[i], stride s):
  *     snake.alpha [Cin], convT.w [Cin][Cout][2s], convT.b [Cout],
  *     for each dilation d: snake1.alpha [Cout], conv1.w [Cout][Cout][Kres],

@@ -84,7 +84,8 @@ class _ArchC(ctypes.Structure):
                 ("strides", ctypes.POINTER(ctypes.c_int)), ("widths", ctypes.POINTER(ctypes.c_int)),
                 ("n_dilations", ctypes.c_int), ("dilations", ctypes.POINTER(ctypes.c_int)),
                 ("res_kernel", ctypes.c_int), ("out_kernel", ctypes.c_int),
-                ("padding", ctypes.c_int), ("flags", ctypes.c_int)]
+                ("padding", ctypes.c_int), ("flags", ctypes.c_int),
+                ("in_proj_channels", ctypes.c_int)]
 
 
 def fold_weight_norm(g: np.ndarray, v: np.ndarray) -> np.ndarray:
@@ -152,6 +153,9 @@ def fold_params(params: Sequence) -> list:
         if hasattr(p, "g"):
             out.append(fold_weight_norm(p.g, p.v))
             out.append(None if p.b is None else np.ascontiguousarray(p.b, dtype=np.float64))
+        elif hasattr(p, "w"):  # a convolution stored without weight norm
+            out.append(np.ascontiguousarray(p.w, dtype=np.float64))
+            out.append(None if p.b is None else np.ascontiguousarray(p.b, dtype=np.float64))
         else:
             out.append(np.ascontiguousarray(p, dtype=np.float64))
     return out
@@ -171,7 +175,7 @@ def decode(arch, params: Sequence, latent: np.ndarray, flags: int = 0, folded: O
     dils = (ctypes.c_int * len(arch.dilations))(*arch.dilations)
     a = _ArchC(arch.latent_channels, arch.channels0, arch.in_kernel, len(arch.strides), strides,
                widths, len(arch.dilations), dils, arch.res_kernel, arch.out_kernel, arch.padding,
-               flags)
+               flags, getattr(arch, "in_proj_channels", 0))
     n = lib.oracle_param_count(ctypes.byref(a))
     assert n == len(folded), (n, len(folded))
     ptrs = (ctypes.POINTER(ctypes.c_double) * n)()

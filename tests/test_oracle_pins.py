@@ -430,3 +430,44 @@ def test_windowed_stitch_equals_single_pass():
     full = O.decode(arch, wl.params, cont, 0, folded)
     assert st.shape == full.shape == (2, 1589248)
     np.testing.assert_allclose(st, full, rtol=0, atol=1e-13)
+
+
+def test_full_music_model_parameter_count():
+    """The published music decoder with its input projection (dec_in_proj 64 -> 1024, not
+    weight normalised, then conv_in 1024 -> 1536) has 54 M parameters per the pages; the
+    folded tensors of the architecture add up to that (weight-norm gains are not stored
+    once folded)."""
+    with open(os.path.join(GOLDEN, "pages_values.json")) as f:
+        gold = json.load(f)
+    n = sum(int(np.prod(s)) for _, s in W.MUSIC_FULL.param_shapes())
+    assert round(n / 1e6) == gold["music_vocoder_params_millions"]
+    assert n == 54157665
+    # the oracle sees the same tensor list
+    assert len(W.MUSIC_FULL.param_shapes()) == len(W.MUSIC.param_shapes()) + 2
+
+
+def test_identity_projection_reproduces_plain_decoder():
+    """An input projection that copies the C_lat latent channels into the first C_lat of
+    its P outputs (zero bias), followed by a conv_in whose weights on the extra P - C_lat
+    channels are zero, decodes exactly like the decoder without the projection."""
+    base = W.Arch(latent_channels=6, channels0=24, strides=(4, 2), widths=(12, 8))
+    full = W.Arch(latent_channels=6, channels0=24, strides=(4, 2), widths=(12, 8),
+                  in_proj_channels=16)
+    wl = W.make_custom(base, B=2, T=18, seed=77)
+    folded = O.fold_params(wl.params)
+    w_in = folded[0]  # conv_in [C0][C_lat][K]
+    proj = np.zeros((16, 6, 1))
+    proj[:6, :, 0] = np.eye(6)
+    w_in_full = np.zeros((24, 16, w_in.shape[2]))
+    w_in_full[:, :6, :] = w_in
+    folded_full = [proj, np.zeros(16), w_in_full] + folded[1:]
+    y0 = O.decode(base, None, wl.latent, 0, folded)
+    y1 = O.decode(full, None, wl.latent, 0, folded_full)
+    np.testing.assert_array_equal(y0, y1)
+    # and a non-trivial projection changes the result
+    proj2 = proj.copy()
+    proj2[7, 0, 0] = 1.0
+    w_in_full2 = w_in_full.copy()
+    w_in_full2[:, 7, :] = w_in[:, 0, :]
+    y2 = O.decode(full, None, wl.latent, 0, [proj2, np.zeros(16), w_in_full2] + folded[1:])
+    assert np.max(np.abs(y2 - y0)) > 1e-3
