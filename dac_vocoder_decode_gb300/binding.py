@@ -15,7 +15,7 @@ import numpy as np
 
 from . import build as _build
 
-VOC_ABI_VERSION = 3
+VOC_ABI_VERSION = 4
 VOC_OK = 0
 VOC_INVALID_ARG = -1
 VOC_UNSUPPORTED = -2
@@ -62,7 +62,8 @@ class VocDesc(ctypes.Structure):
                 ("dilations", ctypes.POINTER(ctypes.c_int)), ("res_kernel", ctypes.c_int),
                 ("out_kernel", ctypes.c_int), ("out_channels", ctypes.c_int),
                 ("padding", ctypes.c_int), ("precision", ctypes.c_int),
-                ("fuse_max_channels", ctypes.c_int), ("cta_pair", ctypes.c_int)]
+                ("fuse_max_channels", ctypes.c_int), ("cta_pair", ctypes.c_int),
+                ("in_proj_channels", ctypes.c_int)]
 
 
 _lib = None
@@ -164,7 +165,8 @@ def make_desc(arch, fuse_max_channels: int = 0, cta_pair: int = 0) -> VocDesc:
     dils = (ctypes.c_int * len(arch.dilations))(*arch.dilations)
     d = VocDesc(VOC_ABI_VERSION, arch.latent_channels, arch.in_kernel, arch.channels0,
                 len(arch.strides), strides, widths, len(arch.dilations), dils, arch.res_kernel,
-                arch.out_kernel, 1, arch.padding, VOC_PREC_BF16X3, fuse_max_channels, cta_pair)
+                arch.out_kernel, 1, arch.padding, VOC_PREC_BF16X3, fuse_max_channels, cta_pair,
+                getattr(arch, "in_proj_channels", 0))
     d._keep = (strides, widths, dils)
     return d
 
@@ -338,6 +340,9 @@ def fold_params(params) -> list:
     for p in params:
         if hasattr(p, "g"):
             out.append(vocoder_fold_weight_norm(p.g, p.v))
+            out.append(None if p.b is None else np.ascontiguousarray(p.b, dtype=np.float32))
+        elif hasattr(p, "w"):  # a convolution stored without weight norm
+            out.append(np.ascontiguousarray(p.w, dtype=np.float32))
             out.append(None if p.b is None else np.ascontiguousarray(p.b, dtype=np.float32))
         else:
             out.append(np.ascontiguousarray(p, dtype=np.float32))

@@ -517,6 +517,7 @@ bool check_desc(const voc_desc *d, std::string &why) {
   if (!d->strides || !d->widths) return why = "strides / widths NULL", false;
   if (d->n_dilations < 1 || d->n_dilations > 4 || !d->dilations) return why = "dilations", false;
   if (d->out_channels != 1) return why = "out_channels must be 1", false;
+  if (d->in_proj_channels < 0 || d->in_proj_channels > 8192) return why = "in_proj_channels", false;
   if (d->padding != VOC_PAD_SYMMETRIC && d->padding != VOC_PAD_CAUSAL) return why = "padding", false;
   if (d->precision != VOC_PREC_BF16X3) return why = "precision", false;
   if (d->cta_pair < -1 || d->cta_pair > 1) return why = "cta_pair must be -1, 0 or 1", false;
@@ -533,11 +534,13 @@ bool check_desc(const voc_desc *d, std::string &why) {
   return true;
 }
 
-int param_count(const voc_desc *d) { return 2 + d->n_stages * (3 + 6 * d->n_dilations) + 3; }
+int param_count(const voc_desc *d) {
+  return (d->in_proj_channels > 0 ? 2 : 0) + 2 + d->n_stages * (3 + 6 * d->n_dilations) + 3;
+}
 
 // kind of every canonical parameter: 'w' weight, 'b' bias, 'a' Snake alpha
 std::string param_kinds(const voc_desc *d) {
-  std::string k = "wb";
+  std::string k = d->in_proj_channels > 0 ? "wbwb" : "wb";
   for (int i = 0; i < d->n_stages; ++i) {
     k += "awb";
     for (int j = 0; j < d->n_dilations; ++j) k += "awbawb";
@@ -553,7 +556,8 @@ long long level_len(const vocoder *ctx, int lv, int T) {
 }
 
 size_t buf_bytes(const vocoder *ctx, int B, int T) {
-  size_t m = (size_t)B * T * std::max(ctx->Cp_lat, rup(ctx->desc.channels0, 16));
+  size_t m = (size_t)B * T *
+             std::max({ctx->Cp_lat, rup(ctx->desc.channels0, 16), rup(ctx->desc.in_proj_channels, 16)});
   for (int i = 0; i < ctx->desc.n_stages; ++i)
     m = std::max(m, (size_t)B * (size_t)level_len(ctx, i + 1, T) * (size_t)rup(ctx->widths[i], 16));
   return rupz(m * 4, 256);
@@ -752,7 +756,14 @@ VOC_API voc_status vocoder_param_shape(const voc_desc *d, int index, int dims[3]
     dims[0] = a, dims[1] = b, dims[2] = c;
     return VOC_OK;
   };
-  if (index == 0) return set(3, d->channels0, d->latent_channels, d->in_kernel);
+  int c_in = d->latent_channels;
+  if (d->in_proj_channels > 0) {  // in_proj.w [P][C_lat][1], in_proj.b [P]
+    if (index == 0) return set(3, d->in_proj_channels, d->latent_channels, 1);
+    if (index == 1) return set(1, d->in_proj_channels);
+    index -= 2;
+    c_in = d->in_proj_channels;
+  }
+  if (index == 0) return set(3, d->channels0, c_in, d->in_kernel);
   if (index == 1) return set(1, d->channels0);
   int i = index - 2;
   int C = d->channels0;
@@ -872,19 +883,36 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
   const int nd = desc->n_dilations;
   int p = 0;
   voc_status st;
+  // optional 1x1 input projection (no Snake around it; its epilogue only splits hi/lo)
+  int conv_in_src = BUF_H0;
+  if (desc->in_proj_channels > 0) {
+    Layer L;
+    L.name = "in_proj";
+    L.Cin = desc->latent_channels, L.Cout = desc->in_proj_channels, L.K = 1, L.dil = 1;
+    L.level = 0;
+    if (!plan_layer(ctx->use_pair, L, pad, false, why))
+      return bail(fail(ctx, VOC_UNSUPPORTED, "in_proj: " + why));
+    L.in_buf = BUF_H0, L.hl_buf = BUF_HB;
+    st = upload_layer(ctx, ctx->allocs, L, pad, params[0], params[1], nullptr);
+    if (st != VOC_OK) return bail(st);
+    ctx->layers.push_back(L);
+    conv_in_src = BUF_HB;
+    p = 2;
+  }
   // conv_in (no Snake in front); its epilogue applies the Snake of stage 0's ConvT
   {
     Layer L;
     L.name = "conv_in";
-    L.Cin = desc->latent_channels, L.Cout = desc->channels0, L.K = desc->in_kernel, L.dil = 1;
+    L.Cin = desc->in_proj_channels > 0 ? desc->in_proj_channels : desc->latent_channels;
+    L.Cout = desc->channels0, L.K = desc->in_kernel, L.dil = 1;
     L.level = 0;
     if (!plan_layer(ctx->use_pair, L, pad, false, why))
       return bail(fail(ctx, VOC_UNSUPPORTED, "conv_in: " + why));
-    L.in_buf = BUF_H0, L.hl_buf = BUF_H1;
-    st = upload_layer(ctx, ctx->allocs, L, pad, params[0], params[1], params[2]);
+    L.in_buf = conv_in_src, L.hl_buf = BUF_H1;
+    st = upload_layer(ctx, ctx->allocs, L, pad, params[p], params[p + 1], params[p + 2]);
     if (st != VOC_OK) return bail(st);
     ctx->layers.push_back(L);
-    p = 2;
+    p += 2;
   }
   // Three equal hi/lo buffers (H0, H1, HB) and the fp32 residual stream FY.  A layer that
   // reads a hi/lo buffer with a halo never writes that buffer in the same launch (other

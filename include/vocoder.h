@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define VOC_ABI_VERSION 3
+#define VOC_ABI_VERSION 4
 
 typedef struct vocoder vocoder_t;             /* opaque context */
 typedef struct CUstream_st *voc_stream_t;     /* a cudaStream_t */
@@ -98,6 +98,10 @@ typedef struct {
                            256-row MMA, each SM staging half of the weights):
                            0 = library default (off), 1 = on, -1 = off.  A
                            performance choice only, like fuse_max_channels.     */
+  int in_proj_channels; /* 0, or P > 0: a 1x1 projection C_lat -> P with bias and no
+                           weight norm runs before conv_in, which then maps P -> C0
+                           (the published music model's dec_in_proj 64 -> 1024,
+                           minimaxmusic.cpp Architecture, "Flow VAE")          */
 } voc_desc;
 
 /* ABI version of the library (VOC_ABI_VERSION of the build). */
@@ -105,7 +109,8 @@ int vocoder_abi_version(void);
 
 /* Number of parameter tensors of the architecture, or -1 for an invalid desc.
  * Canonical order and PyTorch layouts (weights already folded):
- *   conv_in.w [C0][C_lat][in_kernel], conv_in.b [C0],
+ *   [in_proj.w [P][C_lat][1], in_proj.b [P]]   (only when in_proj_channels = P > 0)
+ *   conv_in.w [C0][C_lat or P][in_kernel], conv_in.b [C0],
  *   per stage i (C_in -> C_out = widths[i], stride s):
  *     snake.alpha [C_in], convT.w [C_in][C_out][2s], convT.b [C_out],
  *     per dilation: snake1.alpha [C_out], conv1.w [C_out][C_out][res_kernel],

@@ -61,7 +61,8 @@ def test_c99_consumer(lib, tmp_path):
     assert "abi_c ok" in res.stdout
 
 
-@pytest.mark.parametrize("arch", [W.TINY, W.MUSIC, W.SPEECH], ids=["tiny", "music", "speech"])
+@pytest.mark.parametrize("arch", [W.TINY, W.MUSIC, W.SPEECH, W.MUSIC_FULL],
+                         ids=["tiny", "music", "speech", "music_full"])
 def test_param_shapes_match_layer_list(lib, arch):
     shapes = arch.param_shapes()
     assert V.vocoder_param_count(arch) == len(shapes)

@@ -230,6 +230,35 @@ def test_decode_fusion_variants(arch, fuse):
     G.compare_audio(ref, got, f"fuse={fuse}")
 
 
+PROJ_MUSIC = W.Arch(latent_channels=64, channels0=384, strides=(8, 8, 4, 2), widths=(192, 96, 96, 48),
+                    in_proj_channels=256)
+
+
+def test_decode_input_projection():
+    """The 1x1 input projection (no weight norm) in front of conv_in, over several waves,
+    against the oracle sample by sample."""
+    wl = W.make_custom(PROJ_MUSIC, B=2, T=60, seed=74)
+    voc = V.Vocoder(PROJ_MUSIC, V.fold_params(wl.params))
+    got = G.gpu_decode(voc, wl.latent)
+    ref = O.decode(PROJ_MUSIC, wl.params, wl.latent)
+    G.compare_audio(ref, got, "in_proj")
+
+
+def test_decode_full_music_model_sampled():
+    """The published 54 M music decoder (dec_in_proj 64 -> 1024, conv_in 1024 -> 1536) on the
+    one-window music latent, checked on sampled windows against the oracle."""
+    wl = W.make_custom(W.MUSIC_FULL, B=2, T=689, seed=2000)
+    folded = O.fold_params(wl.params)
+    voc = V.Vocoder(W.MUSIC_FULL, V.fold_params(wl.params))
+    got = G.gpu_decode(voc, wl.latent)
+    hop = wl.arch.hop
+    assert got.shape == (2, 689 * hop)
+    for item in range(2):
+        for (a, b) in G.sampled_windows(wl.arch, wl.T, n=3, width=8):
+            ref = G.oracle_window(wl, folded, item, a, b)
+            G.compare_audio(ref, got[item, a * hop:b * hop], f"full[{item}][{a}:{b}]")
+
+
 ODD_HEAD = W.Arch(latent_channels=16, channels0=64, strides=(4, 2), widths=(32, 16),
                   in_kernel=5, res_kernel=5, out_kernel=9)
 
