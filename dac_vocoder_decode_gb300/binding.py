@@ -45,6 +45,8 @@ EXPORTED = [
     "vocoder_op_conv_transpose1d", "vocoder_op_residual_unit", "vocoder_launches_per_decode",
     "vocoder_profile_count",
     "vocoder_profile_entry", "vocoder_last_error", "vocoder_destroy",
+    "vocoder_stream_create", "vocoder_stream_decode", "vocoder_stream_reset",
+    "vocoder_stream_destroy",
 ]
 
 
@@ -133,6 +135,14 @@ def load_library():
     lib.vocoder_last_error.argtypes = [P]
     lib.vocoder_destroy.restype = None
     lib.vocoder_destroy.argtypes = [P]
+    lib.vocoder_stream_create.restype = I
+    lib.vocoder_stream_create.argtypes = [P, I, I, ctypes.POINTER(P)]
+    lib.vocoder_stream_decode.restype = I
+    lib.vocoder_stream_decode.argtypes = [P, P, I, P, P, ctypes.c_uint]
+    lib.vocoder_stream_reset.restype = I
+    lib.vocoder_stream_reset.argtypes = [P, P]
+    lib.vocoder_stream_destroy.restype = None
+    lib.vocoder_stream_destroy.argtypes = [P]
     _lib = lib
     return lib
 
@@ -347,6 +357,62 @@ def fold_params(params) -> list:
         else:
             out.append(np.ascontiguousarray(p, dtype=np.float32))
     return out
+
+
+def vocoder_stream_create(h, B: int, max_frames: int) -> ctypes.c_void_p:
+    s = ctypes.c_void_p()
+    _check(load_library().vocoder_stream_create(h, B, max_frames, ctypes.byref(s)), h)
+    return s
+
+
+def vocoder_stream_decode(h, s, latent, audio, stream=None, flags: int = 0) -> None:
+    """latent [B, C_lat, frames] and audio [B, 1, frames*hop]: contiguous fp32 CUDA tensors."""
+    frames = int(latent.shape[2])
+    _check(load_library().vocoder_stream_decode(s, ctypes.c_void_p(latent.data_ptr()), frames,
+                                                 ctypes.c_void_p(audio.data_ptr()),
+                                                 _stream_ptr(stream), flags), h)
+
+
+def vocoder_stream_reset(h, s, stream=None) -> None:
+    _check(load_library().vocoder_stream_reset(s, _stream_ptr(stream)), h)
+
+
+def vocoder_stream_destroy(s) -> None:
+    load_library().vocoder_stream_destroy(s)
+
+
+class VocoderStream:
+    """Stateful chunk-by-chunk decoding of B sequences on a causal decoder (see
+    vocoder_stream_create in include/vocoder.h)."""
+
+    def __init__(self, voc: "Vocoder", B: int, max_frames: int):
+        self.voc = voc
+        self.B = B
+        self.max_frames = max_frames
+        self.handle = vocoder_stream_create(voc.handle, B, max_frames)
+
+    def decode(self, latent, audio=None, stream=None, flags: int = 0):
+        import torch
+        if audio is None:
+            audio = torch.empty((self.B, 1, latent.shape[2] * self.voc.hop), dtype=torch.float32,
+                                device=latent.device)
+        vocoder_stream_decode(self.voc.handle, self.handle, latent.contiguous(), audio, stream,
+                              flags)
+        return audio
+
+    def reset(self, stream=None):
+        vocoder_stream_reset(self.voc.handle, self.handle, stream)
+
+    def close(self):
+        if self.handle:
+            vocoder_stream_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class Vocoder:

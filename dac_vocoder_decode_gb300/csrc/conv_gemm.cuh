@@ -89,9 +89,14 @@ struct ConvGemmArgs {
   const float *alpha;      // [N_total] Snake alpha of the next layer, or null
   const float *invb;       // [N_total] 1/(alpha + 1e-9)
   const float *skip;       // fp32 residual (chunk-major, Cp_out channels) or null: read via TMA
-  float *out_f32;          // fp32 output, chunk-major [B][Cp_out/4][L_in*s_rows][4], or null
-  __nv_bfloat16 *out_hl;   // hi/lo output, chunk-major [B][2*Cp_out/8][L_in*s_rows][8], or null
+  float *out_f32;          // fp32 output, chunk-major [B][Cp_out/4][f32_L][4], or null
+  __nv_bfloat16 *out_hl;   // hi/lo output, chunk-major [B][2*Cp_out/8][hl_L][8], or null
   int Cp_out, s_rows;      // output channels (padded), output rows per D row
+  // Row placement (stateful streaming keeps each layer's left context in front of its new
+  // rows): A row r of D row t is input row in_row0 + t + offset; output row t*s_rows + ph
+  // goes to row f32_row0 + ... of planes of f32_L rows (hl_row0 / hl_L for the hi/lo
+  // output).  A plain decode has 0 offsets and planes of L_in * s_rows rows.
+  int in_row0, f32_row0, f32_L, hl_row0, hl_L;
   int flags;
   int b_resident;          // 1: the nb = taps * nkb weight slots hold this CTA's whole column
                            // tile, loaded once (every CTA keeps one column tile)
@@ -190,9 +195,10 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
   if (t >= p.L_in) return true;
   const int ph = n0 / p.Cp_out;  // ConvT phase of these columns (0 for a conv)
   const int co0 = n0 - ph * p.Cp_out;
-  const size_t L_out = (size_t)p.L_in * p.s_rows;
-  const size_t row = (size_t)t * p.s_rows + ph;
+  const size_t row_t = (size_t)t * p.s_rows + ph;
   if (p.out_f32) {
+    const size_t L_out = static_cast<size_t>(p.f32_L);
+    const size_t row = row_t + p.f32_row0;
     const float *src = (p.flags & EPI_F32_SNAKE) ? sn : v;
     VOC_CHECK((((long long)b * (p.Cp_out / 4) + co0 / 4 + CW / 4 - 1) * (long long)L_out + row) * 4 + 4 <= p.f32_elems,
               14, b, co0, row);
@@ -213,6 +219,8 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
       hw[i] = pack_bf16x2(h0, h1);
       lw[i] = pack_bf16x2(l0, l1);
     }
+    const size_t L_out = static_cast<size_t>(p.hl_L);
+    const size_t row = row_t + p.hl_row0;
     const size_t item = (size_t)b * (2 * p.Cp_out / 8);
     VOC_CHECK((((long long)item + p.Cp_out / 8 + co0 / 8 + CW / 8 - 1) * (long long)L_out + row) * 8 + 8 <= p.hl_elems,
               15, b, co0, row);
@@ -366,7 +374,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int rest = job / p.n_tiles;
         const int mt = rest % p.m_tiles;
         const int b = rest / p.m_tiles;
-        const int y0 = mt * kM + row0 + p.off_min;
+        const int y0 = p.in_row0 + mt * kM + row0 + p.off_min;
         for (int kb = 0; kb < p.nkb; ++kb) {
           const int sa = ia % p.na;
           const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;

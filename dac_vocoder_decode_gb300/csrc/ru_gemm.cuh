@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
         const int mt = tile % p.m_tiles;
         const int b = tile / p.m_tiles;
-        const int y0 = mt * kTileM + p.off_min;
+        const int y0 = p.in_row0 + mt * kTileM + p.off_min;
         for (int kb = 0; kb < p.nkb && ok; ++kb) {
           const int sa = ia % p.na;
           const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;

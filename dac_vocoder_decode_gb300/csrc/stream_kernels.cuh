@@ -14,13 +14,13 @@
 
 namespace voc {
 
-// x [B][C][T] fp32 -> hl chunk-major [B][2*Cp/8][T][8] bf16: 8-channel chunks of the
-// hi parts, then of the lo parts (hi = bf16(v), lo = bf16(v - hi)); channels C..Cp-1
-// are zeros.  alpha == nullptr: no Snake.  One thread per (b, chunk, t):
+// x [B][C][T] fp32 -> hl chunk-major [B][2*Cp/8][Lp][8] bf16 at rows row0..row0+T-1:
+// 8-channel chunks of the hi parts, then of the lo parts (hi = bf16(v), lo = bf16(v - hi));
+// channels C..Cp-1 are zeros.  alpha == nullptr: no Snake.  One thread per (b, chunk, t):
 // block 256, grid (ceil(T/256), Cp/8, B).
 __global__ void prep_hl_kernel(const float *__restrict__ x, int C, int T, int Cp,
                                const float *__restrict__ alpha, const float *__restrict__ invb,
-                               __nv_bfloat16 *__restrict__ hl) {
+                               __nv_bfloat16 *__restrict__ hl, int row0, long long Lp) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   const int c8 = blockIdx.y;
   const int b = blockIdx.z;
@@ -47,14 +47,16 @@ __global__ void prep_hl_kernel(const float *__restrict__ x, int C, int T, int Cp
                 (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
   }
   const size_t item = (size_t)b * (2 * Cp / 8);
-  *reinterpret_cast<uint4 *>(hl + ((item + c8) * T + t) * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-  *reinterpret_cast<uint4 *>(hl + ((item + Cp / 8 + c8) * T + t) * 8) =
+  const size_t r = (size_t)row0 + t;
+  *reinterpret_cast<uint4 *>(hl + ((item + c8) * Lp + r) * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4 *>(hl + ((item + Cp / 8 + c8) * Lp + r) * 8) =
       make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
-// audio[b][t] = tanh(bias + sum_k sum_c w[c][k] * y[b][c][t + k - pad_left]), y zero outside
-// [0, L).  y is fp32 chunk-major [B][Cp/4][L][4] (already Snake'd), w [Cp][K] (zero past the
-// real channels).  One thread per output sample, TILE samples per block; the block stages
+// audio[b][t] = tanh(bias + sum_k sum_c w[c][k] * y[b][c][t + k - pad_left]) for t in [0, L),
+// y zero before row 0 and from row L on.  y is fp32 chunk-major [B][Cp/4][Ly][4] (already
+// Snake'd) with y's row 0 stored at row in_row0 of its planes (the rows before it, if any,
+// hold earlier samples and are read as such), w [Cp][K] (zero past the real channels).  One thread per output sample, TILE samples per block; the block stages
 // its rows chunk by chunk in shared memory ([Cp/4][TILE+K-1][4]), so the global reads are
 // contiguous runs and a warp's shared reads hit consecutive 16-byte words.
 template <int TILE>
@@ -62,7 +64,8 @@ __global__ void __launch_bounds__(TILE) out_head_kernel(const float *__restrict_
                                                         int K, int pad_left,
                                                         const float *__restrict__ w,
                                                         const float *__restrict__ bias,
-                                                        float *__restrict__ audio) {
+                                                        float *__restrict__ audio, int in_row0,
+                                                        long long Ly) {
   extern __shared__ float4 sm4[];
   const int b = blockIdx.y;
   const int t0 = blockIdx.x * TILE;
@@ -71,11 +74,12 @@ __global__ void __launch_bounds__(TILE) out_head_kernel(const float *__restrict_
   float4 *xs = sm4;                                            // [nch][rows]
   float *ws = reinterpret_cast<float *>(sm4 + (size_t)nch * rows);  // [Cp][K]
   for (int i = threadIdx.x; i < Cp * K; i += TILE) ws[i] = w[i];
-  const float4 *yb = reinterpret_cast<const float4 *>(y) + (size_t)b * nch * L;
+  const float4 *yb = reinterpret_cast<const float4 *>(y) + (size_t)b * nch * Ly;
   for (int i = threadIdx.x; i < nch * rows; i += TILE) {
     const int j = i / rows, r = i - j * rows;
-    const int t = t0 - pad_left + r;
-    xs[i] = (t >= 0 && t < L) ? __ldg(yb + (size_t)j * L + t) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const long long t = (long long)in_row0 + t0 - pad_left + r;  // stored row
+    xs[i] = (t >= 0 && t < (long long)in_row0 + L) ? __ldg(yb + (size_t)j * Ly + t)
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
   const int t = t0 + threadIdx.x;
@@ -104,28 +108,30 @@ __global__ void __launch_bounds__(256) out_head_reg_kernel(const float *__restri
                                                             int Cp, int pad_left,
                                                             const float4 *__restrict__ w4,
                                                             const float *__restrict__ bias,
-                                                            float *__restrict__ audio) {
+                                                            float *__restrict__ audio, int in_row0,
+                                                            long long Ly) {
   constexpr int R = TPT + K - 1;  // input rows per chunk
   const int b = blockIdx.y;
   const long long t0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * TPT;
   if (t0 >= L) return;
   const int nch = Cp / 4;
-  const float4 *yb = reinterpret_cast<const float4 *>(y) + (size_t)b * nch * L;
+  const float4 *yb = reinterpret_cast<const float4 *>(y) + (size_t)b * nch * Ly;
   float acc[TPT];
 #pragma unroll
   for (int i = 0; i < TPT; ++i) acc[i] = 0.f;
-  const long long r0 = t0 - pad_left;
-  const bool interior = r0 >= 0 && r0 + R <= L;
+  const long long r0 = in_row0 + t0 - pad_left;  // stored row of the first input
+  const long long rend = (long long)in_row0 + L;  // rows from here on read as zero
+  const bool interior = r0 >= 0 && r0 + R <= rend;
   for (int j0 = 0; j0 < nch; j0 += 2) {
     float4 xs[2][R];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const float4 *row = yb + (size_t)(j0 + u) * L;
+      const float4 *row = yb + (size_t)(j0 + u) * Ly;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const long long t = r0 + r;
-        xs[u][r] = (interior || (t >= 0 && t < L)) ? __ldg(row + t)
-                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        xs[u][r] = (interior || (t >= 0 && t < rend)) ? __ldg(row + t)
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #pragma unroll
@@ -147,6 +153,28 @@ __global__ void __launch_bounds__(256) out_head_reg_kernel(const float *__restri
 #pragma unroll
   for (int i = 0; i < TPT; ++i)
     if (t0 + i < L) audio[(size_t)b * L + t0 + i] = tanhf(bb + acc[i]);
+}
+
+// Row-block copies between chunk-major buffers: job j copies `rows` rows starting at
+// src_row0 + frames * src_rate of each of its `planes` planes (16-byte rows, plane lengths
+// src_L and dst_L) to rows [dst_row0, ...).  Source and destination never overlap.
+// grid (blocks, n_jobs), block 256.
+struct RowCopyJob {
+  const uint4 *src;
+  uint4 *dst;
+  long long src_L, dst_L;
+  int src_row0, src_rate;  // first source row: src_row0 + frames * src_rate
+  int dst_row0, rows, planes;
+};
+__global__ void row_copy_kernel(const RowCopyJob *__restrict__ jobs, int frames) {
+  const RowCopyJob j = jobs[blockIdx.y];
+  const long long n = (long long)j.planes * j.rows;
+  const long long s0 = j.src_row0 + (long long)frames * j.src_rate;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long pl = i / j.rows, r = i - pl * j.rows;
+    j.dst[pl * j.dst_L + j.dst_row0 + r] = j.src[pl * j.src_L + s0 + r];
+  }
 }
 
 // Overlap-crop stitch (minimaxmusic.cpp Architecture, "Decode and stitch"):

@@ -617,6 +617,9 @@ void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *co
   a.out_f32 = L.f32_buf >= 0 ? static_cast<float *>(bufs[L.f32_buf]) : nullptr;
   a.out_hl = L.hl_buf >= 0 ? static_cast<__nv_bfloat16 *>(bufs[L.hl_buf]) : nullptr;
   a.flags = L.epi_flags;
+  a.in_row0 = 0;
+  a.f32_row0 = a.hl_row0 = 0;
+  a.f32_L = a.hl_L = static_cast<int>(L_in * L.g.s_rows);
   a.timeout = ctx->wait_budget;
   a.err = ctx->err_dev;
   a.f32_elems = L.f32_buf >= 0 ? (long long)(bbytes / 4) : 0;
@@ -704,14 +707,17 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
   return VOC_OK;
 }
 
+// y: fp32 chunk-major with planes of Ly rows, sample 0 at row in_row0 (streaming keeps the
+// head's left context in the rows before it); a plain decode passes in_row0 = 0, Ly = L.
 voc_status launch_out_head(vocoder *ctx, const OutHead &h, const float *y, int B, long long L,
-                           float *audio, cudaStream_t stream) {
+                           float *audio, cudaStream_t stream, int in_row0 = 0, long long Ly = -1) {
+  if (Ly < 0) Ly = L;
   if (h.K == 7 && h.w4_dev) {
     const long long threads = (L + kHeadTpt - 1) / kHeadTpt;
     dim3 grid(static_cast<unsigned>((threads + 255) / 256), static_cast<unsigned>(B));
     voc::out_head_reg_kernel<7, kHeadTpt><<<grid, 256, 0, stream>>>(
         y, static_cast<int>(L), h.Cp, h.pad_left, reinterpret_cast<const float4 *>(h.w4_dev),
-        h.b_dev, audio);
+        h.b_dev, audio, in_row0, Ly);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(ctx, e, "launch out_head");
     return VOC_OK;
@@ -719,16 +725,18 @@ voc_status launch_out_head(vocoder *ctx, const OutHead &h, const float *y, int B
   const size_t smem = ((size_t)(kHeadTile + h.K - 1) * h.Cp + (size_t)h.Cp * h.K) * 4;
   dim3 grid(static_cast<unsigned>((L + kHeadTile - 1) / kHeadTile), static_cast<unsigned>(B));
   voc::out_head_kernel<kHeadTile><<<grid, kHeadTile, smem, stream>>>(
-      y, static_cast<int>(L), h.Cp, h.K, h.pad_left, h.w_dev, h.b_dev, audio);
+      y, static_cast<int>(L), h.Cp, h.K, h.pad_left, h.w_dev, h.b_dev, audio, in_row0, Ly);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch out_head");
   return VOC_OK;
 }
 
 voc_status launch_prep(vocoder *ctx, const float *x, int B, int C, int T, int Cp, const float *alpha,
-                       const float *invb, __nv_bfloat16 *hl, cudaStream_t stream) {
+                       const float *invb, __nv_bfloat16 *hl, cudaStream_t stream, int row0 = 0,
+                       long long Lp = -1) {
   dim3 grid((T + 255) / 256, Cp / 8, B);
-  voc::prep_hl_kernel<<<grid, 256, 0, stream>>>(x, C, T, Cp, alpha, invb, hl);
+  voc::prep_hl_kernel<<<grid, 256, 0, stream>>>(x, C, T, Cp, alpha, invb, hl, row0,
+                                                Lp < 0 ? (long long)T : Lp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch prep");
   return VOC_OK;
@@ -1519,4 +1527,262 @@ VOC_API voc_status vocoder_profile_entry(vocoder *ctx, int index, const char **n
 
 VOC_API const char *vocoder_last_error(const vocoder *ctx) {
   return ctx ? ctx->err.c_str() : g_err.c_str();
+}
+
+// ------------------------------------------------------------------ stateful streaming
+// Causal decoders only (VOC_PAD_CAUSAL): every layer looks left only, so decoding a
+// sequence chunk by chunk, with each layer's last input rows carried from one chunk to the
+// next, reproduces the whole-sequence decode exactly (qwentts.cpp Architecture,
+// "Streaming decode (stateful path)").  Each layer reads a dedicated hi/lo input buffer
+// whose planes hold `ctx` rows of left context (the layer's halo, (K-1)*dilation rows for
+// a k-tap conv, one row for a transposed conv) followed by the chunk's new rows; the
+// output head's fp32 input likewise.  The contexts are saved after each chunk and restored
+// before the next; all of them start at zero, which matches the zero padding of a decode
+// that starts at frame 0.  Every layer runs with the plan of the context's whole-sequence
+// decode, so the results are identical, bit for bit.
+struct vocoder_stream {
+  vocoder *ctx = nullptr;
+  int B = 0, max_frames = 0;
+  struct LayerIO {
+    uint8_t *in = nullptr;      // hi/lo input planes: ctx rows, then up to max_frames*rate rows
+    long long plane = 0;        // rows per plane
+    int ctx_rows = 0;
+    int rate = 1;               // input rows per latent frame
+    int consumer = -1;          // layer reading this layer's hi/lo output (-1: none)
+    CUtensorMap map{}, smap{};
+  };
+  std::vector<LayerIO> io;
+  uint8_t *fy = nullptr;        // fp32 residual stream, planes of max_frames*rate rows
+  size_t fy_bytes = 0;
+  uint8_t *head_in = nullptr;   // Snake'd fp32 input of the head: ctx rows, then new rows
+  long long head_plane = 0;
+  int head_ctx = 0;
+  uint8_t *state = nullptr;     // all saved contexts, one contiguous block
+  size_t state_bytes = 0;
+  voc::RowCopyJob *jobs = nullptr;  // device: restore jobs, then save jobs
+  int n_restore = 0, n_save = 0, max_job_elems = 0;
+  uint8_t *block = nullptr;     // the single device allocation holding all of the above
+};
+
+namespace {
+voc_status stream_fail(voc_status st, const std::string &msg) { return fail(nullptr, st, msg); }
+}  // namespace
+
+VOC_API voc_status vocoder_stream_create(vocoder *ctx, int B, int max_frames,
+                                         vocoder_stream **out) {
+  if (!out) return stream_fail(VOC_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!ctx) return stream_fail(VOC_INVALID_ARG, "ctx is NULL");
+  if (ctx->desc.padding != VOC_PAD_CAUSAL)
+    return stream_fail(VOC_UNSUPPORTED, "streaming needs a causal decoder (VOC_PAD_CAUSAL)");
+  if (B < 1 || max_frames < 1 || (long long)max_frames * ctx->hop > 0x7FFFFFFFLL)
+    return stream_fail(VOC_INVALID_ARG, "invalid B / max_frames");
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != ctx->device) return stream_fail(VOC_INVALID_ARG, "current device differs from the context's");
+
+  vocoder_stream *s = new vocoder_stream();
+  s->ctx = ctx, s->B = B, s->max_frames = max_frames;
+  const int nl = static_cast<int>(ctx->layers.size());
+  s->io.resize(nl);
+  // geometry: context rows, input rate, consumer of each hi/lo output
+  for (int l = 0; l < nl; ++l) {
+    const Layer &L = ctx->layers[l];
+    vocoder_stream::LayerIO &io = s->io[l];
+    io.ctx_rows = -L.g.off_min;
+    io.rate = static_cast<int>(level_len(ctx, L.level, 1));
+    io.plane = io.ctx_rows + (long long)max_frames * io.rate;
+    if (L.hl_buf >= 0)
+      for (int m = l + 1; m < nl; ++m)
+        if (ctx->layers[m].in_buf == L.hl_buf) {
+          io.consumer = m;
+          break;
+        }
+  }
+  const OutHead &h = ctx->head;
+  s->head_ctx = h.pad_left;
+  s->head_plane = s->head_ctx + (long long)max_frames * ctx->hop;
+  // sizes of the buffers inside one allocation (each 256-byte aligned)
+  auto hl_bytes = [&](int l) {
+    return rupz((size_t)B * 2 * (ctx->layers[l].Cp_in / 8) * s->io[l].plane * 16, 256);
+  };
+  size_t fy_rows = 0;
+  for (int l = 0; l < nl; ++l) {
+    const Layer &L = ctx->layers[l];
+    const int lv_out = L.convT ? L.level + 1 : L.level;
+    fy_rows = std::max(fy_rows, (size_t)B * (L.Cp_out / 4) * (size_t)max_frames *
+                                    (size_t)level_len(ctx, lv_out, 1));
+  }
+  s->fy_bytes = rupz(fy_rows * 16, 256);
+  const size_t head_bytes = rupz((size_t)B * (h.Cp / 4) * s->head_plane * 16, 256);
+  size_t state_bytes = 0;
+  std::vector<size_t> state_off(nl + 1, 0);
+  for (int l = 0; l < nl; ++l) {
+    state_off[l] = state_bytes;
+    state_bytes += rupz((size_t)B * 2 * (ctx->layers[l].Cp_in / 8) * s->io[l].ctx_rows * 16, 256);
+  }
+  state_off[nl] = state_bytes;  // head context
+  state_bytes += rupz((size_t)B * (h.Cp / 4) * s->head_ctx * 16, 256);
+  s->state_bytes = state_bytes;
+  size_t total = s->fy_bytes + head_bytes + state_bytes;
+  for (int l = 0; l < nl; ++l) total += hl_bytes(l);
+  const size_t jobs_bytes = rupz(sizeof(voc::RowCopyJob) * 2 * (nl + 1), 256);
+  total += jobs_bytes;
+  cudaError_t e = cudaMalloc(&s->block, total);
+  if (e != cudaSuccess) {
+    delete s;
+    return cuda_fail(nullptr, e, "cudaMalloc (stream buffers)");
+  }
+  uint8_t *cur = s->block;
+  for (int l = 0; l < nl; ++l) s->io[l].in = cur, cur += hl_bytes(l);
+  s->fy = cur, cur += s->fy_bytes;
+  s->head_in = cur, cur += head_bytes;
+  s->state = cur, cur += state_bytes;
+  s->jobs = reinterpret_cast<voc::RowCopyJob *>(cur);
+  // copy jobs: restore (state -> context rows), then save (last ctx rows of [ctx | new] -> state)
+  std::vector<voc::RowCopyJob> restore, save;
+  auto add = [&](uint8_t *buf, long long plane, uint8_t *st, int ctx_rows, int rate, int planes) {
+    if (ctx_rows <= 0) return;
+    voc::RowCopyJob r{};
+    r.src = reinterpret_cast<const uint4 *>(st), r.dst = reinterpret_cast<uint4 *>(buf);
+    r.src_L = ctx_rows, r.dst_L = plane, r.src_row0 = 0, r.src_rate = 0, r.dst_row0 = 0;
+    r.rows = ctx_rows, r.planes = planes;
+    restore.push_back(r);
+    voc::RowCopyJob w{};
+    w.src = reinterpret_cast<const uint4 *>(buf), w.dst = reinterpret_cast<uint4 *>(st);
+    w.src_L = plane, w.dst_L = ctx_rows, w.src_row0 = 0, w.src_rate = rate, w.dst_row0 = 0;
+    w.rows = ctx_rows, w.planes = planes;
+    save.push_back(w);
+    s->max_job_elems = std::max(s->max_job_elems, ctx_rows * planes);
+  };
+  for (int l = 0; l < nl; ++l)
+    add(s->io[l].in, s->io[l].plane, s->state + state_off[l], s->io[l].ctx_rows, s->io[l].rate,
+        B * 2 * (ctx->layers[l].Cp_in / 8));
+  add(s->head_in, s->head_plane, s->state + state_off[nl], s->head_ctx, static_cast<int>(ctx->hop),
+      B * (h.Cp / 4));
+  s->n_restore = static_cast<int>(restore.size());
+  s->n_save = static_cast<int>(save.size());
+  std::vector<voc::RowCopyJob> all(restore);
+  all.insert(all.end(), save.begin(), save.end());
+  voc_status st = VOC_OK;
+  if (!all.empty()) {
+    e = cudaMemcpy(s->jobs, all.data(), sizeof(voc::RowCopyJob) * all.size(), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) st = cuda_fail(nullptr, e, "cudaMemcpy (stream jobs)");
+  }
+  if (st == VOC_OK) {
+    e = cudaMemset(s->state, 0, state_bytes);  // zero context = the decode's zero padding
+    if (e != cudaSuccess) st = cuda_fail(nullptr, e, "cudaMemset (stream state)");
+  }
+  // TMA descriptors: fixed buffers and plane lengths
+  for (int l = 0; l < nl && st == VOC_OK; ++l) {
+    const Layer &L = ctx->layers[l];
+    st = encode_map(ctx, &s->io[l].map, s->io[l].in, L.Cp_in, s->io[l].plane, B, L.g.rows, L.g.KB / 8);
+    if (st == VOC_OK && L.skip_buf >= 0)
+      st = encode_skip_map(ctx, &s->io[l].smap, s->fy, L.Cp_out,
+                           (long long)max_frames * level_len(ctx, L.level, 1), B, L.cw);
+    if (st != VOC_OK) g_err = ctx->err;
+  }
+  if (st != VOC_OK) {
+    cudaFree(s->block);
+    delete s;
+    return st;
+  }
+  *out = s;
+  return VOC_OK;
+}
+
+VOC_API voc_status vocoder_stream_reset(vocoder_stream *s, voc_stream_t stream) {
+  if (!s) return stream_fail(VOC_INVALID_ARG, "stream is NULL");
+  cudaError_t e = cudaMemsetAsync(s->state, 0, s->state_bytes, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(s->ctx, e, "cudaMemsetAsync (stream state)");
+  return VOC_OK;
+}
+
+VOC_API voc_status vocoder_stream_decode(vocoder_stream *s, const float *latent_dev, int frames,
+                                         float *audio_dev, voc_stream_t stream_, unsigned flags) {
+  if (!s) return stream_fail(VOC_INVALID_ARG, "stream is NULL");
+  vocoder *ctx = s->ctx;
+  if (!latent_dev || !audio_dev) return fail(ctx, VOC_INVALID_ARG, "latent / audio NULL");
+  if (frames < 1 || frames > s->max_frames)
+    return fail(ctx, VOC_INVALID_ARG, "frames out of [1, max_frames]");
+  if (flags & ~static_cast<unsigned>(VOC_FLAG_SYNC))
+    return fail(ctx, VOC_INVALID_ARG, "only VOC_FLAG_SYNC is accepted");
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != ctx->device) return fail(ctx, VOC_INVALID_ARG, "current device differs from the context's");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const int B = s->B;
+  const int nl = static_cast<int>(ctx->layers.size());
+  cudaError_t e;
+  auto copies = [&](int first, int n) -> voc_status {
+    if (n == 0) return VOC_OK;
+    const int blocks = std::max(1, std::min((s->max_job_elems + 255) / 256, 64));
+    voc::row_copy_kernel<<<dim3(blocks, n), 256, 0, stream>>>(s->jobs + first, frames);
+    cudaError_t ce = cudaGetLastError();
+    return ce == cudaSuccess ? VOC_OK : cuda_fail(ctx, ce, "launch row_copy");
+  };
+  voc_status st = copies(0, s->n_restore);  // contexts of the previous chunk
+  if (st != VOC_OK) return st;
+  st = launch_prep(ctx, latent_dev, B, ctx->desc.latent_channels, frames, ctx->Cp_lat, nullptr,
+                   nullptr, reinterpret_cast<__nv_bfloat16 *>(s->io[0].in), stream, s->io[0].ctx_rows,
+                   s->io[0].plane);
+  if (st != VOC_OK) return st;
+  void *dummy[BUF_COUNT] = {nullptr, nullptr, nullptr, nullptr};
+  for (int l = 0; l < nl; ++l) {
+    const Layer &L = ctx->layers[l];
+    const vocoder_stream::LayerIO &io = s->io[l];
+    ConvGemmArgs a;
+    gemm_launch_args(ctx, L, B, frames, dummy, 0, a);  // rows and tiles of this chunk
+    a.in_row0 = io.ctx_rows;
+    a.skip = L.skip_buf >= 0 ? reinterpret_cast<const float *>(s->fy) : nullptr;
+    a.out_hl = nullptr, a.out_f32 = nullptr;
+    if (L.hl_buf >= 0) {
+      if (io.consumer < 0) return fail(ctx, VOC_UNSUPPORTED, L.name + ": no consumer of its output");
+      const vocoder_stream::LayerIO &c = s->io[io.consumer];
+      a.out_hl = reinterpret_cast<__nv_bfloat16 *>(c.in);
+      a.hl_row0 = c.ctx_rows;
+      a.hl_L = static_cast<int>(c.plane);
+      a.hl_elems = (long long)B * 2 * (L.Cp_out / 8) * c.plane * 8;
+    }
+    if (L.f32_buf >= 0) {
+      if (L.epi_flags & voc::EPI_F32_SNAKE) {  // the head's input, after its context rows
+        a.out_f32 = reinterpret_cast<float *>(s->head_in);
+        a.f32_row0 = s->head_ctx;
+        a.f32_L = static_cast<int>(s->head_plane);
+        a.f32_elems = (long long)B * (L.Cp_out / 4) * s->head_plane * 4;
+      } else {
+        const int lv_out = L.convT ? L.level + 1 : L.level;
+        a.out_f32 = reinterpret_cast<float *>(s->fy);
+        a.f32_row0 = 0;
+        a.f32_L = static_cast<int>((long long)s->max_frames * level_len(ctx, lv_out, 1));
+        a.f32_elems = static_cast<long long>(s->fy_bytes / 4);
+      }
+    }
+    a.L_a = static_cast<int>(io.plane);
+    st = launch_gemm(ctx, L, io.map, io.smap, a, stream);
+    if (st != VOC_OK) return st;
+#ifdef VOC_CHECKS
+    if ((st = check_launch(ctx, "stream " + L.name, stream)) != VOC_OK) return st;
+#endif
+  }
+  const long long Lf = (long long)frames * ctx->hop;
+  st = launch_out_head(ctx, ctx->head, reinterpret_cast<const float *>(s->head_in), B, Lf, audio_dev,
+                       stream, s->head_ctx, s->head_plane);
+  if (st != VOC_OK) return st;
+  st = copies(s->n_restore, s->n_save);  // this chunk's contexts for the next one
+  if (st != VOC_OK) return st;
+  if (flags & VOC_FLAG_SYNC) {
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+    int word = 0;
+    cudaMemcpy(&word, ctx->err_dev, sizeof(int), cudaMemcpyDeviceToHost);
+    if (word) return fail(ctx, VOC_DEVICE_TIMEOUT, "a kernel gave up a bounded wait");
+  }
+  return VOC_OK;
+}
+
+VOC_API void vocoder_stream_destroy(vocoder_stream *s) {
+  if (!s) return;
+  cudaFree(s->block);
+  delete s;
 }

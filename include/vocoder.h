@@ -258,6 +258,40 @@ const char *vocoder_last_error(const vocoder_t *ctx);
 /* Free the context and its device weights (NULL is ignored). */
 void vocoder_destroy(vocoder_t *ctx);
 
+/* ---------------------------------------------------------------- stateful streaming
+ * qwentts.cpp Architecture, "Streaming decode (stateful path)": every layer of a causal
+ * decoder looks left only, so decoding a sequence chunk by chunk (down to one latent frame
+ * at a time) with each layer's left context carried between chunks reproduces the decode
+ * of the whole sequence exactly, with no recomputed context and no seams.  Here each
+ * stride-1 conv keeps its last (K-1)*dilation input rows and each transposed conv its last
+ * input row (its overlap with the next chunk's first outputs); all contexts start at
+ * zero, the zero padding of a decode that starts at frame 0.  The layers run with the
+ * context's own plans, so a streamed sequence equals vocoder_decode of the whole
+ * sequence bit for bit.  Causal decoders (VOC_PAD_CAUSAL) only. */
+typedef struct vocoder_stream vocoder_stream_t;
+
+/* Stream state for B sequences decoded in chunks of up to max_frames latent frames.
+ * Allocates its own device buffers (the per-layer inputs with their context rows, the
+ * saved contexts; about B * max_frames * hop * 200 bytes for the speech decoder) and zeroes
+ * the contexts (synchronously).  ctx must outlive the stream.  VOC_UNSUPPORTED for a
+ * non-causal decoder; VOC_INVALID_ARG for bad sizes or a different current device. */
+voc_status vocoder_stream_create(vocoder_t *ctx, int B, int max_frames, vocoder_stream_t **out);
+
+/* Decode the next `frames` (1..max_frames) latent frames of every sequence:
+ * latent_dev [B][C_lat][frames] fp32 (device), audio_dev [B][1][frames*hop] fp32 (device),
+ * asynchronous on `stream` like vocoder_decode.  Calls on one stream object must be
+ * ordered (one stream, or synchronised); they update its contexts.  flags: 0 or
+ * VOC_FLAG_SYNC (wait and report VOC_DEVICE_TIMEOUT).  Errors as vocoder_decode; the
+ * message is vocoder_last_error(ctx). */
+voc_status vocoder_stream_decode(vocoder_stream_t *s, const float *latent_dev, int frames,
+                                 float *audio_dev, voc_stream_t stream, unsigned flags);
+
+/* Zero every context (asynchronous on `stream`): the next chunk starts a new sequence. */
+voc_status vocoder_stream_reset(vocoder_stream_t *s, voc_stream_t stream);
+
+/* Free the stream's device buffers (NULL is ignored). */
+void vocoder_stream_destroy(vocoder_stream_t *s);
+
 #ifdef __cplusplus
 }
 #endif
