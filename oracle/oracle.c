@@ -249,3 +249,78 @@ int oracle_stitch(const double *decoded, int n_win, int n_sides, int win_frames,
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------ output stage */
+/* minimaxmusic.cpp Architecture, "Post-processing" (readings in oracle.h). */
+static int cmp_double(const void *a, const void *b) {
+  const double x = *(const double *)a, y = *(const double *)b;
+  return (x > y) - (x < y);
+}
+
+double oracle_abs_percentile(const float *x, long n, int peak_clip) {
+  if (n <= 0) return 0.0;
+  double *v = (double *)malloc((size_t)n * sizeof(double));
+  if (!v) return -1.0;
+  for (long i = 0; i < n; ++i) v[i] = fabs((double)x[i]);
+  qsort(v, (size_t)n, sizeof(double), cmp_double);
+  const double q = 1.0 - (double)peak_clip / 1e6;
+  long k = (long)ceil(q * (double)n); /* 1-based rank */
+  if (k < 1) k = 1;
+  if (k > n) k = n;
+  const double r = v[k - 1];
+  free(v);
+  return r;
+}
+
+long oracle_wav_bytes(int n_ch, long len, int bits) {
+  if (n_ch < 1 || len < 0 || (bits != 16 && bits != 24 && bits != 32)) return -1;
+  return 44 + (long)n_ch * len * (bits / 8);
+}
+
+static void put_le(unsigned char *p, unsigned long v, int nbytes) {
+  for (int i = 0; i < nbytes; ++i) p[i] = (unsigned char)((v >> (8 * i)) & 0xFFu);
+}
+
+int oracle_encode_wav(const float *planar, int n_ch, long len, int sample_rate, int bits,
+                      int peak_clip, unsigned char *out) {
+  const long total = oracle_wav_bytes(n_ch, len, bits);
+  if (total < 0 || !planar || !out || sample_rate <= 0 || peak_clip < 0 || peak_clip > 1000000)
+    return -1;
+  const int bps = bits / 8;
+  const long data = (long)n_ch * len * bps;
+  /* RIFF header */
+  memcpy(out, "RIFF", 4);
+  put_le(out + 4, (unsigned long)(36 + data), 4);
+  memcpy(out + 8, "WAVEfmt ", 8);
+  put_le(out + 16, 16, 4);
+  put_le(out + 20, bits == 32 ? 3 : 1, 2);
+  put_le(out + 22, (unsigned long)n_ch, 2);
+  put_le(out + 24, (unsigned long)sample_rate, 4);
+  put_le(out + 28, (unsigned long)sample_rate * n_ch * bps, 4);
+  put_le(out + 32, (unsigned long)(n_ch * bps), 2);
+  put_le(out + 34, (unsigned long)bits, 2);
+  memcpy(out + 36, "data", 4);
+  put_le(out + 40, (unsigned long)data, 4);
+  unsigned char *p = out + 44;
+  if (bits == 32) {
+    for (long t = 0; t < len; ++t)
+      for (int c = 0; c < n_ch; ++c, p += 4) memcpy(p, planar + (long)c * len + t, 4);
+    return 0;
+  }
+  const double level = oracle_abs_percentile(planar, (long)n_ch * len, peak_clip);
+  if (level < 0.0) return -1;
+  /* the gain and the quantisation in IEEE single precision: the integer each sample
+     rounds to is decided in the precision of the GPU path (the level is one of the
+     |x| values, exact in float) */
+  const float gain = level > 0.0 ? 1.0f / (float)level : 1.0f;
+  const float full = (float)((1L << (bits - 1)) - 1);
+  for (long t = 0; t < len; ++t)
+    for (int c = 0; c < n_ch; ++c, p += bps) {
+      float y = planar[(long)c * len + t] * gain;
+      if (y > 1.0f) y = 1.0f;
+      if (y < -1.0f) y = -1.0f;
+      const long q = (long)nearbyintf(y * full); /* default rounding mode: half to even */
+      put_le(p, (unsigned long)q, bps);           /* two's complement, little endian */
+    }
+  return 0;
+}

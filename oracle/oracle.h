@@ -120,3 +120,27 @@ int oracle_stitch(const double *decoded, int n_win, int n_sides, int win_frames,
 }
 #endif
 #endif
+
+/* ------------------------------------------------------------------ output stage
+ * minimaxmusic.cpp Architecture, "Post-processing": planar float output, then percentile
+ * peak normalisation targeting the 1 - peak_clip/1e6 percentile (peak_clip = 0: plain peak
+ * normalisation; 32-bit float output is written raw, without normalisation), then WAV
+ * encoding in memory.  Readings: the percentile is the nearest-rank order statistic of
+ * |x| over every sample of every channel (the ceil(q*n)-th smallest, q = 1 - peak_clip/1e6);
+ * the gain maps it to full scale 1.0 (gain 1 when it is 0); integer samples are
+ * round-half-even(clamp(x*gain, -1, 1) * (2^(bits-1) - 1)) with the gain, the product and
+ * the rounding in IEEE single precision; a WAV file is the 44-byte RIFF
+ * header (PCM format 1 for 16 and 24 bits, IEEE float format 3 for 32 bits) followed by
+ * the samples interleaved across channels, little endian. */
+
+/* The nearest-rank percentile of |x| described above (0 for n = 0). */
+double oracle_abs_percentile(const float *x, long n, int peak_clip);
+
+/* Size in bytes of the WAV file of n_ch channels of len samples at `bits` (16, 24, 32). */
+long oracle_wav_bytes(int n_ch, long len, int bits);
+
+/* Write the WAV file: planar [n_ch][len] float -> out[oracle_wav_bytes(...)].  bits 16 or
+ * 24 apply the normalisation with peak_clip; bits 32 writes the floats unchanged.
+ * Returns 0, or -1 for bad arguments. */
+int oracle_encode_wav(const float *planar, int n_ch, long len, int sample_rate, int bits,
+                      int peak_clip, unsigned char *out);

@@ -66,6 +66,14 @@ def _load():
             lib.oracle_stitch.restype = ctypes.c_int
             lib.oracle_param_count.argtypes = [ctypes.c_void_p]
             lib.oracle_param_count.restype = ctypes.c_int
+            lib.oracle_abs_percentile.argtypes = [F, ctypes.c_long, ctypes.c_int]
+            lib.oracle_abs_percentile.restype = ctypes.c_double
+            lib.oracle_wav_bytes.argtypes = [ctypes.c_int, ctypes.c_long, ctypes.c_int]
+            lib.oracle_wav_bytes.restype = ctypes.c_long
+            lib.oracle_encode_wav.argtypes = [F, ctypes.c_int, ctypes.c_long, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int,
+                                              ctypes.POINTER(ctypes.c_ubyte)]
+            lib.oracle_encode_wav.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -207,3 +215,26 @@ def stitch(decoded: np.ndarray, n_win: int, n_sides: int, win_frames: int, crop_
                            _d(out))
     assert rc == 0
     return out
+
+
+def abs_percentile(x: np.ndarray, peak_clip: int) -> float:
+    """Nearest-rank 1 - peak_clip/1e6 percentile of |x| (output stage normalisation level)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    return float(_load().oracle_abs_percentile(_f(x), x.size, peak_clip))
+
+
+def encode_wav(planar: np.ndarray, sample_rate: int, bits: int, peak_clip: int = 0) -> bytes:
+    """Planar [n_ch, len] float -> WAV file bytes (16/24-bit normalised PCM, or 32-bit float)."""
+    planar = np.ascontiguousarray(planar, dtype=np.float32)
+    if planar.ndim == 1:
+        planar = planar[None]
+    n_ch, n = planar.shape
+    lib = _load()
+    size = lib.oracle_wav_bytes(n_ch, n, bits)
+    if size < 0:
+        raise ValueError("bad WAV geometry")
+    out = (ctypes.c_ubyte * size)()
+    rc = lib.oracle_encode_wav(_f(planar), n_ch, n, sample_rate, bits, peak_clip, out)
+    if rc != 0:
+        raise ValueError("oracle_encode_wav failed")
+    return bytes(out)
