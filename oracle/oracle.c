@@ -12,6 +12,7 @@
  */
 #include "oracle.h"
 
+#include <float.h>
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -312,7 +313,10 @@ int oracle_encode_wav(const float *planar, int n_ch, long len, int sample_rate, 
   /* the gain and the quantisation in IEEE single precision: the integer each sample
      rounds to is decided in the precision of the GPU path (the level is one of the
      |x| values, exact in float) */
-  const float gain = level > 0.0 ? 1.0f / (float)level : 1.0f;
+  float gain = level > 0.0 ? 1.0f / (float)level : 1.0f;
+  /* a subnormal level whose reciprocal overflows takes the largest finite gain, so that
+     zeros stay zero (0 * inf would be undefined) */
+  if (gain > FLT_MAX) gain = FLT_MAX;
   const float full = (float)((1L << (bits - 1)) - 1);
   for (long t = 0; t < len; ++t)
     for (int c = 0; c < n_ch; ++c, p += bps) {

@@ -35,7 +35,9 @@ def _pcm_reference(planar, bits, peak_clip):
     """Samples written with numpy float32 arithmetic and packed by the standard library."""
     x = np.asarray(planar, np.float32)
     level = np.float32(O.abs_percentile(x, peak_clip))
-    gain = np.float32(1.0) / level if level > 0 else np.float32(1.0)
+    with np.errstate(over="ignore"):
+        gain = np.float32(1.0) / level if level > 0 else np.float32(1.0)
+    gain = min(gain, np.finfo(np.float32).max)  # reciprocal of a subnormal level overflows
     full = np.float32((1 << (bits - 1)) - 1)
     y = np.clip(x * gain, np.float32(-1), np.float32(1))
     q = np.rint(y * full).astype(np.int64)  # numpy rounds half to even
@@ -69,6 +71,20 @@ def test_pcm_edge_values():
     assert O.abs_percentile(x, 250000) == 1.0
     vals = np.frombuffer(wav[44:], dtype="<i2")
     assert vals.tolist() == [32767, -32767, 16384, -16384, 32767, -32767, 0, 0]
+
+
+def test_subnormal_level_keeps_zeros_and_order():
+    """All-subnormal input: 1/level overflows single precision; the largest finite gain is
+    used, zeros stay zero and the loudest sample maps to round(level * FLT_MAX * 32767)."""
+    k = np.array([[3, -7, 0, 12, -12, 0, 5]], np.float32)
+    x = k * np.float32(1e-44)  # multiples of 2^-149 * 7 (subnormal)
+    assert 0 < abs(float(x[0, 3])) < float(np.finfo(np.float32).tiny)
+    wav = O.encode_wav(x, 44100, 16, 0)
+    assert wav == _pcm_reference(x, 16, 0)
+    # x = k * 7 * 2^-149 exactly; times FLT_MAX (about 2^128) and 32767 that is k * 0.1093:
+    # 0.33, 0.77, 1.31 and 0.55 for |k| = 3, 7, 12 and 5
+    vals = np.frombuffer(wav[44:], dtype="<i2")
+    assert vals.tolist() == [0, -1, 0, 1, -1, 0, 1]
 
 
 def test_float_wav_is_raw():
