@@ -46,7 +46,8 @@ EXPORTED = [
     "vocoder_profile_count",
     "vocoder_profile_entry", "vocoder_last_error", "vocoder_destroy",
     "vocoder_stream_create", "vocoder_stream_decode", "vocoder_stream_reset",
-    "vocoder_stream_destroy",
+    "vocoder_stream_destroy", "vocoder_wav_bytes", "vocoder_wav_scratch_bytes",
+    "vocoder_encode_wav",
 ]
 
 
@@ -135,6 +136,13 @@ def load_library():
     lib.vocoder_last_error.argtypes = [P]
     lib.vocoder_destroy.restype = None
     lib.vocoder_destroy.argtypes = [P]
+    lib.vocoder_wav_bytes.restype = ctypes.c_size_t
+    lib.vocoder_wav_bytes.argtypes = [I, ctypes.c_longlong, I]
+    lib.vocoder_wav_scratch_bytes.restype = ctypes.c_size_t
+    lib.vocoder_wav_scratch_bytes.argtypes = []
+    lib.vocoder_encode_wav.restype = I
+    lib.vocoder_encode_wav.argtypes = [P, I, ctypes.c_longlong, I, I, I, P, ctypes.c_size_t, P,
+                                       ctypes.c_size_t, P]
     lib.vocoder_stream_create.restype = I
     lib.vocoder_stream_create.argtypes = [P, I, I, ctypes.POINTER(P)]
     lib.vocoder_stream_decode.restype = I
@@ -379,6 +387,44 @@ def vocoder_stream_reset(h, s, stream=None) -> None:
 
 def vocoder_stream_destroy(s) -> None:
     load_library().vocoder_stream_destroy(s)
+
+
+def vocoder_wav_bytes(n_ch: int, length: int, bits: int) -> int:
+    return int(load_library().vocoder_wav_bytes(n_ch, length, bits))
+
+
+def vocoder_wav_scratch_bytes() -> int:
+    return int(load_library().vocoder_wav_scratch_bytes())
+
+
+def vocoder_encode_wav(planar, sample_rate: int, bits: int, peak_clip: int, out, scratch=None,
+                       stream=None) -> None:
+    """planar: contiguous fp32 CUDA tensor [n_ch, len]; out: uint8 CUDA tensor of at least
+    vocoder_wav_bytes bytes; scratch: uint8 CUDA tensor of vocoder_wav_scratch_bytes (16/24
+    bits)."""
+    n_ch, length = (1, int(planar.shape[0])) if planar.dim() == 1 else map(int, planar.shape)
+    sp = ctypes.c_void_p(scratch.data_ptr()) if scratch is not None else None
+    sb = scratch.numel() if scratch is not None else 0
+    _check(load_library().vocoder_encode_wav(ctypes.c_void_p(planar.data_ptr()), n_ch, length,
+                                              sample_rate, bits, peak_clip,
+                                              ctypes.c_void_p(out.data_ptr()), out.numel(), sp,
+                                              sb, _stream_ptr(stream)), None)
+
+
+def encode_wav(planar, sample_rate: int, bits: int = 16, peak_clip: int = 0, stream=None):
+    """Peak-normalise and encode planar [n_ch, len] device audio as a WAV file in a new uint8
+    CUDA tensor (see vocoder_encode_wav in include/vocoder.h)."""
+    import torch
+    planar = planar.contiguous()
+    n_ch, length = (1, planar.shape[0]) if planar.dim() == 1 else planar.shape
+    size = vocoder_wav_bytes(int(n_ch), int(length), bits)
+    if size == 0:
+        raise VocoderError(-1, "bad WAV geometry")
+    # 256 bytes of head room keep the scratch that follows the file 256-byte aligned
+    off = (size + 255) // 256 * 256
+    buf = torch.empty(off + vocoder_wav_scratch_bytes(), dtype=torch.uint8, device=planar.device)
+    vocoder_encode_wav(planar, sample_rate, bits, peak_clip, buf[:size], buf[off:], stream)
+    return buf[:size]
 
 
 class VocoderStream:

@@ -18,6 +18,7 @@
 #include "conv_gemm.cuh"
 #include "ru_gemm.cuh"
 #include "stream_kernels.cuh"
+#include "output_stage.cuh"
 
 #define VOC_API extern "C" __attribute__((visibility("default")))
 
@@ -1785,4 +1786,85 @@ VOC_API void vocoder_stream_destroy(vocoder_stream *s) {
   if (!s) return;
   cudaFree(s->block);
   delete s;
+}
+
+// ------------------------------------------------------------------ output stage
+// minimaxmusic.cpp Architecture, "Post-processing" (see output_stage.cuh).
+namespace {
+constexpr size_t kWavScratch = 256 + 2048 * 4;  // select state, then one 2048-bin histogram
+
+__global__ void select_init_kernel(voc::SelectState *st, unsigned long long k) {
+  if (threadIdx.x == 0) {
+    st->k = k, st->prefix = 0u, st->mask = 0u, st->level = 0.f, st->gain = 1.f;
+  }
+}
+}  // namespace
+
+VOC_API size_t vocoder_wav_bytes(int n_ch, long long len, int bits) {
+  if (n_ch < 1 || n_ch > 65535 || len < 0 || (bits != 16 && bits != 24 && bits != 32)) return 0;
+  const unsigned long long data = (unsigned long long)n_ch * (unsigned long long)len * (bits / 8);
+  if (36 + data > 0xFFFFFFFFull) return 0;  // the RIFF size field is 32 bits
+  return static_cast<size_t>(44 + data);
+}
+
+VOC_API size_t vocoder_wav_scratch_bytes(void) { return kWavScratch; }
+
+VOC_API voc_status vocoder_encode_wav(const float *planar_dev, int n_ch, long long len,
+                                      int sample_rate, int bits, int peak_clip, void *out_dev,
+                                      size_t out_bytes, void *scratch_dev, size_t scratch_bytes,
+                                      voc_stream_t stream_) {
+  const size_t need = vocoder_wav_bytes(n_ch, len, bits);
+  if (!need) return fail(nullptr, VOC_INVALID_ARG, "bad channel count, length or bits (16, 24, 32)");
+  if (sample_rate <= 0 || peak_clip < 0 || peak_clip > 1000000)
+    return fail(nullptr, VOC_INVALID_ARG, "sample_rate must be > 0 and peak_clip in [0, 1e6]");
+  if ((!planar_dev && len > 0) || !out_dev || (reinterpret_cast<uintptr_t>(out_dev) & 3))
+    return fail(nullptr, VOC_INVALID_ARG, "planar / out NULL, or out not 4-byte aligned");
+  if (out_bytes < need) return fail(nullptr, VOC_WORKSPACE_TOO_SMALL, "out smaller than vocoder_wav_bytes");
+  if (bits != 32 && (!scratch_dev || scratch_bytes < kWavScratch ||
+                     (reinterpret_cast<uintptr_t>(scratch_dev) & 255)))
+    return fail(nullptr, VOC_WORKSPACE_TOO_SMALL, "scratch NULL, unaligned or smaller than vocoder_wav_scratch_bytes");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const long long n = (long long)n_ch * len;
+  const uint32_t bps = static_cast<uint32_t>(bits / 8);
+  const uint32_t data = static_cast<uint32_t>(n * bps);
+  voc::WavHeader h{};
+  h.w[0] = 0x46464952u;  // "RIFF"
+  h.w[1] = 36u + data;
+  h.w[2] = 0x45564157u;  // "WAVE"
+  h.w[3] = 0x20746d66u;  // "fmt "
+  h.w[4] = 16u;
+  h.w[5] = (bits == 32 ? 3u : 1u) | (static_cast<uint32_t>(n_ch) << 16);
+  h.w[6] = static_cast<uint32_t>(sample_rate);
+  h.w[7] = static_cast<uint32_t>(sample_rate) * static_cast<uint32_t>(n_ch) * bps;
+  h.w[8] = (static_cast<uint32_t>(n_ch) * bps) | (static_cast<uint32_t>(bits) << 16);
+  h.w[9] = 0x61746164u;  // "data"
+  h.w[10] = data;
+  uint8_t *out = static_cast<uint8_t *>(out_dev);
+  voc::wav_header_kernel<<<1, 32, 0, stream>>>(h, out);
+  voc::SelectState *st = static_cast<voc::SelectState *>(scratch_dev);
+  if (bits != 32 && n > 0) {
+    // rank of the level: ceil(q * n) with q = 1 - peak_clip / 1e6, in double (as specified)
+    const double q = 1.0 - static_cast<double>(peak_clip) / 1e6;
+    long long k = static_cast<long long>(std::ceil(q * static_cast<double>(n)));
+    k = std::min(std::max(k, 1LL), n);
+    unsigned int *hist = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(scratch_dev) + 256);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 4LL * std::max(sms, 1)));
+    cudaMemsetAsync(hist, 0, 2048 * 4, stream);
+    select_init_kernel<<<1, 32, 0, stream>>>(st, static_cast<unsigned long long>(k));
+    voc::select_hist_kernel<11><<<blocks, 256, 0, stream>>>(planar_dev, n, 21, st, hist);
+    voc::select_pick_kernel<11><<<1, 256, 0, stream>>>(st, hist, 21, 0);
+    voc::select_hist_kernel<11><<<blocks, 256, 0, stream>>>(planar_dev, n, 10, st, hist);
+    voc::select_pick_kernel<11><<<1, 256, 0, stream>>>(st, hist, 10, 0);
+    voc::select_hist_kernel<10><<<blocks, 256, 0, stream>>>(planar_dev, n, 0, st, hist);
+    voc::select_pick_kernel<10><<<1, 256, 0, stream>>>(st, hist, 0, 1);
+  }
+  if (n > 0)
+    voc::wav_encode_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+        planar_dev, n_ch, len, static_cast<int>(bps), st, out + 44);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "launch output stage");
+  return VOC_OK;
 }

@@ -292,6 +292,32 @@ voc_status vocoder_stream_reset(vocoder_stream_t *s, voc_stream_t stream);
 /* Free the stream's device buffers (NULL is ignored). */
 void vocoder_stream_destroy(vocoder_stream_t *s);
 
+/* ---------------------------------------------------------------- output stage
+ * minimaxmusic.cpp Architecture, "Post-processing": the planar float output is peak
+ * normalised to the 1 - peak_clip/1e6 percentile (peak_clip = 0: plain peak
+ * normalisation) and encoded as a WAV file in memory; 32-bit float files are written raw,
+ * without normalisation.  The level is the ceil(q*n)-th smallest |x| over all samples of
+ * all channels (q = 1 - peak_clip/1e6, computed in double), found exactly on the device;
+ * the gain is 1/level in IEEE single precision (1 for a level of 0); integer samples are
+ * round-half-even(clamp(x*gain, -1, 1) * (2^(bits-1) - 1)) in single precision.  The
+ * file is a 44-byte RIFF/WAVE header (PCM format 1 for 16/24 bits, IEEE float format 3
+ * for 32 bits) followed by the samples interleaved across channels, little endian. */
+
+/* Size of the WAV file of n_ch channels x len samples at `bits` (16, 24 or 32), or 0 for
+ * invalid arguments or a file beyond the format's 4 GiB limit. */
+size_t vocoder_wav_bytes(int n_ch, long long len, int bits);
+
+/* Device scratch the 16/24-bit encoder needs (256-byte aligned; a few KB). */
+size_t vocoder_wav_scratch_bytes(void);
+
+/* Encode planar [n_ch][len] fp32 (device) into the WAV file at out_dev (device, at least
+ * vocoder_wav_bytes, 4-byte aligned), asynchronously on `stream`.  scratch_dev (device,
+ * vocoder_wav_scratch_bytes, caller-owned) is used for bits 16 and 24 and may be NULL for
+ * 32.  VOC_INVALID_ARG for bad arguments, VOC_WORKSPACE_TOO_SMALL for short buffers. */
+voc_status vocoder_encode_wav(const float *planar_dev, int n_ch, long long len, int sample_rate,
+                              int bits, int peak_clip, void *out_dev, size_t out_bytes,
+                              void *scratch_dev, size_t scratch_bytes, voc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

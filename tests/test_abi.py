@@ -96,6 +96,19 @@ def test_stitched_length(lib):
     assert O.stitched_length(3, 10, 6, 5, 4) == -1
 
 
+def test_wav_sizes(lib):
+    """Host-only size queries of the output stage agree with the oracle's file layout."""
+    for n_ch, n, bits in [(1, 0, 16), (2, 7, 24), (3, 999, 32), (2, 1000, 16)]:
+        wav = O.encode_wav(np.zeros((n_ch, n), np.float32), 44100, bits)
+        assert V.vocoder_wav_bytes(n_ch, n, bits) == len(wav)
+    assert V.vocoder_wav_bytes(2, 1589248, 24) == 44 + 2 * 1589248 * 3
+    assert V.vocoder_wav_bytes(1, 10, 8) == 0
+    assert V.vocoder_wav_bytes(0, 10, 16) == 0
+    assert V.vocoder_wav_bytes(1, -1, 16) == 0
+    assert V.vocoder_wav_bytes(1, 1 << 31, 16) == 0  # beyond the 32-bit RIFF size field
+    assert V.vocoder_wav_scratch_bytes() >= 256 + 4 * 2048
+
+
 def test_create_validates_before_device_work(lib):
     bad = W.Arch(latent_channels=4, channels0=8, strides=(3, 2), widths=(4, 4))  # odd, symmetric
     with pytest.raises(V.VocoderError) as e:
