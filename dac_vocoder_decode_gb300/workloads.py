@@ -10,7 +10,9 @@ Distributions (no trained weights exist for this decoder here, so every input
 is synthetic):
 
 * latent ~ N(0, 1) fp32, shape [B, C_lat, T].
-* alpha  ~ U(0.5, 1.5) per channel for every Snake.
+* alpha  ~ U(0.5, 1.5) per channel for every Snake; for SnakeBeta decoders (log-scale
+  alpha and beta) log U(0.5, 1.5) for each of the two, so that exp(alpha) and exp(beta)
+  have the plain Snake's alpha distribution.
 * convolution weights in weight-norm form (g, v):
   - "literal" (tiny decoder): g, v, bias ~ N(0, 0.02).
   - "calibrated" (all other workloads): v ~ N(0, 1), g = gain * U(0.9, 1.1),
@@ -49,6 +51,9 @@ class Arch:
     # 0, or P: a 1x1 projection C_lat -> P (bias, no weight norm) before conv_in (the
     # published music model's dec_in_proj 64 -> 1024; conv_in then maps P -> channels0)
     in_proj_channels: int = 0
+    # SnakeBeta activations (the speech codec's, qwentts.cpp Architecture): every Snake
+    # parameter is [2, C], log-scale alpha then log-scale beta
+    snake_beta: bool = False
 
     @property
     def hop(self) -> int:
@@ -63,8 +68,12 @@ class Arch:
         """Canonical order and PyTorch layouts of the folded parameter tensors.
 
         conv weights [C_out, C_in, K]; transposed-conv weights [C_in, C_out, K];
-        biases [C_out]; Snake alphas [C]."""
+        biases [C_out]; Snake alphas [C] (SnakeBeta: [2, C], log alpha and log beta)."""
         out: List[Tuple[str, Tuple[int, ...]]] = []
+
+        def sn(c):
+            return (2, c) if self.snake_beta else (c,)
+
         c_in = self.latent_channels
         if self.in_proj_channels:
             out.append(("in_proj.w", (self.in_proj_channels, self.latent_channels, 1)))
@@ -73,18 +82,18 @@ class Arch:
         out.append(("conv_in.w", (self.channels0, c_in, self.in_kernel)))
         out.append(("conv_in.b", (self.channels0,)))
         for i, ((cin, cout), s) in enumerate(zip(self.stage_channels(), self.strides)):
-            out.append((f"block{i}.snake.alpha", (cin,)))
+            out.append((f"block{i}.snake.alpha", sn(cin)))
             out.append((f"block{i}.convT.w", (cin, cout, 2 * s)))
             out.append((f"block{i}.convT.b", (cout,)))
             for j, _d in enumerate(self.dilations):
-                out.append((f"block{i}.res{j}.snake1.alpha", (cout,)))
+                out.append((f"block{i}.res{j}.snake1.alpha", sn(cout)))
                 out.append((f"block{i}.res{j}.conv1.w", (cout, cout, self.res_kernel)))
                 out.append((f"block{i}.res{j}.conv1.b", (cout,)))
-                out.append((f"block{i}.res{j}.snake2.alpha", (cout,)))
+                out.append((f"block{i}.res{j}.snake2.alpha", sn(cout)))
                 out.append((f"block{i}.res{j}.conv2.w", (cout, cout, 1)))
                 out.append((f"block{i}.res{j}.conv2.b", (cout,)))
         c_last = self.widths[-1]
-        out.append(("snake_out.alpha", (c_last,)))
+        out.append(("snake_out.alpha", sn(c_last)))
         out.append(("conv_out.w", (1, c_last, self.out_kernel)))
         out.append(("conv_out.b", (1,)))
         return out
@@ -179,8 +188,10 @@ def gen_params(arch: Arch, recipe: str, seed_w: int, seed_a: int) -> list:
     def bias(n):
         return (rw.standard_normal((n,), dtype=np.float32) * np.float32(0.02))
 
-    def alpha(n):
-        return ra.uniform(0.5, 1.5, size=(n,)).astype(np.float32)
+    def alpha(shape):
+        if len(shape) == 2:  # SnakeBeta: log alpha, log beta
+            return np.log(ra.uniform(0.5, 1.5, size=shape)).astype(np.float32)
+        return ra.uniform(0.5, 1.5, size=shape).astype(np.float32)
 
     shapes = arch.param_shapes()
     out = []
@@ -188,7 +199,7 @@ def gen_params(arch: Arch, recipe: str, seed_w: int, seed_a: int) -> list:
     while i < len(shapes):
         name, shape = shapes[i]
         if name.endswith(".alpha"):
-            out.append(alpha(shape[0]))
+            out.append(alpha(shape))
             i += 1
             continue
         assert name.endswith(".w")

@@ -54,6 +54,17 @@ void oracle_snake_row(const double *x, long n, double alpha, int identity, doubl
   }
 }
 
+/* qwentts.cpp Architecture, "Audio tokenizer decoder": SnakeBeta exponentiates its stored
+   alpha and beta; the divisor keeps the 1e-9 of the Snake formula. */
+void oracle_snake_beta_row(const double *x, long n, double log_alpha, double log_beta, double *y) {
+  const double a = exp(log_alpha);
+  const double inv_b = 1.0 / (exp(log_beta) + 1e-9);
+  for (long i = 0; i < n; ++i) {
+    double s = sin(a * x[i]);
+    y[i] = x[i] + s * s * inv_b;
+  }
+}
+
 int oracle_conv1d(const double *x, int Cin, int T, const double *w, const double *b, int Cout,
                   int K, int dil, int pad_left, int pad_right, double *y) {
   long T_out = (long)T + pad_left + pad_right - (long)dil * (K - 1);
@@ -103,11 +114,17 @@ int oracle_conv_transpose1d(const double *x, int Cin, int T, const double *w, co
   return 0;
 }
 
-/* Snake applied per channel row of a [C][L] activation, alpha[c] per channel. */
-static void snake_rows(const double *x, int C, long L, const double *alpha, int identity,
+/* Snake applied per channel row of a [C][L] activation: alpha[c] per channel, or for
+   SnakeBeta (beta != 0) log alpha in p[c] and log beta in p[C + c]. */
+static void snake_rows(const double *x, int C, long L, const double *p, int identity, int beta,
                        double *y) {
 #pragma omp parallel for schedule(static)
-  for (int c = 0; c < C; ++c) oracle_snake_row(x + (long)c * L, L, alpha[c], identity, y + (long)c * L);
+  for (int c = 0; c < C; ++c) {
+    if (beta && !identity)
+      oracle_snake_beta_row(x + (long)c * L, L, p[c], p[C + c], y + (long)c * L);
+    else
+      oracle_snake_row(x + (long)c * L, L, p[c], identity, y + (long)c * L);
+  }
 }
 
 static void conv_pads(int padding, int K, int dil, int *pl, int *pr) {
@@ -183,7 +200,7 @@ int oracle_decode(const oracle_arch *a, const double *const *params, const float
       const int stride = a->strides[st];
       const int Cout = a->widths[st];
       /* snake -> transposed conv, k = 2s */
-      snake_rows(x, C, L, params[p], ident, s);
+      snake_rows(x, C, L, params[p], ident, a->snake_beta, s);
       const int Kt = 2 * stride;
       const int pad_t = (a->padding == ORACLE_PAD_CAUSAL) ? 0 : stride / 2;
       oracle_conv_transpose1d(s, C, (int)L, params[p + 1], params[p + 2], Cout, Kt, stride, pad_t,
@@ -194,17 +211,17 @@ int oracle_decode(const oracle_arch *a, const double *const *params, const float
       /* residual units */
       for (int r = 0; r < a->n_dilations; ++r) {
         const int d = a->dilations[r];
-        snake_rows(x, C, L, params[p], ident, s);
+        snake_rows(x, C, L, params[p], ident, a->snake_beta, s);
         conv_pads(a->padding, a->res_kernel, d, &pl, &pr);
         oracle_conv1d(s, C, (int)L, params[p + 1], params[p + 2], C, a->res_kernel, d, pl, pr, h);
-        snake_rows(h, C, L, params[p + 3], ident, s);
+        snake_rows(h, C, L, params[p + 3], ident, a->snake_beta, s);
         oracle_conv1d(s, C, (int)L, params[p + 4], params[p + 5], C, 1, 1, 0, 0, h);
         for (long i = 0; i < (long)C * L; ++i) x[i] += h[i];
         p += 6;
       }
     }
     /* snake_out -> conv_out (with bias) -> tanh */
-    snake_rows(x, C, L, params[p], ident, s);
+    snake_rows(x, C, L, params[p], ident, a->snake_beta, s);
     conv_pads(a->padding, a->out_kernel, 1, &pl, &pr);
     double *y = audio + (long)bi * L_out;
     oracle_conv1d(s, C, (int)L, params[p + 1], params[p + 2], 1, a->out_kernel, 1, pl, pr, y);

@@ -63,6 +63,9 @@ typedef struct {
   int in_proj_channels;/* 0, or P: a 1x1 projection C_lat -> P (with bias, no weight norm)
                           before conv_in, which then maps P -> C_0 (the published music
                           model's dec_in_proj 64 -> 1024)                              */
+  int snake_beta;      /* 0: Snake with alpha used as stored; 1: SnakeBeta, every Snake
+                          parameter holds two rows [2][C] of log-scale alpha and beta
+                          (qwentts.cpp Architecture, "Audio tokenizer decoder")         */
 } oracle_arch;
 
 /* number of parameter tensors of the stack, in the canonical order:
@@ -72,7 +75,8 @@ typedef struct {
  *     snake.alpha [Cin], convT.w [Cin][Cout][2s], convT.b [Cout],
  *     for each dilation d: snake1.alpha [Cout], conv1.w [Cout][Cout][Kres],
  *       conv1.b [Cout], snake2.alpha [Cout], conv2.w [Cout][Cout][1], conv2.b [Cout]
- *   snake_out.alpha [C_last], conv_out.w [1][C_last][Kout], conv_out.b [1]      */
+ *   snake_out.alpha [C_last], conv_out.w [1][C_last][Kout], conv_out.b [1]
+ * With snake_beta every snake*.alpha entry is [2][C] instead: log alpha, then log beta. */
 int oracle_param_count(const oracle_arch *a);
 
 /* w[i, :] = g[i] * v[i, :] / ||v[i, :]||, the norm taken over everything but
@@ -84,6 +88,10 @@ int oracle_fold_weight_norm(const float *g, const float *v, int dim0, long rest,
 /* y[i] = x[i] + sin^2(alpha*x[i]) / (alpha + 1e-9) for one channel row of n values.
  * identity != 0 gives y = x. */
 void oracle_snake_row(const double *x, long n, double alpha, int identity, double *y);
+
+/* SnakeBeta with log-scale parameters: y[i] = x[i] + sin^2(e^la * x[i]) / (e^lb + 1e-9)
+ * for one channel row of n values (exp applied to the stored alpha and beta). */
+void oracle_snake_beta_row(const double *x, long n, double log_alpha, double log_beta, double *y);
 
 /* y[co][t] = b[co] + sum_ci sum_k w[co][ci][k] * x[ci][t + k*dil - pad_left],
  * x taken as zero outside [0, T).  Output length T + pad_left + pad_right - dil*(K-1).

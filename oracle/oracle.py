@@ -49,6 +49,9 @@ def _load():
             lib.oracle_fold_weight_norm.restype = ctypes.c_int
             lib.oracle_snake_row.argtypes = [D, ctypes.c_long, ctypes.c_double, ctypes.c_int, D]
             lib.oracle_snake_row.restype = None
+            lib.oracle_snake_beta_row.argtypes = [D, ctypes.c_long, ctypes.c_double,
+                                                  ctypes.c_double, D]
+            lib.oracle_snake_beta_row.restype = None
             lib.oracle_conv1d.argtypes = [D, ctypes.c_int, ctypes.c_int, D, D, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, D]
             lib.oracle_conv1d.restype = ctypes.c_int
@@ -93,7 +96,7 @@ class _ArchC(ctypes.Structure):
                 ("n_dilations", ctypes.c_int), ("dilations", ctypes.POINTER(ctypes.c_int)),
                 ("res_kernel", ctypes.c_int), ("out_kernel", ctypes.c_int),
                 ("padding", ctypes.c_int), ("flags", ctypes.c_int),
-                ("in_proj_channels", ctypes.c_int)]
+                ("in_proj_channels", ctypes.c_int), ("snake_beta", ctypes.c_int)]
 
 
 def fold_weight_norm(g: np.ndarray, v: np.ndarray) -> np.ndarray:
@@ -117,6 +120,17 @@ def snake(x: np.ndarray, alpha: np.ndarray, identity: bool = False) -> np.ndarra
     C, L = x.shape
     for c in range(C):
         lib.oracle_snake_row(_d(x[c]), L, float(alpha[c]), int(identity), _d(y[c]))
+    return y
+
+
+def snake_beta(x: np.ndarray, log_alpha: np.ndarray, log_beta: np.ndarray) -> np.ndarray:
+    """Per-channel SnakeBeta (log-scale alpha and beta) of a [C, L] array."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    C, L = x.shape
+    for c in range(C):
+        lib.oracle_snake_beta_row(_d(x[c]), L, float(log_alpha[c]), float(log_beta[c]), _d(y[c]))
     return y
 
 
@@ -183,7 +197,7 @@ def decode(arch, params: Sequence, latent: np.ndarray, flags: int = 0, folded: O
     dils = (ctypes.c_int * len(arch.dilations))(*arch.dilations)
     a = _ArchC(arch.latent_channels, arch.channels0, arch.in_kernel, len(arch.strides), strides,
                widths, len(arch.dilations), dils, arch.res_kernel, arch.out_kernel, arch.padding,
-               flags, getattr(arch, "in_proj_channels", 0))
+               flags, getattr(arch, "in_proj_channels", 0), int(getattr(arch, "snake_beta", False)))
     n = lib.oracle_param_count(ctypes.byref(a))
     assert n == len(folded), (n, len(folded))
     ptrs = (ctypes.POINTER(ctypes.c_double) * n)()

@@ -471,3 +471,69 @@ def test_identity_projection_reproduces_plain_decoder():
     w_in_full2[:, 7, :] = w_in[:, 0, :]
     y2 = O.decode(full, None, wl.latent, 0, [proj2, np.zeros(16), w_in_full2] + folded[1:])
     assert np.max(np.abs(y2 - y0)) > 1e-3
+
+
+# ----------------------------------------------------------------------------- SnakeBeta
+@pytest.mark.parametrize("la,lb", [(0.0, 0.0), (math.log(1.37), math.log(0.61)), (-0.4, 0.9)])
+def test_snake_beta_closed_form_points(la, lb):
+    """y = x + sin^2(e^la x) / (e^lb + 1e-9): zero at the zeros of sin, 1/(e^lb + 1e-9) added
+    at its peaks, and sin^2 = 1/2 at an eighth of the period."""
+    a, b = math.exp(la), math.exp(lb)
+    k = np.arange(-5, 6, dtype=np.float64)
+    zeros = k * math.pi / a
+    peaks = (k + 0.5) * math.pi / a
+    eighth = (k + 0.25) * math.pi / a
+    y0 = O.snake_beta(zeros[None], [la], [lb])[0]
+    y1 = O.snake_beta(peaks[None], [la], [lb])[0]
+    y2 = O.snake_beta(eighth[None], [la], [lb])[0]
+    np.testing.assert_allclose(y0, zeros, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(y1, peaks + 1.0 / (b + 1e-9), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(y2, eighth + 0.5 / (b + 1e-9), rtol=0, atol=1e-12)
+
+
+def test_snake_beta_period_and_equal_parameters():
+    rng = np.random.default_rng(31)
+    x = rng.uniform(-20, 20, size=(1, 500))
+    la, lb = 0.3, -0.2
+    per = math.pi / math.exp(la)
+    d0 = O.snake_beta(x, [la], [lb]) - x
+    d1 = O.snake_beta(x + per, [la], [lb]) - (x + per)
+    np.testing.assert_allclose(d0, d1, rtol=0, atol=1e-11)
+    # alpha = beta: plain Snake with alpha = e^la
+    np.testing.assert_allclose(O.snake_beta(x, [la], [la]), O.snake(x, [math.exp(la)]),
+                               rtol=0, atol=1e-13)
+
+
+def test_snake_beta_decoder_uses_both_rows():
+    """The decoder reads every SnakeBeta parameter as [log alpha; log beta]:
+    (a) beta = alpha decodes like the plain-Snake decoder with alpha' = e^alpha;
+    (b) beta = 80 (divisor e^80) decodes like the decoder with Snake replaced by identity,
+    and swapping the rows (alpha = 80) does not."""
+    plain = W.Arch(latent_channels=6, channels0=24, strides=(4, 2), widths=(12, 8))
+    beta = W.Arch(latent_channels=6, channels0=24, strides=(4, 2), widths=(12, 8),
+                  snake_beta=True)
+    wl = W.make_custom(plain, B=2, T=14, seed=91)
+    folded = O.fold_params(wl.params)
+    kinds = [n for n, _ in plain.param_shapes()]
+    rng = np.random.default_rng(5)
+
+    def with_snakes(fn):
+        return [fn(f) if k.endswith(".alpha") else f for k, f in zip(kinds, folded)]
+
+    logs = {}
+
+    def equal_rows(f):
+        la = np.log(rng.uniform(0.5, 1.5, size=f.shape))
+        logs[id(f)] = la
+        return np.stack([la, la])
+
+    fb = with_snakes(equal_rows)
+    fp = [np.exp(logs[id(f)]) if k.endswith(".alpha") else f for k, f in zip(kinds, folded)]
+    np.testing.assert_allclose(O.decode(beta, None, wl.latent, 0, fb),
+                               O.decode(plain, None, wl.latent, 0, fp), rtol=0, atol=1e-12)
+
+    fb80 = with_snakes(lambda f: np.stack([np.full(f.shape, 0.3), np.full(f.shape, 80.0)]))
+    ident = O.decode(plain, None, wl.latent, O.FLAG_SNAKE_IDENTITY, folded)
+    np.testing.assert_allclose(O.decode(beta, None, wl.latent, 0, fb80), ident, rtol=0, atol=1e-12)
+    swapped = with_snakes(lambda f: np.stack([np.full(f.shape, 80.0), np.full(f.shape, 0.3)]))
+    assert np.max(np.abs(O.decode(beta, None, wl.latent, 0, swapped) - ident)) > 1e-3
