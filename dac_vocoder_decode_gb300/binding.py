@@ -15,7 +15,7 @@ import numpy as np
 
 from . import build as _build
 
-VOC_ABI_VERSION = 4
+VOC_ABI_VERSION = 5
 VOC_OK = 0
 VOC_INVALID_ARG = -1
 VOC_UNSUPPORTED = -2
@@ -28,6 +28,8 @@ VOC_DEVICE_TIMEOUT = -8
 VOC_PAD_SYMMETRIC = 0
 VOC_PAD_CAUSAL = 1
 VOC_PREC_BF16X3 = 0
+VOC_SNAKE = 0
+VOC_SNAKE_BETA = 1
 VOC_FLAG_CHECK_FINITE = 1
 VOC_FLAG_SYNC = 2
 VOC_FLAG_PROFILE = 4
@@ -66,7 +68,7 @@ class VocDesc(ctypes.Structure):
                 ("out_kernel", ctypes.c_int), ("out_channels", ctypes.c_int),
                 ("padding", ctypes.c_int), ("precision", ctypes.c_int),
                 ("fuse_max_channels", ctypes.c_int), ("cta_pair", ctypes.c_int),
-                ("in_proj_channels", ctypes.c_int)]
+                ("in_proj_channels", ctypes.c_int), ("snake", ctypes.c_int)]
 
 
 _lib = None
@@ -184,7 +186,8 @@ def make_desc(arch, fuse_max_channels: int = 0, cta_pair: int = 0) -> VocDesc:
     d = VocDesc(VOC_ABI_VERSION, arch.latent_channels, arch.in_kernel, arch.channels0,
                 len(arch.strides), strides, widths, len(arch.dilations), dils, arch.res_kernel,
                 arch.out_kernel, 1, arch.padding, VOC_PREC_BF16X3, fuse_max_channels, cta_pair,
-                getattr(arch, "in_proj_channels", 0))
+                getattr(arch, "in_proj_channels", 0),
+                VOC_SNAKE_BETA if getattr(arch, "snake_beta", False) else VOC_SNAKE)
     d._keep = (strides, widths, dils)
     return d
 

@@ -447,25 +447,51 @@ voc_status upload(vocoder *ctx, std::vector<void *> &allocs, const std::vector<T
   return VOC_OK;
 }
 
+// Per-channel coefficients of one Snake: y = x + sin^2(a x) * ib.  Snake: a = alpha,
+// ib = 1 / (alpha + 1e-9); SnakeBeta (log-scale parameters, p = [log alpha | log beta]):
+// a = e^alpha, ib = 1 / (e^beta + 1e-9); formed in double, rounded once to fp32.  Empty:
+// no Snake.
+struct SnakeCoef {
+  std::vector<float> a, ib;
+};
+
+SnakeCoef snake_coef(const float *p, int C, int kind) {
+  SnakeCoef s;
+  if (!p) return s;
+  s.a.resize(C);
+  s.ib.resize(C);
+  for (int c = 0; c < C; ++c) {
+    if (kind == VOC_SNAKE_BETA) {
+      s.a[c] = static_cast<float>(std::exp(static_cast<double>(p[c])));
+      s.ib[c] = static_cast<float>(1.0 / (std::exp(static_cast<double>(p[C + c])) + 1e-9));
+    } else {
+      s.a[c] = p[c];
+      s.ib[c] = static_cast<float>(1.0 / (static_cast<double>(p[c]) + 1e-9));
+    }
+  }
+  return s;
+}
+
 // Per-column epilogue vectors of a layer: bias, and the Snake of the layer that
-// consumes this output (alpha == nullptr: none).
+// consumes this output (empty coefficients: none).
 voc_status upload_columns(vocoder *ctx, std::vector<void *> &allocs, Layer &L, const float *bias,
-                          const float *alpha) {
+                          const SnakeCoef &sn) {
   const int N = L.g.N_total;
+  const bool has_snake = !sn.a.empty();
   std::vector<float> b(N, 0.f), a(N, 1.f), ib(N, 0.f);
   for (int n = 0; n < N; ++n) {
     const int co = n % L.Cp_out;
     if (co < L.Cout) {
       if (bias) b[n] = bias[co];
-      if (alpha) {
-        a[n] = alpha[co];
-        ib[n] = static_cast<float>(1.0 / (static_cast<double>(alpha[co]) + 1e-9));
+      if (has_snake) {
+        a[n] = sn.a[co];
+        ib[n] = sn.ib[co];
       }
     }
   }
   voc_status st = upload(ctx, allocs, b, &L.bias_dev);
   if (st != VOC_OK) return st;
-  if (alpha) {
+  if (has_snake) {
     st = upload(ctx, allocs, a, &L.alpha_dev);
     if (st != VOC_OK) return st;
     st = upload(ctx, allocs, ib, &L.invb_dev);
@@ -475,7 +501,7 @@ voc_status upload_columns(vocoder *ctx, std::vector<void *> &allocs, Layer &L, c
 }
 
 voc_status upload_layer(vocoder *ctx, std::vector<void *> &allocs, Layer &L, int padding,
-                        const float *w, const float *bias, const float *alpha) {
+                        const float *w, const float *bias, const SnakeCoef &alpha) {
   std::vector<uint16_t> packed = pack_weights(L, padding, w);
   uint16_t *wd = nullptr;
   voc_status st = upload(ctx, allocs, packed, &wd);
@@ -487,8 +513,8 @@ voc_status upload_layer(vocoder *ctx, std::vector<void *> &allocs, Layer &L, int
 // Weights of a fused residual unit: conv1 (L.K taps) and conv2 (1x1) packed with the same
 // k-block and column tile; epilogue 1 columns from (b1, alpha2), epilogue 2 from (b2, next).
 voc_status upload_ru(vocoder *ctx, std::vector<void *> &allocs, Layer &L, int padding,
-                     const float *w1, const float *b1, const float *a2, const float *w2,
-                     const float *b2, const float *next_alpha) {
+                     const float *w1, const float *b1, const SnakeCoef &a2, const float *w2,
+                     const float *b2, const SnakeCoef &next_alpha) {
   voc_status st = upload_layer(ctx, allocs, L, padding, w1, b2, next_alpha);
   if (st != VOC_OK) return st;
   Layer L2 = L;
@@ -522,6 +548,7 @@ bool check_desc(const voc_desc *d, std::string &why) {
   if (d->padding != VOC_PAD_SYMMETRIC && d->padding != VOC_PAD_CAUSAL) return why = "padding", false;
   if (d->precision != VOC_PREC_BF16X3) return why = "precision", false;
   if (d->cta_pair < -1 || d->cta_pair > 1) return why = "cta_pair must be -1, 0 or 1", false;
+  if (d->snake != VOC_SNAKE && d->snake != VOC_SNAKE_BETA) return why = "snake", false;
   for (int i = 0; i < d->n_stages; ++i) {
     if (d->strides[i] < 1 || d->strides[i] > 16) return why = "stride out of [1, 16]", false;
     if (d->padding == VOC_PAD_SYMMETRIC && d->strides[i] % 2)
@@ -777,21 +804,23 @@ VOC_API voc_status vocoder_param_shape(const voc_desc *d, int index, int dims[3]
   int i = index - 2;
   int C = d->channels0;
   const int per_stage = 3 + 6 * d->n_dilations;
+  auto snake = [&](int c) { return d->snake == VOC_SNAKE_BETA ? set(2, 2, c) : set(1, c); };
   for (int s = 0; s < d->n_stages; ++s) {
     const int Co = d->widths[s];
     if (i < per_stage) {
-      if (i == 0) return set(1, C);
+      if (i == 0) return snake(C);
       if (i == 1) return set(3, C, Co, 2 * d->strides[s]);
       if (i == 2) return set(1, Co);
       const int j = (i - 3) % 6;
       if (j == 1) return set(3, Co, Co, d->res_kernel);
       if (j == 4) return set(3, Co, Co, 1);
+      if (j == 0 || j == 3) return snake(Co);
       return set(1, Co);
     }
     i -= per_stage;
     C = Co;
   }
-  if (i == 0) return set(1, C);
+  if (i == 0) return snake(C);
   if (i == 1) return set(3, 1, C, d->out_kernel);
   return set(1, 1);
 }
@@ -849,8 +878,10 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       const float x = params[i][k];
       if (!std::isfinite(x))
         return fail(nullptr, VOC_INVALID_ARG, "params[" + std::to_string(i) + "] not finite");
-      if (kinds[i] == 'a' && !(x > 0.f))
+      if (kinds[i] == 'a' && desc->snake == VOC_SNAKE && !(x > 0.f))
         return fail(nullptr, VOC_INVALID_ARG, "Snake alpha must be positive");
+      if (kinds[i] == 'a' && desc->snake == VOC_SNAKE_BETA && !(std::fabs(x) <= 80.f))
+        return fail(nullptr, VOC_INVALID_ARG, "SnakeBeta log alpha / log beta must be in [-80, 80]");
     }
   }
   if (!set_kernel_attrs(why)) return fail(nullptr, VOC_CUDA_ERROR, why);
@@ -902,7 +933,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     if (!plan_layer(ctx->use_pair, L, pad, false, why))
       return bail(fail(ctx, VOC_UNSUPPORTED, "in_proj: " + why));
     L.in_buf = BUF_H0, L.hl_buf = BUF_HB;
-    st = upload_layer(ctx, ctx->allocs, L, pad, params[0], params[1], nullptr);
+    st = upload_layer(ctx, ctx->allocs, L, pad, params[0], params[1], SnakeCoef{});
     if (st != VOC_OK) return bail(st);
     ctx->layers.push_back(L);
     conv_in_src = BUF_HB;
@@ -918,7 +949,8 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     if (!plan_layer(ctx->use_pair, L, pad, false, why))
       return bail(fail(ctx, VOC_UNSUPPORTED, "conv_in: " + why));
     L.in_buf = conv_in_src, L.hl_buf = BUF_H1;
-    st = upload_layer(ctx, ctx->allocs, L, pad, params[p], params[p + 1], params[p + 2]);
+    st = upload_layer(ctx, ctx->allocs, L, pad, params[p], params[p + 1],
+                      snake_coef(params[p + 2], L.Cout, desc->snake));
     if (st != VOC_OK) return bail(st);
     ctx->layers.push_back(L);
     p += 2;
@@ -946,17 +978,20 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       if (!plan_layer(ctx->use_pair, L, pad, false, why))
         return bail(fail(ctx, VOC_UNSUPPORTED, L.name + ": " + why));
       L.in_buf = x_buf, L.f32_buf = BUF_FY, L.hl_buf = cur;
-      st = upload_layer(ctx, ctx->allocs, L, pad, params[p + 1], params[p + 2], params[p + 3]);
+      st = upload_layer(ctx, ctx->allocs, L, pad, params[p + 1], params[p + 2],
+                        snake_coef(params[p + 3], L.Cout, desc->snake));
       if (st != VOC_OK) return bail(st);
       ctx->layers.push_back(L);
       p += 3;
     }
     C = Co;
     for (int j = 0; j < nd; ++j) {
-      const float *w1 = params[p + 1], *b1 = params[p + 2], *a2 = params[p + 3];
+      const float *w1 = params[p + 1], *b1 = params[p + 2];
+      const SnakeCoef a2 = snake_coef(params[p + 3], C, desc->snake);
       const float *w2 = params[p + 4], *b2 = params[p + 5];
       p += 6;
-      const float *next_alpha = params[p];  // next snake1 / next stage's snake / snake_out
+      // next snake1 / next stage's snake / snake_out, all over this stage's C channels
+      const SnakeCoef next_alpha = snake_coef(params[p], C, desc->snake);
       const bool last_stage = (i == desc->n_stages - 1);
       Layer R;  // the whole unit in one kernel when it fits and is enabled
       R.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".ru";
@@ -1323,7 +1358,7 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
     for (void *p : tmp.allocs) cudaFree(p);
     return st;
   };
-  voc_status st = upload_layer(&tmp, tmp.allocs, L, padding, w_host, b_host, nullptr);
+  voc_status st = upload_layer(&tmp, tmp.allocs, L, padding, w_host, b_host, SnakeCoef{});
   if (st != VOC_OK) return done(st);
   cudaError_t e;
   float *alpha_d = nullptr, *invb_d = nullptr;
@@ -1463,8 +1498,8 @@ VOC_API voc_status vocoder_op_residual_unit(const float *x_dev, int B, int C, in
   R.Cin = C, R.Cout = C, R.K = K, R.dil = dil;
   if (plan_ru(R, padding, why)) {
     R.in_buf = BUF_H0, R.skip_buf = BUF_FY, R.f32_buf = BUF_FY;
-    if ((st = upload_ru(&tmp, tmp.allocs, R, padding, w1_host, b1_host, alpha2_host, w2_host,
-                        b2_host, nullptr)) != VOC_OK)
+    if ((st = upload_ru(&tmp, tmp.allocs, R, padding, w1_host, b1_host,
+                        snake_coef(alpha2_host, C, VOC_SNAKE), w2_host, b2_host, SnakeCoef{})) != VOC_OK)
       return done(st);
     layers.push_back(R);
   } else {
@@ -1476,8 +1511,9 @@ VOC_API voc_status vocoder_op_residual_unit(const float *x_dev, int B, int C, in
       return done(fail(&tmp, VOC_UNSUPPORTED, why));
     L1.in_buf = BUF_H0, L1.hl_buf = BUF_HB;
     L2.in_buf = BUF_HB, L2.skip_buf = BUF_FY, L2.f32_buf = BUF_FY;
-    if ((st = upload_layer(&tmp, tmp.allocs, L1, padding, w1_host, b1_host, alpha2_host)) != VOC_OK ||
-        (st = upload_layer(&tmp, tmp.allocs, L2, padding, w2_host, b2_host, nullptr)) != VOC_OK)
+    if ((st = upload_layer(&tmp, tmp.allocs, L1, padding, w1_host, b1_host,
+                           snake_coef(alpha2_host, C, VOC_SNAKE))) != VOC_OK ||
+        (st = upload_layer(&tmp, tmp.allocs, L2, padding, w2_host, b2_host, SnakeCoef{})) != VOC_OK)
       return done(st);
     layers.push_back(L1);
     layers.push_back(L2);

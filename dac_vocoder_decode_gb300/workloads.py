@@ -145,6 +145,8 @@ SPEECH = Arch(latent_channels=1024, channels0=1536, strides=(8, 5, 4, 4, 3),
 TINY = Arch(latent_channels=16, channels0=64, strides=(8, 8, 4, 2), widths=(32, 16, 8, 4))
 # the published music model's front end: dec_in_proj 64 -> 1024, conv_in 1024 -> 1536
 MUSIC_FULL = dataclasses.replace(MUSIC, in_proj_channels=1024)
+# the speech codec's own activation (qwentts.cpp Architecture, "Audio tokenizer decoder")
+SPEECH_BETA = dataclasses.replace(SPEECH, snake_beta=True)
 
 # name -> (index used for seeds, arch, latent shape, weight recipe, description)
 WORKLOADS = {
@@ -160,6 +162,9 @@ WORKLOADS = {
                    "music vocoder, 180 s single pass [2,64,15504] -> [2,1,7938048]"),
     "speech": (5, SPEECH, (8, 1024, 250), "calibrated",
                "speech codec DAC decoder, causal, hop 1920, [8,1024,250] -> [8,1,480000]"),
+    "speech_snakebeta": (6, SPEECH_BETA, (8, 1024, 250), "calibrated",
+                         "speech codec DAC decoder with SnakeBeta activations, causal, hop 1920, "
+                         "[8,1024,250] -> [8,1,480000]"),
 }
 
 # overlap-crop stitch of the windowed music workload (minimaxmusic.cpp

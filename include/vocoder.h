@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define VOC_ABI_VERSION 4
+#define VOC_ABI_VERSION 5
 
 typedef struct vocoder vocoder_t;             /* opaque context */
 typedef struct CUstream_st *voc_stream_t;     /* a cudaStream_t */
@@ -65,6 +65,10 @@ typedef enum {
 
 enum { VOC_PAD_SYMMETRIC = 0, VOC_PAD_CAUSAL = 1 };
 enum { VOC_PREC_BF16X3 = 0 };
+/* activation: Snake with alpha as stored, or SnakeBeta with log-scale alpha and beta,
+ * x + sin^2(e^alpha x) / (e^beta + 1e-9) (qwentts.cpp Architecture, "Audio tokenizer
+ * decoder": exp applied to both stored parameters) */
+enum { VOC_SNAKE = 0, VOC_SNAKE_BETA = 1 };
 
 /* flags of vocoder_decode / vocoder_decode_host */
 enum {
@@ -102,6 +106,7 @@ typedef struct {
                            weight norm runs before conv_in, which then maps P -> C0
                            (the published music model's dec_in_proj 64 -> 1024,
                            minimaxmusic.cpp Architecture, "Flow VAE")          */
+  int snake;            /* VOC_SNAKE | VOC_SNAKE_BETA (ABI 5)                    */
 } voc_desc;
 
 /* ABI version of the library (VOC_ABI_VERSION of the build). */
@@ -116,7 +121,9 @@ int vocoder_abi_version(void);
  *     per dilation: snake1.alpha [C_out], conv1.w [C_out][C_out][res_kernel],
  *                   conv1.b [C_out], snake2.alpha [C_out], conv2.w [C_out][C_out][1],
  *                   conv2.b [C_out],
- *   snake_out.alpha [C_last], conv_out.w [1][C_last][out_kernel], conv_out.b [1]. */
+ *   snake_out.alpha [C_last], conv_out.w [1][C_last][out_kernel], conv_out.b [1].
+ * With VOC_SNAKE_BETA every snake*.alpha entry is [2][C] instead: log alpha, then log
+ * beta, each in [-80, 80] (plain Snake alphas must be > 0). */
 int vocoder_param_count(const voc_desc *desc);
 
 /* Shape of parameter `index`: writes up to 3 dims and their count. */

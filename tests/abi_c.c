@@ -43,6 +43,12 @@ int main(void) {
   CHECK(vocoder_abi_version() == VOC_ABI_VERSION);
   CHECK(vocoder_param_count(&d) == 2 + 4 * (3 + 6 * 3) + 3);
   CHECK(vocoder_param_count((const voc_desc *)0) == -1);
+  d.snake = VOC_SNAKE_BETA; /* SnakeBeta: every Snake parameter is [2][C] */
+  CHECK(vocoder_param_shape(&d, 2, dims, &nd) == VOC_OK && nd == 2 && dims[0] == 2 && dims[1] == 1536);
+  d.snake = 2;
+  CHECK(vocoder_param_count(&d) == -1);
+  d.snake = VOC_SNAKE;
+  CHECK(vocoder_param_shape(&d, 2, dims, &nd) == VOC_OK && nd == 1 && dims[0] == 1536);
   CHECK(vocoder_param_shape(&d, 3, dims, &nd) == VOC_OK && nd == 3 && dims[0] == 1536 &&
         dims[1] == 768 && dims[2] == 16);
   CHECK(vocoder_param_shape(&d, 1000, dims, &nd) == VOC_INVALID_ARG);

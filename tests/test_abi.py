@@ -5,6 +5,7 @@ and with the oracle's weight-norm fold."""
 from __future__ import annotations
 
 import ctypes
+import dataclasses
 import os
 import re
 import subprocess
@@ -61,8 +62,9 @@ def test_c99_consumer(lib, tmp_path):
     assert "abi_c ok" in res.stdout
 
 
-@pytest.mark.parametrize("arch", [W.TINY, W.MUSIC, W.SPEECH, W.MUSIC_FULL],
-                         ids=["tiny", "music", "speech", "music_full"])
+@pytest.mark.parametrize("arch", [W.TINY, W.MUSIC, W.SPEECH, W.MUSIC_FULL,
+                                  dataclasses.replace(W.SPEECH, snake_beta=True)],
+                         ids=["tiny", "music", "speech", "music_full", "speech_snake_beta"])
 def test_param_shapes_match_layer_list(lib, arch):
     shapes = arch.param_shapes()
     assert V.vocoder_param_count(arch) == len(shapes)

@@ -14,6 +14,8 @@ lo*lo term and the two splits), so |err| <= 2^-14 * sum |w x| leaves a 4x margin
 over the fp32-accumulated worst case of these sizes."""
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -315,6 +317,23 @@ def test_decode_music_window_sampled_cta_pair():
 
 def test_decode_speech_sampled():
     _sampled_full_size("speech", n_items=3)
+
+
+def test_decode_speech_snakebeta_sampled():
+    """The speech codec with SnakeBeta activations (log-scale alpha and beta, exponentiated
+    on the host), at the full workload size, on sampled windows."""
+    _sampled_full_size("speech_snakebeta", n_items=2)
+
+
+@pytest.mark.parametrize("arch", [MID_MUSIC, MID_SPEECH], ids=["music", "speech_causal"])
+def test_decode_snake_beta(arch):
+    """Every Snake as SnakeBeta, whole outputs against the oracle (fused and unfused
+    residual units both run: the mid-size stages span both sides of the fusion limit)."""
+    beta_arch = dataclasses.replace(arch, snake_beta=True)
+    wl = W.make_custom(beta_arch, B=2, T=21, seed=303)
+    voc = V.Vocoder(beta_arch, V.fold_params(wl.params))
+    got = G.gpu_decode(voc, wl.latent)
+    G.compare_audio(O.decode(beta_arch, wl.params, wl.latent), got, "snake_beta")
 
 
 @pytest.mark.slow
