@@ -32,8 +32,8 @@
 // TMEM lane quadrant, group g taking column chunks g, g+3, ... (TMEM -> registers ->
 // bias, residual, Snake of the next layer, hi/lo split -> global; with the chunk-major
 // layout the 32 lanes of a warp store 32 consecutive rows of one chunk: 512 contiguous
-// bytes), warps 14..16 prefetch the residual input of the three groups by TMA, warp 17
-// issues the weight copies.
+// bytes), warp 14 prefetches the residual input of the three groups by TMA, warp 15
+// issues the weight copies (16 warps: up to 128 registers per thread).
 // The grid is persistent; 2 to 4 TMEM accumulators let the epilogue of one tile
 // overlap the mainloop of the next.
 #pragma once
@@ -49,10 +49,11 @@ constexpr int kTileM = 128;
 constexpr int kEpiGroups = 3;                           // epilogue groups of 4 warps (one per
                                                         // TMEM lane quadrant)
 constexpr int kEpiWarps = 4 * kEpiGroups;               // warps 2..13
-constexpr int kSkipWarp = 2 + kEpiWarps;                // residual prefetch, one warp per group
-constexpr int kBWarp = kSkipWarp + kEpiGroups;          // weight copies
+constexpr int kSkipWarp = 2 + kEpiWarps;                // residual prefetch for every group
+constexpr int kBWarp = kSkipWarp + 1;                   // weight copies
 constexpr int kBWarps = 1;
-constexpr int kGemmThreads = 32 * (kBWarp + kBWarps);   // 576
+// 16 warps: four per SM sub-partition, so each thread may hold up to 128 registers
+constexpr int kGemmThreads = 32 * (kBWarp + kBWarps);   // 512
 // the fused residual-unit kernel: 8 epilogue warps (two per quadrant), one residual warp
 constexpr int kRuEpiWarps = 8;
 constexpr int kRuSkipWarp = 2 + kRuEpiWarps;
@@ -156,23 +157,57 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
   VOC_CHECK((taddr & 0xFFFFu) + CW <= (uint32_t)(p.n_acc * p.acc_cols), 11, taddr & 0xFFFF, CW, 0);
   VOC_CHECK(n0 + CW <= p.N_total, 12, n0, p.N_total, 0);
   float v[CW];
-  tmem_ld(taddr, v);
-  {
+  if constexpr (CW <= 16) {
+    // Issue the independent loads first: the bias (L1-resident), the TMEM read and, once
+    // its slot has landed, the residual tile; then wait for the TMEM data.
     float bb[CW];
     ldg_vec(p.bias + n0, bb);
+    uint32_t r[CW];
+    tmem_ld_issue<CW>(taddr, r);
+    if (p.skip) {
+      VOC_CHECK(sslot >= smem_lo && sslot + skip_slot_bytes(CW) <= smem_hi, 13, sslot, smem_lo, smem_hi);
+      const bool landed = mbar_wait(sfull, sparity, p.timeout, abort_flag);
+      uint4 sk[CW / 4];
+      if (landed) {
 #pragma unroll
-    for (int i = 0; i < CW; ++i) v[i] += bb[i];
-  }
-  if (p.skip) {
-    VOC_CHECK(sslot >= smem_lo && sslot + skip_slot_bytes(CW) <= smem_hi, 13, sslot, smem_lo, smem_hi);
-    if (!mbar_wait(sfull, sparity, p.timeout, abort_flag)) return false;
+        for (int j = 0; j < CW / 4; ++j)
+          sk[j] = lds128(sslot + static_cast<uint32_t>((j * kTileM + row_in_tile) * 16));
+        mbar_arrive(sempty);
+      }
+      tmem_ld_wait<CW>(r);  // the TMEM read completes before any return
+      if (!landed) return false;
 #pragma unroll
-    for (int j = 0; j < CW / 4; ++j) {
-      const uint4 x = lds128(sslot + static_cast<uint32_t>((j * kTileM + row_in_tile) * 16));
-      v[4 * j] += __uint_as_float(x.x), v[4 * j + 1] += __uint_as_float(x.y);
-      v[4 * j + 2] += __uint_as_float(x.z), v[4 * j + 3] += __uint_as_float(x.w);
+      for (int j = 0; j < CW / 4; ++j) {  // (acc + bias) + skip
+        v[4 * j] = (__uint_as_float(r[4 * j]) + bb[4 * j]) + __uint_as_float(sk[j].x);
+        v[4 * j + 1] = (__uint_as_float(r[4 * j + 1]) + bb[4 * j + 1]) + __uint_as_float(sk[j].y);
+        v[4 * j + 2] = (__uint_as_float(r[4 * j + 2]) + bb[4 * j + 2]) + __uint_as_float(sk[j].z);
+        v[4 * j + 3] = (__uint_as_float(r[4 * j + 3]) + bb[4 * j + 3]) + __uint_as_float(sk[j].w);
+      }
+    } else {
+      tmem_ld_wait<CW>(r);
+#pragma unroll
+      for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]) + bb[i];
     }
-    mbar_arrive(sempty);
+  } else {
+    // wider chunks (the fused unit's 32 columns): in order, within the register budget
+    tmem_ld(taddr, v);
+    {
+      float bb[CW];
+      ldg_vec(p.bias + n0, bb);
+#pragma unroll
+      for (int i = 0; i < CW; ++i) v[i] += bb[i];
+    }
+    if (p.skip) {
+      VOC_CHECK(sslot >= smem_lo && sslot + skip_slot_bytes(CW) <= smem_hi, 13, sslot, smem_lo, smem_hi);
+      if (!mbar_wait(sfull, sparity, p.timeout, abort_flag)) return false;
+#pragma unroll
+      for (int j = 0; j < CW / 4; ++j) {
+        const uint4 x = lds128(sslot + static_cast<uint32_t>((j * kTileM + row_in_tile) * 16));
+        v[4 * j] += __uint_as_float(x.x), v[4 * j + 1] += __uint_as_float(x.y);
+        v[4 * j + 2] += __uint_as_float(x.z), v[4 * j + 3] += __uint_as_float(x.w);
+      }
+      mbar_arrive(sempty);
+    }
   }
   float sn[CW];
   if (p.alpha) {
@@ -587,50 +622,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         drain_ring_strided(fullB + j, p.nb / kBWarps, kBWarps, mine, p.timeout);
       }
     }
-  } else if (warp >= kSkipWarp && warp < kBWarp) {
+  } else if (warp == kSkipWarp) {
     if (lane == 0 && p.skip) {
       // ------------------------------------------------------------ residual prefetch
       prefetch_tmap(&tmapS);
       // Chunk c of a tile is consumed by epilogue group c % kEpiGroups; each group has its
-      // own ring of ns / kEpiGroups slots, filled by its own warp in that group's
-      // consumption order, so a slot is only ever waited on by one sequence of consumers,
-      // at most one fill ahead.
+      // own ring of ns / kEpiGroups slots, filled in that group's consumption order, so a
+      // slot is only ever waited on by one sequence of consumers, at most one fill ahead.
+      // One thread fills the three rings, chunk by chunk in column order.
       const uint32_t bytes = static_cast<uint32_t>(skip_slot_bytes(CW));
       const int nsh = p.ns / kEpiGroups;
-      const int h = warp - kSkipWarp;
-      int cnt = 0;
+      int cnt[kEpiGroups] = {};  // fills issued into each group's ring
+      int pos[kEpiGroups] = {};  // their ring positions and phases, advanced incrementally
+      uint32_t ph[kEpiGroups] = {};
       bool ok = true;
       for (int job = job0; job < total_jobs && ok; job += job_step) {
         const int nt = job % p.n_tiles;
         const int rest = job / p.n_tiles;
         const int mt = rest % p.m_tiles;
         const int b = rest / p.m_tiles;
-        for (int c = h; c < n_chunks; c += kEpiGroups) {
-          const int k = cnt++;
-          const int slot = h * nsh + k % nsh;
-          const uint32_t ph = static_cast<uint32_t>(k / nsh) & 1u;
-          if (!mbar_wait(smem_u32(skipEmpty + slot), ph ^ 1u, p.timeout, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fs = smem_u32(skipFull + slot);
+        for (int c0 = 0; c0 < n_chunks && ok; c0 += kEpiGroups) {
+#pragma unroll
+          for (int h = 0; h < kEpiGroups; ++h) {
+            const int c = c0 + h;
+            if (c >= n_chunks || !ok) continue;
+            const int slot = h * nsh + pos[h];
+            if (!mbar_wait(smem_u32(skipEmpty + slot), ph[h] ^ 1u, p.timeout, abort_flag)) {
+              ok = false;
+              continue;
+            }
+            const uint32_t fs = smem_u32(skipFull + slot);
 #ifdef VOC_CHECKS
-          if (!(smem_u32(smS + (size_t)(slot + 1) * bytes) <= smem_u32(bars) &&
-                (nt * p.N_tile + c * CW) / 4 + CW / 4 <= p.chunks_s)) {
-            check_fail(p, abort_flag, 41, slot, nt * p.N_tile + c * CW, p.chunks_s);
-            ok = false;
-            break;
-          }
+            if (!(smem_u32(smS + (size_t)(slot + 1) * bytes) <= smem_u32(bars) &&
+                  (nt * p.N_tile + c * CW) / 4 + CW / 4 <= p.chunks_s)) {
+              check_fail(p, abort_flag, 41, slot, nt * p.N_tile + c * CW, p.chunks_s);
+              ok = false;
+              continue;
+            }
 #endif
-          mbar_arrive_expect_tx(fs, bytes);
-          tma_load_4d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, 0, mt * kM + row0,
-                      (nt * p.N_tile + c * CW) / 4, b);
+            mbar_arrive_expect_tx(fs, bytes);
+            tma_load_4d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, 0, mt * kM + row0,
+                        (nt * p.N_tile + c * CW) / 4, b);
+            ++cnt[h];
+            if (++pos[h] == nsh) pos[h] = 0, ph[h] ^= 1u;
+          }
         }
       }
       if (!ok) {
         atomicOr(p.err, ERR_TIMEOUT_SKIP);
         raise_abort();
-        drain_ring(skipFull + h * nsh, nsh, cnt, p.timeout);
+#pragma unroll
+        for (int h = 0; h < kEpiGroups; ++h) drain_ring(skipFull + h * nsh, nsh, cnt[h], p.timeout);
       }
     }
   } else {

@@ -68,7 +68,7 @@ struct Layer {
   float *bias_dev = nullptr, *alpha_dev = nullptr, *invb_dev = nullptr;
   int in_buf = -1, f32_buf = -1, hl_buf = -1, skip_buf = -1;
   int epi_flags = 0;
-  int cw = 32;              // epilogue column chunk (32, or 16 when 32 does not divide the tile)
+  int cw = 16;              // epilogue column chunk (conv kernel: 16; fused unit: 16 or 32)
   bool pair = false;        // CTA-pair kernel: 256-row tiles, half of each weight tile per CTA
   int max_clusters = 0;     // pair: co-resident 2-CTA clusters of this launch shape
   // fused residual unit (conv1 k-tap + conv2 1x1 in one kernel)
@@ -101,14 +101,8 @@ bool set_kernel_attrs(std::string &why) {
   static cudaError_t st = cudaErrorUnknown;
   static std::once_flag once;
   std::call_once(once, [] {
-    st = cudaFuncSetAttribute(voc::conv_gemm_kernel<32, false>,
+    st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (st == cudaSuccess)
-      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (st == cudaSuccess)
-      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<32, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
@@ -226,7 +220,7 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     return false;
   }
   // epilogue column chunk: 16 columns (three groups of epilogue warps take every third
-  // chunk; 16-column chunks keep the register footprint within the 576-thread block)
+  // chunk; 16-column chunks keep the register footprint within the 512-thread block)
   L.cw = 16;
   // weight columns staged per CTA: the whole tile, or (CTA pair) one half of it
   const int n_stage = L.pair ? g.N_tile / 2 : g.N_tile;
@@ -310,9 +304,7 @@ int pair_clusters(const Layer &L) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  const cudaError_t e =
-      (L.cw == 32) ? cudaOccupancyMaxActiveClusters(&n, voc::conv_gemm_kernel<32, true>, &cfg)
-                   : cudaOccupancyMaxActiveClusters(&n, voc::conv_gemm_kernel<16, true>, &cfg);
+  const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, voc::conv_gemm_kernel<16, true>, &cfg);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
@@ -712,9 +704,7 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = (L.cw == 32)
-                        ? cudaLaunchKernelEx(&cfg, voc::conv_gemm_kernel<32, true>, map, smap, a)
-                        : cudaLaunchKernelEx(&cfg, voc::conv_gemm_kernel<16, true>, map, smap, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, voc::conv_gemm_kernel<16, true>, map, smap, a);
     if (e != cudaSuccess) return cuda_fail(ctx, e, ("launch " + L.name).c_str());
     return VOC_OK;
   }
@@ -725,8 +715,6 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
       voc::ru_gemm_kernel<32><<<grid, voc::kRuThreads, L.smem, stream>>>(map, smap, a, L.rx);
     else
       voc::ru_gemm_kernel<16><<<grid, voc::kRuThreads, L.smem, stream>>>(map, smap, a, L.rx);
-  } else if (L.cw == 32) {
-    voc::conv_gemm_kernel<32, false><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
   } else {
     voc::conv_gemm_kernel<16, false><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
   }
