@@ -96,8 +96,13 @@ struct ConvGemmArgs {
   // Row placement (stateful streaming keeps each layer's left context in front of its new
   // rows): A row r of D row t is input row in_row0 + t + offset; output row t*s_rows + ph
   // goes to row f32_row0 + ... of planes of f32_L rows (hl_row0 / hl_L for the hi/lo
-  // output).  A plain decode has 0 offsets and planes of L_in * s_rows rows.
+  // output).  A plain decode has 0 offsets and planes of L_in * s_rows rows rounded up to a
+  // multiple of 8.
   int in_row0, f32_row0, f32_L, hl_row0, hl_L;
+  // Output rows (t * s_rows + ph) below rows_valid are results; rows in [rows_valid,
+  // rows_pad) are written as zeros (the padding rows up to the next multiple of 8 that
+  // the next layer's 8-row TMA groups read); rows from rows_pad on are not written.
+  int rows_valid, rows_pad;
   int flags;
   int b_resident;          // 1: the nb = taps * nkb weight slots hold this CTA's whole column
                            // tile, loaded once (every CTA keeps one column tile)
@@ -135,6 +140,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b
   return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
          (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
+
+// floor(x / 8) for any sign (the row groups of the tensor maps; a negative group is
+// out of range and reads as zeros)
+__device__ __forceinline__ int floor_div8(int x) { return x >= 0 ? x / 8 : -((7 - x) / 8); }
 
 template <int N>
 __device__ __forceinline__ void ldg_vec(const float *src, float (&v)[N]) {
@@ -227,10 +236,15 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
 #pragma unroll
     for (int i = 0; i < CW; ++i) sn[i] = v[i];
   }
-  if (t >= p.L_in) return true;
   const int ph = n0 / p.Cp_out;  // ConvT phase of these columns (0 for a conv)
   const int co0 = n0 - ph * p.Cp_out;
-  const size_t row_t = (size_t)t * p.s_rows + ph;
+  const long long out_row = (long long)t * p.s_rows + ph;
+  if (out_row >= p.rows_pad) return true;
+  if (out_row >= p.rows_valid) {  // padding rows: zeros
+#pragma unroll
+    for (int i = 0; i < CW; ++i) v[i] = 0.f, sn[i] = 0.f;
+  }
+  const size_t row_t = static_cast<size_t>(out_row);
   if (p.out_f32) {
     const size_t L_out = static_cast<size_t>(p.f32_L);
     const size_t row = row_t + p.f32_row0;
@@ -409,7 +423,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int rest = job / p.n_tiles;
         const int mt = rest % p.m_tiles;
         const int b = rest / p.m_tiles;
-        const int y0 = p.in_row0 + mt * kM + row0 + p.off_min;
+        // first staged row, rounded down to the 8-row group the tensor map addresses (the
+        // host adds the remainder, the same for every job, to the MMA row shift)
+        const int yg = floor_div8(p.in_row0 + mt * kM + row0 + p.off_min);
         for (int kb = 0; kb < p.nkb; ++kb) {
           const int sa = ia % p.na;
           const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;
@@ -428,7 +444,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
 #endif
           mbar_arrive_expect_tx(fa, a_tx);
-          tma_load_5d(dstA, &tmapA, fa, 0, y0, kb * kchunks, 0, b);  // hi and lo chunks
+          tma_load_5d(dstA, &tmapA, fa, 0, yg, kb * kchunks, 0, b);  // hi and lo chunks
           ++ia;
         }
       }
@@ -661,7 +677,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
 #endif
             mbar_arrive_expect_tx(fs, bytes);
-            tma_load_4d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, 0, mt * kM + row0,
+            tma_load_4d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, 0, (mt * kM + row0) / 8,
                         (nt * p.N_tile + c * CW) / 4, b);
             ++cnt[h];
             if (++pos[h] == nsh) pos[h] = 0, ph[h] ^= 1u;

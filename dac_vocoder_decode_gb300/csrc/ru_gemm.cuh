@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
         const int mt = tile % p.m_tiles;
         const int b = tile / p.m_tiles;
-        const int y0 = p.in_row0 + mt * kTileM + p.off_min;
+        const int yg = floor_div8(p.in_row0 + mt * kTileM + p.off_min);  // 8-row group
         for (int kb = 0; kb < p.nkb && ok; ++kb) {
           const int sa = ia % p.na;
           const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
           const uint32_t fa = smem_u32(fullA + sa);
           const uint32_t dstA = smem_u32(smA + (size_t)sa * p.a_bytes);
           mbar_arrive_expect_tx(fa, a_tx);
-          tma_load_5d(dstA, &tmapA, fa, 0, y0, kb * kchunks, 0, b);  // hi and lo chunks
+          tma_load_5d(dstA, &tmapA, fa, 0, yg, kb * kchunks, 0, b);  // hi and lo chunks
           ++ia;
           for (int tap = 0; tap < p.taps && ok; ++tap)
             ok = load_b(p.wB + ((size_t)tap * p.nkb + kb) * p.b_bytes);
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
           }
           const uint32_t fs = smem_u32(skipFull + slot);
           mbar_arrive_expect_tx(fs, bytes);
-          tma_load_4d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, 0, mt * kTileM,
+          tma_load_4d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, 0, mt * kTileM / 8,
                       (c * CW) / 4, b);
         }
       }

@@ -16,15 +16,16 @@ namespace voc {
 
 // x [B][C][T] fp32 -> hl chunk-major [B][2*Cp/8][Lp][8] bf16 at rows row0..row0+T-1:
 // 8-channel chunks of the hi parts, then of the lo parts (hi = bf16(v), lo = bf16(v - hi));
-// channels C..Cp-1 are zeros.  alpha == nullptr: no Snake.  One thread per (b, chunk, t):
-// block 256, grid (ceil(T/256), Cp/8, B).
-__global__ void prep_hl_kernel(const float *__restrict__ x, int C, int T, int Cp,
+// channels C..Cp-1 are zeros, and so are rows T..T_pad-1 (the padding rows read by the
+// 8-row TMA groups).  alpha == nullptr: no Snake.  One thread per (b, chunk, t):
+// block 256, grid (ceil(T_pad/256), Cp/8, B).
+__global__ void prep_hl_kernel(const float *__restrict__ x, int C, int T, int T_pad, int Cp,
                                const float *__restrict__ alpha, const float *__restrict__ invb,
                                __nv_bfloat16 *__restrict__ hl, int row0, long long Lp) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   const int c8 = blockIdx.y;
   const int b = blockIdx.z;
-  if (t >= T) return;
+  if (t >= T_pad) return;
   uint32_t hw[4], lw[4];
 #pragma unroll
   for (int e = 0; e < 8; e += 2) {
@@ -33,7 +34,7 @@ __global__ void prep_hl_kernel(const float *__restrict__ x, int C, int T, int Cp
     for (int u = 0; u < 2; ++u) {
       const int c = c8 * 8 + e + u;
       v[u] = 0.f;
-      if (c < C) {
+      if (c < C && t < T) {
         v[u] = x[((size_t)b * C + c) * T + t];
         if (alpha) v[u] = snake(v[u], alpha[c], invb[c]);
       }
@@ -208,15 +209,15 @@ __global__ void finite_check_kernel(const float *__restrict__ x, long long n, in
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(flag, 1);
 }
 
-// fp32 chunk-major [B][Cp/4][L][4] -> channels-first [B][C][L] (first C channels).
-// One thread per (b, 4-channel chunk, t): block 256, grid (ceil(L/256), Cp/4, B).
-__global__ void rows_to_cf_kernel(const float *__restrict__ src, int L, int Cp, int C,
-                                  float *__restrict__ cf) {
+// fp32 chunk-major [B][Cp/4][Lp][4] (planes of Lp rows) -> channels-first [B][C][L] (first
+// C channels).  One thread per (b, 4-channel chunk, t): block 256, grid (ceil(L/256), Cp/4, B).
+__global__ void rows_to_cf_kernel(const float *__restrict__ src, int L, long long Lp, int Cp,
+                                  int C, float *__restrict__ cf) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   const int j = blockIdx.y;
   const int b = blockIdx.z;
   if (t >= L) return;
-  const float4 v = reinterpret_cast<const float4 *>(src)[((size_t)b * (Cp / 4) + j) * L + t];
+  const float4 v = reinterpret_cast<const float4 *>(src)[((size_t)b * (Cp / 4) + j) * Lp + t];
   const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
@@ -225,21 +226,22 @@ __global__ void rows_to_cf_kernel(const float *__restrict__ src, int L, int Cp, 
   }
 }
 
-// channels-first fp32 [B][C][L] -> chunk-major fp32 [B][Cp/4][L][4] (zeros past C).
-// One thread per (b, 4-channel chunk, t): block 256, grid (ceil(L/256), Cp/4, B).
-__global__ void cf_to_rows_kernel(const float *__restrict__ cf, int L, int Cp, int C,
+// channels-first fp32 [B][C][L] -> chunk-major fp32 [B][Cp/4][Lp][4] (zeros past C and in
+// rows L..Lp-1).  One thread per (b, 4-channel chunk, row): block 256, grid (ceil(Lp/256),
+// Cp/4, B).
+__global__ void cf_to_rows_kernel(const float *__restrict__ cf, int L, int Lp, int Cp, int C,
                                   float *__restrict__ dst) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   const int j = blockIdx.y;
   const int b = blockIdx.z;
-  if (t >= L) return;
+  if (t >= Lp) return;
   float e[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const int c = 4 * j + u;
-    e[u] = (c < C) ? cf[((size_t)b * C + c) * L + t] : 0.f;
+    e[u] = (c < C && t < L) ? cf[((size_t)b * C + c) * L + t] : 0.f;
   }
-  reinterpret_cast<float4 *>(dst)[((size_t)b * (Cp / 4) + j) * L + t] =
+  reinterpret_cast<float4 *>(dst)[((size_t)b * (Cp / 4) + j) * (size_t)Lp + t] =
       make_float4(e[0], e[1], e[2], e[3]);
 }
 

@@ -40,6 +40,10 @@ constexpr int kBStageMax = 36 * 1024;  // bytes of one weight stage (per CTA)
 thread_local std::string g_err;  // last error without a context
 
 int rup(int x, int m) { return (x + m - 1) / m * m; }
+// Rows of a chunk-major plane: a multiple of 8, the row group the tensor maps address.
+long long pitch8(long long rows) { return (rows + 7) / 8 * 8; }
+// x mod 8 in [0, 8) for any sign
+int mod8(int x) { return ((x % 8) + 8) % 8; }
 size_t rupz(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
 uint16_t f2bf(float f) {  // round to nearest even (finite inputs)
@@ -214,7 +218,9 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   g.n_tiles = g.N_total / g.N_tile;
   g.q_split_tile = (L.convT && padding == VOC_PAD_SYMMETRIC) ? group / g.N_tile : g.n_tiles;
   g.off_min = off_min;
-  g.rows = rup(voc::kTileM + off_max - off_min, 8);
+  // the staged rows start at the 8-row group holding the first row (mod8(off_min) rows
+  // earlier when the input rows start at a multiple of 8)
+  g.rows = rup(voc::kTileM + off_max - off_min + mod8(off_min), 8);
   if (g.rows > 256) {
     why = "tap span too wide for one staged tile (" + std::to_string(off_max - off_min) + ")";
     return false;
@@ -350,7 +356,7 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
   g.off_min = -pad_left;
   g.shift0_q0 = g.shift0_q1 = 0;
   g.tap_step = L.dil;
-  g.rows = rup(voc::kTileM + span, 8);
+  g.rows = rup(voc::kTileM + span + mod8(-pad_left), 8);
   if (g.rows > 256) {
     why = "tap span too wide for one staged tile";
     return false;
@@ -576,24 +582,29 @@ long long level_len(const vocoder *ctx, int lv, int T) {
 }
 
 size_t buf_bytes(const vocoder *ctx, int B, int T) {
-  size_t m = (size_t)B * T *
+  size_t m = (size_t)B * (size_t)pitch8(T) *
              std::max({ctx->Cp_lat, rup(ctx->desc.channels0, 16), rup(ctx->desc.in_proj_channels, 16)});
   for (int i = 0; i < ctx->desc.n_stages; ++i)
-    m = std::max(m, (size_t)B * (size_t)level_len(ctx, i + 1, T) * (size_t)rup(ctx->widths[i], 16));
+    m = std::max(m, (size_t)B * (size_t)pitch8(level_len(ctx, i + 1, T)) *
+                        (size_t)rup(ctx->widths[i], 16));
   return rupz(m * 4, 256);
 }
 
-// A operand: bf16 hi/lo chunk-major [B][2*Cp/8][L][8], read in boxes of 8 channels x
-// `rows` time rows x `kchunks` chunks (zero fill outside [0, L)).
+// A operand: bf16 hi/lo chunk-major [B][2*Cp/8][L][8] with planes of L rows (L a multiple
+// of 8), read in boxes of `rows` time rows x `kchunks` chunks of both planes.  The rows of
+// a plane are addressed in groups of 8 (128 contiguous bytes): a box whose innermost extent
+// is a single 16-byte row caps TMA reads near 4 TB/s on GB300, 128-byte rows reach the
+// HBM rate.  Groups outside [0, L/8) read as zeros.
 voc_status encode_map(vocoder *ctx, CUtensorMap *map, const void *base, int Cp, long long L, int B,
                       int rows, int kchunks) {
   auto enc = encode_fn();
   if (!enc) return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled entry point unavailable");
-  // [B][hi|lo][Cp/8][L][8]: one box covers `kchunks` chunks of both planes
-  const cuuint64_t dims[5] = {8u, (cuuint64_t)L, (cuuint64_t)(Cp / 8), 2u, (cuuint64_t)B};
-  const cuuint64_t strides[4] = {16u, 16u * (cuuint64_t)L, 16u * (cuuint64_t)L * (Cp / 8),
+  if (L % 8 || rows % 8) return fail(ctx, VOC_CUDA_ERROR, "tensor map: rows not in groups of 8");
+  // [B][hi|lo][Cp/8][L/8][8 rows x 8 channels]: one box covers `kchunks` chunks of both planes
+  const cuuint64_t dims[5] = {64u, (cuuint64_t)(L / 8), (cuuint64_t)(Cp / 8), 2u, (cuuint64_t)B};
+  const cuuint64_t strides[4] = {128u, 16u * (cuuint64_t)L, 16u * (cuuint64_t)L * (Cp / 8),
                                  16u * (cuuint64_t)L * (2 * Cp / 8)};
-  const cuuint32_t box[5] = {8u, (cuuint32_t)rows, (cuuint32_t)kchunks, 2u, 1u};
+  const cuuint32_t box[5] = {64u, (cuuint32_t)(rows / 8), (cuuint32_t)kchunks, 2u, 1u};
   const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -603,15 +614,17 @@ voc_status encode_map(vocoder *ctx, CUtensorMap *map, const void *base, int Cp, 
   return VOC_OK;
 }
 
-// Residual (skip) input of an epilogue: fp32 chunk-major [B][Cp/4][L][4], read in boxes of
-// 4 channels x 128 rows x cw/4 chunks.
+// Residual (skip) input of an epilogue: fp32 chunk-major [B][Cp/4][L][4] (L a multiple of
+// 8), read in boxes of 128 rows x cw/4 chunks, rows addressed in groups of 8 (see
+// encode_map).
 voc_status encode_skip_map(vocoder *ctx, CUtensorMap *map, const void *base, int Cp, long long L,
                            int B, int cw) {
   auto enc = encode_fn();
   if (!enc) return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled entry point unavailable");
-  const cuuint64_t dims[4] = {4u, (cuuint64_t)L, (cuuint64_t)(Cp / 4), (cuuint64_t)B};
-  const cuuint64_t strides[3] = {16u, 16u * (cuuint64_t)L, 16u * (cuuint64_t)L * (Cp / 4)};
-  const cuuint32_t box[4] = {4u, (cuuint32_t)voc::kTileM, (cuuint32_t)(cw / 4), 1u};
+  if (L % 8) return fail(ctx, VOC_CUDA_ERROR, "residual tensor map: rows not in groups of 8");
+  const cuuint64_t dims[4] = {32u, (cuuint64_t)(L / 8), (cuuint64_t)(Cp / 4), (cuuint64_t)B};
+  const cuuint64_t strides[3] = {128u, 16u * (cuuint64_t)L, 16u * (cuuint64_t)L * (Cp / 4)};
+  const cuuint32_t box[4] = {32u, (cuuint32_t)(voc::kTileM / 8), (cuuint32_t)(cw / 4), 1u};
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -619,6 +632,15 @@ voc_status encode_skip_map(vocoder *ctx, CUtensorMap *map, const void *base, int
   if (r != CUDA_SUCCESS)
     return fail(ctx, VOC_CUDA_ERROR, "cuTensorMapEncodeTiled (residual) failed (" + std::to_string((int)r) + ")");
   return VOC_OK;
+}
+
+// Input row offset of a launch: the A tensor map addresses rows in groups of 8, so the MMA
+// row shift grows by the offset of the first staged row within its group.
+void set_in_row0(const Layer &L, ConvGemmArgs &a, int in_row0) {
+  a.in_row0 = in_row0;
+  const int extra = mod8(in_row0 + L.g.off_min);
+  a.shift0_q0 = L.g.shift0_q0 + extra;
+  a.shift0_q1 = L.g.shift0_q1 + extra;
 }
 
 void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *const *bufs,
@@ -637,16 +659,18 @@ void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *co
   a.out_f32 = L.f32_buf >= 0 ? static_cast<float *>(bufs[L.f32_buf]) : nullptr;
   a.out_hl = L.hl_buf >= 0 ? static_cast<__nv_bfloat16 *>(bufs[L.hl_buf]) : nullptr;
   a.flags = L.epi_flags;
-  a.in_row0 = 0;
+  set_in_row0(L, a, 0);
   a.f32_row0 = a.hl_row0 = 0;
-  a.f32_L = a.hl_L = static_cast<int>(L_in * L.g.s_rows);
+  a.f32_L = a.hl_L = static_cast<int>(pitch8(L_in * L.g.s_rows));
+  a.rows_valid = static_cast<int>(L_in * L.g.s_rows);
+  a.rows_pad = a.f32_L;  // zero rows up to the plane's 8-row boundary
   a.timeout = ctx->wait_budget;
   a.err = ctx->err_dev;
   a.f32_elems = L.f32_buf >= 0 ? (long long)(bbytes / 4) : 0;
   a.hl_elems = L.hl_buf >= 0 ? (long long)(bbytes / 2) : 0;
   a.w_bytes = (long long)L.g.n_tiles * (L.pair ? 2 : 1) * L.g.taps * L.g.nkb * L.g.b_bytes;
   a.smem_bytes = static_cast<int>(L.smem);
-  a.L_a = static_cast<int>(L_in);
+  a.L_a = static_cast<int>(pitch8(L_in));
   a.chunks_a = 2 * L.Cp_in / 8;
   a.chunks_s = L.Cp_out / 4;
   a.dbg = ctx->err_dev + 4;
@@ -747,12 +771,15 @@ voc_status launch_out_head(vocoder *ctx, const OutHead &h, const float *y, int B
   return VOC_OK;
 }
 
+// Lp < 0: planes of rup8(T) rows, rows T.. zero-filled; else planes of Lp rows from row0
+// (streaming: no padding rows are written).
 voc_status launch_prep(vocoder *ctx, const float *x, int B, int C, int T, int Cp, const float *alpha,
                        const float *invb, __nv_bfloat16 *hl, cudaStream_t stream, int row0 = 0,
                        long long Lp = -1) {
-  dim3 grid((T + 255) / 256, Cp / 8, B);
-  voc::prep_hl_kernel<<<grid, 256, 0, stream>>>(x, C, T, Cp, alpha, invb, hl, row0,
-                                                Lp < 0 ? (long long)T : Lp);
+  const int T_pad = Lp < 0 ? rup(T, 8) : T;
+  dim3 grid((T_pad + 255) / 256, Cp / 8, B);
+  voc::prep_hl_kernel<<<grid, 256, 0, stream>>>(x, C, T, T_pad, Cp, alpha, invb, hl, row0,
+                                                Lp < 0 ? (long long)T_pad : Lp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch prep");
   return VOC_OK;
@@ -1104,10 +1131,10 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
     for (size_t i = 0; i < ctx->layers.size(); ++i) {
       const Layer &L = ctx->layers[i];
       voc_status st = encode_map(ctx, &ctx->maps[i], bufs[L.in_buf], L.Cp_in,
-                                 level_len(ctx, L.level, T), B, L.g.rows, L.g.KB / 8);
+                                 pitch8(level_len(ctx, L.level, T)), B, L.g.rows, L.g.KB / 8);
       if (st == VOC_OK && L.skip_buf >= 0)
         st = encode_skip_map(ctx, &ctx->skip_maps[i], bufs[L.skip_buf], L.Cp_out,
-                             level_len(ctx, L.level, T), B, L.cw);
+                             pitch8(level_len(ctx, L.level, T)), B, L.cw);
       if (st != VOC_OK) {
         ctx->map_ws = nullptr;
         return st;
@@ -1170,7 +1197,7 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
   const long long Lf = level_len(ctx, ctx->desc.n_stages, T);
   rec(0);
   st = launch_out_head(ctx, ctx->head, static_cast<const float *>(bufs[BUF_FY]), B, Lf, audio,
-                       stream);
+                       stream, 0, pitch8(Lf));
   if (st != VOC_OK) return st;
 #ifdef VOC_CHECKS
   if ((st = check_launch(ctx, "out_head", stream)) != VOC_OK) return st;
@@ -1357,18 +1384,19 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
     if ((st = upload(&tmp, tmp.allocs, ib, &invb_d)) != VOC_OK) return done(st);
   }
   const int s = L.convT ? L.stride : 1;
+  const long long Tp = pitch8(T), Yp = pitch8((long long)T * s);  // plane rows
   void *hl = nullptr, *rows = nullptr;
-  e = cudaMalloc(&hl, (size_t)B * T * L.Cp_in * 4);
+  e = cudaMalloc(&hl, (size_t)B * Tp * L.Cp_in * 4);
   if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
   tmp.allocs.push_back(hl);
-  e = cudaMalloc(&rows, (size_t)B * T * s * L.Cp_out * 4);
+  e = cudaMalloc(&rows, (size_t)B * Yp * L.Cp_out * 4);
   if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
   tmp.allocs.push_back(rows);
   if ((st = launch_prep(&tmp, x_dev, B, L.Cin, T, L.Cp_in, alpha_d, invb_d,
                         static_cast<__nv_bfloat16 *>(hl), stream)) != VOC_OK)
     return done(st);
   CUtensorMap map;
-  if ((st = encode_map(&tmp, &map, hl, L.Cp_in, T, B, L.g.rows, L.g.KB / 8)) != VOC_OK) return done(st);
+  if ((st = encode_map(&tmp, &map, hl, L.Cp_in, Tp, B, L.g.rows, L.g.KB / 8)) != VOC_OK) return done(st);
   void *bufs[BUF_COUNT] = {hl, nullptr, nullptr, rows};
   L.level = 0;
   L.in_buf = 0, L.f32_buf = BUF_FY;
@@ -1377,11 +1405,11 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
   if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
   tmp.allocs.push_back(tmp.err_dev);
   cudaMemsetAsync(tmp.err_dev, 0, 8 * sizeof(int), stream);
-  gemm_launch_args(&tmp, L, B, T, bufs, (size_t)B * T * s * L.Cp_out * 4, a);
+  gemm_launch_args(&tmp, L, B, T, bufs, (size_t)B * Yp * L.Cp_out * 4, a);
   const CUtensorMap no_skip{};
   if ((st = launch_gemm(&tmp, L, map, no_skip, a, stream)) != VOC_OK) return done(st);
   dim3 grid((T * s + 255) / 256, L.Cp_out / 4, B);
-  voc::rows_to_cf_kernel<<<grid, 256, 0, stream>>>(static_cast<const float *>(rows), T * s,
+  voc::rows_to_cf_kernel<<<grid, 256, 0, stream>>>(static_cast<const float *>(rows), T * s, Yp,
                                                    L.Cp_out, L.Cout, y_dev);
   e = cudaGetLastError();
   if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "launch rows_to_cf"));
@@ -1455,7 +1483,8 @@ VOC_API voc_status vocoder_op_residual_unit(const float *x_dev, int B, int C, in
     return st;
   };
   const int Cp = rup(C, 16);
-  const size_t bb = (size_t)B * T * Cp * 4;
+  const long long Tp = pitch8(T);  // plane rows
+  const size_t bb = (size_t)B * Tp * Cp * 4;
   void *bufs[BUF_COUNT] = {nullptr, nullptr, nullptr, nullptr};
   for (int i : {(int)BUF_H0, (int)BUF_HB, (int)BUF_FY}) {
     cudaError_t e = cudaMalloc(&bufs[i], bb);
@@ -1478,8 +1507,8 @@ VOC_API voc_status vocoder_op_residual_unit(const float *x_dev, int B, int C, in
   if ((st = launch_prep(&tmp, x_dev, B, C, T, Cp, alpha_d, invb_d,
                         static_cast<__nv_bfloat16 *>(bufs[BUF_H0]), stream)) != VOC_OK)
     return done(st);
-  voc::cf_to_rows_kernel<<<dim3((T + 255) / 256, Cp / 4, B), 256, 0, stream>>>(
-      x_dev, T, Cp, C, static_cast<float *>(bufs[BUF_FY]));
+  voc::cf_to_rows_kernel<<<dim3(static_cast<unsigned>((Tp + 255) / 256), Cp / 4, B), 256, 0, stream>>>(
+      x_dev, T, static_cast<int>(Tp), Cp, C, static_cast<float *>(bufs[BUF_FY]));
   std::vector<Layer> layers;
   Layer R;
   R.name = "op_ru";
@@ -1508,17 +1537,17 @@ VOC_API voc_status vocoder_op_residual_unit(const float *x_dev, int B, int C, in
   }
   for (const Layer &L : layers) {
     CUtensorMap map, smap{};
-    if ((st = encode_map(&tmp, &map, bufs[L.in_buf], L.Cp_in, T, B, L.g.rows, L.g.KB / 8)) != VOC_OK)
+    if ((st = encode_map(&tmp, &map, bufs[L.in_buf], L.Cp_in, Tp, B, L.g.rows, L.g.KB / 8)) != VOC_OK)
       return done(st);
     if (L.skip_buf >= 0 &&
-        (st = encode_skip_map(&tmp, &smap, bufs[L.skip_buf], L.Cp_out, T, B, L.cw)) != VOC_OK)
+        (st = encode_skip_map(&tmp, &smap, bufs[L.skip_buf], L.Cp_out, Tp, B, L.cw)) != VOC_OK)
       return done(st);
     ConvGemmArgs a;
     gemm_launch_args(&tmp, L, B, T, bufs, bb, a);
     if ((st = launch_gemm(&tmp, L, map, smap, a, stream)) != VOC_OK) return done(st);
   }
   voc::rows_to_cf_kernel<<<dim3((T + 255) / 256, Cp / 4, B), 256, 0, stream>>>(
-      static_cast<const float *>(bufs[BUF_FY]), T, Cp, C, y_dev);
+      static_cast<const float *>(bufs[BUF_FY]), T, Tp, Cp, C, y_dev);
   e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "residual unit"));
@@ -1616,7 +1645,7 @@ VOC_API voc_status vocoder_stream_create(vocoder *ctx, int B, int max_frames,
     vocoder_stream::LayerIO &io = s->io[l];
     io.ctx_rows = -L.g.off_min;
     io.rate = static_cast<int>(level_len(ctx, L.level, 1));
-    io.plane = io.ctx_rows + (long long)max_frames * io.rate;
+    io.plane = pitch8(io.ctx_rows + (long long)max_frames * io.rate);
     if (L.hl_buf >= 0)
       for (int m = l + 1; m < nl; ++m)
         if (ctx->layers[m].in_buf == L.hl_buf) {
@@ -1635,8 +1664,8 @@ VOC_API voc_status vocoder_stream_create(vocoder *ctx, int B, int max_frames,
   for (int l = 0; l < nl; ++l) {
     const Layer &L = ctx->layers[l];
     const int lv_out = L.convT ? L.level + 1 : L.level;
-    fy_rows = std::max(fy_rows, (size_t)B * (L.Cp_out / 4) * (size_t)max_frames *
-                                    (size_t)level_len(ctx, lv_out, 1));
+    fy_rows = std::max(fy_rows, (size_t)B * (L.Cp_out / 4) *
+                                    (size_t)pitch8((long long)max_frames * level_len(ctx, lv_out, 1)));
   }
   s->fy_bytes = rupz(fy_rows * 16, 256);
   const size_t head_bytes = rupz((size_t)B * (h.Cp / 4) * s->head_plane * 16, 256);
@@ -1704,7 +1733,7 @@ VOC_API voc_status vocoder_stream_create(vocoder *ctx, int B, int max_frames,
     st = encode_map(ctx, &s->io[l].map, s->io[l].in, L.Cp_in, s->io[l].plane, B, L.g.rows, L.g.KB / 8);
     if (st == VOC_OK && L.skip_buf >= 0)
       st = encode_skip_map(ctx, &s->io[l].smap, s->fy, L.Cp_out,
-                           (long long)max_frames * level_len(ctx, L.level, 1), B, L.cw);
+                           pitch8((long long)max_frames * level_len(ctx, L.level, 1)), B, L.cw);
     if (st != VOC_OK) g_err = ctx->err;
   }
   if (st != VOC_OK) {
@@ -1758,7 +1787,8 @@ VOC_API voc_status vocoder_stream_decode(vocoder_stream *s, const float *latent_
     const vocoder_stream::LayerIO &io = s->io[l];
     ConvGemmArgs a;
     gemm_launch_args(ctx, L, B, frames, dummy, 0, a);  // rows and tiles of this chunk
-    a.in_row0 = io.ctx_rows;
+    set_in_row0(L, a, io.ctx_rows);
+    a.rows_pad = a.rows_valid;  // causal: no layer reads past its chunk's rows
     a.skip = L.skip_buf >= 0 ? reinterpret_cast<const float *>(s->fy) : nullptr;
     a.out_hl = nullptr, a.out_f32 = nullptr;
     if (L.hl_buf >= 0) {
@@ -1779,7 +1809,7 @@ VOC_API voc_status vocoder_stream_decode(vocoder_stream *s, const float *latent_
         const int lv_out = L.convT ? L.level + 1 : L.level;
         a.out_f32 = reinterpret_cast<float *>(s->fy);
         a.f32_row0 = 0;
-        a.f32_L = static_cast<int>((long long)s->max_frames * level_len(ctx, lv_out, 1));
+        a.f32_L = static_cast<int>(pitch8((long long)s->max_frames * level_len(ctx, lv_out, 1)));
         a.f32_elems = static_cast<long long>(s->fy_bytes / 4);
       }
     }
