@@ -93,6 +93,8 @@ struct ConvGemmArgs {
   float *out_f32;          // fp32 output, chunk-major [B][Cp_out/4][f32_L][4], or null
   __nv_bfloat16 *out_hl;   // hi/lo output, chunk-major [B][2*Cp_out/8][hl_L][8], or null
   int Cp_out, s_rows;      // output channels (padded), output rows per D row
+  int phase_group;         // ConvT with columns in phase pairs: phases per group G (even);
+                           // 0: phase-major columns (n = phase * Cp_out + channel)
   // Row placement (stateful streaming keeps each layer's left context in front of its new
   // rows): A row r of D row t is input row in_row0 + t + offset; output row t*s_rows + ph
   // goes to row f32_row0 + ... of planes of f32_L rows (hl_row0 / hl_L for the hi/lo
@@ -153,6 +155,65 @@ __device__ __forceinline__ void ldg_vec(const float *src, float (&v)[N]) {
     const float4 a = __ldg(s4 + j);
     v[4 * j] = a.x, v[4 * j + 1] = a.y, v[4 * j + 2] = a.z, v[4 * j + 3] = a.w;
   }
+}
+
+// ConvT outputs with phase-pair columns: the 16 columns at n0 are 8 channels at two
+// consecutive output rows (phases r, r+1 of input row t), written as 32-byte stores: fp32
+// two planes of 4 channels, hi and lo one plane of 8 channels each.  The rows start at an
+// even row (s even, r even), so every store is 32-byte aligned.
+template <int CW>
+__device__ __forceinline__ bool store_phase_pair(const ConvGemmArgs &p, volatile int *abort_flag,
+                                                 int b, int t, int n0, float (&v)[CW],
+                                                 float (&sn)[CW]) {
+  static_assert(CW == 16, "two phases of 8 channels");
+  const int G = p.phase_group;
+  const int gw = G * p.Cp_out;  // columns of one phase group
+  const int q = n0 / gw;
+  const int nn = n0 - q * gw;
+  const int cg = nn / (8 * G);            // 8-channel block
+  const int rl = (nn - cg * 8 * G) / 8;   // first phase within the group (even)
+  const long long out_row = (long long)t * p.s_rows + q * G + rl;  // rows out_row, out_row + 1
+  if (out_row >= p.rows_pad) return true;
+  if (out_row >= p.rows_valid) {  // padding rows (both: rows_pad and out_row are even)
+#pragma unroll
+    for (int i = 0; i < CW; ++i) v[i] = 0.f, sn[i] = 0.f;
+  }
+  if (p.out_f32) {
+    const size_t L_out = static_cast<size_t>(p.f32_L);
+    const size_t row = static_cast<size_t>(out_row) + p.f32_row0;
+    const float *src = (p.flags & EPI_F32_SNAKE) ? sn : v;
+    VOC_CHECK((((long long)b * (p.Cp_out / 4) + 2 * cg + 1) * (long long)L_out + row + 1) * 4 + 4 <= p.f32_elems,
+              16, b, cg, (int)row);
+    float *base = p.out_f32 + ((size_t)b * (p.Cp_out / 4) + 2 * cg) * L_out * 4 + row * 4;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t w[8] = {__float_as_uint(src[4 * j]), __float_as_uint(src[4 * j + 1]),
+                             __float_as_uint(src[4 * j + 2]), __float_as_uint(src[4 * j + 3]),
+                             __float_as_uint(src[8 + 4 * j]), __float_as_uint(src[8 + 4 * j + 1]),
+                             __float_as_uint(src[8 + 4 * j + 2]), __float_as_uint(src[8 + 4 * j + 3])};
+      st_global_v8(base + (size_t)j * L_out * 4, w);
+    }
+  }
+  if (p.out_hl) {
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(sn[2 * i]);
+      const __nv_bfloat16 h1 = __float2bfloat16_rn(sn[2 * i + 1]);
+      const __nv_bfloat16 l0 = __float2bfloat16_rn(sn[2 * i] - __bfloat162float(h0));
+      const __nv_bfloat16 l1 = __float2bfloat16_rn(sn[2 * i + 1] - __bfloat162float(h1));
+      hw[i] = pack_bf16x2(h0, h1);
+      lw[i] = pack_bf16x2(l0, l1);
+    }
+    const size_t L_out = static_cast<size_t>(p.hl_L);
+    const size_t row = static_cast<size_t>(out_row) + p.hl_row0;
+    const size_t item = (size_t)b * (2 * p.Cp_out / 8);
+    VOC_CHECK((((long long)item + p.Cp_out / 8 + cg) * (long long)L_out + row + 1) * 8 + 8 <= p.hl_elems,
+              17, b, cg, (int)row);
+    st_global_v8(p.out_hl + ((item + cg) * L_out + row) * 8, hw);
+    st_global_v8(p.out_hl + ((item + p.Cp_out / 8 + cg) * L_out + row) * 8, lw);
+  }
+  return true;
 }
 
 // Epilogue of one warp for 32 rows (its TMEM lane quadrant) x CW columns
@@ -235,6 +296,9 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
   } else {
 #pragma unroll
     for (int i = 0; i < CW; ++i) sn[i] = v[i];
+  }
+  if constexpr (CW == 16) {
+    if (p.phase_group) return store_phase_pair<CW>(p, abort_flag, b, t, n0, v, sn);
   }
   const int ph = n0 / p.Cp_out;  // ConvT phase of these columns (0 for a conv)
   const int co0 = n0 - ph * p.Cp_out;

@@ -194,6 +194,12 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
       g.shift0_q0 = 1, g.shift0_q1 = 1;
     }
     g.tap_step = -1;
+    // Output columns of a phase group of G phases: with G even, each 8-channel block holds
+    // its G phases consecutively (8 columns per phase), so a 16-column epilogue chunk holds
+    // two consecutive output rows of 8 channels and is written with 32-byte stores; with G
+    // odd, phase-major (n = r * Cp_out + co within the group).
+    const int G = (padding == VOC_PAD_SYMMETRIC) ? s / 2 : s;
+    g.phase_group = (G % 2 == 0 && L.Cp_out % 8 == 0) ? G : 0;
   } else {
     const int span = L.dil * (L.K - 1);
     const int pad_left = (padding == VOC_PAD_CAUSAL) ? span : span / 2;
@@ -395,6 +401,22 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
 }
 
 // Value of the GEMM weight for column n, input channel ci, tap `tap`.
+// ConvT column n -> (phase r, output channel co) in the column order of plan_gemm.
+void convT_column(const Layer &L, int padding, int n, int &r, int &co) {
+  const int s = L.stride;
+  const int G = (padding == VOC_PAD_SYMMETRIC) ? s / 2 : s;  // phases of one group
+  if (L.g.phase_group) {
+    const int gw = G * L.Cp_out;  // columns of one phase group
+    const int q = n / gw, nn = n % gw;
+    const int cg = nn / (8 * G), rem = nn % (8 * G);
+    r = q * G + rem / 8;
+    co = cg * 8 + rem % 8;
+  } else {
+    r = n / L.Cp_out;
+    co = n % L.Cp_out;
+  }
+}
+
 float weight_value(const Layer &L, int padding, const float *w, int n, int ci, int tap) {
   if (ci >= L.Cin) return 0.f;
   if (!L.convT) {
@@ -402,7 +424,8 @@ float weight_value(const Layer &L, int padding, const float *w, int n, int ci, i
     return w[((size_t)n * L.Cin + ci) * L.K + tap];
   }
   const int s = L.stride;
-  const int r = n / L.Cp_out, co = n % L.Cp_out;
+  int r, co;
+  convT_column(L, padding, n, r, co);
   if (co >= L.Cout) return 0.f;
   const int p = (padding == VOC_PAD_CAUSAL) ? 0 : s / 2;
   const int k = (r + p) % s + tap * s;  // tap 0: k0 at row t+q, tap 1: k0+s at row t+q-1
@@ -472,13 +495,14 @@ SnakeCoef snake_coef(const float *p, int C, int kind) {
 
 // Per-column epilogue vectors of a layer: bias, and the Snake of the layer that
 // consumes this output (empty coefficients: none).
-voc_status upload_columns(vocoder *ctx, std::vector<void *> &allocs, Layer &L, const float *bias,
-                          const SnakeCoef &sn) {
+voc_status upload_columns(vocoder *ctx, std::vector<void *> &allocs, Layer &L, int padding,
+                          const float *bias, const SnakeCoef &sn) {
   const int N = L.g.N_total;
   const bool has_snake = !sn.a.empty();
   std::vector<float> b(N, 0.f), a(N, 1.f), ib(N, 0.f);
   for (int n = 0; n < N; ++n) {
-    const int co = n % L.Cp_out;
+    int r = 0, co = n;
+    if (L.convT) convT_column(L, padding, n, r, co);
     if (co < L.Cout) {
       if (bias) b[n] = bias[co];
       if (has_snake) {
@@ -505,7 +529,7 @@ voc_status upload_layer(vocoder *ctx, std::vector<void *> &allocs, Layer &L, int
   voc_status st = upload(ctx, allocs, packed, &wd);
   if (st != VOC_OK) return st;
   L.w_dev = reinterpret_cast<uint8_t *>(wd);
-  return upload_columns(ctx, allocs, L, bias, alpha);
+  return upload_columns(ctx, allocs, L, padding, bias, alpha);
 }
 
 // Weights of a fused residual unit: conv1 (L.K taps) and conv2 (1x1) packed with the same
@@ -523,7 +547,7 @@ voc_status upload_ru(vocoder *ctx, std::vector<void *> &allocs, Layer &L, int pa
   if ((st = upload(ctx, allocs, packed, &wd)) != VOC_OK) return st;
   L.rx.wB2 = reinterpret_cast<const uint8_t *>(wd);
   Layer Lh = L;
-  if ((st = upload_columns(ctx, allocs, Lh, b1, a2)) != VOC_OK) return st;
+  if ((st = upload_columns(ctx, allocs, Lh, padding, b1, a2)) != VOC_OK) return st;
   L.rx.bias_h = Lh.bias_dev, L.rx.alpha_h = Lh.alpha_dev, L.rx.invb_h = Lh.invb_dev;
   return VOC_OK;
 }
