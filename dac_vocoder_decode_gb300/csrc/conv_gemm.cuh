@@ -95,6 +95,10 @@ struct ConvGemmArgs {
   int Cp_out, s_rows;      // output channels (padded), output rows per D row
   int phase_group;         // ConvT with columns in phase pairs: phases per group G (even);
                            // 0: phase-major columns (n = phase * Cp_out + channel)
+  int b2;                  // 1 (the kernel's B2 form): each weight chunk holds its hi rows then its lo rows, and a K
+                           // step is two MMAs: A_hi x [W_hi | W_lo] into 2 N_tile accumulator
+                           // columns, then A_lo x W_hi into the first N_tile; the epilogue adds
+                           // the two column halves.  0: three MMAs of N_tile columns.
   // Row placement (stateful streaming keeps each layer's left context in front of its new
   // rows): A row r of D row t is input row in_row0 + t + offset; output row t*s_rows + ph
   // goes to row f32_row0 + ... of planes of f32_L rows (hl_row0 / hl_L for the hi/lo
@@ -218,13 +222,14 @@ __device__ __forceinline__ bool store_phase_pair(const ConvGemmArgs &p, volatile
 
 // Epilogue of one warp for 32 rows (its TMEM lane quadrant) x CW columns
 // n0..n0+CW-1, which lie in one ConvT phase because CW divides C_out.
-template <int CW>
+template <int CW, bool B2 = false>
 __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t sslot,
                                                uint32_t sfull, uint32_t sempty, uint32_t sparity,
                                                volatile int *abort_flag, int row_in_tile,
                                                int b, int t, int n0, uint32_t taddr,
                                                uint32_t smem_lo, uint32_t smem_hi) {
-  VOC_CHECK((taddr & 0xFFFFu) + CW <= (uint32_t)(p.n_acc * p.acc_cols), 11, taddr & 0xFFFF, CW, 0);
+  VOC_CHECK((taddr & 0xFFFFu) + CW + (p.b2 ? p.N_tile : 0) <= (uint32_t)(p.n_acc * p.acc_cols), 11,
+            taddr & 0xFFFF, CW, p.b2);
   VOC_CHECK(n0 + CW <= p.N_total, 12, n0, p.N_total, 0);
   float v[CW];
   if constexpr (CW <= 16) {
@@ -232,8 +237,9 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
     // its slot has landed, the residual tile; then wait for the TMEM data.
     float bb[CW];
     ldg_vec(p.bias + n0, bb);
-    uint32_t r[CW];
+    uint32_t r[CW], r2[CW];
     tmem_ld_issue<CW>(taddr, r);
+    if constexpr (B2) tmem_ld_issue<CW>(taddr + static_cast<uint32_t>(p.N_tile), r2);
     if (p.skip) {
       VOC_CHECK(sslot >= smem_lo && sslot + skip_slot_bytes(CW) <= smem_hi, 13, sslot, smem_lo, smem_hi);
       const bool landed = mbar_wait(sfull, sparity, p.timeout, abort_flag);
@@ -244,7 +250,12 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
           sk[j] = lds128(sslot + static_cast<uint32_t>((j * kTileM + row_in_tile) * 16));
         mbar_arrive(sempty);
       }
-      tmem_ld_wait<CW>(r);  // the TMEM read completes before any return
+      tmem_ld_wait<CW>(r);  // the TMEM reads complete before any return
+      if constexpr (B2) {
+        tmem_ld16_after_wait(r2);
+#pragma unroll
+        for (int i = 0; i < CW; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+      }
       if (!landed) return false;
 #pragma unroll
       for (int j = 0; j < CW / 4; ++j) {  // (acc + bias) + skip
@@ -255,6 +266,11 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
       }
     } else {
       tmem_ld_wait<CW>(r);
+      if constexpr (B2) {
+        tmem_ld16_after_wait(r2);
+#pragma unroll
+        for (int i = 0; i < CW; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+      }
 #pragma unroll
       for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]) + bb[i];
     }
@@ -379,7 +395,7 @@ __device__ __forceinline__ void drain_ring_strided(uint64_t *full, int slots, in
   }
 }
 
-template <int CW, bool PAIR>
+template <int CW, bool PAIR, bool B2 = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap tmapA,
                      const __grid_constant__ CUtensorMap tmapS, const ConvGemmArgs p) {
@@ -571,16 +587,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mma_commit_warp(smem_u32(bar));
       };
       const uint32_t idesc = idesc_bf16_f32(kM, p.N_tile);
+      const uint32_t idesc2 = idesc_bf16_f32(kM, 2 * p.N_tile);  // b2: [W_hi | W_lo]
       // Descriptor low words step by 16-byte units: +1 is +16 bytes of start address.  The
       // ring positions (slot, phase) advance incrementally: this loop is issue-bound, so it
       // avoids divisions by run-time ring sizes.
       const uint32_t dA_lo = (kchunks * chunkA) >> 4;
       const uint32_t dA_k = (2 * chunkA) >> 4;
+      // b2: the chunks of a weight stage hold 2 * n rows (hi, then lo), so chunks lie
+      // 2 * chunkB apart
+      const uint32_t chunkB_stride = B2 ? 2 * chunkB : chunkB;
       const uint32_t dB_lo = (kchunks * chunkB) >> 4;
-      const uint32_t dB_k = (2 * chunkB) >> 4;
+      const uint32_t dB_k = (2 * chunkB_stride) >> 4;
       const uint32_t desc_hi = static_cast<uint32_t>(smem_desc(0u, 0u, 128) >> 32);
       const uint32_t a_desc0 = static_cast<uint32_t>(smem_desc(smem_u32(smA), chunkA, 128));
-      const uint32_t b_desc0 = static_cast<uint32_t>(smem_desc(smem_u32(smB), chunkB, 128));
+      const uint32_t b_desc0 = static_cast<uint32_t>(smem_desc(smem_u32(smB), chunkB_stride, 128));
       const uint32_t a_slot_step = static_cast<uint32_t>(p.a_bytes) >> 4;
       const uint32_t b_slot_step = static_cast<uint32_t>(p.b_bytes) >> 4;
       const int nks = kchunks / 2;
@@ -606,14 +626,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           uint32_t a0 = a_desc0 + sa * a_slot_step + static_cast<uint32_t>(shift0);
           for (int tap = 0; tap < p.taps; ++tap, a0 += static_cast<uint32_t>(p.tap_step)) {
-            // a resident slot completes its first phase only
-            const uint32_t wph = p.b_resident ? 0u : phb;
-            if (!wait_all(smem_u32(fullB + sb), wph, false) ||
-                (PAIR && !wait_all(smem_u32(pairB + sb), wph, true))) {
-              ok = false;
-              break;
+            // a resident slot completes its first phase only, in this CTA's first job;
+            // later jobs issue on it without a wait
+            if (!p.b_resident || job == job0) {
+              const uint32_t wph = p.b_resident ? 0u : phb;
+              if (!wait_all(smem_u32(fullB + sb), wph, false) ||
+                  (PAIR && !wait_all(smem_u32(pairB + sb), wph, true))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
             }
-            tc_fence_after();
 #ifdef VOC_CHECKS
             {
               const int sh = shift0 + tap * p.tap_step;
@@ -625,11 +648,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
 #endif
             uint32_t a_hi = a0, b_hi = b_desc0 + sb * b_slot_step;
-            for (int ks = 0; ks < nks; ++ks, a_hi += dA_k, b_hi += dB_k) {
-              mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi, desc_hi, idesc, accum);
-              mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi + dB_lo, desc_hi, idesc, 1u);
-              mma_bf16_warp_lo<PAIR>(d_tmem, a_hi + dA_lo, b_hi, desc_hi, idesc, 1u);
-              accum = 1u;
+            if constexpr (B2) {
+              for (int ks = 0; ks < nks; ++ks, a_hi += dA_k, b_hi += dB_k) {
+                mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi, desc_hi, idesc2, accum);
+                mma_bf16_warp_lo<PAIR>(d_tmem, a_hi + dA_lo, b_hi, desc_hi, idesc, 1u);
+                accum = 1u;
+              }
+            } else {
+              for (int ks = 0; ks < nks; ++ks, a_hi += dA_k, b_hi += dB_k) {
+                mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi, desc_hi, idesc, accum);
+                mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi + dB_lo, desc_hi, idesc, 1u);
+                mma_bf16_warp_lo<PAIR>(d_tmem, a_hi + dA_lo, b_hi, desc_hi, idesc, 1u);
+                accum = 1u;
+              }
             }
             if (!p.b_resident) commit(emptyB + sb);
             if (++sb == p.nb) sb = 0, phb ^= 1u;
@@ -786,7 +817,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                              (static_cast<uint32_t>(quad * 32) << 16);
       for (int c = half; c < n_chunks && ok; c += kEpiGroups) {
         const int slot = half * nsh + kslot;
-        ok = epilogue_chunk<CW>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
+        ok = epilogue_chunk<CW, B2>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
                                 smem_u32(skipFull + slot), smem_u32(skipEmpty + slot), kph,
                                 abort_flag, row_in_tile, b, t, nt * p.N_tile + c * CW,
                                 tbase + c * CW, sbase, smem_u32(bars));

@@ -108,6 +108,9 @@ bool set_kernel_attrs(std::string &why) {
     st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
@@ -295,8 +298,11 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     return false;
   }
   g.nkb = L.Cp_in / g.KB;
+  // Two MMAs per K step where the doubled column count fits one MMA (N <= 256): narrow
+  // layers issue a third fewer MMA instructions, whose rate limits them.
+  g.b2 = (!L.pair && 2 * g.N_tile <= 256) ? 1 : 0;
   int ac = 32;
-  while (ac < g.N_tile) ac *= 2;
+  while (ac < (g.b2 ? 2 * g.N_tile : g.N_tile)) ac *= 2;
   g.acc_cols = ac;
   g.n_acc = std::min(voc::kMaxAcc, 512 / ac);
   L.smem = 1024 + (size_t)g.na * g.a_bytes + (size_t)g.nb * g.b_bytes +
@@ -343,7 +349,9 @@ bool plan_layer(bool pair, Layer &L, int padding, bool has_skip, std::string &wh
 // geometry of plan_gemm, one column tile (N = Cp <= kRuMaxC), the conv1 result kept in a
 // shared H tile of 128 rows x Cp hi/lo pairs, and a k-block common to both convolutions.
 constexpr int kRuMaxC = 192;
-constexpr int kFuseDefault = 64;  // fused units win when their k-blocks need not shrink
+// Residual units run as two kernels by default: with two-MMA K steps for narrow layers the
+// pair of kernels is faster than the fused unit at every width measured (C = 48 to 192).
+constexpr int kFuseDefault = 0;
 bool plan_ru(Layer &L, int padding, std::string &why) {
   ConvGemmArgs &g = L.g;
   L.Cp_in = L.Cp_out = rup(L.Cout, 16);
@@ -432,8 +440,9 @@ float weight_value(const Layer &L, int padding, const float *w, int n, int ci, i
   return w[((size_t)ci * L.Cout + co) * (2 * s) + k];
 }
 
-// Weight tiles as the kernel stages them: [tile][tap][kb][hi|lo][chunk][n][8] with tiles of
-// `pw` columns (N_tile, or N_tile / 2 for the CTA pair: CTA r of a pair stages tile 2 nt + r).
+// Weight tiles as the kernel stages them: [tile][tap][kb][hi|lo][chunk][n][8] (b2:
+// [tile][tap][kb][chunk][hi|lo][n][8]) with tiles of `pw` columns (N_tile, or N_tile / 2 for
+// the CTA pair: CTA r of a pair stages tile 2 nt + r).
 std::vector<uint16_t> pack_weights(const Layer &L, int padding, const float *w) {
   const ConvGemmArgs &g = L.g;
   const int pw = L.pair ? g.N_tile / 2 : g.N_tile;
@@ -450,9 +459,14 @@ std::vector<uint16_t> pack_weights(const Layer &L, int padding, const float *w) 
               const float v = weight_value(L, padding, w, nt * pw + n, kb * g.KB + c * 8 + e, tap);
               const uint16_t hi = f2bf(v);
               const uint16_t lo = f2bf(v - bf2f(hi));
-              const size_t idx = ((size_t)c * pw + n) * 8 + e;
-              base[idx] = hi;
-              base[(size_t)g.KB * pw + idx] = lo;
+              if (g.b2) {
+                base[(((size_t)c * 2 + 0) * pw + n) * 8 + e] = hi;
+                base[(((size_t)c * 2 + 1) * pw + n) * 8 + e] = lo;
+              } else {
+                const size_t idx = ((size_t)c * pw + n) * 8 + e;
+                base[idx] = hi;
+                base[(size_t)g.KB * pw + idx] = lo;
+              }
             }
       }
   return out;
@@ -764,7 +778,10 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
     else
       voc::ru_gemm_kernel<16><<<grid, voc::kRuThreads, L.smem, stream>>>(map, smap, a, L.rx);
   } else {
-    voc::conv_gemm_kernel<16, false><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
+    if (L.g.b2)
+      voc::conv_gemm_kernel<16, false, true><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
+    else
+      voc::conv_gemm_kernel<16, false><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, ("launch " + L.name).c_str());

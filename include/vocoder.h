@@ -95,8 +95,8 @@ typedef struct {
   int padding;          /* VOC_PAD_SYMMETRIC | VOC_PAD_CAUSAL                */
   int precision;        /* VOC_PREC_BF16X3                                   */
   int fuse_max_channels;/* residual units of up to this many channels run as one
-                           kernel (conv1 result kept on chip); 0 = library default,
-                           -1 = never.  A performance choice only: results agree
+                           kernel (conv1 result kept on chip); 0 = library default
+                           (never), -1 = never.  A performance choice only: results agree
                            within the decode tolerance either way.              */
   int cta_pair;         /* conv layers run on CTA pairs (2-CTA clusters sharing one
                            256-row MMA, each SM staging half of the weights):
