@@ -484,6 +484,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+  pdl_launch_dependents();
 
   const int total_jobs = p.B * p.m_tiles * p.n_tiles;
   const int kchunks = p.KB / 8;
@@ -496,6 +497,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       // ------------------------------------------------------------ A producer
       prefetch_tmap(&tmapA);
+      pdl_wait();  // the previous layer's output
       const uint32_t a_tx = 2u * kchunks * chunkA;
       int ia = 0;
       bool ok = true;
@@ -737,6 +739,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0 && p.skip) {
       // ------------------------------------------------------------ residual prefetch
       prefetch_tmap(&tmapS);
+      pdl_wait();
       // Chunk c of a tile is consumed by epilogue group c % kEpiGroups; each group has its
       // own ring of ns / kEpiGroups slots, filled in that group's consumption order, so a
       // slot is only ever waited on by one sequence of consumers, at most one fill ahead.
@@ -788,6 +791,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
+    pdl_wait();  // this layer's outputs overwrite buffers earlier layers read
     const int e = warp - 2;     // epilogue warp 0..kEpiWarps-1
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int half = e / 4;     // this warp's group: column chunks half, half + kEpiGroups, ...

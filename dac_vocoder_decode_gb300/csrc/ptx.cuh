@@ -10,6 +10,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------------------------ programmatic launch
+// Kernels are launched with programmatic stream serialization: the next kernel on the stream
+// may start while this one finishes.  pdl_wait blocks the calling thread until every earlier
+// kernel of the stream has completed and its memory operations are visible: each thread calls
+// it before its first access to memory that an earlier kernel writes or reads (activations,
+// outputs); weights written at create time may be read before it.  pdl_launch_dependents
+// lets the next kernel be scheduled as soon as this one's CTAs have called it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+  pdl_launch_dependents();
 
   const int total_tiles = p.B * p.m_tiles;  // one column tile: N_tile = Cp
   const int kchunks = p.KB / 8;
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
     if (lane == 0) {
       // ------------------------------------------------------------ A / weight producer
       prefetch_tmap(&tmapA);
+      pdl_wait();  // the previous layer's output
       const uint32_t a_tx = 2u * kchunks * chunkA;
       int ia = 0, ib = 0;
       bool ok = true;
@@ -298,6 +300,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
     if (lane == 0 && p.skip) {
       // ------------------------------------------------------------ residual prefetch
       prefetch_tmap(&tmapS);
+      pdl_wait();
       const uint32_t bytes = static_cast<uint32_t>(skip_slot_bytes(CW));
       const int nsh = p.ns / 2;
       int cnt[2] = {0, 0};
@@ -329,6 +332,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
+    pdl_wait();  // this unit's outputs overwrite buffers earlier layers read
     const int e = warp - 2;
     const int quad = warp & 3;
     const int half = e / 4;

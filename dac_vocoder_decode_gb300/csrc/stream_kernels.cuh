@@ -10,6 +10,7 @@
 
 #include <cstdint>
 
+#include "ptx.cuh"
 #include "snake.cuh"
 
 namespace voc {
@@ -22,6 +23,8 @@ namespace voc {
 __global__ void prep_hl_kernel(const float *__restrict__ x, int C, int T, int T_pad, int Cp,
                                const float *__restrict__ alpha, const float *__restrict__ invb,
                                __nv_bfloat16 *__restrict__ hl, int row0, long long Lp) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   const int c8 = blockIdx.y;
   const int b = blockIdx.z;
@@ -67,6 +70,8 @@ __global__ void __launch_bounds__(TILE) out_head_kernel(const float *__restrict_
                                                         const float *__restrict__ bias,
                                                         float *__restrict__ audio, int in_row0,
                                                         long long Ly) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ float4 sm4[];
   const int b = blockIdx.y;
   const int t0 = blockIdx.x * TILE;
@@ -112,6 +117,8 @@ __global__ void __launch_bounds__(256) out_head_reg_kernel(const float *__restri
                                                             float *__restrict__ audio, int in_row0,
                                                             long long Ly) {
   constexpr int R = TPT + K - 1;  // input rows per chunk
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.y;
   const long long t0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * TPT;
   if (t0 >= L) return;
@@ -168,7 +175,9 @@ struct RowCopyJob {
   int dst_row0, rows, planes;
 };
 __global__ void row_copy_kernel(const RowCopyJob *__restrict__ jobs, int frames) {
-  const RowCopyJob j = jobs[blockIdx.y];
+  pdl_launch_dependents();
+  const RowCopyJob j = jobs[blockIdx.y];  // written at stream creation
+  pdl_wait();
   const long long n = (long long)j.planes * j.rows;
   const long long s0 = j.src_row0 + (long long)frames * j.src_rate;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -183,6 +192,8 @@ __global__ void row_copy_kernel(const RowCopyJob *__restrict__ jobs, int frames)
 // concatenated per side and clamped to [-1, 1].  grid (ceil(len/256), n_sides).
 __global__ void stitch_kernel(const float *__restrict__ dec, int n_win, int n_sides, int Wf,
                               int cl, int cr, int hop, long long len, float *__restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long j = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int side = blockIdx.y;
   if (j >= len) return;
@@ -202,6 +213,8 @@ __global__ void stitch_kernel(const float *__restrict__ dec, int n_win, int n_si
 }
 
 __global__ void finite_check_kernel(const float *__restrict__ x, long long n, int *flag) {
+  pdl_launch_dependents();
+  pdl_wait();
   int bad = 0;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)

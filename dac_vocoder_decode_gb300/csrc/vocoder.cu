@@ -12,6 +12,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "vocoder.h"
@@ -40,6 +41,25 @@ constexpr int kBStageMax = 36 * 1024;  // bytes of one weight stage (per CTA)
 thread_local std::string g_err;  // last error without a context
 
 int rup(int x, int m) { return (x + m - 1) / m * m; }
+// Launch with programmatic stream serialization: the kernel may be scheduled while the
+// previous kernel of the stream finishes; it orders its own accesses with griddepcontrol.wait
+// (pdl_wait in the kernels).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Rows of a chunk-major plane: a multiple of 8, the row group the tensor maps address.
 long long pitch8(long long rows) { return (rows + 7) / 8 * 8; }
 // x mod 8 in [0, 8) for any sign
@@ -757,33 +777,38 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
   };
   if (L.pair) {  // persistent grid of 2-CTA clusters, at most as many as can be resident
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2, attr[0].val.clusterDim.y = 1, attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * static_cast<unsigned>(persistent(L.max_clusters)));
     cfg.blockDim = dim3(voc::kGemmThreads);
     cfg.dynamicSmemBytes = L.smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, voc::conv_gemm_kernel<16, true>, map, smap, a);
     if (e != cudaSuccess) return cuda_fail(ctx, e, ("launch " + L.name).c_str());
     return VOC_OK;
   }
   const int grid = static_cast<int>(L.ru ? std::min<long long>(tiles, ctx->num_sms)
                                          : persistent(ctx->num_sms));
+  cudaError_t e;
   if (L.ru) {
     if (L.cw == 32)
-      voc::ru_gemm_kernel<32><<<grid, voc::kRuThreads, L.smem, stream>>>(map, smap, a, L.rx);
+      e = launch_pdl(voc::ru_gemm_kernel<32>, dim3(grid), dim3(voc::kRuThreads), L.smem, stream,
+                     map, smap, a, L.rx);
     else
-      voc::ru_gemm_kernel<16><<<grid, voc::kRuThreads, L.smem, stream>>>(map, smap, a, L.rx);
+      e = launch_pdl(voc::ru_gemm_kernel<16>, dim3(grid), dim3(voc::kRuThreads), L.smem, stream,
+                     map, smap, a, L.rx);
+  } else if (L.g.b2) {
+    e = launch_pdl(voc::conv_gemm_kernel<16, false, true>, dim3(grid), dim3(voc::kGemmThreads),
+                   L.smem, stream, map, smap, a);
   } else {
-    if (L.g.b2)
-      voc::conv_gemm_kernel<16, false, true><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
-    else
-      voc::conv_gemm_kernel<16, false><<<grid, voc::kGemmThreads, L.smem, stream>>>(map, smap, a);
+    e = launch_pdl(voc::conv_gemm_kernel<16, false>, dim3(grid), dim3(voc::kGemmThreads), L.smem,
+                   stream, map, smap, a);
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, ("launch " + L.name).c_str());
   return VOC_OK;
 }
@@ -796,18 +821,19 @@ voc_status launch_out_head(vocoder *ctx, const OutHead &h, const float *y, int B
   if (h.K == 7 && h.w4_dev) {
     const long long threads = (L + kHeadTpt - 1) / kHeadTpt;
     dim3 grid(static_cast<unsigned>((threads + 255) / 256), static_cast<unsigned>(B));
-    voc::out_head_reg_kernel<7, kHeadTpt><<<grid, 256, 0, stream>>>(
-        y, static_cast<int>(L), h.Cp, h.pad_left, reinterpret_cast<const float4 *>(h.w4_dev),
-        h.b_dev, audio, in_row0, Ly);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(voc::out_head_reg_kernel<7, kHeadTpt>, grid, dim3(256), 0, stream,
+                               y, static_cast<int>(L), h.Cp, h.pad_left,
+                               reinterpret_cast<const float4 *>(h.w4_dev),
+                               static_cast<const float *>(h.b_dev), audio, in_row0, Ly);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "launch out_head");
     return VOC_OK;
   }
   const size_t smem = ((size_t)(kHeadTile + h.K - 1) * h.Cp + (size_t)h.Cp * h.K) * 4;
   dim3 grid(static_cast<unsigned>((L + kHeadTile - 1) / kHeadTile), static_cast<unsigned>(B));
-  voc::out_head_kernel<kHeadTile><<<grid, kHeadTile, smem, stream>>>(
-      y, static_cast<int>(L), h.Cp, h.K, h.pad_left, h.w_dev, h.b_dev, audio, in_row0, Ly);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(voc::out_head_kernel<kHeadTile>, grid, dim3(kHeadTile), smem, stream,
+                             y, static_cast<int>(L), h.Cp, h.K, h.pad_left,
+                             static_cast<const float *>(h.w_dev), static_cast<const float *>(h.b_dev),
+                             audio, in_row0, Ly);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch out_head");
   return VOC_OK;
 }
@@ -819,9 +845,8 @@ voc_status launch_prep(vocoder *ctx, const float *x, int B, int C, int T, int Cp
                        long long Lp = -1) {
   const int T_pad = Lp < 0 ? rup(T, 8) : T;
   dim3 grid((T_pad + 255) / 256, Cp / 8, B);
-  voc::prep_hl_kernel<<<grid, 256, 0, stream>>>(x, C, T, T_pad, Cp, alpha, invb, hl, row0,
-                                                Lp < 0 ? (long long)T_pad : Lp);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(voc::prep_hl_kernel, grid, dim3(256), 0, stream, x, C, T, T_pad, Cp,
+                             alpha, invb, hl, row0, Lp < 0 ? (long long)T_pad : Lp);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch prep");
   return VOC_OK;
 }
@@ -1385,9 +1410,9 @@ VOC_API voc_status vocoder_stitch(const float *decoded_dev, int n_win, int n_sid
   if (len < 0) return fail(nullptr, VOC_INVALID_ARG, "stitch: invalid window geometry");
   if (len == 0) return VOC_OK;
   dim3 grid(static_cast<unsigned>((len + 255) / 256), static_cast<unsigned>(n_sides));
-  voc::stitch_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      decoded_dev, n_win, n_sides, win_frames, crop_left, crop_right, hop, len, out_dev);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(voc::stitch_kernel, grid, dim3(256), 0,
+                             reinterpret_cast<cudaStream_t>(stream), decoded_dev, n_win, n_sides,
+                             win_frames, crop_left, crop_right, hop, len, out_dev);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "launch stitch");
   return VOC_OK;
 }
@@ -1812,8 +1837,8 @@ VOC_API voc_status vocoder_stream_decode(vocoder_stream *s, const float *latent_
   auto copies = [&](int first, int n) -> voc_status {
     if (n == 0) return VOC_OK;
     const int blocks = std::max(1, std::min((s->max_job_elems + 255) / 256, 64));
-    voc::row_copy_kernel<<<dim3(blocks, n), 256, 0, stream>>>(s->jobs + first, frames);
-    cudaError_t ce = cudaGetLastError();
+    cudaError_t ce = launch_pdl(voc::row_copy_kernel, dim3(blocks, n), dim3(256), 0, stream,
+                                static_cast<const voc::RowCopyJob *>(s->jobs + first), frames);
     return ce == cudaSuccess ? VOC_OK : cuda_fail(ctx, ce, "launch row_copy");
   };
   voc_status st = copies(0, s->n_restore);  // contexts of the previous chunk
