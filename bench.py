@@ -35,7 +35,7 @@ from dac_vocoder_decode_gb300 import workloads as W  # noqa: E402
 METRIC = "vocoder audio samples/sec"
 UNIT = "samples/s"
 SAMPLE_RATE = {"music_window": 44100, "music_batch8": 44100, "music_long": 44100, "speech": 24000,
-               "tiny": 44100, "tiny_cal": 44100}
+               "speech_snakebeta": 24000, "tiny": 44100, "tiny_cal": 44100}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 

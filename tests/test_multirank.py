@@ -58,3 +58,14 @@ def test_single_process_max_is_identity():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
+
+
+def test_every_workload_has_a_sample_rate_and_config():
+    """bench.py can report every workload it accepts (--workload choices)."""
+    import bench
+    from dac_vocoder_decode_gb300 import workloads as W
+    for name in W.WORKLOADS:
+        assert name in bench.SAMPLE_RATE, name
+        wl = W.make_workload(name, T=2, B=1)
+        cfg = bench.config_of(wl, name)
+        assert cfg["sample_rate"] == bench.SAMPLE_RATE[name]
