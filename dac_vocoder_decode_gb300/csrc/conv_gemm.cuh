@@ -93,8 +93,11 @@ struct ConvGemmArgs {
   float *out_f32;          // fp32 output, chunk-major [B][Cp_out/4][f32_L][4], or null
   __nv_bfloat16 *out_hl;   // hi/lo output, chunk-major [B][2*Cp_out/8][hl_L][8], or null
   int Cp_out, s_rows;      // output channels (padded), output rows per D row
-  int phase_group;         // ConvT with columns in phase pairs: phases per group G (even);
-                           // 0: phase-major columns (n = phase * Cp_out + channel)
+  int phase_group;         // ConvT, columns in 8-channel blocks of the G phases of a group
+                           // (n = q G Cp + (co / 8) 8 G + r 8 + co % 8): G even, stored by
+                           // 16-column chunks (phase pairs); G odd, by whole blocks with lane
+                           // pairs (see convT_block_odd).  0: phase-major columns
+                           // (n = phase * Cp_out + channel).
   int b2;                  // 1 (the kernel's B2 form): each weight chunk holds its hi rows then its lo rows, and a K
                            // step is two MMAs: A_hi x [W_hi | W_lo] into 2 N_tile accumulator
                            // columns, then A_lo x W_hi into the first N_tile; the epilogue adds
@@ -220,6 +223,130 @@ __device__ __forceinline__ bool store_phase_pair(const ConvGemmArgs &p, volatile
   return true;
 }
 
+// ConvT with an odd number G of phases per group (causal s = 3, 5): one 8-channel block of the
+// G phases (8 G columns from n0, TMEM columns from taddr) for this warp's 32 rows.  Input row
+// t owns output rows t G .. t G + G - 1; a lane pair (t even, t + 1) owns 2G rows starting at
+// the even row t G, which split into G aligned row pairs: the even lane stores its phases
+// (0, 1), (2, 3), ... and (G - 1, the odd lane's phase 0), the odd lane its phases (1, 2),
+// (3, 4), ...  Each pair goes out as 32-byte stores (16-byte stores of the first row when the
+// second is past the rows to write).  Two passes (fp32 output, then hi/lo output) keep at most
+// three phases of 8 values live; phases are re-read from TMEM in each pass.
+__device__ __forceinline__ bool convT_block_odd(const ConvGemmArgs &p, volatile int *abort_flag,
+                                                int b, int t, int n0, uint32_t taddr, int lane) {
+  const int G = p.phase_group;
+  const bool odd_lane = (lane & 1) != 0;
+  const int cg = n0 / (8 * G);               // causal: one phase group
+  const long long row0 = (long long)t * p.s_rows;  // this lane's first output row
+  const bool f_snake = (p.flags & EPI_F32_SNAKE) != 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 0 ? !p.out_f32 : !p.out_hl) continue;
+    const bool snake_it = (pass == 1 || f_snake) && p.alpha;  // hi/lo always carry the Snake
+    float bb[8], a[8], ib[8];
+    ldg_vec(p.bias + n0, bb);  // the same for every phase of the block
+    if (snake_it) {
+      ldg_vec(p.alpha + n0, a);
+      ldg_vec(p.invb + n0, ib);
+    }
+    // this lane's value of phase r (8 channels)
+    auto value = [&](int r, float (&out)[8]) {
+      uint32_t q[8];
+      tmem_ld8_issue(taddr + static_cast<uint32_t>(8 * r), q);
+      tmem_ld8_wait(q);
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(q[i]) + bb[i];
+      if (snake_it) {
+        snake_n<8>(v, a, ib, out);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) out[i] = v[i];
+      }
+    };
+    float prev[8];
+    value(0, prev);
+    for (int k = 0; 2 * k < G; ++k) {
+      float p1[8], p2[8];
+      if (2 * k + 1 < G) {
+        value(2 * k + 1, p1);
+      } else {  // the even lane's last pair ends with the odd lane's phase 0
+        float z[8];
+        value(0, z);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p1[i] = __shfl_down_sync(0xffffffffu, z[i], 1);
+      }
+      const bool have2 = 2 * k + 2 < G;
+      if (have2) {
+        value(2 * k + 2, p2);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p2[i] = 0.f;
+      }
+      // even lane: rows (2k, 2k+1) = phases (2k, 2k+1); odd lane: phases (2k+1, 2k+2)
+      const long long R = row0 + 2 * k + (odd_lane ? 1 : 0);
+      const bool active = !odd_lane || have2;
+      if (active && R < p.rows_pad) {
+        const bool two = R + 1 < p.rows_pad;
+        const bool z0 = R >= p.rows_valid, z1 = R + 1 >= p.rows_valid;  // padding rows: zeros
+        float A[8], B[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          A[i] = z0 ? 0.f : (odd_lane ? p1[i] : prev[i]);
+          B[i] = z1 ? 0.f : (odd_lane ? p2[i] : p1[i]);
+        }
+        if (pass == 0) {
+          const size_t L_out = static_cast<size_t>(p.f32_L);
+          const size_t row = static_cast<size_t>(R) + p.f32_row0;
+          VOC_CHECK((((long long)b * (p.Cp_out / 4) + 2 * cg + 1) * (long long)L_out + row + 1) * 4 + 4 <=
+                        p.f32_elems, 18, b, cg, (int)row);
+          float *base = p.out_f32 + ((size_t)b * (p.Cp_out / 4) + 2 * cg) * L_out * 4 + row * 4;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float *q = base + (size_t)j * L_out * 4;
+            if (two) {
+              const uint32_t w[8] = {__float_as_uint(A[4 * j]), __float_as_uint(A[4 * j + 1]),
+                                     __float_as_uint(A[4 * j + 2]), __float_as_uint(A[4 * j + 3]),
+                                     __float_as_uint(B[4 * j]), __float_as_uint(B[4 * j + 1]),
+                                     __float_as_uint(B[4 * j + 2]), __float_as_uint(B[4 * j + 3])};
+              st_global_v8(q, w);
+            } else {
+              *reinterpret_cast<float4 *>(q) = make_float4(A[4 * j], A[4 * j + 1], A[4 * j + 2], A[4 * j + 3]);
+            }
+          }
+        } else {
+          uint32_t hw[8], lw[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float x0 = i < 4 ? A[2 * i] : B[2 * i - 8];
+            const float x1 = i < 4 ? A[2 * i + 1] : B[2 * i - 7];
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+            const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
+            const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
+            hw[i] = pack_bf16x2(h0, h1);
+            lw[i] = pack_bf16x2(l0, l1);
+          }
+          const size_t L_out = static_cast<size_t>(p.hl_L);
+          const size_t row = static_cast<size_t>(R) + p.hl_row0;
+          const size_t item = (size_t)b * (2 * p.Cp_out / 8);
+          VOC_CHECK((((long long)item + p.Cp_out / 8 + cg) * (long long)L_out + row + 1) * 8 + 8 <=
+                        p.hl_elems, 19, b, cg, (int)row);
+          __nv_bfloat16 *hq = p.out_hl + ((item + cg) * L_out + row) * 8;
+          __nv_bfloat16 *lq = p.out_hl + ((item + p.Cp_out / 8 + cg) * L_out + row) * 8;
+          if (two) {
+            st_global_v8(hq, hw);
+            st_global_v8(lq, lw);
+          } else {
+            *reinterpret_cast<uint4 *>(hq) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(lq) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) prev[i] = p2[i];
+    }
+  }
+  return true;
+}
+
 // Epilogue of one warp for 32 rows (its TMEM lane quadrant) x CW columns
 // n0..n0+CW-1, which lie in one ConvT phase because CW divides C_out.
 template <int CW, bool B2 = false>
@@ -314,7 +441,8 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
     for (int i = 0; i < CW; ++i) sn[i] = v[i];
   }
   if constexpr (CW == 16) {
-    if (p.phase_group) return store_phase_pair<CW>(p, abort_flag, b, t, n0, v, sn);
+    if (p.phase_group && !(p.phase_group & 1))
+      return store_phase_pair<CW>(p, abort_flag, b, t, n0, v, sn);
   }
   const int ph = n0 / p.Cp_out;  // ConvT phase of these columns (0 for a conv)
   const int co0 = n0 - ph * p.Cp_out;
@@ -395,7 +523,10 @@ __device__ __forceinline__ void drain_ring_strided(uint64_t *full, int slots, in
   }
 }
 
-template <int CW, bool PAIR, bool B2 = false>
+// B2: the two-MMA K step (ConvGemmArgs::b2).  ODDT: a transposed conv with an odd number of
+// phases per group, stored by convT_block_odd.  Separate instantiations keep the common form's
+// register budget.
+template <int CW, bool PAIR, bool B2 = false, bool ODDT = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap tmapA,
                      const __grid_constant__ CUtensorMap tmapS, const ConvGemmArgs p) {
@@ -798,6 +929,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row_in_tile = quad * 32 + lane;
     const uint32_t sbase = smem_u32(smS);
     const int nsh = p.ns > 0 ? p.ns / kEpiGroups : 1;  // residual slots of this group's ring
+    constexpr bool odd_blocks = ODDT;
     // where this warp reports a free accumulator: this CTA's barrier, or the even CTA's
     const uint32_t acc_empty0 = PAIR ? mapa_shared(smem_u32(accEmpty), 0u) : smem_u32(accEmpty);
     int kslot = 0;                           // this group's residual ring position
@@ -819,7 +951,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int t = mt * kM + row0 + row_in_tile;
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * p.acc_cols) +
                              (static_cast<uint32_t>(quad * 32) << 16);
-      for (int c = half; c < n_chunks && ok; c += kEpiGroups) {
+      if constexpr (odd_blocks) {  // ConvT with an odd number of phases: whole 8-channel blocks
+        const int bw = 8 * p.phase_group;
+        for (int blk = half; blk < p.N_tile / bw && ok; blk += kEpiGroups) {
+          ok = convT_block_odd(p, abort_flag, b, t, nt * p.N_tile + blk * bw, tbase + blk * bw, lane);
+          ok = __all_sync(0xffffffffu, ok);
+        }
+      }
+      for (int c = half; c < n_chunks && ok && !odd_blocks; c += kEpiGroups) {
         const int slot = half * nsh + kslot;
         ok = epilogue_chunk<CW, B2>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
                                 smem_u32(skipFull + slot), smem_u32(skipEmpty + slot), kph,

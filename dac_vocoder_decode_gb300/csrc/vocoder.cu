@@ -131,6 +131,9 @@ bool set_kernel_attrs(std::string &why) {
       st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false, false, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
@@ -221,8 +224,13 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     // its G phases consecutively (8 columns per phase), so a 16-column epilogue chunk holds
     // two consecutive output rows of 8 channels and is written with 32-byte stores; with G
     // odd, phase-major (n = r * Cp_out + co within the group).
+    // With G odd (causal s = 3, 5) the columns are blocked the same way and the epilogue
+    // stores whole blocks through lane pairs (the causal output rows of a lane pair are 2G
+    // consecutive rows); the column tile then holds whole blocks.
     const int G = (padding == VOC_PAD_SYMMETRIC) ? s / 2 : s;
-    g.phase_group = (G % 2 == 0 && L.Cp_out % 8 == 0) ? G : 0;
+    // (the CTA-pair kernel has no odd-phase epilogue)
+    g.phase_group = (L.Cp_out % 8 == 0 && (G % 2 == 0 || (padding == VOC_PAD_CAUSAL && !L.pair)))
+                        ? G : 0;
   } else {
     const int span = L.dil * (L.K - 1);
     const int pad_left = (padding == VOC_PAD_CAUSAL) ? span : span / 2;
@@ -236,10 +244,18 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   }
   g.N_tile = 0;
   for (int t = 256; t >= 16; t -= 16)
-    if (group % t == 0) {
+    if (group % t == 0 && !(L.convT && (g.phase_group & 1) && t % (8 * g.phase_group))) {
       g.N_tile = t;
       break;
     }
+  if (!g.N_tile && L.convT && (g.phase_group & 1)) {  // no tile of whole blocks: phase-major
+    g.phase_group = 0;
+    for (int t = 256; t >= 16; t -= 16)
+      if (group % t == 0) {
+        g.N_tile = t;
+        break;
+      }
+  }
   if (!g.N_tile) {
     why = "no column tile divides " + std::to_string(group);
     return false;
@@ -320,7 +336,8 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   g.nkb = L.Cp_in / g.KB;
   // Two MMAs per K step where the doubled column count fits one MMA (N <= 256): narrow
   // layers issue a third fewer MMA instructions, whose rate limits them.
-  g.b2 = (!L.pair && 2 * g.N_tile <= 256) ? 1 : 0;
+  // (not with the odd-phase ConvT epilogue, which has its own kernel form)
+  g.b2 = (!L.pair && 2 * g.N_tile <= 256 && !(L.convT && (g.phase_group & 1))) ? 1 : 0;
   int ac = 32;
   while (ac < (g.b2 ? 2 * g.N_tile : g.N_tile)) ac *= 2;
   g.acc_cols = ac;
@@ -805,6 +822,9 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
   } else if (L.g.b2) {
     e = launch_pdl(voc::conv_gemm_kernel<16, false, true>, dim3(grid), dim3(voc::kGemmThreads),
                    L.smem, stream, map, smap, a);
+  } else if (L.convT && (L.g.phase_group & 1)) {
+    e = launch_pdl(voc::conv_gemm_kernel<16, false, false, true>, dim3(grid),
+                   dim3(voc::kGemmThreads), L.smem, stream, map, smap, a);
   } else {
     e = launch_pdl(voc::conv_gemm_kernel<16, false>, dim3(grid), dim3(voc::kGemmThreads), L.smem,
                    stream, map, smap, a);

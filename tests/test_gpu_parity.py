@@ -108,6 +108,7 @@ CONVT_CASES = [
     (2, 768, 384, 65, 5, W.PAD_CAUSAL),
     (1, 192, 96, 131, 4, W.PAD_CAUSAL),
     (1, 8, 4, 50, 2, W.PAD_SYMMETRIC),           # padded channels
+    (1, 24, 12, 33, 3, W.PAD_CAUSAL),            # odd phase count, padded channels, odd length
 ]
 
 
