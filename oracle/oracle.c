@@ -21,6 +21,27 @@ int oracle_param_count(const oracle_arch *a) {
   return (a->in_proj_channels > 0 ? 2 : 0) + 2 + a->n_stages * (3 + 6 * a->n_dilations) + 3;
 }
 
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.  A finite
+   value a is a multiple of its quantum 2^(e - 10), e = floor(log2 a), and of 2^-24 below the
+   normal range; rounding is to the nearest multiple, ties to the even multiple. */
+static double round_half_one(double x) {
+  const float f = (float)x; /* the library receives single-precision weights */
+  const double a = fabs((double)f);
+  if (a == 0.0 || !isfinite(a)) return (double)f;
+  if (a >= 65520.0) return copysign(INFINITY, (double)f); /* halfway to 2^16 rounds up */
+  int E;
+  frexp(a, &E);        /* a = m 2^E, m in [0.5, 1): floor(log2 a) = E - 1 */
+  int e = E - 1;
+  if (e < -14) e = -14; /* subnormals share the quantum of the smallest binade */
+  const double q = ldexp(1.0, e - 10);
+  const double r = nearbyint(a / q); /* exact quotient; default rounding: ties to even */
+  return copysign(r * q, (double)f);
+}
+
+void oracle_round_half(const double *x, long n, double *y) {
+  for (long i = 0; i < n; ++i) y[i] = round_half_one(x[i]);
+}
+
 long oracle_hop(const oracle_arch *a) {
   long h = 1;
   for (int i = 0; i < a->n_stages; ++i) h *= a->strides[i];

@@ -79,6 +79,13 @@ typedef struct {
  * With snake_beta every snake*.alpha entry is [2][C] instead: log alpha, then log beta. */
 int oracle_param_count(const oracle_arch *a);
 
+/* y[i] = x[i] rounded to single precision, then to IEEE 754 binary16 (half precision),
+ * both round to nearest, ties to even: the convolution weights of the F16-weight precision
+ * variant (minimaxmusic.cpp Architecture, "Flow VAE": conv weights are stored F16 on the
+ * device with F32 activations).  Values at or beyond 65520 in magnitude become infinite;
+ * magnitudes below 2^-14 use the subnormal quantum 2^-24. */
+void oracle_round_half(const double *x, long n, double *y);
+
 /* w[i, :] = g[i] * v[i, :] / ||v[i, :]||, the norm taken over everything but
  * axis 0 of the stored tensor (Conv1d [Cout][Cin][K]: per output channel;
  * ConvTranspose1d [Cin][Cout][K]: per input channel).  Returns -1 when a row of

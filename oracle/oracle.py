@@ -47,6 +47,8 @@ def _load():
             F = ctypes.POINTER(ctypes.c_float)
             lib.oracle_fold_weight_norm.argtypes = [F, F, ctypes.c_int, ctypes.c_long, D]
             lib.oracle_fold_weight_norm.restype = ctypes.c_int
+            lib.oracle_round_half.argtypes = [D, ctypes.c_long, D]
+            lib.oracle_round_half.restype = None
             lib.oracle_snake_row.argtypes = [D, ctypes.c_long, ctypes.c_double, ctypes.c_int, D]
             lib.oracle_snake_row.restype = None
             lib.oracle_snake_beta_row.argtypes = [D, ctypes.c_long, ctypes.c_double,
@@ -167,16 +169,27 @@ def conv_transpose1d(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray], stri
     return y
 
 
-def fold_params(params: Sequence) -> list:
+def round_half(x: np.ndarray) -> np.ndarray:
+    """Round to single, then to IEEE half precision (both to nearest, ties to even)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    _load().oracle_round_half(_d(x), x.size, _d(y))
+    return y
+
+
+def fold_params(params: Sequence, f16_weights: bool = False) -> list:
     """Raw canonical parameters (RawConv / alpha arrays) -> list of double arrays
-    (folded weight, bias, alpha, ...) in the canonical order."""
+    (folded weight, bias, alpha, ...) in the canonical order.  f16_weights: every
+    convolution weight rounded to half precision (the F16-weight precision variant);
+    biases and Snake parameters are kept."""
     out = []
+    wf = round_half if f16_weights else (lambda w: w)
     for p in params:
         if hasattr(p, "g"):
-            out.append(fold_weight_norm(p.g, p.v))
+            out.append(wf(fold_weight_norm(p.g, p.v)))
             out.append(None if p.b is None else np.ascontiguousarray(p.b, dtype=np.float64))
         elif hasattr(p, "w"):  # a convolution stored without weight norm
-            out.append(np.ascontiguousarray(p.w, dtype=np.float64))
+            out.append(wf(np.ascontiguousarray(p.w, dtype=np.float64)))
             out.append(None if p.b is None else np.ascontiguousarray(p.b, dtype=np.float64))
         else:
             out.append(np.ascontiguousarray(p, dtype=np.float64))

@@ -537,3 +537,50 @@ def test_snake_beta_decoder_uses_both_rows():
     np.testing.assert_allclose(O.decode(beta, None, wl.latent, 0, fb80), ident, rtol=0, atol=1e-12)
     swapped = with_snakes(lambda f: np.stack([np.full(f.shape, 80.0), np.full(f.shape, 0.3)]))
     assert np.max(np.abs(O.decode(beta, None, wl.latent, 0, swapped) - ident)) > 1e-3
+
+
+# ----------------------------------------------------------------------------- F16 weights
+def test_round_half_matches_numpy():
+    """Single then half precision, ties to even, against numpy's float32 -> float16 casts."""
+    rng = np.random.default_rng(17)
+    mags = 10.0 ** rng.uniform(-9, 5, size=4000)
+    x = mags * rng.choice([-1.0, 1.0], size=mags.size)
+    ties = []
+    for e in range(-24, 16):  # exact halfway points between neighbouring halves
+        q = 2.0 ** max(e - 10, -24)
+        for k in (1, 2, 3, 1023, 1024, 2047):
+            ties.append((k + 0.5) * q)
+    edges = [0.0, -0.0, 65504.0, 65519.99, 65520.0, -65520.0, 6.1e-5, 2.0 ** -24, 2.0 ** -25,
+             1.5 * 2.0 ** -25]
+    x = np.concatenate([x, np.array(ties), -np.array(ties), np.array(edges)])
+    with np.errstate(over="ignore"):
+        ref = np.float16(np.float32(x)).astype(np.float64)
+    got = O.round_half(x)
+    assert np.array_equal(np.signbit(got), np.signbit(ref))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_f16_weights_round_only_convolution_weights():
+    """fold_params(f16_weights=True) rounds every convolution weight (weight-normalised or
+    not) and leaves biases and Snake parameters as they are."""
+    arch = W.Arch(latent_channels=6, channels0=24, strides=(4, 2), widths=(12, 8),
+                  in_proj_channels=10)
+    wl = W.make_custom(arch, B=1, T=9, seed=5)
+    full = O.fold_params(wl.params)
+    half = O.fold_params(wl.params, f16_weights=True)
+    names = [n for n, _ in arch.param_shapes()]
+    changed = 0
+    for n, a, b in zip(names, full, half):
+        if n.endswith(".w"):
+            np.testing.assert_array_equal(b, O.round_half(a))
+            changed += int(np.any(a != b))
+        elif a is None:
+            assert b is None
+        else:
+            np.testing.assert_array_equal(a, b)
+    assert changed == sum(n.endswith(".w") for n in names)
+    # half-precision weights move the decode by about the weights' relative rounding (2^-11)
+    y0 = O.decode(arch, None, wl.latent, 0, full)
+    y1 = O.decode(arch, None, wl.latent, 0, half)
+    d = np.max(np.abs(y1 - y0))
+    assert 1e-7 < d < 1e-2
