@@ -28,6 +28,7 @@ VOC_DEVICE_TIMEOUT = -8
 VOC_PAD_SYMMETRIC = 0
 VOC_PAD_CAUSAL = 1
 VOC_PREC_BF16X3 = 0
+VOC_PREC_F16W = 1
 VOC_SNAKE = 0
 VOC_SNAKE_BETA = 1
 VOC_FLAG_CHECK_FINITE = 1
@@ -178,14 +179,15 @@ def _stream_ptr(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(int(stream))
 
 
-def make_desc(arch, fuse_max_channels: int = 0, cta_pair: int = 0) -> VocDesc:
+def make_desc(arch, fuse_max_channels: int = 0, cta_pair: int = 0,
+              precision: int = VOC_PREC_BF16X3) -> VocDesc:
     """voc_desc for an Arch (layer shapes from workloads.Arch or any object with the same fields)."""
     strides = (ctypes.c_int * len(arch.strides))(*arch.strides)
     widths = (ctypes.c_int * len(arch.widths))(*arch.widths)
     dils = (ctypes.c_int * len(arch.dilations))(*arch.dilations)
     d = VocDesc(VOC_ABI_VERSION, arch.latent_channels, arch.in_kernel, arch.channels0,
                 len(arch.strides), strides, widths, len(arch.dilations), dils, arch.res_kernel,
-                arch.out_kernel, 1, arch.padding, VOC_PREC_BF16X3, fuse_max_channels, cta_pair,
+                arch.out_kernel, 1, arch.padding, precision, fuse_max_channels, cta_pair,
                 getattr(arch, "in_proj_channels", 0),
                 VOC_SNAKE_BETA if getattr(arch, "snake_beta", False) else VOC_SNAKE)
     d._keep = (strides, widths, dils)
@@ -220,13 +222,14 @@ def vocoder_fold_weight_norm(g: np.ndarray, v: np.ndarray) -> np.ndarray:
 
 
 def vocoder_create(arch, params: Sequence[Optional[np.ndarray]],
-                   fuse_max_channels: int = 0, cta_pair: int = 0) -> ctypes.c_void_p:
+                   fuse_max_channels: int = 0, cta_pair: int = 0,
+                   precision: int = VOC_PREC_BF16X3) -> ctypes.c_void_p:
     """params: folded fp32 arrays in the canonical order (None for a zero bias)."""
     lib = load_library()
     keep = [None if p is None else np.ascontiguousarray(p, dtype=np.float32) for p in params]
     arr = (ctypes.POINTER(ctypes.c_float) * len(keep))(*[_fptr(p) for p in keep])
     h = ctypes.c_void_p()
-    _check(lib.vocoder_create(ctypes.byref(make_desc(arch, fuse_max_channels, cta_pair)), arr,
+    _check(lib.vocoder_create(ctypes.byref(make_desc(arch, fuse_max_channels, cta_pair, precision)), arr,
                               len(keep),
                               ctypes.byref(h)))
     return h
@@ -467,9 +470,10 @@ class VocoderStream:
 class Vocoder:
     """A decoder on the current CUDA device (owns its library context)."""
 
-    def __init__(self, arch, folded_params, fuse_max_channels: int = 0, cta_pair: int = 0):
+    def __init__(self, arch, folded_params, fuse_max_channels: int = 0, cta_pair: int = 0,
+                 precision: int = VOC_PREC_BF16X3):
         self.arch = arch
-        self.handle = vocoder_create(arch, folded_params, fuse_max_channels, cta_pair)
+        self.handle = vocoder_create(arch, folded_params, fuse_max_channels, cta_pair, precision)
         self.hop = vocoder_hop(self.handle)
 
     def close(self):

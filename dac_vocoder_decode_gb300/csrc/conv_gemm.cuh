@@ -40,6 +40,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "hilo.cuh"
 #include "ptx.cuh"
 #include "snake.cuh"
 
@@ -168,7 +169,7 @@ __device__ __forceinline__ void ldg_vec(const float *src, float (&v)[N]) {
 // consecutive output rows (phases r, r+1 of input row t), written as 32-byte stores: fp32
 // two planes of 4 channels, hi and lo one plane of 8 channels each.  The rows start at an
 // even row (s even, r even), so every store is 32-byte aligned.
-template <int CW>
+template <int CW, bool F16>
 __device__ __forceinline__ bool store_phase_pair(const ConvGemmArgs &p, volatile int *abort_flag,
                                                  int b, int t, int n0, float (&v)[CW],
                                                  float (&sn)[CW]) {
@@ -204,14 +205,7 @@ __device__ __forceinline__ bool store_phase_pair(const ConvGemmArgs &p, volatile
   if (p.out_hl) {
     uint32_t hw[8], lw[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(sn[2 * i]);
-      const __nv_bfloat16 h1 = __float2bfloat16_rn(sn[2 * i + 1]);
-      const __nv_bfloat16 l0 = __float2bfloat16_rn(sn[2 * i] - __bfloat162float(h0));
-      const __nv_bfloat16 l1 = __float2bfloat16_rn(sn[2 * i + 1] - __bfloat162float(h1));
-      hw[i] = pack_bf16x2(h0, h1);
-      lw[i] = pack_bf16x2(l0, l1);
-    }
+    for (int i = 0; i < 8; ++i) split_pair<F16>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
     const size_t L_out = static_cast<size_t>(p.hl_L);
     const size_t row = static_cast<size_t>(out_row) + p.hl_row0;
     const size_t item = (size_t)b * (2 * p.Cp_out / 8);
@@ -231,6 +225,7 @@ __device__ __forceinline__ bool store_phase_pair(const ConvGemmArgs &p, volatile
 // (3, 4), ...  Each pair goes out as 32-byte stores (16-byte stores of the first row when the
 // second is past the rows to write).  Two passes (fp32 output, then hi/lo output) keep at most
 // three phases of 8 values live; phases are re-read from TMEM in each pass.
+template <bool F16>
 __device__ __forceinline__ bool convT_block_odd(const ConvGemmArgs &p, volatile int *abort_flag,
                                                 int b, int t, int n0, uint32_t taddr, int lane) {
   const int G = p.phase_group;
@@ -318,11 +313,7 @@ __device__ __forceinline__ bool convT_block_odd(const ConvGemmArgs &p, volatile 
           for (int i = 0; i < 8; ++i) {
             const float x0 = i < 4 ? A[2 * i] : B[2 * i - 8];
             const float x1 = i < 4 ? A[2 * i + 1] : B[2 * i - 7];
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-            const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
-            const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
-            hw[i] = pack_bf16x2(h0, h1);
-            lw[i] = pack_bf16x2(l0, l1);
+            split_pair<F16>(x0, x1, hw[i], lw[i]);
           }
           const size_t L_out = static_cast<size_t>(p.hl_L);
           const size_t row = static_cast<size_t>(R) + p.hl_row0;
@@ -349,7 +340,7 @@ __device__ __forceinline__ bool convT_block_odd(const ConvGemmArgs &p, volatile 
 
 // Epilogue of one warp for 32 rows (its TMEM lane quadrant) x CW columns
 // n0..n0+CW-1, which lie in one ConvT phase because CW divides C_out.
-template <int CW, bool B2 = false>
+template <int CW, bool B2 = false, bool F16 = false>
 __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t sslot,
                                                uint32_t sfull, uint32_t sempty, uint32_t sparity,
                                                volatile int *abort_flag, int row_in_tile,
@@ -442,7 +433,7 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
   }
   if constexpr (CW == 16) {
     if (p.phase_group && !(p.phase_group & 1))
-      return store_phase_pair<CW>(p, abort_flag, b, t, n0, v, sn);
+      return store_phase_pair<CW, F16>(p, abort_flag, b, t, n0, v, sn);
   }
   const int ph = n0 / p.Cp_out;  // ConvT phase of these columns (0 for a conv)
   const int co0 = n0 - ph * p.Cp_out;
@@ -468,14 +459,7 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
   if (p.out_hl) {
     uint32_t hw[CW / 2], lw[CW / 2];
 #pragma unroll
-    for (int i = 0; i < CW / 2; ++i) {
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(sn[2 * i]);
-      const __nv_bfloat16 h1 = __float2bfloat16_rn(sn[2 * i + 1]);
-      const __nv_bfloat16 l0 = __float2bfloat16_rn(sn[2 * i] - __bfloat162float(h0));
-      const __nv_bfloat16 l1 = __float2bfloat16_rn(sn[2 * i + 1] - __bfloat162float(h1));
-      hw[i] = pack_bf16x2(h0, h1);
-      lw[i] = pack_bf16x2(l0, l1);
-    }
+    for (int i = 0; i < CW / 2; ++i) split_pair<F16>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
     const size_t L_out = static_cast<size_t>(p.hl_L);
     const size_t row = row_t + p.hl_row0;
     const size_t item = (size_t)b * (2 * p.Cp_out / 8);
@@ -524,9 +508,10 @@ __device__ __forceinline__ void drain_ring_strided(uint64_t *full, int slots, in
 }
 
 // B2: the two-MMA K step (ConvGemmArgs::b2).  ODDT: a transposed conv with an odd number of
-// phases per group, stored by convT_block_odd.  Separate instantiations keep the common form's
-// register budget.
-template <int CW, bool PAIR, bool B2 = false, bool ODDT = false>
+// phases per group, stored by convT_block_odd.  F16: the F16-weight precision (f16 operands,
+// one weight plane, two MMAs per K step: A_hi x W and A_lo x W; f16 hi/lo outputs).  Separate
+// instantiations keep the common form's register budget.
+template <int CW, bool PAIR, bool B2 = false, bool ODDT = false, bool F16 = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap tmapA,
                      const __grid_constant__ CUtensorMap tmapS, const ConvGemmArgs p) {
@@ -719,7 +704,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else
           mma_commit_warp(smem_u32(bar));
       };
-      const uint32_t idesc = idesc_bf16_f32(kM, p.N_tile);
+      const uint32_t idesc = F16 ? idesc_f16_f32(kM, p.N_tile) : idesc_bf16_f32(kM, p.N_tile);
       const uint32_t idesc2 = idesc_bf16_f32(kM, 2 * p.N_tile);  // b2: [W_hi | W_lo]
       // Descriptor low words step by 16-byte units: +1 is +16 bytes of start address.  The
       // ring positions (slot, phase) advance incrementally: this loop is issue-bound, so it
@@ -781,7 +766,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
 #endif
             uint32_t a_hi = a0, b_hi = b_desc0 + sb * b_slot_step;
-            if constexpr (B2) {
+            if constexpr (F16) {  // one f16 weight plane
+              for (int ks = 0; ks < nks; ++ks, a_hi += dA_k, b_hi += dB_k) {
+                mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi, desc_hi, idesc, accum);
+                mma_bf16_warp_lo<PAIR>(d_tmem, a_hi + dA_lo, b_hi, desc_hi, idesc, 1u);
+                accum = 1u;
+              }
+            } else if constexpr (B2) {
               for (int ks = 0; ks < nks; ++ks, a_hi += dA_k, b_hi += dB_k) {
                 mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi, desc_hi, idesc2, accum);
                 mma_bf16_warp_lo<PAIR>(d_tmem, a_hi + dA_lo, b_hi, desc_hi, idesc, 1u);
@@ -954,13 +945,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if constexpr (odd_blocks) {  // ConvT with an odd number of phases: whole 8-channel blocks
         const int bw = 8 * p.phase_group;
         for (int blk = half; blk < p.N_tile / bw && ok; blk += kEpiGroups) {
-          ok = convT_block_odd(p, abort_flag, b, t, nt * p.N_tile + blk * bw, tbase + blk * bw, lane);
+          ok = convT_block_odd<F16>(p, abort_flag, b, t, nt * p.N_tile + blk * bw, tbase + blk * bw, lane);
           ok = __all_sync(0xffffffffu, ok);
         }
       }
       for (int c = half; c < n_chunks && ok && !odd_blocks; c += kEpiGroups) {
         const int slot = half * nsh + kslot;
-        ok = epilogue_chunk<CW, B2>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
+        ok = epilogue_chunk<CW, B2, F16>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
                                 smem_u32(skipFull + slot), smem_u32(skipEmpty + slot), kph,
                                 abort_flag, row_in_tile, b, t, nt * p.N_tile + c * CW,
                                 tbase + c * CW, sbase, smem_u32(bars));

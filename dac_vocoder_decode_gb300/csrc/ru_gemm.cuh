@@ -49,7 +49,7 @@ __device__ __forceinline__ void ru_epilogue1(const ConvGemmArgs &p, const RuExtr
     const float s0 = sn[2 * i], s1 = sn[2 * i + 1];
     const __nv_bfloat16 h0 = __float2bfloat16_rn(s0), h1 = __float2bfloat16_rn(s1);
     const __nv_bfloat16 l0 = __float2bfloat16_rn(s0 - __bfloat162float(h0));
-    const __nv_bfloat16 l1 = __float2bfloat16_rn(s1 - __bfloat162float(h1));
+    const __nv_bfloat16 l1 = __float2bfloat16_rn(s1 - __bfloat162float(h1));  // bf16x3 only
     hw[i] = pack_bf16x2(h0, h1);
     lw[i] = pack_bf16x2(l0, l1);
   }

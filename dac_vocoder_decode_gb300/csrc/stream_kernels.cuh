@@ -10,19 +10,21 @@
 
 #include <cstdint>
 
+#include "hilo.cuh"
 #include "ptx.cuh"
 #include "snake.cuh"
 
 namespace voc {
 
-// x [B][C][T] fp32 -> hl chunk-major [B][2*Cp/8][Lp][8] bf16 at rows row0..row0+T-1:
-// 8-channel chunks of the hi parts, then of the lo parts (hi = bf16(v), lo = bf16(v - hi));
+// x [B][C][T] fp32 -> hl chunk-major [B][2*Cp/8][Lp][8] at rows row0..row0+T-1: 8-channel
+// chunks of the hi parts, then of the lo parts (hi = r(v), lo = r(v - hi), r the rounding to
+// bf16, or to f16 when f16 != 0);
 // channels C..Cp-1 are zeros, and so are rows T..T_pad-1 (the padding rows read by the
 // 8-row TMA groups).  alpha == nullptr: no Snake.  One thread per (b, chunk, t):
 // block 256, grid (ceil(T_pad/256), Cp/8, B).
 __global__ void prep_hl_kernel(const float *__restrict__ x, int C, int T, int T_pad, int Cp,
                                const float *__restrict__ alpha, const float *__restrict__ invb,
-                               __nv_bfloat16 *__restrict__ hl, int row0, long long Lp) {
+                               __nv_bfloat16 *__restrict__ hl, int row0, long long Lp, int f16) {
   pdl_launch_dependents();
   pdl_wait();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
@@ -42,13 +44,10 @@ __global__ void prep_hl_kernel(const float *__restrict__ x, int C, int T, int T_
         if (alpha) v[u] = snake(v[u], alpha[c], invb[c]);
       }
     }
-    const __nv_bfloat16 h0 = __float2bfloat16_rn(v[0]), h1 = __float2bfloat16_rn(v[1]);
-    const __nv_bfloat16 l0 = __float2bfloat16_rn(v[0] - __bfloat162float(h0));
-    const __nv_bfloat16 l1 = __float2bfloat16_rn(v[1] - __bfloat162float(h1));
-    hw[e / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
-                (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
-    lw[e / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
-                (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+    if (f16)
+      split_pair<true>(v[0], v[1], hw[e / 2], lw[e / 2]);
+    else
+      split_pair<false>(v[0], v[1], hw[e / 2], lw[e / 2]);
   }
   const size_t item = (size_t)b * (2 * Cp / 8);
   const size_t r = (size_t)row0 + t;

@@ -84,6 +84,7 @@ enum Buf { BUF_H0 = 0, BUF_H1 = 1, BUF_HB = 2, BUF_FY = 3, BUF_COUNT = 4 };
 struct Layer {
   std::string name;
   bool convT = false;
+  bool f16 = false;         // F16-weight precision: one f16 weight plane, f16 hi/lo operands
   int Cin = 0, Cout = 0, Cp_in = 0, Cp_out = 0, K = 0, dil = 1, stride = 1;
   int level = 0;            // input rate: L_in = T * prod(strides[0..level-1])
   ConvGemmArgs g{};         // geometry; sizes and pointers filled per launch
@@ -134,6 +135,12 @@ bool set_kernel_attrs(std::string &why) {
       st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false, false, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false, false, false, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false, false, true, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
@@ -167,6 +174,7 @@ struct vocoder {
   long long wait_budget = kWaitBudget;
   int fuse_max_c = 0;       // residual units of up to this many (padded) channels run fused
   bool use_pair = true;     // conv layers on CTA pairs
+  bool f16 = false;         // VOC_PREC_F16W: f16 weights, f16 hi/lo activations
   // TMA descriptors for the last (workspace, B, T)
   void *map_ws = nullptr;
   int map_B = -1, map_T = -1;
@@ -287,7 +295,8 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   // pairs) fits beside the A ring and the residual slots, it is loaded once and kept; the
   // k-block is then the largest that leaves three A stages (else two) and at least
   // kMinAInFlight bytes of A in flight (the 1x1 convs wait on their A loads otherwise).
-  const int w_tile = 4 * L.Cp_in * n_stage * g.taps;
+  const int wb = L.f16 ? 2 : 4;  // weight bytes per (channel, column): f16, or bf16 hi + lo
+  const int w_tile = wb * L.Cp_in * n_stage * g.taps;
   for (int min_na = 3; min_na >= 2 && !g.KB && g.n_tiles <= kMaxResidentTiles; --min_na)
     for (int kb = L.Cp_in - L.Cp_in % 16; kb >= 16 && !g.KB; kb -= 16) {
       if (L.Cp_in % kb || 4 * kb * g.rows > 72 * 1024) continue;
@@ -298,7 +307,7 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
       // a 1x1 conv consumes each A stage almost at once: its A ring hides the HBM latency
       const int na = std::min(g.taps == 1 ? 8 : 4, avail / a_bytes);
       if (na < min_na || na * a_bytes < kMinAInFlight) continue;
-      g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = 4 * kb * n_stage, g.na = na, g.ns = ns;
+      g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = wb * kb * n_stage, g.na = na, g.ns = ns;
       g.nb = g.taps * (L.Cp_in / kb);
       g.b_resident = 1;
     }
@@ -306,9 +315,9 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   // consumed at once; its weight stages come from L2), a k-tap conv two
   const int na_want = g.taps == 1 ? 4 : 2;
   for (int kb = L.Cp_in - L.Cp_in % 16; kb >= 16 && !g.KB; kb -= 16) {
-    if (L.Cp_in % kb || 4 * kb * n_stage > kBStageMax || 4 * kb * g.rows > 72 * 1024) continue;
+    if (L.Cp_in % kb || wb * kb * n_stage > kBStageMax || 4 * kb * g.rows > 72 * 1024) continue;
     const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
-    const int b_bytes = 4 * kb * n_stage;
+    const int b_bytes = wb * kb * n_stage;
     int na = na_want;
     while (na > 2 && kSmemMax - 1024 - kBarrierBytes - na * a_bytes < 3 * b_bytes) --na;
     int avail = kSmemMax - 1024 - kBarrierBytes - na * a_bytes;
@@ -337,7 +346,7 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   // Two MMAs per K step where the doubled column count fits one MMA (N <= 256): narrow
   // layers issue a third fewer MMA instructions, whose rate limits them.
   // (not with the odd-phase ConvT epilogue, which has its own kernel form)
-  g.b2 = (!L.pair && 2 * g.N_tile <= 256 && !(L.convT && (g.phase_group & 1))) ? 1 : 0;
+  g.b2 = (!L.pair && !L.f16 && 2 * g.N_tile <= 256 && !(L.convT && (g.phase_group & 1))) ? 1 : 0;
   int ac = 32;
   while (ac < (g.b2 ? 2 * g.N_tile : g.N_tile)) ac *= 2;
   g.acc_cols = ac;
@@ -484,7 +493,7 @@ std::vector<uint16_t> pack_weights(const Layer &L, int padding, const float *w) 
   const ConvGemmArgs &g = L.g;
   const int pw = L.pair ? g.N_tile / 2 : g.N_tile;
   const int n_pt = g.N_total / pw;
-  const size_t tile = (size_t)2 * g.KB * pw;
+  const size_t tile = (size_t)(L.f16 ? 1 : 2) * g.KB * pw;
   std::vector<uint16_t> out((size_t)n_pt * g.taps * g.nkb * tile);
   for (int nt = 0; nt < n_pt; ++nt)
     for (int tap = 0; tap < g.taps; ++tap)
@@ -494,6 +503,10 @@ std::vector<uint16_t> pack_weights(const Layer &L, int padding, const float *w) 
           for (int n = 0; n < pw; ++n)
             for (int e = 0; e < 8; ++e) {
               const float v = weight_value(L, padding, w, nt * pw + n, kb * g.KB + c * 8 + e, tap);
+              if (L.f16) {  // one plane of f16 weights, rounded to nearest even
+                base[((size_t)c * pw + n) * 8 + e] = __half_as_ushort(__float2half_rn(v));
+                continue;
+              }
               const uint16_t hi = f2bf(v);
               const uint16_t lo = f2bf(v - bf2f(hi));
               if (g.b2) {
@@ -619,7 +632,9 @@ bool check_desc(const voc_desc *d, std::string &why) {
   if (d->out_channels != 1) return why = "out_channels must be 1", false;
   if (d->in_proj_channels < 0 || d->in_proj_channels > 8192) return why = "in_proj_channels", false;
   if (d->padding != VOC_PAD_SYMMETRIC && d->padding != VOC_PAD_CAUSAL) return why = "padding", false;
-  if (d->precision != VOC_PREC_BF16X3) return why = "precision", false;
+  if (d->precision != VOC_PREC_BF16X3 && d->precision != VOC_PREC_F16W) return why = "precision", false;
+  if (d->precision == VOC_PREC_F16W && d->cta_pair > 0)
+    return why = "cta_pair is not available with VOC_PREC_F16W", false;
   if (d->cta_pair < -1 || d->cta_pair > 1) return why = "cta_pair must be -1, 0 or 1", false;
   if (d->snake != VOC_SNAKE && d->snake != VOC_SNAKE_BETA) return why = "snake", false;
   for (int i = 0; i < d->n_stages; ++i) {
@@ -819,6 +834,13 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
     else
       e = launch_pdl(voc::ru_gemm_kernel<16>, dim3(grid), dim3(voc::kRuThreads), L.smem, stream,
                      map, smap, a, L.rx);
+  } else if (L.f16) {
+    if (L.convT && (L.g.phase_group & 1))
+      e = launch_pdl(voc::conv_gemm_kernel<16, false, false, true, true>, dim3(grid),
+                     dim3(voc::kGemmThreads), L.smem, stream, map, smap, a);
+    else
+      e = launch_pdl(voc::conv_gemm_kernel<16, false, false, false, true>, dim3(grid),
+                     dim3(voc::kGemmThreads), L.smem, stream, map, smap, a);
   } else if (L.g.b2) {
     e = launch_pdl(voc::conv_gemm_kernel<16, false, true>, dim3(grid), dim3(voc::kGemmThreads),
                    L.smem, stream, map, smap, a);
@@ -866,7 +888,8 @@ voc_status launch_prep(vocoder *ctx, const float *x, int B, int C, int T, int Cp
   const int T_pad = Lp < 0 ? rup(T, 8) : T;
   dim3 grid((T_pad + 255) / 256, Cp / 8, B);
   cudaError_t e = launch_pdl(voc::prep_hl_kernel, grid, dim3(256), 0, stream, x, C, T, T_pad, Cp,
-                             alpha, invb, hl, row0, Lp < 0 ? (long long)T_pad : Lp);
+                             alpha, invb, hl, row0, Lp < 0 ? (long long)T_pad : Lp,
+                             ctx->f16 ? 1 : 0);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch prep");
   return VOC_OK;
 }
@@ -1000,6 +1023,8 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
   ctx->fuse_max_c = desc->fuse_max_channels == 0 ? kFuseDefault
                     : (desc->fuse_max_channels < 0 ? 0 : desc->fuse_max_channels);
   ctx->use_pair = desc->cta_pair > 0;
+  ctx->f16 = desc->precision == VOC_PREC_F16W;
+  if (ctx->f16) ctx->fuse_max_c = 0;  // the fused unit exists in the bf16x3 form only
   auto bail = [&](voc_status st) {
     g_err = ctx->err;
     vocoder_destroy(ctx);
@@ -1021,6 +1046,10 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
   cudaMemset(ctx->err_dev, 0, 8 * sizeof(int));
 
   const int pad = desc->padding;
+  auto plan = [&](Layer &L, bool has_skip) {
+    L.f16 = ctx->f16;
+    return plan_layer(ctx->use_pair, L, pad, has_skip, why);
+  };
   const int nd = desc->n_dilations;
   int p = 0;
   voc_status st;
@@ -1031,7 +1060,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     L.name = "in_proj";
     L.Cin = desc->latent_channels, L.Cout = desc->in_proj_channels, L.K = 1, L.dil = 1;
     L.level = 0;
-    if (!plan_layer(ctx->use_pair, L, pad, false, why))
+    if (!plan(L, false))
       return bail(fail(ctx, VOC_UNSUPPORTED, "in_proj: " + why));
     L.in_buf = BUF_H0, L.hl_buf = BUF_HB;
     st = upload_layer(ctx, ctx->allocs, L, pad, params[0], params[1], SnakeCoef{});
@@ -1047,7 +1076,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     L.Cin = desc->in_proj_channels > 0 ? desc->in_proj_channels : desc->latent_channels;
     L.Cout = desc->channels0, L.K = desc->in_kernel, L.dil = 1;
     L.level = 0;
-    if (!plan_layer(ctx->use_pair, L, pad, false, why))
+    if (!plan(L, false))
       return bail(fail(ctx, VOC_UNSUPPORTED, "conv_in: " + why));
     L.in_buf = conv_in_src, L.hl_buf = BUF_H1;
     st = upload_layer(ctx, ctx->allocs, L, pad, params[p], params[p + 1],
@@ -1076,7 +1105,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       L.convT = true;
       L.Cin = C, L.Cout = Co, L.stride = ctx->strides[i], L.K = 2 * L.stride;
       L.level = i;
-      if (!plan_layer(ctx->use_pair, L, pad, false, why))
+      if (!plan(L, false))
         return bail(fail(ctx, VOC_UNSUPPORTED, L.name + ": " + why));
       L.in_buf = x_buf, L.f32_buf = BUF_FY, L.hl_buf = cur;
       st = upload_layer(ctx, ctx->allocs, L, pad, params[p + 1], params[p + 2],
@@ -1119,7 +1148,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       L1.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".conv1";
       L1.Cin = C, L1.Cout = C, L1.K = desc->res_kernel, L1.dil = ctx->dils[j];
       L1.level = i + 1;
-      if (!plan_layer(ctx->use_pair, L1, pad, false, why))
+      if (!plan(L1, false))
         return bail(fail(ctx, VOC_UNSUPPORTED, L1.name + ": " + why));
       L1.in_buf = cur, L1.hl_buf = tmp;
       st = upload_layer(ctx, ctx->allocs, L1, pad, w1, b1, a2);
@@ -1130,7 +1159,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       L2.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".conv2";
       L2.Cin = C, L2.Cout = C, L2.K = 1, L2.dil = 1;
       L2.level = i + 1;
-      if (!plan_layer(ctx->use_pair, L2, pad, true, why))
+      if (!plan(L2, true))
         return bail(fail(ctx, VOC_UNSUPPORTED, L2.name + ": " + why));
       L2.in_buf = tmp, L2.skip_buf = BUF_FY;
       if (j < nd - 1) {
@@ -1152,7 +1181,11 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     h.C = C, h.Cp = rup(C, 16), h.K = desc->out_kernel;
     h.pad_left = (pad == VOC_PAD_CAUSAL) ? h.K - 1 : (h.K - 1) / 2;
     h.level = desc->n_stages;
-    const float *w = params[p + 1], *b = params[p + 2];
+    const float *w_in = params[p + 1], *b = params[p + 2];
+    // F16-weight precision: the head's weights are rounded to f16 like every conv weight
+    std::vector<float> w((size_t)C * h.K);
+    for (size_t i = 0; i < w.size(); ++i)
+      w[i] = ctx->f16 ? __half2float(__float2half_rn(w_in[i])) : w_in[i];
     std::vector<float> wp((size_t)h.Cp * h.K, 0.f), bp(1, b ? b[0] : 0.f);
     for (int c = 0; c < C; ++c)
       for (int k = 0; k < h.K; ++k) wp[(size_t)c * h.K + k] = w[(size_t)c * h.K + k];

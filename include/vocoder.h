@@ -64,7 +64,14 @@ typedef enum {
 } voc_status;
 
 enum { VOC_PAD_SYMMETRIC = 0, VOC_PAD_CAUSAL = 1 };
-enum { VOC_PREC_BF16X3 = 0 };
+/* precision: VOC_PREC_BF16X3 -- weights and activations as bf16 hi/lo pairs, three bf16
+ * products per multiply (about 16 significant bits per operand), fp32 accumulation;
+ * VOC_PREC_F16W -- every convolution weight rounded to IEEE half precision, as the pages'
+ * port stores them (minimaxmusic.cpp Architecture, "Flow VAE": conv weights F16 on the
+ * device with F32 activations); activations as f16 hi/lo pairs (about 22 significant bits,
+ * |x| < 65504), two f16 products per multiply, fp32 accumulation.  Biases and Snake
+ * parameters stay fp32.  VOC_PREC_F16W runs neither fused residual units nor CTA pairs. */
+enum { VOC_PREC_BF16X3 = 0, VOC_PREC_F16W = 1 };
 /* activation: Snake with alpha as stored, or SnakeBeta with log-scale alpha and beta,
  * x + sin^2(e^alpha x) / (e^beta + 1e-9) (qwentts.cpp Architecture, "Audio tokenizer
  * decoder": exp applied to both stored parameters) */
@@ -93,7 +100,7 @@ typedef struct {
   int out_kernel;       /* conv_out taps (odd; 7)                            */
   int out_channels;     /* 1                                                 */
   int padding;          /* VOC_PAD_SYMMETRIC | VOC_PAD_CAUSAL                */
-  int precision;        /* VOC_PREC_BF16X3                                   */
+  int precision;        /* VOC_PREC_BF16X3 | VOC_PREC_F16W                   */
   int fuse_max_channels;/* residual units of up to this many channels run as one
                            kernel (conv1 result kept on chip); 0 = library default
                            (never), -1 = never.  A performance choice only: results agree

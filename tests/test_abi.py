@@ -121,3 +121,17 @@ def test_create_validates_before_device_work(lib):
         V.vocoder_create(W.TINY, [None] * (n - 1))
     assert e.value.status == V.VOC_INVALID_ARG
     assert "n_params" in V.vocoder_last_error()
+
+
+def test_precision_field_validation(lib):
+    """VOC_PREC_F16W is a valid precision (same parameter list); unknown precisions and the
+    F16-weight precision with CTA pairs are rejected before any device work."""
+    n = V.vocoder_param_count(W.TINY)
+    d = V.make_desc(W.TINY, precision=V.VOC_PREC_F16W)
+    assert lib.vocoder_param_count(ctypes.byref(d)) == n
+    d = V.make_desc(W.TINY, precision=2)
+    assert lib.vocoder_param_count(ctypes.byref(d)) == -1
+    with pytest.raises(V.VocoderError) as e:
+        V.vocoder_create(W.TINY, [None] * n, cta_pair=1, precision=V.VOC_PREC_F16W)
+    assert e.value.status == V.VOC_INVALID_ARG
+    assert "cta_pair" in V.vocoder_last_error()
