@@ -237,7 +237,9 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     peaks, peaks_kind = load_peaks()
     wl = W.make_workload(args.workload)
-    voc = V.Vocoder(wl.arch, V.fold_params(wl.params))
+    f16w = args.precision == "f16w"
+    voc = V.Vocoder(wl.arch, V.fold_params(wl.params),
+                    precision=V.VOC_PREC_F16W if f16w else V.VOC_PREC_BF16X3)
     B, T, hop = wl.B, wl.T, wl.arch.hop
     stream = torch.cuda.Stream(device=dev)
     lat = torch.from_numpy(wl.latent).to(dev)
@@ -299,7 +301,10 @@ def run_ours(args, rank, world, local_rank):
 
     # per-kernel roofline: bf16x3 issues three bf16 MMAs per useful multiply-add
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    tc_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) / 3.0
+    # bf16x3 issues three bf16 MMAs per useful multiply-add, f16w two f16 MMAs (f16 and bf16
+    # share the dense tensor rate)
+    mmas_per_mac = 2.0 if f16w else 3.0
+    tc_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) / mmas_per_mac
     ridge = tc_peak * 1e12 / (hbm * 1e9)
     stages = []
     for i in sorted(per_kernel):
@@ -321,7 +326,9 @@ def run_ours(args, rank, world, local_rank):
                 "traffic": traffic,
                 "per_launch": {"flops": dom_rec["flops"], "bytes": dom_rec["bytes"],
                                "avg_ms": dom["ms"]},
-                "peak_note": f"bf16 dense {peaks_kind} burst / 3 (three bf16 MMAs per useful MAC)"}
+                "peak_note": (f"bf16 dense {peaks_kind} burst / 2 (two f16 MMAs per useful MAC)"
+                              if f16w else
+                              f"bf16 dense {peaks_kind} burst / 3 (three bf16 MMAs per useful MAC)")}
     else:
         roof = {"bound": "hbm", "kernel": dom["name"], "achieved": dom["gbs"], "peak": hbm,
                 "unit": "GB/s", "frac": dom["frac"], "traffic": traffic,
@@ -336,9 +343,10 @@ def run_ours(args, rank, world, local_rank):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "bf16x3 (hi/lo split, fp32 accumulate)", "data": "synthetic",
+                "dtype": ("f16w (f16 weights, f16 hi/lo activations, fp32 accumulate)" if f16w
+                          else "bf16x3 (hi/lo split, fp32 accumulate)"), "data": "synthetic",
                 "x_realtime": tracks * T * hop / rate / (ms_max / 1e3),
-                "config": config_of(wl, args.workload),
+                "config": dict(config_of(wl, args.workload), precision=args.precision),
                 "e2e": {"value": total_samples / e2e_t, "unit": UNIT,
                         "h2d_bytes_per_step": int(wl.latent.nbytes),
                         "d2h_bytes_per_step": int(B * T * hop * 4),
@@ -366,6 +374,9 @@ def main():
     ap.add_argument("--ref-frames", type=int, default=48,
                     help="latent frames of one item per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--precision", choices=["bf16x3", "f16w"], default="bf16x3",
+                    help="bf16x3 (default): full fp32-equivalent inputs; f16w: the pages' F16 "
+                         "conv weights")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
