@@ -99,6 +99,60 @@ class Arch:
         return out
 
 
+@dataclasses.dataclass(frozen=True)
+class EncArch:
+    """Layer shapes of the mirror encoder (minimaxmusic.cpp Architecture, "Flow VAE": per
+    side, conv_in, blocks of residual units followed by Snake and a strided conv k = 2s,
+    Snake, conv_out k3 and the posterior mean projection k1)."""
+
+    in_channels: int
+    channels0: int
+    strides: Tuple[int, ...]
+    widths: Tuple[int, ...]  # output channels of each block's strided conv
+    latent_channels: int
+    dilations: Tuple[int, ...] = (1, 3, 9)
+    in_kernel: int = 7
+    res_kernel: int = 7
+    out_kernel: int = 3
+    snake_beta: bool = False
+
+    @property
+    def hop(self) -> int:
+        return int(np.prod(self.strides))
+
+    def block_channels(self) -> List[Tuple[int, int]]:
+        """(C_in, C_out) of every downsampling block."""
+        cins = [self.channels0] + list(self.widths[:-1])
+        return list(zip(cins, self.widths))
+
+    def param_shapes(self) -> List[Tuple[str, Tuple[int, ...]]]:
+        """Canonical order and PyTorch layouts (conv weights [C_out, C_in, K])."""
+        def sn(c):
+            return (2, c) if self.snake_beta else (c,)
+
+        out: List[Tuple[str, Tuple[int, ...]]] = []
+        out.append(("conv_in.w", (self.channels0, self.in_channels, self.in_kernel)))
+        out.append(("conv_in.b", (self.channels0,)))
+        for i, ((cin, cout), s) in enumerate(zip(self.block_channels(), self.strides)):
+            for j, _d in enumerate(self.dilations):
+                out.append((f"block{i}.res{j}.snake1.alpha", sn(cin)))
+                out.append((f"block{i}.res{j}.conv1.w", (cin, cin, self.res_kernel)))
+                out.append((f"block{i}.res{j}.conv1.b", (cin,)))
+                out.append((f"block{i}.res{j}.snake2.alpha", sn(cin)))
+                out.append((f"block{i}.res{j}.conv2.w", (cin, cin, 1)))
+                out.append((f"block{i}.res{j}.conv2.b", (cin,)))
+            out.append((f"block{i}.snake.alpha", sn(cin)))
+            out.append((f"block{i}.down.w", (cout, cin, 2 * s)))
+            out.append((f"block{i}.down.b", (cout,)))
+        c_last = self.widths[-1]
+        out.append(("snake_out.alpha", sn(c_last)))
+        out.append(("conv_out.w", (c_last, c_last, self.out_kernel)))
+        out.append(("conv_out.b", (c_last,)))
+        out.append(("proj.w", (self.latent_channels, c_last, 1)))
+        out.append(("proj.b", (self.latent_channels,)))
+        return out
+
+
 @dataclasses.dataclass
 class RawConv:
     """A convolution in weight-norm form: w = g * v / ||v|| along axis 0 of v."""
@@ -220,6 +274,8 @@ def gen_params(arch: Arch, recipe: str, seed_w: int, seed_a: int) -> list:
         elif ".convT." in name:
             stride = shape[2] // 2
             gain = math.sqrt(stride / 2.0)
+        elif ".down." in name or name.startswith("proj"):
+            gain = 1.0  # the norm runs over every input a strided or 1x1 output sees
         elif name.startswith("conv_out"):
             gain = 0.3
         else:
@@ -267,6 +323,22 @@ def make_custom(arch: Arch, B: int, T: int, seed: int, recipe: str = "calibrated
     rl = np.random.Generator(np.random.PCG64(seed))
     lat = rl.standard_normal((B, arch.latent_channels, T), dtype=np.float32)
     return Workload(name=f"custom{seed}", arch=arch, latent=lat, params=params)
+
+
+# the music model's encoder: 64 -> 128 -> 256 -> 512 -> 1024 over strides 2, 4, 8, 8 (x512)
+ENC_MUSIC = EncArch(in_channels=1, channels0=64, strides=(2, 4, 8, 8), widths=(128, 256, 512, 1024),
+                    latent_channels=64)
+
+
+def make_encode_workload(arch: EncArch, B: int, frames: int, seed: int,
+                         recipe: str = "calibrated") -> Workload:
+    """Audio [B, in_channels, frames * hop] in (-1, 1) (tanh of N(0, 0.5^2) samples) and the
+    encoder's raw parameters; the audio is stored in the workload's `latent` field."""
+    params = gen_params(arch, recipe, seed + 1, seed + 2)
+    rl = np.random.Generator(np.random.PCG64(seed))
+    audio = np.tanh(rl.standard_normal((B, arch.in_channels, frames * arch.hop),
+                                       dtype=np.float32) * np.float32(0.5)).astype(np.float32)
+    return Workload(name=f"encode{seed}", arch=arch, latent=audio, params=params)
 
 
 def slice_latent(latent: np.ndarray, t0: int, t1: int) -> np.ndarray:

@@ -257,6 +257,104 @@ int oracle_decode(const oracle_arch *a, const double *const *params, const float
 /* minimaxmusic.cpp Architecture, "Decode and stitch": the first window keeps
  * its left edge, later windows crop crop_left latents on the left, all but the
  * last crop crop_right on the right; segments are concatenated and clamped. */
+/* ------------------------------------------------------------------ mirror encoder */
+int oracle_enc_param_count(const oracle_enc_arch *a) {
+  return 2 + a->n_stages * (6 * a->n_dilations + 3) + 3 + 2;
+}
+
+/* Conv1d with a stride: the definition, zero outside [0, T). */
+int oracle_conv1d_strided(const double *x, int Cin, int T, const double *w, const double *b,
+                          int Cout, int K, int stride, int pad_left, int T_out, double *y) {
+  if (T_out < 0 || Cin <= 0 || Cout <= 0 || K <= 0 || stride <= 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int co = 0; co < Cout; ++co) {
+    double *yr = y + (long)co * T_out;
+    for (long t = 0; t < T_out; ++t) yr[t] = b ? b[co] : 0.0;
+    for (int ci = 0; ci < Cin; ++ci) {
+      const double *xr = x + (long)ci * T;
+      const double *wr = w + ((long)co * Cin + ci) * K;
+      for (int k = 0; k < K; ++k) {
+        const double wk = wr[k];
+        for (long t = 0; t < T_out; ++t) {
+          const long j = t * stride + k - pad_left;
+          if (j >= 0 && j < T) yr[t] += wk * xr[j];
+        }
+      }
+    }
+  }
+  return 0;
+}
+
+/* minimaxmusic.cpp Architecture, "Flow VAE" (the encoder, the decoder's mirror). */
+int oracle_encode(const oracle_enc_arch *a, const double *const *params, const float *audio,
+                  int B, long L, double *latent) {
+  if (!a || !params || !audio || !latent || B <= 0 || L <= 0) return -1;
+  long hop = 1;
+  for (int i = 0; i < a->n_stages; ++i) hop *= a->strides[i];
+  if (L % hop) return -1;
+  const int ident = (a->flags & ORACLE_FLAG_SNAKE_IDENTITY) != 0;
+  long max_elems = (long)a->in_channels * L;
+  {
+    long Lc = L;
+    int C = a->channels0;
+    if ((long)C * Lc > max_elems) max_elems = (long)C * Lc;
+    for (int i = 0; i < a->n_stages; ++i) {
+      Lc /= a->strides[i];
+      C = a->widths[i];
+      if ((long)C * Lc > max_elems) max_elems = (long)C * Lc;
+    }
+  }
+  double *x = (double *)malloc((size_t)max_elems * sizeof(double));
+  double *s = (double *)malloc((size_t)max_elems * sizeof(double));
+  double *h = (double *)malloc((size_t)max_elems * sizeof(double));
+  if (!x || !s || !h) {
+    free(x), free(s), free(h);
+    return -2;
+  }
+  const long L_lat = L / hop;
+  for (int bi = 0; bi < B; ++bi) {
+    int p = 0;
+    const float *au = audio + (long)bi * a->in_channels * L;
+    for (long i = 0; i < (long)a->in_channels * L; ++i) s[i] = (double)au[i];
+    int pl, pr;
+    conv_pads(ORACLE_PAD_SYMMETRIC, a->in_kernel, 1, &pl, &pr);
+    oracle_conv1d(s, a->in_channels, (int)L, params[p], params[p + 1], a->channels0, a->in_kernel, 1,
+                  pl, pr, x);
+    p += 2;
+    int C = a->channels0;
+    long Lc = L;
+    for (int st = 0; st < a->n_stages; ++st) {
+      for (int r = 0; r < a->n_dilations; ++r) { /* residual units, as in the decoder */
+        const int d = a->dilations[r];
+        snake_rows(x, C, Lc, params[p], ident, a->snake_beta, s);
+        conv_pads(ORACLE_PAD_SYMMETRIC, a->res_kernel, d, &pl, &pr);
+        oracle_conv1d(s, C, (int)Lc, params[p + 1], params[p + 2], C, a->res_kernel, d, pl, pr, h);
+        snake_rows(h, C, Lc, params[p + 3], ident, a->snake_beta, s);
+        oracle_conv1d(s, C, (int)Lc, params[p + 4], params[p + 5], C, 1, 1, 0, 0, h);
+        for (long i = 0; i < (long)C * Lc; ++i) x[i] += h[i];
+        p += 6;
+      }
+      /* snake -> strided conv, k = 2s, pad s/2 */
+      const int sd = a->strides[st];
+      const int Co = a->widths[st];
+      snake_rows(x, C, Lc, params[p], ident, a->snake_beta, s);
+      oracle_conv1d_strided(s, C, (int)Lc, params[p + 1], params[p + 2], Co, 2 * sd, sd, sd / 2,
+                            (int)(Lc / sd), x);
+      p += 3;
+      C = Co;
+      Lc /= sd;
+    }
+    /* snake_out -> conv_out -> posterior mean projection */
+    snake_rows(x, C, Lc, params[p], ident, a->snake_beta, s);
+    conv_pads(ORACLE_PAD_SYMMETRIC, a->out_kernel, 1, &pl, &pr);
+    oracle_conv1d(s, C, (int)Lc, params[p + 1], params[p + 2], C, a->out_kernel, 1, pl, pr, h);
+    oracle_conv1d(h, C, (int)Lc, params[p + 3], params[p + 4], a->latent_channels, 1, 1, 0, 0,
+                  latent + (long)bi * a->latent_channels * L_lat);
+  }
+  free(x), free(s), free(h);
+  return 0;
+}
+
 long oracle_stitched_length(int n_win, int win_frames, int crop_left, int crop_right, int hop) {
   if (n_win <= 0 || win_frames <= 0 || hop <= 0 || crop_left < 0 || crop_right < 0) return -1;
   long frames = 0;

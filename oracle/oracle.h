@@ -131,10 +131,6 @@ long oracle_stitched_length(int n_win, int win_frames, int crop_left, int crop_r
 int oracle_stitch(const double *decoded, int n_win, int n_sides, int win_frames, int crop_left,
                   int crop_right, int hop, double *out);
 
-#ifdef __cplusplus
-}
-#endif
-#endif
 
 /* ------------------------------------------------------------------ output stage
  * minimaxmusic.cpp Architecture, "Post-processing": planar float output, then percentile
@@ -159,3 +155,53 @@ long oracle_wav_bytes(int n_ch, long len, int bits);
  * Returns 0, or -1 for bad arguments. */
 int oracle_encode_wav(const float *planar, int n_ch, long len, int sample_rate, int bits,
                       int peak_clip, unsigned char *out);
+
+/* ------------------------------------------------------------------ mirror encoder
+ * minimaxmusic.cpp Architecture, "Flow VAE": the encoder is the decoder's mirror, per side
+ *   conv_in k7 (1 -> C0)
+ *   for every block (stride s, C_in -> C_out): 3 residual units at C_in (dilations 1, 3, 9),
+ *       then Snake and a strided conv (k = 2s, stride s, pad s/2, C_in -> C_out),
+ *   Snake -> conv_out (k3, C_last -> C_last) -> posterior mean projection (k1, C_last -> Cl).
+ * Readings: the widths double block by block (64 -> 128 -> 256 -> 512 -> 1024 for the music
+ * model); conv_out pads 1 on each side; no Snake between conv_out and the projection; all
+ * convs have a bias; the same Snake as the decoder. */
+typedef struct {
+  int in_channels;     /* 1 (one side of a stereo track)                         */
+  int channels0;       /* C0, conv_in output channels                             */
+  int in_kernel;       /* conv_in taps (7)                                        */
+  int n_stages;        /* downsampling blocks                                     */
+  const int *strides;  /* [n_stages] (2, 4, 8, 8)                                 */
+  const int *widths;   /* [n_stages] output channels of each block's strided conv */
+  int n_dilations;     /* residual units per block (3)                            */
+  const int *dilations;/* [n_dilations] (1, 3, 9)                                 */
+  int res_kernel;      /* dilated conv taps (7)                                   */
+  int out_kernel;      /* conv_out taps (3)                                       */
+  int latent_channels; /* Cl, projection output channels (64)                     */
+  int flags;           /* ORACLE_FLAG_SNAKE_IDENTITY honoured                     */
+  int snake_beta;      /* as oracle_arch                                          */
+} oracle_enc_arch;
+
+/* Parameter tensors, canonical order:
+ *   conv_in.w [C0][Cin][Kin], conv_in.b [C0],
+ *   per block i (C = C_in of the block, C' = widths[i], stride s):
+ *     per dilation: snake1.alpha [C], conv1.w [C][C][Kres], conv1.b [C], snake2.alpha [C],
+ *                   conv2.w [C][C][1], conv2.b [C],
+ *     snake.alpha [C], down.w [C'][C][2s], down.b [C'],
+ *   snake_out.alpha [C_last], conv_out.w [C_last][C_last][Kout], conv_out.b [C_last],
+ *   proj.w [Cl][C_last][1], proj.b [Cl]. */
+int oracle_enc_param_count(const oracle_enc_arch *a);
+
+/* y[co][t] = b[co] + sum_ci sum_k w[co][ci][k] * x[ci][t*stride + k - pad_left], x zero
+ * outside [0, T), for t in [0, T_out).  b may be NULL. */
+int oracle_conv1d_strided(const double *x, int Cin, int T, const double *w, const double *b,
+                          int Cout, int K, int stride, int pad_left, int T_out, double *y);
+
+/* Full encode: audio [B][Cin][L] fp32 (L a multiple of the product of the strides) ->
+ * latent [B][Cl][L / prod(strides)] double.  0 on success. */
+int oracle_encode(const oracle_enc_arch *a, const double *const *params, const float *audio,
+                  int B, long L, double *latent);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

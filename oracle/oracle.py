@@ -69,6 +69,15 @@ def _load():
             lib.oracle_stitch.argtypes = [D, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, D]
             lib.oracle_stitch.restype = ctypes.c_int
+            lib.oracle_enc_param_count.argtypes = [ctypes.c_void_p]
+            lib.oracle_enc_param_count.restype = ctypes.c_int
+            lib.oracle_conv1d_strided.argtypes = [D, ctypes.c_int, ctypes.c_int, D, D, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, D]
+            lib.oracle_conv1d_strided.restype = ctypes.c_int
+            lib.oracle_encode.argtypes = [ctypes.c_void_p, ctypes.POINTER(D), F, ctypes.c_int,
+                                          ctypes.c_long, D]
+            lib.oracle_encode.restype = ctypes.c_int
             lib.oracle_param_count.argtypes = [ctypes.c_void_p]
             lib.oracle_param_count.restype = ctypes.c_int
             lib.oracle_abs_percentile.argtypes = [F, ctypes.c_long, ctypes.c_int]
@@ -99,6 +108,16 @@ class _ArchC(ctypes.Structure):
                 ("res_kernel", ctypes.c_int), ("out_kernel", ctypes.c_int),
                 ("padding", ctypes.c_int), ("flags", ctypes.c_int),
                 ("in_proj_channels", ctypes.c_int), ("snake_beta", ctypes.c_int)]
+
+
+class _EncArchC(ctypes.Structure):
+    _fields_ = [("in_channels", ctypes.c_int), ("channels0", ctypes.c_int),
+                ("in_kernel", ctypes.c_int), ("n_stages", ctypes.c_int),
+                ("strides", ctypes.POINTER(ctypes.c_int)), ("widths", ctypes.POINTER(ctypes.c_int)),
+                ("n_dilations", ctypes.c_int), ("dilations", ctypes.POINTER(ctypes.c_int)),
+                ("res_kernel", ctypes.c_int), ("out_kernel", ctypes.c_int),
+                ("latent_channels", ctypes.c_int), ("flags", ctypes.c_int),
+                ("snake_beta", ctypes.c_int)]
 
 
 def fold_weight_norm(g: np.ndarray, v: np.ndarray) -> np.ndarray:
@@ -224,6 +243,50 @@ def decode(arch, params: Sequence, latent: np.ndarray, flags: int = 0, folded: O
     if rc != 0:
         raise RuntimeError(f"oracle_decode failed ({rc})")
     return (audio, pre) if return_pre_tanh else audio
+
+
+def conv1d_strided(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray], stride: int,
+                   pad_left: int, T_out: int) -> np.ndarray:
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    Cin, T = x.shape
+    Cout, Cin2, K = w.shape
+    assert Cin2 == Cin
+    y = np.empty((Cout, T_out), dtype=np.float64)
+    bb = None if b is None else np.ascontiguousarray(b, dtype=np.float64)
+    rc = lib.oracle_conv1d_strided(_d(x), Cin, T, _d(w), None if bb is None else _d(bb), Cout, K,
+                                   stride, pad_left, T_out, _d(y))
+    assert rc == 0
+    return y
+
+
+def encode(arch, params: Sequence, audio: np.ndarray, flags: int = 0,
+           folded: Optional[list] = None) -> np.ndarray:
+    """Mirror encoder: audio [B, Cin, L] -> latent [B, Cl, L / hop] (double)."""
+    lib = _load()
+    if folded is None:
+        folded = fold_params(params)
+    audio = np.ascontiguousarray(audio, dtype=np.float32)
+    B, Ci, L = audio.shape
+    assert Ci == arch.in_channels
+    strides = (ctypes.c_int * len(arch.strides))(*arch.strides)
+    widths = (ctypes.c_int * len(arch.widths))(*arch.widths)
+    dils = (ctypes.c_int * len(arch.dilations))(*arch.dilations)
+    a = _EncArchC(arch.in_channels, arch.channels0, arch.in_kernel, len(arch.strides), strides,
+                  widths, len(arch.dilations), dils, arch.res_kernel, arch.out_kernel,
+                  arch.latent_channels, flags, int(arch.snake_beta))
+    n = lib.oracle_enc_param_count(ctypes.byref(a))
+    assert n == len(folded), (n, len(folded))
+    ptrs = (ctypes.POINTER(ctypes.c_double) * n)()
+    for i, t in enumerate(folded):
+        ptrs[i] = ctypes.cast(None, ctypes.POINTER(ctypes.c_double)) if t is None else _d(t)
+    hop = int(np.prod(arch.strides))
+    out = np.empty((B, arch.latent_channels, L // hop), dtype=np.float64)
+    rc = lib.oracle_encode(ctypes.byref(a), ptrs, _f(audio), B, L, _d(out))
+    if rc != 0:
+        raise RuntimeError(f"oracle_encode failed ({rc})")
+    return out
 
 
 def stitched_length(n_win, win_frames, crop_left, crop_right, hop) -> int:
