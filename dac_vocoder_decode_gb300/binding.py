@@ -51,6 +51,10 @@ EXPORTED = [
     "vocoder_stream_create", "vocoder_stream_decode", "vocoder_stream_reset",
     "vocoder_stream_destroy", "vocoder_wav_bytes", "vocoder_wav_scratch_bytes",
     "vocoder_encode_wav",
+    "vocoder_encoder_param_count", "vocoder_encoder_param_shape", "vocoder_encoder_create",
+    "vocoder_encoder_hop", "vocoder_encoder_workspace_bytes", "vocoder_encode",
+    "vocoder_encoder_launches", "vocoder_encoder_profile_count", "vocoder_encoder_profile_entry",
+    "vocoder_encoder_last_error", "vocoder_encoder_destroy",
 ]
 
 
@@ -70,6 +74,16 @@ class VocDesc(ctypes.Structure):
                 ("padding", ctypes.c_int), ("precision", ctypes.c_int),
                 ("fuse_max_channels", ctypes.c_int), ("cta_pair", ctypes.c_int),
                 ("in_proj_channels", ctypes.c_int), ("snake", ctypes.c_int)]
+
+
+class VocEncDesc(ctypes.Structure):
+    _fields_ = [("abi_version", ctypes.c_int), ("in_channels", ctypes.c_int),
+                ("channels0", ctypes.c_int), ("in_kernel", ctypes.c_int),
+                ("n_stages", ctypes.c_int), ("strides", ctypes.POINTER(ctypes.c_int)),
+                ("widths", ctypes.POINTER(ctypes.c_int)), ("n_dilations", ctypes.c_int),
+                ("dilations", ctypes.POINTER(ctypes.c_int)), ("res_kernel", ctypes.c_int),
+                ("out_kernel", ctypes.c_int), ("latent_channels", ctypes.c_int),
+                ("precision", ctypes.c_int), ("snake", ctypes.c_int)]
 
 
 _lib = None
@@ -154,6 +168,33 @@ def load_library():
     lib.vocoder_stream_reset.argtypes = [P, P]
     lib.vocoder_stream_destroy.restype = None
     lib.vocoder_stream_destroy.argtypes = [P]
+    ED = ctypes.POINTER(VocEncDesc)
+    lib.vocoder_encoder_param_count.restype = I
+    lib.vocoder_encoder_param_count.argtypes = [ED]
+    lib.vocoder_encoder_param_shape.restype = I
+    lib.vocoder_encoder_param_shape.argtypes = [ED, I, ctypes.POINTER(I), ctypes.POINTER(I)]
+    lib.vocoder_encoder_create.restype = I
+    lib.vocoder_encoder_create.argtypes = [ED, ctypes.POINTER(F), I, ctypes.POINTER(P)]
+    lib.vocoder_encoder_hop.restype = ctypes.c_longlong
+    lib.vocoder_encoder_hop.argtypes = [P]
+    lib.vocoder_encoder_workspace_bytes.restype = ctypes.c_size_t
+    lib.vocoder_encoder_workspace_bytes.argtypes = [P, I, ctypes.c_longlong]
+    lib.vocoder_encode.restype = I
+    lib.vocoder_encode.argtypes = [P, P, I, ctypes.c_longlong, P, P, ctypes.c_size_t, P,
+                                   ctypes.c_uint]
+    lib.vocoder_encoder_launches.restype = I
+    lib.vocoder_encoder_launches.argtypes = [P]
+    lib.vocoder_encoder_profile_count.restype = I
+    lib.vocoder_encoder_profile_count.argtypes = [P]
+    lib.vocoder_encoder_profile_entry.restype = I
+    lib.vocoder_encoder_profile_entry.argtypes = [P, I, ctypes.POINTER(ctypes.c_char_p),
+                                                  ctypes.POINTER(ctypes.c_double),
+                                                  ctypes.POINTER(ctypes.c_double),
+                                                  ctypes.POINTER(ctypes.c_double)]
+    lib.vocoder_encoder_last_error.restype = ctypes.c_char_p
+    lib.vocoder_encoder_last_error.argtypes = [P]
+    lib.vocoder_encoder_destroy.restype = None
+    lib.vocoder_encoder_destroy.argtypes = [P]
     _lib = lib
     return lib
 
@@ -504,3 +545,127 @@ class Vocoder:
             audio = torch.empty((B, 1, T * self.hop), dtype=torch.float32, device=latent.device)
         vocoder_decode(self.handle, latent, audio, ws, stream, flags)
         return audio
+
+
+# ------------------------------------------------------------------ mirror encoder
+def _check_enc(status: int, handle=None):
+    if status != VOC_OK:
+        msg = load_library().vocoder_encoder_last_error(handle)
+        raise VocoderError(status, msg.decode() if msg else "")
+
+
+def make_enc_desc(arch, precision: int = VOC_PREC_BF16X3) -> VocEncDesc:
+    """voc_enc_desc for an encoder architecture (workloads.EncArch or the same fields)."""
+    strides = (ctypes.c_int * len(arch.strides))(*arch.strides)
+    widths = (ctypes.c_int * len(arch.widths))(*arch.widths)
+    dils = (ctypes.c_int * len(arch.dilations))(*arch.dilations)
+    d = VocEncDesc(VOC_ABI_VERSION, arch.in_channels, arch.channels0, arch.in_kernel,
+                   len(arch.strides), strides, widths, len(arch.dilations), dils,
+                   arch.res_kernel, arch.out_kernel, arch.latent_channels, precision,
+                   VOC_SNAKE_BETA if getattr(arch, "snake_beta", False) else VOC_SNAKE)
+    d._keep = (strides, widths, dils)
+    return d
+
+
+def vocoder_encoder_param_count(arch) -> int:
+    return load_library().vocoder_encoder_param_count(ctypes.byref(make_enc_desc(arch)))
+
+
+def vocoder_encoder_param_shape(arch, index: int):
+    dims = (ctypes.c_int * 3)()
+    nd = ctypes.c_int()
+    _check_enc(load_library().vocoder_encoder_param_shape(ctypes.byref(make_enc_desc(arch)), index,
+                                                          dims, ctypes.byref(nd)))
+    return tuple(dims[i] for i in range(nd.value))
+
+
+def vocoder_encoder_create(arch, params: Sequence[Optional[np.ndarray]],
+                           precision: int = VOC_PREC_BF16X3) -> ctypes.c_void_p:
+    """params: folded fp32 arrays in the encoder's canonical order (None for a zero bias)."""
+    keep = [None if p is None else np.ascontiguousarray(p, dtype=np.float32) for p in params]
+    arr = (ctypes.POINTER(ctypes.c_float) * len(keep))(*[_fptr(p) for p in keep])
+    h = ctypes.c_void_p()
+    _check_enc(load_library().vocoder_encoder_create(ctypes.byref(make_enc_desc(arch, precision)),
+                                                     arr, len(keep), ctypes.byref(h)))
+    return h
+
+
+def vocoder_encoder_destroy(h) -> None:
+    load_library().vocoder_encoder_destroy(h)
+
+
+def vocoder_encoder_hop(h) -> int:
+    return int(load_library().vocoder_encoder_hop(h))
+
+
+def vocoder_encoder_workspace_bytes(h, B: int, L: int) -> int:
+    return int(load_library().vocoder_encoder_workspace_bytes(h, B, L))
+
+
+def vocoder_encoder_launches(h) -> int:
+    return int(load_library().vocoder_encoder_launches(h))
+
+
+def vocoder_encode(h, audio, latent, ws, stream=None, flags: int = 0) -> None:
+    """audio [B, C_in, L] fp32 CUDA tensor -> latent [B, C_lat, L / hop] fp32 CUDA tensor."""
+    B, _, L = audio.shape
+    _check_enc(load_library().vocoder_encode(h, ctypes.c_void_p(audio.data_ptr()), B, L,
+                                             ctypes.c_void_p(latent.data_ptr()),
+                                             ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                             _stream_ptr(stream), flags), h)
+
+
+def vocoder_encoder_profile(h) -> List[dict]:
+    """Per-kernel records of the last encode run with VOC_FLAG_PROFILE."""
+    lib = load_library()
+    out = []
+    for i in range(lib.vocoder_encoder_profile_count(h)):
+        name = ctypes.c_char_p()
+        ms, fl, by = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+        _check_enc(lib.vocoder_encoder_profile_entry(h, i, ctypes.byref(name), ctypes.byref(ms),
+                                                     ctypes.byref(fl), ctypes.byref(by)), h)
+        out.append(dict(name=name.value.decode(), ms=ms.value, flops=fl.value, bytes=by.value))
+    return out
+
+
+def vocoder_encoder_last_error(h=None) -> str:
+    m = load_library().vocoder_encoder_last_error(h)
+    return m.decode() if m else ""
+
+
+class Encoder:
+    """The mirror encoder on the current CUDA device (owns its library context)."""
+
+    def __init__(self, arch, folded_params, precision: int = VOC_PREC_BF16X3):
+        self.arch = arch
+        self.handle = vocoder_encoder_create(arch, folded_params, precision)
+        self.hop = vocoder_encoder_hop(self.handle)
+
+    def close(self):
+        if self.handle:
+            vocoder_encoder_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace_bytes(self, B: int, L: int) -> int:
+        return vocoder_encoder_workspace_bytes(self.handle, B, L)
+
+    def alloc_workspace(self, B: int, L: int):
+        import torch
+        return torch.empty(self.workspace_bytes(B, L), dtype=torch.uint8, device="cuda")
+
+    def encode(self, audio, ws=None, latent=None, stream=None, flags: int = 0):
+        import torch
+        B, _, L = audio.shape
+        if ws is None:
+            ws = self.alloc_workspace(B, L)
+        if latent is None:
+            latent = torch.empty((B, self.arch.latent_channels, L // self.hop), dtype=torch.float32,
+                                 device=audio.device)
+        vocoder_encode(self.handle, audio.contiguous(), latent, ws, stream, flags)
+        return latent

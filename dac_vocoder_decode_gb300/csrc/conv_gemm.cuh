@@ -99,6 +99,8 @@ struct ConvGemmArgs {
                            // 16-column chunks (phase pairs); G odd, by whole blocks with lane
                            // pairs (see convT_block_odd).  0: phase-major columns
                            // (n = phase * Cp_out + channel).
+  int split_s;             // 1, or S > 1: the hi/lo output is phase-split for a strided conv of
+                           // stride S (row t -> row t / S of plane chunk * S + t % S)
   int b2;                  // 1 (the kernel's B2 form): each weight chunk holds its hi rows then its lo rows, and a K
                            // step is two MMAs: A_hi x [W_hi | W_lo] into 2 N_tile accumulator
                            // columns, then A_lo x W_hi into the first N_tile; the epilogue adds
@@ -461,6 +463,26 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
 #pragma unroll
     for (int i = 0; i < CW / 2; ++i) split_pair<F16>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
     const size_t L_out = static_cast<size_t>(p.hl_L);
+    if (p.split_s > 1) {
+      // Phase-split output for a strided conv of stride ss: row t goes to row t / ss of the
+      // plane (chunk * ss + t % ss), so that the strided conv reads its input as a 3-tap conv
+      // over ss * Cp_out channels (see the encoder in vocoder.cu).
+      const size_t ss = static_cast<size_t>(p.split_s);
+      const size_t ph = row_t % ss, row = row_t / ss + p.hl_row0;
+      const size_t half = ss * (p.Cp_out / 8);  // planes of the hi (and of the lo) parts
+      const size_t item = (size_t)b * 2 * half;
+      VOC_CHECK((((long long)(item + half + (co0 / 8 + CW / 8 - 1) * ss + ph)) * (long long)L_out + row) * 8 + 8 <=
+                    p.hl_elems, 20, b, co0, row);
+#pragma unroll
+      for (int j = 0; j < CW / 8; ++j) {
+        const size_t plane = (co0 / 8 + j) * ss + ph;
+        *reinterpret_cast<uint4 *>(p.out_hl + ((item + plane) * L_out + row) * 8) =
+            make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
+        *reinterpret_cast<uint4 *>(p.out_hl + ((item + half + plane) * L_out + row) * 8) =
+            make_uint4(lw[4 * j], lw[4 * j + 1], lw[4 * j + 2], lw[4 * j + 3]);
+      }
+      return true;
+    }
     const size_t row = row_t + p.hl_row0;
     const size_t item = (size_t)b * (2 * p.Cp_out / 8);
     VOC_CHECK((((long long)item + p.Cp_out / 8 + co0 / 8 + CW / 8 - 1) * (long long)L_out + row) * 8 + 8 <= p.hl_elems,

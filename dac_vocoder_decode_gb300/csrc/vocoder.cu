@@ -85,6 +85,9 @@ struct Layer {
   std::string name;
   bool convT = false;
   bool f16 = false;         // F16-weight precision: one f16 weight plane, f16 hi/lo operands
+  // strided conv of the encoder (stride down_s, k = 2 down_s, pad down_s / 2, down_c real
+  // input channels), run as a 3-tap conv over the phase-split input: Cin = down_s * Cp(down_c)
+  int down_s = 0, down_c = 0;
   int Cin = 0, Cout = 0, Cp_in = 0, Cp_out = 0, K = 0, dil = 1, stride = 1;
   int level = 0;            // input rate: L_in = T * prod(strides[0..level-1])
   ConvGemmArgs g{};         // geometry; sizes and pointers filled per launch
@@ -473,6 +476,17 @@ void convT_column(const Layer &L, int padding, int n, int &r, int &co) {
 
 float weight_value(const Layer &L, int padding, const float *w, int n, int ci, int tap) {
   if (ci >= L.Cin) return 0.f;
+  if (L.down_s) {
+    // input channel ci = (chunk * s + r) * 8 + e holds channel chunk * 8 + e at phase r (row
+    // u s + r of the strided conv's input); tap du - 1 in {-1, 0, 1} reads row u + du, i.e.
+    // original tap k = du s + r + s / 2 of the k = 2s kernel
+    const int sd = L.down_s;
+    const int chunk = ci / (8 * sd), r = (ci / 8) % sd, e = ci % 8;
+    const int c = chunk * 8 + e;
+    const int k = (tap - 1) * sd + r + sd / 2;
+    if (n >= L.Cout || c >= L.down_c || k < 0 || k >= 2 * sd) return 0.f;
+    return w[((size_t)n * L.down_c + c) * (2 * sd) + k];
+  }
   if (!L.convT) {
     if (n >= L.Cout) return 0.f;
     return w[((size_t)n * L.Cin + ci) * L.K + tap];
@@ -733,10 +747,10 @@ void set_in_row0(const Layer &L, ConvGemmArgs &a, int in_row0) {
   a.shift0_q1 = L.g.shift0_q1 + extra;
 }
 
-void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *const *bufs,
-                      size_t bbytes, ConvGemmArgs &a) {
+// Launch arguments of a layer whose GEMM has L_in rows per item.
+void gemm_args_rows(const vocoder *ctx, const Layer &L, int B, long long L_in, void *const *bufs,
+                    size_t bbytes, ConvGemmArgs &a) {
   a = L.g;
-  const long long L_in = level_len(ctx, L.level, T);
   a.B = B;
   a.L_in = static_cast<int>(L_in);
   const int kM = L.pair ? 2 * voc::kTileM : voc::kTileM;  // rows of one tile job
@@ -764,6 +778,11 @@ void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *co
   a.chunks_a = 2 * L.Cp_in / 8;
   a.chunks_s = L.Cp_out / 4;
   a.dbg = ctx->err_dev + 4;
+}
+
+void gemm_launch_args(const vocoder *ctx, const Layer &L, int B, int T, void *const *bufs,
+                      size_t bbytes, ConvGemmArgs &a) {
+  gemm_args_rows(ctx, L, B, level_len(ctx, L.level, T), bufs, bbytes, a);
 }
 
 #ifdef VOC_CHECKS
@@ -2040,4 +2059,488 @@ VOC_API voc_status vocoder_encode_wav(const float *planar_dev, int n_ch, long lo
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "launch output stage");
   return VOC_OK;
+}
+
+// =================================================================== mirror encoder
+// minimaxmusic.cpp Architecture, "Flow VAE": conv_in, blocks of residual units each followed
+// by Snake and a strided conv (k = 2s, stride s, pad s/2), Snake, conv_out and the posterior
+// mean projection, all non-causal, on the decoder's conv kernel.  A strided conv runs as a
+// 3-tap stride-1 conv over its input split into s phases: output row u reads input rows
+// u s + k - s/2 for k < 2s, i.e. rows u + du of phase r for du in {-1, 0, 1}; the residual
+// unit before it writes its hi/lo output in that phase-split layout, so the conv reads
+// s * Cp(C) channels of L / s rows through the ordinary tensor maps.
+struct vocoder_encoder {
+  vocoder core;  // device, error words, precision, allocations, profile records
+  voc_enc_desc desc{};
+  std::vector<int> strides, widths, dils;
+  long long hop = 1;
+  int Cp_audio = 0, Cp_lat = 0;
+  std::vector<Layer> layers;
+  std::vector<long long> div;  // per layer: GEMM rows per item = L / div
+  std::vector<int> split;      // per layer: 0, or the stride s of its phase-split hi/lo output
+  // TMA descriptors for the last (workspace, B, L)
+  void *map_ws = nullptr;
+  int map_B = -1;
+  long long map_L = -1;
+  std::vector<CUtensorMap> maps, skip_maps;
+};
+
+namespace {
+
+long long rup_ll(long long x, long long m) { return (x + m - 1) / m * m; }
+
+// Device of the current thread: sm_103 check, SM count, the kernels' error words.
+voc_status init_device(vocoder *ctx) {
+  cudaError_t e = cudaGetDevice(&ctx->device);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDevice");
+  e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaDeviceGetAttribute");
+  int cc_major = 0, cc_minor = 0;
+  cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, ctx->device);
+  cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
+  if (cc_major != 10 || cc_minor != 3)
+    return fail(ctx, VOC_UNSUPPORTED, "this build targets sm_103 (GB300) only");
+  e = cudaMalloc(&ctx->err_dev, 8 * sizeof(int));  // [0] error word, [1] finite flag, [4..7] checks
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMalloc");
+  ctx->allocs.push_back(ctx->err_dev);
+  ctx->flag_dev = ctx->err_dev + 1;
+  e = cudaMemset(ctx->err_dev, 0, 8 * sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemset");
+  return VOC_OK;
+}
+
+bool check_enc_desc(const voc_enc_desc *d, std::string &why) {
+  if (!d) return why = "desc is NULL", false;
+  if (d->abi_version != VOC_ABI_VERSION)
+    return why = "abi_version " + std::to_string(d->abi_version) + " != " +
+                 std::to_string(VOC_ABI_VERSION),
+           false;
+  if (d->in_channels < 1 || d->in_channels > 16) return why = "in_channels must be in [1, 16]", false;
+  if (d->channels0 < 1 || d->channels0 > 8192) return why = "channels0", false;
+  if (d->latent_channels < 1 || d->latent_channels > 8192) return why = "latent_channels", false;
+  for (int k : {d->in_kernel, d->res_kernel, d->out_kernel})
+    if (k < 1 || k > 15 || k % 2 == 0) return why = "kernel sizes must be odd in [1, 15]", false;
+  if (d->n_stages < 1 || d->n_stages > 8) return why = "n_stages", false;
+  if (!d->strides || !d->widths) return why = "strides / widths NULL", false;
+  if (d->n_dilations < 1 || d->n_dilations > 4 || !d->dilations) return why = "dilations", false;
+  if (d->precision != VOC_PREC_BF16X3 && d->precision != VOC_PREC_F16W) return why = "precision", false;
+  if (d->snake != VOC_SNAKE && d->snake != VOC_SNAKE_BETA) return why = "snake", false;
+  for (int i = 0; i < d->n_stages; ++i) {
+    if (d->strides[i] < 1 || d->strides[i] > 16) return why = "stride out of [1, 16]", false;
+    if (d->widths[i] < 1 || d->widths[i] > 8192) return why = "width out of range", false;
+  }
+  for (int j = 0; j < d->n_dilations; ++j)
+    if (d->dilations[j] < 1 || d->dilations[j] * (d->res_kernel - 1) > 120)
+      return why = "dilation * (res_kernel - 1) must be in [1, 120]", false;
+  return true;
+}
+
+int enc_param_count(const voc_enc_desc *d) {
+  return 2 + d->n_stages * (6 * d->n_dilations + 3) + 5;
+}
+
+// kind of every canonical encoder parameter: 'w' weight, 'b' bias, 'a' Snake parameters
+std::string enc_param_kinds(const voc_enc_desc *d) {
+  std::string k = "wb";
+  for (int i = 0; i < d->n_stages; ++i) {
+    for (int j = 0; j < d->n_dilations; ++j) k += "awbawb";
+    k += "awb";
+  }
+  return k + "awbwb";
+}
+
+// Largest hi/lo or fp32 plane set of one encode, in bytes: B items of max over the
+// levels of Cp(C) x rows (the phase-split outputs fill whole groups of 8 s rows).
+size_t enc_buf_bytes(const vocoder_encoder *enc, int B, long long L) {
+  long long Li = L;
+  int C = enc->desc.channels0;
+  size_t m = (size_t)pitch8(L) * (size_t)std::max(enc->Cp_audio, rup(C, 16));
+  for (int i = 0; i < enc->desc.n_stages; ++i) {
+    const int s = enc->strides[i];
+    m = std::max(m, (size_t)rup_ll(Li, 8LL * s) * (size_t)rup(C, 16));
+    Li /= s;
+    C = enc->widths[i];
+    m = std::max(m, (size_t)pitch8(Li) * (size_t)rup(C, 16));
+  }
+  m = std::max(m, (size_t)pitch8(Li) * (size_t)enc->Cp_lat);
+  return rupz(m * (size_t)B * 4, 256);
+}
+
+// Algorithmic cost of an encoder layer with L_in GEMM rows per item: a strided conv counts
+// its 2s taps over the C real channels, not the zero taps of its 3-tap form.
+void enc_layer_cost(const Layer &L, int B, long long L_in, double &flops, double &bytes) {
+  const double rows = (double)B * (double)L_in;
+  const double k = L.down_s ? 2.0 * L.down_s : (double)L.K;
+  const double cin = L.down_s ? (double)L.down_c : (double)L.Cin;
+  flops = 2.0 * cin * L.Cout * k * rows;
+  const ConvGemmArgs &g = L.g;
+  double by = 4.0 * rows * L.Cp_in + (double)g.n_tiles * g.taps * g.nkb * g.b_bytes;
+  const double out_elems = rows * L.Cp_out;
+  if (L.skip_buf >= 0) by += 4.0 * out_elems;
+  if (L.f32_buf >= 0) by += 4.0 * out_elems;
+  if (L.hl_buf >= 0) by += 4.0 * out_elems;
+  bytes = by;
+}
+
+}  // namespace
+
+VOC_API int vocoder_encoder_param_count(const voc_enc_desc *desc) {
+  std::string why;
+  if (!check_enc_desc(desc, why)) return -1;
+  return enc_param_count(desc);
+}
+
+VOC_API voc_status vocoder_encoder_param_shape(const voc_enc_desc *d, int index, int dims[3],
+                                               int *ndim) {
+  std::string why;
+  if (!check_enc_desc(d, why)) return fail(nullptr, VOC_INVALID_ARG, why);
+  if (!dims || !ndim) return fail(nullptr, VOC_INVALID_ARG, "dims / ndim NULL");
+  if (index < 0 || index >= enc_param_count(d)) return fail(nullptr, VOC_INVALID_ARG, "index out of range");
+  auto set = [&](int nd, int a, int b = 0, int c = 0) {
+    *ndim = nd;
+    dims[0] = a, dims[1] = b, dims[2] = c;
+    return VOC_OK;
+  };
+  auto snake = [&](int c) { return d->snake == VOC_SNAKE_BETA ? set(2, 2, c) : set(1, c); };
+  if (index == 0) return set(3, d->channels0, d->in_channels, d->in_kernel);
+  if (index == 1) return set(1, d->channels0);
+  int i = index - 2, C = d->channels0;
+  const int units = 6 * d->n_dilations;
+  for (int s = 0; s < d->n_stages; ++s) {
+    const int Co = d->widths[s];
+    if (i < units + 3) {
+      if (i < units) {
+        const int j = i % 6;
+        if (j == 0 || j == 3) return snake(C);
+        if (j == 1) return set(3, C, C, d->res_kernel);
+        if (j == 4) return set(3, C, C, 1);
+        return set(1, C);
+      }
+      if (i == units) return snake(C);
+      if (i == units + 1) return set(3, Co, C, 2 * d->strides[s]);
+      return set(1, Co);
+    }
+    i -= units + 3;
+    C = Co;
+  }
+  if (i == 0) return snake(C);
+  if (i == 1) return set(3, C, C, d->out_kernel);
+  if (i == 2) return set(1, C);
+  if (i == 3) return set(3, d->latent_channels, C, 1);
+  return set(1, d->latent_channels);
+}
+
+VOC_API void vocoder_encoder_destroy(vocoder_encoder *enc) {
+  if (!enc) return;
+  for (void *p : enc->core.allocs) cudaFree(p);
+  for (cudaEvent_t e : enc->core.events) cudaEventDestroy(e);
+  delete enc;
+}
+
+VOC_API voc_status vocoder_encoder_create(const voc_enc_desc *desc, const float *const *params,
+                                          int n_params, vocoder_encoder **out) {
+  if (!out) return fail(nullptr, VOC_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  std::string why;
+  if (!check_enc_desc(desc, why)) return fail(nullptr, VOC_INVALID_ARG, "desc: " + why);
+  if (!params) return fail(nullptr, VOC_INVALID_ARG, "params is NULL");
+  if (n_params != enc_param_count(desc))
+    return fail(nullptr, VOC_INVALID_ARG, "n_params " + std::to_string(n_params) + " != " +
+                                              std::to_string(enc_param_count(desc)));
+  const std::string kinds = enc_param_kinds(desc);
+  for (int i = 0; i < n_params; ++i) {
+    if (!params[i]) {
+      if (kinds[i] == 'b') continue;
+      return fail(nullptr, VOC_INVALID_ARG, "params[" + std::to_string(i) + "] is NULL");
+    }
+    int dims[3], nd;
+    vocoder_encoder_param_shape(desc, i, dims, &nd);
+    size_t n = 1;
+    for (int k = 0; k < nd; ++k) n *= dims[k];
+    for (size_t k = 0; k < n; ++k) {
+      const float x = params[i][k];
+      if (!std::isfinite(x))
+        return fail(nullptr, VOC_INVALID_ARG, "params[" + std::to_string(i) + "] not finite");
+      if (kinds[i] == 'a' && desc->snake == VOC_SNAKE && !(x > 0.f))
+        return fail(nullptr, VOC_INVALID_ARG, "Snake alpha must be positive");
+      if (kinds[i] == 'a' && desc->snake == VOC_SNAKE_BETA && !(std::fabs(x) <= 80.f))
+        return fail(nullptr, VOC_INVALID_ARG, "SnakeBeta log alpha / log beta must be in [-80, 80]");
+    }
+  }
+  if (!set_kernel_attrs(why)) return fail(nullptr, VOC_CUDA_ERROR, why);
+
+  vocoder_encoder *enc = new vocoder_encoder();
+  vocoder *ctx = &enc->core;
+  enc->desc = *desc;
+  enc->strides.assign(desc->strides, desc->strides + desc->n_stages);
+  enc->widths.assign(desc->widths, desc->widths + desc->n_stages);
+  enc->dils.assign(desc->dilations, desc->dilations + desc->n_dilations);
+  enc->desc.strides = enc->strides.data();
+  enc->desc.widths = enc->widths.data();
+  enc->desc.dilations = enc->dils.data();
+  for (int s : enc->strides) enc->hop *= s;
+  enc->Cp_audio = rup(desc->in_channels, 16);
+  enc->Cp_lat = rup(desc->latent_channels, 16);
+  ctx->f16 = desc->precision == VOC_PREC_F16W;
+  ctx->use_pair = false;
+  ctx->fuse_max_c = 0;
+  auto bail = [&](voc_status st) {
+    g_err = ctx->err;
+    vocoder_encoder_destroy(enc);
+    return st;
+  };
+  voc_status st = init_device(ctx);
+  if (st != VOC_OK) return bail(st);
+
+  const int pad = VOC_PAD_SYMMETRIC;
+  auto add = [&](Layer &L, bool has_skip, const float *w, const float *b, const SnakeCoef &sn,
+                 long long div, int split) {
+    L.f16 = ctx->f16;
+    if (!plan_layer(false, L, pad, has_skip, why))
+      return fail(ctx, VOC_UNSUPPORTED, L.name + ": " + why);
+    const voc_status s = upload_layer(ctx, ctx->allocs, L, pad, w, b, sn);
+    if (s != VOC_OK) return s;
+    enc->layers.push_back(L);
+    enc->div.push_back(div);
+    enc->split.push_back(split > 1 ? split : 0);
+    return VOC_OK;
+  };
+  // hi/lo buffers H0, H1, HB and the fp32 residual stream FY, used as in the decoder: a
+  // layer never writes the hi/lo buffer it reads with a halo
+  auto other = [](int a) { return a == BUF_H0 ? (int)BUF_H1 : (int)BUF_H0; };
+  const int nd = desc->n_dilations;
+  int C = desc->channels0;
+  long long div = 1;
+  int cur = BUF_H1;
+  {  // conv_in (no Snake in front); its epilogue applies the first residual unit's Snake1
+    Layer L;
+    L.name = "conv_in";
+    L.Cin = desc->in_channels, L.Cout = C, L.K = desc->in_kernel, L.dil = 1;
+    L.in_buf = BUF_H0, L.f32_buf = BUF_FY, L.hl_buf = cur;
+    if ((st = add(L, false, params[0], params[1], snake_coef(params[2], C, desc->snake), div, 0)) != VOC_OK)
+      return bail(st);
+  }
+  int p = 2;
+  for (int i = 0; i < desc->n_stages; ++i) {
+    const int s = enc->strides[i], Co = enc->widths[i];
+    const std::string blk = "b" + std::to_string(i);
+    for (int j = 0; j < nd; ++j) {
+      const float *w1 = params[p + 1], *b1 = params[p + 2];
+      const SnakeCoef a2 = snake_coef(params[p + 3], C, desc->snake);
+      const float *w2 = params[p + 4], *b2 = params[p + 5];
+      p += 6;
+      // the next unit's Snake1, or (last unit) the Snake in front of the strided conv
+      const SnakeCoef next = snake_coef(params[p], C, desc->snake);
+      const int tmp = other(cur);
+      Layer L1;
+      L1.name = blk + "r" + std::to_string(j) + ".conv1";
+      L1.Cin = C, L1.Cout = C, L1.K = desc->res_kernel, L1.dil = enc->dils[j];
+      L1.in_buf = cur, L1.hl_buf = tmp;
+      if ((st = add(L1, false, w1, b1, a2, div, 0)) != VOC_OK) return bail(st);
+      Layer L2;  // 1x1: reads `tmp` row for row, so it may write `cur`
+      L2.name = blk + "r" + std::to_string(j) + ".conv2";
+      L2.Cin = C, L2.Cout = C, L2.K = 1, L2.dil = 1;
+      L2.in_buf = tmp, L2.skip_buf = BUF_FY, L2.hl_buf = cur;
+      if (j < nd - 1) L2.f32_buf = BUF_FY;  // the last unit's sum is only read through its Snake
+      if ((st = add(L2, true, w2, b2, next, div, j == nd - 1 ? s : 0)) != VOC_OK) return bail(st);
+    }
+    {  // strided conv over the phase-split Snake'd input
+      const float *w = params[p + 1], *b = params[p + 2];
+      p += 3;
+      const bool last = i == desc->n_stages - 1;
+      // the next block's first Snake1, or Snake_out
+      const SnakeCoef next = snake_coef(params[p], Co, desc->snake);
+      const int o = other(cur);
+      Layer L;
+      L.name = blk + ".down";
+      L.down_s = s, L.down_c = C;
+      L.Cin = s * rup(C, 16), L.Cout = Co, L.K = 3, L.dil = 1;
+      L.in_buf = cur, L.hl_buf = o;
+      if (!last) L.f32_buf = BUF_FY;
+      div *= s;
+      if ((st = add(L, false, w, b, next, div, 0)) != VOC_OK) return bail(st);
+      cur = o;
+      C = Co;
+    }
+  }
+  {  // conv_out (its input already Snake'd), then the 1x1 posterior mean projection
+    const int o = other(cur);
+    Layer L;
+    L.name = "conv_out";
+    L.Cin = C, L.Cout = C, L.K = desc->out_kernel, L.dil = 1;
+    L.in_buf = cur, L.hl_buf = o;
+    if ((st = add(L, false, params[p + 1], params[p + 2], SnakeCoef{}, div, 0)) != VOC_OK)
+      return bail(st);
+    Layer P;
+    P.name = "proj";
+    P.Cin = C, P.Cout = desc->latent_channels, P.K = 1, P.dil = 1;
+    P.in_buf = o, P.f32_buf = BUF_FY;
+    if ((st = add(P, false, params[p + 3], params[p + 4], SnakeCoef{}, div, 0)) != VOC_OK)
+      return bail(st);
+  }
+  *out = enc;
+  return VOC_OK;
+}
+
+VOC_API long long vocoder_encoder_hop(const vocoder_encoder *enc) { return enc ? enc->hop : -1; }
+
+VOC_API size_t vocoder_encoder_workspace_bytes(const vocoder_encoder *enc, int B, long long L) {
+  if (!enc || B < 1 || B > 65535 || L < 1 || L % enc->hop) return 0;
+  if (L > (1LL << 30)) return 0;  // GEMM rows of one item stay in the kernels' int range
+  return 3 * enc_buf_bytes(enc, B, L);  // H0, H1 and FY (the encoder needs no third hi/lo buffer)
+}
+
+VOC_API int vocoder_encoder_launches(const vocoder_encoder *enc) {
+  return enc ? 2 + static_cast<int>(enc->layers.size()) : -1;
+}
+
+VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, int B, long long L,
+                                  float *latent_dev, void *ws, size_t ws_bytes,
+                                  voc_stream_t stream_h, unsigned flags) {
+  if (!enc) return fail(nullptr, VOC_INVALID_ARG, "encoder is NULL");
+  vocoder *ctx = &enc->core;
+  if (!audio_dev || !latent_dev) return fail(ctx, VOC_INVALID_ARG, "audio / latent NULL");
+  if (flags & ~(unsigned)(VOC_FLAG_SYNC | VOC_FLAG_PROFILE))
+    return fail(ctx, VOC_INVALID_ARG, "flags: only VOC_FLAG_SYNC and VOC_FLAG_PROFILE apply");
+  const size_t need = vocoder_encoder_workspace_bytes(enc, B, L);
+  if (!need)
+    return fail(ctx, VOC_INVALID_ARG, "B must be in [1, 65535] and L a positive multiple of the hop (" +
+                                          std::to_string(enc->hop) + ") up to 2^30");
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return fail(ctx, VOC_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < need)
+    return fail(ctx, VOC_WORKSPACE_TOO_SMALL,
+                "workspace " + std::to_string(ws_bytes) + " < " + std::to_string(need));
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != ctx->device) return fail(ctx, VOC_INVALID_ARG, "current device differs from the encoder's");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_h);
+
+  const size_t bb = enc_buf_bytes(enc, B, L);
+  void *bufs[BUF_COUNT];
+  uint8_t *base = static_cast<uint8_t *>(ws);
+  bufs[BUF_H0] = base, bufs[BUF_H1] = base + bb, bufs[BUF_HB] = nullptr, bufs[BUF_FY] = base + 2 * bb;
+  const size_t n_layers = enc->layers.size();
+  if (enc->map_ws != ws || enc->map_B != B || enc->map_L != L) {
+    enc->maps.resize(n_layers);
+    enc->skip_maps.assign(n_layers, CUtensorMap{});
+    for (size_t i = 0; i < n_layers; ++i) {
+      const Layer &Ly = enc->layers[i];
+      const long long rows = pitch8(L / enc->div[i]);
+      voc_status st = encode_map(ctx, &enc->maps[i], bufs[Ly.in_buf], Ly.Cp_in, rows, B, Ly.g.rows,
+                                 Ly.g.KB / 8);
+      if (st == VOC_OK && Ly.skip_buf >= 0)
+        st = encode_skip_map(ctx, &enc->skip_maps[i], bufs[Ly.skip_buf], Ly.Cp_out, rows, B, Ly.cw);
+      if (st != VOC_OK) {
+        enc->map_ws = nullptr;
+        return st;
+      }
+    }
+    enc->map_ws = ws, enc->map_B = B, enc->map_L = L;
+  }
+
+  const bool prof = (flags & VOC_FLAG_PROFILE) != 0;
+  const int n_launch = vocoder_encoder_launches(enc);
+  if (prof) {
+    while ((int)ctx->events.size() < 2 * n_launch) {
+      cudaEvent_t ev;
+      cudaError_t e = cudaEventCreate(&ev);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaEventCreate");
+      ctx->events.push_back(ev);
+    }
+    ctx->prof_names.assign(n_launch, "");
+    ctx->prof_flops.assign(n_launch, 0.0);
+    ctx->prof_bytes.assign(n_launch, 0.0);
+    ctx->prof_ms.assign(n_launch, -1.f);
+    ctx->prof_n = n_launch;
+    ctx->prof_ready = false;
+  }
+  int li = 0;
+  auto rec = [&](int which) {
+    if (prof) cudaEventRecord(ctx->events[2 * li + which], stream);
+  };
+  const int Ci = enc->desc.in_channels;
+  rec(0);
+  voc_status st = launch_prep(ctx, audio_dev, B, Ci, static_cast<int>(L), enc->Cp_audio, nullptr,
+                              nullptr, static_cast<__nv_bfloat16 *>(bufs[BUF_H0]), stream);
+  if (st != VOC_OK) return st;
+#ifdef VOC_CHECKS
+  if ((st = check_launch(ctx, "prep_audio", stream)) != VOC_OK) return st;
+#endif
+  rec(1);
+  if (prof) {
+    ctx->prof_names[li] = "prep_audio";
+    ctx->prof_bytes[li] = (double)B * L * (4.0 * Ci + 4.0 * enc->Cp_audio);
+  }
+  ++li;
+  for (size_t i = 0; i < n_layers; ++i, ++li) {
+    const Layer &Ly = enc->layers[i];
+    const long long rows = L / enc->div[i];
+    ConvGemmArgs a;
+    gemm_args_rows(ctx, Ly, B, rows, bufs, bb, a);
+    if (enc->split[i]) {
+      // Phase-split hi/lo output: planes of pitch8(L/s) rows, so rows [L, s pitch8(L/s)) of
+      // the layer are written as zeros -- the strided conv reads row L/s of every phase as
+      // its right padding.  With s not a power of two those rows can lie past the last
+      // 128-row tile of L rows: the launch covers them (its input rows there read as zeros).
+      const int s = enc->split[i];
+      a.split_s = s;
+      a.hl_L = static_cast<int>(pitch8(rows / s));
+      a.rows_pad = static_cast<int>(rup_ll(rows, 8LL * s));
+      a.m_tiles = (a.rows_pad + voc::kTileM - 1) / voc::kTileM;
+    }
+    rec(0);
+    st = launch_gemm(ctx, Ly, enc->maps[i], enc->skip_maps[i], a, stream);
+    if (st != VOC_OK) return st;
+#ifdef VOC_CHECKS
+    if ((st = check_launch(ctx, Ly.name, stream)) != VOC_OK) return st;
+#endif
+    rec(1);
+    if (prof) {
+      ctx->prof_names[li] = Ly.name;
+      enc_layer_cost(Ly, B, rows, ctx->prof_flops[li], ctx->prof_bytes[li]);
+    }
+  }
+  const long long Lz = L / enc->hop;
+  const int Cl = enc->desc.latent_channels;
+  rec(0);
+  voc::rows_to_cf_kernel<<<dim3(static_cast<unsigned>((Lz + 255) / 256), enc->Cp_lat / 4, B), 256, 0,
+                           stream>>>(static_cast<const float *>(bufs[BUF_FY]), static_cast<int>(Lz),
+                                     pitch8(Lz), enc->Cp_lat, Cl, latent_dev);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "launch latent layout");
+  rec(1);
+  if (prof) {
+    ctx->prof_names[li] = "latent_out";
+    ctx->prof_bytes[li] = (double)B * Lz * (4.0 * enc->Cp_lat + 4.0 * Cl);
+    ctx->prof_ready = true;
+  }
+  ++li;
+  if (flags & VOC_FLAG_SYNC) {
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+    int word = 0;
+    e = cudaMemcpy(&word, ctx->err_dev, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "read device error word");
+    if (word) {
+      cudaMemset(ctx->err_dev, 0, sizeof(int));
+      return fail(ctx, VOC_DEVICE_TIMEOUT,
+                  "a kernel gave up a bounded wait (code " + std::to_string(word) + ")");
+    }
+  }
+  return VOC_OK;
+}
+
+VOC_API int vocoder_encoder_profile_count(const vocoder_encoder *enc) {
+  return enc ? vocoder_profile_count(&enc->core) : 0;
+}
+
+VOC_API voc_status vocoder_encoder_profile_entry(vocoder_encoder *enc, int index, const char **name,
+                                                 double *ms, double *flops, double *bytes) {
+  if (!enc) return fail(nullptr, VOC_INVALID_ARG, "encoder is NULL");
+  return vocoder_profile_entry(&enc->core, index, name, ms, flops, bytes);
+}
+
+VOC_API const char *vocoder_encoder_last_error(const vocoder_encoder *enc) {
+  return enc ? enc->core.err.c_str() : g_err.c_str();
 }

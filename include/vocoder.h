@@ -332,6 +332,91 @@ voc_status vocoder_encode_wav(const float *planar_dev, int n_ch, long long len, 
                               int bits, int peak_clip, void *out_dev, size_t out_bytes,
                               void *scratch_dev, size_t scratch_bytes, voc_stream_t stream);
 
+/* ---------------------------------------------------------------- mirror encoder
+ * minimaxmusic.cpp Architecture, "Flow VAE": the encoder mirrors the decoder and maps audio
+ * to the latent's posterior mean:
+ *
+ *   conv_in k7 (C_in -> C0)
+ *   for every downsampling block (stride s, C -> C' = widths[i]):
+ *       3 residual units at C channels (as in the decoder), then
+ *       Snake -> strided Conv1d (k = 2s, stride s, pad s/2 on both sides: L -> L/s)
+ *   Snake -> conv_out k3 (C_last -> C_last) -> posterior mean projection k1 (C_last -> C_lat)
+ *
+ * All convolutions are non-causal (k-tap convs pad (k-1)d/2 on both sides), weights are
+ * folded like the decoder's, and the precision is the decoder's (VOC_PREC_*).  On the
+ * device each strided conv runs as a 3-tap conv over its input split into s phases
+ * (row u s + r of channel c becomes row u of channel (c/8 s + r) 8 + c%8), the split done
+ * by the epilogue of the layer that produces the input. */
+typedef struct vocoder_encoder vocoder_encoder_t;  /* opaque encoder context */
+
+/* Architecture of the encoder; arrays are borrowed for vocoder_encoder_create only. */
+typedef struct {
+  int abi_version;      /* VOC_ABI_VERSION                                       */
+  int in_channels;      /* audio channels C_in (1..16; 1)                         */
+  int channels0;        /* C0, conv_in output channels                            */
+  int in_kernel;        /* conv_in taps (odd, 1..15; 7)                           */
+  int n_stages;         /* downsampling blocks (1..8)                             */
+  const int *strides;   /* [n_stages] strides s (1..16)                           */
+  const int *widths;    /* [n_stages] output channels of each block's strided conv */
+  int n_dilations;      /* residual units per block (1..4; 3)                     */
+  const int *dilations; /* [n_dilations] (1, 3, 9)                                */
+  int res_kernel;       /* dilated conv taps (odd; 7)                             */
+  int out_kernel;       /* conv_out taps (odd; 3)                                 */
+  int latent_channels;  /* C_lat, projection output channels (64)                 */
+  int precision;        /* VOC_PREC_BF16X3 | VOC_PREC_F16W                        */
+  int snake;            /* VOC_SNAKE | VOC_SNAKE_BETA                             */
+} voc_enc_desc;
+
+/* Number of parameter tensors, or -1 for an invalid desc.  Canonical order and PyTorch
+ * layouts (weights already folded), C the input channels of a block, C' = widths[i]:
+ *   conv_in.w [C0][C_in][in_kernel], conv_in.b [C0],
+ *   per block i: per dilation: snake1.alpha [C], conv1.w [C][C][res_kernel], conv1.b [C],
+ *                              snake2.alpha [C], conv2.w [C][C][1], conv2.b [C],
+ *                snake.alpha [C], down.w [C'][C][2s], down.b [C'],
+ *   snake_out.alpha [C_last], conv_out.w [C_last][C_last][out_kernel], conv_out.b [C_last],
+ *   proj.w [C_lat][C_last][1], proj.b [C_lat].
+ * Snake entries are [2][C] with VOC_SNAKE_BETA, as for the decoder. */
+int vocoder_encoder_param_count(const voc_enc_desc *desc);
+voc_status vocoder_encoder_param_shape(const voc_enc_desc *desc, int index, int dims[3],
+                                       int *ndim);
+
+/* Create an encoder on the current device (params as for vocoder_create: host pointers,
+ * NULL biases mean zero, not retained).  On failure *out is NULL and
+ * vocoder_encoder_last_error(NULL) describes the problem. */
+voc_status vocoder_encoder_create(const voc_enc_desc *desc, const float *const *params,
+                                  int n_params, vocoder_encoder_t **out);
+
+/* Downsampling factor (product of the strides), or -1 for NULL. */
+long long vocoder_encoder_hop(const vocoder_encoder_t *enc);
+
+/* Device workspace of one encode of B items of L samples (0 for invalid sizes: L must be a
+ * positive multiple of the hop, B * channels * L within the int range of the kernels). */
+size_t vocoder_encoder_workspace_bytes(const vocoder_encoder_t *enc, int B, long long L);
+
+/* Encode audio_dev [B][C_in][L] fp32 (device) into
+ * latent_dev [B][C_lat][L / hop] fp32 (device), asynchronously on `stream`.  ws_dev: at
+ * least vocoder_encoder_workspace_bytes, 256-byte aligned, caller-owned.  flags: 0,
+ * VOC_FLAG_SYNC (wait and report VOC_DEVICE_TIMEOUT) and VOC_FLAG_PROFILE. */
+voc_status vocoder_encode(vocoder_encoder_t *enc, const float *audio_dev, int B, long long L,
+                          float *latent_dev, void *ws_dev, size_t ws_bytes, voc_stream_t stream,
+                          unsigned flags);
+
+/* Kernel launches of one vocoder_encode. */
+int vocoder_encoder_launches(const vocoder_encoder_t *enc);
+
+/* Per-kernel records of the last encode run with VOC_FLAG_PROFILE, as vocoder_profile_*
+ * for the decoder (a strided conv's FLOPs count its 2s taps over the real channels). */
+int vocoder_encoder_profile_count(const vocoder_encoder_t *enc);
+voc_status vocoder_encoder_profile_entry(vocoder_encoder_t *enc, int index, const char **name,
+                                         double *ms, double *flops, double *bytes);
+
+/* Message of the last failed call on enc (NULL: of the last failure on this thread
+ * without a context). */
+const char *vocoder_encoder_last_error(const vocoder_encoder_t *enc);
+
+/* Free the encoder (NULL is ignored). */
+void vocoder_encoder_destroy(vocoder_encoder_t *enc);
+
 #ifdef __cplusplus
 }
 #endif

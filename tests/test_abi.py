@@ -135,3 +135,38 @@ def test_precision_field_validation(lib):
         V.vocoder_create(W.TINY, [None] * n, cta_pair=1, precision=V.VOC_PREC_F16W)
     assert e.value.status == V.VOC_INVALID_ARG
     assert "cta_pair" in V.vocoder_last_error()
+
+
+ENC_ARCHS = [W.ENC_MUSIC, W.EncArch(1, 16, (2, 4), (32, 48), 8),
+             W.EncArch(2, 24, (3, 5, 1), (40, 56, 56), 12, dilations=(1, 3)),
+             dataclasses.replace(W.ENC_MUSIC, snake_beta=True)]
+
+
+@pytest.mark.parametrize("arch", ENC_ARCHS, ids=["music", "small", "odd_strides", "snake_beta"])
+def test_encoder_param_shapes_match_layer_list(lib, arch):
+    shapes = arch.param_shapes()
+    assert V.vocoder_encoder_param_count(arch) == len(shapes)
+    for i, (_name, shape) in enumerate(shapes):
+        assert V.vocoder_encoder_param_shape(arch, i) == shape
+
+
+def test_encoder_create_validates_before_device_work(lib):
+    n = V.vocoder_encoder_param_count(W.ENC_MUSIC)
+    with pytest.raises(V.VocoderError) as e:
+        V.vocoder_encoder_create(W.ENC_MUSIC, [None] * (n - 1))
+    assert e.value.status == V.VOC_INVALID_ARG
+    assert "n_params" in V.vocoder_encoder_last_error()
+    bad = dataclasses.replace(W.ENC_MUSIC, strides=(2, 17, 8, 8))
+    assert V.vocoder_encoder_param_count(bad) == -1
+    with pytest.raises(V.VocoderError) as e:
+        V.vocoder_encoder_create(bad, [None] * n)
+    assert e.value.status == V.VOC_INVALID_ARG
+    d = V.make_enc_desc(W.ENC_MUSIC, precision=2)
+    assert lib.vocoder_encoder_param_count(ctypes.byref(d)) == -1
+    # a weight is required (only biases may be NULL): rejected before any device call
+    with pytest.raises(V.VocoderError) as e:
+        V.vocoder_encoder_create(W.ENC_MUSIC, [None] * n)
+    assert "params[0]" in V.vocoder_encoder_last_error()
+    assert V.vocoder_encoder_hop(None) == -1
+    assert V.vocoder_encoder_workspace_bytes(None, 1, 512) == 0
+    assert V.vocoder_encoder_launches(None) == -1

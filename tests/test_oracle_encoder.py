@@ -92,3 +92,22 @@ def test_encoder_length_and_affinity():
     lhs = E((0.25 * a1 + 0.5 * a2).astype(np.float32)) - e0
     rhs = 0.25 * (E(a1) - e0) + 0.5 * (E(a2) - e0)
     np.testing.assert_allclose(lhs, rhs, rtol=0, atol=1e-6 * np.max(np.abs(rhs)))
+
+
+def test_encoder_receptive_field_helper_is_tight():
+    """The sampled full-size GPU checks rely on tests.util.encoder_sample_span: changing one
+    audio sample just outside the span of latent frame u leaves z[u] unchanged, and just
+    inside it changes z[u] (the span is neither too small nor loose at its ends)."""
+    from tests.util import encoder_sample_span
+    arch = W.EncArch(1, 8, (2, 4), (8, 8), 4, dilations=(1, 3))
+    frames, u = 24, 12
+    wl = W.make_encode_workload(arch, 1, frames, 5)
+    f = O.fold_params(wl.params)
+    base = O.encode(arch, None, wl.latent, 0, f)[0, :, u]
+    lo, hi = encoder_sample_span(arch, u)
+    assert 0 < lo and hi < frames * arch.hop - 1
+    for pos, inside in [(lo - 1, False), (hi + 1, False), (lo, True), (hi, True)]:
+        a = wl.latent.copy()
+        a[0, 0, pos] += 0.5
+        z = O.encode(arch, None, a, 0, f)[0, :, u]
+        assert (np.max(np.abs(z - base)) > 1e-9) == inside, (pos, inside)

@@ -63,3 +63,33 @@ def snr_db(ref: np.ndarray, got: np.ndarray) -> float:
     if den == 0.0:
         return math.inf
     return 10.0 * math.log10(num / den)
+
+
+def encoder_sample_span(arch, u: int):
+    """Inclusive interval [lo, hi] of audio samples that latent frame u of the (non-causal)
+    mirror encoder can depend on.  Walks from the latent back to the audio: a k-tap conv
+    with dilation d maps [a, b] to [a - d(k-1)/2, b + d(k-1)/2]; a strided conv of stride s,
+    k = 2s, pad s/2 maps [a, b] to [a s - s/2, b s - s/2 + 2s - 1]; a residual unit adds its
+    conv1 span."""
+    a = b = u
+    h = (arch.out_kernel - 1) // 2
+    a, b = a - h, b + h
+    for st in reversed(range(len(arch.strides))):
+        s = arch.strides[st]
+        a, b = a * s - s // 2, b * s - s // 2 + 2 * s - 1
+        for d in reversed(arch.dilations):
+            h = d * (arch.res_kernel - 1) // 2
+            a, b = a - h, b + h
+    h = (arch.in_kernel - 1) // 2
+    return a - h, b + h
+
+
+def encoder_frame_margins(arch):
+    """(left, right) latent frames of audio context that one latent frame reads around its
+    own hop of samples."""
+    hop = arch.hop
+    u = 64
+    lo, hi = encoder_sample_span(arch, u)
+    left = -((lo - u * hop) // hop)
+    right = -(-(hi - (u * hop + hop - 1)) // hop)
+    return max(left, 0), max(right, 0)
