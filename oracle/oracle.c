@@ -42,6 +42,28 @@ void oracle_round_half(const double *x, long n, double *y) {
   for (long i = 0; i < n; ++i) y[i] = round_half_one(x[i]);
 }
 
+/* bfloat16: 8 significant bits (7 stored), binary32's exponent range.  Same steps as
+ * round_half_one: single precision first, then the nearest multiple of the binade's quantum
+ * 2^(e-7), ties to even; subnormals (below 2^-126) share the smallest binade's quantum; a
+ * result of 2^128 or more is infinite. */
+static double round_bf16_one(double x) {
+  const float f = (float)x;
+  const double a = fabs((double)f);
+  if (a == 0.0 || !isfinite(a)) return (double)f;
+  int E;
+  frexp(a, &E);
+  int e = E - 1;
+  if (e < -126) e = -126;
+  const double q = ldexp(1.0, e - 7);
+  const double r = nearbyint(a / q) * q;
+  if (r >= ldexp(1.0, 128)) return copysign(INFINITY, (double)f);
+  return copysign(r, (double)f);
+}
+
+void oracle_round_bf16(const double *x, long n, double *y) {
+  for (long i = 0; i < n; ++i) y[i] = round_bf16_one(x[i]);
+}
+
 long oracle_hop(const oracle_arch *a) {
   long h = 1;
   for (int i = 0; i < a->n_stages; ++i) h *= a->strides[i];

@@ -86,6 +86,12 @@ int oracle_param_count(const oracle_arch *a);
  * magnitudes below 2^-14 use the subnormal quantum 2^-24. */
 void oracle_round_half(const double *x, long n, double *y);
 
+/* y[i] = x[i] rounded to single precision, then to bfloat16 (8 significant bits, binary32's
+ * exponent range), both round to nearest, ties to even: the convolution weights of the
+ * BF16-weight precision variant.  Results of 2^128 or more in magnitude are infinite;
+ * magnitudes below 2^-126 use the subnormal quantum 2^-133. */
+void oracle_round_bf16(const double *x, long n, double *y);
+
 /* w[i, :] = g[i] * v[i, :] / ||v[i, :]||, the norm taken over everything but
  * axis 0 of the stored tensor (Conv1d [Cout][Cin][K]: per output channel;
  * ConvTranspose1d [Cin][Cout][K]: per input channel).  Returns -1 when a row of

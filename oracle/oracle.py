@@ -49,6 +49,8 @@ def _load():
             lib.oracle_fold_weight_norm.restype = ctypes.c_int
             lib.oracle_round_half.argtypes = [D, ctypes.c_long, D]
             lib.oracle_round_half.restype = None
+            lib.oracle_round_bf16.argtypes = [D, ctypes.c_long, D]
+            lib.oracle_round_bf16.restype = None
             lib.oracle_snake_row.argtypes = [D, ctypes.c_long, ctypes.c_double, ctypes.c_int, D]
             lib.oracle_snake_row.restype = None
             lib.oracle_snake_beta_row.argtypes = [D, ctypes.c_long, ctypes.c_double,
@@ -196,13 +198,22 @@ def round_half(x: np.ndarray) -> np.ndarray:
     return y
 
 
-def fold_params(params: Sequence, f16_weights: bool = False) -> list:
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round to single, then to bfloat16 (both to nearest, ties to even)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    _load().oracle_round_bf16(_d(x), x.size, _d(y))
+    return y
+
+
+def fold_params(params: Sequence, f16_weights: bool = False, bf16_weights: bool = False) -> list:
     """Raw canonical parameters (RawConv / alpha arrays) -> list of double arrays
-    (folded weight, bias, alpha, ...) in the canonical order.  f16_weights: every
-    convolution weight rounded to half precision (the F16-weight precision variant);
-    biases and Snake parameters are kept."""
+    (folded weight, bias, alpha, ...) in the canonical order.  f16_weights / bf16_weights:
+    every convolution weight rounded to half precision / bfloat16 (the F16- and BF16-weight
+    precision variants); biases and Snake parameters are kept."""
+    assert not (f16_weights and bf16_weights)
     out = []
-    wf = round_half if f16_weights else (lambda w: w)
+    wf = round_half if f16_weights else round_bf16 if bf16_weights else (lambda w: w)
     for p in params:
         if hasattr(p, "g"):
             out.append(wf(fold_weight_norm(p.g, p.v)))

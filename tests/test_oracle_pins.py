@@ -584,3 +584,60 @@ def test_f16_weights_round_only_convolution_weights():
     y1 = O.decode(arch, None, wl.latent, 0, half)
     d = np.max(np.abs(y1 - y0))
     assert 1e-7 < d < 1e-2
+
+
+# ----------------------------------------------------------------------------- BF16 weights
+def test_round_bf16_matches_torch():
+    """Single then bfloat16 precision, ties to even, against torch's float32 -> bfloat16
+    conversion (a library routine), on random magnitudes over the whole exponent range,
+    exact halfway points and the overflow / subnormal edges."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(19)
+    mags = 10.0 ** rng.uniform(-40, 38, size=4000)
+    x = mags * rng.choice([-1.0, 1.0], size=mags.size)
+    ties = []
+    for e in (-133, -130, -126, -20, -1, 0, 1, 30, 127):  # halfway between neighbouring bf16s
+        q = 2.0 ** max(e - 7, -133)
+        for k in (1, 2, 3, 127, 128, 255):
+            ties.append((k + 0.5) * q)
+    fmax = float(np.finfo(np.float32).max)
+    edges = [0.0, -0.0, fmax, -fmax, 3.3895e38, 3.3896e38, 2.0 ** -126, 2.0 ** -133,
+             2.0 ** -134, 1.5 * 2.0 ** -134, 1e-45]
+    x = np.concatenate([x, np.array(ties), -np.array(ties), np.array(edges)])
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_bf16(x)
+    assert np.array_equal(np.signbit(got), np.signbit(ref))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_round_bf16_hand_values():
+    """Values fixed by the format alone: spacing 2^-7 above 1, ties to the even neighbour."""
+    cases = [(1.0 + 2.0 ** -8, 1.0),                       # halfway, 1.0 is even
+             (1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -6),       # halfway, 1 + 2^-6 is even
+             (1.0 + 2.0 ** -8 + 2.0 ** -20, 1.0 + 2.0 ** -7),
+             (-(1.0 + 5 * 2.0 ** -8), -(1.0 + 2 * 2.0 ** -7)),  # halfway, mantissa 2 is even
+             (255.5, 256.0), (254.5, 254.0), (0.1, 0.10009765625)]
+    for x, want in cases:
+        assert O.round_bf16(np.array([x]))[0] == want, (x, want)
+
+
+def test_bf16_weights_round_only_convolution_weights():
+    """fold_params(bf16_weights=True) rounds every convolution weight and leaves biases and
+    Snake parameters as they are; bf16 rounding moves more weights further than f16's."""
+    arch = W.Arch(latent_channels=6, channels0=24, strides=(4, 2), widths=(12, 8),
+                  in_proj_channels=10)
+    wl = W.make_custom(arch, B=1, T=9, seed=5)
+    full = O.fold_params(wl.params)
+    bf = O.fold_params(wl.params, bf16_weights=True)
+    half = O.fold_params(wl.params, f16_weights=True)
+    names = [n for n, _ in arch.param_shapes()]
+    for n, a, b, h in zip(names, full, bf, half):
+        if n.endswith(".w"):
+            np.testing.assert_array_equal(b, O.round_bf16(a))
+            assert np.max(np.abs(b - a)) >= np.max(np.abs(h - a))
+            rel = np.abs(b - a) / np.maximum(np.abs(a), 1e-30)
+            assert np.max(rel) <= 2.0 ** -8 * (1 + 1e-12)  # half a unit in the 8th bit
+        elif a is None:
+            assert b is None
+        else:
+            np.testing.assert_array_equal(a, b)
