@@ -11,6 +11,9 @@ bracketed by CUDA events on the decode stream; a 256 MiB buffer (larger than the
 scaling with no collective on the data path (a scalar max-reduction of the step
 time only).  Rank 0 prints one JSON line.
 
+--workload encode_music_window times the mirror encoder instead: one step encodes a
+stereo 689-frame window of audio into latents (metric: audio samples encoded per second).
+
 --impl reference times the CPU oracle on this host's cores on a bounded sample
 of the same workload (a slice of latent frames per step)."""
 from __future__ import annotations
@@ -33,8 +36,9 @@ if ROOT not in sys.path:
 from dac_vocoder_decode_gb300 import workloads as W  # noqa: E402
 
 METRIC = "vocoder audio samples/sec"
+ENC_METRIC = "encoder audio samples/sec"  # audio samples encoded into latents per second
 UNIT = "samples/s"
-SAMPLE_RATE = {"music_window": 44100, "music_batch8": 44100, "music_long": 44100, "speech": 24000,
+SAMPLE_RATE = {"encode_music_window": 44100, "music_window": 44100, "music_batch8": 44100, "music_long": 44100, "speech": 24000,
                "speech_snakebeta": 24000, "tiny": 44100, "tiny_cal": 44100}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -169,12 +173,51 @@ def max_over_ranks(value: float, device="cpu") -> float:
     return float(t.item())
 
 
+# ----------------------------------------------------------------------------- workloads
+def is_encode(name: str) -> bool:
+    return name in W.ENC_WORKLOADS
+
+
+def metric_of(name: str) -> str:
+    return ENC_METRIC if is_encode(name) else METRIC
+
+
+def load_workload(name: str, frames=None):
+    return W.make_named_encode_workload(name, frames) if is_encode(name) else W.make_workload(name)
+
+
+def workload_config(wl, name):
+    if not is_encode(name):
+        return config_of(wl, name)
+    arch = wl.arch
+    B, C, L = wl.latent.shape
+    return {"workload": f"{name}: {W.ENC_WORKLOADS[name][4]}", "audio": [B, C, L],
+            "latent": [B, arch.latent_channels, L // arch.hop], "hop": arch.hop,
+            "sample_rate": SAMPLE_RATE[name],
+            "l2": "flushed between timed steps (256 MiB write, outside the timed events)"}
+
+
+def realtime_seconds(wl, name) -> float:
+    """Seconds of music / speech one step handles (a stereo pair counts once)."""
+    if is_encode(name):
+        B, _, L = wl.latent.shape
+        return B / 2.0 * L / SAMPLE_RATE[name]
+    return tracks_per_batch(name, wl.B) * wl.T * wl.arch.hop / SAMPLE_RATE[name]
+
+
 # ----------------------------------------------------------------------------- CPU legs
-def oracle_sample(wl, frames: int, folded=None):
-    """Time the oracle on one item's first `frames` latent frames (bounded CPU work)."""
+def oracle_sample(wl, frames: int, folded=None, encode=False):
+    """Time the oracle on one item's first `frames` latent frames (bounded CPU work); returns
+    (audio samples decoded or encoded, seconds, folded parameters)."""
     from oracle import oracle as O
     if folded is None:
         folded = O.fold_params(wl.params)
+    if encode:
+        hop = wl.arch.hop
+        audio = np.ascontiguousarray(wl.latent[:1, :, :min(frames * hop, wl.latent.shape[2])])
+        t0 = time.perf_counter()
+        O.encode(wl.arch, None, audio, 0, folded)
+        return audio.size, time.perf_counter() - t0, folded
     lat = W.slice_latent(wl.latent[:1], 0, min(frames, wl.T))
     t0 = time.perf_counter()
     y = O.decode(wl.arch, None, lat, 0, folded)
@@ -188,38 +231,43 @@ def cpu_threads():
 
 
 def cpu_baseline(wl, name, frames):
-    samples, dt, _ = oracle_sample(wl, frames)
+    enc = is_encode(name)
+    samples, dt, _ = oracle_sample(wl, frames, encode=enc)
+    what = (f"1 item x {samples} audio samples ({samples // wl.arch.hop} latent frames) of {name} "
+            f"encoded" if enc else
+            f"1 item x {min(frames, wl.T)} latent frames of {name} ({samples} samples) decoded")
     return {"value": samples / dt, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"1 item x {min(frames, wl.T)} latent frames of {name} "
-                      f"({samples} samples) decoded in {dt:.2f} s (fp64 direct loops, OpenMP)"}
+            "sample": f"{what} in {dt:.2f} s (fp64 direct loops, OpenMP)"}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    wl = W.make_workload(args.workload)
+    enc = is_encode(args.workload)
+    wl = load_workload(args.workload)
     frames = args.ref_frames
     folded = None
     for _ in range(args.warmup):
-        _, _, folded = oracle_sample(wl, frames, folded)
+        _, _, folded = oracle_sample(wl, frames, folded, encode=enc)
     times = []
     samples = 0
     for _ in range(args.steps):
-        samples, dt, folded = oracle_sample(wl, frames, folded)
+        samples, dt, folded = oracle_sample(wl, frames, folded, encode=enc)
         times.append(dt)
     ms = 1e3 * statistics.mean(times)
     value = samples / (ms / 1e3)
     rate = SAMPLE_RATE[args.workload]
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+    line = {"impl": "reference", "metric": metric_of(args.workload), "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "x_realtime": value / rate / (2.0 if args.workload.startswith("music") else 1.0),
-            "config": config_of(wl, args.workload),
+            "x_realtime": value / rate / (2.0 if "music" in args.workload else 1.0),
+            "config": workload_config(wl, args.workload),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(),
                              "kind": "oracle",
-                             "sample": f"each step: 1 item x {min(frames, wl.T)} latent frames "
-                                       f"of {args.workload} ({samples} samples)"},
+                             "sample": f"each step: 1 item x {samples} audio samples "
+                                       f"({samples // wl.arch.hop} latent frames) of "
+                                       f"{args.workload}"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -227,6 +275,79 @@ def run_reference(args, rank, world):
 
 
 # ----------------------------------------------------------------------------- GPU leg
+class DecodeJob:
+    """One decode of the workload per step, through vocoder_decode (device buffers) or
+    vocoder_decode_host (host buffers, copies inside the call)."""
+
+    def __init__(self, V, wl, precision, dev):
+        import torch
+        self.V, self.wl = V, wl
+        self.ctx = V.Vocoder(wl.arch, V.fold_params(wl.params), precision=precision)
+        B, T, hop = wl.B, wl.T, wl.arch.hop
+        self.x = torch.from_numpy(wl.latent).to(dev)
+        self.y = torch.empty((B, 1, T * hop), dtype=torch.float32, device=dev)
+        self.ws = self.ctx.alloc_workspace(B, T)
+        self.samples = B * T * hop
+        self.h2d, self.d2h = int(wl.latent.nbytes), int(B * T * hop * 4)
+
+    def step(self, stream, flags=0):
+        self.V.vocoder_decode(self.ctx.handle, self.x, self.y, self.ws, stream, flags)
+
+    def setup_host(self):
+        import torch
+        wl = self.wl
+        self.x_h = torch.from_numpy(wl.latent).pin_memory()
+        self.y_h = torch.empty(tuple(self.y.shape), dtype=torch.float32).pin_memory()
+        self.ws_h = self.ctx.alloc_workspace(wl.B, wl.T, host_io=True)
+
+    def host_step(self, stream):
+        self.V.vocoder_decode_host(self.ctx.handle, self.x_h, self.y_h, self.ws_h, stream)
+
+    def profile(self):
+        return self.V.vocoder_profile(self.ctx.handle)
+
+    def launches(self):
+        return self.V.vocoder_launches_per_decode(self.ctx.handle, self.wl.B, self.wl.T)
+
+    def close(self):
+        self.ctx.close()
+
+
+class EncodeJob(DecodeJob):
+    """One encode of the workload's audio per step (vocoder_encode / vocoder_encode_host)."""
+
+    def __init__(self, V, wl, precision, dev):
+        import torch
+        self.V, self.wl = V, wl
+        self.ctx = V.Encoder(wl.arch, V.fold_params(wl.params), precision=precision)
+        B, C, L = wl.latent.shape
+        self.x = torch.from_numpy(wl.latent).to(dev)
+        self.y = torch.empty((B, wl.arch.latent_channels, L // wl.arch.hop), dtype=torch.float32,
+                             device=dev)
+        self.ws = self.ctx.alloc_workspace(B, L)
+        self.samples = B * L
+        self.h2d, self.d2h = int(wl.latent.nbytes), int(self.y.numel() * 4)
+
+    def step(self, stream, flags=0):
+        self.V.vocoder_encode(self.ctx.handle, self.x, self.y, self.ws, stream, flags)
+
+    def setup_host(self):
+        import torch
+        B, _, L = self.wl.latent.shape
+        self.x_h = torch.from_numpy(self.wl.latent).pin_memory()
+        self.y_h = torch.empty(tuple(self.y.shape), dtype=torch.float32).pin_memory()
+        self.ws_h = self.ctx.alloc_workspace(B, L, host_io=True)
+
+    def host_step(self, stream):
+        self.V.vocoder_encode_host(self.ctx.handle, self.x_h, self.y_h, self.ws_h, stream)
+
+    def profile(self):
+        return self.V.vocoder_encoder_profile(self.ctx.handle)
+
+    def launches(self):
+        return self.V.vocoder_encoder_launches(self.ctx.handle)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -236,15 +357,13 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     peaks, peaks_kind = load_peaks()
-    wl = W.make_workload(args.workload)
+    wl = load_workload(args.workload)
     f16w = args.precision == "f16w"
-    voc = V.Vocoder(wl.arch, V.fold_params(wl.params),
-                    precision=V.VOC_PREC_F16W if f16w else V.VOC_PREC_BF16X3)
-    B, T, hop = wl.B, wl.T, wl.arch.hop
+    one_plane = args.precision in ("f16w", "bf16w")  # one weight plane, two MMAs per MAC
+    prec = {"bf16x3": V.VOC_PREC_BF16X3, "f16w": V.VOC_PREC_F16W,
+            "bf16w": V.VOC_PREC_BF16W}[args.precision]
+    job = (EncodeJob if is_encode(args.workload) else DecodeJob)(V, wl, prec, dev)
     stream = torch.cuda.Stream(device=dev)
-    lat = torch.from_numpy(wl.latent).to(dev)
-    audio = torch.empty((B, 1, T * hop), dtype=torch.float32, device=dev)
-    ws = voc.alloc_workspace(B, T)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
 
@@ -254,10 +373,10 @@ def run_ours(args, rank, world, local_rank):
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            V.vocoder_decode(voc.handle, lat, audio, ws, stream)
+            job.step(stream)
     torch.cuda.synchronize()
 
-    launches = V.vocoder_launches_per_decode(voc.handle, B, T)
+    launches = job.launches()
     per_kernel = {}
     step_ms = []
     clocks = ClockSampler(local_rank)
@@ -270,11 +389,11 @@ def run_ours(args, rank, world, local_rank):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            V.vocoder_decode(voc.handle, lat, audio, ws, stream, V.VOC_FLAG_PROFILE)
+            job.step(stream, V.VOC_FLAG_PROFILE)
             e1.record(stream)
             e1.synchronize()
             step_ms.append(e0.elapsed_time(e1))
-            for i, p in enumerate(V.vocoder_profile(voc.handle)):
+            for i, p in enumerate(job.profile()):
                 rec = per_kernel.setdefault(i, dict(name=p["name"], ms=[], flops=p["flops"],
                                                     bytes=p["bytes"]))
                 rec["ms"].append(p["ms"])
@@ -283,27 +402,25 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, dev)
-    total_samples = B * T * hop * world
+    total_samples = job.samples * world
     value = total_samples / (ms_max / 1e3)
 
-    # end to end through the host-buffer entry point: H2D of the latent, decode, D2H of the audio
-    lat_h = torch.from_numpy(wl.latent).pin_memory()
-    aud_h = torch.empty((B, 1, T * hop), dtype=torch.float32).pin_memory()
-    ws_h = voc.alloc_workspace(B, T, host_io=True)
+    # end to end through the host-buffer entry point: H2D of the input, the whole path, D2H
+    # of the output, inside the timed region
+    job.setup_host()
     for _ in range(max(1, args.warmup)):
-        V.vocoder_decode_host(voc.handle, lat_h, aud_h, ws_h, stream)
+        job.host_step(stream)
     e2e_s = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        V.vocoder_decode_host(voc.handle, lat_h, aud_h, ws_h, stream)
+        job.host_step(stream)
         e2e_s.append(time.perf_counter() - t0)
     e2e_t = max_over_ranks(statistics.mean(e2e_s), dev)
 
-    # per-kernel roofline: bf16x3 issues three bf16 MMAs per useful multiply-add
+    # per-kernel roofline: bf16x3 issues three bf16 MMAs per useful multiply-add, f16w two
+    # f16 MMAs (f16 and bf16 share the dense tensor rate)
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    # bf16x3 issues three bf16 MMAs per useful multiply-add, f16w two f16 MMAs (f16 and bf16
-    # share the dense tensor rate)
-    mmas_per_mac = 2.0 if f16w else 3.0
+    mmas_per_mac = 2.0 if one_plane else 3.0
     tc_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) / mmas_per_mac
     ridge = tc_peak * 1e12 / (hbm * 1e9)
     stages = []
@@ -320,45 +437,43 @@ def run_ours(args, rank, world, local_rank):
     dom = max(stages, key=lambda s: s["ms"])
     dom_rec = next(per_kernel[i] for i in per_kernel if per_kernel[i]["name"] == dom["name"])
     traffic = measured_traffic(args.workload, dom["name"])
+    per_launch = {"flops": dom_rec["flops"], "bytes": dom_rec["bytes"], "avg_ms": dom["ms"]}
     if dom["bound"] == "tensor":
         roof = {"bound": "tensor", "kernel": dom["name"], "achieved": dom["tflops"],
                 "peak": round(tc_peak, 1), "unit": "TFLOP/s", "frac": dom["frac"],
-                "traffic": traffic,
-                "per_launch": {"flops": dom_rec["flops"], "bytes": dom_rec["bytes"],
-                               "avg_ms": dom["ms"]},
-                "peak_note": (f"bf16 dense {peaks_kind} burst / 2 (two f16 MMAs per useful MAC)"
-                              if f16w else
+                "traffic": traffic, "per_launch": per_launch,
+                "peak_note": (f"bf16 dense {peaks_kind} burst / 2 (two {'f16' if f16w else 'bf16'} "
+                              f"MMAs per useful MAC)" if one_plane else
                               f"bf16 dense {peaks_kind} burst / 3 (three bf16 MMAs per useful MAC)")}
     else:
         roof = {"bound": "hbm", "kernel": dom["name"], "achieved": dom["gbs"], "peak": hbm,
-                "unit": "GB/s", "frac": dom["frac"], "traffic": traffic,
-                "per_launch": {"flops": dom_rec["flops"], "bytes": dom_rec["bytes"],
-                               "avg_ms": dom["ms"]},
+                "unit": "GB/s", "frac": dom["frac"], "traffic": traffic, "per_launch": per_launch,
                 "peak_note": f"HBM copy bandwidth ({peaks_kind})"}
 
     line = None
     if rank == 0:
-        rate = SAMPLE_RATE[args.workload]
-        tracks = tracks_per_batch(args.workload, B) * world
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        line = {"metric": metric_of(args.workload), "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": ("f16w (f16 weights, f16 hi/lo activations, fp32 accumulate)" if f16w
-                          else "bf16x3 (hi/lo split, fp32 accumulate)"), "data": "synthetic",
-                "x_realtime": tracks * T * hop / rate / (ms_max / 1e3),
-                "config": dict(config_of(wl, args.workload), precision=args.precision),
+                "dtype": {"f16w": "f16w (f16 weights, f16 hi/lo activations, fp32 accumulate)",
+                          "bf16w": "bf16w (bf16 weights, bf16 hi/lo activations, fp32 accumulate)",
+                          "bf16x3": "bf16x3 (hi/lo split, fp32 accumulate)"}[args.precision],
+                "data": "synthetic",
+                "x_realtime": realtime_seconds(wl, args.workload) * world / (ms_max / 1e3),
+                "config": dict(workload_config(wl, args.workload), precision=args.precision),
                 "e2e": {"value": total_samples / e2e_t, "unit": UNIT,
-                        "h2d_bytes_per_step": int(wl.latent.nbytes),
-                        "d2h_bytes_per_step": int(B * T * hop * 4),
+                        "h2d_bytes_per_step": job.h2d, "d2h_bytes_per_step": job.d2h,
                         "ms_per_step": e2e_t * 1e3},
                 "gpu_launches": launches * args.steps,
                 "roofline": roof,
                 "clocks": clk,
                 "stages": stages}
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(wl, args.workload, args.cpu_frames)
+            frames = args.cpu_frames if args.cpu_frames is not None else (
+                256 if is_encode(args.workload) else 689)
+            line["cpu_baseline"] = cpu_baseline(wl, args.workload, frames)
         print(json.dumps(line), flush=True)
-    voc.close()
+    job.close()
     return 0
 
 
@@ -368,15 +483,17 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="music_window", choices=sorted(W.WORKLOADS))
-    ap.add_argument("--cpu-frames", type=int, default=689,
-                    help="latent frames of one item the CPU baseline decodes (about 10 s on 16 cores)")
+    ap.add_argument("--workload", default="music_window",
+                    choices=sorted(W.WORKLOADS) + sorted(W.ENC_WORKLOADS))
+    ap.add_argument("--cpu-frames", type=int, default=None,
+                    help="latent frames of one item the CPU baseline decodes or encodes (about "
+                         "10 s on 16 cores; default 689 to decode, 256 to encode)")
     ap.add_argument("--ref-frames", type=int, default=48,
                     help="latent frames of one item per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--precision", choices=["bf16x3", "f16w"], default="bf16x3",
+    ap.add_argument("--precision", choices=["bf16x3", "f16w", "bf16w"], default="bf16x3",
                     help="bf16x3 (default): full fp32-equivalent inputs; f16w: the pages' F16 "
-                         "conv weights")
+                         "conv weights; bf16w: bfloat16 conv weights")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

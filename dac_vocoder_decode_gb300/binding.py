@@ -29,6 +29,7 @@ VOC_PAD_SYMMETRIC = 0
 VOC_PAD_CAUSAL = 1
 VOC_PREC_BF16X3 = 0
 VOC_PREC_F16W = 1
+VOC_PREC_BF16W = 2
 VOC_SNAKE = 0
 VOC_SNAKE_BETA = 1
 VOC_FLAG_CHECK_FINITE = 1
@@ -53,6 +54,7 @@ EXPORTED = [
     "vocoder_encode_wav",
     "vocoder_encoder_param_count", "vocoder_encoder_param_shape", "vocoder_encoder_create",
     "vocoder_encoder_hop", "vocoder_encoder_workspace_bytes", "vocoder_encode",
+    "vocoder_encoder_workspace_bytes_host", "vocoder_encode_host",
     "vocoder_encoder_launches", "vocoder_encoder_profile_count", "vocoder_encoder_profile_entry",
     "vocoder_encoder_last_error", "vocoder_encoder_destroy",
 ]
@@ -182,6 +184,11 @@ def load_library():
     lib.vocoder_encode.restype = I
     lib.vocoder_encode.argtypes = [P, P, I, ctypes.c_longlong, P, P, ctypes.c_size_t, P,
                                    ctypes.c_uint]
+    lib.vocoder_encoder_workspace_bytes_host.restype = ctypes.c_size_t
+    lib.vocoder_encoder_workspace_bytes_host.argtypes = [P, I, ctypes.c_longlong]
+    lib.vocoder_encode_host.restype = I
+    lib.vocoder_encode_host.argtypes = [P, P, I, ctypes.c_longlong, P, P, ctypes.c_size_t, P,
+                                        ctypes.c_uint]
     lib.vocoder_encoder_launches.restype = I
     lib.vocoder_encoder_launches.argtypes = [P]
     lib.vocoder_encoder_profile_count.restype = I
@@ -602,6 +609,19 @@ def vocoder_encoder_workspace_bytes(h, B: int, L: int) -> int:
     return int(load_library().vocoder_encoder_workspace_bytes(h, B, L))
 
 
+def vocoder_encoder_workspace_bytes_host(h, B: int, L: int) -> int:
+    return int(load_library().vocoder_encoder_workspace_bytes_host(h, B, L))
+
+
+def vocoder_encode_host(h, audio_host, latent_host, ws, stream=None, flags: int = 0) -> None:
+    """Host (ideally pinned) CPU tensors in and out; copies happen inside the library."""
+    B, _, L = audio_host.shape
+    _check_enc(load_library().vocoder_encode_host(h, ctypes.c_void_p(audio_host.data_ptr()), B, L,
+                                                  ctypes.c_void_p(latent_host.data_ptr()),
+                                                  ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                                  _stream_ptr(stream), flags), h)
+
+
 def vocoder_encoder_launches(h) -> int:
     return int(load_library().vocoder_encoder_launches(h))
 
@@ -655,9 +675,11 @@ class Encoder:
     def workspace_bytes(self, B: int, L: int) -> int:
         return vocoder_encoder_workspace_bytes(self.handle, B, L)
 
-    def alloc_workspace(self, B: int, L: int):
+    def alloc_workspace(self, B: int, L: int, host_io: bool = False):
         import torch
-        return torch.empty(self.workspace_bytes(B, L), dtype=torch.uint8, device="cuda")
+        n = (vocoder_encoder_workspace_bytes_host if host_io else vocoder_encoder_workspace_bytes)(
+            self.handle, B, L)
+        return torch.empty(n, dtype=torch.uint8, device="cuda")
 
     def encode(self, audio, ws=None, latent=None, stream=None, flags: int = 0):
         import torch

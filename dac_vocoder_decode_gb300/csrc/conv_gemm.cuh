@@ -76,6 +76,9 @@ enum : int {
   ERR_TIMEOUT_SKIP = 8,
 };
 
+// Weight forms of conv_gemm_kernel (the library's VOC_PREC_* values).
+constexpr int kPrecBf16x3 = 0, kPrecF16w = 1, kPrecBf16w = 2;
+
 struct ConvGemmArgs {
   int B, L_in, Cp_in;      // batch, input rows per item, padded input channels
   int KB, nkb, taps;       // channels per k-block, k-blocks, taps
@@ -99,8 +102,6 @@ struct ConvGemmArgs {
                            // 16-column chunks (phase pairs); G odd, by whole blocks with lane
                            // pairs (see convT_block_odd).  0: phase-major columns
                            // (n = phase * Cp_out + channel).
-  int split_s;             // 1, or S > 1: the hi/lo output is phase-split for a strided conv of
-                           // stride S (row t -> row t / S of plane chunk * S + t % S)
   int b2;                  // 1 (the kernel's B2 form): each weight chunk holds its hi rows then its lo rows, and a K
                            // step is two MMAs: A_hi x [W_hi | W_lo] into 2 N_tile accumulator
                            // columns, then A_lo x W_hi into the first N_tile; the epilogue adds
@@ -124,6 +125,9 @@ struct ConvGemmArgs {
   long long f32_elems, hl_elems, w_bytes;
   int smem_bytes, L_a, chunks_a, chunks_s;
   int *dbg;                // [4]: first failed check code and three values
+  int split_s;             // (kernels with SPLIT = true) S > 1: the hi/lo output is phase-split
+                           // for a strided conv of stride S (row t -> row t / S of plane
+                           // chunk * S + t % S); ignored by the other kernels
 };
 
 #ifdef VOC_CHECKS
@@ -342,7 +346,7 @@ __device__ __forceinline__ bool convT_block_odd(const ConvGemmArgs &p, volatile 
 
 // Epilogue of one warp for 32 rows (its TMEM lane quadrant) x CW columns
 // n0..n0+CW-1, which lie in one ConvT phase because CW divides C_out.
-template <int CW, bool B2 = false, bool F16 = false>
+template <int CW, bool B2 = false, bool F16 = false, bool SPLIT = false>
 __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t sslot,
                                                uint32_t sfull, uint32_t sempty, uint32_t sparity,
                                                volatile int *abort_flag, int row_in_tile,
@@ -463,10 +467,10 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
 #pragma unroll
     for (int i = 0; i < CW / 2; ++i) split_pair<F16>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
     const size_t L_out = static_cast<size_t>(p.hl_L);
-    if (p.split_s > 1) {
-      // Phase-split output for a strided conv of stride ss: row t goes to row t / ss of the
-      // plane (chunk * ss + t % ss), so that the strided conv reads its input as a 3-tap conv
-      // over ss * Cp_out channels (see the encoder in vocoder.cu).
+    if constexpr (SPLIT) {
+      // Phase-split output for a strided conv of stride ss = p.split_s (the encoder): row t
+      // goes to row t / ss of plane (chunk * ss + t % ss), so that the strided conv reads its
+      // input as a 3-tap conv over ss * Cp_out channels.
       const size_t ss = static_cast<size_t>(p.split_s);
       const size_t ph = row_t % ss, row = row_t / ss + p.hl_row0;
       const size_t half = ss * (p.Cp_out / 8);  // planes of the hi (and of the lo) parts
@@ -530,13 +534,20 @@ __device__ __forceinline__ void drain_ring_strided(uint64_t *full, int slots, in
 }
 
 // B2: the two-MMA K step (ConvGemmArgs::b2).  ODDT: a transposed conv with an odd number of
-// phases per group, stored by convT_block_odd.  F16: the F16-weight precision (f16 operands,
-// one weight plane, two MMAs per K step: A_hi x W and A_lo x W; f16 hi/lo outputs).  Separate
-// instantiations keep the common form's register budget.
-template <int CW, bool PAIR, bool B2 = false, bool ODDT = false, bool F16 = false>
+// phases per group, stored by convT_block_odd.  PREC: the weight form -- kPrecBf16x3 (bf16
+// hi/lo weight planes, three MMAs per K step, or two in the B2 form), or one weight plane and
+// two MMAs per K step (A_hi x W and A_lo x W): kPrecF16w (f16 operands and f16 hi/lo outputs)
+// or kPrecBf16w (bf16 operands and bf16 hi/lo outputs).  SPLIT:
+// the hi/lo output phase-split for a strided conv (ConvGemmArgs::split_s; the encoder's last
+// residual unit of each block).  Separate instantiations keep the common form's register budget
+// and instruction stream.
+template <int CW, bool PAIR, bool B2 = false, bool ODDT = false, int PREC = kPrecBf16x3,
+          bool SPLIT = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap tmapA,
                      const __grid_constant__ CUtensorMap tmapS, const ConvGemmArgs p) {
+  constexpr bool F16 = PREC == kPrecF16w;        // f16 operands (else bf16)
+  constexpr bool ONE = PREC != kPrecBf16x3;      // one weight plane, two MMAs per K step
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -788,7 +799,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
 #endif
             uint32_t a_hi = a0, b_hi = b_desc0 + sb * b_slot_step;
-            if constexpr (F16) {  // one f16 weight plane
+            if constexpr (ONE) {  // one weight plane
               for (int ks = 0; ks < nks; ++ks, a_hi += dA_k, b_hi += dB_k) {
                 mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi, desc_hi, idesc, accum);
                 mma_bf16_warp_lo<PAIR>(d_tmem, a_hi + dA_lo, b_hi, desc_hi, idesc, 1u);
@@ -973,7 +984,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       for (int c = half; c < n_chunks && ok && !odd_blocks; c += kEpiGroups) {
         const int slot = half * nsh + kslot;
-        ok = epilogue_chunk<CW, B2, F16>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
+        ok = epilogue_chunk<CW, B2, F16, SPLIT>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
                                 smem_u32(skipFull + slot), smem_u32(skipEmpty + slot), kph,
                                 abort_flag, row_in_tile, b, t, nt * p.N_tile + c * CW,
                                 tbase + c * CW, sbase, smem_u32(bars));

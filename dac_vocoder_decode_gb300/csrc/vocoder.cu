@@ -84,7 +84,7 @@ enum Buf { BUF_H0 = 0, BUF_H1 = 1, BUF_HB = 2, BUF_FY = 3, BUF_COUNT = 4 };
 struct Layer {
   std::string name;
   bool convT = false;
-  bool f16 = false;         // F16-weight precision: one f16 weight plane, f16 hi/lo operands
+  int prec = VOC_PREC_BF16X3;  // VOC_PREC_*: bf16 hi/lo weights, or one f16 / bf16 plane
   // strided conv of the encoder (stride down_s, k = 2 down_s, pad down_s / 2, down_c real
   // input channels), run as a 3-tap conv over the phase-split input: Cin = down_s * Cp(down_c)
   int down_s = 0, down_c = 0;
@@ -125,27 +125,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Conv kernel forms used for the precision PREC (voc::kPrec*): plain, odd-phase ConvT and
+// phase-split output; the bf16x3 precision also has the B2 forms and the CTA-pair kernel.
+template <int PREC>
+cudaError_t set_conv_attrs() {
+  auto set = [](auto kernel) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  };
+  cudaError_t st = set(voc::conv_gemm_kernel<16, false, false, false, PREC>);
+  if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, false, false, true, PREC>);
+  if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, false, false, false, PREC, true>);
+  if constexpr (PREC == voc::kPrecBf16x3) {
+    if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, false, true>);
+    if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, false, true, false, PREC, true>);
+    if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, true>);
+  }
+  return st;
+}
+
 bool set_kernel_attrs(std::string &why) {
   static cudaError_t st = cudaErrorUnknown;
   static std::once_flag once;
   std::call_once(once, [] {
-    st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (st == cudaSuccess)
-      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (st == cudaSuccess)
-      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false, false, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (st == cudaSuccess)
-      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false, false, false, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (st == cudaSuccess)
-      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, false, false, true, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (st == cudaSuccess)
-      st = cudaFuncSetAttribute(voc::conv_gemm_kernel<16, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    st = set_conv_attrs<voc::kPrecBf16x3>();
+    if (st == cudaSuccess) st = set_conv_attrs<voc::kPrecF16w>();
+    if (st == cudaSuccess) st = set_conv_attrs<voc::kPrecBf16w>();
     if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::ru_gemm_kernel<32>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
@@ -177,7 +181,7 @@ struct vocoder {
   long long wait_budget = kWaitBudget;
   int fuse_max_c = 0;       // residual units of up to this many (padded) channels run fused
   bool use_pair = true;     // conv layers on CTA pairs
-  bool f16 = false;         // VOC_PREC_F16W: f16 weights, f16 hi/lo activations
+  int prec = VOC_PREC_BF16X3;  // VOC_PREC_*: the weight form of every conv
   // TMA descriptors for the last (workspace, B, T)
   void *map_ws = nullptr;
   int map_B = -1, map_T = -1;
@@ -298,7 +302,8 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   // pairs) fits beside the A ring and the residual slots, it is loaded once and kept; the
   // k-block is then the largest that leaves three A stages (else two) and at least
   // kMinAInFlight bytes of A in flight (the 1x1 convs wait on their A loads otherwise).
-  const int wb = L.f16 ? 2 : 4;  // weight bytes per (channel, column): f16, or bf16 hi + lo
+  // weight bytes per (channel, column): one f16 or bf16 value, or bf16 hi + lo
+  const int wb = L.prec != VOC_PREC_BF16X3 ? 2 : 4;
   const int w_tile = wb * L.Cp_in * n_stage * g.taps;
   for (int min_na = 3; min_na >= 2 && !g.KB && g.n_tiles <= kMaxResidentTiles; --min_na)
     for (int kb = L.Cp_in - L.Cp_in % 16; kb >= 16 && !g.KB; kb -= 16) {
@@ -349,7 +354,7 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   // Two MMAs per K step where the doubled column count fits one MMA (N <= 256): narrow
   // layers issue a third fewer MMA instructions, whose rate limits them.
   // (not with the odd-phase ConvT epilogue, which has its own kernel form)
-  g.b2 = (!L.pair && !L.f16 && 2 * g.N_tile <= 256 && !(L.convT && (g.phase_group & 1))) ? 1 : 0;
+  g.b2 = (!L.pair && L.prec == VOC_PREC_BF16X3 && 2 * g.N_tile <= 256 && !(L.convT && (g.phase_group & 1))) ? 1 : 0;
   int ac = 32;
   while (ac < (g.b2 ? 2 * g.N_tile : g.N_tile)) ac *= 2;
   g.acc_cols = ac;
@@ -507,7 +512,7 @@ std::vector<uint16_t> pack_weights(const Layer &L, int padding, const float *w) 
   const ConvGemmArgs &g = L.g;
   const int pw = L.pair ? g.N_tile / 2 : g.N_tile;
   const int n_pt = g.N_total / pw;
-  const size_t tile = (size_t)(L.f16 ? 1 : 2) * g.KB * pw;
+  const size_t tile = (size_t)(L.prec != VOC_PREC_BF16X3 ? 1 : 2) * g.KB * pw;
   std::vector<uint16_t> out((size_t)n_pt * g.taps * g.nkb * tile);
   for (int nt = 0; nt < n_pt; ++nt)
     for (int tap = 0; tap < g.taps; ++tap)
@@ -517,8 +522,10 @@ std::vector<uint16_t> pack_weights(const Layer &L, int padding, const float *w) 
           for (int n = 0; n < pw; ++n)
             for (int e = 0; e < 8; ++e) {
               const float v = weight_value(L, padding, w, nt * pw + n, kb * g.KB + c * 8 + e, tap);
-              if (L.f16) {  // one plane of f16 weights, rounded to nearest even
-                base[((size_t)c * pw + n) * 8 + e] = __half_as_ushort(__float2half_rn(v));
+              if (L.prec != VOC_PREC_BF16X3) {  // one plane of f16 / bf16 weights (nearest even)
+                base[((size_t)c * pw + n) * 8 + e] = L.prec == VOC_PREC_F16W
+                                                         ? __half_as_ushort(__float2half_rn(v))
+                                                         : f2bf(v);
                 continue;
               }
               const uint16_t hi = f2bf(v);
@@ -646,9 +653,11 @@ bool check_desc(const voc_desc *d, std::string &why) {
   if (d->out_channels != 1) return why = "out_channels must be 1", false;
   if (d->in_proj_channels < 0 || d->in_proj_channels > 8192) return why = "in_proj_channels", false;
   if (d->padding != VOC_PAD_SYMMETRIC && d->padding != VOC_PAD_CAUSAL) return why = "padding", false;
-  if (d->precision != VOC_PREC_BF16X3 && d->precision != VOC_PREC_F16W) return why = "precision", false;
-  if (d->precision == VOC_PREC_F16W && d->cta_pair > 0)
-    return why = "cta_pair is not available with VOC_PREC_F16W", false;
+  if (d->precision != VOC_PREC_BF16X3 && d->precision != VOC_PREC_F16W &&
+      d->precision != VOC_PREC_BF16W)
+    return why = "precision", false;
+  if (d->precision != VOC_PREC_BF16X3 && d->cta_pair > 0)
+    return why = "cta_pair is available with VOC_PREC_BF16X3 only", false;
   if (d->cta_pair < -1 || d->cta_pair > 1) return why = "cta_pair must be -1, 0 or 1", false;
   if (d->snake != VOC_SNAKE && d->snake != VOC_SNAKE_BETA) return why = "snake", false;
   for (int i = 0; i < d->n_stages; ++i) {
@@ -817,6 +826,29 @@ void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops,
   bytes = by;
 }
 
+// One launch of the single-CTA conv kernel of precision PREC in the form the layer needs.
+template <int PREC>
+cudaError_t launch_conv(const Layer &L, const ConvGemmArgs &a, int grid, const CUtensorMap &map,
+                        const CUtensorMap &smap, cudaStream_t stream) {
+  const dim3 g(grid), blk(voc::kGemmThreads);
+  constexpr bool kB2 = PREC == voc::kPrecBf16x3;  // the B2 form exists for bf16x3 only
+  if (a.split_s > 1) {  // phase-split hi/lo output
+    if (kB2 && L.g.b2)
+      return launch_pdl(voc::conv_gemm_kernel<16, false, kB2, false, PREC, true>, g, blk, L.smem,
+                        stream, map, smap, a);
+    return launch_pdl(voc::conv_gemm_kernel<16, false, false, false, PREC, true>, g, blk, L.smem,
+                      stream, map, smap, a);
+  }
+  if (L.convT && (L.g.phase_group & 1))
+    return launch_pdl(voc::conv_gemm_kernel<16, false, false, true, PREC>, g, blk, L.smem, stream,
+                      map, smap, a);
+  if (kB2 && L.g.b2)
+    return launch_pdl(voc::conv_gemm_kernel<16, false, kB2, false, PREC>, g, blk, L.smem, stream,
+                      map, smap, a);
+  return launch_pdl(voc::conv_gemm_kernel<16, false, false, false, PREC>, g, blk, L.smem, stream,
+                    map, smap, a);
+}
+
 voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
                        const CUtensorMap &smap, const ConvGemmArgs &a, cudaStream_t stream) {
   const long long tiles = (long long)a.B * a.m_tiles * a.n_tiles;
@@ -826,6 +858,8 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
     if (tiles <= units) return tiles;
     return a.b_resident ? units - units % a.n_tiles : units;
   };
+  if (a.split_s > 1 && (L.pair || L.convT || L.ru))
+    return fail(ctx, VOC_UNSUPPORTED, L.name + ": a phase-split output needs a plain conv kernel");
   if (L.pair) {  // persistent grid of 2-CTA clusters, at most as many as can be resident
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -853,22 +887,12 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
     else
       e = launch_pdl(voc::ru_gemm_kernel<16>, dim3(grid), dim3(voc::kRuThreads), L.smem, stream,
                      map, smap, a, L.rx);
-  } else if (L.f16) {
-    if (L.convT && (L.g.phase_group & 1))
-      e = launch_pdl(voc::conv_gemm_kernel<16, false, false, true, true>, dim3(grid),
-                     dim3(voc::kGemmThreads), L.smem, stream, map, smap, a);
-    else
-      e = launch_pdl(voc::conv_gemm_kernel<16, false, false, false, true>, dim3(grid),
-                     dim3(voc::kGemmThreads), L.smem, stream, map, smap, a);
-  } else if (L.g.b2) {
-    e = launch_pdl(voc::conv_gemm_kernel<16, false, true>, dim3(grid), dim3(voc::kGemmThreads),
-                   L.smem, stream, map, smap, a);
-  } else if (L.convT && (L.g.phase_group & 1)) {
-    e = launch_pdl(voc::conv_gemm_kernel<16, false, false, true>, dim3(grid),
-                   dim3(voc::kGemmThreads), L.smem, stream, map, smap, a);
+  } else if (L.prec == VOC_PREC_F16W) {
+    e = launch_conv<voc::kPrecF16w>(L, a, grid, map, smap, stream);
+  } else if (L.prec == VOC_PREC_BF16W) {
+    e = launch_conv<voc::kPrecBf16w>(L, a, grid, map, smap, stream);
   } else {
-    e = launch_pdl(voc::conv_gemm_kernel<16, false>, dim3(grid), dim3(voc::kGemmThreads), L.smem,
-                   stream, map, smap, a);
+    e = launch_conv<voc::kPrecBf16x3>(L, a, grid, map, smap, stream);
   }
   if (e != cudaSuccess) return cuda_fail(ctx, e, ("launch " + L.name).c_str());
   return VOC_OK;
@@ -908,7 +932,7 @@ voc_status launch_prep(vocoder *ctx, const float *x, int B, int C, int T, int Cp
   dim3 grid((T_pad + 255) / 256, Cp / 8, B);
   cudaError_t e = launch_pdl(voc::prep_hl_kernel, grid, dim3(256), 0, stream, x, C, T, T_pad, Cp,
                              alpha, invb, hl, row0, Lp < 0 ? (long long)T_pad : Lp,
-                             ctx->f16 ? 1 : 0);
+                             ctx->prec == VOC_PREC_F16W ? 1 : 0);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch prep");
   return VOC_OK;
 }
@@ -1042,8 +1066,8 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
   ctx->fuse_max_c = desc->fuse_max_channels == 0 ? kFuseDefault
                     : (desc->fuse_max_channels < 0 ? 0 : desc->fuse_max_channels);
   ctx->use_pair = desc->cta_pair > 0;
-  ctx->f16 = desc->precision == VOC_PREC_F16W;
-  if (ctx->f16) ctx->fuse_max_c = 0;  // the fused unit exists in the bf16x3 form only
+  ctx->prec = desc->precision;
+  if (ctx->prec != VOC_PREC_BF16X3) ctx->fuse_max_c = 0;  // the fused unit is bf16x3 only
   auto bail = [&](voc_status st) {
     g_err = ctx->err;
     vocoder_destroy(ctx);
@@ -1066,7 +1090,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
 
   const int pad = desc->padding;
   auto plan = [&](Layer &L, bool has_skip) {
-    L.f16 = ctx->f16;
+    L.prec = ctx->prec;
     return plan_layer(ctx->use_pair, L, pad, has_skip, why);
   };
   const int nd = desc->n_dilations;
@@ -1201,10 +1225,12 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     h.pad_left = (pad == VOC_PAD_CAUSAL) ? h.K - 1 : (h.K - 1) / 2;
     h.level = desc->n_stages;
     const float *w_in = params[p + 1], *b = params[p + 2];
-    // F16-weight precision: the head's weights are rounded to f16 like every conv weight
+    // F16 / BF16-weight precision: the head's weights are rounded like every conv weight
     std::vector<float> w((size_t)C * h.K);
     for (size_t i = 0; i < w.size(); ++i)
-      w[i] = ctx->f16 ? __half2float(__float2half_rn(w_in[i])) : w_in[i];
+      w[i] = ctx->prec == VOC_PREC_F16W    ? __half2float(__float2half_rn(w_in[i]))
+             : ctx->prec == VOC_PREC_BF16W ? bf2f(f2bf(w_in[i]))
+                                           : w_in[i];
     std::vector<float> wp((size_t)h.Cp * h.K, 0.f), bp(1, b ? b[0] : 0.f);
     for (int c = 0; c < C; ++c)
       for (int k = 0; k < h.K; ++k) wp[(size_t)c * h.K + k] = w[(size_t)c * h.K + k];
@@ -2123,7 +2149,9 @@ bool check_enc_desc(const voc_enc_desc *d, std::string &why) {
   if (d->n_stages < 1 || d->n_stages > 8) return why = "n_stages", false;
   if (!d->strides || !d->widths) return why = "strides / widths NULL", false;
   if (d->n_dilations < 1 || d->n_dilations > 4 || !d->dilations) return why = "dilations", false;
-  if (d->precision != VOC_PREC_BF16X3 && d->precision != VOC_PREC_F16W) return why = "precision", false;
+  if (d->precision != VOC_PREC_BF16X3 && d->precision != VOC_PREC_F16W &&
+      d->precision != VOC_PREC_BF16W)
+    return why = "precision", false;
   if (d->snake != VOC_SNAKE && d->snake != VOC_SNAKE_BETA) return why = "snake", false;
   for (int i = 0; i < d->n_stages; ++i) {
     if (d->strides[i] < 1 || d->strides[i] > 16) return why = "stride out of [1, 16]", false;
@@ -2281,7 +2309,7 @@ VOC_API voc_status vocoder_encoder_create(const voc_enc_desc *desc, const float 
   for (int s : enc->strides) enc->hop *= s;
   enc->Cp_audio = rup(desc->in_channels, 16);
   enc->Cp_lat = rup(desc->latent_channels, 16);
-  ctx->f16 = desc->precision == VOC_PREC_F16W;
+  ctx->prec = desc->precision;
   ctx->use_pair = false;
   ctx->fuse_max_c = 0;
   auto bail = [&](voc_status st) {
@@ -2295,7 +2323,7 @@ VOC_API voc_status vocoder_encoder_create(const voc_enc_desc *desc, const float 
   const int pad = VOC_PAD_SYMMETRIC;
   auto add = [&](Layer &L, bool has_skip, const float *w, const float *b, const SnakeCoef &sn,
                  long long div, int split) {
-    L.f16 = ctx->f16;
+    L.prec = ctx->prec;
     if (!plan_layer(false, L, pad, has_skip, why))
       return fail(ctx, VOC_UNSUPPORTED, L.name + ": " + why);
     const voc_status s = upload_layer(ctx, ctx->allocs, L, pad, w, b, sn);
@@ -2543,4 +2571,43 @@ VOC_API voc_status vocoder_encoder_profile_entry(vocoder_encoder *enc, int index
 
 VOC_API const char *vocoder_encoder_last_error(const vocoder_encoder *enc) {
   return enc ? enc->core.err.c_str() : g_err.c_str();
+}
+
+VOC_API size_t vocoder_encoder_workspace_bytes_host(const vocoder_encoder *enc, int B, long long L) {
+  const size_t w = vocoder_encoder_workspace_bytes(enc, B, L);
+  if (!w) return 0;
+  return w + rupz((size_t)B * enc->desc.in_channels * (size_t)L * 4, 256) +
+         rupz((size_t)B * enc->desc.latent_channels * (size_t)(L / enc->hop) * 4, 256);
+}
+
+VOC_API voc_status vocoder_encode_host(vocoder_encoder *enc, const float *audio_host, int B,
+                                       long long L, float *latent_host, void *ws_dev,
+                                       size_t ws_bytes, voc_stream_t stream, unsigned flags) {
+  if (!enc) return fail(nullptr, VOC_INVALID_ARG, "encoder is NULL");
+  vocoder *ctx = &enc->core;
+  if (!audio_host || !latent_host) return fail(ctx, VOC_INVALID_ARG, "audio / latent NULL");
+  const size_t need = vocoder_encoder_workspace_bytes_host(enc, B, L);
+  if (!need)
+    return fail(ctx, VOC_INVALID_ARG, "B must be in [1, 65535] and L a positive multiple of the hop");
+  if (!ws_dev || (reinterpret_cast<uintptr_t>(ws_dev) & 255))
+    return fail(ctx, VOC_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+  if (ws_bytes < need)
+    return fail(ctx, VOC_WORKSPACE_TOO_SMALL,
+                "workspace " + std::to_string(ws_bytes) + " < " + std::to_string(need));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t wenc = vocoder_encoder_workspace_bytes(enc, B, L);
+  const size_t in_bytes = (size_t)B * enc->desc.in_channels * (size_t)L * 4;
+  const size_t out_bytes = (size_t)B * enc->desc.latent_channels * (size_t)(L / enc->hop) * 4;
+  uint8_t *base = static_cast<uint8_t *>(ws_dev);
+  float *aud_d = reinterpret_cast<float *>(base + wenc);
+  float *lat_d = reinterpret_cast<float *>(base + wenc + rupz(in_bytes, 256));
+  cudaError_t e = cudaMemcpyAsync(aud_d, audio_host, in_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "copy audio in");
+  voc_status st = vocoder_encode(enc, aud_d, B, L, lat_d, ws_dev, wenc, stream, flags);
+  if (st != VOC_OK) return st;
+  e = cudaMemcpyAsync(latent_host, lat_d, out_bytes, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "copy latent out");
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+  return VOC_OK;
 }

@@ -341,6 +341,19 @@ def make_encode_workload(arch: EncArch, B: int, frames: int, seed: int,
     return Workload(name=f"encode{seed}", arch=arch, latent=audio, params=params)
 
 
+# Encoder workloads: (arch, B, frames, seed, description); audio of frames * hop samples.
+ENC_WORKLOADS = {
+    "encode_music_window": (ENC_MUSIC, 2, 689, 21,
+                            "music encoder, one stereo 689-frame window: audio [2,1,352768] -> "
+                            "latent [2,64,689]"),
+}
+
+
+def make_named_encode_workload(name: str, frames: Optional[int] = None) -> Workload:
+    arch, B, fr, seed, _desc = ENC_WORKLOADS[name]
+    return make_encode_workload(arch, B, frames or fr, seed)
+
+
 def slice_latent(latent: np.ndarray, t0: int, t1: int) -> np.ndarray:
     """Frames [t0, t1) of a latent (a copy), for receptive-field sampled checks."""
     return np.ascontiguousarray(latent[:, :, t0:t1])

@@ -70,8 +70,12 @@ enum { VOC_PAD_SYMMETRIC = 0, VOC_PAD_CAUSAL = 1 };
  * port stores them (minimaxmusic.cpp Architecture, "Flow VAE": conv weights F16 on the
  * device with F32 activations); activations as f16 hi/lo pairs (about 22 significant bits,
  * |x| < 65504), two f16 products per multiply, fp32 accumulation.  Biases and Snake
- * parameters stay fp32.  VOC_PREC_F16W runs neither fused residual units nor CTA pairs. */
-enum { VOC_PREC_BF16X3 = 0, VOC_PREC_F16W = 1 };
+ * parameters stay fp32.  VOC_PREC_BF16W (ABI 5, added with the encoder) -- every
+ * convolution weight rounded to bfloat16 (8 significant bits), the precision checkpoints
+ * are commonly distributed in; activations as bf16 hi/lo pairs, two bf16 products per
+ * multiply, fp32 accumulation.  The one-plane precisions (F16W, BF16W) run neither fused
+ * residual units nor CTA pairs. */
+enum { VOC_PREC_BF16X3 = 0, VOC_PREC_F16W = 1, VOC_PREC_BF16W = 2 };
 /* activation: Snake with alpha as stored, or SnakeBeta with log-scale alpha and beta,
  * x + sin^2(e^alpha x) / (e^beta + 1e-9) (qwentts.cpp Architecture, "Audio tokenizer
  * decoder": exp applied to both stored parameters) */
@@ -400,6 +404,15 @@ size_t vocoder_encoder_workspace_bytes(const vocoder_encoder_t *enc, int B, long
 voc_status vocoder_encode(vocoder_encoder_t *enc, const float *audio_dev, int B, long long L,
                           float *latent_dev, void *ws_dev, size_t ws_bytes, voc_stream_t stream,
                           unsigned flags);
+
+/* Same encode from and to HOST buffers: copies the audio in, encodes, copies the latent
+ * out and synchronises `stream` before returning.  ws_bytes >=
+ * vocoder_encoder_workspace_bytes_host(enc, B, L) (the device workspace plus room for the
+ * staging copies).  Page-locked host buffers give asynchronous copies. */
+size_t vocoder_encoder_workspace_bytes_host(const vocoder_encoder_t *enc, int B, long long L);
+voc_status vocoder_encode_host(vocoder_encoder_t *enc, const float *audio_host, int B,
+                               long long L, float *latent_host, void *ws_dev, size_t ws_bytes,
+                               voc_stream_t stream, unsigned flags);
 
 /* Kernel launches of one vocoder_encode. */
 int vocoder_encoder_launches(const vocoder_encoder_t *enc);

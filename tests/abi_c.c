@@ -88,6 +88,47 @@ int main(void) {
   CHECK(vocoder_profile_entry((vocoder_t *)0, 0, (const char **)0, (double *)0, (double *)0,
                               (double *)0) == VOC_INVALID_ARG);
   vocoder_destroy((vocoder_t *)0);
+  {  /* the mirror encoder: music layout 1 -> 64, strides 2, 4, 8, 8, widths up to 1024 */
+    int es[4] = {2, 4, 8, 8};
+    int ew[4] = {128, 256, 512, 1024};
+    vocoder_encoder_t *enc = (vocoder_encoder_t *)0;
+    voc_enc_desc e;
+    memset(&e, 0, sizeof e);
+    e.abi_version = VOC_ABI_VERSION;
+    e.in_channels = 1;
+    e.channels0 = 64;
+    e.in_kernel = 7;
+    e.n_stages = 4;
+    e.strides = es;
+    e.widths = ew;
+    e.n_dilations = 3;
+    e.dilations = dils;
+    e.res_kernel = 7;
+    e.out_kernel = 3;
+    e.latent_channels = 64;
+    e.precision = VOC_PREC_BF16W;
+    e.snake = VOC_SNAKE;
+    CHECK(vocoder_encoder_param_count(&e) == 2 + 4 * 21 + 5);
+    CHECK(vocoder_encoder_param_shape(&e, 2 + 18 + 1, dims, &nd) == VOC_OK);  /* block 0 down.w */
+    CHECK(nd == 3 && dims[0] == 128 && dims[1] == 64 && dims[2] == 4);
+    CHECK(vocoder_encoder_create(&e, (const float *const *)0, 91, &enc) == VOC_INVALID_ARG);
+    CHECK(enc == (vocoder_encoder_t *)0);
+    CHECK(strlen(vocoder_encoder_last_error((const vocoder_encoder_t *)0)) > 0);
+    CHECK(vocoder_encoder_hop((const vocoder_encoder_t *)0) == -1);
+    CHECK(vocoder_encoder_workspace_bytes((const vocoder_encoder_t *)0, 1, 512) == 0);
+    CHECK(vocoder_encoder_workspace_bytes_host((const vocoder_encoder_t *)0, 1, 512) == 0);
+    CHECK(vocoder_encode((vocoder_encoder_t *)0, (const float *)0, 1, 512, (float *)0, (void *)0,
+                         0, (voc_stream_t)0, 0) == VOC_INVALID_ARG);
+    CHECK(vocoder_encode_host((vocoder_encoder_t *)0, (const float *)0, 1, 512, (float *)0,
+                              (void *)0, 0, (voc_stream_t)0, 0) == VOC_INVALID_ARG);
+    CHECK(vocoder_encoder_launches((const vocoder_encoder_t *)0) == -1);
+    CHECK(vocoder_encoder_profile_count((const vocoder_encoder_t *)0) == 0);
+    CHECK(vocoder_encoder_profile_entry((vocoder_encoder_t *)0, 0, (const char **)0, (double *)0,
+                                        (double *)0, (double *)0) == VOC_INVALID_ARG);
+    e.strides = (const int *)0;
+    CHECK(vocoder_encoder_param_count(&e) == -1);
+    vocoder_encoder_destroy((vocoder_encoder_t *)0);
+  }
   printf("abi_c ok\n");
   return 0;
 }

@@ -124,13 +124,19 @@ def test_create_validates_before_device_work(lib):
 
 
 def test_precision_field_validation(lib):
-    """VOC_PREC_F16W is a valid precision (same parameter list); unknown precisions and the
-    F16-weight precision with CTA pairs are rejected before any device work."""
+    """VOC_PREC_F16W and VOC_PREC_BF16W are valid precisions (same parameter list); unknown
+    precisions and the one-plane precisions with CTA pairs are rejected before any device
+    work."""
     n = V.vocoder_param_count(W.TINY)
     d = V.make_desc(W.TINY, precision=V.VOC_PREC_F16W)
     assert lib.vocoder_param_count(ctypes.byref(d)) == n
-    d = V.make_desc(W.TINY, precision=2)
+    d = V.make_desc(W.TINY, precision=V.VOC_PREC_BF16W)
+    assert lib.vocoder_param_count(ctypes.byref(d)) == n
+    d = V.make_desc(W.TINY, precision=3)
     assert lib.vocoder_param_count(ctypes.byref(d)) == -1
+    with pytest.raises(V.VocoderError) as e:
+        V.vocoder_create(W.TINY, [None] * n, cta_pair=1, precision=V.VOC_PREC_BF16W)
+    assert e.value.status == V.VOC_INVALID_ARG
     with pytest.raises(V.VocoderError) as e:
         V.vocoder_create(W.TINY, [None] * n, cta_pair=1, precision=V.VOC_PREC_F16W)
     assert e.value.status == V.VOC_INVALID_ARG
@@ -161,7 +167,7 @@ def test_encoder_create_validates_before_device_work(lib):
     with pytest.raises(V.VocoderError) as e:
         V.vocoder_encoder_create(bad, [None] * n)
     assert e.value.status == V.VOC_INVALID_ARG
-    d = V.make_enc_desc(W.ENC_MUSIC, precision=2)
+    d = V.make_enc_desc(W.ENC_MUSIC, precision=3)
     assert lib.vocoder_encoder_param_count(ctypes.byref(d)) == -1
     # a weight is required (only biases may be NULL): rejected before any device call
     with pytest.raises(V.VocoderError) as e:

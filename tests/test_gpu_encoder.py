@@ -143,7 +143,9 @@ MUSIC_WINDOW_FRAMES = 689  # one decode window of the music pipeline: [2, 1, 689
 
 @functools.lru_cache(maxsize=1)
 def music_window():
-    return W.make_encode_workload(W.ENC_MUSIC, 2, MUSIC_WINDOW_FRAMES, 21)
+    wl = W.make_named_encode_workload("encode_music_window")  # the bench's encoder workload
+    assert wl.latent.shape == (2, 1, MUSIC_WINDOW_FRAMES * W.ENC_MUSIC.hop)
+    return wl
 
 
 def test_music_window_sampled_frames():
@@ -165,3 +167,18 @@ def test_music_window_sampled_frames():
         piece = np.ascontiguousarray(wl.latent[item:item + 1, :, f0 * hop:f1 * hop])
         ref = O.encode(arch, None, piece, folded=folded)[0, :, a - f0:b - f0]
         compare(ref, got[item, :, a:b], f"item {item} frames [{a}, {b})")
+
+
+def test_encode_host_matches_device_encode():
+    """vocoder_encode_host (pinned host buffers, copies inside the call) gives the device
+    entry point's latents bit for bit."""
+    arch, B, frames, seed = CASES["odd_strides"]
+    wl = W.make_encode_workload(arch, B, frames, seed)
+    enc = V.Encoder(arch, V.fold_params(wl.params))
+    z_dev = gpu_encode(enc, wl.latent)
+    audio_h = torch.from_numpy(wl.latent).pin_memory()
+    z_h = torch.empty((B, arch.latent_channels, frames), dtype=torch.float32).pin_memory()
+    ws = enc.alloc_workspace(B, audio_h.shape[2], host_io=True)
+    V.vocoder_encode_host(enc.handle, audio_h, z_h, ws)
+    assert np.array_equal(z_h.numpy().astype(np.float64), z_dev)
+    enc.close()

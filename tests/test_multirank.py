@@ -69,3 +69,10 @@ def test_every_workload_has_a_sample_rate_and_config():
         wl = W.make_workload(name, T=2, B=1)
         cfg = bench.config_of(wl, name)
         assert cfg["sample_rate"] == bench.SAMPLE_RATE[name]
+    for name in W.ENC_WORKLOADS:  # encoder workloads: audio in, latents out
+        assert name in bench.SAMPLE_RATE, name
+        wl = bench.load_workload(name, frames=2)
+        cfg = bench.workload_config(wl, name)
+        assert cfg["sample_rate"] == bench.SAMPLE_RATE[name]
+        assert cfg["latent"][2] * cfg["hop"] == cfg["audio"][2]
+        assert bench.metric_of(name) == bench.ENC_METRIC
