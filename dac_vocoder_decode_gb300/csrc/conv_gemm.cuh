@@ -125,10 +125,24 @@ struct ConvGemmArgs {
   long long f32_elems, hl_elems, w_bytes;
   int smem_bytes, L_a, chunks_a, chunks_s;
   int *dbg;                // [4]: first failed check code and three values
-  int split_s;             // (kernels with SPLIT = true) S > 1: the hi/lo output is phase-split
-                           // for a strided conv of stride S (row t -> row t / S of plane
-                           // chunk * S + t % S); ignored by the other kernels
+  // Encoder forms (kernels with ENC = true; ignored by the others):
+  int split_s;             // S > 1: the hi/lo output is phase-split for a strided conv of
+                           // stride S (see phase_plane)
+  int kb_split;            // k-blocks kb < kb_split use taps [tap_lo0, tap_hi0), the others
+  int tap_lo0, tap_hi0, tap_lo1, tap_hi1;  // [tap_lo1, tap_hi1) (a strided conv's two
+                                           // phase groups each read two of its three taps)
 };
+
+// Plane (8-channel group) of channel chunk `ch`, phase `ph` in the phase-split layout of a
+// strided conv's input with stride ss over cpc chunks: the phases r < R0 = ceil(ss/2) come
+// first (plane ch * R0 + r), then the phases r >= R0 (plane R0 cpc + ch (ss - R0) + r - R0).
+// Phases r < R0 read input row shifts {0, +1} of the conv's three taps, the others {-1, 0},
+// so each group's k-blocks skip one tap.
+__host__ __device__ __forceinline__ size_t phase_plane(size_t ch, size_t ph, size_t ss,
+                                                       size_t cpc) {
+  const size_t r0 = (ss + 1) / 2;
+  return ph < r0 ? ch * r0 + ph : r0 * cpc + ch * (ss - r0) + (ph - r0);
+}
 
 #ifdef VOC_CHECKS
 // Record the first failed check (code, three values), raise the abort flag; the caller skips
@@ -346,7 +360,7 @@ __device__ __forceinline__ bool convT_block_odd(const ConvGemmArgs &p, volatile 
 
 // Epilogue of one warp for 32 rows (its TMEM lane quadrant) x CW columns
 // n0..n0+CW-1, which lie in one ConvT phase because CW divides C_out.
-template <int CW, bool B2 = false, bool F16 = false, bool SPLIT = false>
+template <int CW, bool B2 = false, bool F16 = false, bool ENC = false>
 __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t sslot,
                                                uint32_t sfull, uint32_t sempty, uint32_t sparity,
                                                volatile int *abort_flag, int row_in_tile,
@@ -467,19 +481,20 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
 #pragma unroll
     for (int i = 0; i < CW / 2; ++i) split_pair<F16>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
     const size_t L_out = static_cast<size_t>(p.hl_L);
-    if constexpr (SPLIT) {
-      // Phase-split output for a strided conv of stride ss = p.split_s (the encoder): row t
-      // goes to row t / ss of plane (chunk * ss + t % ss), so that the strided conv reads its
-      // input as a 3-tap conv over ss * Cp_out channels.
-      const size_t ss = static_cast<size_t>(p.split_s);
+    if constexpr (ENC) {
+      // Phase-split output for a strided conv of stride ss = split_s (ss = 1: the plain
+      // layout): row t goes to row t / ss of plane phase_plane(chunk, t % ss), so that the
+      // strided conv reads its input as a 3-tap conv over ss * Cp_out channels.
+      const size_t ss = static_cast<size_t>(p.split_s > 1 ? p.split_s : 1);
       const size_t ph = row_t % ss, row = row_t / ss + p.hl_row0;
-      const size_t half = ss * (p.Cp_out / 8);  // planes of the hi (and of the lo) parts
+      const size_t cpc = p.Cp_out / 8;
+      const size_t half = ss * cpc;  // planes of the hi (and of the lo) parts
       const size_t item = (size_t)b * 2 * half;
-      VOC_CHECK((((long long)(item + half + (co0 / 8 + CW / 8 - 1) * ss + ph)) * (long long)L_out + row) * 8 + 8 <=
-                    p.hl_elems, 20, b, co0, row);
 #pragma unroll
       for (int j = 0; j < CW / 8; ++j) {
-        const size_t plane = (co0 / 8 + j) * ss + ph;
+        const size_t plane = phase_plane(co0 / 8 + j, ph, ss, cpc);
+        VOC_CHECK(((long long)(item + half + plane) * (long long)L_out + row) * 8 + 8 <= p.hl_elems,
+                  20, b, co0, row);
         *reinterpret_cast<uint4 *>(p.out_hl + ((item + plane) * L_out + row) * 8) =
             make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
         *reinterpret_cast<uint4 *>(p.out_hl + ((item + half + plane) * L_out + row) * 8) =
@@ -502,6 +517,13 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
     }
   }
   return true;
+}
+
+// Taps [tap0, tap1) that k-block kb reads (the encoder's strided convs skip one of three).
+__device__ __forceinline__ void tap_window(const ConvGemmArgs &p, int kb, int &tap0, int &tap1) {
+  const bool second = kb >= p.kb_split;
+  tap0 = second ? p.tap_lo1 : p.tap_lo0;
+  tap1 = second ? p.tap_hi1 : p.tap_hi0;
 }
 
 // Wait (bounded) until every fill issued into a ring of `slots` barriers has
@@ -537,12 +559,12 @@ __device__ __forceinline__ void drain_ring_strided(uint64_t *full, int slots, in
 // phases per group, stored by convT_block_odd.  PREC: the weight form -- kPrecBf16x3 (bf16
 // hi/lo weight planes, three MMAs per K step, or two in the B2 form), or one weight plane and
 // two MMAs per K step (A_hi x W and A_lo x W): kPrecF16w (f16 operands and f16 hi/lo outputs)
-// or kPrecBf16w (bf16 operands and bf16 hi/lo outputs).  SPLIT:
-// the hi/lo output phase-split for a strided conv (ConvGemmArgs::split_s; the encoder's last
-// residual unit of each block).  Separate instantiations keep the common form's register budget
+// or kPrecBf16w (bf16 operands and bf16 hi/lo outputs).  ENC: the encoder's forms -- a
+// phase-split hi/lo output for a strided conv (ConvGemmArgs::split_s; the last residual unit
+// of each block) and per-k-block tap windows (kb_split, tap_lo*, tap_hi*; the strided conv).  Separate instantiations keep the common form's register budget
 // and instruction stream.
 template <int CW, bool PAIR, bool B2 = false, bool ODDT = false, int PREC = kPrecBf16x3,
-          bool SPLIT = false>
+          bool ENC = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap tmapA,
                      const __grid_constant__ CUtensorMap tmapS, const ConvGemmArgs p) {
@@ -775,8 +797,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          uint32_t a0 = a_desc0 + sa * a_slot_step + static_cast<uint32_t>(shift0);
-          for (int tap = 0; tap < p.taps; ++tap, a0 += static_cast<uint32_t>(p.tap_step)) {
+          int tap0 = 0, tap1 = p.taps;
+          if constexpr (ENC) tap_window(p, kb, tap0, tap1);
+          uint32_t a0 = a_desc0 + sa * a_slot_step + static_cast<uint32_t>(shift0 + tap0 * p.tap_step);
+          for (int tap = tap0; tap < tap1; ++tap, a0 += static_cast<uint32_t>(p.tap_step)) {
             // a resident slot completes its first phase only, in this CTA's first job;
             // later jobs issue on it without a wait
             if (!p.b_resident || job == job0) {
@@ -858,7 +882,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int nt = job % p.n_tiles;
         const int wt = PAIR ? 2 * nt + static_cast<int>(rank) : nt;  // packed weight tile
         for (int kb = 0; kb < p.nkb && ok; ++kb) {
-          for (int tap = 0; tap < p.taps; ++tap, ++ib) {
+          int tap0 = 0, tap1 = p.taps;
+          if constexpr (ENC) tap_window(p, kb, tap0, tap1);
+          for (int tap = tap0; tap < tap1; ++tap, ++ib) {
             if (ib % kBWarps != j) continue;
             const int sb = ib % p.nb;
             const uint32_t phb = static_cast<uint32_t>(ib / p.nb) & 1u;
@@ -984,7 +1010,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       for (int c = half; c < n_chunks && ok && !odd_blocks; c += kEpiGroups) {
         const int slot = half * nsh + kslot;
-        ok = epilogue_chunk<CW, B2, F16, SPLIT>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
+        ok = epilogue_chunk<CW, B2, F16, ENC>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
                                 smem_u32(skipFull + slot), smem_u32(skipEmpty + slot), kph,
                                 abort_flag, row_in_tile, b, t, nt * p.N_tile + c * CW,
                                 tbase + c * CW, sbase, smem_u32(bars));

@@ -304,11 +304,17 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   // kMinAInFlight bytes of A in flight (the 1x1 convs wait on their A loads otherwise).
   // weight bytes per (channel, column): one f16 or bf16 value, or bf16 hi + lo
   const int wb = L.prec != VOC_PREC_BF16X3 ? 2 : 4;
-  const int w_tile = wb * L.Cp_in * n_stage * g.taps;
+  // a strided conv (down_s) reads two of its three taps per k-block: its k-blocks lie within
+  // one phase group (ceil(s/2) Cp or floor(s/2) Cp channels)
+  const int taps_eff = L.down_s ? 2 : g.taps;
+  const int grp0 = L.down_s ? ((L.down_s + 1) / 2) * (L.Cin / L.down_s) : L.Cp_in;
+  const int grp1 = L.down_s ? (L.down_s / 2) * (L.Cin / L.down_s) : 0;
+  auto kb_ok = [&](int kb) { return L.Cp_in % kb == 0 && grp0 % kb == 0 && grp1 % kb == 0; };
+  const int w_tile = wb * L.Cp_in * n_stage * taps_eff;
   for (int min_na = 3; min_na >= 2 && !g.KB && g.n_tiles <= kMaxResidentTiles; --min_na)
     for (int kb = L.Cp_in - L.Cp_in % 16; kb >= 16 && !g.KB; kb -= 16) {
-      if (L.Cp_in % kb || 4 * kb * g.rows > 72 * 1024) continue;
-      if (g.taps * (L.Cp_in / kb) > kMaxResidentStages) continue;
+      if (!kb_ok(kb) || 4 * kb * g.rows > 72 * 1024) continue;
+      if (taps_eff * (L.Cp_in / kb) > kMaxResidentStages) continue;
       const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
       const int ns = has_skip ? 2 * voc::kEpiGroups : 0;
       const int avail = kSmemMax - 1024 - kBarrierBytes - w_tile - ns * sb;
@@ -316,14 +322,14 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
       const int na = std::min(g.taps == 1 ? 8 : 4, avail / a_bytes);
       if (na < min_na || na * a_bytes < kMinAInFlight) continue;
       g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = wb * kb * n_stage, g.na = na, g.ns = ns;
-      g.nb = g.taps * (L.Cp_in / kb);
+      g.nb = taps_eff * (L.Cp_in / kb);
       g.b_resident = 1;
     }
   // streaming weights: a 1x1 conv gets up to four A stages (its A comes from HBM and is
   // consumed at once; its weight stages come from L2), a k-tap conv two
   const int na_want = g.taps == 1 ? 4 : 2;
   for (int kb = L.Cp_in - L.Cp_in % 16; kb >= 16 && !g.KB; kb -= 16) {
-    if (L.Cp_in % kb || wb * kb * n_stage > kBStageMax || 4 * kb * g.rows > 72 * 1024) continue;
+    if (!kb_ok(kb) || wb * kb * n_stage > kBStageMax || 4 * kb * g.rows > 72 * 1024) continue;
     const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
     const int b_bytes = wb * kb * n_stage;
     int na = na_want;
@@ -351,6 +357,11 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     return false;
   }
   g.nkb = L.Cp_in / g.KB;
+  // taps of each k-block (the encoder kernels read these): all, or for a strided conv taps
+  // 1, 2 (row shifts 0, +1) in the first phase group and 0, 1 (-1, 0) in the second
+  g.kb_split = L.down_s ? grp0 / g.KB : g.nkb;
+  g.tap_lo0 = L.down_s ? 1 : 0, g.tap_hi0 = g.taps;
+  g.tap_lo1 = 0, g.tap_hi1 = L.down_s ? 2 : g.taps;
   // Two MMAs per K step where the doubled column count fits one MMA (N <= 256): narrow
   // layers issue a third fewer MMA instructions, whose rate limits them.
   // (not with the odd-phase ConvT epilogue, which has its own kernel form)
@@ -482,11 +493,14 @@ void convT_column(const Layer &L, int padding, int n, int &r, int &co) {
 float weight_value(const Layer &L, int padding, const float *w, int n, int ci, int tap) {
   if (ci >= L.Cin) return 0.f;
   if (L.down_s) {
-    // input channel ci = (chunk * s + r) * 8 + e holds channel chunk * 8 + e at phase r (row
-    // u s + r of the strided conv's input); tap du - 1 in {-1, 0, 1} reads row u + du, i.e.
-    // original tap k = du s + r + s / 2 of the k = 2s kernel
+    // input channel ci = 8 * voc::phase_plane(chunk, r) + e holds channel chunk * 8 + e at
+    // phase r (row u s + r of the strided conv's input); tap du + 1 (du in {-1, 0, 1}) reads
+    // row u + du, i.e. original tap k = du s + r + s / 2 of the k = 2s kernel
     const int sd = L.down_s;
-    const int chunk = ci / (8 * sd), r = (ci / 8) % sd, e = ci % 8;
+    const int cpc = L.Cin / (8 * sd), r0 = (sd + 1) / 2;
+    const int pl = ci / 8, e = ci % 8;
+    const int chunk = pl < r0 * cpc ? pl / r0 : (pl - r0 * cpc) / (sd - r0);
+    const int r = pl < r0 * cpc ? pl % r0 : r0 + (pl - r0 * cpc) % (sd - r0);
     const int c = chunk * 8 + e;
     const int k = (tap - 1) * sd + r + sd / 2;
     if (n >= L.Cout || c >= L.down_c || k < 0 || k >= 2 * sd) return 0.f;
@@ -832,7 +846,7 @@ cudaError_t launch_conv(const Layer &L, const ConvGemmArgs &a, int grid, const C
                         const CUtensorMap &smap, cudaStream_t stream) {
   const dim3 g(grid), blk(voc::kGemmThreads);
   constexpr bool kB2 = PREC == voc::kPrecBf16x3;  // the B2 form exists for bf16x3 only
-  if (a.split_s > 1) {  // phase-split hi/lo output
+  if (a.split_s > 1 || L.down_s) {  // encoder forms: phase-split output, tap windows
     if (kB2 && L.g.b2)
       return launch_pdl(voc::conv_gemm_kernel<16, false, kB2, false, PREC, true>, g, blk, L.smem,
                         stream, map, smap, a);
@@ -858,8 +872,8 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
     if (tiles <= units) return tiles;
     return a.b_resident ? units - units % a.n_tiles : units;
   };
-  if (a.split_s > 1 && (L.pair || L.convT || L.ru))
-    return fail(ctx, VOC_UNSUPPORTED, L.name + ": a phase-split output needs a plain conv kernel");
+  if ((a.split_s > 1 || L.down_s) && (L.pair || L.convT || L.ru))
+    return fail(ctx, VOC_UNSUPPORTED, L.name + ": the encoder forms need a plain conv kernel");
   if (L.pair) {  // persistent grid of 2-CTA clusters, at most as many as can be resident
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
