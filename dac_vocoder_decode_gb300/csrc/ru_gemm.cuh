@@ -13,6 +13,11 @@
 // accumulator 2; the epilogue finishes the tile from accumulator 2 exactly like the
 // separate conv2 kernel.  Two accumulator pairs (when they fit in TMEM) let conv1 of the
 // next tile overlap the epilogue of this one.
+//
+// B2 (units of up to 128 channels): both mainloops take the two-MMA K step of the conv kernel's
+// B2 form -- A_hi x [W_hi | W_lo] into 2N accumulator columns, then A_lo x W_hi into the first
+// N -- and both epilogues add the two column halves.  A narrow layer's MMAs cost about the same
+// whatever their N (the A operand is re-read for each), so this removes a third of them.
 #pragma once
 #include "conv_gemm.cuh"
 
@@ -30,11 +35,22 @@ struct RuExtra {
 // Epilogue 1 of one warp: rows quad*32.. of accumulator 1, columns n0..n0+CW-1 ->
 // Snake2(acc + b1) split into hi/lo, stored into the H tile: 8-channel chunk j of the hi
 // parts at H + j*2048, of the lo parts at H + (Cp/8 + j)*2048, row r at +16*r.
-template <int CW>
+template <int CW, bool B2>
 __device__ __forceinline__ void ru_epilogue1(const ConvGemmArgs &p, const RuExtra &x, uint32_t hbase,
                                              int row_in_tile, int n0, uint32_t taddr) {
   float v[CW];
-  tmem_ld(taddr, v);
+  if constexpr (B2) {  // (CW = 16) the two column halves of the accumulator
+    static_assert(CW == 16, "the B2 epilogue reads 16-column chunks");
+    uint32_t r[CW], r2[CW];
+    tmem_ld_issue<CW>(taddr, r);
+    tmem_ld_issue<CW>(taddr + static_cast<uint32_t>(p.N_tile), r2);
+    tmem_ld_wait<CW>(r);
+    tmem_ld16_after_wait(r2);
+#pragma unroll
+    for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]) + __uint_as_float(r2[i]);
+  } else {
+    tmem_ld(taddr, v);
+  }
   float bb[CW], a[CW], ib[CW];
   ldg_vec(x.bias_h + n0, bb);
   ldg_vec(x.alpha_h + n0, a);
@@ -64,7 +80,7 @@ __device__ __forceinline__ void ru_epilogue1(const ConvGemmArgs &p, const RuExtr
   }
 }
 
-template <int CW>
+template <int CW, bool B2 = false>
 __global__ void __launch_bounds__(kRuThreads, 1)
     ru_gemm_kernel(const __grid_constant__ CUtensorMap tmapA,
                    const __grid_constant__ CUtensorMap tmapS, const ConvGemmArgs p,
@@ -195,10 +211,13 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.timeout, abort_flag));
       };
       const uint32_t idesc = idesc_bf16_f32(kTileM, p.N_tile);
+      const uint32_t idesc2 = idesc_bf16_f32(kTileM, 2 * p.N_tile);  // B2: [W_hi | W_lo]
+      // B2: each chunk of a weight stage holds its N hi rows, then its N lo rows
+      const uint32_t chunkB_stride = B2 ? 2 * chunkB : chunkB;
       const uint64_t dA_lo = (uint64_t)((kchunks * chunkA) >> 4);
       const uint64_t dA_k = (uint64_t)((2 * chunkA) >> 4);
       const uint64_t dB_lo = (uint64_t)((kchunks * chunkB) >> 4);
-      const uint64_t dB_k = (uint64_t)((2 * chunkB) >> 4);
+      const uint64_t dB_k = (uint64_t)((2 * chunkB_stride) >> 4);
       const uint64_t dH_lo = (uint64_t)(((p.Cp_out / 8) * chunkH) >> 4);
       const uint64_t dH_k = (uint64_t)((2 * chunkH) >> 4);
       const uint64_t h0 = smem_desc(smem_u32(smH), chunkH, 128);
@@ -210,7 +229,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
       auto wait_b = [&](uint64_t &b0) -> bool {
         if (!wait_all(smem_u32(fullB + sb), phb)) return false;
         tc_fence_after();
-        b0 = smem_desc(smem_u32(smB + (size_t)sb * p.b_bytes), chunkB, 128);
+        b0 = smem_desc(smem_u32(smB + (size_t)sb * p.b_bytes), chunkB_stride, 128);
         return true;
       };
       auto release_b = [&]() {
@@ -245,9 +264,14 @@ __global__ void __launch_bounds__(kRuThreads, 1)
               const uint64_t a_hi = a0 + ks * dA_k, a_lo = a_hi + dA_lo;
               const uint64_t b_hi = b0 + ks * dB_k, b_lo = b_hi + dB_lo;
               const uint32_t accum = (kb | tap | ks) ? 1u : 0u;
-              mma_bf16_warp(d1, a_hi, b_hi, idesc, accum);
-              mma_bf16_warp(d1, a_hi, b_lo, idesc, 1u);
-              mma_bf16_warp(d1, a_lo, b_hi, idesc, 1u);
+              if constexpr (B2) {
+                mma_bf16_warp(d1, a_hi, b_hi, idesc2, accum);
+                mma_bf16_warp(d1, a_lo, b_hi, idesc, 1u);
+              } else {
+                mma_bf16_warp(d1, a_hi, b_hi, idesc, accum);
+                mma_bf16_warp(d1, a_hi, b_lo, idesc, 1u);
+                mma_bf16_warp(d1, a_lo, b_hi, idesc, 1u);
+              }
             }
             release_b();
           }
@@ -275,9 +299,14 @@ __global__ void __launch_bounds__(kRuThreads, 1)
             const uint64_t a_hi = a0 + ks * dH_k, a_lo = a_hi + dH_lo;
             const uint64_t b_hi = b0 + ks * dB_k, b_lo = b_hi + dB_lo;
             const uint32_t accum = (kb | ks) ? 1u : 0u;
-            mma_bf16_warp(d2, a_hi, b_hi, idesc, accum);
-            mma_bf16_warp(d2, a_hi, b_lo, idesc, 1u);
-            mma_bf16_warp(d2, a_lo, b_hi, idesc, 1u);
+            if constexpr (B2) {
+              mma_bf16_warp(d2, a_hi, b_hi, idesc2, accum);
+              mma_bf16_warp(d2, a_lo, b_hi, idesc, 1u);
+            } else {
+              mma_bf16_warp(d2, a_hi, b_hi, idesc, accum);
+              mma_bf16_warp(d2, a_hi, b_lo, idesc, 1u);
+              mma_bf16_warp(d2, a_lo, b_hi, idesc, 1u);
+            }
           }
           release_b();
         }
@@ -360,7 +389,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
       }
       tc_fence_after();
       for (int c = half; c < n_chunks; c += 2)
-        ru_epilogue1<CW>(p, x, hbase, row_in_tile, c * CW, t1 + c * CW);
+        ru_epilogue1<CW, B2>(p, x, hbase, row_in_tile, c * CW, t1 + c * CW);
       fence_proxy_async_smem();  // make the H stores visible to the tensor cores
       tc_fence_before();
       mbar_arrive(smem_u32(acc1Empty + j));
@@ -374,7 +403,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
       const int t = mt * kTileM + row_in_tile;
       for (int c = half; c < n_chunks && ok; c += 2, ++kh) {
         const int slot = half * nsh + kh % nsh;
-        ok = epilogue_chunk<CW>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
+        ok = epilogue_chunk<CW, B2>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
                                 smem_u32(skipFull + slot), smem_u32(skipEmpty + slot),
                                 static_cast<uint32_t>(kh / nsh) & 1u, abort_flag, row_in_tile, b,
                                 t, c * CW, t2 + c * CW, sbase, smem_u32(bars));

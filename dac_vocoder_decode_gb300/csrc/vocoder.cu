@@ -157,6 +157,9 @@ bool set_kernel_attrs(std::string &why) {
       st = cudaFuncSetAttribute(voc::ru_gemm_kernel<16>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(voc::ru_gemm_kernel<16, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::out_head_kernel<kHeadTile>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
   });
@@ -440,7 +443,10 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
     why = "tap span too wide for one staged tile";
     return false;
   }
-  L.cw = (g.N_tile % 64 == 0) ? 32 : 16;  // an even number of chunks, as in plan_gemm
+  // B2 form (two MMAs per K step) when the doubled column count fits one MMA; it reads
+  // 16-column epilogue chunks
+  g.b2 = (2 * g.N_tile <= 256) ? 1 : 0;
+  L.cw = (!g.b2 && g.N_tile % 64 == 0) ? 32 : 16;
   L.rx.h_bytes = 4 * voc::kTileM * L.Cp_out;
   const int chunkA = g.rows * 16;
   const int sb = voc::skip_slot_bytes(L.cw);
@@ -463,7 +469,7 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
   }
   g.nkb = L.Cp_in / g.KB;
   int ac = 32;
-  while (ac < g.N_tile) ac *= 2;
+  while (ac < (g.b2 ? 2 * g.N_tile : g.N_tile)) ac *= 2;
   g.acc_cols = ac;
   L.rx.n_buf = (4 * ac <= 512) ? 2 : 1;
   g.n_acc = 2 * L.rx.n_buf;  // accumulators in TMEM (conv1 and conv2 of each buffer)
@@ -895,7 +901,10 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
                                          : persistent(ctx->num_sms));
   cudaError_t e;
   if (L.ru) {
-    if (L.cw == 32)
+    if (L.g.b2)
+      e = launch_pdl(voc::ru_gemm_kernel<16, true>, dim3(grid), dim3(voc::kRuThreads), L.smem,
+                     stream, map, smap, a, L.rx);
+    else if (L.cw == 32)
       e = launch_pdl(voc::ru_gemm_kernel<32>, dim3(grid), dim3(voc::kRuThreads), L.smem, stream,
                      map, smap, a, L.rx);
     else
