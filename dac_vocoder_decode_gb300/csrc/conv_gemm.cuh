@@ -131,7 +131,19 @@ struct ConvGemmArgs {
   int kb_split;            // k-blocks kb < kb_split use taps [tap_lo0, tap_hi0), the others
   int tap_lo0, tap_hi0, tap_lo1, tap_hi1;  // [tap_lo1, tap_hi1) (a strided conv's two
                                            // phase groups each read two of its three taps)
+  // Output head folded into this layer's epilogue (kernels with HEAD = true): the layer
+  // writes no activations; each warp reduces its 32 rows x 16 channels of Snake_out(y) to
+  // the 32 + head_K - 1 partial sums of the head's outputs those rows reach
+  // (head_slice_len), stored at head_part[((b * head_slices + row / 32) * (Cp_out / 16)
+  // + chunk) * head_slice_len + j] for output row 32 (row / 32) + j - (head_K - 1) + head_pad.
+  const float *head_w;     // [head_K][Cp_out] head weights (zero past the real channels)
+  float *head_part;
+  int head_K, head_pad, head_slices, head_slice_len;
 };
+
+// Taps of the head fold (the conv kernel's HEAD form): the decoder's 7-tap head; a shorter head
+// is folded with its weights zero-padded to 7 taps (head_K = 7, the same head_pad).
+constexpr int kHeadFoldMaxK = 7;
 
 // Plane (8-channel group) of channel chunk `ch`, phase `ph` in the phase-split layout of a
 // strided conv's input with stride ss over cpc chunks: the phases r < R0 = ceil(ss/2) come
@@ -360,12 +372,15 @@ __device__ __forceinline__ bool convT_block_odd(const ConvGemmArgs &p, volatile 
 
 // Epilogue of one warp for 32 rows (its TMEM lane quadrant) x CW columns
 // n0..n0+CW-1, which lie in one ConvT phase because CW divides C_out.
-template <int CW, bool B2 = false, bool F16 = false, bool ENC = false>
+// HEAD: instead of storing, hp[k] = sum over the chunk's channels c of head_w[k][c] *
+// Snake_out(y)[c] for this lane's row (zero for padding rows; the caller reduces and stores).
+template <int CW, bool B2 = false, bool F16 = false, bool ENC = false, bool HEAD = false>
 __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t sslot,
                                                uint32_t sfull, uint32_t sempty, uint32_t sparity,
                                                volatile int *abort_flag, int row_in_tile,
                                                int b, int t, int n0, uint32_t taddr,
-                                               uint32_t smem_lo, uint32_t smem_hi) {
+                                               uint32_t smem_lo, uint32_t smem_hi,
+                                               float *hp = nullptr) {
   VOC_CHECK((taddr & 0xFFFFu) + CW + (p.b2 ? p.N_tile : 0) <= (uint32_t)(p.n_acc * p.acc_cols), 11,
             taddr & 0xFFFF, CW, p.b2);
   VOC_CHECK(n0 + CW <= p.N_total, 12, n0, p.N_total, 0);
@@ -464,6 +479,20 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
     for (int i = 0; i < CW; ++i) v[i] = 0.f, sn[i] = 0.f;
   }
   const size_t row_t = static_cast<size_t>(out_row);
+  if constexpr (HEAD) {  // the folded output head: this row's partial products per tap
+#pragma unroll
+    for (int k = 0; k < kHeadFoldMaxK; ++k) {
+      float w[CW];
+      ldg_vec(p.head_w + (size_t)k * p.Cp_out + co0, w);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < CW; ++i) acc = fmaf(w[i], sn[i], acc);
+      hp[k] = acc;
+      // one tap's weights in registers at a time (the loads are L1 hits)
+      asm volatile("" ::: "memory");
+    }
+    return true;
+  }
   if (p.out_f32) {
     const size_t L_out = static_cast<size_t>(p.f32_L);
     const size_t row = row_t + p.f32_row0;
@@ -519,6 +548,35 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
   return true;
 }
 
+// The folded output head, for one warp and one 16-channel chunk: lane l holds hp[k], the
+// products of head tap k with its row (32 s + l) summed over the chunk; output row
+// 32 s + j - (K - 1) + head_pad (j < 32 + K - 1) receives hp[k] of the lane j - (K - 1) + k.
+// Lane l forms the sums j = l and (l < K - 1) j = 32 + l by shuffles and stores them.  Every
+// lane of the warp calls this (the shuffles are warp-collective).
+__device__ __forceinline__ bool head_fold_store(const ConvGemmArgs &p, const float (&hp)[kHeadFoldMaxK],
+                                                int b, int slice, int chunk, int lane,
+                                                volatile int *abort_flag) {
+  constexpr int K = kHeadFoldMaxK;
+  float y0 = 0.f, y1 = 0.f;  // j = lane, j = 32 + lane
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const int up = K - 1 - k;  // j = lane reads lane - up
+    const float a = __shfl_up_sync(0xffffffffu, hp[k], up);
+    if (lane >= up) y0 += a;
+    const int src = lane + 32 - up;  // j = 32 + lane reads lane + 32 - up (< 32 only)
+    const float c = __shfl_sync(0xffffffffu, hp[k], src & 31);
+    if (src < 32) y1 += c;
+  }
+  const long long base =
+      (((long long)b * p.head_slices + slice) * (p.Cp_out / 16) + chunk) * p.head_slice_len;
+  VOC_CHECK(slice < p.head_slices && chunk < p.Cp_out / 16 && p.head_K == K &&
+                p.head_slice_len == 32 + K - 1,
+            23, slice, chunk, p.head_slice_len);
+  p.head_part[base + lane] = y0;
+  if (lane < K - 1) p.head_part[base + 32 + lane] = y1;
+  return true;
+}
+
 // Taps [tap0, tap1) that k-block kb reads (the encoder's strided convs skip one of three).
 __device__ __forceinline__ void tap_window(const ConvGemmArgs &p, int kb, int &tap0, int &tap1) {
   const bool second = kb >= p.kb_split;
@@ -561,10 +619,11 @@ __device__ __forceinline__ void drain_ring_strided(uint64_t *full, int slots, in
 // two MMAs per K step (A_hi x W and A_lo x W): kPrecF16w (f16 operands and f16 hi/lo outputs)
 // or kPrecBf16w (bf16 operands and bf16 hi/lo outputs).  ENC: the encoder's forms -- a
 // phase-split hi/lo output for a strided conv (ConvGemmArgs::split_s; the last residual unit
-// of each block) and per-k-block tap windows (kb_split, tap_lo*, tap_hi*; the strided conv).  Separate instantiations keep the common form's register budget
+// of each block) and per-k-block tap windows (kb_split, tap_lo*, tap_hi*; the strided conv).
+// HEAD: the decoder's output head folded into the epilogue (ConvGemmArgs::head_*).  Separate instantiations keep the common form's register budget
 // and instruction stream.
 template <int CW, bool PAIR, bool B2 = false, bool ODDT = false, int PREC = kPrecBf16x3,
-          bool ENC = false>
+          bool ENC = false, bool HEAD = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     conv_gemm_kernel(const __grid_constant__ CUtensorMap tmapA,
                      const __grid_constant__ CUtensorMap tmapS, const ConvGemmArgs p) {
@@ -1010,11 +1069,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       for (int c = half; c < n_chunks && ok && !odd_blocks; c += kEpiGroups) {
         const int slot = half * nsh + kslot;
-        ok = epilogue_chunk<CW, B2, F16, ENC>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
+        float hp[kHeadFoldMaxK] = {};
+        ok = epilogue_chunk<CW, B2, F16, ENC, HEAD>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
                                 smem_u32(skipFull + slot), smem_u32(skipEmpty + slot), kph,
                                 abort_flag, row_in_tile, b, t, nt * p.N_tile + c * CW,
-                                tbase + c * CW, sbase, smem_u32(bars));
+                                tbase + c * CW, sbase, smem_u32(bars), hp);
         ok = __all_sync(0xffffffffu, ok);
+        if constexpr (HEAD) {
+          if (ok)
+            ok = head_fold_store(p, hp, b, (mt * kM + row0) / 32 + quad, nt * (p.N_tile / CW) + c,
+                                 lane, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+        }
         if (++kslot == nsh) kslot = 0, kph ^= 1u;
       }
       // every lane's TMEM reads of this accumulator are complete before lane 0 frees it

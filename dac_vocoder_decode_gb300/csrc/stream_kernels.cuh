@@ -3,6 +3,7 @@
 //   out_head_kernel     Snake'd chunk-major fp32 -> k-tap conv to one channel (+bias) -> tanh
 //   out_head_reg_kernel the same for 7 taps, register-blocked (the decoder's head)
 //   stitch_kernel       overlap-crop stitch + clamp of windowed decodes
+//   head_finish_kernel  the folded output head: partial sums of the last conv2 -> audio
 //   finite_check_kernel flags a NaN / Inf in a buffer
 //   rows_to_cf_kernel   chunk-major fp32 -> channels-first fp32 (single-layer ops)
 #pragma once
@@ -209,6 +210,32 @@ __global__ void stitch_kernel(const float *__restrict__ dec, int n_win, int n_si
   const long long src = (long long)(lo + (f - start)) * hop + ph;
   const float v = dec[(size_t)(w * n_sides + side) * (size_t)Wf * hop + src];
   out[(size_t)side * len + j] = v < -1.f ? -1.f : (v > 1.f ? 1.f : v);
+}
+
+// Output head folded into the last conv2 (the conv kernel's HEAD form): audio[b][t] =
+// tanh(bias + the partial sums that the 32-row slices reaching output t stored, over all
+// channel chunks).  Slice s of chunk c holds slice_len = 32 + K - 1 sums, entry j for
+// output row 32 s + j - (K - 1) + pad, so output t reads the slices s with
+// 0 <= t - 32 s + K - 1 - pad < slice_len (at most two).  One thread per output sample:
+// block 256, grid (ceil(L / 256), B).
+__global__ void head_finish_kernel(const float *__restrict__ part, int L, int slices, int nch,
+                                   int K, int pad, const float *__restrict__ bias,
+                                   float *__restrict__ audio) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int b = blockIdx.y;
+  if (t >= L) return;
+  const int slice_len = 32 + K - 1;
+  const int u = t + K - 1 - pad;  // = 32 s + j
+  float acc = bias[0];
+  for (int s = max(0, (u - slice_len + 32) / 32); s <= u / 32 && s < slices; ++s) {
+    const int j = u - 32 * s;
+    if (j < 0 || j >= slice_len) continue;
+    const float *src = part + ((size_t)b * slices + s) * nch * slice_len + j;
+    for (int c = 0; c < nch; ++c) acc += src[(size_t)c * slice_len];
+  }
+  audio[(size_t)b * L + t] = tanhf(acc);
 }
 
 __global__ void finite_check_kernel(const float *__restrict__ x, long long n, int *flag) {

@@ -99,6 +99,10 @@ struct Layer {
   int cw = 16;              // epilogue column chunk (conv kernel: 16; fused unit: 16 or 32)
   bool pair = false;        // CTA-pair kernel: 256-row tiles, half of each weight tile per CTA
   int max_clusters = 0;     // pair: co-resident 2-CTA clusters of this launch shape
+  // the output head folded into this layer's epilogue (the decoder's last conv2, in a
+  // whole-sequence decode): partial sums go to hi/lo buffer head_buf, which it does not read
+  bool head_fold = false;
+  int head_buf = -1;
   // fused residual unit (conv1 k-tap + conv2 1x1 in one kernel)
   bool ru = false;
   voc::RuExtra rx{};
@@ -108,6 +112,7 @@ struct OutHead {
   int C = 0, Cp = 0, K = 0, pad_left = 0, level = 0;
   float *w_dev = nullptr, *b_dev = nullptr;
   float *w4_dev = nullptr;  // [K][Cp/4] channel quadruples for the register-blocked kernel
+  float *wk_dev = nullptr;  // [K][Cp] for the head folded into the last conv2
 };
 constexpr int kHeadTpt = 2;  // samples per thread of the register-blocked head
 
@@ -135,9 +140,11 @@ cudaError_t set_conv_attrs() {
   cudaError_t st = set(voc::conv_gemm_kernel<16, false, false, false, PREC>);
   if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, false, false, true, PREC>);
   if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, false, false, false, PREC, true>);
+  if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, false, false, false, PREC, false, true>);
   if constexpr (PREC == voc::kPrecBf16x3) {
     if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, false, true>);
     if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, false, true, false, PREC, true>);
+    if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, false, true, false, PREC, false, true>);
     if (st == cudaSuccess) st = set(voc::conv_gemm_kernel<16, true>);
   }
   return st;
@@ -831,7 +838,16 @@ voc_status check_launch(vocoder *ctx, const std::string &name, cudaStream_t stre
 }
 #endif
 
-void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops, double &bytes) {
+// Partial sums per item of the head folded into layer L (L_f output rows).
+double head_part_floats(const vocoder *ctx, const Layer &L, long long Lf) {
+  const long long slices = 4 * ((Lf + voc::kTileM - 1) / voc::kTileM);
+  return (double)slices * (L.Cp_out / 16) * (32 + voc::kHeadFoldMaxK - 1);
+}
+
+// folded: whether this launch of L carries the folded output head (L.head_fold and room for
+// its partial sums)
+void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops, double &bytes,
+                bool folded = false) {
   const double L_in = (double)level_len(ctx, L.level, T);
   const double L_out = L_in * (L.convT ? L.stride : 1);
   flops = L.convT ? 4.0 * L.Cin * L.Cout * B * L_out : 2.0 * L.Cin * L.Cout * L.K * B * L_in;
@@ -841,8 +857,12 @@ void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops,
               (double)g.n_tiles * (L.pair ? 2 : 1) * (g.taps + (L.ru ? 1 : 0)) * g.nkb * g.b_bytes;
   const double out_elems = (double)B * L_out * L.Cp_out;
   if (L.skip_buf >= 0) by += 4.0 * out_elems;
-  if (L.f32_buf >= 0) by += 4.0 * out_elems;
+  if (L.f32_buf >= 0 && !folded) by += 4.0 * out_elems;
   if (L.hl_buf >= 0) by += 4.0 * out_elems;
+  if (folded) {  // the head's partial sums instead of the activations, and its products
+    by += 4.0 * B * head_part_floats(ctx, L, (long long)L_out);
+    flops += 2.0 * ctx->head.C * ctx->head.K * B * L_out;
+  }
   bytes = by;
 }
 
@@ -852,6 +872,13 @@ cudaError_t launch_conv(const Layer &L, const ConvGemmArgs &a, int grid, const C
                         const CUtensorMap &smap, cudaStream_t stream) {
   const dim3 g(grid), blk(voc::kGemmThreads);
   constexpr bool kB2 = PREC == voc::kPrecBf16x3;  // the B2 form exists for bf16x3 only
+  if (a.head_part) {  // the output head folded into the epilogue
+    if (kB2 && L.g.b2)
+      return launch_pdl(voc::conv_gemm_kernel<16, false, kB2, false, PREC, false, true>, g, blk,
+                        L.smem, stream, map, smap, a);
+    return launch_pdl(voc::conv_gemm_kernel<16, false, false, false, PREC, false, true>, g, blk,
+                      L.smem, stream, map, smap, a);
+  }
   if (a.split_s > 1 || L.down_s) {  // encoder forms: phase-split output, tap windows
     if (kB2 && L.g.b2)
       return launch_pdl(voc::conv_gemm_kernel<16, false, kB2, false, PREC, true>, g, blk, L.smem,
@@ -1266,6 +1293,29 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     if (st != VOC_OK) return bail(st);
     st = upload(ctx, ctx->allocs, bp, &h.b_dev);
     if (st != VOC_OK) return bail(st);
+    // Fold the head into the last conv2 when that layer is a plain conv of one column tile
+    // writing Snake_out(y) (not a fused unit, not a CTA pair) and the head has at most
+    // kHeadFoldMaxK taps; its partial sums go to a hi/lo buffer the layer does not read.
+    // Causal decoders keep the separate head: their chunk-by-chunk stream decode runs it, and
+    // a streamed sequence must equal the whole-sequence decode bit for bit (the folded head
+    // adds its products in another order).
+    Layer &last = ctx->layers.back();
+    if (pad == VOC_PAD_SYMMETRIC && !last.ru && !last.pair && !last.convT &&
+        (last.epi_flags & voc::EPI_F32_SNAKE) &&
+        last.g.n_tiles == 1 && h.K <= voc::kHeadFoldMaxK && last.Cp_out == h.Cp) {
+      // [k][c], zero-padded to kHeadFoldMaxK taps (same left padding)
+      std::vector<float> wk((size_t)voc::kHeadFoldMaxK * h.Cp, 0.f);
+      for (int c = 0; c < C; ++c)
+        for (int k = 0; k < h.K; ++k) wk[(size_t)k * h.Cp + c] = w[(size_t)c * h.K + k];
+      st = upload(ctx, ctx->allocs, wk, &h.wk_dev);
+      if (st != VOC_OK) return bail(st);
+      last.head_fold = true;
+      for (int c : {(int)BUF_H0, (int)BUF_H1, (int)BUF_HB})
+        if (c != last.in_buf) {
+          last.head_buf = c;
+          break;
+        }
+    }
   }
   *out = ctx;
   return VOC_OK;
@@ -1292,6 +1342,29 @@ VOC_API int vocoder_launches_per_decode(const vocoder *ctx, int B, int T) {
 }
 
 namespace {
+void head_fold_args(const vocoder *ctx, const Layer &L, void *const *bufs, ConvGemmArgs &a) {
+  a.out_f32 = nullptr;  // the layer writes the head's partial sums instead
+  a.head_w = ctx->head.wk_dev;
+  a.head_part = static_cast<float *>(bufs[L.head_buf]);
+  a.head_K = voc::kHeadFoldMaxK;  // the weights are zero-padded to this many taps
+  a.head_pad = ctx->head.pad_left;
+  a.head_slices = 4 * a.m_tiles;
+  a.head_slice_len = 32 + voc::kHeadFoldMaxK - 1;
+}
+
+voc_status launch_head_finish(vocoder *ctx, const Layer &L, void *const *bufs, int B, long long Lf,
+                              float *audio, cudaStream_t stream) {
+  const OutHead &h = ctx->head;
+  const int slices = static_cast<int>(4 * ((Lf + voc::kTileM - 1) / voc::kTileM));
+  dim3 grid(static_cast<unsigned>((Lf + 255) / 256), static_cast<unsigned>(B));
+  cudaError_t e = launch_pdl(voc::head_finish_kernel, grid, dim3(256), 0, stream,
+                             static_cast<const float *>(bufs[L.head_buf]), static_cast<int>(Lf),
+                             slices, L.Cp_out / 16, voc::kHeadFoldMaxK, h.pad_left,
+                             static_cast<const float *>(h.b_dev), audio);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "launch head_finish");
+  return VOC_OK;
+}
+
 voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *audio, void *ws,
                        size_t ws_bytes, cudaStream_t stream, unsigned flags) {
   const size_t need = vocoder_workspace_bytes(ctx, B, T);
@@ -1351,6 +1424,10 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
     if (prof) cudaEventRecord(ctx->events[2 * li + which], stream);
   };
 
+  // the head folded into the last conv2, when its partial sums fit the buffer they borrow
+  const long long Lf_out = level_len(ctx, ctx->desc.n_stages, T);
+  const bool fold = ctx->layers.back().head_fold &&
+                    (double)B * head_part_floats(ctx, ctx->layers.back(), Lf_out) * 4.0 <= (double)bb;
   voc_status st;
   rec(0);
   st = launch_prep(ctx, latent, B, ctx->desc.latent_channels, T, ctx->Cp_lat, nullptr, nullptr,
@@ -1369,6 +1446,7 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
     const Layer &L = ctx->layers[i];
     ConvGemmArgs a;
     gemm_launch_args(ctx, L, B, T, bufs, bb, a);
+    if (L.head_fold && fold) head_fold_args(ctx, L, bufs, a);
     rec(0);
     st = launch_gemm(ctx, L, ctx->maps[i], ctx->skip_maps[i], a, stream);
     if (st != VOC_OK) return st;
@@ -1378,13 +1456,17 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
     rec(1);
     if (prof) {
       ctx->prof_names[li] = L.name;
-      layer_cost(ctx, L, B, T, ctx->prof_flops[li], ctx->prof_bytes[li]);
+      layer_cost(ctx, L, B, T, ctx->prof_flops[li], ctx->prof_bytes[li], L.head_fold && fold);
     }
   }
   const long long Lf = level_len(ctx, ctx->desc.n_stages, T);
+  const Layer &last = ctx->layers.back();
   rec(0);
-  st = launch_out_head(ctx, ctx->head, static_cast<const float *>(bufs[BUF_FY]), B, Lf, audio,
-                       stream, 0, pitch8(Lf));
+  if (fold)
+    st = launch_head_finish(ctx, last, bufs, B, Lf, audio, stream);
+  else
+    st = launch_out_head(ctx, ctx->head, static_cast<const float *>(bufs[BUF_FY]), B, Lf, audio,
+                         stream, 0, pitch8(Lf));
   if (st != VOC_OK) return st;
 #ifdef VOC_CHECKS
   if ((st = check_launch(ctx, "out_head", stream)) != VOC_OK) return st;
@@ -1393,7 +1475,10 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
   if (prof) {
     ctx->prof_names[li] = "out_head";
     ctx->prof_flops[li] = 2.0 * ctx->head.C * ctx->head.K * B * (double)Lf;
-    ctx->prof_bytes[li] = (double)B * Lf * (4.0 * ctx->head.Cp + 4.0);
+    // folded: the last conv2 did the products; this launch reads their partial sums
+    ctx->prof_bytes[li] = fold
+                              ? (double)B * head_part_floats(ctx, last, Lf) * 4.0 + 4.0 * B * Lf
+                              : (double)B * Lf * (4.0 * ctx->head.Cp + 4.0);
     ctx->prof_ready = true;
   }
   ++li;
