@@ -201,10 +201,16 @@ def workload_config(wl, name):
 
 
 def realtime_seconds(wl, name) -> float:
-    """Seconds of music / speech one step handles (a stereo pair counts once)."""
+    """Seconds of music / speech one step delivers (a stereo pair counts once; the windowed
+    workload delivers its stitched track, not the overlapping windows)."""
     if is_encode(name):
         B, _, L = wl.latent.shape
         return B / 2.0 * L / SAMPLE_RATE[name]
+    if getattr(wl, "stitch", None):
+        st = wl.stitch
+        frames = (st["win_frames"] - st["crop_left"] - st["crop_right"]) * (st["n_win"] - 1) \
+            + st["win_frames"]
+        return frames * st["hop"] / SAMPLE_RATE[name]
     return tracks_per_batch(name, wl.B) * wl.T * wl.arch.hop / SAMPLE_RATE[name]
 
 
@@ -280,7 +286,8 @@ def run_reference(args, rank, world):
 # ----------------------------------------------------------------------------- GPU leg
 class DecodeJob:
     """One decode of the workload per step, through vocoder_decode (device buffers) or
-    vocoder_decode_host (host buffers, copies inside the call)."""
+    vocoder_decode_host (host buffers, copies inside the call).  A windowed workload (`stitch`
+    set) also runs the overlap-crop stitch of its decoded windows in every step."""
 
     def __init__(self, V, wl, precision, dev):
         import torch
@@ -291,26 +298,68 @@ class DecodeJob:
         self.y = torch.empty((B, 1, T * hop), dtype=torch.float32, device=dev)
         self.ws = self.ctx.alloc_workspace(B, T)
         self.samples = B * T * hop
-        self.h2d, self.d2h = int(wl.latent.nbytes), int(B * T * hop * 4)
+        self.st = wl.stitch
+        self.z = None
+        if self.st:
+            st = self.st
+            self.stitched = V.vocoder_stitched_length(st["n_win"], st["win_frames"],
+                                                      st["crop_left"], st["crop_right"], st["hop"])
+            self.z = torch.empty((st["n_sides"], self.stitched), dtype=torch.float32, device=dev)
+        self.h2d = int(wl.latent.nbytes)
+        self.d2h = int((self.z if self.st else self.y).numel() * 4)
+        self.stitch_ms = []
+
+    def _stitch(self, stream, y, z):
+        st = self.st
+        self.V.vocoder_stitch(y, st["n_win"], st["n_sides"], st["win_frames"], st["crop_left"],
+                              st["crop_right"], st["hop"], z, stream)
 
     def step(self, stream, flags=0):
         self.V.vocoder_decode(self.ctx.handle, self.x, self.y, self.ws, stream, flags)
+        if self.st:
+            if flags & self.V.VOC_FLAG_PROFILE:  # the stitch's own launch time
+                import torch
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                self._stitch(stream, self.y, self.z)
+                e1.record(stream)
+                e1.synchronize()
+                self.stitch_ms.append(e0.elapsed_time(e1))
+            else:
+                self._stitch(stream, self.y, self.z)
 
     def setup_host(self):
         import torch
         wl = self.wl
         self.x_h = torch.from_numpy(wl.latent).pin_memory()
-        self.y_h = torch.empty(tuple(self.y.shape), dtype=torch.float32).pin_memory()
+        out = self.z if self.st else self.y
+        self.y_h = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
         self.ws_h = self.ctx.alloc_workspace(wl.B, wl.T, host_io=True)
 
     def host_step(self, stream):
-        self.V.vocoder_decode_host(self.ctx.handle, self.x_h, self.y_h, self.ws_h, stream)
+        if not self.st:
+            self.V.vocoder_decode_host(self.ctx.handle, self.x_h, self.y_h, self.ws_h, stream)
+            return
+        # windows: latent in, decode, stitch, the stitched track out (host copies on the stream)
+        import torch
+        with torch.cuda.stream(stream):
+            self.x.copy_(self.x_h, non_blocking=True)
+            self.V.vocoder_decode(self.ctx.handle, self.x, self.y, self.ws, stream)
+            self._stitch(stream, self.y, self.z)
+            self.y_h.copy_(self.z, non_blocking=True)
+        stream.synchronize()
 
     def profile(self):
-        return self.V.vocoder_profile(self.ctx.handle)
+        prof = self.V.vocoder_profile(self.ctx.handle)
+        if self.st and self.stitch_ms:
+            n = self.z.numel()
+            prof.append(dict(name="stitch", ms=self.stitch_ms[-1], flops=0.0, bytes=8.0 * n))
+        return prof
 
     def launches(self):
-        return self.V.vocoder_launches_per_decode(self.ctx.handle, self.wl.B, self.wl.T)
+        return (self.V.vocoder_launches_per_decode(self.ctx.handle, self.wl.B, self.wl.T)
+                + (1 if self.st else 0))
 
     def close(self):
         self.ctx.close()
@@ -480,6 +529,9 @@ def run_ours(args, rank, world, local_rank):
                         "ms_per_step": e2e_t * 1e3},
                 "gpu_launches": launches * args.steps,
                 "profiled_ms_per_step": statistics.mean(prof_ms),
+                **({"stitched_samples_per_s": job.z.numel() * world / (ms_max / 1e3),
+                    "stitched_track_s": realtime_seconds(wl, args.workload)}
+                   if getattr(job, "z", None) is not None else {}),
                 "roofline": roof,
                 "clocks": clk,
                 "stages": stages}
