@@ -365,6 +365,77 @@ class DecodeJob:
         self.ctx.close()
 
 
+class StreamJob(DecodeJob):
+    """A causal decoder's latent decoded chunk by chunk (vocoder_stream_decode, `frames`
+    latent frames per call, contexts carried between calls); one step decodes the whole
+    workload this way, from reset contexts.  The profiled steps run whole-sequence decodes
+    (the same kernels) for the per-kernel rooflines."""
+
+    def __init__(self, V, wl, precision, dev, frames):
+        import torch
+        super().__init__(V, wl, precision, dev)
+        self.F = frames
+        B, T, hop = wl.B, wl.T, wl.arch.hop
+        self.n_calls = (T + frames - 1) // frames
+        self.chunks = [self.x[:, :, i * frames:min(T, (i + 1) * frames)].contiguous()
+                       for i in range(self.n_calls)]
+        # one contiguous audio buffer per call ([B, 1, frames of this call * hop])
+        self.ys = [torch.empty((B, 1, c.shape[2] * hop), dtype=torch.float32, device=dev)
+                   for c in self.chunks]
+        self.sh = V.VocoderStream(self.ctx, B, frames)
+        self.call_ms = []
+
+    def _chunks(self, stream, chunks):
+        self.sh.reset(stream)
+        for i, c in enumerate(chunks):
+            self.sh.decode(c, audio=self.ys[i], stream=stream)
+
+    def step(self, stream, flags=0):
+        if flags & self.V.VOC_FLAG_PROFILE:
+            super().step(stream, flags)
+            return
+        self._chunks(stream, self.chunks)
+
+    def time_calls(self, stream, n=50):
+        """Latency of single calls (events around each), after a reset."""
+        import torch
+        self.sh.reset(stream)
+        with torch.cuda.stream(stream):
+            for i in range(min(n, self.n_calls)):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                self.sh.decode(self.chunks[i], audio=self.ys[i], stream=stream)
+                e1.record(stream)
+                e1.synchronize()
+                self.call_ms.append(e0.elapsed_time(e1))
+
+    def setup_host(self):
+        import torch
+        self.x_h = [c.cpu().pin_memory() for c in self.chunks]
+        self.y_h = [torch.empty(tuple(y.shape), dtype=torch.float32).pin_memory() for y in self.ys]
+
+    def host_step(self, stream):
+        # each call as a streaming client makes it: its latent chunk in, the call, its audio out
+        import torch
+        with torch.cuda.stream(stream):
+            self.sh.reset(stream)
+            for i in range(self.n_calls):
+                self.chunks[i].copy_(self.x_h[i], non_blocking=True)
+                self.sh.decode(self.chunks[i], audio=self.ys[i], stream=stream)
+                self.y_h[i].copy_(self.ys[i], non_blocking=True)
+        stream.synchronize()
+
+    def launches(self):
+        # per call: the decode's launches plus the two context copies
+        per = self.V.vocoder_launches_per_decode(self.ctx.handle, self.wl.B, self.F) + 2
+        return per * self.n_calls
+
+    def close(self):
+        self.sh.close()
+        super().close()
+
+
 class EncodeJob(DecodeJob):
     """One encode of the workload's audio per step (vocoder_encode / vocoder_encode_host)."""
 
@@ -414,7 +485,12 @@ def run_ours(args, rank, world, local_rank):
     one_plane = args.precision in ("f16w", "bf16w")  # one weight plane, two MMAs per MAC
     prec = {"bf16x3": V.VOC_PREC_BF16X3, "f16w": V.VOC_PREC_F16W,
             "bf16w": V.VOC_PREC_BF16W}[args.precision]
-    job = (EncodeJob if is_encode(args.workload) else DecodeJob)(V, wl, prec, dev)
+    if args.stream_frames > 0:
+        if is_encode(args.workload) or wl.arch.padding != W.PAD_CAUSAL:
+            raise SystemExit("--stream-frames needs a causal decoder workload (speech)")
+        job = StreamJob(V, wl, prec, dev, args.stream_frames)
+    else:
+        job = (EncodeJob if is_encode(args.workload) else DecodeJob)(V, wl, prec, dev)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
@@ -467,6 +543,9 @@ def run_ours(args, rank, world, local_rank):
     ms_max = max_over_ranks(ms, dev)
     total_samples = job.samples * world
     value = total_samples / (ms_max / 1e3)
+
+    if isinstance(job, StreamJob):
+        job.time_calls(stream)
 
     # end to end through the host-buffer entry point: H2D of the input, the whole path, D2H
     # of the output, inside the timed region
@@ -523,12 +602,19 @@ def run_ours(args, rank, world, local_rank):
                           "bf16x3": "bf16x3 (hi/lo split, fp32 accumulate)"}[args.precision],
                 "data": "synthetic",
                 "x_realtime": realtime_seconds(wl, args.workload) * world / (ms_max / 1e3),
-                "config": dict(workload_config(wl, args.workload), precision=args.precision),
+                "config": dict(workload_config(wl, args.workload), precision=args.precision,
+                               **({"stream_frames": args.stream_frames}
+                                  if args.stream_frames > 0 else {})),
                 "e2e": {"value": total_samples / e2e_t, "unit": UNIT,
                         "h2d_bytes_per_step": job.h2d, "d2h_bytes_per_step": job.d2h,
                         "ms_per_step": e2e_t * 1e3},
                 "gpu_launches": launches * args.steps,
                 "profiled_ms_per_step": statistics.mean(prof_ms),
+                **({"stream": {"frames_per_call": job.F, "calls_per_step": job.n_calls,
+                               "ms_per_call": statistics.median(job.call_ms),
+                               "audio_ms_per_call": job.F * wl.arch.hop * 1e3 / SAMPLE_RATE[args.workload],
+                               "stages_from": "whole-sequence decodes (same kernels)"}}
+                   if isinstance(job, StreamJob) else {}),
                 **({"stitched_samples_per_s": job.z.numel() * world / (ms_max / 1e3),
                     "stitched_track_s": realtime_seconds(wl, args.workload)}
                    if getattr(job, "z", None) is not None else {}),
@@ -558,6 +644,9 @@ def main():
     ap.add_argument("--ref-frames", type=int, default=48,
                     help="latent frames of one item per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stream-frames", type=int, default=0,
+                    help="decode a causal workload chunk by chunk, this many latent frames per "
+                         "call (vocoder_stream_decode); 0: whole-sequence decode")
     ap.add_argument("--precision", choices=["bf16x3", "f16w", "bf16w"], default="bf16x3",
                     help="bf16x3 (default): full fp32-equivalent inputs; f16w: the pages' F16 "
                          "conv weights; bf16w: bfloat16 conv weights")

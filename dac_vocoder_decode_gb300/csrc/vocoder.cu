@@ -1887,6 +1887,11 @@ struct vocoder_stream {
   size_t state_bytes = 0;
   voc::RowCopyJob *jobs = nullptr;  // device: restore jobs, then save jobs
   int n_restore = 0, n_save = 0, max_job_elems = 0;
+  // CUDA-graph replay: the launches of one chunk, captured once per chunk size on `cap`
+  // over the staging buffers (the caller's latent is copied in, the audio copied out)
+  float *lat_stage = nullptr, *aud_stage = nullptr;
+  cudaStream_t cap = nullptr;
+  std::vector<cudaGraphExec_t> graphs;  // [frames], null until first used
   uint8_t *block = nullptr;     // the single device allocation holding all of the above
 };
 
@@ -1954,6 +1959,9 @@ VOC_API voc_status vocoder_stream_create(vocoder *ctx, int B, int max_frames,
   for (int l = 0; l < nl; ++l) total += hl_bytes(l);
   const size_t jobs_bytes = rupz(sizeof(voc::RowCopyJob) * 2 * (nl + 1), 256);
   total += jobs_bytes;
+  const size_t lat_bytes = rupz((size_t)B * ctx->desc.latent_channels * max_frames * 4, 256);
+  const size_t aud_bytes = rupz((size_t)B * max_frames * ctx->hop * 4, 256);
+  total += lat_bytes + aud_bytes;
   cudaError_t e = cudaMalloc(&s->block, total);
   if (e != cudaSuccess) {
     delete s;
@@ -1964,6 +1972,8 @@ VOC_API voc_status vocoder_stream_create(vocoder *ctx, int B, int max_frames,
   s->fy = cur, cur += s->fy_bytes;
   s->head_in = cur, cur += head_bytes;
   s->state = cur, cur += state_bytes;
+  s->lat_stage = reinterpret_cast<float *>(cur), cur += lat_bytes;
+  s->aud_stage = reinterpret_cast<float *>(cur), cur += aud_bytes;
   s->jobs = reinterpret_cast<voc::RowCopyJob *>(cur);
   // copy jobs: restore (state -> context rows), then save (last ctx rows of [ctx | new] -> state)
   std::vector<voc::RowCopyJob> restore, save;
@@ -2008,11 +2018,17 @@ VOC_API voc_status vocoder_stream_create(vocoder *ctx, int B, int max_frames,
                            pitch8((long long)max_frames * level_len(ctx, L.level, 1)), B, L.cw);
     if (st != VOC_OK) g_err = ctx->err;
   }
+  if (st == VOC_OK) {
+    e = cudaStreamCreateWithFlags(&s->cap, cudaStreamNonBlocking);
+    if (e != cudaSuccess) st = cuda_fail(nullptr, e, "cudaStreamCreateWithFlags");
+  }
   if (st != VOC_OK) {
+    if (s->cap) cudaStreamDestroy(s->cap);
     cudaFree(s->block);
     delete s;
     return st;
   }
+  s->graphs.assign(max_frames + 1, nullptr);
   *out = s;
   return VOC_OK;
 }
@@ -2024,22 +2040,14 @@ VOC_API voc_status vocoder_stream_reset(vocoder_stream *s, voc_stream_t stream) 
   return VOC_OK;
 }
 
-VOC_API voc_status vocoder_stream_decode(vocoder_stream *s, const float *latent_dev, int frames,
-                                         float *audio_dev, voc_stream_t stream_, unsigned flags) {
-  if (!s) return stream_fail(VOC_INVALID_ARG, "stream is NULL");
+namespace {
+// The launches of one chunk: restore the contexts, the latent's hi/lo split, every layer, the
+// head, save the contexts.
+voc_status stream_launches(vocoder_stream *s, const float *latent_dev, int frames,
+                           float *audio_dev, cudaStream_t stream) {
   vocoder *ctx = s->ctx;
-  if (!latent_dev || !audio_dev) return fail(ctx, VOC_INVALID_ARG, "latent / audio NULL");
-  if (frames < 1 || frames > s->max_frames)
-    return fail(ctx, VOC_INVALID_ARG, "frames out of [1, max_frames]");
-  if (flags & ~static_cast<unsigned>(VOC_FLAG_SYNC))
-    return fail(ctx, VOC_INVALID_ARG, "only VOC_FLAG_SYNC is accepted");
-  int dev = -1;
-  cudaGetDevice(&dev);
-  if (dev != ctx->device) return fail(ctx, VOC_INVALID_ARG, "current device differs from the context's");
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const int B = s->B;
   const int nl = static_cast<int>(ctx->layers.size());
-  cudaError_t e;
   auto copies = [&](int first, int n) -> voc_status {
     if (n == 0) return VOC_OK;
     const int blocks = std::max(1, std::min((s->max_job_elems + 255) / 256, 64));
@@ -2096,8 +2104,59 @@ VOC_API voc_status vocoder_stream_decode(vocoder_stream *s, const float *latent_
   st = launch_out_head(ctx, ctx->head, reinterpret_cast<const float *>(s->head_in), B, Lf, audio_dev,
                        stream, s->head_ctx, s->head_plane);
   if (st != VOC_OK) return st;
-  st = copies(s->n_restore, s->n_save);  // this chunk's contexts for the next one
+  return copies(s->n_restore, s->n_save);  // this chunk's contexts for the next one
+}
+}  // namespace
+
+VOC_API voc_status vocoder_stream_decode(vocoder_stream *s, const float *latent_dev, int frames,
+                                         float *audio_dev, voc_stream_t stream_, unsigned flags) {
+  if (!s) return stream_fail(VOC_INVALID_ARG, "stream is NULL");
+  vocoder *ctx = s->ctx;
+  if (!latent_dev || !audio_dev) return fail(ctx, VOC_INVALID_ARG, "latent / audio NULL");
+  if (frames < 1 || frames > s->max_frames)
+    return fail(ctx, VOC_INVALID_ARG, "frames out of [1, max_frames]");
+  if (flags & ~static_cast<unsigned>(VOC_FLAG_SYNC))
+    return fail(ctx, VOC_INVALID_ARG, "only VOC_FLAG_SYNC is accepted");
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != ctx->device) return fail(ctx, VOC_INVALID_ARG, "current device differs from the context's");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  cudaError_t e;
+  voc_status st;
+#ifdef VOC_CHECKS
+  // the self-checking build synchronises after every launch, which a capture cannot hold
+  st = stream_launches(s, latent_dev, frames, audio_dev, stream);
   if (st != VOC_OK) return st;
+#else
+  // A chunk is a fixed sequence of about 40 small launches: it is captured once per chunk
+  // size into a CUDA graph over the staging buffers and replayed on the caller's stream.
+  if (!s->graphs[frames]) {
+    e = cudaStreamBeginCapture(s->cap, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamBeginCapture");
+    st = stream_launches(s, s->lat_stage, frames, s->aud_stage, s->cap);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(s->cap, &g);
+    if (st == VOC_OK && e != cudaSuccess) st = cuda_fail(ctx, e, "cudaStreamEndCapture");
+    cudaGraphExec_t exec = nullptr;
+    if (st == VOC_OK) {
+      e = cudaGraphInstantiate(&exec, g, 0);
+      if (e != cudaSuccess) st = cuda_fail(ctx, e, "cudaGraphInstantiate");
+    }
+    if (g) cudaGraphDestroy(g);
+    if (st != VOC_OK) {
+      (void)cudaGetLastError();
+      return st;
+    }
+    s->graphs[frames] = exec;
+  }
+  const size_t lat_bytes = (size_t)s->B * ctx->desc.latent_channels * frames * 4;
+  const size_t aud_bytes = (size_t)s->B * frames * ctx->hop * 4;
+  e = cudaMemcpyAsync(s->lat_stage, latent_dev, lat_bytes, cudaMemcpyDeviceToDevice, stream);
+  if (e == cudaSuccess) e = cudaGraphLaunch(s->graphs[frames], stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(audio_dev, s->aud_stage, aud_bytes, cudaMemcpyDeviceToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "stream chunk (graph replay)");
+#endif
   if (flags & VOC_FLAG_SYNC) {
     e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
@@ -2110,6 +2169,9 @@ VOC_API voc_status vocoder_stream_decode(vocoder_stream *s, const float *latent_
 
 VOC_API void vocoder_stream_destroy(vocoder_stream *s) {
   if (!s) return;
+  for (cudaGraphExec_t g : s->graphs)
+    if (g) cudaGraphExecDestroy(g);
+  if (s->cap) cudaStreamDestroy(s->cap);
   cudaFree(s->block);
   delete s;
 }
