@@ -468,7 +468,8 @@ class EncodeJob(DecodeJob):
         return self.V.vocoder_encoder_profile(self.ctx.handle)
 
     def launches(self):
-        return self.V.vocoder_encoder_launches(self.ctx.handle)
+        B, _, L = self.wl.latent.shape
+        return self.V.vocoder_encoder_launches(self.ctx.handle, B, L)
 
 
 def run_ours(args, rank, world, local_rank):

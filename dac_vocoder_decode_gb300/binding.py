@@ -190,7 +190,7 @@ def load_library():
     lib.vocoder_encode_host.argtypes = [P, P, I, ctypes.c_longlong, P, P, ctypes.c_size_t, P,
                                         ctypes.c_uint]
     lib.vocoder_encoder_launches.restype = I
-    lib.vocoder_encoder_launches.argtypes = [P]
+    lib.vocoder_encoder_launches.argtypes = [P, I, ctypes.c_longlong]
     lib.vocoder_encoder_profile_count.restype = I
     lib.vocoder_encoder_profile_count.argtypes = [P]
     lib.vocoder_encoder_profile_entry.restype = I
@@ -622,8 +622,8 @@ def vocoder_encode_host(h, audio_host, latent_host, ws, stream=None, flags: int 
                                                   _stream_ptr(stream), flags), h)
 
 
-def vocoder_encoder_launches(h) -> int:
-    return int(load_library().vocoder_encoder_launches(h))
+def vocoder_encoder_launches(h, B: int, L: int) -> int:
+    return int(load_library().vocoder_encoder_launches(h, B, L))
 
 
 def vocoder_encode(h, audio, latent, ws, stream=None, flags: int = 0) -> None:

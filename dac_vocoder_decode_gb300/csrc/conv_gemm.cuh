@@ -131,6 +131,10 @@ struct ConvGemmArgs {
   int kb_split;            // k-blocks kb < kb_split use taps [tap_lo0, tap_hi0), the others
   int tap_lo0, tap_hi0, tap_lo1, tap_hi1;  // [tap_lo1, tap_hi1) (a strided conv's two
                                            // phase groups each read two of its three taps)
+  int ksplit;              // >= 1: the k-blocks are split into ksplit ranges of kb_per_split,
+  int kb_per_split;        // one job per (range, tile); with ksplit > 1 the epilogue stores the
+  float *part;             // raw sums to part[((ks * B + b) * Cp_out/4 + chunk4) * part_L + row]
+  long long part_L;        // (4 floats each) and ksplit_reduce_kernel finishes the layer
   // Output head folded into this layer's epilogue (kernels with HEAD = true): the layer
   // writes no activations; each warp reduces its 32 rows x 16 channels of Snake_out(y) to
   // the 32 + head_K - 1 partial sums of the head's outputs those rows reach
@@ -577,6 +581,33 @@ __device__ __forceinline__ bool head_fold_store(const ConvGemmArgs &p, const flo
   return true;
 }
 
+// Split k (the encoder forms): one warp's 32 rows x CW columns of a k range's raw sums (the
+// two halves added in the B2 form), stored fp32 chunk-major for ksplit_reduce_kernel.  Every
+// lane reads TMEM (a warp-collective read) before the row check.
+template <int CW, bool B2>
+__device__ __forceinline__ bool raw_chunk_store(const ConvGemmArgs &p, volatile int *abort_flag,
+                                                int b, int t, int ks, int n0, uint32_t taddr) {
+  static_assert(CW == 16, "split k stores 16-column chunks");
+  uint32_t r[CW], r2[CW];
+  tmem_ld_issue<CW>(taddr, r);
+  if constexpr (B2) tmem_ld_issue<CW>(taddr + static_cast<uint32_t>(p.N_tile), r2);
+  tmem_ld_wait<CW>(r);
+  if constexpr (B2) {
+    tmem_ld16_after_wait(r2);
+#pragma unroll
+    for (int i = 0; i < CW; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+  }
+  if (t >= p.rows_pad) return true;
+  const size_t L = static_cast<size_t>(p.part_L);
+  const size_t base = (((size_t)ks * p.B + b) * (p.Cp_out / 4) + n0 / 4) * L + t;
+  VOC_CHECK(t < p.part_L && n0 + CW <= p.Cp_out && ks < p.ksplit, 24, t, n0, ks);
+#pragma unroll
+  for (int j = 0; j < CW / 4; ++j)
+    *reinterpret_cast<uint4 *>(p.part + (base + j * L) * 4) =
+        make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+  return true;
+}
+
 // Taps [tap0, tap1) that k-block kb reads (the encoder's strided convs skip one of three).
 __device__ __forceinline__ void tap_window(const ConvGemmArgs &p, int kb, int &tap0, int &tap1) {
   const bool second = kb >= p.kb_split;
@@ -716,7 +747,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
   pdl_launch_dependents();
 
-  const int total_jobs = p.B * p.m_tiles * p.n_tiles;
+  const int per_split = p.B * p.m_tiles * p.n_tiles;  // jobs of one k range
+  const int total_jobs = ENC ? per_split * p.ksplit : per_split;
+  // the tile index and the k-block range of a job (split k in the encoder forms)
+  auto job_range = [&](int job, int &jj, int &kb0, int &kb1, int &ks) {
+    if constexpr (ENC) {
+      ks = job / per_split;
+      jj = job - ks * per_split;
+      kb0 = ks * p.kb_per_split;
+      kb1 = min(p.nkb, kb0 + p.kb_per_split);
+    } else {
+      ks = 0, jj = job, kb0 = 0, kb1 = p.nkb;
+    }
+  };
   const int kchunks = p.KB / 8;
   const uint32_t chunkA = static_cast<uint32_t>(p.rows) * 16u;
   const int n_half = PAIR ? p.N_tile / 2 : p.N_tile;  // weight rows staged by this CTA
@@ -732,13 +775,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int ia = 0;
       bool ok = true;
       for (int job = job0; job < total_jobs && ok; job += job_step) {
-        const int rest = job / p.n_tiles;
+        int jj, kb0, kb1, ks;
+        job_range(job, jj, kb0, kb1, ks);
+        const int rest = jj / p.n_tiles;
         const int mt = rest % p.m_tiles;
         const int b = rest / p.m_tiles;
         // first staged row, rounded down to the 8-row group the tensor map addresses (the
         // host adds the remainder, the same for every job, to the MMA row shift)
         const int yg = floor_div8(p.in_row0 + mt * kM + row0 + p.off_min);
-        for (int kb = 0; kb < p.nkb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           const int sa = ia % p.na;
           const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;
           if (!mbar_wait(smem_u32(emptyA + sa), pha ^ 1u, p.timeout, abort_flag)) {
@@ -840,7 +885,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t pha = 0, phb = 0, phacc = 0;
       bool ok = true;
       for (int job = job0; job < total_jobs && ok; job += job_step) {
-        const int nt = job % p.n_tiles;
+        int jj, kb0, kb1, ks;
+        job_range(job, jj, kb0, kb1, ks);
+        const int nt = jj % p.n_tiles;
         const int shift0 = (nt >= p.q_split_tile) ? p.shift0_q1 : p.shift0_q0;
         if (!wait_all(smem_u32(accEmpty + acc), phacc ^ 1u, PAIR)) {
           ok = false;
@@ -849,7 +896,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * p.acc_cols);
         uint32_t accum = 0u;  // the first MMA of a job overwrites the accumulator
-        for (int kb = 0; kb < p.nkb && ok; ++kb) {
+        for (int kb = kb0; kb < kb1 && ok; ++kb) {
           if (!wait_all(smem_u32(fullA + sa), pha, false) ||
               (PAIR && !wait_all(smem_u32(pairA + sa), pha, true))) {
             ok = false;
@@ -938,9 +985,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // resident weights: one pass over the stages of the first job fills every slot
       const int job_end = p.b_resident ? min(total_jobs, job0 + 1) : total_jobs;
       for (int job = job0; job < job_end && ok; job += job_step) {
-        const int nt = job % p.n_tiles;
+        int jj, kb0, kb1, ks;
+        job_range(job, jj, kb0, kb1, ks);
+        const int nt = jj % p.n_tiles;
         const int wt = PAIR ? 2 * nt + static_cast<int>(rank) : nt;  // packed weight tile
-        for (int kb = 0; kb < p.nkb && ok; ++kb) {
+        for (int kb = kb0; kb < kb1 && ok; ++kb) {
           int tap0 = 0, tap1 = p.taps;
           if constexpr (ENC) tap_window(p, kb, tap0, tap1);
           for (int tap = tap0; tap < tap1; ++tap, ++ib) {
@@ -1047,8 +1096,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phacc = 0;
     bool ok = true;
     for (int job = job0; job < total_jobs && ok; job += job_step) {
-      const int nt = job % p.n_tiles;
-      const int rest = job / p.n_tiles;
+      int jj, kb0, kb1, ks;
+      job_range(job, jj, kb0, kb1, ks);
+      const int nt = jj % p.n_tiles;
+      const int rest = jj / p.n_tiles;
       const int mt = rest % p.m_tiles;
       const int b = rest / p.m_tiles;
       // decisions stay warp-uniform: tcgen05.ld is a warp-collective instruction
@@ -1065,6 +1116,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int blk = half; blk < p.N_tile / bw && ok; blk += kEpiGroups) {
           ok = convT_block_odd<F16>(p, abort_flag, b, t, nt * p.N_tile + blk * bw, tbase + blk * bw, lane);
           ok = __all_sync(0xffffffffu, ok);
+        }
+      }
+      if constexpr (ENC) {
+        if (p.ksplit > 1) {  // split k: this range's raw sums, finished by ksplit_reduce_kernel
+          for (int c = half; c < n_chunks && ok; c += kEpiGroups) {
+            ok = raw_chunk_store<CW, B2>(p, abort_flag, b, t, ks, nt * p.N_tile + c * CW,
+                                         tbase + c * CW);
+            ok = __all_sync(0xffffffffu, ok);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (!ok) break;
+          if (lane == 0) mbar_arrive(smem_u32(accEmpty + acc));
+          if (++acc == p.n_acc) acc = 0, phacc ^= 1u;
+          continue;
         }
       }
       for (int c = half; c < n_chunks && ok && !odd_blocks; c += kEpiGroups) {

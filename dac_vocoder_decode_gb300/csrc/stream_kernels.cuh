@@ -4,6 +4,7 @@
 //   out_head_reg_kernel the same for 7 taps, register-blocked (the decoder's head)
 //   stitch_kernel       overlap-crop stitch + clamp of windowed decodes
 //   head_finish_kernel  the folded output head: partial sums of the last conv2 -> audio
+//   ksplit_reduce_kernel the epilogue of a conv run with split k (the encoder's deep layers)
 //   finite_check_kernel flags a NaN / Inf in a buffer
 //   rows_to_cf_kernel   chunk-major fp32 -> channels-first fp32 (single-layer ops)
 #pragma once
@@ -236,6 +237,63 @@ __global__ void head_finish_kernel(const float *__restrict__ part, int L, int sl
     for (int c = 0; c < nch; ++c) acc += src[(size_t)c * slice_len];
   }
   audio[(size_t)b * L + t] = tanhf(acc);
+}
+
+// Split k: y = bias + the ksplit raw sums of part ([ks][B][Cp/4][part_L][4], added in ks
+// order), then the conv kernel's epilogue: fp32 output (y, or Snake(y) with f32_snake), and the
+// hi/lo split of Snake(y) (or y without alpha) into chunk-major planes; rows in
+// [rows_valid, rows_pad) are written as zeros.  One thread per (b, 8 channels, row): block
+// 256, grid (ceil(rows_pad / 256), Cp / 8, B).
+__global__ void ksplit_reduce_kernel(const float *__restrict__ part, int ksplit, int B, int Cp,
+                                     long long part_L, int rows_valid, int rows_pad,
+                                     const float *__restrict__ bias, const float *__restrict__ alpha,
+                                     const float *__restrict__ invb, int f32_snake,
+                                     float *__restrict__ out_f32, long long f32_L,
+                                     __nv_bfloat16 *__restrict__ out_hl, long long hl_L, int f16) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int g = blockIdx.y;  // 8-channel group
+  const int b = blockIdx.z;
+  if (t >= rows_pad) return;
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int ks = 0; ks < ksplit; ++ks) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float4 x = reinterpret_cast<const float4 *>(
+          part)[(((size_t)ks * B + b) * (Cp / 4) + 2 * g + h) * part_L + t];
+      v[4 * h] += x.x, v[4 * h + 1] += x.y, v[4 * h + 2] += x.z, v[4 * h + 3] += x.w;
+    }
+  }
+  float sn[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int c = 8 * g + i;
+    v[i] += bias[c];
+    sn[i] = alpha ? snake(v[i], alpha[c], invb[c]) : v[i];
+    if (t >= rows_valid) v[i] = 0.f, sn[i] = 0.f;
+  }
+  if (out_f32) {
+    const float *src = f32_snake ? sn : v;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      reinterpret_cast<float4 *>(out_f32)[((size_t)b * (Cp / 4) + 2 * g + h) * f32_L + t] =
+          make_float4(src[4 * h], src[4 * h + 1], src[4 * h + 2], src[4 * h + 3]);
+  }
+  if (out_hl) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (f16)
+        split_pair<true>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
+      else
+        split_pair<false>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
+    }
+    const size_t item = (size_t)b * (2 * Cp / 8);
+    *reinterpret_cast<uint4 *>(out_hl + ((item + g) * hl_L + t) * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4 *>(out_hl + ((item + Cp / 8 + g) * hl_L + t) * 8) =
+        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
 }
 
 __global__ void finite_check_kernel(const float *__restrict__ x, long long n, int *flag) {

@@ -369,6 +369,7 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   g.nkb = L.Cp_in / g.KB;
   // taps of each k-block (the encoder kernels read these): all, or for a strided conv taps
   // 1, 2 (row shifts 0, +1) in the first phase group and 0, 1 (-1, 0) in the second
+  g.ksplit = 1, g.kb_per_split = g.nkb;  // split k is chosen per encode (encoder layers)
   g.kb_split = L.down_s ? grp0 / g.KB : g.nkb;
   g.tap_lo0 = L.down_s ? 1 : 0, g.tap_hi0 = g.taps;
   g.tap_lo1 = 0, g.tap_hi1 = L.down_s ? 2 : g.taps;
@@ -879,7 +880,7 @@ cudaError_t launch_conv(const Layer &L, const ConvGemmArgs &a, int grid, const C
     return launch_pdl(voc::conv_gemm_kernel<16, false, false, false, PREC, false, true>, g, blk,
                       L.smem, stream, map, smap, a);
   }
-  if (a.split_s > 1 || L.down_s) {  // encoder forms: phase-split output, tap windows
+  if (a.split_s > 1 || L.down_s || a.ksplit > 1) {  // encoder forms: phase split, tap windows, split k
     if (kB2 && L.g.b2)
       return launch_pdl(voc::conv_gemm_kernel<16, false, kB2, false, PREC, true>, g, blk, L.smem,
                         stream, map, smap, a);
@@ -898,14 +899,15 @@ cudaError_t launch_conv(const Layer &L, const ConvGemmArgs &a, int grid, const C
 
 voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
                        const CUtensorMap &smap, const ConvGemmArgs &a, cudaStream_t stream) {
-  const long long tiles = (long long)a.B * a.m_tiles * a.n_tiles;
+  // jobs: tiles, times the k ranges of a split-k layer (encoder forms)
+  const long long tiles = (long long)a.B * a.m_tiles * a.n_tiles * std::max(1, a.ksplit);
   // Persistent grid: one CTA (or cluster) per unit, at most one per job.  With resident
   // weights every CTA must keep one column tile, so its job stride is a multiple of n_tiles.
   auto persistent = [&](long long units) {
     if (tiles <= units) return tiles;
     return a.b_resident ? units - units % a.n_tiles : units;
   };
-  if ((a.split_s > 1 || L.down_s) && (L.pair || L.convT || L.ru))
+  if ((a.split_s > 1 || L.down_s || a.ksplit > 1) && (L.pair || L.convT || L.ru))
     return fail(ctx, VOC_UNSUPPORTED, L.name + ": the encoder forms need a plain conv kernel");
   if (L.pair) {  // persistent grid of 2-CTA clusters, at most as many as can be resident
     cudaLaunchConfig_t cfg = {};
@@ -2364,6 +2366,30 @@ size_t enc_buf_bytes(const vocoder_encoder *enc, int B, long long L) {
   return rupz(m * (size_t)B * 4, 256);
 }
 
+// Split k for an encoder layer with `rows` GEMM rows per item: the number of k ranges (1..4)
+// that fills the SMs best when its tiles alone would leave many idle (the deep layers of the
+// low-rate blocks).  Only for layers without a residual input or phase-split output and with
+// streamed weights; each range holds at least one k-block and the raw sums of all ranges stay
+// within 64 MB (L2-sized) and the workspace slot that holds them.
+constexpr size_t kSplitPartMax = 64ull << 20;
+int enc_ksplit(const vocoder_encoder *enc, size_t i, int B, long long rows, size_t slot_bytes) {
+  const Layer &L = enc->layers[i];
+  if (L.skip_buf >= 0 || enc->split[i] || L.g.b_resident || L.g.nkb < 2) return 1;
+  const long long jobs = (long long)B * ((rows + voc::kTileM - 1) / voc::kTileM) * L.g.n_tiles;
+  const long long sms = std::max(1, enc->core.num_sms);
+  auto eff = [&](long long S) {
+    const long long n = S * jobs;
+    return (double)n / (double)(((n + sms - 1) / sms) * sms);
+  };
+  const size_t part1 = (size_t)B * L.Cp_out * (size_t)pitch8(rows) * 4;
+  int best = 1;
+  for (int S = 2; S <= std::min(4, L.g.nkb); ++S) {
+    if ((size_t)S * part1 > std::min(kSplitPartMax, slot_bytes)) break;
+    if (eff(S) > eff(best) + 1e-9) best = S;
+  }
+  return eff(best) >= 1.25 * eff(1) ? best : 1;  // at least a quarter more SMs busy
+}
+
 // Algorithmic cost of an encoder layer with L_in GEMM rows per item: a strided conv counts
 // its 2s taps over the C real channels, not the zero taps of its 3-tap form.
 void enc_layer_cost(const Layer &L, int B, long long L_in, double &flops, double &bytes) {
@@ -2585,11 +2611,16 @@ VOC_API long long vocoder_encoder_hop(const vocoder_encoder *enc) { return enc ?
 VOC_API size_t vocoder_encoder_workspace_bytes(const vocoder_encoder *enc, int B, long long L) {
   if (!enc || B < 1 || B > 65535 || L < 1 || L % enc->hop) return 0;
   if (L > (1LL << 30)) return 0;  // GEMM rows of one item stay in the kernels' int range
-  return 3 * enc_buf_bytes(enc, B, L);  // H0, H1 and FY (the encoder needs no third hi/lo buffer)
+  return 4 * enc_buf_bytes(enc, B, L);  // H0, H1, FY and the split-k raw sums
 }
 
-VOC_API int vocoder_encoder_launches(const vocoder_encoder *enc) {
-  return enc ? 2 + static_cast<int>(enc->layers.size()) : -1;
+VOC_API int vocoder_encoder_launches(const vocoder_encoder *enc, int B, long long L) {
+  if (!vocoder_encoder_workspace_bytes(enc, B, L)) return -1;
+  const size_t bb = enc_buf_bytes(enc, B, L);
+  int n = 2 + static_cast<int>(enc->layers.size());
+  for (size_t i = 0; i < enc->layers.size(); ++i)
+    if (enc_ksplit(enc, i, B, L / enc->div[i], bb) > 1) ++n;  // its reduce kernel
+  return n;
 }
 
 VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, int B, long long L,
@@ -2617,7 +2648,9 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
   const size_t bb = enc_buf_bytes(enc, B, L);
   void *bufs[BUF_COUNT];
   uint8_t *base = static_cast<uint8_t *>(ws);
-  bufs[BUF_H0] = base, bufs[BUF_H1] = base + bb, bufs[BUF_HB] = nullptr, bufs[BUF_FY] = base + 2 * bb;
+  // H0, H1, FY and (in the HB slot) the raw sums of split-k layers
+  bufs[BUF_H0] = base, bufs[BUF_H1] = base + bb, bufs[BUF_FY] = base + 2 * bb;
+  bufs[BUF_HB] = base + 3 * bb;
   const size_t n_layers = enc->layers.size();
   if (enc->map_ws != ws || enc->map_B != B || enc->map_L != L) {
     enc->maps.resize(n_layers);
@@ -2638,7 +2671,7 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
   }
 
   const bool prof = (flags & VOC_FLAG_PROFILE) != 0;
-  const int n_launch = vocoder_encoder_launches(enc);
+  const int n_launch = vocoder_encoder_launches(enc, B, L);
   if (prof) {
     while ((int)ctx->events.size() < 2 * n_launch) {
       cudaEvent_t ev;
@@ -2687,6 +2720,15 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
       a.rows_pad = static_cast<int>(rup_ll(rows, 8LL * s));
       a.m_tiles = (a.rows_pad + voc::kTileM - 1) / voc::kTileM;
     }
+    const int S = enc_ksplit(enc, i, B, rows, bb);
+    ConvGemmArgs fin = a;  // the layer's outputs, written by the reduce kernel when split
+    if (S > 1) {
+      a.ksplit = S;
+      a.kb_per_split = (Ly.g.nkb + S - 1) / S;
+      a.ksplit = (Ly.g.nkb + a.kb_per_split - 1) / a.kb_per_split;  // no empty range
+      a.part = static_cast<float *>(bufs[BUF_HB]);
+      a.part_L = pitch8(rows);
+    }
     rec(0);
     st = launch_gemm(ctx, Ly, enc->maps[i], enc->skip_maps[i], a, stream);
     if (st != VOC_OK) return st;
@@ -2697,6 +2739,33 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
     if (prof) {
       ctx->prof_names[li] = Ly.name;
       enc_layer_cost(Ly, B, rows, ctx->prof_flops[li], ctx->prof_bytes[li]);
+      if (S > 1)  // the outputs are the reduce kernel's
+        ctx->prof_bytes[li] += 4.0 * a.ksplit * B * (double)rows * Ly.Cp_out -
+                               (Ly.f32_buf >= 0 ? 4.0 : 0.0) * B * (double)rows * Ly.Cp_out -
+                               (Ly.hl_buf >= 0 ? 4.0 : 0.0) * B * (double)rows * Ly.Cp_out;
+    }
+    if (S > 1) {
+      ++li;
+      rec(0);
+      dim3 grid(static_cast<unsigned>((fin.rows_pad + 255) / 256), Ly.Cp_out / 8, B);
+      cudaError_t ce = launch_pdl(
+          voc::ksplit_reduce_kernel, grid, dim3(256), 0, stream,
+          static_cast<const float *>(a.part), a.ksplit, B, Ly.Cp_out, a.part_L, fin.rows_valid,
+          fin.rows_pad, static_cast<const float *>(Ly.bias_dev),
+          static_cast<const float *>(Ly.alpha_dev), static_cast<const float *>(Ly.invb_dev),
+          (Ly.epi_flags & voc::EPI_F32_SNAKE) ? 1 : 0, fin.out_f32, (long long)fin.f32_L,
+          fin.out_hl, (long long)fin.hl_L, ctx->prec == VOC_PREC_F16W ? 1 : 0);
+      if (ce != cudaSuccess) return cuda_fail(ctx, ce, ("launch reduce " + Ly.name).c_str());
+#ifdef VOC_CHECKS
+      if ((st = check_launch(ctx, Ly.name + ".reduce", stream)) != VOC_OK) return st;
+#endif
+      rec(1);
+      if (prof) {
+        ctx->prof_names[li] = Ly.name + ".reduce";
+        ctx->prof_flops[li] = 0.0;
+        ctx->prof_bytes[li] = 4.0 * B * (double)rows * Ly.Cp_out *
+                              (a.ksplit + (Ly.f32_buf >= 0 ? 1 : 0) + (Ly.hl_buf >= 0 ? 1 : 0));
+      }
     }
   }
   const long long Lz = L / enc->hop;

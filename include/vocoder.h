@@ -414,8 +414,9 @@ voc_status vocoder_encode_host(vocoder_encoder_t *enc, const float *audio_host, 
                                long long L, float *latent_host, void *ws_dev, size_t ws_bytes,
                                voc_stream_t stream, unsigned flags);
 
-/* Kernel launches of one vocoder_encode. */
-int vocoder_encoder_launches(const vocoder_encoder_t *enc);
+/* Kernel launches of one vocoder_encode of B items of L samples (-1 for invalid sizes): the
+ * deep layers of the low-rate blocks may run with split k, which adds a reduce launch each. */
+int vocoder_encoder_launches(const vocoder_encoder_t *enc, int B, long long L);
 
 /* Per-kernel records of the last encode run with VOC_FLAG_PROFILE, as vocoder_profile_*
  * for the decoder (a strided conv's FLOPs count its 2s taps over the real channels). */

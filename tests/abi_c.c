@@ -121,7 +121,7 @@ int main(void) {
                          0, (voc_stream_t)0, 0) == VOC_INVALID_ARG);
     CHECK(vocoder_encode_host((vocoder_encoder_t *)0, (const float *)0, 1, 512, (float *)0,
                               (void *)0, 0, (voc_stream_t)0, 0) == VOC_INVALID_ARG);
-    CHECK(vocoder_encoder_launches((const vocoder_encoder_t *)0) == -1);
+    CHECK(vocoder_encoder_launches((const vocoder_encoder_t *)0, 1, 512) == -1);
     CHECK(vocoder_encoder_profile_count((const vocoder_encoder_t *)0) == 0);
     CHECK(vocoder_encoder_profile_entry((vocoder_encoder_t *)0, 0, (const char **)0, (double *)0,
                                         (double *)0, (double *)0) == VOC_INVALID_ARG);

@@ -175,4 +175,4 @@ def test_encoder_create_validates_before_device_work(lib):
     assert "params[0]" in V.vocoder_encoder_last_error()
     assert V.vocoder_encoder_hop(None) == -1
     assert V.vocoder_encoder_workspace_bytes(None, 1, 512) == 0
-    assert V.vocoder_encoder_launches(None) == -1
+    assert V.vocoder_encoder_launches(None, 1, 512) == -1

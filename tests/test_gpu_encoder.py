@@ -129,7 +129,7 @@ def test_encode_profile_records_every_launch():
     enc = V.Encoder(arch, V.fold_params(wl.params))
     gpu_encode(enc, wl.latent, flags=V.VOC_FLAG_PROFILE)
     prof = V.vocoder_encoder_profile(enc.handle)
-    assert len(prof) == V.vocoder_encoder_launches(enc.handle)
+    assert len(prof) == V.vocoder_encoder_launches(enc.handle, B, wl.latent.shape[2])
     names = [p["name"] for p in prof]
     assert names[0] == "prep_audio" and names[-1] == "latent_out"
     assert "b0.down" in names and "b1.down" in names

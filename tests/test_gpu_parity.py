@@ -416,3 +416,19 @@ def test_profile_records_every_launch():
     assert len(prof) == V.vocoder_launches_per_decode(voc.handle, 1, wl.T)
     assert all(p["ms"] >= 0 for p in prof)
     assert sum(p["flops"] for p in prof) > 0
+
+
+@pytest.mark.parametrize("T", [1, 3, 4, 8, 9])
+def test_folded_head_and_its_fallback(T):
+    """The output head folded into the last conv2 (non-causal decoders) and its fallback to the
+    separate head when the fold's partial sums would not fit the buffer it borrows (a one-stage
+    decoder whose last stage is its widest: T <= 4 falls back, T >= 8 folds), both against the
+    oracle; and a causal decoder of the same shape (always the separate head)."""
+    sym = W.Arch(latent_channels=8, channels0=16, strides=(2,), widths=(64,))
+    for arch in (sym, dataclasses.replace(sym, strides=(3,), padding=W.PAD_CAUSAL)):
+        wl = W.make_custom(arch, B=2, T=T, seed=31 + T)
+        voc = V.Vocoder(arch, V.fold_params(wl.params))
+        got = G.gpu_decode(voc, wl.latent)
+        ref = O.decode(arch, wl.params, wl.latent)
+        G.compare_audio(ref, got, f"T={T} padding={arch.padding}")
+        voc.close()
