@@ -324,6 +324,10 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   for (int min_na = 3; min_na >= 2 && !g.KB && g.n_tiles <= kMaxResidentTiles; --min_na)
     for (int kb = L.Cp_in - L.Cp_in % 16; kb >= 16 && !g.KB; kb -= 16) {
       if (!kb_ok(kb) || 4 * kb * g.rows > 72 * 1024) continue;
+      // a k-tap conv keeps its weights resident only when one k-block covers its channels:
+      // with smaller k-blocks every tile restages its halo rows once per k-block, which costs
+      // more than streaming the weights (the encoder's C = 64 dilated convs: 0.167 -> 0.122 ms)
+      if (g.taps > 1 && kb != L.Cp_in) continue;
       if (taps_eff * (L.Cp_in / kb) > kMaxResidentStages) continue;
       const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
       const int ns = has_skip ? 2 * voc::kEpiGroups : 0;
