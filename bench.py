@@ -597,6 +597,7 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0:
         line = {"metric": metric_of(args.workload), "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+                "ms_per_step_median": max_over_ranks(statistics.median(step_ms), dev),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": {"f16w": "f16w (f16 weights, f16 hi/lo activations, fp32 accumulate)",
                           "bf16w": "bf16w (bf16 weights, bf16 hi/lo activations, fp32 accumulate)",
