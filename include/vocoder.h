@@ -300,7 +300,11 @@ voc_status vocoder_stream_create(vocoder_t *ctx, int B, int max_frames, vocoder_
  * asynchronous on `stream` like vocoder_decode.  Calls on one stream object must be
  * ordered (one stream, or synchronised); they update its contexts.  flags: 0 or
  * VOC_FLAG_SYNC (wait and report VOC_DEVICE_TIMEOUT).  Errors as vocoder_decode; the
- * message is vocoder_last_error(ctx). */
+ * message is vocoder_last_error(ctx).  The chunk's launches are captured into a CUDA graph the
+ * first time a chunk size is used (on a stream of the stream object's own; that call also
+ * instantiates the graph) and replayed afterwards: the call copies the latent into a staging
+ * buffer, launches the graph and copies the audio out, all on `stream`.  The stream object is
+ * therefore not usable from inside another stream capture. */
 voc_status vocoder_stream_decode(vocoder_stream_t *s, const float *latent_dev, int frames,
                                  float *audio_dev, voc_stream_t stream, unsigned flags);
 
