@@ -5,6 +5,7 @@
 //   stitch_kernel       overlap-crop stitch + clamp of windowed decodes
 //   head_finish_kernel  the folded output head: partial sums of the last conv2 -> audio
 //   ksplit_reduce_kernel the epilogue of a conv run with split k (the encoder's deep layers)
+//   audio_conv_in_kernel the encoder's conv_in on a few audio channels, direct in fp32
 //   finite_check_kernel flags a NaN / Inf in a buffer
 //   rows_to_cf_kernel   chunk-major fp32 -> channels-first fp32 (single-layer ops)
 #pragma once
@@ -292,6 +293,83 @@ __global__ void ksplit_reduce_kernel(const float *__restrict__ part, int ksplit,
     const size_t item = (size_t)b * (2 * Cp / 8);
     *reinterpret_cast<uint4 *>(out_hl + ((item + g) * hl_L + t) * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     *reinterpret_cast<uint4 *>(out_hl + ((item + Cp / 8 + g) * hl_L + t) * 8) =
+        make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+}
+
+// The encoder's conv_in on Cin (few) audio channels: y[c][t] = b[c] + sum_ci sum_k
+// w[c][ci][k] x[ci][t + k - pad], x zero outside [0, L), in fp32 on the CUDA cores (a 1-channel
+// input would fill one sixteenth of a tensor-core operand).  Writes the fp32 residual stream
+// y ([B][Cp/4][Lp][4]) and the hi/lo split of Snake(y) ([B][2 Cp/8][Lp][8], f16 parts when
+// f16 != 0); channels past C read zero weights, rows L..Lp-1 are zeros.  A block takes 8
+// channels (blockIdx.y) and kAudioRows x 256 rows: its weights (8 x Cin x K <= 8 x 4 x 15) are
+// staged in shared memory once, and each thread takes every 256th row of the block's range, so
+// every store is coalesced.  Grid (ceil(Lp / (256 kAudioRows)), Cp / 8, B), block 256.
+constexpr int kAudioRows = 8;
+constexpr int kAudioMaxW = 8 * 4 * 15;
+__global__ void audio_conv_in_kernel(const float *__restrict__ x, int Cin, int L, long long Lp,
+                                     int K, int pad, const float *__restrict__ w, int C,
+                                     const float *__restrict__ bias, const float *__restrict__ alpha,
+                                     const float *__restrict__ invb, int Cp,
+                                     float *__restrict__ out_f32, __nv_bfloat16 *__restrict__ out_hl,
+                                     int f16) {
+  __shared__ float ws[kAudioMaxW];  // [i][ci][k] for the block's channels 8 g + i
+  pdl_launch_dependents();
+  const int g = blockIdx.y;
+  const int b = blockIdx.z;
+  const int nw = 8 * Cin * K;
+  for (int e = threadIdx.x; e < nw && e < kAudioMaxW; e += blockDim.x) {
+    const int i = e / (Cin * K), r = e % (Cin * K);
+    const int c = 8 * g + i;
+    ws[e] = c < C ? w[(size_t)c * Cin * K + r] : 0.f;
+  }
+  float bb[8], a[8], ib[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int c = 8 * g + i;
+    bb[i] = bias[c];
+    a[i] = alpha ? alpha[c] : 0.f;
+    ib[i] = alpha ? invb[c] : 0.f;
+  }
+  __syncthreads();
+  pdl_wait();
+  const size_t item = (size_t)b * (2 * Cp / 8);
+  for (int j = 0; j < kAudioRows; ++j) {
+    const long long t = ((long long)blockIdx.x * kAudioRows + j) * blockDim.x + threadIdx.x;
+    if (t >= Lp) break;
+    float v[8], sn[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = bb[i];
+    if (t < L) {
+      for (int ci = 0; ci < Cin; ++ci) {
+        const float *xr = x + ((size_t)b * Cin + ci) * L;
+        for (int k = 0; k < K; ++k) {
+          const long long u = t + k - pad;
+          const float xv = (u >= 0 && u < L) ? __ldg(xr + u) : 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = fmaf(ws[(i * Cin + ci) * K + k], xv, v[i]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      sn[i] = alpha ? snake(v[i], a[i], ib[i]) : v[i];
+      if (t >= L) v[i] = 0.f, sn[i] = 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      reinterpret_cast<float4 *>(out_f32)[((size_t)b * (Cp / 4) + 2 * g + h) * Lp + t] =
+          make_float4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]);
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (f16)
+        split_pair<true>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
+      else
+        split_pair<false>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
+    }
+    *reinterpret_cast<uint4 *>(out_hl + ((item + g) * Lp + t) * 8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4 *>(out_hl + ((item + Cp / 8 + g) * Lp + t) * 8) =
         make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
 }

@@ -99,6 +99,10 @@ struct Layer {
   int cw = 16;              // epilogue column chunk (conv kernel: 16; fused unit: 16 or 32)
   bool pair = false;        // CTA-pair kernel: 256-row tiles, half of each weight tile per CTA
   int max_clusters = 0;     // pair: co-resident 2-CTA clusters of this launch shape
+  // the encoder's conv_in on a few audio channels, run directly in fp32 (audio_conv_in_kernel,
+  // weights wf_dev [Cout][Cin][K]) instead of as a GEMM over 16 padded channels
+  bool direct = false;
+  float *wf_dev = nullptr;
   // the output head folded into this layer's epilogue (the decoder's last conv2, in a
   // whole-sequence decode): partial sums go to hi/lo buffer head_buf, which it does not read
   bool head_fold = false;
@@ -2376,9 +2380,11 @@ size_t enc_buf_bytes(const vocoder_encoder *enc, int B, long long L) {
 // streamed weights; each range holds at least one k-block and the raw sums of all ranges stay
 // within 64 MB (L2-sized) and the workspace slot that holds them.
 constexpr size_t kSplitPartMax = 64ull << 20;
+// audio channels up to which the encoder's conv_in runs directly (audio_conv_in_kernel)
+constexpr int kAudioDirectMaxC = 4;
 int enc_ksplit(const vocoder_encoder *enc, size_t i, int B, long long rows, size_t slot_bytes) {
   const Layer &L = enc->layers[i];
-  if (L.skip_buf >= 0 || enc->split[i] || L.g.b_resident || L.g.nkb < 2) return 1;
+  if (L.direct || L.skip_buf >= 0 || enc->split[i] || L.g.b_resident || L.g.nkb < 2) return 1;
   const long long jobs = (long long)B * ((rows + voc::kTileM - 1) / voc::kTileM) * L.g.n_tiles;
   const long long sms = std::max(1, enc->core.num_sms);
   auto eff = [&](long long S) {
@@ -2545,8 +2551,31 @@ VOC_API voc_status vocoder_encoder_create(const voc_enc_desc *desc, const float 
     L.name = "conv_in";
     L.Cin = desc->in_channels, L.Cout = C, L.K = desc->in_kernel, L.dil = 1;
     L.in_buf = BUF_H0, L.f32_buf = BUF_FY, L.hl_buf = cur;
-    if ((st = add(L, false, params[0], params[1], snake_coef(params[2], C, desc->snake), div, 0)) != VOC_OK)
+    if (desc->in_channels <= kAudioDirectMaxC && desc->in_kernel <= 15) {  // weights fit kAudioMaxW
+      // direct fp32 kernel on the audio: weights as given (rounded like every conv weight in
+      // the one-plane precisions), the epilogue vectors of a plain conv
+      L.direct = true;
+      L.prec = ctx->prec;
+      L.Cp_in = rup(L.Cin, 16), L.Cp_out = rup(L.Cout, 16);
+      L.g.N_total = L.Cp_out, L.g.Cp_out = L.Cp_out;
+      std::vector<float> wf((size_t)L.Cout * L.Cin * L.K);
+      for (size_t k = 0; k < wf.size(); ++k) {
+        const float x = params[0][k];
+        wf[k] = ctx->prec == VOC_PREC_F16W    ? __half2float(__float2half_rn(x))
+                : ctx->prec == VOC_PREC_BF16W ? bf2f(f2bf(x))
+                                              : x;
+      }
+      if ((st = upload(ctx, ctx->allocs, wf, &L.wf_dev)) != VOC_OK) return bail(st);
+      if ((st = upload_columns(ctx, ctx->allocs, L, pad, params[1],
+                               snake_coef(params[2], C, desc->snake))) != VOC_OK)
+        return bail(st);
+      enc->layers.push_back(L);
+      enc->div.push_back(div);
+      enc->split.push_back(0);
+    } else if ((st = add(L, false, params[0], params[1], snake_coef(params[2], C, desc->snake), div,
+                         0)) != VOC_OK) {
       return bail(st);
+    }
   }
   int p = 2;
   for (int i = 0; i < desc->n_stages; ++i) {
@@ -2621,7 +2650,7 @@ VOC_API size_t vocoder_encoder_workspace_bytes(const vocoder_encoder *enc, int B
 VOC_API int vocoder_encoder_launches(const vocoder_encoder *enc, int B, long long L) {
   if (!vocoder_encoder_workspace_bytes(enc, B, L)) return -1;
   const size_t bb = enc_buf_bytes(enc, B, L);
-  int n = 2 + static_cast<int>(enc->layers.size());
+  int n = 2 + static_cast<int>(enc->layers.size()) - (enc->layers[0].direct ? 1 : 0);
   for (size_t i = 0; i < enc->layers.size(); ++i)
     if (enc_ksplit(enc, i, B, L / enc->div[i], bb) > 1) ++n;  // its reduce kernel
   return n;
@@ -2661,6 +2690,7 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
     enc->skip_maps.assign(n_layers, CUtensorMap{});
     for (size_t i = 0; i < n_layers; ++i) {
       const Layer &Ly = enc->layers[i];
+      if (Ly.direct) continue;  // reads the audio itself
       const long long rows = pitch8(L / enc->div[i]);
       voc_status st = encode_map(ctx, &enc->maps[i], bufs[Ly.in_buf], Ly.Cp_in, rows, B, Ly.g.rows,
                                  Ly.g.KB / 8);
@@ -2695,22 +2725,49 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
     if (prof) cudaEventRecord(ctx->events[2 * li + which], stream);
   };
   const int Ci = enc->desc.in_channels;
-  rec(0);
-  voc_status st = launch_prep(ctx, audio_dev, B, Ci, static_cast<int>(L), enc->Cp_audio, nullptr,
-                              nullptr, static_cast<__nv_bfloat16 *>(bufs[BUF_H0]), stream);
-  if (st != VOC_OK) return st;
+  voc_status st = VOC_OK;
+  if (!enc->layers[0].direct) {  // the audio as hi/lo planes for the conv_in GEMM
+    rec(0);
+    st = launch_prep(ctx, audio_dev, B, Ci, static_cast<int>(L), enc->Cp_audio, nullptr, nullptr,
+                     static_cast<__nv_bfloat16 *>(bufs[BUF_H0]), stream);
+    if (st != VOC_OK) return st;
 #ifdef VOC_CHECKS
-  if ((st = check_launch(ctx, "prep_audio", stream)) != VOC_OK) return st;
+    if ((st = check_launch(ctx, "prep_audio", stream)) != VOC_OK) return st;
 #endif
-  rec(1);
-  if (prof) {
-    ctx->prof_names[li] = "prep_audio";
-    ctx->prof_bytes[li] = (double)B * L * (4.0 * Ci + 4.0 * enc->Cp_audio);
+    rec(1);
+    if (prof) {
+      ctx->prof_names[li] = "prep_audio";
+      ctx->prof_bytes[li] = (double)B * L * (4.0 * Ci + 4.0 * enc->Cp_audio);
+    }
+    ++li;
   }
-  ++li;
   for (size_t i = 0; i < n_layers; ++i, ++li) {
     const Layer &Ly = enc->layers[i];
     const long long rows = L / enc->div[i];
+    if (Ly.direct) {  // conv_in on the audio, fp32 on the CUDA cores
+      const long long Lp = pitch8(rows);
+      rec(0);
+      cudaError_t ce = launch_pdl(
+          voc::audio_conv_in_kernel,
+          dim3(static_cast<unsigned>((Lp + 256 * voc::kAudioRows - 1) / (256 * voc::kAudioRows)),
+               Ly.Cp_out / 8, B),
+          dim3(256), 0, stream, audio_dev, Ci, static_cast<int>(rows), Lp, Ly.K, (Ly.K - 1) / 2,
+          static_cast<const float *>(Ly.wf_dev), Ly.Cout, static_cast<const float *>(Ly.bias_dev),
+          static_cast<const float *>(Ly.alpha_dev), static_cast<const float *>(Ly.invb_dev),
+          Ly.Cp_out, static_cast<float *>(bufs[Ly.f32_buf]),
+          static_cast<__nv_bfloat16 *>(bufs[Ly.hl_buf]), ctx->prec == VOC_PREC_F16W ? 1 : 0);
+      if (ce != cudaSuccess) return cuda_fail(ctx, ce, "launch audio conv_in");
+#ifdef VOC_CHECKS
+      if ((st = check_launch(ctx, Ly.name, stream)) != VOC_OK) return st;
+#endif
+      rec(1);
+      if (prof) {
+        ctx->prof_names[li] = Ly.name;
+        ctx->prof_flops[li] = 2.0 * Ly.Cin * Ly.Cout * Ly.K * B * (double)rows;
+        ctx->prof_bytes[li] = (double)B * rows * (4.0 * Ci + 8.0 * Ly.Cp_out);
+      }
+      continue;
+    }
     ConvGemmArgs a;
     gemm_args_rows(ctx, Ly, B, rows, bufs, bb, a);
     if (enc->split[i]) {

@@ -37,6 +37,8 @@ MIN_SNR_DB = 60.0
 SMALL = W.EncArch(1, 16, (2, 4), (32, 48), 8)
 ODD = W.EncArch(2, 24, (3, 5, 1), (40, 56, 56), 12, dilations=(1, 3))
 WIDE = W.EncArch(1, 48, (4, 2), (96, 200), 20)  # 200 channels: two column tiles, padded
+# more audio channels than the direct fp32 conv_in takes (4): conv_in as a tensor-core GEMM
+MULTI = W.EncArch(6, 16, (2, 4), (32, 48), 8)
 
 CASES = {
     # name: (arch, B, frames, seed)
@@ -46,6 +48,7 @@ CASES = {
     "wide": (WIDE, 1, 50, 14),
     "snake_beta": (dataclasses.replace(SMALL, snake_beta=True), 2, 21, 15),
     "music_short": (W.ENC_MUSIC, 1, 24, 16),
+    "six_channels": (MULTI, 2, 20, 17),
 }
 
 
@@ -131,9 +134,19 @@ def test_encode_profile_records_every_launch():
     prof = V.vocoder_encoder_profile(enc.handle)
     assert len(prof) == V.vocoder_encoder_launches(enc.handle, B, wl.latent.shape[2])
     names = [p["name"] for p in prof]
-    assert names[0] == "prep_audio" and names[-1] == "latent_out"
+    # one audio channel: conv_in runs directly on the audio (no hi/lo preparation launch)
+    assert names[0] == "conv_in" and names[-1] == "latent_out"
     assert "b0.down" in names and "b1.down" in names
     assert all(p["ms"] >= 0 for p in prof)
+    enc.close()
+    # six audio channels: the audio is prepared as hi/lo planes for the conv_in GEMM
+    arch, B, frames, seed = CASES["six_channels"]
+    wl = W.make_encode_workload(arch, B, frames, seed)
+    enc = V.Encoder(arch, V.fold_params(wl.params))
+    gpu_encode(enc, wl.latent, flags=V.VOC_FLAG_PROFILE)
+    names = [p["name"] for p in V.vocoder_encoder_profile(enc.handle)]
+    assert names[0] == "prep_audio" and names[1] == "conv_in"
+    assert len(names) == V.vocoder_encoder_launches(enc.handle, B, wl.latent.shape[2])
     enc.close()
 
 
