@@ -108,3 +108,24 @@ def test_cpu_threads_follows_omp(monkeypatch):
     assert bench.cpu_threads() == 3
     monkeypatch.delenv("OMP_NUM_THREADS")
     assert bench.cpu_threads() == (os.cpu_count() or 1)
+
+
+def test_clock_sampler_reads_a_fake_nvidia_smi(tmp_path, monkeypatch):
+    """start()/stop() around a stand-in nvidia-smi on PATH that prints three samples and then
+    keeps running until it is terminated, as the real one does with -lms."""
+    fake = tmp_path / "nvidia-smi"
+    rows = [smi_line(1900, 2070), smi_line(1920, 2070, pcap="Active"), smi_line(1940, 2070)]
+    fake.write_text("#!/bin/sh\n" + "".join(f"echo '{r}'\n" for r in rows) + "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ.get('PATH', '')}")
+    s = bench.ClockSampler(0)
+    s.start()
+    out = s.stop()
+    assert out == {"sm_mhz": 1920.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+
+
+def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
+    monkeypatch.setenv("PATH", str(tmp_path))  # an empty directory: no nvidia-smi to start
+    s = bench.ClockSampler(0)
+    s.start()
+    assert s.stop() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
