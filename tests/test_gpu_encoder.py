@@ -112,12 +112,17 @@ def test_encode_rejects_bad_lengths_and_workspace():
     wl = W.make_encode_workload(arch, B, frames, seed)
     enc = V.Encoder(arch, V.fold_params(wl.params))
     assert enc.workspace_bytes(B, enc.hop * frames + 1) == 0
+    assert enc.workspace_bytes(B, 0) == 0 and enc.workspace_bytes(0, enc.hop) == 0
     audio = torch.zeros((B, 1, enc.hop * 4 + 3), device="cuda")
     z = torch.empty((B, arch.latent_channels, 4), device="cuda")
     ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
     with pytest.raises(V.VocoderError) as e:
         V.vocoder_encode(enc.handle, audio, z, ws)
     assert e.value.status == V.VOC_INVALID_ARG
+    for empty in (audio[:, :, :0], audio[:0]):  # no samples, no items
+        with pytest.raises(V.VocoderError) as e:
+            V.vocoder_encode(enc.handle, empty, z, ws)
+        assert e.value.status == V.VOC_INVALID_ARG
     audio = torch.zeros((B, 1, enc.hop * 4), device="cuda")
     small = torch.empty(256, dtype=torch.uint8, device="cuda")
     with pytest.raises(V.VocoderError) as e:

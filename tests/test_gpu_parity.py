@@ -205,6 +205,26 @@ def test_decode_edge_lengths(T):
     G.compare_audio(ref, got, f"T={T}")
 
 
+def test_empty_inputs_are_rejected_and_leave_the_context_usable():
+    """B = 0 or T = 0 (zero-length views of a real latent, so the pointers are valid) is an
+    invalid argument, rejected before any launch; the next decode through the same context
+    gives the same audio bit for bit."""
+    wl = G.workload("tiny_cal")
+    voc = G.gpu_decoder(wl)
+    before = G.gpu_decode(voc, wl.latent)
+    lat = torch.from_numpy(wl.latent).cuda()
+    audio = torch.empty((wl.B, 1, wl.T * voc.hop), device="cuda")
+    ws = voc.alloc_workspace(wl.B, wl.T)
+    for bad in (lat[:, :, :0], lat[:0]):
+        with pytest.raises(V.VocoderError) as e:
+            V.vocoder_decode(voc.handle, bad, audio, ws)
+        assert e.value.status == V.VOC_INVALID_ARG
+    assert voc.workspace_bytes(0, wl.T) == 0 and voc.workspace_bytes(wl.B, 0) == 0
+    after = G.gpu_decode(voc, wl.latent)
+    assert np.array_equal(before, after)
+    voc.close()
+
+
 def test_batch_equals_items():
     """Items of a batch decode independently: identical to one-item decodes, bit for bit."""
     wl = G.workload("tiny_cal")

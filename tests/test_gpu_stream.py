@@ -78,9 +78,11 @@ def test_stream_rejections():
     voc = V.Vocoder(MID_CAUSAL, V.fold_params(wl.params))
     s = V.VocoderStream(voc, 1, 2)
     lat = torch.from_numpy(wl.latent).cuda()
-    with pytest.raises(V.VocoderError) as e:
-        s.decode(lat[:, :, :3].contiguous())
-    assert e.value.status == V.VOC_INVALID_ARG
+    for frames in (3, 0):  # more than max_frames, none
+        with pytest.raises(V.VocoderError) as e:
+            V.vocoder_stream_decode(voc.handle, s.handle, lat[:, :, :frames],
+                                    torch.empty((1, 1, 3 * voc.hop), device="cuda"))
+        assert e.value.status == V.VOC_INVALID_ARG
     music = G.workload("tiny")
     vm = G.gpu_decoder(music)
     with pytest.raises(V.VocoderError) as e:
