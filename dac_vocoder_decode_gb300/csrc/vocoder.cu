@@ -238,7 +238,17 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     g.taps = 2;
     g.N_total = s * L.Cp_out;
     g.s_rows = s;
-    if (padding == VOC_PAD_SYMMETRIC) {
+    // stride 2, symmetric: phase 0 reads rows t-1 and t, phase 1 rows t and t+1.  Both phases
+    // share one column tile as a 3-shift conv over rows t-1, t, t+1 (each phase's weights are
+    // zero on the shift it does not read), so a row block stages its input once and its two
+    // output rows leave as row pairs, instead of two half-width tiles staging the rows twice.
+    const bool shifts3 = padding == VOC_PAD_SYMMETRIC && s == 2 && L.Cp_out % 8 == 0;
+    if (shifts3) {
+      g.taps = 3;
+      group = g.N_total;
+      off_min = -1, off_max = 1;
+      g.shift0_q0 = g.shift0_q1 = 0;
+    } else if (padding == VOC_PAD_SYMMETRIC) {
       // phases r < s/2 read rows t and t-1 (q = 0), phases r >= s/2 rows t+1 and t (q = 1)
       group = (s / 2) * L.Cp_out;
       off_min = -1, off_max = 1;
@@ -248,7 +258,7 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
       off_min = -1, off_max = 0;
       g.shift0_q0 = 1, g.shift0_q1 = 1;
     }
-    g.tap_step = -1;
+    g.tap_step = shifts3 ? 1 : -1;
     // Output columns of a phase group of G phases: with G even, each 8-channel block holds
     // its G phases consecutively (8 columns per phase), so a 16-column epilogue chunk holds
     // two consecutive output rows of 8 channels and is written with 32-byte stores; with G
@@ -256,7 +266,7 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     // With G odd (causal s = 3, 5) the columns are blocked the same way and the epilogue
     // stores whole blocks through lane pairs (the causal output rows of a lane pair are 2G
     // consecutive rows); the column tile then holds whole blocks.
-    const int G = (padding == VOC_PAD_SYMMETRIC) ? s / 2 : s;
+    const int G = shifts3 ? 2 : (padding == VOC_PAD_SYMMETRIC) ? s / 2 : s;
     // (the CTA-pair kernel has no odd-phase epilogue)
     g.phase_group = (L.Cp_out % 8 == 0 && (G % 2 == 0 || (padding == VOC_PAD_CAUSAL && !L.pair)))
                         ? G : 0;
@@ -290,7 +300,8 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
     return false;
   }
   g.n_tiles = g.N_total / g.N_tile;
-  g.q_split_tile = (L.convT && padding == VOC_PAD_SYMMETRIC) ? group / g.N_tile : g.n_tiles;
+  g.q_split_tile = (L.convT && padding == VOC_PAD_SYMMETRIC && g.taps == 2) ? group / g.N_tile
+                                                                            : g.n_tiles;
   g.off_min = off_min;
   // the staged rows start at the 8-row group holding the first row (mod8(off_min) rows
   // earlier when the input rows start at a multiple of 8)
@@ -497,10 +508,9 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
 
 // Value of the GEMM weight for column n, input channel ci, tap `tap`.
 // ConvT column n -> (phase r, output channel co) in the column order of plan_gemm.
-void convT_column(const Layer &L, int padding, int n, int &r, int &co) {
-  const int s = L.stride;
-  const int G = (padding == VOC_PAD_SYMMETRIC) ? s / 2 : s;  // phases of one group
+void convT_column(const Layer &L, int n, int &r, int &co) {
   if (L.g.phase_group) {
+    const int G = L.g.phase_group;  // phases of one group
     const int gw = G * L.Cp_out;  // columns of one phase group
     const int q = n / gw, nn = n % gw;
     const int cg = nn / (8 * G), rem = nn % (8 * G);
@@ -534,9 +544,13 @@ float weight_value(const Layer &L, int padding, const float *w, int n, int ci, i
   }
   const int s = L.stride;
   int r, co;
-  convT_column(L, padding, n, r, co);
+  convT_column(L, n, r, co);
   if (co >= L.Cout) return 0.f;
   const int p = (padding == VOC_PAD_CAUSAL) ? 0 : s / 2;
+  if (L.g.taps == 3) {  // stride 2: tap u reads row t + u - 1, output row 2t + r
+    const int k = r + p - s * (tap - 1);
+    return (k < 0 || k >= 2 * s) ? 0.f : w[((size_t)ci * L.Cout + co) * (2 * s) + k];
+  }
   const int k = (r + p) % s + tap * s;  // tap 0: k0 at row t+q, tap 1: k0+s at row t+q-1
   return w[((size_t)ci * L.Cout + co) * (2 * s) + k];
 }
@@ -623,7 +637,7 @@ voc_status upload_columns(vocoder *ctx, std::vector<void *> &allocs, Layer &L, i
   std::vector<float> b(N, 0.f), a(N, 1.f), ib(N, 0.f);
   for (int n = 0; n < N; ++n) {
     int r = 0, co = n;
-    if (L.convT) convT_column(L, padding, n, r, co);
+    if (L.convT) convT_column(L, n, r, co);
     if (co < L.Cout) {
       if (bias) b[n] = bias[co];
       if (has_snake) {
