@@ -61,24 +61,39 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+# Workloads whose per-launch DRAM traffic is taken from another workload's ncu capture,
+# scaled by the ratio of latent frames per item (same architecture and batch): a capture of
+# the full-length decode would hold tens of GB on the device, and each layer's traffic grows
+# in proportion to its rows (the weights stay in L2).
+TRAFFIC_SCALED_FROM = {"music_long": "music_window"}
+
+
 def measured_traffic(workload: str, layer: str):
-    """DRAM bytes (read + write) of one launch of `layer`, from the ncu summary committed
-    under profiles/, or None when there is none or it was taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.md")
+    """DRAM bytes (read + write) of one launch of `layer` and where they come from, from the
+    ncu summary committed under profiles/; (None, None) when there is none or it was taken on
+    other kernel sources."""
+    src = TRAFFIC_SCALED_FROM.get(workload, workload)
+    path = os.path.join(ROOT, "profiles", f"traffic_{src}.md")
     if not os.path.exists(path):
-        return None
+        return None, None
     with open(path) as f:
         text = f.read()
     if f"source hash: {source_hash()}" not in text:
-        return None
+        return None, None
     for ln in text.splitlines():
         cells = [c.strip() for c in ln.strip().strip("|").split("|")]
         if len(cells) >= 4 and cells[0] == layer:
             try:
-                return int(cells[3])
+                value = int(cells[3])
             except ValueError:
-                return None
-    return None
+                return None, None
+            if src == workload:
+                return value, f"ncu capture of {workload} (profiles/traffic_{src}.md)"
+            T_src, T_dst = W.WORKLOADS[src][2][2], W.WORKLOADS[workload][2][2]
+            return (int(round(value * T_dst / T_src)),
+                    f"ncu capture of {src} (profiles/traffic_{src}.md) scaled by "
+                    f"{T_dst}/{T_src} latent frames per item")
+    return None, None
 
 
 def load_peaks():
@@ -532,7 +547,8 @@ def run_ours(args, rank, world, local_rank):
                 if flags & V.VOC_FLAG_PROFILE:
                     for i, p in enumerate(job.profile()):
                         rec = per_kernel.setdefault(i, dict(name=p["name"], ms=[],
-                                                            flops=p["flops"], bytes=p["bytes"]))
+                                                            flops=p["flops"], bytes=p["bytes"],
+                                                            impl_bytes=p.get("impl_bytes")))
                         rec["ms"].append(p["ms"])
 
     clocks = ClockSampler(local_rank)
@@ -583,22 +599,27 @@ def run_ours(args, rank, world, local_rank):
         ai = r["flops"] / r["bytes"] if r["bytes"] else 0.0
         bound = "tensor" if (r["flops"] > 0 and ai > ridge) else "hbm"
         frac = tfl / tc_peak if bound == "tensor" else gbs / hbm
+        impl = r.get("impl_bytes") or 0.0
         stages.append(dict(name=r["name"], ms=round(avg, 4), tflops=round(tfl, 2),
-                           gbs=round(gbs, 1), ai=round(ai, 1), bound=bound, frac=round(frac, 3)))
+                           gbs=round(gbs, 1), ai=round(ai, 1), bound=bound, frac=round(frac, 3),
+                           bytes=r["bytes"], impl_bytes=impl,
+                           impl_gbs=round(impl / (avg / 1e3) / 1e9, 1) if avg > 0 else 0.0))
     dom = max(stages, key=lambda s: s["ms"])
     dom_rec = next(per_kernel[i] for i in per_kernel if per_kernel[i]["name"] == dom["name"])
-    traffic = measured_traffic(args.workload, dom["name"])
-    per_launch = {"flops": dom_rec["flops"], "bytes": dom_rec["bytes"], "avg_ms": dom["ms"]}
+    traffic, traffic_src = measured_traffic(args.workload, dom["name"])
+    per_launch = {"flops": dom_rec["flops"], "bytes": dom_rec["bytes"],
+                  "impl_bytes": dom_rec.get("impl_bytes"), "avg_ms": dom["ms"]}
     if dom["bound"] == "tensor":
         roof = {"bound": "tensor", "kernel": dom["name"], "achieved": dom["tflops"],
                 "peak": round(tc_peak, 1), "unit": "TFLOP/s", "frac": dom["frac"],
-                "traffic": traffic, "per_launch": per_launch,
+                "traffic": traffic, "traffic_source": traffic_src, "per_launch": per_launch,
                 "peak_note": (f"bf16 dense {peaks_kind} burst / 2 (two {'f16' if f16w else 'bf16'} "
                               f"MMAs per useful MAC)" if one_plane else
                               f"bf16 dense {peaks_kind} burst / 3 (three bf16 MMAs per useful MAC)")}
     else:
         roof = {"bound": "hbm", "kernel": dom["name"], "achieved": dom["gbs"], "peak": hbm,
-                "unit": "GB/s", "frac": dom["frac"], "traffic": traffic, "per_launch": per_launch,
+                "unit": "GB/s", "frac": dom["frac"], "traffic": traffic,
+                "traffic_source": traffic_src, "per_launch": per_launch,
                 "peak_note": f"HBM copy bandwidth ({peaks_kind})"}
 
     line = None
@@ -646,7 +667,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="music_window",
+    ap.add_argument("--workload", default="music_long",
                     choices=sorted(W.WORKLOADS) + sorted(W.ENC_WORKLOADS))
     ap.add_argument("--cpu-frames", type=int, default=None,
                     help="latent frames of one item the CPU baseline decodes or encodes (about "

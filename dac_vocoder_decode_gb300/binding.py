@@ -48,7 +48,9 @@ EXPORTED = [
     "vocoder_stitched_length", "vocoder_stitch", "vocoder_op_conv1d",
     "vocoder_op_conv_transpose1d", "vocoder_op_residual_unit", "vocoder_launches_per_decode",
     "vocoder_profile_count",
-    "vocoder_profile_entry", "vocoder_last_error", "vocoder_destroy",
+    "vocoder_profile_entry", "vocoder_profile_impl_bytes", "vocoder_last_error",
+    "vocoder_destroy", "vocoder_set_cancel_flag", "vocoder_set_wait_budget",
+    "vocoder_debug_fail_allocation", "vocoder_debug_live_allocations",
     "vocoder_stream_create", "vocoder_stream_decode", "vocoder_stream_reset",
     "vocoder_stream_destroy", "vocoder_wav_bytes", "vocoder_wav_scratch_bytes",
     "vocoder_encode_wav",
@@ -56,6 +58,7 @@ EXPORTED = [
     "vocoder_encoder_hop", "vocoder_encoder_workspace_bytes", "vocoder_encode",
     "vocoder_encoder_workspace_bytes_host", "vocoder_encode_host",
     "vocoder_encoder_launches", "vocoder_encoder_profile_count", "vocoder_encoder_profile_entry",
+    "vocoder_encoder_profile_impl_bytes",
     "vocoder_encoder_last_error", "vocoder_encoder_destroy",
 ]
 
@@ -151,10 +154,20 @@ def load_library():
                                           ctypes.POINTER(ctypes.c_double),
                                           ctypes.POINTER(ctypes.c_double),
                                           ctypes.POINTER(ctypes.c_double)]
+    lib.vocoder_profile_impl_bytes.restype = I
+    lib.vocoder_profile_impl_bytes.argtypes = [P, I, ctypes.POINTER(ctypes.c_double)]
     lib.vocoder_last_error.restype = ctypes.c_char_p
     lib.vocoder_last_error.argtypes = [P]
     lib.vocoder_destroy.restype = None
     lib.vocoder_destroy.argtypes = [P]
+    lib.vocoder_set_cancel_flag.restype = I
+    lib.vocoder_set_cancel_flag.argtypes = [P, P]
+    lib.vocoder_set_wait_budget.restype = I
+    lib.vocoder_set_wait_budget.argtypes = [P, ctypes.c_longlong]
+    lib.vocoder_debug_fail_allocation.restype = None
+    lib.vocoder_debug_fail_allocation.argtypes = [I]
+    lib.vocoder_debug_live_allocations.restype = ctypes.c_longlong
+    lib.vocoder_debug_live_allocations.argtypes = []
     lib.vocoder_wav_bytes.restype = ctypes.c_size_t
     lib.vocoder_wav_bytes.argtypes = [I, ctypes.c_longlong, I]
     lib.vocoder_wav_scratch_bytes.restype = ctypes.c_size_t
@@ -198,6 +211,8 @@ def load_library():
                                                   ctypes.POINTER(ctypes.c_double),
                                                   ctypes.POINTER(ctypes.c_double),
                                                   ctypes.POINTER(ctypes.c_double)]
+    lib.vocoder_encoder_profile_impl_bytes.restype = I
+    lib.vocoder_encoder_profile_impl_bytes.argtypes = [P, I, ctypes.POINTER(ctypes.c_double)]
     lib.vocoder_encoder_last_error.restype = ctypes.c_char_p
     lib.vocoder_encoder_last_error.argtypes = [P]
     lib.vocoder_encoder_destroy.restype = None
@@ -395,8 +410,30 @@ def vocoder_profile(h) -> List[dict]:
         ms, fl, by = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
         _check(lib.vocoder_profile_entry(h, i, ctypes.byref(name), ctypes.byref(ms),
                                           ctypes.byref(fl), ctypes.byref(by)), h)
-        out.append(dict(name=name.value.decode(), ms=ms.value, flops=fl.value, bytes=by.value))
+        ib = ctypes.c_double()
+        _check(lib.vocoder_profile_impl_bytes(h, i, ctypes.byref(ib)), h)
+        out.append(dict(name=name.value.decode(), ms=ms.value, flops=fl.value, bytes=by.value,
+                        impl_bytes=ib.value))
     return out
+
+
+def vocoder_set_cancel_flag(h, flag: Optional[ctypes.c_int]) -> None:
+    """Register a host int (a ctypes.c_int the caller keeps alive) as the context's cancel
+    flag; None removes it."""
+    ptr = ctypes.cast(ctypes.pointer(flag), ctypes.c_void_p) if flag is not None else None
+    _check(load_library().vocoder_set_cancel_flag(h, ptr), h)
+
+
+def vocoder_set_wait_budget(h, cycles: int) -> None:
+    _check(load_library().vocoder_set_wait_budget(h, int(cycles)), h)
+
+
+def vocoder_debug_fail_allocation(n: int) -> None:
+    load_library().vocoder_debug_fail_allocation(int(n))
+
+
+def vocoder_debug_live_allocations() -> int:
+    return int(load_library().vocoder_debug_live_allocations())
 
 
 def vocoder_last_error(h=None) -> str:
@@ -644,7 +681,10 @@ def vocoder_encoder_profile(h) -> List[dict]:
         ms, fl, by = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
         _check_enc(lib.vocoder_encoder_profile_entry(h, i, ctypes.byref(name), ctypes.byref(ms),
                                                      ctypes.byref(fl), ctypes.byref(by)), h)
-        out.append(dict(name=name.value.decode(), ms=ms.value, flops=fl.value, bytes=by.value))
+        ib = ctypes.c_double()
+        _check_enc(lib.vocoder_encoder_profile_impl_bytes(h, i, ctypes.byref(ib)), h)
+        out.append(dict(name=name.value.decode(), ms=ms.value, flops=fl.value, bytes=by.value,
+                        impl_bytes=ib.value))
     return out
 
 

@@ -60,6 +60,11 @@ constexpr int kRuEpiWarps = 8;
 constexpr int kRuSkipWarp = 2 + kRuEpiWarps;
 constexpr int kRuThreads = 32 * (kRuSkipWarp + 1);      // 352
 constexpr int kMaxAcc = 4;
+// Bound on the waits of a kernel that has given up (ConvGemmArgs::timeout ran out, or another
+// role raised the abort flag) for its own copies and MMAs in flight: those were issued and
+// complete in microseconds, so the bound is long and independent of the pipeline waits' budget
+// -- a CTA must not exit (and free its shared memory and TMEM) while they can still land.
+constexpr long long kDrainBudget = 4000000000LL;
 
 // bytes of one residual slot (128 rows x cw fp32 columns, as cw/4 chunks of 128 x 16 B)
 __host__ __device__ constexpr int skip_slot_bytes(int cw) { return kTileM * cw * 4; }
@@ -808,7 +813,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) {
         atomicOr(p.err, ERR_TIMEOUT_PRODUCER);
         raise_abort();
-        drain_ring(fullA, p.na, ia, p.timeout);  // copies in flight land before the CTA exits
+        drain_ring(fullA, p.na, ia, kDrainBudget);  // copies in flight land before the CTA exits
       }
     }
   } else if (warp == 1) {
@@ -971,7 +976,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else
           mma_commit_warp(smem_u32(drain));
         const volatile int never = 0;
-        mbar_wait(smem_u32(drain), 0u, p.timeout, &never);
+        mbar_wait(smem_u32(drain), 0u, kDrainBudget, &never);
       }
     }
   } else if (warp >= kBWarp) {
@@ -1021,7 +1026,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         atomicOr(p.err, ERR_TIMEOUT_PRODUCER);
         raise_abort();
         // this warp's slots j, j + kBWarps, ... form a ring of nb / kBWarps slots
-        drain_ring_strided(fullB + j, p.nb / kBWarps, kBWarps, mine, p.timeout);
+        drain_ring_strided(fullB + j, p.nb / kBWarps, kBWarps, mine, kDrainBudget);
       }
     }
   } else if (warp == kSkipWarp) {
@@ -1075,7 +1080,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         atomicOr(p.err, ERR_TIMEOUT_SKIP);
         raise_abort();
 #pragma unroll
-        for (int h = 0; h < kEpiGroups; ++h) drain_ring(skipFull + h * nsh, nsh, cnt[h], p.timeout);
+        for (int h = 0; h < kEpiGroups; ++h) drain_ring(skipFull + h * nsh, nsh, cnt[h], kDrainBudget);
       }
     }
   } else {

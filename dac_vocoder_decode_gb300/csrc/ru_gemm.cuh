@@ -199,8 +199,8 @@ __global__ void __launch_bounds__(kRuThreads, 1)
       if (!ok) {
         atomicOr(p.err, ERR_TIMEOUT_PRODUCER);
         *abort_flag = 1;
-        drain_ring(fullA, p.na, ia, p.timeout);
-        drain_ring(fullB, p.nb, ib, p.timeout);
+        drain_ring(fullA, p.na, ia, kDrainBudget);
+        drain_ring(fullB, p.nb, ib, kDrainBudget);
       }
     }
   } else if (warp == 1) {
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         }
         mma_commit_warp(smem_u32(drain));
         const volatile int never = 0;
-        mbar_wait(smem_u32(drain), 0u, p.timeout, &never);
+        mbar_wait(smem_u32(drain), 0u, kDrainBudget, &never);
       }
     }
   } else if (warp == kRuSkipWarp) {
@@ -355,8 +355,8 @@ __global__ void __launch_bounds__(kRuThreads, 1)
       if (!ok) {
         atomicOr(p.err, ERR_TIMEOUT_SKIP);
         *abort_flag = 1;
-        drain_ring(skipFull, nsh, cnt[0], p.timeout);
-        drain_ring(skipFull + nsh, nsh, cnt[1], p.timeout);
+        drain_ring(skipFull, nsh, cnt[0], kDrainBudget);
+        drain_ring(skipFull + nsh, nsh, cnt[1], kDrainBudget);
       }
     }
   } else {

@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <utility>
@@ -39,6 +40,30 @@ constexpr int kMinAInFlight = 48 * 1024;  // A ring bytes a resident plan must k
 constexpr int kBStageMax = 36 * 1024;  // bytes of one weight stage (per CTA)
 
 thread_local std::string g_err;  // last error without a context
+
+// Every device allocation of the library goes through dev_alloc / dev_free, which keep a
+// count of the live ones and can be told to fail one on purpose (the allocation-failure
+// test hook vocoder_debug_fail_allocation).
+std::atomic<long long> g_live_allocs{0};
+std::atomic<int> g_fail_countdown{-1};  // >= 0: allocations to let through before one fails
+
+cudaError_t dev_alloc(void **p, size_t bytes) {
+  int n = g_fail_countdown.load();
+  while (n >= 0 && !g_fail_countdown.compare_exchange_weak(n, n - 1)) {
+  }
+  if (n == 0) {  // this one fails, as cudaMalloc does when the device is out of memory
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  const cudaError_t e = cudaMalloc(p, bytes);
+  if (e == cudaSuccess) ++g_live_allocs;
+  return e;
+}
+
+void dev_free(void *p) {
+  if (!p) return;
+  if (cudaFree(p) == cudaSuccess) --g_live_allocs;
+}
 
 int rup(int x, int m) { return (x + m - 1) / m * m; }
 // Launch with programmatic stream serialization: the kernel may be scheduled while the
@@ -196,14 +221,22 @@ struct vocoder {
   int fuse_max_c = 0;       // residual units of up to this many (padded) channels run fused
   bool use_pair = true;     // conv layers on CTA pairs
   int prec = VOC_PREC_BF16X3;  // VOC_PREC_*: the weight form of every conv
-  // TMA descriptors for the last (workspace, B, T)
-  void *map_ws = nullptr;
-  int map_B = -1, map_T = -1;
-  std::vector<CUtensorMap> maps, skip_maps;
+  // TMA descriptors of the two most recent (workspace, B, T) of a decode, each set sized for
+  // every layer at create time, so that a decode encodes descriptors only for a new
+  // combination and never resizes them (a caller alternating two workspaces, e.g. its own
+  // and the no-allocation decode's, re-encodes nothing)
+  struct MapSet {
+    void *ws = nullptr;
+    int B = -1, T = -1;
+    std::vector<CUtensorMap> maps, skip_maps;
+  };
+  MapSet map_sets[2];
+  int map_lru = 0;  // the set a new combination replaces
+  const volatile int *cancel = nullptr;  // caller's cancel flag (vocoder_set_cancel_flag)
   // profiling of the last decode with VOC_FLAG_PROFILE
   std::vector<cudaEvent_t> events;
   std::vector<std::string> prof_names;
-  std::vector<double> prof_flops, prof_bytes;
+  std::vector<double> prof_flops, prof_bytes, prof_impl;  // algorithmic / implementation bytes
   std::vector<float> prof_ms;
   int prof_n = 0;
   bool prof_ready = false;
@@ -595,7 +628,7 @@ std::vector<uint16_t> pack_weights(const Layer &L, int padding, const float *w) 
 
 template <class T>
 voc_status upload(vocoder *ctx, std::vector<void *> &allocs, const std::vector<T> &host, T **dev) {
-  cudaError_t e = cudaMalloc(reinterpret_cast<void **>(dev), host.size() * sizeof(T));
+  cudaError_t e = dev_alloc(reinterpret_cast<void **>(dev), host.size() * sizeof(T));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMalloc");
   allocs.push_back(*dev);
   e = cudaMemcpy(*dev, host.data(), host.size() * sizeof(T), cudaMemcpyHostToDevice);
@@ -867,14 +900,25 @@ double head_part_floats(const vocoder *ctx, const Layer &L, long long Lf) {
   return (double)slices * (L.Cp_out / 16) * (32 + voc::kHeadFoldMaxK - 1);
 }
 
-// folded: whether this launch of L carries the folded output head (L.head_fold and room for
-// its partial sums)
-void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops, double &bytes,
-                bool folded = false) {
+// Cost of one launch of layer L for the per-kernel rooflines.  flops: 2 per multiply-add of
+// the method (a transposed conv without its zero-stuffed taps).  alg: the algorithmic HBM
+// bytes -- every input of the layer read once and every output written once, as fp32 values
+// of the real channels (a k-tap conv 4 Cin + 4 Cout per row; a 1x1 conv with the residual add
+// also reads the skip, 4 Cout more; a transposed conv 4 Cin per input row and 4 Cout per output
+// sample; a fused residual unit reads x once, for conv1 and for the skip, and writes y).  A
+// launch carrying the folded output head (`folded`) writes no activations: its result leaves
+// through the head, whose audio is counted on the finishing launch.  impl: the bytes the
+// implementation moves by its own count -- padded channels, the weight stream, the fp32
+// stream and the hi/lo operand copies of every output.
+void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops, double &alg,
+                double &impl, bool folded = false) {
   const double L_in = (double)level_len(ctx, L.level, T);
   const double L_out = L_in * (L.convT ? L.stride : 1);
   flops = L.convT ? 4.0 * L.Cin * L.Cout * B * L_out : 2.0 * L.Cin * L.Cout * L.K * B * L_in;
   if (L.ru) flops = 2.0 * L.Cin * L.Cout * (L.K + 1) * B * L_in;
+  alg = 4.0 * L.Cin * B * L_in;
+  if (L.skip_buf >= 0 && !L.ru) alg += 4.0 * L.Cout * B * L_out;
+  if (!folded) alg += 4.0 * L.Cout * B * L_out;
   const ConvGemmArgs &g = L.g;
   double by = 4.0 * B * L_in * L.Cp_in +
               (double)g.n_tiles * (L.pair ? 2 : 1) * (g.taps + (L.ru ? 1 : 0)) * g.nkb * g.b_bytes;
@@ -886,7 +930,7 @@ void layer_cost(const vocoder *ctx, const Layer &L, int B, int T, double &flops,
     by += 4.0 * B * head_part_floats(ctx, L, (long long)L_out);
     flops += 2.0 * ctx->head.C * ctx->head.K * B * L_out;
   }
-  bytes = by;
+  impl = by;
 }
 
 // One launch of the single-CTA conv kernel of precision PREC in the form the layer needs.
@@ -1089,10 +1133,44 @@ VOC_API voc_status vocoder_fold_weight_norm(const float *g, const float *v, int 
 
 VOC_API void vocoder_destroy(vocoder *ctx) {
   if (!ctx) return;
-  for (void *p : ctx->allocs) cudaFree(p);
+  for (void *p : ctx->allocs) dev_free(p);
   for (cudaEvent_t e : ctx->events) cudaEventDestroy(e);
   delete ctx;
 }
+
+// ------------------------------------------------------------------ no-allocation workspace
+// The workspace of vocoder_decode_static: one array per device, in the library's module.
+static __device__ __align__(256) uint8_t g_static_ws[VOC_STATIC_WORKSPACE_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_ws_addr[kMaxDevices] = {};  // device address of g_static_ws, per device
+
+// Set-up of the no-allocation decode on the current device (vocoder_create calls it with the
+// context's device current): look up the device address of g_static_ws once per device.  Host
+// code may not take &g_static_ws itself -- on the host that name is a stand-in, not a device
+// address.
+voc_status static_ws_setup(vocoder *ctx) {
+  if (ctx->device < 0 || ctx->device >= kMaxDevices) return VOC_OK;  // decode_static refuses
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ws_addr[ctx->device]) return VOC_OK;
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_ws);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetSymbolAddress (no-allocation workspace)");
+  g_static_ws_addr[ctx->device] = p;
+  return VOC_OK;
+}
+
+void *static_ws_addr(int device) {
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  return g_static_ws_addr[device];
+}
+
+// The caller's cancel flag is set: nothing may be enqueued.
+bool cancelled(const vocoder *ctx) { return ctx->cancel && *ctx->cancel != 0; }
+}  // namespace
 
 VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *params, int n_params,
                                   vocoder **out) {
@@ -1147,6 +1225,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     vocoder_destroy(ctx);
     return st;
   };
+  voc_status st0;
   cudaError_t e = cudaGetDevice(&ctx->device);
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaGetDevice"));
   e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
@@ -1156,11 +1235,12 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
   cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
   if (cc_major != 10 || cc_minor != 3)
     return bail(fail(ctx, VOC_UNSUPPORTED, "this build targets sm_103 (GB300) only"));
-  e = cudaMalloc(&ctx->err_dev, 8 * sizeof(int));  // [0] error word, [1] finite flag, [4..7] checks
+  e = dev_alloc(reinterpret_cast<void **>(&ctx->err_dev), 8 * sizeof(int));  // [0] error word, [1] finite flag, [4..7] checks
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaMalloc"));
   ctx->allocs.push_back(ctx->err_dev);
   ctx->flag_dev = ctx->err_dev + 1;
   cudaMemset(ctx->err_dev, 0, 8 * sizeof(int));
+  if ((st0 = static_ws_setup(ctx)) != VOC_OK) return bail(st0);
 
   const int pad = desc->padding;
   auto plan = [&](Layer &L, bool has_skip) {
@@ -1341,6 +1421,10 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
         }
     }
   }
+  for (vocoder::MapSet &c : ctx->map_sets) {
+    c.maps.assign(ctx->layers.size(), CUtensorMap{});
+    c.skip_maps.assign(ctx->layers.size(), CUtensorMap{});
+  }
   *out = ctx;
   return VOC_OK;
 }
@@ -1409,22 +1493,29 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
   for (int i = 0; i < BUF_COUNT; ++i) bufs[i] = static_cast<uint8_t *>(ws) + i * bb;
 
   // TMA descriptors depend on the workspace address and the sizes only
-  if (ctx->map_ws != ws || ctx->map_B != B || ctx->map_T != T) {
-    ctx->maps.resize(ctx->layers.size());
-    ctx->skip_maps.assign(ctx->layers.size(), CUtensorMap{});
+  vocoder::MapSet *ms = nullptr;
+  for (int k = 0; k < 2; ++k) {
+    vocoder::MapSet &c = ctx->map_sets[k];
+    if (c.ws == ws && c.B == B && c.T == T) {
+      ms = &c;
+      ctx->map_lru = 1 - k;
+    }
+  }
+  if (!ms) {
+    ms = &ctx->map_sets[ctx->map_lru];
+    ctx->map_lru = 1 - ctx->map_lru;
+    ms->ws = nullptr;  // invalid until every descriptor is encoded
     for (size_t i = 0; i < ctx->layers.size(); ++i) {
       const Layer &L = ctx->layers[i];
-      voc_status st = encode_map(ctx, &ctx->maps[i], bufs[L.in_buf], L.Cp_in,
+      voc_status st = encode_map(ctx, &ms->maps[i], bufs[L.in_buf], L.Cp_in,
                                  pitch8(level_len(ctx, L.level, T)), B, L.g.rows, L.g.KB / 8);
+      ms->skip_maps[i] = CUtensorMap{};
       if (st == VOC_OK && L.skip_buf >= 0)
-        st = encode_skip_map(ctx, &ctx->skip_maps[i], bufs[L.skip_buf], L.Cp_out,
+        st = encode_skip_map(ctx, &ms->skip_maps[i], bufs[L.skip_buf], L.Cp_out,
                              pitch8(level_len(ctx, L.level, T)), B, L.cw);
-      if (st != VOC_OK) {
-        ctx->map_ws = nullptr;
-        return st;
-      }
+      if (st != VOC_OK) return st;
     }
-    ctx->map_ws = ws, ctx->map_B = B, ctx->map_T = T;
+    ms->ws = ws, ms->B = B, ms->T = T;
   }
 
   const bool prof = (flags & VOC_FLAG_PROFILE) != 0;
@@ -1439,6 +1530,7 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
     ctx->prof_names.assign(n_launch, "");
     ctx->prof_flops.assign(n_launch, 0.0);
     ctx->prof_bytes.assign(n_launch, 0.0);
+    ctx->prof_impl.assign(n_launch, 0.0);
     ctx->prof_ms.assign(n_launch, -1.f);
     ctx->prof_n = n_launch;
     ctx->prof_ready = false;
@@ -1462,8 +1554,9 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
 #endif
   rec(1);
   if (prof) {
-    ctx->prof_names[li] = "prep_latent";
-    ctx->prof_bytes[li] = (double)B * T * (4.0 * ctx->desc.latent_channels + 4.0 * ctx->Cp_lat);
+    ctx->prof_names[li] = "prep_latent";  // the API layout into the kernels' operand layout
+    ctx->prof_bytes[li] = (double)B * T * 8.0 * ctx->desc.latent_channels;
+    ctx->prof_impl[li] = (double)B * T * (4.0 * ctx->desc.latent_channels + 4.0 * ctx->Cp_lat);
   }
   ++li;
   for (size_t i = 0; i < ctx->layers.size(); ++i, ++li) {
@@ -1472,7 +1565,7 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
     gemm_launch_args(ctx, L, B, T, bufs, bb, a);
     if (L.head_fold && fold) head_fold_args(ctx, L, bufs, a);
     rec(0);
-    st = launch_gemm(ctx, L, ctx->maps[i], ctx->skip_maps[i], a, stream);
+    st = launch_gemm(ctx, L, ms->maps[i], ms->skip_maps[i], a, stream);
     if (st != VOC_OK) return st;
 #ifdef VOC_CHECKS
     if ((st = check_launch(ctx, L.name, stream)) != VOC_OK) return st;
@@ -1480,7 +1573,8 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
     rec(1);
     if (prof) {
       ctx->prof_names[li] = L.name;
-      layer_cost(ctx, L, B, T, ctx->prof_flops[li], ctx->prof_bytes[li], L.head_fold && fold);
+      layer_cost(ctx, L, B, T, ctx->prof_flops[li], ctx->prof_bytes[li], ctx->prof_impl[li],
+                 L.head_fold && fold);
     }
   }
   const long long Lf = level_len(ctx, ctx->desc.n_stages, T);
@@ -1499,10 +1593,11 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
   if (prof) {
     ctx->prof_names[li] = "out_head";
     ctx->prof_flops[li] = 2.0 * ctx->head.C * ctx->head.K * B * (double)Lf;
-    // folded: the last conv2 did the products; this launch reads their partial sums
-    ctx->prof_bytes[li] = fold
-                              ? (double)B * head_part_floats(ctx, last, Lf) * 4.0 + 4.0 * B * Lf
-                              : (double)B * Lf * (4.0 * ctx->head.Cp + 4.0);
+    // folded: the last conv2 did the products; this launch finishes them into the audio
+    ctx->prof_bytes[li] = fold ? 4.0 * B * (double)Lf : (double)B * Lf * (4.0 * ctx->head.C + 4.0);
+    ctx->prof_impl[li] = fold
+                             ? (double)B * head_part_floats(ctx, last, Lf) * 4.0 + 4.0 * B * Lf
+                             : (double)B * Lf * (4.0 * ctx->head.Cp + 4.0);
     ctx->prof_ready = true;
   }
   ++li;
@@ -1540,6 +1635,7 @@ VOC_API voc_status vocoder_decode(vocoder *ctx, const float *latent_dev, int B, 
   if (!ctx) return fail(nullptr, VOC_INVALID_ARG, "ctx is NULL");
   if (!latent_dev || !audio_dev) return fail(ctx, VOC_INVALID_ARG, "latent / audio NULL");
   if (B < 1 || T < 1) return fail(ctx, VOC_INVALID_ARG, "B and T must be positive");
+  if (cancelled(ctx)) return fail(ctx, VOC_CANCELLED, "cancelled: the caller's cancel flag is set");
   return decode_impl(ctx, latent_dev, B, T, audio_dev, ws_dev, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream), flags);
 }
@@ -1557,6 +1653,7 @@ VOC_API voc_status vocoder_decode_host(vocoder *ctx, const float *latent_host, i
   if (ws_bytes < need)
     return fail(ctx, VOC_WORKSPACE_TOO_SMALL,
                 "workspace " + std::to_string(ws_bytes) + " < " + std::to_string(need));
+  if (cancelled(ctx)) return fail(ctx, VOC_CANCELLED, "cancelled: the caller's cancel flag is set");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t wdec = vocoder_workspace_bytes(ctx, B, T);
   const size_t lat_bytes = (size_t)B * ctx->desc.latent_channels * T * 4;
@@ -1575,19 +1672,13 @@ VOC_API voc_status vocoder_decode_host(vocoder *ctx, const float *latent_host, i
   return VOC_OK;
 }
 
-// ------------------------------------------------------------------ no-allocation decode
-// The workspace of vocoder_decode_static: one array per device, in the library's module.
-static __device__ __align__(256) uint8_t g_static_ws[VOC_STATIC_WORKSPACE_BYTES];
-
-namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_static_mu;
-void *g_static_ws_addr[kMaxDevices] = {};  // device address of g_static_ws, per device
-}  // namespace
-
 VOC_API voc_status vocoder_decode_static(vocoder *ctx, const float *latent_dev, int B, int T,
                                          float *audio_dev, voc_stream_t stream, unsigned flags) {
   if (!ctx) return fail(nullptr, VOC_INVALID_ARG, "ctx is NULL");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDevice");
+  if (dev != ctx->device) return fail(ctx, VOC_INVALID_ARG, "current device differs from the context's");
   if (!latent_dev || !audio_dev) return fail(ctx, VOC_INVALID_ARG, "latent / audio NULL");
   if (B < 1 || T < 1) return fail(ctx, VOC_INVALID_ARG, "B and T must be positive");
   if (flags & VOC_FLAG_PROFILE)
@@ -1599,21 +1690,9 @@ VOC_API voc_status vocoder_decode_static(vocoder *ctx, const float *latent_dev, 
                 "B=" + std::to_string(B) + ", T=" + std::to_string(T) + " needs " +
                     std::to_string(need) + " bytes of workspace; the built-in array holds " +
                     std::to_string(VOC_STATIC_WORKSPACE_BYTES) + " (use vocoder_decode)");
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(ctx, VOC_UNSUPPORTED, "device index too large");
-  void *ws = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_ws_addr[dev]) {
-      void *p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_static_ws);  // host code may not use &g_static_ws itself
-      if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetSymbolAddress");
-      g_static_ws_addr[dev] = p;
-    }
-    ws = g_static_ws_addr[dev];
-  }
+  void *ws = static_ws_addr(dev);  // looked up by vocoder_create on this device
+  if (!ws) return fail(ctx, VOC_UNSUPPORTED, "no built-in workspace on this device");
+  if (cancelled(ctx)) return fail(ctx, VOC_CANCELLED, "cancelled: the caller's cancel flag is set");
   return decode_impl(ctx, latent_dev, B, T, audio_dev, ws, VOC_STATIC_WORKSPACE_BYTES,
                      reinterpret_cast<cudaStream_t>(stream), flags);
 }
@@ -1666,7 +1745,7 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
   tmp.strides = {L.convT ? L.stride : 1};
   auto done = [&](voc_status st) {
     if (st != VOC_OK) g_err = tmp.err;
-    for (void *p : tmp.allocs) cudaFree(p);
+    for (void *p : tmp.allocs) dev_free(p);
     return st;
   };
   voc_status st = upload_layer(&tmp, tmp.allocs, L, padding, w_host, b_host, SnakeCoef{});
@@ -1682,10 +1761,10 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
   const int s = L.convT ? L.stride : 1;
   const long long Tp = pitch8(T), Yp = pitch8((long long)T * s);  // plane rows
   void *hl = nullptr, *rows = nullptr;
-  e = cudaMalloc(&hl, (size_t)B * Tp * L.Cp_in * 4);
+  e = dev_alloc(reinterpret_cast<void **>(&hl), (size_t)B * Tp * L.Cp_in * 4);
   if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
   tmp.allocs.push_back(hl);
-  e = cudaMalloc(&rows, (size_t)B * Yp * L.Cp_out * 4);
+  e = dev_alloc(reinterpret_cast<void **>(&rows), (size_t)B * Yp * L.Cp_out * 4);
   if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
   tmp.allocs.push_back(rows);
   if ((st = launch_prep(&tmp, x_dev, B, L.Cin, T, L.Cp_in, alpha_d, invb_d,
@@ -1697,7 +1776,7 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
   L.level = 0;
   L.in_buf = 0, L.f32_buf = BUF_FY;
   ConvGemmArgs a;
-  e = cudaMalloc(&tmp.err_dev, 8 * sizeof(int));
+  e = dev_alloc(reinterpret_cast<void **>(&tmp.err_dev), 8 * sizeof(int));
   if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
   tmp.allocs.push_back(tmp.err_dev);
   cudaMemsetAsync(tmp.err_dev, 0, 8 * sizeof(int), stream);
@@ -1775,7 +1854,7 @@ VOC_API voc_status vocoder_op_residual_unit(const float *x_dev, int B, int C, in
   tmp.strides = {1};
   auto done = [&](voc_status st) {
     if (st != VOC_OK) g_err = tmp.err;
-    for (void *q : tmp.allocs) cudaFree(q);
+    for (void *q : tmp.allocs) dev_free(q);
     return st;
   };
   const int Cp = rup(C, 16);
@@ -1783,11 +1862,11 @@ VOC_API voc_status vocoder_op_residual_unit(const float *x_dev, int B, int C, in
   const size_t bb = (size_t)B * Tp * Cp * 4;
   void *bufs[BUF_COUNT] = {nullptr, nullptr, nullptr, nullptr};
   for (int i : {(int)BUF_H0, (int)BUF_HB, (int)BUF_FY}) {
-    cudaError_t e = cudaMalloc(&bufs[i], bb);
+    cudaError_t e = dev_alloc(&bufs[i], bb);
     if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
     tmp.allocs.push_back(bufs[i]);
   }
-  cudaError_t e = cudaMalloc(&tmp.err_dev, 8 * sizeof(int));
+  cudaError_t e = dev_alloc(reinterpret_cast<void **>(&tmp.err_dev), 8 * sizeof(int));
   if (e != cudaSuccess) return done(cuda_fail(&tmp, e, "cudaMalloc"));
   tmp.allocs.push_back(tmp.err_dev);
   cudaMemsetAsync(tmp.err_dev, 0, 8 * sizeof(int), stream);
@@ -1875,9 +1954,35 @@ VOC_API voc_status vocoder_profile_entry(vocoder *ctx, int index, const char **n
   return VOC_OK;
 }
 
+VOC_API voc_status vocoder_profile_impl_bytes(vocoder *ctx, int index, double *bytes) {
+  if (!ctx) return fail(nullptr, VOC_INVALID_ARG, "ctx is NULL");
+  if (!bytes) return fail(ctx, VOC_INVALID_ARG, "bytes is NULL");
+  if (!ctx->prof_ready || index < 0 || index >= ctx->prof_n)
+    return fail(ctx, VOC_INVALID_ARG, "no profile entry " + std::to_string(index));
+  *bytes = ctx->prof_impl[index];
+  return VOC_OK;
+}
+
 VOC_API const char *vocoder_last_error(const vocoder *ctx) {
   return ctx ? ctx->err.c_str() : g_err.c_str();
 }
+
+VOC_API voc_status vocoder_set_wait_budget(vocoder *ctx, long long cycles) {
+  if (!ctx) return fail(nullptr, VOC_INVALID_ARG, "ctx is NULL");
+  if (cycles < 0) return fail(ctx, VOC_INVALID_ARG, "wait budget must be >= 0");
+  ctx->wait_budget = cycles == 0 ? kWaitBudget : cycles;
+  return VOC_OK;
+}
+
+VOC_API voc_status vocoder_set_cancel_flag(vocoder *ctx, const volatile int *flag) {
+  if (!ctx) return fail(nullptr, VOC_INVALID_ARG, "ctx is NULL");
+  ctx->cancel = flag;
+  return VOC_OK;
+}
+
+VOC_API void vocoder_debug_fail_allocation(int n) { g_fail_countdown.store(n < 0 ? -1 : n); }
+
+VOC_API long long vocoder_debug_live_allocations(void) { return g_live_allocs.load(); }
 
 // ------------------------------------------------------------------ stateful streaming
 // Causal decoders only (VOC_PAD_CAUSAL): every layer looks left only, so decoding a
@@ -1986,7 +2091,7 @@ VOC_API voc_status vocoder_stream_create(vocoder *ctx, int B, int max_frames,
   const size_t lat_bytes = rupz((size_t)B * ctx->desc.latent_channels * max_frames * 4, 256);
   const size_t aud_bytes = rupz((size_t)B * max_frames * ctx->hop * 4, 256);
   total += lat_bytes + aud_bytes;
-  cudaError_t e = cudaMalloc(&s->block, total);
+  cudaError_t e = dev_alloc(reinterpret_cast<void **>(&s->block), total);
   if (e != cudaSuccess) {
     delete s;
     return cuda_fail(nullptr, e, "cudaMalloc (stream buffers)");
@@ -2048,7 +2153,7 @@ VOC_API voc_status vocoder_stream_create(vocoder *ctx, int B, int max_frames,
   }
   if (st != VOC_OK) {
     if (s->cap) cudaStreamDestroy(s->cap);
-    cudaFree(s->block);
+    dev_free(s->block);
     delete s;
     return st;
   }
@@ -2144,6 +2249,7 @@ VOC_API voc_status vocoder_stream_decode(vocoder_stream *s, const float *latent_
   int dev = -1;
   cudaGetDevice(&dev);
   if (dev != ctx->device) return fail(ctx, VOC_INVALID_ARG, "current device differs from the context's");
+  if (cancelled(ctx)) return fail(ctx, VOC_CANCELLED, "cancelled: the caller's cancel flag is set");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   cudaError_t e;
   voc_status st;
@@ -2196,7 +2302,7 @@ VOC_API void vocoder_stream_destroy(vocoder_stream *s) {
   for (cudaGraphExec_t g : s->graphs)
     if (g) cudaGraphExecDestroy(g);
   if (s->cap) cudaStreamDestroy(s->cap);
-  cudaFree(s->block);
+  dev_free(s->block);
   delete s;
 }
 
@@ -2320,7 +2426,7 @@ voc_status init_device(vocoder *ctx) {
   cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
   if (cc_major != 10 || cc_minor != 3)
     return fail(ctx, VOC_UNSUPPORTED, "this build targets sm_103 (GB300) only");
-  e = cudaMalloc(&ctx->err_dev, 8 * sizeof(int));  // [0] error word, [1] finite flag, [4..7] checks
+  e = dev_alloc(reinterpret_cast<void **>(&ctx->err_dev), 8 * sizeof(int));  // [0] error word, [1] finite flag, [4..7] checks
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMalloc");
   ctx->allocs.push_back(ctx->err_dev);
   ctx->flag_dev = ctx->err_dev + 1;
@@ -2414,20 +2520,26 @@ int enc_ksplit(const vocoder_encoder *enc, size_t i, int B, long long rows, size
   return eff(best) >= 1.25 * eff(1) ? best : 1;  // at least a quarter more SMs busy
 }
 
-// Algorithmic cost of an encoder layer with L_in GEMM rows per item: a strided conv counts
-// its 2s taps over the C real channels, not the zero taps of its 3-tap form.
-void enc_layer_cost(const Layer &L, int B, long long L_in, double &flops, double &bytes) {
+// Cost of an encoder layer with L_in GEMM rows per item, as layer_cost for the decoder: a
+// strided conv counts its 2s taps over the C real channels (not the zero taps of its 3-tap
+// form) and reads its s L_in input rows once; `alg` counts the real channels' inputs read
+// once and outputs written once (the output of a split-k layer is its reduce launch's).
+void enc_layer_cost(const Layer &L, int B, long long L_in, bool split_k, double &flops,
+                    double &alg, double &impl) {
   const double rows = (double)B * (double)L_in;
   const double k = L.down_s ? 2.0 * L.down_s : (double)L.K;
   const double cin = L.down_s ? (double)L.down_c : (double)L.Cin;
   flops = 2.0 * cin * L.Cout * k * rows;
+  alg = 4.0 * cin * rows * (L.down_s ? L.down_s : 1);
+  if (L.skip_buf >= 0) alg += 4.0 * L.Cout * rows;
+  if (!split_k) alg += 4.0 * L.Cout * rows;
   const ConvGemmArgs &g = L.g;
   double by = 4.0 * rows * L.Cp_in + (double)g.n_tiles * g.taps * g.nkb * g.b_bytes;
   const double out_elems = rows * L.Cp_out;
   if (L.skip_buf >= 0) by += 4.0 * out_elems;
   if (L.f32_buf >= 0) by += 4.0 * out_elems;
   if (L.hl_buf >= 0) by += 4.0 * out_elems;
-  bytes = by;
+  impl = by;
 }
 
 }  // namespace
@@ -2480,7 +2592,7 @@ VOC_API voc_status vocoder_encoder_param_shape(const voc_enc_desc *d, int index,
 
 VOC_API void vocoder_encoder_destroy(vocoder_encoder *enc) {
   if (!enc) return;
-  for (void *p : enc->core.allocs) cudaFree(p);
+  for (void *p : enc->core.allocs) dev_free(p);
   for (cudaEvent_t e : enc->core.events) cudaEventDestroy(e);
   delete enc;
 }
@@ -2730,6 +2842,7 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
     ctx->prof_names.assign(n_launch, "");
     ctx->prof_flops.assign(n_launch, 0.0);
     ctx->prof_bytes.assign(n_launch, 0.0);
+    ctx->prof_impl.assign(n_launch, 0.0);
     ctx->prof_ms.assign(n_launch, -1.f);
     ctx->prof_n = n_launch;
     ctx->prof_ready = false;
@@ -2751,7 +2864,8 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
     rec(1);
     if (prof) {
       ctx->prof_names[li] = "prep_audio";
-      ctx->prof_bytes[li] = (double)B * L * (4.0 * Ci + 4.0 * enc->Cp_audio);
+      ctx->prof_bytes[li] = (double)B * L * 8.0 * Ci;
+      ctx->prof_impl[li] = (double)B * L * (4.0 * Ci + 4.0 * enc->Cp_audio);
     }
     ++li;
   }
@@ -2778,7 +2892,8 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
       if (prof) {
         ctx->prof_names[li] = Ly.name;
         ctx->prof_flops[li] = 2.0 * Ly.Cin * Ly.Cout * Ly.K * B * (double)rows;
-        ctx->prof_bytes[li] = (double)B * rows * (4.0 * Ci + 8.0 * Ly.Cp_out);
+        ctx->prof_bytes[li] = (double)B * rows * (4.0 * Ci + 4.0 * Ly.Cout);
+        ctx->prof_impl[li] = (double)B * rows * (4.0 * Ci + 8.0 * Ly.Cp_out);
       }
       continue;
     }
@@ -2813,9 +2928,10 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
     rec(1);
     if (prof) {
       ctx->prof_names[li] = Ly.name;
-      enc_layer_cost(Ly, B, rows, ctx->prof_flops[li], ctx->prof_bytes[li]);
+      enc_layer_cost(Ly, B, rows, S > 1, ctx->prof_flops[li], ctx->prof_bytes[li],
+                     ctx->prof_impl[li]);
       if (S > 1)  // the outputs are the reduce kernel's
-        ctx->prof_bytes[li] += 4.0 * a.ksplit * B * (double)rows * Ly.Cp_out -
+        ctx->prof_impl[li] += 4.0 * a.ksplit * B * (double)rows * Ly.Cp_out -
                                (Ly.f32_buf >= 0 ? 4.0 : 0.0) * B * (double)rows * Ly.Cp_out -
                                (Ly.hl_buf >= 0 ? 4.0 : 0.0) * B * (double)rows * Ly.Cp_out;
     }
@@ -2838,7 +2954,8 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
       if (prof) {
         ctx->prof_names[li] = Ly.name + ".reduce";
         ctx->prof_flops[li] = 0.0;
-        ctx->prof_bytes[li] = 4.0 * B * (double)rows * Ly.Cp_out *
+        ctx->prof_bytes[li] = 4.0 * B * (double)rows * Ly.Cout;  // the layer's output
+        ctx->prof_impl[li] = 4.0 * B * (double)rows * Ly.Cp_out *
                               (a.ksplit + (Ly.f32_buf >= 0 ? 1 : 0) + (Ly.hl_buf >= 0 ? 1 : 0));
       }
     }
@@ -2854,7 +2971,8 @@ VOC_API voc_status vocoder_encode(vocoder_encoder *enc, const float *audio_dev, 
   rec(1);
   if (prof) {
     ctx->prof_names[li] = "latent_out";
-    ctx->prof_bytes[li] = (double)B * Lz * (4.0 * enc->Cp_lat + 4.0 * Cl);
+    ctx->prof_bytes[li] = (double)B * Lz * 8.0 * Cl;
+    ctx->prof_impl[li] = (double)B * Lz * (4.0 * enc->Cp_lat + 4.0 * Cl);
     ctx->prof_ready = true;
   }
   ++li;
@@ -2881,6 +2999,12 @@ VOC_API voc_status vocoder_encoder_profile_entry(vocoder_encoder *enc, int index
                                                  double *ms, double *flops, double *bytes) {
   if (!enc) return fail(nullptr, VOC_INVALID_ARG, "encoder is NULL");
   return vocoder_profile_entry(&enc->core, index, name, ms, flops, bytes);
+}
+
+VOC_API voc_status vocoder_encoder_profile_impl_bytes(vocoder_encoder *enc, int index,
+                                                      double *bytes) {
+  if (!enc) return fail(nullptr, VOC_INVALID_ARG, "encoder is NULL");
+  return vocoder_profile_impl_bytes(&enc->core, index, bytes);
 }
 
 VOC_API const char *vocoder_encoder_last_error(const vocoder_encoder *enc) {

@@ -59,7 +59,7 @@ typedef enum {
   VOC_OOM = -4,                 /* device or host allocation failed                 */
   VOC_WORKSPACE_TOO_SMALL = -5, /* ws_bytes below vocoder_workspace_bytes()         */
   VOC_NONFINITE = -6,           /* VOC_FLAG_CHECK_FINITE found a NaN / Inf          */
-  VOC_CANCELLED = -7,           /* reserved for cancellable entry points            */
+  VOC_CANCELLED = -7,           /* the caller's cancel flag was set: nothing enqueued */
   VOC_DEVICE_TIMEOUT = -8       /* a kernel gave up a bounded wait (see VOC_FLAG_SYNC) */
 } voc_status;
 
@@ -153,7 +153,17 @@ voc_status vocoder_fold_weight_norm(const float *g, const float *v, int dim0, lo
  * host pointers in the canonical order; a NULL bias means zero, every other
  * entry is required.  The weights are re-laid out per tap, split into bf16 hi/lo
  * and copied to the device; the host arrays are not retained.  On failure *out
- * is NULL and vocoder_last_error(NULL) describes the problem. */
+ * is NULL, every device allocation made so far is freed, and
+ * vocoder_last_error(NULL) describes the problem (VOC_OOM when the device ran out
+ * of memory).  Create also looks up, once per device, the device address of the
+ * built-in workspace of vocoder_decode_static (cudaGetSymbolAddress, with the
+ * context's device current).
+ * Relation to the boundary sketched for this library: its `voc_weights` struct is
+ * this array of `params` pointers in the canonical order above, and its precision
+ * pair 3xTF32 / TF32 is VOC_PREC_BF16X3 (three bf16 products of hi/lo splits,
+ * about 16 significant bits per operand, at bf16 tensor rate) / the one-plane
+ * VOC_PREC_F16W and VOC_PREC_BF16W (two products per multiply, the cost of one
+ * TF32 pass on this GPU, keeping more of the activations' bits than TF32). */
 voc_status vocoder_create(const voc_desc *desc, const float *const *params, int n_params,
                           vocoder_t **out);
 
@@ -192,14 +202,15 @@ voc_status vocoder_decode_host(vocoder_t *ctx, const float *latent_host, int B, 
  * forbids allocations behind its back.  The context must still be created
  * beforehand (vocoder_create allocates the weights once, at set-up time).
  *
- * Same inputs, outputs and results as vocoder_decode, but the workspace is a
- * file-scope device array of VOC_STATIC_WORKSPACE_BYTES inside the library,
- * which every GPU that loads the library holds until the process exits.
+ * Same inputs, outputs and results (bit for bit) as vocoder_decode, but the
+ * workspace is a file-scope device array of VOC_STATIC_WORKSPACE_BYTES inside
+ * the library, which every GPU that loads the library holds until the process
+ * exits.
  *   - Sizes whose vocoder_workspace_bytes(ctx, B, T) exceeds
  *     VOC_STATIC_WORKSPACE_BYTES are rejected with VOC_WORKSPACE_TOO_SMALL.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - The array's device address is looked up by vocoder_create, once per
+ *     device, with that device current; this call only reads the cached
+ *     address.  A call with another device current is VOC_INVALID_ARG.
  *   - Every call shares the one array, which keeps the contents of the last
  *     call.  The decode writes each workspace byte before reading it, so
  *     nothing needs clearing, but calls that overlap on the GPU (other
@@ -207,7 +218,12 @@ voc_status vocoder_decode_host(vocoder_t *ctx, const float *latent_host, int B, 
  *     each other's audio: serialise them.
  *   - VOC_FLAG_PROFILE is rejected (VOC_INVALID_ARG); the other flags behave
  *     as in vocoder_decode.
- * The function itself calls no cudaMalloc, cudaFree or allocating routine. */
+ * The function calls no cudaMalloc, cudaFree or allocating routine on the
+ * device.  On the host it allocates nothing while it alternates between at
+ * most two (workspace, B, T) combinations on a context (for example this one
+ * and one vocoder_decode workspace): the context keeps the tensor-map
+ * descriptors of the two most recent combinations in storage sized at create
+ * time; an error message is the only other host allocation. */
 #define VOC_STATIC_WORKSPACE_BYTES (64ull << 20)
 voc_status vocoder_decode_static(vocoder_t *ctx, const float *latent_dev, int B, int T,
                                  float *audio_dev, voc_stream_t stream, unsigned flags);
@@ -264,14 +280,54 @@ int vocoder_launches_per_decode(const vocoder_t *ctx, int B, int T);
 /* Per-kernel record of the last decode that ran with VOC_FLAG_PROFILE (valid
  * after the stream has been synchronised): name, device time (ms), algorithmic
  * FLOPs (2 per multiply-add, transposed conv counted without zero-stuffing) and
- * algorithmic bytes (each input read once, each output written once). */
+ * algorithmic bytes: each input of the launch's layers read once and each output
+ * written once, as fp32 values of the real channels -- a k-tap conv 4 Cin + 4 Cout
+ * bytes per row, a 1x1 conv with the residual add 4 Cin + 8 Cout (it also reads
+ * the skip), a transposed conv 4 Cin per input row + 4 Cout per output sample, a
+ * fused residual unit 8 C per row (x read once for conv1 and the skip, y written
+ * once), the output head 4 C + 4 per sample.  A launch that carries the folded
+ * output head counts its inputs only; the head's finishing launch counts the audio. */
 int vocoder_profile_count(const vocoder_t *ctx);
 voc_status vocoder_profile_entry(vocoder_t *ctx, int index, const char **name, double *ms,
                                  double *flops, double *bytes);
 
+/* The bytes entry `index` of the same record moves by the implementation's own count:
+ * channels padded to 16, the streamed weights, and every copy of an output (the fp32
+ * residual stream and the bf16 hi/lo operand of the next layer).  Diagnostic: compare
+ * it with the algorithmic bytes and with measured DRAM traffic. */
+voc_status vocoder_profile_impl_bytes(vocoder_t *ctx, int index, double *bytes);
+
 /* Message of the last failed call on ctx (ctx == NULL: of the last failure on
  * this thread without a context).  Valid until the next call on ctx. */
 const char *vocoder_last_error(const vocoder_t *ctx);
+
+/* Cancellation (the pattern of minimaxmusic.cpp Architecture, "mm-server reference",
+ * "Concurrency": a cancel flag polled between VAE windows).  `flag` is a host int that
+ * another thread may set to nonzero; while it is nonzero, vocoder_decode,
+ * vocoder_decode_host, vocoder_decode_static and vocoder_stream_decode on ctx return
+ * VOC_CANCELLED before enqueuing anything (outputs untouched, stream state unchanged).
+ * A caller decoding a long track window by window (or a stream chunk by chunk)
+ * therefore stops at the next window boundary; work already enqueued runs to its
+ * end.  The library only reads the flag; NULL removes it.  The flag must outlive its
+ * registration. */
+voc_status vocoder_set_cancel_flag(vocoder_t *ctx, const volatile int *flag);
+
+/* Bound, in SM clock cycles, on each wait inside the kernels that later calls on ctx
+ * enqueue (decode and its variants): a kernel whose wait runs past it gives up, waits for
+ * its own copies and tensor-core work in flight, frees its tensor memory and returns, and
+ * the call reports VOC_DEVICE_TIMEOUT when made with VOC_FLAG_SYNC.  0 restores the
+ * default of 4e9 cycles (about 2 s); a negative value is VOC_INVALID_ARG.  A stream
+ * object's chunk graphs keep the bound they were captured with.  A bound of a few hundred
+ * cycles makes every decode give up: it exists to exercise that path. */
+voc_status vocoder_set_wait_budget(vocoder_t *ctx, long long cycles);
+
+/* Test hooks for the allocation-failure path (process-wide).  After
+ * vocoder_debug_fail_allocation(n), the library's device allocations let n through and
+ * make the next one fail as an out-of-memory cudaMalloc would (n < 0 disarms it; it
+ * fires once).  vocoder_debug_live_allocations() counts the device allocations the
+ * library currently holds, for every context, stream object and encoder. */
+void vocoder_debug_fail_allocation(int n);
+long long vocoder_debug_live_allocations(void);
 
 /* Free the context and its device weights (NULL is ignored). */
 void vocoder_destroy(vocoder_t *ctx);
@@ -427,6 +483,8 @@ int vocoder_encoder_launches(const vocoder_encoder_t *enc, int B, long long L);
 int vocoder_encoder_profile_count(const vocoder_encoder_t *enc);
 voc_status vocoder_encoder_profile_entry(vocoder_encoder_t *enc, int index, const char **name,
                                          double *ms, double *flops, double *bytes);
+voc_status vocoder_encoder_profile_impl_bytes(vocoder_encoder_t *enc, int index,
+                                              double *bytes);
 
 /* Message of the last failed call on enc (NULL: of the last failure on this thread
  * without a context). */

@@ -87,6 +87,15 @@ int main(void) {
   CHECK(vocoder_profile_count((const vocoder_t *)0) == 0);
   CHECK(vocoder_profile_entry((vocoder_t *)0, 0, (const char **)0, (double *)0, (double *)0,
                               (double *)0) == VOC_INVALID_ARG);
+  {
+    double ib = 0.0;
+    volatile int cancel = 0;
+    CHECK(vocoder_profile_impl_bytes((vocoder_t *)0, 0, &ib) == VOC_INVALID_ARG);
+    CHECK(vocoder_set_cancel_flag((vocoder_t *)0, &cancel) == VOC_INVALID_ARG);
+    CHECK(vocoder_set_wait_budget((vocoder_t *)0, 0) == VOC_INVALID_ARG);
+    vocoder_debug_fail_allocation(-1);
+    CHECK(vocoder_debug_live_allocations() >= 0);
+  }
   vocoder_destroy((vocoder_t *)0);
   {  /* the mirror encoder: music layout 1 -> 64, strides 2, 4, 8, 8, widths up to 1024 */
     int es[4] = {2, 4, 8, 8};
@@ -125,6 +134,10 @@ int main(void) {
     CHECK(vocoder_encoder_profile_count((const vocoder_encoder_t *)0) == 0);
     CHECK(vocoder_encoder_profile_entry((vocoder_encoder_t *)0, 0, (const char **)0, (double *)0,
                                         (double *)0, (double *)0) == VOC_INVALID_ARG);
+    {
+      double ib = 0.0;
+      CHECK(vocoder_encoder_profile_impl_bytes((vocoder_encoder_t *)0, 0, &ib) == VOC_INVALID_ARG);
+    }
     e.strides = (const int *)0;
     CHECK(vocoder_encoder_param_count(&e) == -1);
     vocoder_encoder_destroy((vocoder_encoder_t *)0);

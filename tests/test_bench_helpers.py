@@ -57,18 +57,33 @@ def test_measured_traffic_is_gated_by_the_source_hash(tmp_path, monkeypatch):
     table = ("| layer | launches | ms | dram bytes | alg bytes |\n|---|---|---|---|---|\n"
              "| conv_in | 1 | 0.02 | 123456 | 100000 |\n| s0r0.conv1 | 1 | 0.15 | n/a | 5 |\n")
     (tmp_path / "profiles" / "traffic_wl.md").write_text(f"source hash: {h}\n\n{table}")
-    assert bench.measured_traffic("wl", "conv_in") == 123456
-    assert bench.measured_traffic("wl", "s0r0.conv1") is None  # unparsable cell
-    assert bench.measured_traffic("wl", "convT0") is None  # no such row
-    assert bench.measured_traffic("other", "conv_in") is None  # no such summary
+    assert bench.measured_traffic("wl", "conv_in")[0] == 123456
+    assert bench.measured_traffic("wl", "s0r0.conv1") == (None, None)  # unparsable cell
+    assert bench.measured_traffic("wl", "convT0") == (None, None)  # no such row
+    assert bench.measured_traffic("other", "conv_in") == (None, None)  # no such summary
     # any change to a kernel source or the header retires the committed counters
     (tmp_path / "dac_vocoder_decode_gb300" / "csrc" / "k.cu").write_text("__global__ void k() {;}\n")
     assert bench.source_hash() != h
-    assert bench.measured_traffic("wl", "conv_in") is None
+    assert bench.measured_traffic("wl", "conv_in") == (None, None)
     (tmp_path / "dac_vocoder_decode_gb300" / "csrc" / "k.cu").write_text("__global__ void k() {}\n")
-    assert bench.measured_traffic("wl", "conv_in") == 123456
+    assert bench.measured_traffic("wl", "conv_in")[0] == 123456
     (tmp_path / "include" / "k2.h").write_text("\n")
-    assert bench.measured_traffic("wl", "conv_in") is None
+    assert bench.measured_traffic("wl", "conv_in") == (None, None)
+
+
+def test_long_decode_traffic_is_scaled_from_the_window_capture(tmp_path, monkeypatch):
+    """music_long (15504 frames per item) takes music_window's (689 frames) per-launch DRAM
+    bytes scaled by the frame ratio, and says so."""
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    make_tree(tmp_path, "")
+    table = ("| layer | launches | ms | dram bytes | alg bytes |\n|---|---|---|---|---|\n"
+             "| convT3 | 1 | 0.18 | 689000 | 1 |\n")
+    (tmp_path / "profiles" / "traffic_music_window.md").write_text(
+        f"source hash: {bench.source_hash()}\n\n{table}")
+    value, src = bench.measured_traffic("music_long", "convT3")
+    assert value == 15504000
+    assert "music_window" in src and "15504/689" in src
+    assert bench.measured_traffic("music_window", "convT3")[0] == 689000
 
 
 def test_peaks_fall_back_without_the_measured_file(tmp_path, monkeypatch):
