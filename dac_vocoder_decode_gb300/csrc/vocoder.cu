@@ -1592,8 +1592,9 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
   rec(1);
   if (prof) {
     ctx->prof_names[li] = "out_head";
-    ctx->prof_flops[li] = 2.0 * ctx->head.C * ctx->head.K * B * (double)Lf;
-    // folded: the last conv2 did the products; this launch finishes them into the audio
+    // folded: the last conv2 did the products (its launch counts them); this launch adds the
+    // partial sums into the audio
+    ctx->prof_flops[li] = fold ? 0.0 : 2.0 * ctx->head.C * ctx->head.K * B * (double)Lf;
     ctx->prof_bytes[li] = fold ? 4.0 * B * (double)Lf : (double)B * Lf * (4.0 * ctx->head.C + 4.0);
     ctx->prof_impl[li] = fold
                              ? (double)B * head_part_floats(ctx, last, Lf) * 4.0 + 4.0 * B * Lf

@@ -86,7 +86,7 @@ def test_injected_allocation_failure_in_create_frees_everything():
     wl = G.workload("tiny_cal")
     folded = V.fold_params(wl.params)
     voc, live0 = _create_fails_cleanly(lambda: V.Vocoder(wl.arch, folded), "vocoder_create",
-                                      min_failures=20)
+                                      min_failures=10)
     assert V.vocoder_debug_live_allocations() > live0
     # the decoder that finally came up decodes correctly; destroying it frees everything
     G.compare_audio(O.decode(wl.arch, wl.params, wl.latent), G.gpu_decode(voc, wl.latent),
