@@ -55,10 +55,6 @@ constexpr int kBWarp = kSkipWarp + 1;                   // weight copies
 constexpr int kBWarps = 1;
 // 16 warps: four per SM sub-partition, so each thread may hold up to 128 registers
 constexpr int kGemmThreads = 32 * (kBWarp + kBWarps);   // 512
-// the fused residual-unit kernel: 8 epilogue warps (two per quadrant), one residual warp
-constexpr int kRuEpiWarps = 8;
-constexpr int kRuSkipWarp = 2 + kRuEpiWarps;
-constexpr int kRuThreads = 32 * (kRuSkipWarp + 1);      // 352
 constexpr int kMaxAcc = 4;
 // Bound on the waits of a kernel that has given up (ConvGemmArgs::timeout ran out, or another
 // role raised the abort flag) for its own copies and MMAs in flight: those were issued and

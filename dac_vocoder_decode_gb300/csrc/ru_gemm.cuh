@@ -1,117 +1,268 @@
-// ru_gemm.cuh -- one residual unit of the decoder in one kernel, for stages of up to
-// 192 channels (minimaxmusic.cpp Architecture, "Flow VAE": res_unit = skip -> snake1
-// -> conv1 k7 dil d -> snake2 -> conv2 k1 -> + skip):
+// ru_gemm.cuh -- one residual unit of the decoder in one kernel, for units of up to 192
+// channels (minimaxmusic.cpp Architecture, "Flow VAE": res_unit = skip -> snake1 -> conv1 k7
+// dil d -> snake2 -> conv2 k1 -> + skip):
 //
-//   h  = conv1(A) + b1                     A = Snake1(x) as bf16 hi/lo, from HBM (TMA, halo)
-//   H  = Snake2(h) as bf16 hi/lo           written by the epilogue into SHARED memory, in
-//                                          the canonical K-major layout of an MMA operand
-//   y  = x + conv2(H) + b2                 x streamed in by the residual prefetch warp
+//   h = conv1(A) + b1            A = Snake1(x) as bf16 hi/lo, from HBM (TMA, halo of the taps)
+//   H = Snake2(h) as bf16 hi/lo  written by the epilogue into SHARED memory, in the canonical
+//                                K-major layout of an MMA operand
+//   y = x + conv2(H) + b2        x (fp32) read by the epilogue warps from HBM
 //
-// so the conv1 result never goes to HBM.  Per 128-row tile the MMA warp runs the 7-tap
-// mainloop into accumulator 1, waits until the epilogue warps have turned accumulator 1
-// into H, then runs the 1x1 mainloop (A = H, weights streamed through the same ring) into
-// accumulator 2; the epilogue finishes the tile from accumulator 2 exactly like the
-// separate conv2 kernel.  Two accumulator pairs (when they fit in TMEM) let conv1 of the
-// next tile overlap the epilogue of this one.
+// so the conv1 result never goes to HBM: per row the unit reads 4 C bytes of A and 4 C of x
+// and writes its outputs, instead of also writing and re-reading h (8 C more).
 //
-// B2 (units of up to 128 channels): both mainloops take the two-MMA K step of the conv kernel's
-// B2 form -- A_hi x [W_hi | W_lo] into 2N accumulator columns, then A_lo x W_hi into the first
-// N -- and both epilogues add the two column halves.  A narrow layer's MMAs cost about the same
-// whatever their N (the A operand is re-read for each), so this removes a third of them.
+// Schedule (per CTA, over its 128-row tiles i = 0, 1, ...): the MMA warp issues
+//   conv1(0), conv1(1), conv2(0), conv1(2), conv2(1), ...
+// into one conv1 accumulator (acc1) and one conv2 accumulator (acc2) in TMEM.  When conv1(i)
+// completes, the epilogue warps first copy acc1 into registers and release it -- while the
+// tensor cores run the short conv2(i-1) -- so conv1(i+1) follows without a gap; then they apply
+// bias and Snake2, wait until conv2(i-1) has read H, write H(i), and finish tile i-1 from acc2
+// (bias, residual, Snake of the next layer, fp32 and hi/lo stores) while conv1(i+1) runs.
+// Epilogue work therefore overlaps the tensor cores instead of sitting between conv1 and conv2.
+//
+// Roles (15 warps): warp 0 lane 0 issues the A copies (one 5-D TMA box per k-block), warp 1
+// issues the MMAs (convergently; an elected lane issues), warps 2..13 are the epilogue: three
+// groups of four warps, one warp per TMEM lane quadrant, group g taking the 16-column chunks
+// g, g+3, ...; warp 14 lane 0 streams the weight stages (conv1's taps x k-blocks, then conv2's
+// k-blocks, in the MMA warp's order).
+//
+// B2 (units of up to 128 channels): both convolutions take the conv kernel's two-MMA K step --
+// A_hi x [W_hi | W_lo] into 2N accumulator columns, then A_lo x W_hi into the first N -- and the
+// epilogues add the two column halves.  The arithmetic of each epilogue is the separate conv
+// kernel's, so the fused unit computes the same values as conv1 + conv2 run as two kernels.
 #pragma once
 #include "conv_gemm.cuh"
 
 namespace voc {
 
+constexpr int kRuEpiWarps = 4 * kEpiGroups;          // warps 2..13
+constexpr int kRuBWarp = 2 + kRuEpiWarps;            // 14: weight copies
+constexpr int kRuThreads = 32 * (kRuBWarp + 1);      // 480
+// 16-column chunks of one epilogue group: C <= 192 has 12 chunks (4 per group); the B2 form
+// (C <= 128) at most 8 (3 per group)
+template <bool B2>
+__host__ __device__ constexpr int ru_max_chunks() { return B2 ? 3 : 4; }
+
 struct RuExtra {
-  const uint8_t *wB2;      // packed k1 weight tiles [kb][hi|lo][chunk][n][8]
+  const uint8_t *wB2;      // packed 1x1 weight stages [kb][...], the layout of a conv1 stage
   const float *bias_h;     // [N] conv1 bias
   const float *alpha_h;    // [N] Snake2 alpha
   const float *invb_h;     // [N] Snake2 1/(alpha + 1e-9)
   int h_bytes;             // bytes of the H tile (4 * 128 * Cp)
-  int n_buf;               // accumulator pairs (1 or 2)
+  int skip_L;              // rows of one plane of the fp32 residual input x
+  long long skip_elems;    // floats of the residual input (the self-checking build's bound)
 };
 
-// Epilogue 1 of one warp: rows quad*32.. of accumulator 1, columns n0..n0+CW-1 ->
-// Snake2(acc + b1) split into hi/lo, stored into the H tile: 8-channel chunk j of the hi
-// parts at H + j*2048, of the lo parts at H + (Cp/8 + j)*2048, row r at +16*r.
-template <int CW, bool B2>
-__device__ __forceinline__ void ru_epilogue1(const ConvGemmArgs &p, const RuExtra &x, uint32_t hbase,
-                                             int row_in_tile, int n0, uint32_t taddr) {
-  float v[CW];
-  if constexpr (B2) {  // (CW = 16) the two column halves of the accumulator
-    static_assert(CW == 16, "the B2 epilogue reads 16-column chunks");
-    uint32_t r[CW], r2[CW];
-    tmem_ld_issue<CW>(taddr, r);
-    tmem_ld_issue<CW>(taddr + static_cast<uint32_t>(p.N_tile), r2);
-    tmem_ld_wait<CW>(r);
-    tmem_ld16_after_wait(r2);
+// Epilogue 1, first part: this warp's 32 rows of its group's chunks of acc1, copied into
+// registers (B2: the two column halves added), so that acc1 can be released at once.
+template <bool B2, int MC>
+__device__ __forceinline__ void ru_drain1(const ConvGemmArgs &p, int grp, int n_chunks,
+                                          uint32_t t1, uint32_t (&dr)[MC][16]) {
 #pragma unroll
-    for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]) + __uint_as_float(r2[i]);
-  } else {
-    tmem_ld(taddr, v);
-  }
-  float bb[CW], a[CW], ib[CW];
-  ldg_vec(x.bias_h + n0, bb);
-  ldg_vec(x.alpha_h + n0, a);
-  ldg_vec(x.invb_h + n0, ib);
+  for (int j = 0; j < MC; ++j) {
+    const int c = grp + kEpiGroups * j;
+    if (c < n_chunks) {  // warp-uniform: tcgen05.ld is warp-collective
+      tmem_ld_issue<16>(t1 + static_cast<uint32_t>(16 * c), dr[j]);
+      if constexpr (B2) {
+        uint32_t r2[16];
+        tmem_ld_issue<16>(t1 + static_cast<uint32_t>(16 * c + p.N_tile), r2);
+        tmem_ld_wait<16>(dr[j]);
+        tmem_ld16_after_wait(r2);
 #pragma unroll
-  for (int i = 0; i < CW; ++i) v[i] += bb[i];
-  float sn[CW];
-  snake_n<CW>(v, a, ib, sn);
-  uint32_t hw[CW / 2], lw[CW / 2];
-#pragma unroll
-  for (int i = 0; i < CW / 2; ++i) {
-    const float s0 = sn[2 * i], s1 = sn[2 * i + 1];
-    const __nv_bfloat16 h0 = __float2bfloat16_rn(s0), h1 = __float2bfloat16_rn(s1);
-    const __nv_bfloat16 l0 = __float2bfloat16_rn(s0 - __bfloat162float(h0));
-    const __nv_bfloat16 l1 = __float2bfloat16_rn(s1 - __bfloat162float(h1));  // bf16x3 only
-    hw[i] = pack_bf16x2(h0, h1);
-    lw[i] = pack_bf16x2(l0, l1);
-  }
-  const int lo0 = p.Cp_out / 8;
-#pragma unroll
-  for (int g = 0; g < CW / 8; ++g) {
-    const int j = n0 / 8 + g;
-    sts128(hbase + static_cast<uint32_t>(j * (kTileM * 16) + row_in_tile * 16),
-           make_uint4(hw[4 * g], hw[4 * g + 1], hw[4 * g + 2], hw[4 * g + 3]));
-    sts128(hbase + static_cast<uint32_t>((lo0 + j) * (kTileM * 16) + row_in_tile * 16),
-           make_uint4(lw[4 * g], lw[4 * g + 1], lw[4 * g + 2], lw[4 * g + 3]));
+        for (int i = 0; i < 16; ++i)
+          dr[j][i] = __float_as_uint(__uint_as_float(dr[j][i]) + __uint_as_float(r2[i]));
+      } else {
+        tmem_ld_wait<16>(dr[j]);
+      }
+    }
   }
 }
 
-template <int CW, bool B2 = false>
+// Epilogue 1, second part: Snake2(h + b1) split into bf16 hi/lo, in place: chunk j's 16
+// values become [hi 0..7 | lo 0..7 | hi 8..15 | lo 8..15] as packed pairs (4 words each).
+template <int MC>
+__device__ __forceinline__ void ru_act1(const RuExtra &x, int grp, int n_chunks,
+                                        uint32_t (&dr)[MC][16]) {
+#pragma unroll
+  for (int j = 0; j < MC; ++j) {
+    const int c = grp + kEpiGroups * j;
+    if (c < n_chunks) {
+#pragma unroll
+      for (int h = 0; h < 16; h += 8) {
+        const int n0 = 16 * c + h;
+        float bb[8], a[8], ib[8], v[8], sn[8];
+        ldg_vec(x.bias_h + n0, bb);
+        ldg_vec(x.alpha_h + n0, a);
+        ldg_vec(x.invb_h + n0, ib);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(dr[j][h + i]) + bb[i];
+        snake_n<8>(v, a, ib, sn);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_pair<false>(sn[2 * i], sn[2 * i + 1], dr[j][h + i], dr[j][h + 4 + i]);
+      }
+    }
+  }
+}
+
+// Epilogue 1, last part: the packed chunks into the H tile (8-channel chunk k of the hi parts
+// at H + k * 2048, of the lo parts at H + (Cp/8 + k) * 2048, row r at + 16 r).  A warp writes
+// 32 consecutive rows of a chunk: 512 contiguous bytes.
+template <int MC>
+__device__ __forceinline__ void ru_store_h(uint32_t hbase, int Cp, int row, int grp, int n_chunks,
+                                           const uint32_t (&dr)[MC][16]) {
+  const int lo0 = Cp / 8;
+#pragma unroll
+  for (int j = 0; j < MC; ++j) {
+    const int c = grp + kEpiGroups * j;
+    if (c < n_chunks) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {  // 8-channel chunk 2c + q: words 8q..8q+3 hi, 8q+4.. lo
+        const int k = 2 * c + q;
+        sts128(hbase + static_cast<uint32_t>((k * kTileM + row) * 16),
+               make_uint4(dr[j][8 * q], dr[j][8 * q + 1], dr[j][8 * q + 2], dr[j][8 * q + 3]));
+        sts128(hbase + static_cast<uint32_t>(((lo0 + k) * kTileM + row) * 16),
+               make_uint4(dr[j][8 * q + 4], dr[j][8 * q + 5], dr[j][8 * q + 6], dr[j][8 * q + 7]));
+      }
+    }
+  }
+}
+
+// Epilogue 2 of one warp for its 32 rows x the 16 columns n0.. of acc2 (taddr): bias, the
+// residual x (fp32 chunk-major, read from global memory), Snake of the next layer, hi/lo split
+// and stores -- the conv kernel's epilogue of a 1x1 conv with a residual input.  HEAD: the
+// output head's partial products of this row instead of stores (see epilogue_chunk).
+template <bool B2, bool HEAD>
+__device__ __forceinline__ bool ru_epilogue2(const ConvGemmArgs &p, const RuExtra &x,
+                                             volatile int *abort_flag, int b, int t, int n0,
+                                             uint32_t taddr, float (&hp)[kHeadFoldMaxK]) {
+  VOC_CHECK(t >= x.skip_L ||
+                (((long long)b * (p.Cp_out / 4) + n0 / 4 + 3) * (long long)x.skip_L + t) * 4 + 4 <=
+                    x.skip_elems,
+            51, b, n0, t);
+  float bb[16];
+  ldg_vec(p.bias + n0, bb);
+  uint32_t r[16], r2[16];
+  tmem_ld_issue<16>(taddr, r);
+  if constexpr (B2) tmem_ld_issue<16>(taddr + static_cast<uint32_t>(p.N_tile), r2);
+  float sk[16];
+  if (t < x.skip_L) {  // rows past the plane (the last tile's tail) are not results
+    const float4 *s = reinterpret_cast<const float4 *>(p.skip) +
+                      ((size_t)b * (p.Cp_out / 4) + n0 / 4) * (size_t)x.skip_L + t;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 q = s[(size_t)j * x.skip_L];
+      sk[4 * j] = q.x, sk[4 * j + 1] = q.y, sk[4 * j + 2] = q.z, sk[4 * j + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sk[i] = 0.f;
+  }
+  tmem_ld_wait<16>(r);  // the TMEM reads complete before any return
+  if constexpr (B2) {
+    tmem_ld16_after_wait(r2);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+  }
+  float v[16], sn[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = (__uint_as_float(r[i]) + bb[i]) + sk[i];
+  if (p.alpha) {
+    float a[16], ib[16];
+    ldg_vec(p.alpha + n0, a);
+    ldg_vec(p.invb + n0, ib);
+    snake_n<16>(v, a, ib, sn);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sn[i] = v[i];
+  }
+  if (t >= p.rows_pad) return true;
+  if (t >= p.rows_valid) {  // padding rows: zeros
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.f, sn[i] = 0.f;
+  }
+  if constexpr (HEAD) {  // the folded output head: this row's partial products per tap
+#pragma unroll
+    for (int k = 0; k < kHeadFoldMaxK; ++k) {
+      float w[16];
+      ldg_vec(p.head_w + (size_t)k * p.Cp_out + n0, w);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc = fmaf(w[i], sn[i], acc);
+      hp[k] = acc;
+      asm volatile("" ::: "memory");  // one tap's weights in registers at a time
+    }
+    return true;
+  }
+  if (p.out_f32) {
+    const size_t L_out = static_cast<size_t>(p.f32_L);
+    const size_t row = static_cast<size_t>(t) + p.f32_row0;
+    const float *src = (p.flags & EPI_F32_SNAKE) ? sn : v;
+    VOC_CHECK((((long long)b * (p.Cp_out / 4) + n0 / 4 + 3) * (long long)L_out + row) * 4 + 4 <=
+                  p.f32_elems, 52, b, n0, row);
+    float *base = p.out_f32 + ((size_t)b * (p.Cp_out / 4) + n0 / 4) * L_out * 4 + row * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<float4 *>(base + (size_t)j * L_out * 4) =
+          make_float4(src[4 * j], src[4 * j + 1], src[4 * j + 2], src[4 * j + 3]);
+  }
+  if (p.out_hl) {
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) split_pair<false>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
+    const size_t L_out = static_cast<size_t>(p.hl_L);
+    const size_t row = static_cast<size_t>(t) + p.hl_row0;
+    const size_t item = (size_t)b * (2 * p.Cp_out / 8);
+    VOC_CHECK((((long long)item + p.Cp_out / 8 + n0 / 8 + 1) * (long long)L_out + row) * 8 + 8 <=
+                  p.hl_elems, 53, b, n0, row);
+    __nv_bfloat16 *hbase = p.out_hl + (item + n0 / 8) * L_out * 8 + row * 8;
+    __nv_bfloat16 *lbase = p.out_hl + (item + p.Cp_out / 8 + n0 / 8) * L_out * 8 + row * 8;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      *reinterpret_cast<uint4 *>(hbase + (size_t)j * L_out * 8) =
+          make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]);
+      *reinterpret_cast<uint4 *>(lbase + (size_t)j * L_out * 8) =
+          make_uint4(lw[4 * j], lw[4 * j + 1], lw[4 * j + 2], lw[4 * j + 3]);
+    }
+  }
+  return true;
+}
+
+template <bool B2, bool HEAD = false>
 __global__ void __launch_bounds__(kRuThreads, 1)
-    ru_gemm_kernel(const __grid_constant__ CUtensorMap tmapA,
-                   const __grid_constant__ CUtensorMap tmapS, const ConvGemmArgs p,
+    ru_gemm_kernel(const __grid_constant__ CUtensorMap tmapA, const ConvGemmArgs p,
                    const RuExtra x) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   uint8_t *smA = smem;
   uint8_t *smB = smA + (size_t)p.na * p.a_bytes;
-  uint8_t *smH = smB + (size_t)p.nb * p.b_bytes;    // conv2 operand (conv1 result)
-  uint8_t *smS = smH + x.h_bytes;                   // residual slots
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smS + (size_t)p.ns * skip_slot_bytes(CW));
+  uint8_t *smH = smB + (size_t)p.nb * p.b_bytes;    // conv2 operand (Snake2 of conv1)
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smH + x.h_bytes);
   uint64_t *fullA = bars;
   uint64_t *emptyA = fullA + p.na;
   uint64_t *fullB = emptyA + p.na;
   uint64_t *emptyB = fullB + p.nb;
   uint64_t *acc1Full = emptyB + p.nb;
-  uint64_t *acc1Empty = acc1Full + 2;
-  uint64_t *acc2Full = acc1Empty + 2;
-  uint64_t *acc2Empty = acc2Full + 2;
-  uint64_t *hFull = acc2Empty + 2;
+  uint64_t *acc1Empty = acc1Full + 1;
+  uint64_t *acc2Full = acc1Empty + 1;
+  uint64_t *acc2Empty = acc2Full + 1;
+  uint64_t *hFull = acc2Empty + 1;
   uint64_t *hEmpty = hFull + 1;
-  uint64_t *skipFull = hEmpty + 1;
-  uint64_t *skipEmpty = skipFull + p.ns;
-  uint64_t *drain = skipEmpty + p.ns;
+  uint64_t *drain = hEmpty + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t tmem_cols = static_cast<uint32_t>(2 * x.n_buf * p.acc_cols);
+  const uint32_t tmem_cols = static_cast<uint32_t>(2 * p.acc_cols);  // acc1, acc2
+#ifdef VOC_CHECKS
+  if (reinterpret_cast<const volatile uint8_t *>(abort_flag + 1) > smem_raw + p.smem_bytes) {
+    if (threadIdx.x == 0 && atomicCAS(p.dbg, 0, 1) == 0) {
+      p.dbg[1] = static_cast<int>(reinterpret_cast<const volatile uint8_t *>(abort_flag + 1) - smem_raw);
+      p.dbg[2] = p.smem_bytes;
+    }
+    return;  // uniform over the grid
+  }
+#endif
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.na; ++i) {
@@ -122,18 +273,12 @@ __global__ void __launch_bounds__(kRuThreads, 1)
       mbar_init(smem_u32(fullB + i), 1);
       mbar_init(smem_u32(emptyB + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(acc1Full + i), 1);
-      mbar_init(smem_u32(acc1Empty + i), kRuEpiWarps * 32);
-      mbar_init(smem_u32(acc2Full + i), 1);
-      mbar_init(smem_u32(acc2Empty + i), kRuEpiWarps * 32);
-    }
+    mbar_init(smem_u32(acc1Full), 1);
+    mbar_init(smem_u32(acc1Empty), kRuEpiWarps * 32);  // every epilogue thread arrives
+    mbar_init(smem_u32(acc2Full), 1);
+    mbar_init(smem_u32(acc2Empty), kRuEpiWarps * 32);
     mbar_init(smem_u32(hFull), kRuEpiWarps * 32);
     mbar_init(smem_u32(hEmpty), 1);
-    for (int i = 0; i < p.ns; ++i) {
-      mbar_init(smem_u32(skipFull + i), 1);
-      mbar_init(smem_u32(skipEmpty + i), 4 * 32);
-    }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -150,20 +295,185 @@ __global__ void __launch_bounds__(kRuThreads, 1)
   pdl_launch_dependents();
 
   const int total_tiles = p.B * p.m_tiles;  // one column tile: N_tile = Cp
+  // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ... (the grid is <= total_tiles)
+  const int n_my = (total_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                   static_cast<int>(gridDim.x);
   const int kchunks = p.KB / 8;
   const int nkb2 = p.Cp_out / p.KB;
   const uint32_t chunkA = static_cast<uint32_t>(p.rows) * 16u;
   const uint32_t chunkB = static_cast<uint32_t>(p.N_tile) * 16u;
   const uint32_t chunkH = kTileM * 16u;
-  const int n_chunks = p.N_tile / CW;
+  const int n_chunks = p.N_tile / 16;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------------------ A / weight producer
+      // ------------------------------------------------------------ A producer
       prefetch_tmap(&tmapA);
       pdl_wait();  // the previous layer's output
       const uint32_t a_tx = 2u * kchunks * chunkA;
-      int ia = 0, ib = 0;
+      int ia = 0;
+      bool ok = true;
+      for (int it = 0; it < n_my && ok; ++it) {
+        const int tile = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
+        const int mt = tile % p.m_tiles;
+        const int b = tile / p.m_tiles;
+        const int yg = floor_div8(p.in_row0 + mt * kTileM + p.off_min);  // 8-row group
+        for (int kb = 0; kb < p.nkb; ++kb) {
+          const int sa = ia % p.na;
+          const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;
+          if (!mbar_wait(smem_u32(emptyA + sa), pha ^ 1u, p.timeout, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fa = smem_u32(fullA + sa);
+          const uint32_t dstA = smem_u32(smA + (size_t)sa * p.a_bytes);
+#ifdef VOC_CHECKS
+          if (!(dstA + a_tx <= smem_u32(smB) && (kb + 1) * kchunks <= p.chunks_a / 2 &&
+                a_tx <= (uint32_t)p.a_bytes)) {
+            check_fail(p, abort_flag, 54, dstA, kb, p.chunks_a);
+            ok = false;
+            break;
+          }
+#endif
+          mbar_arrive_expect_tx(fa, a_tx);
+          tma_load_5d(dstA, &tmapA, fa, 0, yg, kb * kchunks, 0, b);  // hi and lo chunks
+          ++ia;
+        }
+      }
+      if (!ok) {
+        atomicOr(p.err, ERR_TIMEOUT_PRODUCER);
+        *abort_flag = 1;
+        drain_ring(fullA, p.na, ia, kDrainBudget);  // copies in flight land before the CTA exits
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer (whole warp)
+    // warp-uniform waits; one elected lane issues each MMA and commit
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.timeout, abort_flag));
+    };
+    const uint32_t idesc = idesc_bf16_f32(kTileM, p.N_tile);
+    const uint32_t idesc2 = idesc_bf16_f32(kTileM, 2 * p.N_tile);  // B2: [W_hi | W_lo]
+    // B2: each chunk of a weight stage holds its N hi rows, then its N lo rows
+    const uint32_t chunkB_stride = B2 ? 2 * chunkB : chunkB;
+    // descriptor low words, stepped in 16-byte units (see mma_bf16_warp_lo)
+    const uint32_t dA_lo = (kchunks * chunkA) >> 4;
+    const uint32_t dA_k = (2 * chunkA) >> 4;
+    const uint32_t dB_lo = (kchunks * chunkB) >> 4;
+    const uint32_t dB_k = (2 * chunkB_stride) >> 4;
+    const uint32_t dH_lo = ((p.Cp_out / 8) * chunkH) >> 4;
+    const uint32_t dH_k = (2 * chunkH) >> 4;
+    const uint32_t desc_hi = static_cast<uint32_t>(smem_desc(0u, 0u, 128) >> 32);
+    const uint32_t a_desc0 = static_cast<uint32_t>(smem_desc(smem_u32(smA), chunkA, 128));
+    const uint32_t b_desc0 = static_cast<uint32_t>(smem_desc(smem_u32(smB), chunkB_stride, 128));
+    const uint32_t h_desc0 = static_cast<uint32_t>(smem_desc(smem_u32(smH), chunkH, 128));
+    const uint32_t a_slot_step = static_cast<uint32_t>(p.a_bytes) >> 4;
+    const uint32_t b_slot_step = static_cast<uint32_t>(p.b_bytes) >> 4;
+    const int nks = kchunks / 2;
+    const uint32_t d1 = tmem_base;
+    const uint32_t d2 = tmem_base + static_cast<uint32_t>(p.acc_cols);
+    int sa = 0, sb = 0;
+    uint32_t pha = 0, phb = 0;
+    // the K steps of one weight stage: A (hi at a_hi, lo a_lo further), B at b_hi
+    auto ksteps = [&](uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t a_k, uint32_t b_hi,
+                      uint32_t accum) {
+      for (int ks = 0; ks < nks; ++ks, a_hi += a_k, b_hi += dB_k) {
+        if constexpr (B2) {
+          mma_bf16_warp_lo<false>(d, a_hi, b_hi, desc_hi, idesc2, accum);
+          mma_bf16_warp_lo<false>(d, a_hi + a_lo, b_hi, desc_hi, idesc, 1u);
+        } else {
+          mma_bf16_warp_lo<false>(d, a_hi, b_hi, desc_hi, idesc, accum);
+          mma_bf16_warp_lo<false>(d, a_hi, b_hi + dB_lo, desc_hi, idesc, 1u);
+          mma_bf16_warp_lo<false>(d, a_hi + a_lo, b_hi, desc_hi, idesc, 1u);
+        }
+        accum = 1u;
+      }
+    };
+    bool ok = true;
+    for (int it = 0; it <= n_my && ok; ++it) {
+      if (it < n_my) {  // conv1 (k taps, dilated) of tile it -> acc1
+        if (!wait_all(smem_u32(acc1Empty), (static_cast<uint32_t>(it) & 1u) ^ 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t accum = 0u;
+        for (int kb = 0; kb < p.nkb && ok; ++kb) {
+          if (!wait_all(smem_u32(fullA + sa), pha)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t a0 = a_desc0 + sa * a_slot_step + static_cast<uint32_t>(p.shift0_q0);
+          for (int tap = 0; tap < p.taps; ++tap, a0 += static_cast<uint32_t>(p.tap_step)) {
+            if (!wait_all(smem_u32(fullB + sb), phb)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#ifdef VOC_CHECKS
+            {
+              const int sh = p.shift0_q0 + tap * p.tap_step;
+              if (!__all_sync(0xffffffffu, sh >= 0 && sh + kTileM <= p.rows)) {
+                if (lane == 0) check_fail(p, abort_flag, 55, sh, tap, p.rows);
+                ok = false;
+                break;
+              }
+            }
+#endif
+            ksteps(d1, a0, dA_lo, dA_k, b_desc0 + sb * b_slot_step, accum);
+            accum = 1u;
+            mma_commit_warp(smem_u32(emptyB + sb));
+            if (++sb == p.nb) sb = 0, phb ^= 1u;
+          }
+          if (!ok) break;
+          mma_commit_warp(smem_u32(emptyA + sa));
+          if (++sa == p.na) sa = 0, pha ^= 1u;
+        }
+        if (!ok) break;
+        mma_commit_warp(smem_u32(acc1Full));
+      }
+      if (it >= 1) {  // conv2 (1x1) of tile it - 1 on H -> acc2
+        const uint32_t jp = static_cast<uint32_t>(it - 1) & 1u;
+        if (!wait_all(smem_u32(hFull), jp) || !wait_all(smem_u32(acc2Empty), jp ^ 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t accum = 0u;
+        for (int kb = 0; kb < nkb2; ++kb) {
+          if (!wait_all(smem_u32(fullB + sb), phb)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          ksteps(d2, h_desc0 + static_cast<uint32_t>(kb * kchunks) * (chunkH >> 4), dH_lo, dH_k,
+                 b_desc0 + sb * b_slot_step, accum);
+          accum = 1u;
+          mma_commit_warp(smem_u32(emptyB + sb));
+          if (++sb == p.nb) sb = 0, phb ^= 1u;
+        }
+        if (!ok) break;
+        mma_commit_warp(smem_u32(acc2Full));
+        mma_commit_warp(smem_u32(hEmpty));  // H may be rewritten once these MMAs have read it
+      }
+    }
+    if (!ok) {
+      if (lane == 0) {
+        atomicOr(p.err, ERR_TIMEOUT_MMA);
+        *abort_flag = 1;
+      }
+      // wait until every MMA issued so far has finished reading shared memory and TMEM
+      mma_commit_warp(smem_u32(drain));
+      const volatile int never = 0;
+      mbar_wait(smem_u32(drain), 0u, kDrainBudget, &never);
+    }
+  } else if (warp == kRuBWarp) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ weight producer
+      // Stages in the MMA warp's order: conv1 of tile it (k-blocks x taps), then conv2 of
+      // tile it - 1 (k-blocks).
+      int ib = 0;
       bool ok = true;
       auto load_b = [&](const uint8_t *src) -> bool {
         const int sb = ib % p.nb;
@@ -175,242 +485,83 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         ++ib;
         return true;
       };
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-        const int mt = tile % p.m_tiles;
-        const int b = tile / p.m_tiles;
-        const int yg = floor_div8(p.in_row0 + mt * kTileM + p.off_min);  // 8-row group
-        for (int kb = 0; kb < p.nkb && ok; ++kb) {
-          const int sa = ia % p.na;
-          const uint32_t pha = static_cast<uint32_t>(ia / p.na) & 1u;
-          if (!mbar_wait(smem_u32(emptyA + sa), pha ^ 1u, p.timeout, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fa = smem_u32(fullA + sa);
-          const uint32_t dstA = smem_u32(smA + (size_t)sa * p.a_bytes);
-          mbar_arrive_expect_tx(fa, a_tx);
-          tma_load_5d(dstA, &tmapA, fa, 0, yg, kb * kchunks, 0, b);  // hi and lo chunks
-          ++ia;
-          for (int tap = 0; tap < p.taps && ok; ++tap)
-            ok = load_b(p.wB + ((size_t)tap * p.nkb + kb) * p.b_bytes);
-        }
-        for (int kb = 0; kb < nkb2 && ok; ++kb) ok = load_b(x.wB2 + (size_t)kb * p.b_bytes);
+      for (int it = 0; it <= n_my && ok; ++it) {
+        if (it < n_my)
+          for (int kb = 0; kb < p.nkb && ok; ++kb)
+            for (int tap = 0; tap < p.taps && ok; ++tap)
+              ok = load_b(p.wB + ((size_t)tap * p.nkb + kb) * p.b_bytes);
+        if (it >= 1)
+          for (int kb = 0; kb < nkb2 && ok; ++kb) ok = load_b(x.wB2 + (size_t)kb * p.b_bytes);
       }
       if (!ok) {
         atomicOr(p.err, ERR_TIMEOUT_PRODUCER);
         *abort_flag = 1;
-        drain_ring(fullA, p.na, ia, kDrainBudget);
         drain_ring(fullB, p.nb, ib, kDrainBudget);
       }
     }
-  } else if (warp == 1) {
-    {
-      // ------------------------------------------------------------ MMA issuer (whole warp)
-      // warp-uniform waits, one elected lane issues each MMA and commit
-      auto wait_all = [&](uint32_t bar, uint32_t parity) {
-        return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.timeout, abort_flag));
-      };
-      const uint32_t idesc = idesc_bf16_f32(kTileM, p.N_tile);
-      const uint32_t idesc2 = idesc_bf16_f32(kTileM, 2 * p.N_tile);  // B2: [W_hi | W_lo]
-      // B2: each chunk of a weight stage holds its N hi rows, then its N lo rows
-      const uint32_t chunkB_stride = B2 ? 2 * chunkB : chunkB;
-      const uint64_t dA_lo = (uint64_t)((kchunks * chunkA) >> 4);
-      const uint64_t dA_k = (uint64_t)((2 * chunkA) >> 4);
-      const uint64_t dB_lo = (uint64_t)((kchunks * chunkB) >> 4);
-      const uint64_t dB_k = (uint64_t)((2 * chunkB_stride) >> 4);
-      const uint64_t dH_lo = (uint64_t)(((p.Cp_out / 8) * chunkH) >> 4);
-      const uint64_t dH_k = (uint64_t)((2 * chunkH) >> 4);
-      const uint64_t h0 = smem_desc(smem_u32(smH), chunkH, 128);
-      // ring positions advance incrementally (no divisions in the issue loop)
-      int sa = 0, sb = 0, j = 0;
-      uint32_t pha = 0, phb = 0, ph = 0;
-      int it = 0;
-      bool ok = true;
-      auto wait_b = [&](uint64_t &b0) -> bool {
-        if (!wait_all(smem_u32(fullB + sb), phb)) return false;
-        tc_fence_after();
-        b0 = smem_desc(smem_u32(smB + (size_t)sb * p.b_bytes), chunkB_stride, 128);
-        return true;
-      };
-      auto release_b = [&]() {
-        mma_commit_warp(smem_u32(emptyB + sb));
-        if (++sb == p.nb) sb = 0, phb ^= 1u;
-      };
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
-        const uint32_t d1 = tmem_base + static_cast<uint32_t>(2 * j * p.acc_cols);
-        const uint32_t d2 = d1 + static_cast<uint32_t>(p.acc_cols);
-        // conv1 (k taps, dilated) -> accumulator 1
-        if (!wait_all(smem_u32(acc1Empty + j), ph ^ 1u)) {
+  } else if (warp >= 2 && warp < 2 + kRuEpiWarps) {
+    // -------------------------------------------------------------- epilogue
+    pdl_wait();  // the residual input is the previous layer's output; this unit's outputs
+                 // overwrite buffers earlier layers read
+    const int e = warp - 2;
+    const int quad = warp & 3;   // TMEM lane quadrant this warp may access
+    const int grp = e / 4;       // column chunks grp, grp + 3, ...
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t t1 = tmem_base + lanes;
+    const uint32_t t2 = t1 + static_cast<uint32_t>(p.acc_cols);
+    const uint32_t hbase = smem_u32(smH);
+    constexpr int MC = ru_max_chunks<B2>();
+    uint32_t dr[MC][16];
+    bool ok = true;
+    for (int it = 0; it <= n_my && ok; ++it) {
+      if (it < n_my) {
+        // epilogue 1 of tile it: acc1 -> registers (acc1 released), Snake2 -> H
+        const uint32_t ip = static_cast<uint32_t>(it) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(acc1Full), ip, p.timeout, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int kb = 0; kb < p.nkb && ok; ++kb) {
-          if (!wait_all(smem_u32(fullA + sa), pha)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t aBase = smem_u32(smA + (size_t)sa * p.a_bytes);
-          for (int tap = 0; tap < p.taps; ++tap) {
-            uint64_t b0;
-            if (!wait_b(b0)) {
-              ok = false;
-              break;
-            }
-            const uint64_t a0 = smem_desc(
-                aBase + static_cast<uint32_t>(p.shift0_q0 + tap * p.tap_step) * 16u, chunkA, 128);
-            for (int ks = 0; ks < kchunks / 2; ++ks) {
-              const uint64_t a_hi = a0 + ks * dA_k, a_lo = a_hi + dA_lo;
-              const uint64_t b_hi = b0 + ks * dB_k, b_lo = b_hi + dB_lo;
-              const uint32_t accum = (kb | tap | ks) ? 1u : 0u;
-              if constexpr (B2) {
-                mma_bf16_warp(d1, a_hi, b_hi, idesc2, accum);
-                mma_bf16_warp(d1, a_lo, b_hi, idesc, 1u);
-              } else {
-                mma_bf16_warp(d1, a_hi, b_hi, idesc, accum);
-                mma_bf16_warp(d1, a_hi, b_lo, idesc, 1u);
-                mma_bf16_warp(d1, a_lo, b_hi, idesc, 1u);
-              }
-            }
-            release_b();
-          }
-          if (!ok) break;
-          mma_commit_warp(smem_u32(emptyA + sa));
-          if (++sa == p.na) sa = 0, pha ^= 1u;
-        }
-        if (!ok) break;
-        mma_commit_warp(smem_u32(acc1Full + j));
-        // conv2 (1x1) on H -> accumulator 2, once the epilogue has written H
-        if (!wait_all(smem_u32(hFull), static_cast<uint32_t>(it) & 1u) ||
-            !wait_all(smem_u32(acc2Empty + j), ph ^ 1u)) {
+        ru_drain1<B2, MC>(p, grp, n_chunks, t1, dr);
+        tc_fence_before();
+        mbar_arrive(smem_u32(acc1Empty));
+        ru_act1<MC>(x, grp, n_chunks, dr);
+        // H is free once conv2 of the previous tile has read it
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(hEmpty), ip ^ 1u, p.timeout, abort_flag))) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        for (int kb = 0; kb < nkb2 && ok; ++kb) {
-          uint64_t b0;
-          if (!wait_b(b0)) {
-            ok = false;
-            break;
-          }
-          const uint64_t a0 = h0 + (uint64_t)((kb * kchunks * chunkH) >> 4);
-          for (int ks = 0; ks < kchunks / 2; ++ks) {
-            const uint64_t a_hi = a0 + ks * dH_k, a_lo = a_hi + dH_lo;
-            const uint64_t b_hi = b0 + ks * dB_k, b_lo = b_hi + dB_lo;
-            const uint32_t accum = (kb | ks) ? 1u : 0u;
-            if constexpr (B2) {
-              mma_bf16_warp(d2, a_hi, b_hi, idesc2, accum);
-              mma_bf16_warp(d2, a_lo, b_hi, idesc, 1u);
-            } else {
-              mma_bf16_warp(d2, a_hi, b_hi, idesc, accum);
-              mma_bf16_warp(d2, a_hi, b_lo, idesc, 1u);
-              mma_bf16_warp(d2, a_lo, b_hi, idesc, 1u);
-            }
-          }
-          release_b();
-        }
-        if (!ok) break;
-        mma_commit_warp(smem_u32(acc2Full + j));
-        mma_commit_warp(smem_u32(hEmpty));  // H may be rewritten once these MMAs have read it
-        if (++j == x.n_buf) j = 0, ph ^= 1u;
+        ru_store_h<MC>(hbase, p.Cp_out, row_in_tile, grp, n_chunks, dr);
+        fence_proxy_async_smem();  // the H stores become visible to the tensor cores
+        mbar_arrive(smem_u32(hFull));
       }
-      if (!ok) {
-        if (lane == 0) {
-          atomicOr(p.err, ERR_TIMEOUT_MMA);
-          *abort_flag = 1;
-        }
-        mma_commit_warp(smem_u32(drain));
-        const volatile int never = 0;
-        mbar_wait(smem_u32(drain), 0u, kDrainBudget, &never);
-      }
-    }
-  } else if (warp == kRuSkipWarp) {
-    if (lane == 0 && p.skip) {
-      // ------------------------------------------------------------ residual prefetch
-      prefetch_tmap(&tmapS);
-      pdl_wait();
-      const uint32_t bytes = static_cast<uint32_t>(skip_slot_bytes(CW));
-      const int nsh = p.ns / 2;
-      int cnt[2] = {0, 0};
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      if (it >= 1) {
+        // epilogue 2 of tile it - 1: acc2 -> outputs
+        const int jt = it - 1;
+        const int tile = static_cast<int>(blockIdx.x) + jt * static_cast<int>(gridDim.x);
         const int mt = tile % p.m_tiles;
         const int b = tile / p.m_tiles;
-        for (int c = 0; c < n_chunks; ++c) {
-          const int h = c & 1;
-          const int k = cnt[h]++;
-          const int slot = h * nsh + k % nsh;
-          const uint32_t ph = static_cast<uint32_t>(k / nsh) & 1u;
-          if (!mbar_wait(smem_u32(skipEmpty + slot), ph ^ 1u, p.timeout, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fs = smem_u32(skipFull + slot);
-          mbar_arrive_expect_tx(fs, bytes);
-          tma_load_4d(smem_u32(smS + (size_t)slot * bytes), &tmapS, fs, 0, mt * kTileM / 8,
-                      (c * CW) / 4, b);
+        const int t = mt * kTileM + row_in_tile;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(acc2Full), static_cast<uint32_t>(jt) & 1u,
+                                               p.timeout, abort_flag))) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        for (int c = grp; c < n_chunks && ok; c += kEpiGroups) {
+          float hp[kHeadFoldMaxK] = {};
+          ok = ru_epilogue2<B2, HEAD>(p, x, abort_flag, b, t, 16 * c, t2 + static_cast<uint32_t>(16 * c), hp);
+          ok = __all_sync(0xffffffffu, ok);
+          if constexpr (HEAD) {
+            if (ok) ok = head_fold_store(p, hp, b, (mt * kTileM) / 32 + quad, c, lane, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+          }
+        }
+        tc_fence_before();
+        if (!ok) break;
+        mbar_arrive(smem_u32(acc2Empty));
       }
-      if (!ok) {
-        atomicOr(p.err, ERR_TIMEOUT_SKIP);
-        *abort_flag = 1;
-        drain_ring(skipFull, nsh, cnt[0], kDrainBudget);
-        drain_ring(skipFull + nsh, nsh, cnt[1], kDrainBudget);
-      }
-    }
-  } else {
-    // -------------------------------------------------------------- epilogue
-    pdl_wait();  // this unit's outputs overwrite buffers earlier layers read
-    const int e = warp - 2;
-    const int quad = warp & 3;
-    const int half = e / 4;
-    const int row_in_tile = quad * 32 + lane;
-    const uint32_t sbase = smem_u32(smS);
-    const uint32_t hbase = smem_u32(smH);
-    const int nsh = p.ns > 0 ? p.ns / 2 : 1;
-    int kh = 0;
-    int it = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
-      const int mt = tile % p.m_tiles;
-      const int b = tile / p.m_tiles;
-      const int j = it % x.n_buf;
-      const uint32_t ph = static_cast<uint32_t>(it / x.n_buf) & 1u;
-      const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
-      const uint32_t t1 = tmem_base + static_cast<uint32_t>(2 * j * p.acc_cols) + lanes;
-      const uint32_t t2 = t1 + static_cast<uint32_t>(p.acc_cols);
-      // epilogue 1: accumulator 1 -> H (shared), after conv2 of the previous tile read H
-      if (!mbar_wait(smem_u32(acc1Full + j), ph, p.timeout, abort_flag) ||
-          !mbar_wait(smem_u32(hEmpty), (static_cast<uint32_t>(it) & 1u) ^ 1u, p.timeout,
-                     abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      for (int c = half; c < n_chunks; c += 2)
-        ru_epilogue1<CW, B2>(p, x, hbase, row_in_tile, c * CW, t1 + c * CW);
-      fence_proxy_async_smem();  // make the H stores visible to the tensor cores
-      tc_fence_before();
-      mbar_arrive(smem_u32(acc1Empty + j));
-      mbar_arrive(smem_u32(hFull));
-      // epilogue 2: accumulator 2 -> bias, residual, Snake of the next layer, stores
-      if (!mbar_wait(smem_u32(acc2Full + j), ph, p.timeout, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int t = mt * kTileM + row_in_tile;
-      for (int c = half; c < n_chunks && ok; c += 2, ++kh) {
-        const int slot = half * nsh + kh % nsh;
-        ok = epilogue_chunk<CW, B2>(p, sbase + static_cast<uint32_t>(slot * skip_slot_bytes(CW)),
-                                smem_u32(skipFull + slot), smem_u32(skipEmpty + slot),
-                                static_cast<uint32_t>(kh / nsh) & 1u, abort_flag, row_in_tile, b,
-                                t, c * CW, t2 + c * CW, sbase, smem_u32(bars));
-      }
-      if (!ok) break;
-      tc_fence_before();
-      mbar_arrive(smem_u32(acc2Empty + j));
     }
     if (!ok) {
       atomicOr(p.err, ERR_TIMEOUT_EPILOGUE);

@@ -186,15 +186,13 @@ bool set_kernel_attrs(std::string &why) {
     st = set_conv_attrs<voc::kPrecBf16x3>();
     if (st == cudaSuccess) st = set_conv_attrs<voc::kPrecF16w>();
     if (st == cudaSuccess) st = set_conv_attrs<voc::kPrecBf16w>();
-    if (st == cudaSuccess)
-      st = cudaFuncSetAttribute(voc::ru_gemm_kernel<32>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (st == cudaSuccess)
-      st = cudaFuncSetAttribute(voc::ru_gemm_kernel<16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-    if (st == cudaSuccess)
-      st = cudaFuncSetAttribute(voc::ru_gemm_kernel<16, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    auto set_ru = [](auto kernel) {
+      return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    };
+    if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<false, false>);
+    if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<true, false>);
+    if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<false, true>);
+    if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<true, true>);
     if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::out_head_kernel<kHeadTile>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
@@ -473,13 +471,13 @@ bool plan_layer(bool pair, Layer &L, int padding, bool has_skip, std::string &wh
   return true;
 }
 
-// Plan a fused residual unit (L.K taps at dilation L.dil, then 1x1, C -> C): the conv1
-// geometry of plan_gemm, one column tile (N = Cp <= kRuMaxC), the conv1 result kept in a
-// shared H tile of 128 rows x Cp hi/lo pairs, and a k-block common to both convolutions.
+// Plan a fused residual unit (L.K taps at dilation L.dil, then 1x1, C -> C; ru_gemm_kernel):
+// the conv1 geometry of plan_gemm, one column tile (N = Cp <= kRuMaxC), the conv1 result kept
+// in a shared H tile of 128 rows x Cp hi/lo pairs, a k-block common to both convolutions,
+// one conv1 and one conv2 accumulator in TMEM.
 constexpr int kRuMaxC = 192;
-// Residual units run as two kernels by default: with two-MMA K steps for narrow layers the
-// pair of kernels is faster than the fused unit at every width measured (C = 48 to 192).
-constexpr int kFuseDefault = 0;
+// Residual units of up to this many (padded) channels run as one kernel by default.
+constexpr int kFuseDefault = kRuMaxC;
 bool plan_ru(Layer &L, int padding, std::string &why) {
   ConvGemmArgs &g = L.g;
   L.Cp_in = L.Cp_out = rup(L.Cout, 16);
@@ -495,6 +493,7 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
   g.n_tiles = 1;
   g.q_split_tile = 1;
   g.s_rows = 1;
+  g.phase_group = 0;
   g.off_min = -pad_left;
   g.shift0_q0 = g.shift0_q1 = 0;
   g.tap_step = L.dil;
@@ -503,38 +502,44 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
     why = "tap span too wide for one staged tile";
     return false;
   }
-  // B2 form (two MMAs per K step) when the doubled column count fits one MMA; it reads
-  // 16-column epilogue chunks
+  // B2 form (two MMAs per K step) when the doubled column count fits one MMA
   g.b2 = (2 * g.N_tile <= 256) ? 1 : 0;
-  L.cw = (!g.b2 && g.N_tile % 64 == 0) ? 32 : 16;
+  L.cw = 16;
   L.rx.h_bytes = 4 * voc::kTileM * L.Cp_out;
+  int ac = 32;
+  while (ac < (g.b2 ? 2 * g.N_tile : g.N_tile)) ac *= 2;
+  g.acc_cols = ac;  // acc1 at column 0, acc2 at column ac: 2 ac <= 512
+  g.n_acc = 2;
   const int chunkA = g.rows * 16;
-  const int sb = voc::skip_slot_bytes(L.cw);
-  g.na = 2;
+  const int avail = kSmemMax - 1024 - kBarrierBytes - L.rx.h_bytes;
+  // The largest k-block (a multiple of 16 dividing Cp, weight stage <= kBStageMax, A stage
+  // <= 72 KB) that leaves two A stages and at least three weight stages; else two.
   g.KB = 0;
-  for (int kb = 16; kb <= L.Cp_in; kb += 16) {  // largest k-block that leaves >= 2 weight stages
-    if (L.Cp_in % kb || 4 * kb * g.N_tile > 36 * 1024 || 4 * kb * g.rows > 72 * 1024) continue;
-    const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
-    const int b_bytes = 4 * kb * g.N_tile;
-    int avail = kSmemMax - 1024 - kBarrierBytes - g.na * a_bytes - L.rx.h_bytes;
-    const int ns = ((avail - 4 * sb) / b_bytes >= 3) ? 4 : 2;
-    avail -= ns * sb;
-    const int nb = std::min(8, avail / b_bytes);
-    if (nb < 2) continue;
-    g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = b_bytes, g.nb = nb, g.ns = ns;
-  }
+  for (int min_nb = 3; min_nb >= 2 && !g.KB; --min_nb)
+    for (int kb = L.Cp_in; kb >= 16 && !g.KB; kb -= 16) {
+      if (L.Cp_in % kb || 4 * kb * g.N_tile > kBStageMax || 4 * kb * g.rows > 72 * 1024) continue;
+      const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
+      const int b_bytes = 4 * kb * g.N_tile;
+      const int na = 2;
+      const int nb = std::min(8, (avail - na * a_bytes) / b_bytes);
+      if (nb < min_nb) continue;
+      g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = b_bytes, g.na = na, g.nb = nb;
+    }
   if (!g.KB) {
     why = "shared memory plan of the fused residual unit does not fit";
     return false;
   }
+  g.ns = 0;  // the residual input is read by the epilogue warps directly
   g.nkb = L.Cp_in / g.KB;
-  int ac = 32;
-  while (ac < (g.b2 ? 2 * g.N_tile : g.N_tile)) ac *= 2;
-  g.acc_cols = ac;
-  L.rx.n_buf = (4 * ac <= 512) ? 2 : 1;
-  g.n_acc = 2 * L.rx.n_buf;  // accumulators in TMEM (conv1 and conv2 of each buffer)
+  g.b_resident = 0;
+  g.ksplit = 1, g.kb_per_split = g.nkb, g.kb_split = g.nkb;
+  g.tap_lo0 = 0, g.tap_hi0 = g.taps, g.tap_lo1 = 0, g.tap_hi1 = g.taps;
+  if ((2 * g.na + 2 * g.nb + 7) * 8 + 8 > kBarrierBytes) {
+    why = "too many pipeline slots for the barrier block";
+    return false;
+  }
   L.smem = 1024 + (size_t)g.na * g.a_bytes + (size_t)g.nb * g.b_bytes + L.rx.h_bytes +
-           (size_t)g.ns * sb + kBarrierBytes;
+           kBarrierBytes;
   L.ru = true;
   return true;
 }
@@ -963,8 +968,11 @@ cudaError_t launch_conv(const Layer &L, const ConvGemmArgs &a, int grid, const C
                     map, smap, a);
 }
 
+// skip_L: rows of a plane of a fused residual unit's fp32 residual input (< 0: the output
+// planes', a.f32_L); skip_elems its floats (the self-checking build's bound).
 voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
-                       const CUtensorMap &smap, const ConvGemmArgs &a, cudaStream_t stream) {
+                       const CUtensorMap &smap, const ConvGemmArgs &a, cudaStream_t stream,
+                       long long skip_L = -1, long long skip_elems = -1) {
   // jobs: tiles, times the k ranges of a split-k layer (encoder forms)
   const long long tiles = (long long)a.B * a.m_tiles * a.n_tiles * std::max(1, a.ksplit);
   // Persistent grid: one CTA (or cluster) per unit, at most one per job.  With resident
@@ -996,15 +1004,16 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
                                          : persistent(ctx->num_sms));
   cudaError_t e;
   if (L.ru) {
-    if (L.g.b2)
-      e = launch_pdl(voc::ru_gemm_kernel<16, true>, dim3(grid), dim3(voc::kRuThreads), L.smem,
-                     stream, map, smap, a, L.rx);
-    else if (L.cw == 32)
-      e = launch_pdl(voc::ru_gemm_kernel<32>, dim3(grid), dim3(voc::kRuThreads), L.smem, stream,
-                     map, smap, a, L.rx);
+    voc::RuExtra rx = L.rx;
+    rx.skip_L = static_cast<int>(skip_L >= 0 ? skip_L : a.f32_L);
+    rx.skip_elems = skip_elems >= 0 ? skip_elems : a.f32_elems;
+    const dim3 g(grid), blk(voc::kRuThreads);
+    if (a.head_part)
+      e = L.g.b2 ? launch_pdl(voc::ru_gemm_kernel<true, true>, g, blk, L.smem, stream, map, a, rx)
+                 : launch_pdl(voc::ru_gemm_kernel<false, true>, g, blk, L.smem, stream, map, a, rx);
     else
-      e = launch_pdl(voc::ru_gemm_kernel<16>, dim3(grid), dim3(voc::kRuThreads), L.smem, stream,
-                     map, smap, a, L.rx);
+      e = L.g.b2 ? launch_pdl(voc::ru_gemm_kernel<true, false>, g, blk, L.smem, stream, map, a, rx)
+                 : launch_pdl(voc::ru_gemm_kernel<false, false>, g, blk, L.smem, stream, map, a, rx);
   } else if (L.prec == VOC_PREC_F16W) {
     e = launch_conv<voc::kPrecF16w>(L, a, grid, map, smap, stream);
   } else if (L.prec == VOC_PREC_BF16W) {
@@ -1397,14 +1406,14 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
     if (st != VOC_OK) return bail(st);
     st = upload(ctx, ctx->allocs, bp, &h.b_dev);
     if (st != VOC_OK) return bail(st);
-    // Fold the head into the last conv2 when that layer is a plain conv of one column tile
-    // writing Snake_out(y) (not a fused unit, not a CTA pair) and the head has at most
+    // Fold the head into the last conv2 when that layer (a 1x1 conv of one column tile or a
+    // fused residual unit, not a CTA pair) writes Snake_out(y) and the head has at most
     // kHeadFoldMaxK taps; its partial sums go to a hi/lo buffer the layer does not read.
     // Causal decoders keep the separate head: their chunk-by-chunk stream decode runs it, and
     // a streamed sequence must equal the whole-sequence decode bit for bit (the folded head
     // adds its products in another order).
     Layer &last = ctx->layers.back();
-    if (pad == VOC_PAD_SYMMETRIC && !last.ru && !last.pair && !last.convT &&
+    if (pad == VOC_PAD_SYMMETRIC && !last.pair && !last.convT &&
         (last.epi_flags & voc::EPI_F32_SNAKE) &&
         last.g.n_tiles == 1 && h.K <= voc::kHeadFoldMaxK && last.Cp_out == h.Cp) {
       // [k][c], zero-padded to kHeadFoldMaxK taps (same left padding)
@@ -1565,7 +1574,8 @@ voc_status decode_impl(vocoder *ctx, const float *latent, int B, int T, float *a
     gemm_launch_args(ctx, L, B, T, bufs, bb, a);
     if (L.head_fold && fold) head_fold_args(ctx, L, bufs, a);
     rec(0);
-    st = launch_gemm(ctx, L, ms->maps[i], ms->skip_maps[i], a, stream);
+    st = launch_gemm(ctx, L, ms->maps[i], ms->skip_maps[i], a, stream, -1,
+                     L.skip_buf >= 0 ? (long long)(bb / 4) : -1);
     if (st != VOC_OK) return st;
 #ifdef VOC_CHECKS
     if ((st = check_launch(ctx, L.name, stream)) != VOC_OK) return st;
@@ -2224,7 +2234,9 @@ voc_status stream_launches(vocoder_stream *s, const float *latent_dev, int frame
       }
     }
     a.L_a = static_cast<int>(io.plane);
-    st = launch_gemm(ctx, L, io.map, io.smap, a, stream);
+    st = launch_gemm(ctx, L, io.map, io.smap, a, stream,
+                     pitch8((long long)s->max_frames * level_len(ctx, L.level, 1)),
+                     static_cast<long long>(s->fy_bytes / 4));
     if (st != VOC_OK) return st;
 #ifdef VOC_CHECKS
     if ((st = check_launch(ctx, "stream " + L.name, stream)) != VOC_OK) return st;

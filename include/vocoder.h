@@ -105,10 +105,11 @@ typedef struct {
   int out_channels;     /* 1                                                 */
   int padding;          /* VOC_PAD_SYMMETRIC | VOC_PAD_CAUSAL                */
   int precision;        /* VOC_PREC_BF16X3 | VOC_PREC_F16W                   */
-  int fuse_max_channels;/* residual units of up to this many channels run as one
-                           kernel (conv1 result kept on chip); 0 = library default
-                           (never), -1 = never.  A performance choice only: results agree
-                           within the decode tolerance either way.              */
+  int fuse_max_channels;/* residual units of up to this many channels (at most 192)
+                           run as one kernel (conv1 result kept on chip); 0 = library
+                           default (192: every unit that fits), -1 = never.  A
+                           performance choice only: results agree within the decode
+                           tolerance either way.                                 */
   int cta_pair;         /* conv layers run on CTA pairs (2-CTA clusters sharing one
                            256-row MMA, each SM staging half of the weights):
                            0 = library default (off), 1 = on, -1 = off.  A

@@ -253,6 +253,17 @@ def test_decode_fusion_variants(arch, fuse):
     G.compare_audio(ref, got, f"fuse={fuse}")
 
 
+def test_fused_units_match_two_kernel_units_on_the_music_window():
+    """The bench's decoder with its residual units fused (the default) and as conv1 + conv2
+    kernels: the same arithmetic in another summation order, so the two decodes agree within
+    the audio tolerance everywhere, not only where the oracle samples them."""
+    wl = G.workload("music_window")
+    lat = wl.latent[:, :, :160]
+    fused = G.gpu_decode(V.Vocoder(wl.arch, V.fold_params(wl.params)), lat)
+    two = G.gpu_decode(V.Vocoder(wl.arch, V.fold_params(wl.params), fuse_max_channels=-1), lat)
+    G.compare_audio(two, fused, "fused vs two-kernel residual units")
+
+
 PROJ_MUSIC = W.Arch(latent_channels=64, channels0=384, strides=(8, 8, 4, 2), widths=(192, 96, 96, 48),
                     in_proj_channels=256)
 

@@ -19,8 +19,8 @@ from dac_vocoder_decode_gb300 import workloads as W  # noqa: E402
 from oracle import oracle as O  # noqa: E402
 from tests import gpu_common as G  # noqa: E402
 
-# causal; stages of 192 and 96 channels run as two kernels per residual unit, 48 and 32 as
-# one fused kernel; strides 8, 5, 4, 4, 3 as in the speech codec
+# causal; strides 8, 5, 4, 4, 3 as in the speech codec; every residual unit (at most 192
+# channels) runs as one fused kernel by default, as two kernels with fuse_max_channels=-1
 MID_CAUSAL = W.Arch(latent_channels=64, channels0=256, strides=(8, 5, 4, 4, 3),
                     widths=(192, 96, 48, 48, 32), padding=W.PAD_CAUSAL)
 MID_CAUSAL_PROJ = W.Arch(latent_channels=64, channels0=256, strides=(8, 5, 4, 4, 3),
@@ -40,11 +40,12 @@ def _stream(voc, latent, chunks, max_frames, stream_obj=None):
     return torch.cat(outs, dim=2)[:, 0].cpu().numpy().astype(np.float64), s
 
 
-@pytest.mark.parametrize("arch,cta_pair", [(MID_CAUSAL, 0), (MID_CAUSAL, 1), (MID_CAUSAL_PROJ, 0)],
-                         ids=["mid", "mid_cta_pair", "mid_in_proj"])
-def test_stream_equals_whole_decode(arch, cta_pair):
+@pytest.mark.parametrize("arch,cta_pair,fuse", [(MID_CAUSAL, 0, 0), (MID_CAUSAL, 1, 0),
+                                                (MID_CAUSAL_PROJ, 0, 0), (MID_CAUSAL, 0, -1)],
+                         ids=["mid", "mid_cta_pair", "mid_in_proj", "mid_two_kernel_units"])
+def test_stream_equals_whole_decode(arch, cta_pair, fuse):
     wl = W.make_custom(arch, B=2, T=37, seed=81)
-    voc = V.Vocoder(arch, V.fold_params(wl.params), cta_pair=cta_pair)
+    voc = V.Vocoder(arch, V.fold_params(wl.params), cta_pair=cta_pair, fuse_max_channels=fuse)
     whole = G.gpu_decode(voc, wl.latent)
     got, _ = _stream(voc, wl.latent, [1, 1, 2, 5, 8, 3, 8, 8, 1], max_frames=8)
     assert got.shape == whole.shape
