@@ -126,25 +126,11 @@ __device__ __forceinline__ void ru_store_h(uint32_t hbase, int Cp, int row, int 
   }
 }
 
-// Epilogue 2 of one warp for its 32 rows x the 16 columns n0.. of acc2 (taddr): bias, the
-// residual x (fp32 chunk-major, read from global memory), Snake of the next layer, hi/lo split
-// and stores -- the conv kernel's epilogue of a 1x1 conv with a residual input.  HEAD: the
-// output head's partial products of this row instead of stores (see epilogue_chunk).
-template <bool B2, bool HEAD>
-__device__ __forceinline__ bool ru_epilogue2(const ConvGemmArgs &p, const RuExtra &x,
-                                             volatile int *abort_flag, int b, int t, int n0,
-                                             uint32_t taddr, float (&hp)[kHeadFoldMaxK]) {
-  VOC_CHECK(t >= x.skip_L ||
-                (((long long)b * (p.Cp_out / 4) + n0 / 4 + 3) * (long long)x.skip_L + t) * 4 + 4 <=
-                    x.skip_elems,
-            51, b, n0, t);
-  float bb[16];
-  ldg_vec(p.bias + n0, bb);
-  uint32_t r[16], r2[16];
-  tmem_ld_issue<16>(taddr, r);
-  if constexpr (B2) tmem_ld_issue<16>(taddr + static_cast<uint32_t>(p.N_tile), r2);
-  float sk[16];
-  if (t < x.skip_L) {  // rows past the plane (the last tile's tail) are not results
+// The residual x of this thread's row t for the 16 columns n0.. (fp32 chunk-major planes of
+// skip_L rows; zeros past the plane, the last tile's tail rows, which are not results).
+__device__ __forceinline__ void ru_load_skip(const ConvGemmArgs &p, const RuExtra &x, int b, int t,
+                                             int n0, float (&sk)[16]) {
+  if (t < x.skip_L) {
     const float4 *s = reinterpret_cast<const float4 *>(p.skip) +
                       ((size_t)b * (p.Cp_out / 4) + n0 / 4) * (size_t)x.skip_L + t;
 #pragma unroll
@@ -156,6 +142,21 @@ __device__ __forceinline__ bool ru_epilogue2(const ConvGemmArgs &p, const RuExtr
 #pragma unroll
     for (int i = 0; i < 16; ++i) sk[i] = 0.f;
   }
+}
+
+// Epilogue 2 of one warp for its 32 rows x the 16 columns n0.. of acc2 (taddr): bias, the
+// residual x (sk, loaded by the caller from global memory), Snake of the next layer, hi/lo
+// split and stores -- the conv kernel's epilogue of a 1x1 conv with a residual input.  HEAD:
+// the output head's partial products of this row instead of stores (see epilogue_chunk).
+template <bool B2, bool HEAD>
+__device__ __forceinline__ bool ru_epilogue2(const ConvGemmArgs &p, volatile int *abort_flag,
+                                             int b, int t, int n0, uint32_t taddr,
+                                             const float (&sk)[16], float (&hp)[kHeadFoldMaxK]) {
+  float bb[16];
+  ldg_vec(p.bias + n0, bb);
+  uint32_t r[16], r2[16];
+  tmem_ld_issue<16>(taddr, r);
+  if constexpr (B2) tmem_ld_issue<16>(taddr + static_cast<uint32_t>(p.N_tile), r2);
   tmem_ld_wait<16>(r);  // the TMEM reads complete before any return
   if constexpr (B2) {
     tmem_ld16_after_wait(r2);
@@ -515,6 +516,20 @@ __global__ void __launch_bounds__(kRuThreads, 1)
     uint32_t dr[MC][16];
     bool ok = true;
     for (int it = 0; it <= n_my && ok; ++it) {
+      if (it < n_my && quad == 0 && lane == 0) {
+        // the residual rows of tile it, used by its epilogue 2 in the next iteration: into L2
+        // now (one 2 KB run of 128 rows per 4-channel plane of this group's chunks)
+        const int tile = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
+        const int mt = tile % p.m_tiles;
+        const int b = tile / p.m_tiles;
+        const int rows = min(kTileM, x.skip_L - mt * kTileM);
+        if (rows > 0)
+          for (int c = grp; c < n_chunks; c += kEpiGroups)
+            for (int j = 0; j < 4; ++j)
+              bulk_prefetch_l2(p.skip + (((size_t)b * (p.Cp_out / 4) + 4 * c + j) * (size_t)x.skip_L +
+                                         (size_t)mt * kTileM) * 4,
+                               static_cast<uint32_t>(rows) * 16u);
+      }
       if (it < n_my) {
         // epilogue 1 of tile it: acc1 -> registers (acc1 released), Snake2 -> H
         const uint32_t ip = static_cast<uint32_t>(it) & 1u;
@@ -550,8 +565,9 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         }
         tc_fence_after();
         for (int c = grp; c < n_chunks && ok; c += kEpiGroups) {
-          float hp[kHeadFoldMaxK] = {};
-          ok = ru_epilogue2<B2, HEAD>(p, x, abort_flag, b, t, 16 * c, t2 + static_cast<uint32_t>(16 * c), hp);
+          float sk[16], hp[kHeadFoldMaxK] = {};
+          ru_load_skip(p, x, b, t, 16 * c, sk);  // an L2 hit: prefetched one tile earlier
+          ok = ru_epilogue2<B2, HEAD>(p, abort_flag, b, t, 16 * c, t2 + static_cast<uint32_t>(16 * c), sk, hp);
           ok = __all_sync(0xffffffffu, ok);
           if constexpr (HEAD) {
             if (ok) ok = head_fold_store(p, hp, b, (mt * kTileM) / 32 + quad, c, lane, abort_flag);
