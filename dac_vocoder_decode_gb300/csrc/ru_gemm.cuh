@@ -47,7 +47,10 @@ struct RuExtra {
   const float *bias_h;     // [N] conv1 bias
   const float *alpha_h;    // [N] Snake2 alpha
   const float *invb_h;     // [N] Snake2 1/(alpha + 1e-9)
-  int h_bytes;             // bytes of the H tile (4 * 128 * Cp)
+  int h_bytes;             // bytes of the H tile (4 * 128 * Cp / h_parts)
+  int h_parts;             // 1: H holds all Cp channels; 2: H holds half of them at a time
+                           // (conv2 runs in two K halves), leaving shared memory to the
+                           // weight ring of the widest units
   int skip_L;              // rows of one plane of the fp32 residual input x
   long long skip_elems;    // floats of the residual input (the self-checking build's bound)
 };
@@ -103,24 +106,26 @@ __device__ __forceinline__ void ru_act1(const RuExtra &x, int grp, int n_chunks,
   }
 }
 
-// Epilogue 1, last part: the packed chunks into the H tile (8-channel chunk k of the hi parts
-// at H + k * 2048, of the lo parts at H + (Cp/8 + k) * 2048, row r at + 16 r).  A warp writes
-// 32 consecutive rows of a chunk: 512 contiguous bytes.
+// Epilogue 1, last part: the packed chunks of part q (of P) into the H tile.  Part q holds the
+// channels [q Cp/P, (q+1) Cp/P): its 8-channel chunk k of the hi parts at H + k * 2048, of the lo
+// parts at H + (Cp/(8P) + k) * 2048, row r at + 16 r.  A warp writes 32 consecutive rows of a
+// chunk: 512 contiguous bytes.
 template <int MC>
 __device__ __forceinline__ void ru_store_h(uint32_t hbase, int Cp, int row, int grp, int n_chunks,
-                                           const uint32_t (&dr)[MC][16]) {
-  const int lo0 = Cp / 8;
+                                           int q, int P, const uint32_t (&dr)[MC][16]) {
+  const int cpp = n_chunks / P;  // 16-column chunks per part
+  const int lo0 = Cp / (8 * P);
 #pragma unroll
   for (int j = 0; j < MC; ++j) {
     const int c = grp + kEpiGroups * j;
-    if (c < n_chunks) {
+    if (c < n_chunks && c / cpp == q) {
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {  // 8-channel chunk 2c + q: words 8q..8q+3 hi, 8q+4.. lo
-        const int k = 2 * c + q;
+      for (int qq = 0; qq < 2; ++qq) {  // 8-channel chunk 2c + qq: words 8qq..8qq+3 hi, +4.. lo
+        const int k = 2 * (c - q * cpp) + qq;
         sts128(hbase + static_cast<uint32_t>((k * kTileM + row) * 16),
-               make_uint4(dr[j][8 * q], dr[j][8 * q + 1], dr[j][8 * q + 2], dr[j][8 * q + 3]));
+               make_uint4(dr[j][8 * qq], dr[j][8 * qq + 1], dr[j][8 * qq + 2], dr[j][8 * qq + 3]));
         sts128(hbase + static_cast<uint32_t>(((lo0 + k) * kTileM + row) * 16),
-               make_uint4(dr[j][8 * q + 4], dr[j][8 * q + 5], dr[j][8 * q + 6], dr[j][8 * q + 7]));
+               make_uint4(dr[j][8 * qq + 4], dr[j][8 * qq + 5], dr[j][8 * qq + 6], dr[j][8 * qq + 7]));
       }
     }
   }
@@ -362,7 +367,8 @@ __global__ void __launch_bounds__(kRuThreads, 1)
     const uint32_t dA_k = (2 * chunkA) >> 4;
     const uint32_t dB_lo = (kchunks * chunkB) >> 4;
     const uint32_t dB_k = (2 * chunkB_stride) >> 4;
-    const uint32_t dH_lo = ((p.Cp_out / 8) * chunkH) >> 4;
+    const uint32_t dH_lo = ((p.Cp_out / (8 * x.h_parts)) * chunkH) >> 4;  // lo plane of a part
+    const int nkb2p = nkb2 / x.h_parts;  // k-blocks of one part
     const uint32_t dH_k = (2 * chunkH) >> 4;
     const uint32_t desc_hi = static_cast<uint32_t>(smem_desc(0u, 0u, 128) >> 32);
     const uint32_t a_desc0 = static_cast<uint32_t>(smem_desc(smem_u32(smA), chunkA, 128));
@@ -434,29 +440,34 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         if (!ok) break;
         mma_commit_warp(smem_u32(acc1Full));
       }
-      if (it >= 1) {  // conv2 (1x1) of tile it - 1 on H -> acc2
-        const uint32_t jp = static_cast<uint32_t>(it - 1) & 1u;
-        if (!wait_all(smem_u32(hFull), jp) || !wait_all(smem_u32(acc2Empty), jp ^ 1u)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      if (it >= 1) {  // conv2 (1x1) of tile it - 1 on H -> acc2, in h_parts K ranges
+        const int jt = it - 1;
         uint32_t accum = 0u;
-        for (int kb = 0; kb < nkb2; ++kb) {
-          if (!wait_all(smem_u32(fullB + sb), phb)) {
+        for (int q = 0; q < x.h_parts && ok; ++q) {
+          const uint32_t g = static_cast<uint32_t>(jt * x.h_parts + q);  // H fill number
+          if (!wait_all(smem_u32(hFull), g & 1u) ||
+              (q == 0 && !wait_all(smem_u32(acc2Empty), (static_cast<uint32_t>(jt) & 1u) ^ 1u))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          ksteps(d2, h_desc0 + static_cast<uint32_t>(kb * kchunks) * (chunkH >> 4), dH_lo, dH_k,
-                 b_desc0 + sb * b_slot_step, accum);
-          accum = 1u;
-          mma_commit_warp(smem_u32(emptyB + sb));
-          if (++sb == p.nb) sb = 0, phb ^= 1u;
+          for (int kb = 0; kb < nkb2p; ++kb) {
+            if (!wait_all(smem_u32(fullB + sb), phb)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            ksteps(d2, h_desc0 + static_cast<uint32_t>(kb * kchunks) * (chunkH >> 4), dH_lo, dH_k,
+                   b_desc0 + sb * b_slot_step, accum);
+            accum = 1u;
+            mma_commit_warp(smem_u32(emptyB + sb));
+            if (++sb == p.nb) sb = 0, phb ^= 1u;
+          }
+          if (!ok) break;
+          if (q == x.h_parts - 1) mma_commit_warp(smem_u32(acc2Full));
+          mma_commit_warp(smem_u32(hEmpty));  // H may be rewritten once these MMAs have read it
         }
         if (!ok) break;
-        mma_commit_warp(smem_u32(acc2Full));
-        mma_commit_warp(smem_u32(hEmpty));  // H may be rewritten once these MMAs have read it
       }
     }
     if (!ok) {
@@ -530,8 +541,21 @@ __global__ void __launch_bounds__(kRuThreads, 1)
                                          (size_t)mt * kTileM) * 4,
                                static_cast<uint32_t>(rows) * 16u);
       }
+      if (it >= 1 && x.h_parts == 2) {
+        // the second half of H(it - 1), from the registers of tile it - 1, once conv2 has read
+        // the first half
+        const uint32_t g = static_cast<uint32_t>((it - 1) * 2 + 1);  // H fill number
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(hEmpty), (g - 1u) & 1u, p.timeout, abort_flag))) {
+          ok = false;
+          break;
+        }
+        ru_store_h<MC>(hbase, p.Cp_out, row_in_tile, grp, n_chunks, 1, 2, dr);
+        fence_proxy_async_smem();  // the H stores become visible to the tensor cores
+        mbar_arrive(smem_u32(hFull));
+      }
       if (it < n_my) {
-        // epilogue 1 of tile it: acc1 -> registers (acc1 released), Snake2 -> H
+        // epilogue 1 of tile it: acc1 -> registers (acc1 released), Snake2 -> H (the first
+        // half when H holds half of the channels)
         const uint32_t ip = static_cast<uint32_t>(it) & 1u;
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(acc1Full), ip, p.timeout, abort_flag))) {
           ok = false;
@@ -542,12 +566,14 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         tc_fence_before();
         mbar_arrive(smem_u32(acc1Empty));
         ru_act1<MC>(x, grp, n_chunks, dr);
-        // H is free once conv2 of the previous tile has read it
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(hEmpty), ip ^ 1u, p.timeout, abort_flag))) {
+        // H is free once conv2 has read the previous fill
+        const int g = it * x.h_parts;  // H fill number (fill -1 counts as complete)
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(hEmpty), static_cast<uint32_t>(g - 1) & 1u,
+                                               p.timeout, abort_flag))) {
           ok = false;
           break;
         }
-        ru_store_h<MC>(hbase, p.Cp_out, row_in_tile, grp, n_chunks, dr);
+        ru_store_h<MC>(hbase, p.Cp_out, row_in_tile, grp, n_chunks, 0, x.h_parts, dr);
         fence_proxy_async_smem();  // the H stores become visible to the tensor cores
         mbar_arrive(smem_u32(hFull));
       }

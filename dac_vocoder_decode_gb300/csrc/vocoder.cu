@@ -478,6 +478,8 @@ bool plan_layer(bool pair, Layer &L, int padding, bool has_skip, std::string &wh
 constexpr int kRuMaxC = 192;
 // Residual units of up to this many (padded) channels run as one kernel by default.
 constexpr int kFuseDefault = kRuMaxC;
+// Units of at least this many channels keep half of the H tile at a time.
+constexpr int kRuHalfHMinC = 160;
 bool plan_ru(Layer &L, int padding, std::string &why) {
   ConvGemmArgs &g = L.g;
   L.Cp_in = L.Cp_out = rup(L.Cout, 16);
@@ -505,7 +507,11 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
   // B2 form (two MMAs per K step) when the doubled column count fits one MMA
   g.b2 = (2 * g.N_tile <= 256) ? 1 : 0;
   L.cw = 16;
-  L.rx.h_bytes = 4 * voc::kTileM * L.Cp_out;
+  // The widest units keep half of H at a time (conv2 runs in two K halves): the shared memory
+  // this frees goes to the weight ring, which conv1's 7 taps x C^2 weights per tile stream
+  // through (with the whole H tile the ring holds three stages and conv1 waits on weights).
+  L.rx.h_parts = (L.Cp_out >= kRuHalfHMinC && (L.Cp_out / 16) % 2 == 0) ? 2 : 1;
+  L.rx.h_bytes = 4 * voc::kTileM * L.Cp_out / L.rx.h_parts;
   int ac = 32;
   while (ac < (g.b2 ? 2 * g.N_tile : g.N_tile)) ac *= 2;
   g.acc_cols = ac;  // acc1 at column 0, acc2 at column ac: 2 ac <= 512
@@ -517,7 +523,9 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
   g.KB = 0;
   for (int min_nb = 3; min_nb >= 2 && !g.KB; --min_nb)
     for (int kb = L.Cp_in; kb >= 16 && !g.KB; kb -= 16) {
-      if (L.Cp_in % kb || 4 * kb * g.N_tile > kBStageMax || 4 * kb * g.rows > 72 * 1024) continue;
+      if ((L.Cp_in / L.rx.h_parts) % kb || 4 * kb * g.N_tile > kBStageMax ||
+          4 * kb * g.rows > 72 * 1024)
+        continue;
       const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
       const int b_bytes = 4 * kb * g.N_tile;
       const int na = 2;
