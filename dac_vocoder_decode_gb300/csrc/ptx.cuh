@@ -166,6 +166,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 }
 
 // ------------------------------------------------------------------ tcgen05
+// Prefetch the cache line holding `p` into L1 (no completion to wait for).
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned source) from global memory
 // into L2, with no completion to wait for.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {

@@ -149,6 +149,17 @@ __device__ __forceinline__ void ru_load_skip(const ConvGemmArgs &p, const RuExtr
   }
 }
 
+// The four 16-byte rows of this thread's residual x for the columns n0.. into L1 (a warp covers
+// 32 rows x 16 channels: 2 KB), so that epilogue 2 finds them there one chunk later.
+__device__ __forceinline__ void ru_prefetch_skip_l1(const ConvGemmArgs &p, const RuExtra &x,
+                                                    int b, int t, int n0) {
+  if (t >= x.skip_L) return;
+  const float4 *s = reinterpret_cast<const float4 *>(p.skip) +
+                    ((size_t)b * (p.Cp_out / 4) + n0 / 4) * (size_t)x.skip_L + t;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) prefetch_l1(s + (size_t)j * x.skip_L);
+}
+
 // Epilogue 2 of one warp for its 32 rows x the 16 columns n0.. of acc2 (taddr): bias, the
 // residual x (sk, loaded by the caller from global memory), Snake of the next layer, hi/lo
 // split and stores -- the conv kernel's epilogue of a 1x1 conv with a residual input.  HEAD:
@@ -584,6 +595,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         const int mt = tile % p.m_tiles;
         const int b = tile / p.m_tiles;
         const int t = mt * kTileM + row_in_tile;
+        if (grp < n_chunks) ru_prefetch_skip_l1(p, x, b, t, 16 * grp);  // the first chunk's x
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(acc2Full), static_cast<uint32_t>(jt) & 1u,
                                                p.timeout, abort_flag))) {
           ok = false;
@@ -592,7 +604,10 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         tc_fence_after();
         for (int c = grp; c < n_chunks && ok; c += kEpiGroups) {
           float sk[16], hp[kHeadFoldMaxK] = {};
-          ru_load_skip(p, x, b, t, 16 * c, sk);  // an L2 hit: prefetched one tile earlier
+          // x of the warp's next chunk into L1 while this one is processed (into L2 it came one
+          // tile earlier)
+          if (c + kEpiGroups < n_chunks) ru_prefetch_skip_l1(p, x, b, t, 16 * (c + kEpiGroups));
+          ru_load_skip(p, x, b, t, 16 * c, sk);
           ok = ru_epilogue2<B2, HEAD>(p, abort_flag, b, t, 16 * c, t2 + static_cast<uint32_t>(16 * c), sk, hp);
           ok = __all_sync(0xffffffffu, ok);
           if constexpr (HEAD) {
