@@ -166,6 +166,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 }
 
 // ------------------------------------------------------------------ tcgen05
+// Warp-group register reallocation: every warp of a 4-warp group executes the same one.  The
+// block's registers at launch must cover the sum over its warp groups (checked on the host).
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
 // Prefetch the cache line holding `p` into L1 (no completion to wait for).
 __device__ __forceinline__ void prefetch_l1(const void *p) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(p));

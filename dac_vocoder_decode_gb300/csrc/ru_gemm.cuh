@@ -19,11 +19,12 @@
 // (bias, residual, Snake of the next layer, fp32 and hi/lo stores) while conv1(i+1) runs.
 // Epilogue work therefore overlaps the tensor cores instead of sitting between conv1 and conv2.
 //
-// Roles (15 warps): warp 0 lane 0 issues the A copies (one 5-D TMA box per k-block), warp 1
-// issues the MMAs (convergently; an elected lane issues), warps 2..13 are the epilogue: three
-// groups of four warps, one warp per TMEM lane quadrant, group g taking the 16-column chunks
-// g, g+3, ...; warp 14 lane 0 streams the weight stages (conv1's taps x k-blocks, then conv2's
-// k-blocks, in the MMA warp's order).
+// Roles (16 warps): warp 0 lane 0 issues the A copies (one 5-D TMA box per k-block), warp 1
+// issues the MMAs (convergently; an elected lane issues), warp 2 lane 0 streams the weight
+// stages (conv1's taps x k-blocks, then conv2's k-blocks, in the MMA warp's order); warps 4..15
+// are the epilogue: three groups of four warps, one warp per TMEM lane quadrant, group g taking
+// the 16-column chunks g, g+3, ...  The first warp group hands registers to the other three
+// (setmaxnreg), which hold a tile's conv1 accumulator row in registers.
 //
 // B2 (units of up to 128 channels): both convolutions take the conv kernel's two-MMA K step --
 // A_hi x [W_hi | W_lo] into 2N accumulator columns, then A_lo x W_hi into the first N -- and the
@@ -34,9 +35,18 @@
 
 namespace voc {
 
-constexpr int kRuEpiWarps = 4 * kEpiGroups;          // warps 2..13
-constexpr int kRuBWarp = 2 + kRuEpiWarps;            // 14: weight copies
-constexpr int kRuThreads = 32 * (kRuBWarp + 1);      // 480
+// Warp group 0 (warps 0..3) issues copies and MMAs with few registers; warp groups 1..3 are the
+// epilogue, with the registers the others give up (setmaxnreg): 128 x 56 + 384 x 152 = 65536,
+// the 512 threads x 128 registers the block is launched with.
+constexpr int kRuBWarp = 2;                          // weight copies (warp 3 idles)
+constexpr int kRuEpi0 = 4;                           // first epilogue warp
+constexpr int kRuEpiWarps = 4 * kEpiGroups;          // warps 4..15
+constexpr int kRuThreads = 32 * (kRuEpi0 + kRuEpiWarps);  // 512
+constexpr int kRuLaunchRegs = 128;                   // registers per thread at launch
+constexpr int kRuCopyRegs = 56;                      // warp group 0 after the split
+constexpr int kRuEpiRegs = 152;                      // epilogue warp groups after the split
+static_assert(128 * kRuCopyRegs + 32 * kRuEpiWarps * kRuEpiRegs <= kRuThreads * kRuLaunchRegs,
+              "the register split exceeds the launch allocation");
 // 16-column chunks of one epilogue group: C <= 192 has 12 chunks (4 per group); the B2 form
 // (C <= 128) at most 8 (3 per group)
 template <bool B2>
@@ -150,7 +160,7 @@ __device__ __forceinline__ void ru_load_skip(const ConvGemmArgs &p, const RuExtr
 }
 
 // The four 16-byte rows of this thread's residual x for the columns n0.. into L1 (a warp covers
-// 32 rows x 16 channels: 2 KB), so that epilogue 2 finds them there one chunk later.
+// 32 rows x 16 channels: 2 KB), so that epilogue 2 finds them there two chunks later.
 __device__ __forceinline__ void ru_prefetch_skip_l1(const ConvGemmArgs &p, const RuExtra &x,
                                                     int b, int t, int n0) {
   if (t >= x.skip_L) return;
@@ -322,7 +332,11 @@ __global__ void __launch_bounds__(kRuThreads, 1)
   const uint32_t chunkH = kTileM * 16u;
   const int n_chunks = p.N_tile / 16;
 
+  // Each role changes its warp's register count first thing in its own branch (all four warps of
+  // a warp group execute the same change), so that the compiler allocates each role's code
+  // within its own count.
   if (warp == 0) {
+    regs_dec<kRuCopyRegs>();
     if (lane == 0) {
       // ------------------------------------------------------------ A producer
       prefetch_tmap(&tmapA);
@@ -364,6 +378,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
       }
     }
   } else if (warp == 1) {
+    regs_dec<kRuCopyRegs>();
     // -------------------------------------------------------------- MMA issuer (whole warp)
     // warp-uniform waits; one elected lane issues each MMA and commit
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
@@ -492,6 +507,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
       mbar_wait(smem_u32(drain), 0u, kDrainBudget, &never);
     }
   } else if (warp == kRuBWarp) {
+    regs_dec<kRuCopyRegs>();
     if (lane == 0) {
       // ------------------------------------------------------------ weight producer
       // Stages in the MMA warp's order: conv1 of tile it (k-blocks x taps), then conv2 of
@@ -522,11 +538,14 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         drain_ring(fullB, p.nb, ib, kDrainBudget);
       }
     }
-  } else if (warp >= 2 && warp < 2 + kRuEpiWarps) {
+  } else if (warp < kRuEpi0) {
+    regs_dec<kRuCopyRegs>();  // warp 3: no role
+  } else {
+    regs_inc<kRuEpiRegs>();
     // -------------------------------------------------------------- epilogue
     pdl_wait();  // the residual input is the previous layer's output; this unit's outputs
                  // overwrite buffers earlier layers read
-    const int e = warp - 2;
+    const int e = warp - kRuEpi0;
     const int quad = warp & 3;   // TMEM lane quadrant this warp may access
     const int grp = e / 4;       // column chunks grp, grp + 3, ...
     const int row_in_tile = quad * 32 + lane;
@@ -595,19 +614,21 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         const int mt = tile % p.m_tiles;
         const int b = tile / p.m_tiles;
         const int t = mt * kTileM + row_in_tile;
-        if (grp < n_chunks) ru_prefetch_skip_l1(p, x, b, t, 16 * grp);  // the first chunk's x
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(acc2Full), static_cast<uint32_t>(jt) & 1u,
                                                p.timeout, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
+        float skn[16];  // x of the warp's next chunk, loaded one chunk ahead
+        if (grp < n_chunks) ru_load_skip(p, x, b, t, 16 * grp, skn);
         for (int c = grp; c < n_chunks && ok; c += kEpiGroups) {
           float sk[16], hp[kHeadFoldMaxK] = {};
-          // x of the warp's next chunk into L1 while this one is processed (into L2 it came one
-          // tile earlier)
-          if (c + kEpiGroups < n_chunks) ru_prefetch_skip_l1(p, x, b, t, 16 * (c + kEpiGroups));
-          ru_load_skip(p, x, b, t, 16 * c, sk);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sk[i] = skn[i];
+          if (c + kEpiGroups < n_chunks) ru_load_skip(p, x, b, t, 16 * (c + kEpiGroups), skn);
+          // and the chunk after it into L1 (into L2 every chunk came one tile earlier)
+          if (c + 2 * kEpiGroups < n_chunks) ru_prefetch_skip_l1(p, x, b, t, 16 * (c + 2 * kEpiGroups));
           ok = ru_epilogue2<B2, HEAD>(p, abort_flag, b, t, 16 * c, t2 + static_cast<uint32_t>(16 * c), sk, hp);
           ok = __all_sync(0xffffffffu, ok);
           if constexpr (HEAD) {

@@ -179,6 +179,11 @@ cudaError_t set_conv_attrs() {
   return st;
 }
 
+// The fused residual-unit kernel splits its block's registers between warp groups with
+// setmaxnreg, which waits until the registers it asks for are free: it is only launched when the
+// block gets the registers per thread the split assumes (set_kernel_attrs checks every form).
+bool g_ru_regs_ok = false;
+
 bool set_kernel_attrs(std::string &why) {
   static cudaError_t st = cudaErrorUnknown;
   static std::once_flag once;
@@ -193,6 +198,18 @@ bool set_kernel_attrs(std::string &why) {
     if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<true, false>);
     if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<false, true>);
     if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<true, true>);
+    if (st == cudaSuccess) {
+      auto regs_ok = [](auto kernel) {
+        cudaFuncAttributes fa{};
+        return cudaFuncGetAttributes(&fa, kernel) == cudaSuccess &&
+               fa.numRegs * voc::kRuThreads >=
+                   128 * voc::kRuCopyRegs + 32 * voc::kRuEpiWarps * voc::kRuEpiRegs;
+      };
+      g_ru_regs_ok = regs_ok(voc::ru_gemm_kernel<false, false>) &&
+                     regs_ok(voc::ru_gemm_kernel<true, false>) &&
+                     regs_ok(voc::ru_gemm_kernel<false, true>) &&
+                     regs_ok(voc::ru_gemm_kernel<true, true>);
+    }
     if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::out_head_kernel<kHeadTile>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
@@ -485,6 +502,10 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
   L.Cp_in = L.Cp_out = rup(L.Cout, 16);
   if (L.Cp_out > kRuMaxC) {
     why = "too many channels for the fused residual unit";
+    return false;
+  }
+  if (!g_ru_regs_ok) {
+    why = "the fused residual unit's register split does not fit its launch";
     return false;
   }
   g.Cp_in = g.Cp_out = L.Cp_out;
