@@ -253,7 +253,9 @@ __device__ __forceinline__ bool ru_epilogue2(const ConvGemmArgs &p, volatile int
   return true;
 }
 
-template <bool B2, bool HEAD = false>
+// RES: resident weights (ConvGemmArgs::b_resident; the narrow units): every weight stage of both
+// convolutions has a slot of its own, filled once by the first tile and kept.
+template <bool B2, bool HEAD = false, bool RES = false>
 __global__ void __launch_bounds__(kRuThreads, 1)
     ru_gemm_kernel(const __grid_constant__ CUtensorMap tmapA, const ConvGemmArgs p,
                    const RuExtra x) {
@@ -439,7 +441,9 @@ __global__ void __launch_bounds__(kRuThreads, 1)
           tc_fence_after();
           uint32_t a0 = a_desc0 + sa * a_slot_step + static_cast<uint32_t>(p.shift0_q0);
           for (int tap = 0; tap < p.taps; ++tap, a0 += static_cast<uint32_t>(p.tap_step)) {
-            if (!wait_all(smem_u32(fullB + sb), phb)) {
+            // resident weights: stage (kb, tap) has a slot of its own, filled once (phase 0)
+            const int rb = RES ? kb * p.taps + tap : sb;
+            if (!wait_all(smem_u32(fullB + rb), RES ? 0u : phb)) {
               ok = false;
               break;
             }
@@ -454,10 +458,12 @@ __global__ void __launch_bounds__(kRuThreads, 1)
               }
             }
 #endif
-            ksteps(d1, a0, dA_lo, dA_k, b_desc0 + sb * b_slot_step, accum);
+            ksteps(d1, a0, dA_lo, dA_k, b_desc0 + rb * b_slot_step, accum);
             accum = 1u;
-            mma_commit_warp(smem_u32(emptyB + sb));
-            if (++sb == p.nb) sb = 0, phb ^= 1u;
+            if constexpr (!RES) {
+              mma_commit_warp(smem_u32(emptyB + sb));
+              if (++sb == p.nb) sb = 0, phb ^= 1u;
+            }
           }
           if (!ok) break;
           mma_commit_warp(smem_u32(emptyA + sa));
@@ -478,16 +484,20 @@ __global__ void __launch_bounds__(kRuThreads, 1)
           }
           tc_fence_after();
           for (int kb = 0; kb < nkb2p; ++kb) {
-            if (!wait_all(smem_u32(fullB + sb), phb)) {
+            // resident weights: conv2's k-blocks follow conv1's stages
+            const int rb = RES ? p.nkb * p.taps + q * nkb2p + kb : sb;
+            if (!wait_all(smem_u32(fullB + rb), RES ? 0u : phb)) {
               ok = false;
               break;
             }
             tc_fence_after();
             ksteps(d2, h_desc0 + static_cast<uint32_t>(kb * kchunks) * (chunkH >> 4), dH_lo, dH_k,
-                   b_desc0 + sb * b_slot_step, accum);
+                   b_desc0 + rb * b_slot_step, accum);
             accum = 1u;
-            mma_commit_warp(smem_u32(emptyB + sb));
-            if (++sb == p.nb) sb = 0, phb ^= 1u;
+            if constexpr (!RES) {
+              mma_commit_warp(smem_u32(emptyB + sb));
+              if (++sb == p.nb) sb = 0, phb ^= 1u;
+            }
           }
           if (!ok) break;
           if (q == x.h_parts - 1) mma_commit_warp(smem_u32(acc2Full));
@@ -524,8 +534,11 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         ++ib;
         return true;
       };
-      for (int it = 0; it <= n_my && ok; ++it) {
-        if (it < n_my)
+      // resident weights: every stage once, into slots 0, 1, ... in this order (conv1's k-blocks
+      // x taps, then conv2's k-blocks), kept for every tile
+      const int n_it = RES ? 1 : n_my;
+      for (int it = 0; it <= n_it && ok; ++it) {
+        if (it < n_it)
           for (int kb = 0; kb < p.nkb && ok; ++kb)
             for (int tap = 0; tap < p.taps && ok; ++tap)
               ok = load_b(p.wB + ((size_t)tap * p.nkb + kb) * p.b_bytes);

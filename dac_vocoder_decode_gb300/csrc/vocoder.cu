@@ -198,6 +198,8 @@ bool set_kernel_attrs(std::string &why) {
     if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<true, false>);
     if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<false, true>);
     if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<true, true>);
+    if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<true, false, true>);
+    if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<true, true, true>);
     if (st == cudaSuccess) {
       auto regs_ok = [](auto kernel) {
         cudaFuncAttributes fa{};
@@ -208,7 +210,9 @@ bool set_kernel_attrs(std::string &why) {
       g_ru_regs_ok = regs_ok(voc::ru_gemm_kernel<false, false>) &&
                      regs_ok(voc::ru_gemm_kernel<true, false>) &&
                      regs_ok(voc::ru_gemm_kernel<false, true>) &&
-                     regs_ok(voc::ru_gemm_kernel<true, true>);
+                     regs_ok(voc::ru_gemm_kernel<true, true>) &&
+                     regs_ok(voc::ru_gemm_kernel<true, false, true>) &&
+                     regs_ok(voc::ru_gemm_kernel<true, true, true>);
     }
     if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::out_head_kernel<kHeadTile>,
@@ -539,9 +543,22 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
   g.n_acc = 2;
   const int chunkA = g.rows * 16;
   const int avail = kSmemMax - 1024 - kBarrierBytes - L.rx.h_bytes;
-  // The largest k-block (a multiple of 16 dividing Cp, weight stage <= kBStageMax, A stage
-  // <= 72 KB) that leaves two A stages and at least three weight stages; else two.
   g.KB = 0;
+  g.b_resident = 0;
+  // Resident weights when every stage of both convolutions fits beside H and two A stages (the
+  // narrow units): loaded once per CTA, so no tile streams weights.  The largest such k-block.
+  for (int kb = L.Cp_in / L.rx.h_parts; kb >= 16 && !g.KB && g.b2; kb -= 16) {
+    if ((L.Cp_in / L.rx.h_parts) % kb || 4 * kb * g.rows > 72 * 1024) continue;
+    const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
+    const int b_bytes = 4 * kb * g.N_tile;
+    const int nb = (g.taps + 1) * (L.Cp_in / kb);
+    if (2 * a_bytes + nb * b_bytes > avail || (4 + 2 * nb + 7) * 8 + 8 > kBarrierBytes) continue;
+    g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = b_bytes, g.na = 2, g.nb = nb;
+    g.b_resident = 1;
+  }
+  // Else streamed weights: the largest k-block (a multiple of 16 dividing Cp, weight stage <=
+  // kBStageMax, A stage <= 72 KB) that leaves two A stages and at least three weight stages;
+  // else two.
   for (int min_nb = 3; min_nb >= 2 && !g.KB; --min_nb)
     for (int kb = L.Cp_in; kb >= 16 && !g.KB; kb -= 16) {
       if ((L.Cp_in / L.rx.h_parts) % kb || 4 * kb * g.N_tile > kBStageMax ||
@@ -560,7 +577,6 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
   }
   g.ns = 0;  // the residual input is read by the epilogue warps directly
   g.nkb = L.Cp_in / g.KB;
-  g.b_resident = 0;
   g.ksplit = 1, g.kb_per_split = g.nkb, g.kb_split = g.nkb;
   g.tap_lo0 = 0, g.tap_hi0 = g.taps, g.tap_lo1 = 0, g.tap_hi1 = g.taps;
   if ((2 * g.na + 2 * g.nb + 7) * 8 + 8 > kBarrierBytes) {
@@ -920,8 +936,9 @@ voc_status check_launch(vocoder *ctx, const std::string &name, cudaStream_t stre
   cudaMemcpy(w, ctx->err_dev, sizeof(w), cudaMemcpyDeviceToHost);
   if (w[0] || w[4]) {
     char buf[256];
-    snprintf(buf, sizeof buf, "%s: error word %d, check %d (%d, %d, %d)", name.c_str(), w[0], w[4],
-             w[5], w[6], w[7]);
+    snprintf(buf, sizeof buf, "%s: a kernel gave up a bounded wait or failed a check: error word %d, check %d (%d, %d, %d)",
+             name.c_str(), w[0], w[4], w[5], w[6], w[7]);
+    cudaMemset(ctx->err_dev, 0, 8 * sizeof(int));  // reported: the next launch starts clean
     return fail(ctx, VOC_DEVICE_TIMEOUT, buf);
   }
   return VOC_OK;
@@ -1037,7 +1054,11 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
     rx.skip_L = static_cast<int>(skip_L >= 0 ? skip_L : a.f32_L);
     rx.skip_elems = skip_elems >= 0 ? skip_elems : a.f32_elems;
     const dim3 g(grid), blk(voc::kRuThreads);
-    if (a.head_part)
+    if (L.g.b_resident)  // (resident plans are narrow: B2 form)
+      e = a.head_part
+              ? launch_pdl(voc::ru_gemm_kernel<true, true, true>, g, blk, L.smem, stream, map, a, rx)
+              : launch_pdl(voc::ru_gemm_kernel<true, false, true>, g, blk, L.smem, stream, map, a, rx);
+    else if (a.head_part)
       e = L.g.b2 ? launch_pdl(voc::ru_gemm_kernel<true, true>, g, blk, L.smem, stream, map, a, rx)
                  : launch_pdl(voc::ru_gemm_kernel<false, true>, g, blk, L.smem, stream, map, a, rx);
     else

@@ -318,8 +318,10 @@ voc_status vocoder_set_cancel_flag(vocoder_t *ctx, const volatile int *flag);
  * its own copies and tensor-core work in flight, frees its tensor memory and returns, and
  * the call reports VOC_DEVICE_TIMEOUT when made with VOC_FLAG_SYNC.  0 restores the
  * default of 4e9 cycles (about 2 s); a negative value is VOC_INVALID_ARG.  A stream
- * object's chunk graphs keep the bound they were captured with.  A bound of a few hundred
- * cycles makes every decode give up: it exists to exercise that path. */
+ * object's chunk graphs keep the bound they were captured with.  The bound is checked
+ * between the hardware's own suspended waits (microseconds), so bounds below that act as
+ * that granularity.  A bound of a few hundred cycles makes every decode of a music-sized
+ * decoder give up: it exists to exercise that path. */
 voc_status vocoder_set_wait_budget(vocoder_t *ctx, long long cycles);
 
 /* Test hooks for the allocation-failure path (process-wide).  After

@@ -3,8 +3,8 @@ faulting the GPU.
 
 * Bounded waits: a context whose wait bound is a few hundred cycles gives up inside its
   kernels (which drain their own copies and tensor-core work before returning) and the
-  decode reports VOC_DEVICE_TIMEOUT; the same context with the default bound, and a fresh
-  one, then decode correctly.
+  decode reports VOC_DEVICE_TIMEOUT; the same context with the default bound then decodes
+  exactly as a fresh one does.
 * Allocation failure: an out-of-memory cudaMalloc injected at every position of
   vocoder_create (and of vocoder_stream_create) returns VOC_OOM and leaves no device
   allocation behind.
@@ -36,8 +36,9 @@ SMALL_CAUSAL = W.Arch(latent_channels=16, channels0=64, strides=(4, 2), widths=(
 
 
 def test_short_wait_bound_reports_timeout_then_recovers():
-    wl = G.workload("tiny_cal")
-    ref = O.decode(wl.arch, wl.params, wl.latent)
+    """The music decoder (a 32-frame window: every kernel's first waits last tens of
+    microseconds, far longer than one suspended mbarrier wait) under a 300-cycle bound."""
+    wl = G.workload("music_window", T=32, B=1)
     voc = G.gpu_decoder(wl)
     lat = torch.from_numpy(wl.latent).cuda()
     V.vocoder_set_wait_budget(voc.handle, 300)  # cycles: every kernel gives up at once
@@ -48,10 +49,9 @@ def test_short_wait_bound_reports_timeout_then_recovers():
         assert "bounded wait" in V.vocoder_last_error(voc.handle)
     V.vocoder_set_wait_budget(voc.handle, 0)  # the default bound again
     got = G.gpu_decode(voc, wl.latent)
-    G.compare_audio(ref, got, "same context after the timeouts")
     fresh = G.gpu_decoder(wl)
-    G.compare_audio(ref, G.gpu_decode(fresh, wl.latent), "fresh context")
     np.testing.assert_array_equal(got, G.gpu_decode(fresh, wl.latent))
+    assert np.all(np.isfinite(got)) and float(np.max(np.abs(got))) > 0.0
     with pytest.raises(V.VocoderError) as e:
         V.vocoder_set_wait_budget(voc.handle, -1)
     assert e.value.status == V.VOC_INVALID_ARG
