@@ -144,7 +144,33 @@ struct ConvGemmArgs {
   const float *head_w;     // [head_K][Cp_out] head weights (zero past the real channels)
   float *head_part;
   int head_K, head_pad, head_slices, head_slice_len;
+  // Job order: 0 -- row tiles outer, column tiles inner (each wave reads every column tile's
+  // weights); band > 0 -- the row tiles in bands of `band`, and inside a band the column tiles
+  // outer, so that a wave reads a part of the weights (layers whose weights outweigh L2's share).
+  // Not with resident weights (each CTA keeps one column tile).
+  int band;
 };
+
+// Column tile nt, row tile mt and item b of tile job jj (see ConvGemmArgs::band).
+__device__ __forceinline__ void job_tile(const ConvGemmArgs &p, int jj, int &nt, int &mt, int &b) {
+  if (p.band > 0) {
+    const int rows = p.B * p.m_tiles;
+    const int per_band = p.band * p.n_tiles;
+    const int bi = jj / per_band;
+    const int r0 = bi * p.band;
+    const int nr = min(p.band, rows - r0);  // row tiles of this band
+    const int w = jj - bi * per_band;
+    nt = w / nr;
+    const int rr = r0 + (w - nt * nr);
+    mt = rr % p.m_tiles;
+    b = rr / p.m_tiles;
+  } else {
+    nt = jj % p.n_tiles;
+    const int rest = jj / p.n_tiles;
+    mt = rest % p.m_tiles;
+    b = rest / p.m_tiles;
+  }
+}
 
 // Taps of the head fold (the conv kernel's HEAD form): the decoder's 7-tap head; a shorter head
 // is folded with its weights zero-padded to 7 taps (head_K = 7, the same head_pad).
@@ -778,9 +804,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int job = job0; job < total_jobs && ok; job += job_step) {
         int jj, kb0, kb1, ks;
         job_range(job, jj, kb0, kb1, ks);
-        const int rest = jj / p.n_tiles;
-        const int mt = rest % p.m_tiles;
-        const int b = rest / p.m_tiles;
+        int nt_, mt, b;
+        job_tile(p, jj, nt_, mt, b);
         // first staged row, rounded down to the 8-row group the tensor map addresses (the
         // host adds the remainder, the same for every job, to the MMA row shift)
         const int yg = floor_div8(p.in_row0 + mt * kM + row0 + p.off_min);
@@ -888,7 +913,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int job = job0; job < total_jobs && ok; job += job_step) {
         int jj, kb0, kb1, ks;
         job_range(job, jj, kb0, kb1, ks);
-        const int nt = jj % p.n_tiles;
+        int nt, mt_, b_;
+        job_tile(p, jj, nt, mt_, b_);
         const int shift0 = (nt >= p.q_split_tile) ? p.shift0_q1 : p.shift0_q0;
         if (!wait_all(smem_u32(accEmpty + acc), phacc ^ 1u, PAIR)) {
           ok = false;
@@ -988,7 +1014,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int job = job0; job < job_end && ok; job += job_step) {
         int jj, kb0, kb1, ks;
         job_range(job, jj, kb0, kb1, ks);
-        const int nt = jj % p.n_tiles;
+        int nt, mt_, b_;
+        job_tile(p, jj, nt, mt_, b_);
         const int wt = PAIR ? 2 * nt + static_cast<int>(rank) : nt;  // packed weight tile
         for (int kb = kb0; kb < kb1 && ok; ++kb) {
           int tap0 = 0, tap1 = p.taps;
@@ -1041,10 +1068,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t ph[kEpiGroups] = {};
       bool ok = true;
       for (int job = job0; job < total_jobs && ok; job += job_step) {
-        const int nt = job % p.n_tiles;
-        const int rest = job / p.n_tiles;
-        const int mt = rest % p.m_tiles;
-        const int b = rest / p.m_tiles;
+        int nt, mt, b;
+        job_tile(p, job, nt, mt, b);
         for (int c0 = 0; c0 < n_chunks && ok; c0 += kEpiGroups) {
 #pragma unroll
           for (int h = 0; h < kEpiGroups; ++h) {
@@ -1099,10 +1124,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int job = job0; job < total_jobs && ok; job += job_step) {
       int jj, kb0, kb1, ks;
       job_range(job, jj, kb0, kb1, ks);
-      const int nt = jj % p.n_tiles;
-      const int rest = jj / p.n_tiles;
-      const int mt = rest % p.m_tiles;
-      const int b = rest / p.m_tiles;
+      int nt, mt, b;
+      job_tile(p, jj, nt, mt, b);
       // decisions stay warp-uniform: tcgen05.ld is a warp-collective instruction
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(accFull + acc), phacc, p.timeout, abort_flag))) {
         ok = false;

@@ -38,6 +38,8 @@ constexpr int kMaxResidentStages = 32;  // weight slots of a resident plan
 constexpr int kMaxResidentTiles = 8;    // column tiles of a resident plan (one per CTA)
 constexpr int kMinAInFlight = 48 * 1024;  // A ring bytes a resident plan must keep
 constexpr int kBStageMax = 36 * 1024;  // bytes of one weight stage (per CTA)
+constexpr double kBandWeightBytes = 32e6;  // weights from which a layer takes the band job order
+constexpr int kBandRows = 12;             // row tiles of one band
 
 thread_local std::string g_err;  // last error without a context
 
@@ -454,6 +456,11 @@ bool plan_gemm(Layer &L, int padding, bool has_skip, std::string &why) {
   g.n_acc = std::min(voc::kMaxAcc, 512 / ac);
   L.smem = 1024 + (size_t)g.na * g.a_bytes + (size_t)g.nb * g.b_bytes +
            (size_t)g.ns * voc::skip_slot_bytes(L.cw) + kBarrierBytes;
+  // Layers whose weights are a large share of L2 (the first transposed conv: 75 MB) take the
+  // band job order: a wave covers about half of the column tiles for every row tile of a band
+  // instead of every column tile, so each weight byte comes from HBM once.
+  const double w_bytes = (double)g.N_total * L.Cp_in * taps_eff * wb;
+  g.band = (!g.b_resident && !L.pair && w_bytes >= kBandWeightBytes) ? kBandRows : 0;
   return true;
 }
 
