@@ -2597,14 +2597,14 @@ int enc_ksplit(const vocoder_encoder *enc, size_t i, int B, long long rows, size
 void enc_layer_cost(const Layer &L, int B, long long L_in, bool split_k, double &flops,
                     double &alg, double &impl) {
   const double rows = (double)B * (double)L_in;
-  const double k = L.down_s ? 2.0 * L.down_s : (double)L.K;
+  const double k = L.down_s ? 2.0 * L.down_s : (double)L.K + (L.ru ? 1.0 : 0.0);
   const double cin = L.down_s ? (double)L.down_c : (double)L.Cin;
   flops = 2.0 * cin * L.Cout * k * rows;
   alg = 4.0 * cin * rows * (L.down_s ? L.down_s : 1);
-  if (L.skip_buf >= 0) alg += 4.0 * L.Cout * rows;
+  if (L.skip_buf >= 0 && !L.ru) alg += 4.0 * L.Cout * rows;  // a fused unit's skip is its input
   if (!split_k) alg += 4.0 * L.Cout * rows;
   const ConvGemmArgs &g = L.g;
-  double by = 4.0 * rows * L.Cp_in + (double)g.n_tiles * g.taps * g.nkb * g.b_bytes;
+  double by = 4.0 * rows * L.Cp_in + (double)g.n_tiles * (g.taps + (L.ru ? 1 : 0)) * g.nkb * g.b_bytes;
   const double out_elems = rows * L.Cp_out;
   if (L.skip_buf >= 0) by += 4.0 * out_elems;
   if (L.f32_buf >= 0) by += 4.0 * out_elems;
@@ -2713,7 +2713,8 @@ VOC_API voc_status vocoder_encoder_create(const voc_enc_desc *desc, const float 
   enc->Cp_lat = rup(desc->latent_channels, 16);
   ctx->prec = desc->precision;
   ctx->use_pair = false;
-  ctx->fuse_max_c = 0;
+  // residual units before a block's last one run as one fused kernel (bf16x3), as in the decoder
+  ctx->fuse_max_c = ctx->prec == VOC_PREC_BF16X3 ? kFuseDefault : 0;
   auto bail = [&](voc_status st) {
     g_err = ctx->err;
     vocoder_encoder_destroy(enc);
@@ -2785,6 +2786,21 @@ VOC_API voc_status vocoder_encoder_create(const voc_enc_desc *desc, const float 
       // the next unit's Snake1, or (last unit) the Snake in front of the strided conv
       const SnakeCoef next = snake_coef(params[p], C, desc->snake);
       const int tmp = other(cur);
+      Layer R;  // the whole unit in one kernel; the last unit of a block writes the phase-split
+                // input of the strided conv, an epilogue form of the conv kernel only
+      R.name = blk + "r" + std::to_string(j) + ".ru";
+      R.Cin = C, R.Cout = C, R.K = desc->res_kernel, R.dil = enc->dils[j];
+      R.prec = ctx->prec;
+      if (j < nd - 1 && rup(C, 16) <= ctx->fuse_max_c && plan_ru(R, pad, why)) {
+        R.in_buf = cur, R.skip_buf = BUF_FY, R.f32_buf = BUF_FY, R.hl_buf = tmp;
+        if ((st = upload_ru(ctx, ctx->allocs, R, pad, w1, b1, a2, w2, b2, next)) != VOC_OK)
+          return bail(st);
+        enc->layers.push_back(R);
+        enc->div.push_back(div);
+        enc->split.push_back(0);
+        cur = tmp;  // the fused unit reads `cur` with a halo: its output goes to the other buffer
+        continue;
+      }
       Layer L1;
       L1.name = blk + "r" + std::to_string(j) + ".conv1";
       L1.Cin = C, L1.Cout = C, L1.K = desc->res_kernel, L1.dil = enc->dils[j];
