@@ -968,10 +968,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 mma_bf16_warp_lo<PAIR>(d_tmem, a_hi + dA_lo, b_hi, desc_hi, idesc, 1u);
                 accum = 1u;
               }
-            } else {
+            } else {  // A_hi x W_hi and A_hi x W_lo share A through the collector buffer
               for (int ks = 0; ks < nks; ++ks, a_hi += dA_k, b_hi += dB_k) {
-                mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi, desc_hi, idesc, accum);
-                mma_bf16_warp_lo<PAIR>(d_tmem, a_hi, b_hi + dB_lo, desc_hi, idesc, 1u);
+                mma_bf16_warp_lo_col<PAIR, 1>(d_tmem, a_hi, b_hi, desc_hi, idesc, accum);
+                mma_bf16_warp_lo_col<PAIR, 2>(d_tmem, a_hi, b_hi + dB_lo, desc_hi, idesc, 1u);
                 mma_bf16_warp_lo<PAIR>(d_tmem, a_hi + dA_lo, b_hi, desc_hi, idesc, 1u);
                 accum = 1u;
               }

@@ -342,6 +342,33 @@ __device__ __forceinline__ void mma_bf16_warp_lo(uint32_t d_tmem, uint32_t a_lo,
         "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// mma_bf16_warp_lo with a collector-buffer hint for matrix A: COL = 1 (fill) reads A from shared
+// memory and keeps it in the tensor core's collector; COL = 2 (lastuse) takes A from the collector
+// instead of shared memory, then frees it.  The bf16x3 K step issues A_hi x W_hi (fill) and
+// A_hi x W_lo (lastuse) back to back: the second MMA names the same A, so the shared-memory
+// operand traffic drops by one A read per K step.
+template <bool PAIR, int COL>
+__device__ __forceinline__ void mma_bf16_warp_lo_col(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                                     uint32_t desc_hi, uint32_t idesc,
+                                                     uint32_t accumulate) {
+  static_assert(COL == 1 || COL == 2, "fill or lastuse");
+#define VOC_MMA_COL_ASM(GROUP, HINT)                                                         \
+  asm volatile(                                                                              \
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\t"                                    \
+      "mov.b64 da, {%1, %3};\n\t"                                                            \
+      "mov.b64 db, {%2, %3};\n\t"                                                            \
+      "setp.ne.b32 p, %5, 0;\n\t"                                                            \
+      "elect.sync _|e, 0xffffffff;\n\t"                                                      \
+      "@e tcgen05.mma.cta_group::" GROUP ".kind::f16.collector::a::" HINT " [%0], da, db, %4, p;\n\t}\n" :: \
+          "r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)           \
+      : "memory")
+  if (PAIR) {
+    if (COL == 1) VOC_MMA_COL_ASM("2", "fill"); else VOC_MMA_COL_ASM("2", "lastuse");
+  } else {
+    if (COL == 1) VOC_MMA_COL_ASM("1", "fill"); else VOC_MMA_COL_ASM("1", "lastuse");
+  }
+#undef VOC_MMA_COL_ASM
+}
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"

@@ -416,9 +416,9 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         if constexpr (B2) {
           mma_bf16_warp_lo<false>(d, a_hi, b_hi, desc_hi, idesc2, accum);
           mma_bf16_warp_lo<false>(d, a_hi + a_lo, b_hi, desc_hi, idesc, 1u);
-        } else {
-          mma_bf16_warp_lo<false>(d, a_hi, b_hi, desc_hi, idesc, accum);
-          mma_bf16_warp_lo<false>(d, a_hi, b_hi + dB_lo, desc_hi, idesc, 1u);
+        } else {  // A_hi x W_hi and A_hi x W_lo share A through the collector buffer
+          mma_bf16_warp_lo_col<false, 1>(d, a_hi, b_hi, desc_hi, idesc, accum);
+          mma_bf16_warp_lo_col<false, 2>(d, a_hi, b_hi + dB_lo, desc_hi, idesc, 1u);
           mma_bf16_warp_lo<false>(d, a_hi + a_lo, b_hi, desc_hi, idesc, 1u);
         }
         accum = 1u;
