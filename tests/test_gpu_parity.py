@@ -138,6 +138,10 @@ RU_CASES = [
     # B, C, T, dil, padding   (C <= 192: fused kernel; above: conv1 + conv2 kernels)
     (2, 96, 300, 9, W.PAD_SYMMETRIC),
     (1, 96, 257, 1, W.PAD_CAUSAL),
+    (2, 96, 777, 9, W.PAD_SYMMETRIC),   # six 128-row tiles and a ragged one per item
+    (1, 128, 300, 3, W.PAD_CAUSAL),     # the widest B2 form (N = 2 x 128 accumulator columns)
+    (1, 80, 513, 9, W.PAD_SYMMETRIC),   # 5 column chunks over 3 epilogue groups, one row past 4 tiles
+    (2, 112, 40, 1, W.PAD_SYMMETRIC),   # shorter than one tile
     (2, 192, 200, 3, W.PAD_SYMMETRIC),
     (1, 48, 400, 9, W.PAD_CAUSAL),
     (3, 16, 70, 3, W.PAD_SYMMETRIC),
