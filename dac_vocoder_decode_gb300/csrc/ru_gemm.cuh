@@ -30,6 +30,10 @@
 // A_hi x [W_hi | W_lo] into 2N accumulator columns, then A_lo x W_hi into the first N -- and the
 // epilogues add the two column halves.  The arithmetic of each epilogue is the separate conv
 // kernel's, so the fused unit computes the same values as conv1 + conv2 run as two kernels.
+//
+// PREC: the weight form, as in the conv kernel.  The one-plane precisions (f16 or bf16 weights,
+// activations as f16 / bf16 hi/lo pairs) take two MMAs per K step, A_hi x W and A_lo x W, with
+// N columns each, and split their outputs into f16 parts for the F16-weight form.
 #pragma once
 #include "conv_gemm.cuh"
 
@@ -92,7 +96,7 @@ __device__ __forceinline__ void ru_drain1(const ConvGemmArgs &p, int grp, int n_
 
 // Epilogue 1, second part: Snake2(h + b1) split into bf16 hi/lo, in place: chunk j's 16
 // values become [hi 0..7 | lo 0..7 | hi 8..15 | lo 8..15] as packed pairs (4 words each).
-template <int MC>
+template <int MC, bool F16 = false>
 __device__ __forceinline__ void ru_act1(const RuExtra &x, int grp, int n_chunks,
                                         uint32_t (&dr)[MC][16]) {
 #pragma unroll
@@ -110,7 +114,7 @@ __device__ __forceinline__ void ru_act1(const RuExtra &x, int grp, int n_chunks,
         for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(dr[j][h + i]) + bb[i];
         snake_n<8>(v, a, ib, sn);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) split_pair<false>(sn[2 * i], sn[2 * i + 1], dr[j][h + i], dr[j][h + 4 + i]);
+        for (int i = 0; i < 4; ++i) split_pair<F16>(sn[2 * i], sn[2 * i + 1], dr[j][h + i], dr[j][h + 4 + i]);
       }
     }
   }
@@ -174,7 +178,7 @@ __device__ __forceinline__ void ru_prefetch_skip_l1(const ConvGemmArgs &p, const
 // residual x (sk, loaded by the caller from global memory), Snake of the next layer, hi/lo
 // split and stores -- the conv kernel's epilogue of a 1x1 conv with a residual input.  HEAD:
 // the output head's partial products of this row instead of stores (see epilogue_chunk).
-template <bool B2, bool HEAD>
+template <bool B2, bool HEAD, bool F16 = false>
 __device__ __forceinline__ bool ru_epilogue2(const ConvGemmArgs &p, volatile int *abort_flag,
                                              int b, int t, int n0, uint32_t taddr,
                                              const float (&sk)[16], float (&hp)[kHeadFoldMaxK]) {
@@ -234,7 +238,7 @@ __device__ __forceinline__ bool ru_epilogue2(const ConvGemmArgs &p, volatile int
   if (p.out_hl) {
     uint32_t hw[8], lw[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) split_pair<false>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
+    for (int i = 0; i < 8; ++i) split_pair<F16>(sn[2 * i], sn[2 * i + 1], hw[i], lw[i]);
     const size_t L_out = static_cast<size_t>(p.hl_L);
     const size_t row = static_cast<size_t>(t) + p.hl_row0;
     const size_t item = (size_t)b * (2 * p.Cp_out / 8);
@@ -255,7 +259,7 @@ __device__ __forceinline__ bool ru_epilogue2(const ConvGemmArgs &p, volatile int
 
 // RES: resident weights (ConvGemmArgs::b_resident; the narrow units): every weight stage of both
 // convolutions has a slot of its own, filled once by the first tile and kept.
-template <bool B2, bool HEAD = false, bool RES = false>
+template <bool B2, bool HEAD = false, bool RES = false, int PREC = kPrecBf16x3>
 __global__ void __launch_bounds__(kRuThreads, 1)
     ru_gemm_kernel(const __grid_constant__ CUtensorMap tmapA, const ConvGemmArgs p,
                    const RuExtra x) {
@@ -386,7 +390,10 @@ __global__ void __launch_bounds__(kRuThreads, 1)
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.timeout, abort_flag));
     };
-    const uint32_t idesc = idesc_bf16_f32(kTileM, p.N_tile);
+    constexpr bool F16 = PREC == kPrecF16w;   // f16 operands (else bf16)
+    constexpr bool ONE = PREC != kPrecBf16x3;  // one weight plane: A_hi x W + A_lo x W
+    static_assert(!(ONE && (B2 || RES)), "the one-plane forms stream their weights, three-MMA layout");
+    const uint32_t idesc = F16 ? idesc_f16_f32(kTileM, p.N_tile) : idesc_bf16_f32(kTileM, p.N_tile);
     const uint32_t idesc2 = idesc_bf16_f32(kTileM, 2 * p.N_tile);  // B2: [W_hi | W_lo]
     // B2: each chunk of a weight stage holds its N hi rows, then its N lo rows
     const uint32_t chunkB_stride = B2 ? 2 * chunkB : chunkB;
@@ -413,7 +420,10 @@ __global__ void __launch_bounds__(kRuThreads, 1)
     auto ksteps = [&](uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t a_k, uint32_t b_hi,
                       uint32_t accum) {
       for (int ks = 0; ks < nks; ++ks, a_hi += a_k, b_hi += dB_k) {
-        if constexpr (B2) {
+        if constexpr (ONE) {
+          mma_bf16_warp_lo<false>(d, a_hi, b_hi, desc_hi, idesc, accum);
+          mma_bf16_warp_lo<false>(d, a_hi + a_lo, b_hi, desc_hi, idesc, 1u);
+        } else if constexpr (B2) {
           mma_bf16_warp_lo<false>(d, a_hi, b_hi, desc_hi, idesc2, accum);
           mma_bf16_warp_lo<false>(d, a_hi + a_lo, b_hi, desc_hi, idesc, 1u);
         } else {  // A_hi x W_hi and A_hi x W_lo share A through the collector buffer
@@ -608,7 +618,7 @@ __global__ void __launch_bounds__(kRuThreads, 1)
         ru_drain1<B2, MC>(p, grp, n_chunks, t1, dr);
         tc_fence_before();
         mbar_arrive(smem_u32(acc1Empty));
-        ru_act1<MC>(x, grp, n_chunks, dr);
+        ru_act1<MC, PREC == kPrecF16w>(x, grp, n_chunks, dr);
         // H is free once conv2 has read the previous fill
         const int g = it * x.h_parts;  // H fill number (fill -1 counts as complete)
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(hEmpty), static_cast<uint32_t>(g - 1) & 1u,
@@ -642,7 +652,8 @@ __global__ void __launch_bounds__(kRuThreads, 1)
           if (c + kEpiGroups < n_chunks) ru_load_skip(p, x, b, t, 16 * (c + kEpiGroups), skn);
           // and the chunk after it into L1 (into L2 every chunk came one tile earlier)
           if (c + 2 * kEpiGroups < n_chunks) ru_prefetch_skip_l1(p, x, b, t, 16 * (c + 2 * kEpiGroups));
-          ok = ru_epilogue2<B2, HEAD>(p, abort_flag, b, t, 16 * c, t2 + static_cast<uint32_t>(16 * c), sk, hp);
+          ok = ru_epilogue2<B2, HEAD, PREC == kPrecF16w>(p, abort_flag, b, t, 16 * c,
+                                                        t2 + static_cast<uint32_t>(16 * c), sk, hp);
           ok = __all_sync(0xffffffffu, ok);
           if constexpr (HEAD) {
             if (ok) ok = head_fold_store(p, hp, b, (mt * kTileM) / 32 + quad, c, lane, abort_flag);

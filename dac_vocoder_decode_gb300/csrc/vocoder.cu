@@ -202,6 +202,10 @@ bool set_kernel_attrs(std::string &why) {
     if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<true, true>);
     if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<true, false, true>);
     if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<true, true, true>);
+    if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<false, false, false, voc::kPrecF16w>);
+    if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<false, true, false, voc::kPrecF16w>);
+    if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<false, false, false, voc::kPrecBf16w>);
+    if (st == cudaSuccess) st = set_ru(voc::ru_gemm_kernel<false, true, false, voc::kPrecBf16w>);
     if (st == cudaSuccess) {
       auto regs_ok = [](auto kernel) {
         cudaFuncAttributes fa{};
@@ -214,7 +218,11 @@ bool set_kernel_attrs(std::string &why) {
                      regs_ok(voc::ru_gemm_kernel<false, true>) &&
                      regs_ok(voc::ru_gemm_kernel<true, true>) &&
                      regs_ok(voc::ru_gemm_kernel<true, false, true>) &&
-                     regs_ok(voc::ru_gemm_kernel<true, true, true>);
+                     regs_ok(voc::ru_gemm_kernel<true, true, true>) &&
+                     regs_ok(voc::ru_gemm_kernel<false, false, false, voc::kPrecF16w>) &&
+                     regs_ok(voc::ru_gemm_kernel<false, true, false, voc::kPrecF16w>) &&
+                     regs_ok(voc::ru_gemm_kernel<false, false, false, voc::kPrecBf16w>) &&
+                     regs_ok(voc::ru_gemm_kernel<false, true, false, voc::kPrecBf16w>);
     }
     if (st == cudaSuccess)
       st = cudaFuncSetAttribute(voc::out_head_kernel<kHeadTile>,
@@ -240,6 +248,7 @@ struct vocoder {
   int *flag_dev = nullptr;  // finite-check flag
   long long wait_budget = kWaitBudget;
   int fuse_max_c = 0;       // residual units of up to this many (padded) channels run fused
+  int fuse_min_c = 0;       // ... and of at least this many
   bool use_pair = true;     // conv layers on CTA pairs
   int prec = VOC_PREC_BF16X3;  // VOC_PREC_*: the weight form of every conv
   // TMA descriptors of the two most recent (workspace, B, T) of a decode, each set sized for
@@ -506,6 +515,8 @@ bool plan_layer(bool pair, Layer &L, int padding, bool has_skip, std::string &wh
 constexpr int kRuMaxC = 192;
 // Residual units of up to this many (padded) channels run as one kernel by default.
 constexpr int kFuseDefault = kRuMaxC;
+// Smallest unit width fused by default with the one-plane precisions (F16W, BF16W).
+constexpr int kRuOnePlaneMinC = 129;
 // Units of at least this many channels keep half of the H tile at a time.
 constexpr int kRuHalfHMinC = 160;
 bool plan_ru(Layer &L, int padding, std::string &why) {
@@ -536,8 +547,10 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
     why = "tap span too wide for one staged tile";
     return false;
   }
-  // B2 form (two MMAs per K step) when the doubled column count fits one MMA
-  g.b2 = (2 * g.N_tile <= 256) ? 1 : 0;
+  // B2 form (two MMAs per K step) when the doubled column count fits one MMA (bf16x3; the
+  // one-plane precisions take two MMAs per K step of N columns)
+  g.b2 = (L.prec == VOC_PREC_BF16X3 && 2 * g.N_tile <= 256) ? 1 : 0;
+  const int wb = L.prec != VOC_PREC_BF16X3 ? 2 : 4;  // weight bytes per (channel, column)
   L.cw = 16;
   // The widest units keep half of H at a time (conv2 runs in two K halves): the shared memory
   // this frees goes to the weight ring, which conv1's 7 taps x C^2 weights per tile stream
@@ -557,7 +570,7 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
   for (int kb = L.Cp_in / L.rx.h_parts; kb >= 16 && !g.KB && g.b2; kb -= 16) {
     if ((L.Cp_in / L.rx.h_parts) % kb || 4 * kb * g.rows > 72 * 1024) continue;
     const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
-    const int b_bytes = 4 * kb * g.N_tile;
+    const int b_bytes = wb * kb * g.N_tile;
     const int nb = (g.taps + 1) * (L.Cp_in / kb);
     if (2 * a_bytes + nb * b_bytes > avail || (4 + 2 * nb + 7) * 8 + 8 > kBarrierBytes) continue;
     g.KB = kb, g.a_bytes = a_bytes, g.b_bytes = b_bytes, g.na = 2, g.nb = nb;
@@ -568,11 +581,11 @@ bool plan_ru(Layer &L, int padding, std::string &why) {
   // else two.
   for (int min_nb = 3; min_nb >= 2 && !g.KB; --min_nb)
     for (int kb = L.Cp_in; kb >= 16 && !g.KB; kb -= 16) {
-      if ((L.Cp_in / L.rx.h_parts) % kb || 4 * kb * g.N_tile > kBStageMax ||
+      if ((L.Cp_in / L.rx.h_parts) % kb || wb * kb * g.N_tile > kBStageMax ||
           4 * kb * g.rows > 72 * 1024)
         continue;
       const int a_bytes = rup(2 * (kb / 8) * chunkA, 1024);
-      const int b_bytes = 4 * kb * g.N_tile;
+      const int b_bytes = wb * kb * g.N_tile;
       const int na = 2;
       const int nb = std::min(8, (avail - na * a_bytes) / b_bytes);
       if (nb < min_nb) continue;
@@ -1061,7 +1074,15 @@ voc_status launch_gemm(vocoder *ctx, const Layer &L, const CUtensorMap &map,
     rx.skip_L = static_cast<int>(skip_L >= 0 ? skip_L : a.f32_L);
     rx.skip_elems = skip_elems >= 0 ? skip_elems : a.f32_elems;
     const dim3 g(grid), blk(voc::kRuThreads);
-    if (L.g.b_resident)  // (resident plans are narrow: B2 form)
+    if (L.prec == VOC_PREC_F16W)  // one weight plane: three-MMA layout, streamed weights
+      e = a.head_part
+              ? launch_pdl(voc::ru_gemm_kernel<false, true, false, voc::kPrecF16w>, g, blk, L.smem, stream, map, a, rx)
+              : launch_pdl(voc::ru_gemm_kernel<false, false, false, voc::kPrecF16w>, g, blk, L.smem, stream, map, a, rx);
+    else if (L.prec == VOC_PREC_BF16W)
+      e = a.head_part
+              ? launch_pdl(voc::ru_gemm_kernel<false, true, false, voc::kPrecBf16w>, g, blk, L.smem, stream, map, a, rx)
+              : launch_pdl(voc::ru_gemm_kernel<false, false, false, voc::kPrecBf16w>, g, blk, L.smem, stream, map, a, rx);
+    else if (L.g.b_resident)  // (resident plans are narrow: B2 form)
       e = a.head_part
               ? launch_pdl(voc::ru_gemm_kernel<true, true, true>, g, blk, L.smem, stream, map, a, rx)
               : launch_pdl(voc::ru_gemm_kernel<true, false, true>, g, blk, L.smem, stream, map, a, rx);
@@ -1285,7 +1306,10 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
                     : (desc->fuse_max_channels < 0 ? 0 : desc->fuse_max_channels);
   ctx->use_pair = desc->cta_pair > 0;
   ctx->prec = desc->precision;
-  if (ctx->prec != VOC_PREC_BF16X3) ctx->fuse_max_c = 0;  // the fused unit is bf16x3 only
+  // The one-plane precisions fuse by default only the units wider than kRuOnePlaneMinC (their
+  // narrower fused units ran slower than conv1 + conv2: C = 96 0.41 vs 0.36 ms, C = 48 1.04 vs
+  // 1.02 ms; C = 192 0.37 vs 0.40 ms).  An explicit fuse_max_channels fuses every unit up to it.
+  if (ctx->prec != VOC_PREC_BF16X3 && desc->fuse_max_channels == 0) ctx->fuse_min_c = kRuOnePlaneMinC;
   auto bail = [&](voc_status st) {
     g_err = ctx->err;
     vocoder_destroy(ctx);
@@ -1388,9 +1412,10 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
       const bool last_stage = (i == desc->n_stages - 1);
       Layer R;  // the whole unit in one kernel when it fits and is enabled
       R.name = "s" + std::to_string(i) + "r" + std::to_string(j) + ".ru";
+      R.prec = ctx->prec;
       R.Cin = C, R.Cout = C, R.K = desc->res_kernel, R.dil = ctx->dils[j];
       R.level = i + 1;
-      if (rup(C, 16) <= ctx->fuse_max_c && plan_ru(R, pad, why)) {
+      if (rup(C, 16) <= ctx->fuse_max_c && rup(C, 16) >= ctx->fuse_min_c && plan_ru(R, pad, why)) {
         const int out = other(cur, -1);  // never the buffer this unit reads
         R.in_buf = cur, R.skip_buf = BUF_FY;
         if (j < nd - 1) {
@@ -2713,8 +2738,10 @@ VOC_API voc_status vocoder_encoder_create(const voc_enc_desc *desc, const float 
   enc->Cp_lat = rup(desc->latent_channels, 16);
   ctx->prec = desc->precision;
   ctx->use_pair = false;
-  // residual units before a block's last one run as one fused kernel (bf16x3), as in the decoder
-  ctx->fuse_max_c = ctx->prec == VOC_PREC_BF16X3 ? kFuseDefault : 0;
+  // residual units before a block's last one run as one fused kernel, as in the decoder (the
+  // decoder's default: with the one-plane precisions the units wider than kRuOnePlaneMinC)
+  ctx->fuse_max_c = kFuseDefault;
+  if (ctx->prec != VOC_PREC_BF16X3) ctx->fuse_min_c = kRuOnePlaneMinC;
   auto bail = [&](voc_status st) {
     g_err = ctx->err;
     vocoder_encoder_destroy(enc);
@@ -2791,7 +2818,8 @@ VOC_API voc_status vocoder_encoder_create(const voc_enc_desc *desc, const float 
       R.name = blk + "r" + std::to_string(j) + ".ru";
       R.Cin = C, R.Cout = C, R.K = desc->res_kernel, R.dil = enc->dils[j];
       R.prec = ctx->prec;
-      if (j < nd - 1 && rup(C, 16) <= ctx->fuse_max_c && plan_ru(R, pad, why)) {
+      if (j < nd - 1 && rup(C, 16) <= ctx->fuse_max_c && rup(C, 16) >= ctx->fuse_min_c &&
+          plan_ru(R, pad, why)) {
         R.in_buf = cur, R.skip_buf = BUF_FY, R.f32_buf = BUF_FY, R.hl_buf = tmp;
         if ((st = upload_ru(ctx, ctx->allocs, R, pad, w1, b1, a2, w2, b2, next)) != VOC_OK)
           return bail(st);

@@ -104,12 +104,14 @@ typedef struct {
   int out_kernel;       /* conv_out taps (odd; 7)                            */
   int out_channels;     /* 1                                                 */
   int padding;          /* VOC_PAD_SYMMETRIC | VOC_PAD_CAUSAL                */
-  int precision;        /* VOC_PREC_BF16X3 | VOC_PREC_F16W                   */
+  int precision;        /* VOC_PREC_BF16X3 | VOC_PREC_F16W | VOC_PREC_BF16W  */
   int fuse_max_channels;/* residual units of up to this many channels (at most 192)
                            run as one kernel (conv1 result kept on chip); 0 = library
-                           default (192: every unit that fits), -1 = never.  A
-                           performance choice only: results agree within the decode
-                           tolerance either way.                                 */
+                           default (192: every unit that fits; with VOC_PREC_F16W or
+                           VOC_PREC_BF16W only the units wider than 128 channels,
+                           the narrower ones being faster as two kernels there),
+                           -1 = never.  A performance choice only: results agree
+                           within the decode tolerance either way.               */
   int cta_pair;         /* conv layers run on CTA pairs (2-CTA clusters sharing one
                            256-row MMA, each SM staging half of the weights):
                            0 = library default (off), 1 = on, -1 = off.  A

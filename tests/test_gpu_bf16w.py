@@ -44,6 +44,18 @@ def test_bf16w_matches_bf16_weight_oracle(arch):
     assert snr_db(full, got) >= 30.0
 
 
+@pytest.mark.parametrize("arch", [MID_MUSIC, MID_SPEECH], ids=["music", "speech_causal"])
+def test_bf16w_every_unit_fused_matches_the_oracle(arch):
+    """fuse_max_channels=192: the units of at most 128 channels, which this precision runs as
+    two kernels by default, in the fused kernel's one-plane form."""
+    wl = W.make_custom(arch, B=2, T=23, seed=405)
+    voc = V.Vocoder(arch, V.fold_params(wl.params), fuse_max_channels=192,
+                    precision=V.VOC_PREC_BF16W)
+    got = G.gpu_decode(voc, wl.latent)
+    ref = O.decode(arch, None, wl.latent, 0, O.fold_params(wl.params, bf16_weights=True))
+    G.compare_audio(ref, got, "bf16w, every unit fused, vs bf16-weight oracle")
+
+
 def test_bf16w_music_window_sampled():
     """The full-size one-window music decode, on sampled windows."""
     wl = G.workload("music_window")

@@ -45,6 +45,19 @@ def test_f16w_matches_f16_weight_oracle(arch):
     assert snr_db(full, got) >= 40.0
 
 
+@pytest.mark.parametrize("arch", [MID_MUSIC, MID_SPEECH], ids=["music", "speech_causal"])
+def test_f16w_every_unit_fused_matches_the_oracle(arch):
+    """fuse_max_channels=192: the units of at most 128 channels, which this precision runs as
+    two kernels by default, in the fused kernel's one-plane form."""
+    wl = W.make_custom(arch, B=2, T=23, seed=405)
+    voc = V.Vocoder(arch, V.fold_params(wl.params), fuse_max_channels=192,
+                    precision=V.VOC_PREC_F16W)
+    got = G.gpu_decode(voc, wl.latent)
+    ref = O.decode(arch, None, wl.latent, 0, O.fold_params(wl.params, f16_weights=True))
+    G.compare_audio(ref, got, "f16w, every unit fused, vs f16-weight oracle")
+    assert snr_db(ref, got) >= 80.0
+
+
 def test_f16w_music_window_sampled():
     """The full-size one-window music decode, on sampled windows."""
     wl = G.workload("music_window")
