@@ -1324,7 +1324,7 @@ VOC_API voc_status vocoder_create(const voc_desc *desc, const float *const *para
   cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, ctx->device);
   cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
   if (cc_major != 10 || cc_minor != 3)
-    return bail(fail(ctx, VOC_UNSUPPORTED, "this build targets sm_103 (GB300) only"));
+    return bail(fail(ctx, VOC_UNSUPPORTED, "the library is compiled for sm_103 (GB300) only"));
   e = dev_alloc(reinterpret_cast<void **>(&ctx->err_dev), 8 * sizeof(int));  // [0] error word, [1] finite flag, [4..7] checks
   if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaMalloc"));
   ctx->allocs.push_back(ctx->err_dev);
@@ -1831,7 +1831,7 @@ voc_status op_layer(Layer &L, int padding, const float *x_dev, int B, int T, con
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3) return fail(nullptr, VOC_UNSUPPORTED, "this build targets sm_103 only");
+  if (major != 10 || minor != 3) return fail(nullptr, VOC_UNSUPPORTED, "the library is compiled for sm_103 (GB300) only");
   vocoder tmp;  // carries the allocations, the error word and the launch settings
   tmp.num_sms = sms;
   tmp.device = dev;
@@ -1940,7 +1940,7 @@ VOC_API voc_status vocoder_op_residual_unit(const float *x_dev, int B, int C, in
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3) return fail(nullptr, VOC_UNSUPPORTED, "this build targets sm_103 only");
+  if (major != 10 || minor != 3) return fail(nullptr, VOC_UNSUPPORTED, "the library is compiled for sm_103 (GB300) only");
   vocoder tmp;
   tmp.num_sms = sms;
   tmp.device = dev;
@@ -2520,7 +2520,7 @@ voc_status init_device(vocoder *ctx) {
   cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, ctx->device);
   cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, ctx->device);
   if (cc_major != 10 || cc_minor != 3)
-    return fail(ctx, VOC_UNSUPPORTED, "this build targets sm_103 (GB300) only");
+    return fail(ctx, VOC_UNSUPPORTED, "the library is compiled for sm_103 (GB300) only");
   e = dev_alloc(reinterpret_cast<void **>(&ctx->err_dev), 8 * sizeof(int));  // [0] error word, [1] finite flag, [4..7] checks
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMalloc");
   ctx->allocs.push_back(ctx->err_dev);

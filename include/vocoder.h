@@ -54,7 +54,7 @@ typedef struct CUstream_st *voc_stream_t;     /* a cudaStream_t */
 typedef enum {
   VOC_OK = 0,
   VOC_INVALID_ARG = -1,         /* a pointer, size or description is invalid       */
-  VOC_UNSUPPORTED = -2,         /* valid in principle, not supported by this build  */
+  VOC_UNSUPPORTED = -2,         /* valid in principle, not supported by the library  */
   VOC_CUDA_ERROR = -3,          /* a CUDA runtime call or a kernel launch failed    */
   VOC_OOM = -4,                 /* device or host allocation failed                 */
   VOC_WORKSPACE_TOO_SMALL = -5, /* ws_bytes below vocoder_workspace_bytes()         */
