@@ -144,3 +144,13 @@ def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
     s = bench.ClockSampler(0)
     s.start()
     assert s.stop() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+
+
+def test_tensor_peak_takes_the_sustained_figure_for_long_power_capped_runs():
+    peaks = {"bf16_tflops": 1978.8, "bf16_tflops_sustained": 1739.1}
+    assert bench.tensor_peak(peaks, 3.0, 4.2, ["sw_power_cap"]) == (1739.1 / 3.0, "sustained")
+    # a short run, or one without the power cap, is held to the burst rate
+    assert bench.tensor_peak(peaks, 3.0, 0.2, ["sw_power_cap"]) == (1978.8 / 3.0, "burst")
+    assert bench.tensor_peak(peaks, 2.0, 4.2, []) == (1978.8 / 2.0, "burst")
+    # without a measured sustained figure the fallback's
+    assert bench.tensor_peak({}, 3.0, 4.2, ["sw_power_cap"])[0] == bench.FALLBACK_PEAKS["bf16_tflops_sustained"] / 3.0
