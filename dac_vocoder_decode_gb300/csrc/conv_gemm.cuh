@@ -415,69 +415,48 @@ __device__ __forceinline__ bool epilogue_chunk(const ConvGemmArgs &p, uint32_t s
   VOC_CHECK((taddr & 0xFFFFu) + CW + (p.b2 ? p.N_tile : 0) <= (uint32_t)(p.n_acc * p.acc_cols), 11,
             taddr & 0xFFFF, CW, p.b2);
   VOC_CHECK(n0 + CW <= p.N_total, 12, n0, p.N_total, 0);
+  static_assert(CW == 16, "16-column epilogue chunks");
   float v[CW];
-  if constexpr (CW <= 16) {
-    // Issue the independent loads first: the bias (L1-resident), the TMEM read and, once
-    // its slot has landed, the residual tile; then wait for the TMEM data.
-    float bb[CW];
-    ldg_vec(p.bias + n0, bb);
-    uint32_t r[CW], r2[CW];
-    tmem_ld_issue<CW>(taddr, r);
-    if constexpr (B2) tmem_ld_issue<CW>(taddr + static_cast<uint32_t>(p.N_tile), r2);
-    if (p.skip) {
-      VOC_CHECK(sslot >= smem_lo && sslot + skip_slot_bytes(CW) <= smem_hi, 13, sslot, smem_lo, smem_hi);
-      const bool landed = mbar_wait(sfull, sparity, p.timeout, abort_flag);
-      uint4 sk[CW / 4];
-      if (landed) {
+  // Issue the independent loads first: the bias (L1-resident), the TMEM read and, once
+  // its slot has landed, the residual tile; then wait for the TMEM data.
+  float bb[CW];
+  ldg_vec(p.bias + n0, bb);
+  uint32_t r[CW], r2[CW];
+  tmem_ld_issue<CW>(taddr, r);
+  if constexpr (B2) tmem_ld_issue<CW>(taddr + static_cast<uint32_t>(p.N_tile), r2);
+  if (p.skip) {
+    VOC_CHECK(sslot >= smem_lo && sslot + skip_slot_bytes(CW) <= smem_hi, 13, sslot, smem_lo, smem_hi);
+    const bool landed = mbar_wait(sfull, sparity, p.timeout, abort_flag);
+    uint4 sk[CW / 4];
+    if (landed) {
 #pragma unroll
-        for (int j = 0; j < CW / 4; ++j)
-          sk[j] = lds128(sslot + static_cast<uint32_t>((j * kTileM + row_in_tile) * 16));
-        mbar_arrive(sempty);
-      }
-      tmem_ld_wait<CW>(r);  // the TMEM reads complete before any return
-      if constexpr (B2) {
-        tmem_ld16_after_wait(r2);
-#pragma unroll
-        for (int i = 0; i < CW; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
-      }
-      if (!landed) return false;
-#pragma unroll
-      for (int j = 0; j < CW / 4; ++j) {  // (acc + bias) + skip
-        v[4 * j] = (__uint_as_float(r[4 * j]) + bb[4 * j]) + __uint_as_float(sk[j].x);
-        v[4 * j + 1] = (__uint_as_float(r[4 * j + 1]) + bb[4 * j + 1]) + __uint_as_float(sk[j].y);
-        v[4 * j + 2] = (__uint_as_float(r[4 * j + 2]) + bb[4 * j + 2]) + __uint_as_float(sk[j].z);
-        v[4 * j + 3] = (__uint_as_float(r[4 * j + 3]) + bb[4 * j + 3]) + __uint_as_float(sk[j].w);
-      }
-    } else {
-      tmem_ld_wait<CW>(r);
-      if constexpr (B2) {
-        tmem_ld16_after_wait(r2);
-#pragma unroll
-        for (int i = 0; i < CW; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
-      }
-#pragma unroll
-      for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]) + bb[i];
-    }
-  } else {
-    // wider chunks (the fused unit's 32 columns): in order, within the register budget
-    tmem_ld(taddr, v);
-    {
-      float bb[CW];
-      ldg_vec(p.bias + n0, bb);
-#pragma unroll
-      for (int i = 0; i < CW; ++i) v[i] += bb[i];
-    }
-    if (p.skip) {
-      VOC_CHECK(sslot >= smem_lo && sslot + skip_slot_bytes(CW) <= smem_hi, 13, sslot, smem_lo, smem_hi);
-      if (!mbar_wait(sfull, sparity, p.timeout, abort_flag)) return false;
-#pragma unroll
-      for (int j = 0; j < CW / 4; ++j) {
-        const uint4 x = lds128(sslot + static_cast<uint32_t>((j * kTileM + row_in_tile) * 16));
-        v[4 * j] += __uint_as_float(x.x), v[4 * j + 1] += __uint_as_float(x.y);
-        v[4 * j + 2] += __uint_as_float(x.z), v[4 * j + 3] += __uint_as_float(x.w);
-      }
+      for (int j = 0; j < CW / 4; ++j)
+        sk[j] = lds128(sslot + static_cast<uint32_t>((j * kTileM + row_in_tile) * 16));
       mbar_arrive(sempty);
     }
+    tmem_ld_wait<CW>(r);  // the TMEM reads complete before any return
+    if constexpr (B2) {
+      tmem_ld16_after_wait(r2);
+#pragma unroll
+      for (int i = 0; i < CW; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+    }
+    if (!landed) return false;
+#pragma unroll
+    for (int j = 0; j < CW / 4; ++j) {  // (acc + bias) + skip
+      v[4 * j] = (__uint_as_float(r[4 * j]) + bb[4 * j]) + __uint_as_float(sk[j].x);
+      v[4 * j + 1] = (__uint_as_float(r[4 * j + 1]) + bb[4 * j + 1]) + __uint_as_float(sk[j].y);
+      v[4 * j + 2] = (__uint_as_float(r[4 * j + 2]) + bb[4 * j + 2]) + __uint_as_float(sk[j].z);
+      v[4 * j + 3] = (__uint_as_float(r[4 * j + 3]) + bb[4 * j + 3]) + __uint_as_float(sk[j].w);
+    }
+  } else {
+    tmem_ld_wait<CW>(r);
+    if constexpr (B2) {
+      tmem_ld16_after_wait(r2);
+#pragma unroll
+      for (int i = 0; i < CW; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]) + bb[i];
   }
   float sn[CW];
   if (p.alpha) {

@@ -128,15 +128,6 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
-// 3-D tiled tensor load into shared memory, completion counted on `bar`.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint32_t bar, int x,
-                                            int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(tmap), "r"(bar), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
 // 4-D tiled tensor load into shared memory, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, uint32_t bar, int x,
                                             int y, int z, int w) {
@@ -247,74 +238,12 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
          | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive once on `bar` when every tcgen05 operation issued so far by this thread is done.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// Pair MMA, issued by one thread of the even CTA: M = 256 rows, rows 0..127 from the
-// A operand in the even CTA's shared memory and rows 128..255 from the odd CTA's (same
-// descriptor, each CTA's own shared memory); the N columns of B are split in halves, the
-// even CTA holding columns 0..N/2-1.  Each CTA's TMEM receives its 128 rows x N columns.
-__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive once on the mbarrier at shared::cta offset `bar` in every CTA of `cta_mask` when
-// the pair MMAs issued so far by this thread are done.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
-}
-
-// Warp-wide forms: the whole warp executes the call with identical operands and one
+// Warp-wide MMA issue: the whole warp executes the call with identical operands and one
 // elected lane issues the instruction.  Keeping the issuing loop convergent lets the
 // descriptors stay in uniform registers; issued from a single divergent lane, every MMA
-// first pays for moving its operands into them, which starves the tensor pipe.
-__device__ __forceinline__ void mma_bf16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_bf16_pair_warp(uint32_t d_tmem, uint64_t adesc,
-                                                   uint64_t bdesc, uint32_t idesc,
-                                                   uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// As mma_bf16_warp / mma_bf16_pair_warp with the two shared-memory descriptors given as
-// their low words and one common high word (stride field and version bit, equal for A
-// and B).  The start-address field (bits 0..13) of a shared-memory descriptor never
+// first pays for moving its operands into them, which starves the tensor pipe.  The two
+// shared-memory descriptors are given as their low words and one common high word (stride
+// field and version bit, equal for A and B).  The start-address field (bits 0..13) of a shared-memory descriptor never
 // carries into the leading-byte-offset field for offsets inside the 227 KB window, so
 // the low words can be stepped with 32-bit adds.
 template <bool PAIR>
@@ -369,6 +298,9 @@ __device__ __forceinline__ void mma_bf16_warp_lo_col(uint32_t d_tmem, uint32_t a
   }
 #undef VOC_MMA_COL_ASM
 }
+// Warp-wide commits (one elected lane): arrive once on `bar` when every tcgen05 operation this
+// thread issued so far is done; the pair form arrives on the barrier at the same shared::cta
+// offset in every CTA of `cta_mask`.
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -387,46 +319,9 @@ __device__ __forceinline__ void mma_commit_pair_warp(uint32_t bar, uint16_t cta_
       : "memory");
 }
 
-// 32 lanes x 16 consecutive 32-bit columns; thread i of the warp gets lane
-// (warp quadrant base + i).  Load and wait in one asm block so that no use of
-// the registers can be scheduled before the data has arrived.  No memory clobber:
-// the load touches no memory the compiler tracks, and the compiler may then issue
-// independent global or shared loads ahead of it; as a volatile asm it keeps its
-// place among the barrier and fence instructions.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 32 lanes x 32 consecutive 32-bit columns (see tmem_ld16).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// tcgen05.ld of 32 lanes x 16 columns without the wait: the registers hold the data only
-// after tmem_ld_wait on the same array, which lets independent loads overlap the TMEM read.
+// tcgen05.ld of 32 lanes x 16 consecutive 32-bit columns (thread i of the warp gets lane
+// warp quadrant base + i) without the wait: the registers hold the data only after
+// tmem_ld_wait on the same array, which lets independent loads overlap the TMEM read.
 __device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -483,9 +378,6 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[N]) {
   for (int h = 1; h < N / 16; ++h)
     tmem_ld16_after_wait(*reinterpret_cast<uint32_t(*)[16]>(&r[16 * h]));
 }
-
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[16]) { tmem_ld16(taddr, v); }
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[32]) { tmem_ld32(taddr, v); }
 
 // 32-byte global store (st.global.v8.b32): the address must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t (&w)[8]) {

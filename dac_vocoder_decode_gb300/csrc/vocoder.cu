@@ -123,7 +123,7 @@ struct Layer {
   float *bias_dev = nullptr, *alpha_dev = nullptr, *invb_dev = nullptr;
   int in_buf = -1, f32_buf = -1, hl_buf = -1, skip_buf = -1;
   int epi_flags = 0;
-  int cw = 16;              // epilogue column chunk (conv kernel: 16; fused unit: 16 or 32)
+  int cw = 16;              // epilogue column chunk (16 columns in both kernels)
   bool pair = false;        // CTA-pair kernel: 256-row tiles, half of each weight tile per CTA
   int max_clusters = 0;     // pair: co-resident 2-CTA clusters of this launch shape
   // the encoder's conv_in on a few audio channels, run directly in fp32 (audio_conv_in_kernel,
