@@ -13,20 +13,20 @@ namespace voc {
 
 template <bool F16>
 __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &h, uint32_t &l) {
+  // one packed conversion per part (cvt.rn.{f16,bf16}x2.f32: x0 in the low half), the same
+  // round-to-nearest-even values as converting each element on its own
   if constexpr (F16) {
-    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-    const __half l0 = __float2half_rn(x0 - __half2float(h0));
-    const __half l1 = __float2half_rn(x1 - __half2float(h1));
-    h = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-    l = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
+    const __half2 hh = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(hh);
+    const __half2 ll = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    h = *reinterpret_cast<const uint32_t *>(&hh);
+    l = *reinterpret_cast<const uint32_t *>(&ll);
   } else {
-    const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-    const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
-    const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
-    h = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
-        (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
-    l = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
-        (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+    const __nv_bfloat162 hh = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(hh);
+    const __nv_bfloat162 ll = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    h = *reinterpret_cast<const uint32_t *>(&hh);
+    l = *reinterpret_cast<const uint32_t *>(&ll);
   }
 }
 

@@ -45,14 +45,14 @@ __device__ __forceinline__ float snake(float v, float a, float inv_b) {
 template <int N>
 __device__ __forceinline__ void snake_n(const float (&v)[N], const float (&a)[N],
                                         const float (&inv_b)[N], float (&out)[N]) {
-  bool wide = false;
+  float amax = 0.f;  // the largest |a v| of the N (one max per value instead of a compare and an or)
 #pragma unroll
   for (int i = 0; i < N; ++i) {
     const float ax = a[i] * v[i];
-    wide |= fabsf(ax) > 8192.f;
+    amax = fmaxf(amax, fabsf(ax));
     out[i] = fmaf(inv_b[i], sin2_fast(ax), v[i]);
   }
-  if (wide) {  // unrolled too: a run-time index would put the arrays in local memory
+  if (!(amax <= 8192.f)) {  // unrolled too: a run-time index would put the arrays in local memory
 #pragma unroll
     for (int i = 0; i < N; ++i) {
       const float ax = a[i] * v[i];
