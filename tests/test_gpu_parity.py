@@ -101,6 +101,7 @@ def test_snake_accuracy_wide_range():
 CONVT_CASES = [
     # B, Cin, Cout, T, stride, padding
     (2, 192, 96, 300, 2, W.PAD_SYMMETRIC),
+    (1, 320, 160, 77, 2, W.PAD_SYMMETRIC),        # two column tiles, each with phase halves of 80
     (1, 384, 192, 140, 4, W.PAD_SYMMETRIC),
     (2, 768, 384, 129, 8, W.PAD_SYMMETRIC),
     (1, 1536, 768, 40, 8, W.PAD_SYMMETRIC),
