@@ -143,7 +143,9 @@ RU_CASES = [
     (1, 128, 300, 3, W.PAD_CAUSAL),     # the widest B2 form (N = 2 x 128 accumulator columns)
     (1, 80, 513, 9, W.PAD_SYMMETRIC),   # 5 column chunks over 3 epilogue groups, one row past 4 tiles
     (2, 112, 40, 1, W.PAD_SYMMETRIC),   # shorter than one tile
-    (2, 192, 200, 3, W.PAD_SYMMETRIC),
+    (2, 192, 200, 3, W.PAD_SYMMETRIC),  # H as four parts in a ring of two slots
+    (1, 192, 300, 9, W.PAD_SYMMETRIC),  # six parts (the tap span leaves room for 32-channel k-blocks)
+    (1, 160, 260, 1, W.PAD_CAUSAL),     # five parts of 32 channels
     (1, 48, 400, 9, W.PAD_CAUSAL),
     (3, 16, 70, 3, W.PAD_SYMMETRIC),
     (1, 4, 129, 9, W.PAD_SYMMETRIC),
