@@ -40,15 +40,15 @@
 namespace voc {
 
 // Warp group 0 (warps 0..3) issues copies and MMAs with few registers; warp groups 1..3 are the
-// epilogue, with the registers the others give up (setmaxnreg): 128 x 56 + 384 x 152 = 65536,
+// epilogue, with the registers the others give up (setmaxnreg): 128 x 32 + 384 x 160 = 65536,
 // the 512 threads x 128 registers the block is launched with.
 constexpr int kRuBWarp = 2;                          // weight copies (warp 3 idles)
 constexpr int kRuEpi0 = 4;                           // first epilogue warp
 constexpr int kRuEpiWarps = 4 * kEpiGroups;          // warps 4..15
 constexpr int kRuThreads = 32 * (kRuEpi0 + kRuEpiWarps);  // 512
 constexpr int kRuLaunchRegs = 128;                   // registers per thread at launch
-constexpr int kRuCopyRegs = 56;                      // warp group 0 after the split
-constexpr int kRuEpiRegs = 152;                      // epilogue warp groups after the split
+constexpr int kRuCopyRegs = 32;                      // warp group 0 after the split
+constexpr int kRuEpiRegs = 160;                      // epilogue warp groups after the split
 static_assert(128 * kRuCopyRegs + 32 * kRuEpiWarps * kRuEpiRegs <= kRuThreads * kRuLaunchRegs,
               "the register split exceeds the launch allocation");
 // 16-column chunks of one epilogue group: C <= 192 has 12 chunks (4 per group); the B2 form
